@@ -1,0 +1,178 @@
+"""CPU oracle for submanifold sparse 3x3x3 convolution (test infrastructure).
+
+Only the tests, the smoke check in ``__graft_entry__`` and the CPU-baseline leg
+of ``bench.py`` may import this package.  The library's product path never
+does: it shares no code, header or helper with the CUDA implementation.
+
+The arithmetic lives in ``spconv_oracle.cpp`` (plain C++17: a hash-map
+neighbour lookup, ``std::stable_sort`` for the mask order, and an fp64 sum over
+the 27 taps).  This module compiles it with the host C++ compiler and wraps it
+with numpy arrays.  See the C++ file for the conventions and the passages each
+function follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spconv_oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ERR_DUPLICATE = -5
+ERR_RANGE = -6
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (OpenMP if available)."""
+    with _lock:
+        if (not force and os.path.exists(_LIB_PATH)
+                and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            return _LIB_PATH
+        os.makedirs(_BUILD, exist_ok=True)
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        base = ["g++", "-std=c++17", "-O2", "-shared", "-fPIC", _SRC, "-o", tmp]
+        try:
+            subprocess.run(base[:4] + ["-fopenmp"] + base[4:], check=True,
+                           capture_output=True)
+        except subprocess.CalledProcessError:
+            subprocess.run(base, check=True, capture_output=True)
+        os.replace(tmp, _LIB_PATH)
+        return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i64, i32 = ctypes.c_int64, ctypes.c_int32
+        lib.oracle_kernel_map.argtypes = [P, i64, P, i32, P]
+        lib.oracle_kernel_map.restype = ctypes.c_int
+        lib.oracle_masks.argtypes = [P, i64, P]
+        lib.oracle_masks.restype = None
+        lib.oracle_tap_order.argtypes = [P, i64, ctypes.c_int, P]
+        lib.oracle_tap_order.restype = None
+        lib.oracle_sort_keys.argtypes = [P, i64, P, P]
+        lib.oracle_sort_keys.restype = None
+        lib.oracle_perm.argtypes = [P, i64, P]
+        lib.oracle_perm.restype = None
+        lib.oracle_pair_lists.argtypes = [P, P, i64, P, P, P]
+        lib.oracle_pair_lists.restype = i64
+        lib.oracle_conv_f64.argtypes = [P, P, i64, P, P, i32, i32, P, i32]
+        lib.oracle_conv_f64.restype = None
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int):
+        super().__init__({ERR_DUPLICATE: "duplicate coordinate",
+                          ERR_RANGE: "coordinate out of range"}.get(code, f"error {code}"))
+        self.code = code
+
+
+def kernel_map(coords, spatial_shape, batch_size: int) -> np.ndarray:
+    """``nbr[N, 27]`` int32: row of the neighbour at tap k, or -1."""
+    c = np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 4))
+    shape = np.ascontiguousarray(np.asarray(spatial_shape, dtype=np.int32))
+    nbr = np.empty((c.shape[0], 27), dtype=np.int32)
+    rc = _load().oracle_kernel_map(_ptr(c), c.shape[0], _ptr(shape), int(batch_size), _ptr(nbr))
+    if rc != 0:
+        raise OracleError(rc)
+    return nbr
+
+
+def masks(nbr: np.ndarray) -> np.ndarray:
+    nbr = np.ascontiguousarray(nbr, dtype=np.int32)
+    m = np.empty(nbr.shape[0], dtype=np.uint32)
+    _load().oracle_masks(_ptr(nbr), nbr.shape[0], _ptr(m))
+    return m
+
+
+def tap_order(mask: np.ndarray, calibrated: bool = True) -> np.ndarray:
+    mask = np.ascontiguousarray(mask, dtype=np.uint32)
+    order = np.empty(27, dtype=np.int32)
+    _load().oracle_tap_order(_ptr(mask), mask.shape[0], int(bool(calibrated)), _ptr(order))
+    return order
+
+
+def sort_keys(mask: np.ndarray, order: np.ndarray) -> np.ndarray:
+    mask = np.ascontiguousarray(mask, dtype=np.uint32)
+    order = np.ascontiguousarray(order, dtype=np.int32)
+    key = np.empty(mask.shape[0], dtype=np.uint32)
+    _load().oracle_sort_keys(_ptr(mask), mask.shape[0], _ptr(order), _ptr(key))
+    return key
+
+
+def perm(key: np.ndarray) -> np.ndarray:
+    key = np.ascontiguousarray(key, dtype=np.uint32)
+    p = np.empty(key.shape[0], dtype=np.int32)
+    _load().oracle_perm(_ptr(key), key.shape[0], _ptr(p))
+    return p
+
+
+def pair_lists(nbr: np.ndarray, perm_: np.ndarray):
+    """``(tap_off[28], in_rows[P], out_rows[P])`` per tap in ``perm_`` order."""
+    nbr = np.ascontiguousarray(nbr, dtype=np.int32)
+    perm_ = np.ascontiguousarray(perm_, dtype=np.int32)
+    n = nbr.shape[0]
+    tap_off = np.empty(28, dtype=np.int32)
+    cap = max(1, 27 * n)
+    ins = np.empty(cap, dtype=np.int32)
+    outs = np.empty(cap, dtype=np.int32)
+    p = _load().oracle_pair_lists(_ptr(nbr), _ptr(perm_), n, _ptr(tap_off), _ptr(ins), _ptr(outs))
+    return tap_off, ins[:p].copy(), outs[:p].copy()
+
+
+def conv_f64(nbr: np.ndarray, feats, weights, rows=None, threads: int = 0) -> np.ndarray:
+    """fp64 ``out[r] = sum_k sum_c feats[nbr[r][k]][c] * weights[k][c][:]``.
+
+    ``feats`` [N, C_in] and ``weights`` [27, C_in, C_out] are taken as exact
+    fp64 values (bf16 and fp32 inputs convert exactly).  ``rows`` selects the
+    output rows to evaluate (all when None); the result follows its order.
+    """
+    nbr = np.ascontiguousarray(nbr, dtype=np.int32)
+    f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64))
+    w = np.ascontiguousarray(np.asarray(weights, dtype=np.float64))
+    c_in, c_out = int(w.shape[1]), int(w.shape[2])
+    assert w.shape[0] == 27 and f.shape[1] == c_in
+    if rows is None:
+        r_arr, n_rows, rp = None, nbr.shape[0], None
+    else:
+        r_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        n_rows, rp = r_arr.shape[0], _ptr(r_arr)
+    out = np.empty((n_rows, c_out), dtype=np.float64)
+    _load().oracle_conv_f64(_ptr(nbr), rp, n_rows, _ptr(f), _ptr(w), c_in, c_out, _ptr(out),
+                            int(threads))
+    return out
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def subm_conv(coords, spatial_shape, batch_size, feats, weights, calibrated=True, rows=None,
+              threads: int = 0):
+    """The whole path: kernel map, masks, order, pair lists and fp64 output."""
+    nbr = kernel_map(coords, spatial_shape, batch_size)
+    m = masks(nbr)
+    order = tap_order(m, calibrated)
+    p = perm(sort_keys(m, order))
+    lists = pair_lists(nbr, p)
+    out = conv_f64(nbr, feats, weights, rows=rows, threads=threads)
+    return dict(nbr=nbr, mask=m, order=order, perm=p, tap_off=lists[0], in_rows=lists[1],
+                out_rows=lists[2], out=out)

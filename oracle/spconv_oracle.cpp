@@ -1,0 +1,197 @@
+// Plain, slow CPU oracle for submanifold sparse 3x3x3 convolution.
+//
+// TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check of the
+// build entry module and the CPU-baseline leg of the benchmark may load or
+// call this code.  The product path never does, and the two share no code.
+//
+// What it computes (each function names the passage it follows):
+//   * the kernel map: for every active voxel and each of the 27 offsets, the
+//     row of the neighbour at that offset, or -1 -- an exact set lookup
+//     through a hash map ("Sparse convolution in FP32", section "The starting
+//     point": the work is finding which neighbours exist);
+//   * the 27-bit neighbour mask of each row and the rows sorted by it
+//     (same page, "Neighbour masks and sorted rows"; the bit order may be the
+//     plain one or calibrated, same page, "Calibrated bit order");
+//   * the per-tap pair lists in that sorted order (FlyDSL PR #942 summary,
+//     "Compaction is the largest single win": only the valid pairs, grouped
+//     by tap);
+//   * the convolution itself, out[i][o] = sum_k sum_c f[nbr[i][k]][c] W[k][c][o],
+//     in fp64 ("Sparse convolution in FP32", "The starting point").
+//
+// Conventions (the pages leave them open; this is the reading used
+// throughout):
+//   tap k = 9*(dx+1) + 3*(dy+1) + (dz+1), offset d = (dx,dy,dz) in {-1,0,1}^3;
+//   nbr[i][k] = row of the voxel at coords[i] + d_k in the same batch, else -1;
+//   weights are [27][C_in][C_out]; out = sum_k W[k]^T f(p + d_k)
+//   (cross-correlation, as torch conv3d with padding 1).
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <unordered_map>
+#include <vector>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+struct Voxel {
+    int32_t b, x, y, z;
+    bool operator==(const Voxel& o) const {
+        return b == o.b && x == o.x && y == o.y && z == o.z;
+    }
+};
+
+struct VoxelHash {
+    size_t operator()(const Voxel& v) const {
+        uint64_t h = 1469598103934665603ull;
+        const int32_t f[4] = {v.b, v.x, v.y, v.z};
+        for (int i = 0; i < 4; ++i) {
+            h ^= static_cast<uint32_t>(f[i]);
+            h *= 1099511628211ull;
+        }
+        return static_cast<size_t>(h);
+    }
+};
+
+inline int tap_index(int dx, int dy, int dz) { return 9 * (dx + 1) + 3 * (dy + 1) + (dz + 1); }
+
+}  // namespace
+
+extern "C" {
+
+// Error codes match the meaning (not the implementation) of the library's.
+enum { ORACLE_OK = 0, ORACLE_ERR_DUPLICATE = -5, ORACLE_ERR_RANGE = -6 };
+
+// Kernel map by hash lookup.  coords: [n][4] (b,x,y,z).  shape: {X,Y,Z}.
+// A coordinate outside 0 <= b < batch_size, 0 <= x < X, ... is an error, and
+// so is a repeated coordinate.  nbr: [n][27].
+int oracle_kernel_map(const int32_t* coords, int64_t n, const int32_t* shape,
+                      int32_t batch_size, int32_t* nbr) {
+    std::unordered_map<Voxel, int32_t, VoxelHash> where;
+    where.reserve(static_cast<size_t>(n) * 2 + 1);
+    for (int64_t i = 0; i < n; ++i) {
+        Voxel v{coords[4 * i], coords[4 * i + 1], coords[4 * i + 2], coords[4 * i + 3]};
+        if (v.b < 0 || v.b >= batch_size || v.x < 0 || v.x >= shape[0] || v.y < 0 ||
+            v.y >= shape[1] || v.z < 0 || v.z >= shape[2])
+            return ORACLE_ERR_RANGE;
+        if (!where.emplace(v, static_cast<int32_t>(i)).second) return ORACLE_ERR_DUPLICATE;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t* c = coords + 4 * i;
+        for (int dx = -1; dx <= 1; ++dx)
+            for (int dy = -1; dy <= 1; ++dy)
+                for (int dz = -1; dz <= 1; ++dz) {
+                    Voxel q{c[0], c[1] + dx, c[2] + dy, c[3] + dz};
+                    auto it = where.find(q);
+                    nbr[27 * i + tap_index(dx, dy, dz)] = it == where.end() ? -1 : it->second;
+                }
+    }
+    return ORACLE_OK;
+}
+
+// mask[i] bit k set iff nbr[i][k] >= 0.
+void oracle_masks(const int32_t* nbr, int64_t n, uint32_t* mask) {
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t m = 0;
+        for (int k = 0; k < 27; ++k)
+            if (nbr[27 * i + k] >= 0) m |= 1u << k;
+        mask[i] = m;
+    }
+}
+
+// Bit order of the sort key.  order[j] is the tap whose presence sets key bit j.
+// calibrated == 0: plain order, order[j] = j.
+// calibrated != 0: taps by descending number of rows that have them (ties by
+// ascending tap index), so the rarest tap is the most significant key bit and
+// rows that share rare taps end up next to each other.
+void oracle_tap_order(const uint32_t* mask, int64_t n, int calibrated, int32_t* order) {
+    int64_t count[27] = {0};
+    for (int64_t i = 0; i < n; ++i)
+        for (int k = 0; k < 27; ++k) count[k] += (mask[i] >> k) & 1u;
+    std::vector<int32_t> taps(27);
+    for (int k = 0; k < 27; ++k) taps[k] = k;
+    if (calibrated)
+        std::stable_sort(taps.begin(), taps.end(),
+                         [&](int32_t a, int32_t b) { return count[a] > count[b]; });
+    for (int j = 0; j < 27; ++j) order[j] = taps[j];
+}
+
+// key[i] = sum_j [tap order[j] present in row i] << j.
+void oracle_sort_keys(const uint32_t* mask, int64_t n, const int32_t* order, uint32_t* key) {
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t k = 0;
+        for (int j = 0; j < 27; ++j)
+            if ((mask[i] >> order[j]) & 1u) k |= 1u << j;
+        key[i] = k;
+    }
+}
+
+// perm: rows in ascending key order; equal keys keep ascending row order.
+void oracle_perm(const uint32_t* key, int64_t n, int32_t* perm) {
+    std::vector<int32_t> rows(static_cast<size_t>(n));
+    for (int64_t i = 0; i < n; ++i) rows[i] = static_cast<int32_t>(i);
+    std::stable_sort(rows.begin(), rows.end(),
+                     [&](int32_t a, int32_t b) { return key[a] < key[b]; });
+    std::memcpy(perm, rows.data(), sizeof(int32_t) * static_cast<size_t>(n));
+}
+
+// Per-tap pair lists in perm order.  tap_off: [28], CSR offsets.  in_rows /
+// out_rows: room for every pair (27 n at most).  Returns the pair count P.
+int64_t oracle_pair_lists(const int32_t* nbr, const int32_t* perm, int64_t n, int32_t* tap_off,
+                          int32_t* in_rows, int32_t* out_rows) {
+    int64_t p = 0;
+    for (int k = 0; k < 27; ++k) {
+        tap_off[k] = static_cast<int32_t>(p);
+        for (int64_t s = 0; s < n; ++s) {
+            int32_t r = perm[s];
+            int32_t j = nbr[27 * static_cast<int64_t>(r) + k];
+            if (j >= 0) {
+                in_rows[p] = j;
+                out_rows[p] = r;
+                ++p;
+            }
+        }
+    }
+    tap_off[27] = static_cast<int32_t>(p);
+    return p;
+}
+
+// out[r][o] = sum_k sum_c feats[nbr[r][k]][c] * weights[k][c][o] in fp64, for
+// the rows listed in rows[0..n_rows) (all rows when rows == NULL, then
+// n_rows == n).  out is [n_rows][c_out], in the order of rows.
+void oracle_conv_f64(const int32_t* nbr, const int32_t* rows, int64_t n_rows,
+                     const double* feats, const double* weights, int32_t c_in, int32_t c_out,
+                     double* out, int32_t threads) {
+#ifdef _OPENMP
+    if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 64) num_threads(threads)
+#endif
+    for (int64_t t = 0; t < n_rows; ++t) {
+        int64_t r = rows ? rows[t] : t;
+        double* o = out + t * c_out;
+        for (int32_t q = 0; q < c_out; ++q) o[q] = 0.0;
+        for (int k = 0; k < 27; ++k) {
+            int32_t j = nbr[27 * r + k];
+            if (j < 0) continue;
+            const double* f = feats + static_cast<int64_t>(j) * c_in;
+            const double* w = weights + static_cast<int64_t>(k) * c_in * c_out;
+            for (int32_t c = 0; c < c_in; ++c) {
+                const double fc = f[c];
+                const double* wr = w + static_cast<int64_t>(c) * c_out;
+                for (int32_t q = 0; q < c_out; ++q) o[q] += fc * wr[q];
+            }
+        }
+    }
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+}  // extern "C"

@@ -1,0 +1,320 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each check below fixes the oracle to something independent: a hand-derived
+worked example, closed forms on a dense cube, brute-force all-pairs search,
+a library dense convolution (torch ``conv3d`` with padding 1, fp64, CPU) on a
+zero-filled grid, and invariants of the definition.  The mutation tests plant
+plausible mistakes in copies of the oracle's output (or feed it a mistaken
+input) and show that the pins catch them.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from submanifold_sparse_convolution_gb300 import synthetic as S
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def tap_of(dx, dy, dz):
+    return 9 * (dx + 1) + 3 * (dy + 1) + (dz + 1)
+
+
+OFFSETS = [(dx, dy, dz) for dx in (-1, 0, 1) for dy in (-1, 0, 1) for dz in (-1, 0, 1)]
+
+
+def read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *rest = line.split()
+            vals[key] = [int(v) for v in rest]
+    return vals
+
+
+# ---------------------------------------------------------------------------
+# independent checkers
+# ---------------------------------------------------------------------------
+
+def brute_force_nbr(coords):
+    """All-pairs search: j is the tap-k neighbour of i iff c[j] - c[i] == d_k, same b."""
+    c = np.asarray(coords, dtype=np.int64)
+    n = c.shape[0]
+    nbr = np.full((n, 27), -1, dtype=np.int64)
+    diff = c[None, :, :] - c[:, None, :]          # [i, j, 4]
+    same_b = diff[:, :, 0] == 0
+    for k, (dx, dy, dz) in enumerate(OFFSETS):
+        hit = same_b & (diff[:, :, 1] == dx) & (diff[:, :, 2] == dy) & (diff[:, :, 3] == dz)
+        i_idx, j_idx = np.nonzero(hit)
+        nbr[i_idx, k] = j_idx
+    return nbr
+
+
+def dense_conv_reference(coords, shape, batch, feats, weights):
+    """torch conv3d (padding 1, fp64) on a zero-filled dense grid, read at active sites."""
+    X, Y, Z = shape
+    f = torch.as_tensor(np.asarray(feats, dtype=np.float64))
+    w = torch.as_tensor(np.asarray(weights, dtype=np.float64))   # [27, Cin, Cout]
+    c_in, c_out = w.shape[1], w.shape[2]
+    grid = torch.zeros(batch, c_in, X, Y, Z, dtype=torch.float64)
+    c = torch.as_tensor(np.asarray(coords, dtype=np.int64))
+    grid[c[:, 0], :, c[:, 1], c[:, 2], c[:, 3]] = f
+    wd = torch.zeros(c_out, c_in, 3, 3, 3, dtype=torch.float64)
+    for k, (dx, dy, dz) in enumerate(OFFSETS):
+        wd[:, :, dx + 1, dy + 1, dz + 1] = w[k].T
+    out = torch.nn.functional.conv3d(grid, wd, padding=1)
+    return out[c[:, 0], :, c[:, 1], c[:, 2], c[:, 3]].numpy()
+
+
+def pairs_cover_map(nbr, tap_off, in_rows, out_rows):
+    """Full-tap coverage: per tap, the pair set equals {(nbr[i][k], i)}."""
+    for k in range(27):
+        seg = slice(tap_off[k], tap_off[k + 1])
+        got = set(zip(in_rows[seg].tolist(), out_rows[seg].tolist()))
+        rows = np.nonzero(nbr[:, k] >= 0)[0]
+        want = set(zip(nbr[rows, k].tolist(), rows.tolist()))
+        if got != want or len(got) != tap_off[k + 1] - tap_off[k]:
+            return False
+    return True
+
+
+def pairs_follow_perm(perm, tap_off, out_rows):
+    """Within each tap the pairs appear in the order of ``perm``."""
+    pos = np.empty_like(perm)
+    pos[perm] = np.arange(perm.shape[0])
+    for k in range(27):
+        s = pos[out_rows[tap_off[k]:tap_off[k + 1]]]
+        if np.any(np.diff(s) <= 0):
+            return False
+    return True
+
+
+# ---------------------------------------------------------------------------
+# worked example and closed forms
+# ---------------------------------------------------------------------------
+
+def test_golden_line_and_isolated():
+    g = read_golden("line_and_isolated.txt")
+    coords = np.array(g["coords"], dtype=np.int32).reshape(-1, 4)
+    feats = np.array(g["feats"], dtype=np.float64).reshape(-1, 1)
+    weights = (np.arange(27, dtype=np.float64) + 1).reshape(27, 1, 1)
+    res = oracle.subm_conv(coords, g["shape"], g["batch"][0], feats, weights)
+    assert res["out"][:, 0].tolist() == g["out"]
+    assert res["mask"].tolist() == g["masks"]
+    assert int(res["tap_off"][27]) == g["pairs"][0]
+
+
+def test_dense_cube_closed_forms():
+    """A fully occupied 3x3x3 cube: counts factor over the axes."""
+    cells = np.array([(0, x, y, z) for x in range(3) for y in range(3) for z in range(3)],
+                     dtype=np.int32)
+    nbr = oracle.kernel_map(cells, (3, 3, 3), 1)
+    per_axis = {0: 2, 1: 3, 2: 2}
+    for i, (_, x, y, z) in enumerate(cells):
+        assert (nbr[i] >= 0).sum() == per_axis[x] * per_axis[y] * per_axis[z]
+    assert (nbr >= 0).sum() == 7 ** 3
+    centre = [i for i, c in enumerate(cells.tolist()) if c[1:] == [1, 1, 1]][0]
+    assert oracle.masks(nbr)[centre] == (1 << 27) - 1
+
+
+# ---------------------------------------------------------------------------
+# kernel map
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed,n,shape,batch", [(1, 200, (8, 8, 8), 1), (2, 600, (10, 9, 7), 3),
+                                                (3, 1500, (16, 16, 16), 2), (4, 1, (4, 4, 4), 1),
+                                                (5, 512, (8, 8, 8), 1)])
+def test_kernel_map_matches_brute_force(seed, n, shape, batch):
+    wl = S.random_cloud(seed, n, shape=shape, batch_size=batch)
+    nbr = oracle.kernel_map(wl.coords.numpy(), shape, batch)
+    assert np.array_equal(nbr, brute_force_nbr(wl.coords.numpy()))
+
+
+def test_tiny_workload_kernel_map_matches_brute_force():
+    wl = S.make_workload("tiny")
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    assert np.array_equal(nbr, brute_force_nbr(wl.coords.numpy()))
+
+
+def test_kernel_map_invariants():
+    wl = S.random_cloud(11, 3000, shape=(20, 20, 20), batch_size=2)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 2)
+    n = nbr.shape[0]
+    assert np.array_equal(nbr[:, 13], np.arange(n))             # centre tap is the row itself
+    for k in range(27):                                           # symmetry
+        rows = np.nonzero(nbr[:, k] >= 0)[0]
+        assert np.array_equal(nbr[nbr[rows, k], 26 - k], rows)
+    assert (nbr >= 0).sum() >= n
+
+
+def test_isolated_voxel_sees_only_centre():
+    coords = np.array([[0, 0, 0, 0], [0, 5, 5, 5], [0, 2, 2, 2], [1, 3, 3, 3]], dtype=np.int32)
+    nbr = oracle.kernel_map(coords, (8, 8, 8), 2)
+    assert np.array_equal(oracle.masks(nbr), np.full(4, 1 << 13, dtype=np.uint32))
+
+
+def test_batches_never_neighbour():
+    coords = np.array([[0, 1, 1, 1], [1, 1, 1, 2], [1, 1, 1, 1]], dtype=np.int32)
+    nbr = oracle.kernel_map(coords, (4, 4, 4), 2)
+    assert nbr[0].tolist().count(-1) == 26
+    assert nbr[1, tap_of(0, 0, -1)] == 2 and nbr[2, tap_of(0, 0, 1)] == 1
+
+
+def test_kernel_map_errors():
+    dup = np.array([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=np.int32)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.kernel_map(dup, (4, 4, 4), 1)
+    assert e.value.code == oracle.ERR_DUPLICATE
+    for bad in ([0, 4, 0, 0], [0, -1, 0, 0], [1, 0, 0, 0], [0, 0, 0, 9]):
+        with pytest.raises(oracle.OracleError) as e:
+            oracle.kernel_map(np.array([[0, 0, 0, 0], bad], dtype=np.int32), (4, 4, 9), 1)
+        assert e.value.code == oracle.ERR_RANGE
+
+
+def test_mutated_kernel_map_is_caught():
+    wl = S.random_cloud(21, 400, shape=(8, 8, 8))
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1)
+    ref = brute_force_nbr(wl.coords.numpy())
+    bad = nbr.copy()
+    bad[:, [tap_of(-1, 0, 0), tap_of(1, 0, 0)]] = bad[:, [tap_of(1, 0, 0), tap_of(-1, 0, 0)]]
+    assert not np.array_equal(bad, ref)                           # a swapped offset sign
+    bad = nbr.copy()
+    bad[:, [tap_of(0, -1, 0), tap_of(-1, 0, 0)]] = bad[:, [tap_of(-1, 0, 0), tap_of(0, -1, 0)]]
+    assert not np.array_equal(bad, ref)                           # transposed axes
+
+
+# ---------------------------------------------------------------------------
+# masks, order and pair lists
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("calibrated", [False, True])
+def test_order_and_pair_lists(calibrated):
+    wl = S.random_cloud(31, 2500, shape=(16, 16, 16), batch_size=2)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 2)
+    m = oracle.masks(nbr)
+    assert np.array_equal(m, ((nbr >= 0) * (1 << np.arange(27))).sum(1).astype(np.uint32))
+    order = oracle.tap_order(m, calibrated)
+    assert sorted(order.tolist()) == list(range(27))
+    counts = np.array([((m >> t) & 1).sum() for t in range(27)], dtype=np.int64)
+    if calibrated:
+        assert np.all(np.diff(counts[order]) <= 0)
+    else:
+        assert order.tolist() == list(range(27))
+    key = oracle.sort_keys(m, order)
+    popc = lambda a: np.array([bin(int(v)).count("1") for v in a])
+    assert np.array_equal(popc(key), popc(m))
+    if not calibrated:
+        assert np.array_equal(key, m)
+    p = oracle.perm(key)
+    assert sorted(p.tolist()) == list(range(len(p)))
+    ks = key[p]
+    assert np.all(np.diff(ks.astype(np.int64)) >= 0)
+    ties = np.diff(ks.astype(np.int64)) == 0
+    assert np.all(np.diff(p)[ties] > 0)                           # stable: ties by row
+    tap_off, ins, outs = oracle.pair_lists(nbr, p)
+    assert tap_off[0] == 0 and tap_off[27] == (nbr >= 0).sum()
+    assert np.all(np.diff(tap_off) == (nbr >= 0).sum(0))
+    assert pairs_cover_map(nbr, tap_off, ins, outs)
+    assert pairs_follow_perm(p, tap_off, outs)
+
+
+def test_mutated_pair_lists_are_caught():
+    wl = S.random_cloud(32, 800, shape=(10, 10, 10))
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1)
+    p = oracle.perm(oracle.sort_keys(oracle.masks(nbr), oracle.tap_order(oracle.masks(nbr))))
+    tap_off, ins, outs = oracle.pair_lists(nbr, p)
+    # drop one pair (the mutation the pages use to show their coverage test bites)
+    k = 5
+    drop = tap_off[k] + 1
+    ins2, outs2 = np.delete(ins, drop), np.delete(outs, drop)
+    off2 = tap_off.copy()
+    off2[k + 1:] -= 1
+    assert not pairs_cover_map(nbr, off2, ins2, outs2)
+    # swap two pairs inside a tap: coverage holds, order does not
+    outs3 = outs.copy()
+    outs3[tap_off[k]], outs3[tap_off[k] + 1] = outs3[tap_off[k] + 1], outs3[tap_off[k]]
+    assert not pairs_follow_perm(p, tap_off, outs3)
+
+
+# ---------------------------------------------------------------------------
+# features
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed,n,shape,batch,c_in,c_out",
+                         [(41, 300, (9, 8, 7), 2, 5, 3), (42, 900, (12, 12, 12), 1, 16, 16),
+                          (43, 60, (5, 5, 5), 3, 1, 7)])
+def test_conv_matches_dense_conv3d(seed, n, shape, batch, c_in, c_out):
+    wl = S.random_cloud(seed, n, shape=shape, batch_size=batch, c_in=c_in, c_out=c_out)
+    nbr = oracle.kernel_map(wl.coords.numpy(), shape, batch)
+    f = wl.feats.double().numpy()
+    w = wl.weights[0].double().numpy()
+    got = oracle.conv_f64(nbr, f, w)
+    ref = dense_conv_reference(wl.coords.numpy(), shape, batch, f, w)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_mutated_conv_is_caught():
+    """Convolution instead of correlation (mirrored taps) and transposed W both fail."""
+    wl = S.random_cloud(44, 400, shape=(9, 9, 9), c_in=6, c_out=6)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1)
+    f = wl.feats.double().numpy()
+    w = wl.weights[0].double().numpy()
+    ref = dense_conv_reference(wl.coords.numpy(), wl.spatial_shape, 1, f, w)
+    assert not np.allclose(oracle.conv_f64(nbr, f, w[::-1].copy()), ref, atol=1e-6)
+    assert not np.allclose(oracle.conv_f64(nbr, f, w.transpose(0, 2, 1).copy()), ref, atol=1e-6)
+
+
+def test_conv_isolated_voxel_is_centre_tap_product():
+    coords = np.array([[0, 1, 1, 1], [0, 6, 6, 6]], dtype=np.int32)
+    rng = np.random.default_rng(5)
+    f = rng.standard_normal((2, 4))
+    w = rng.standard_normal((27, 4, 3))
+    out = oracle.conv_f64(oracle.kernel_map(coords, (8, 8, 8), 1), f, w)
+    np.testing.assert_allclose(out, f @ w[13], rtol=1e-14)
+
+
+def test_conv_row_permutation_equivariance():
+    wl = S.random_cloud(51, 700, shape=(11, 11, 11), c_in=8, c_out=8)
+    c = wl.coords.numpy()
+    f = wl.feats.double().numpy()
+    w = wl.weights[0].double().numpy()
+    out = oracle.conv_f64(oracle.kernel_map(c, wl.spatial_shape, 1), f, w)
+    q = np.random.default_rng(52).permutation(c.shape[0])
+    out_q = oracle.conv_f64(oracle.kernel_map(c[q], wl.spatial_shape, 1), f[q], w)
+    np.testing.assert_allclose(out_q, out[q], rtol=1e-13, atol=1e-13)
+
+
+def test_conv_linearity_and_batch_isolation():
+    wl = S.random_cloud(61, 600, shape=(10, 10, 10), batch_size=2, c_in=4, c_out=5)
+    c = wl.coords.numpy()
+    nbr = oracle.kernel_map(c, wl.spatial_shape, 2)
+    rng = np.random.default_rng(62)
+    f1, f2 = rng.standard_normal((2, c.shape[0], 4))
+    w1, w2 = rng.standard_normal((2, 27, 4, 5))
+    a, b = 0.75, -1.5
+    lhs = oracle.conv_f64(nbr, a * f1 + b * f2, w1)
+    rhs = a * oracle.conv_f64(nbr, f1, w1) + b * oracle.conv_f64(nbr, f2, w1)
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(oracle.conv_f64(nbr, f1, w1 + w2),
+                               oracle.conv_f64(nbr, f1, w1) + oracle.conv_f64(nbr, f1, w2),
+                               rtol=1e-11, atol=1e-11)
+    # changing frame 1's features leaves frame 0's outputs unchanged
+    f3 = f1.copy()
+    f3[c[:, 0] == 1] = rng.standard_normal(((c[:, 0] == 1).sum(), 4))
+    o1, o3 = oracle.conv_f64(nbr, f1, w1), oracle.conv_f64(nbr, f3, w1)
+    assert np.array_equal(o1[c[:, 0] == 0], o3[c[:, 0] == 0])
+
+
+def test_conv_row_subset_matches_full():
+    wl = S.random_cloud(71, 500, shape=(9, 9, 9), c_in=3, c_out=2)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1)
+    f = wl.feats.double().numpy()
+    w = wl.weights[0].double().numpy()
+    rows = np.array([7, 3, 499, 0, 3], dtype=np.int32)
+    assert np.array_equal(oracle.conv_f64(nbr, f, w, rows=rows), oracle.conv_f64(nbr, f, w)[rows])
