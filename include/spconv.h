@@ -1,0 +1,174 @@
+/*
+ * spconv.h -- C ABI of the GB300 (sm_103a) submanifold sparse 3x3x3 convolution.
+ *
+ * The operation (FlyDSL PR #942, "Add submanifold sparse 3D convolution",
+ * Summary: raw voxel coordinates in, output features out, the kernel map built
+ * internally; "Sparse convolution in FP32", section "The starting point": for
+ * every active voxel, the sum over its 27 neighbours of the neighbour's
+ * features times the weights of that kernel offset):
+ *
+ *     out[i][o] = sum_{k=0..26} sum_{c} f[nbr[i][k]][c] * W[k][c][o]
+ *
+ * over the rows i of the input, where nbr[i][k] is the row of the voxel at
+ * coords[i] + d_k (same batch index), the term skipped when there is none.
+ * Tap order: k = 9*(dx+1) + 3*(dy+1) + (dz+1) for d = (dx,dy,dz) in {-1,0,1}^3
+ * (cross-correlation, as torch conv3d with padding 1).  Outputs live at the
+ * input sites, in the input row order.
+ *
+ * Memory: every pointer argument named *_dev is a device pointer that the
+ * caller owns; host pointers are marked host.  The library allocates only map
+ * handles and packed-weight handles (stream-ordered, on the stream passed to
+ * the creating call) and frees them in the matching destroy call.
+ *
+ * Streams: all work is enqueued on the caller's stream; nothing synchronises
+ * the device except where a function says it does.
+ *
+ * Errors: functions return SPCONV_OK (0) or a negative spconv_status_t.
+ * Argument errors are detected on the host before any work is enqueued.
+ * Data errors found on the device (duplicate or out-of-range coordinates) are
+ * recorded in the map handle and reported by spconv_map_status(); the map's
+ * contents are then unspecified, but every kernel stays within its buffers.
+ * No kernel traps; bounded waits inside kernels report SPCONV_ERR_TIMEOUT.
+ */
+#ifndef SPCONV_H_
+#define SPCONV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPCONV_OK = 0,
+    SPCONV_ERR_INVALID_ARG = -1,   /* null pointer, bad size, bad enum, misaligned buffer */
+    SPCONV_ERR_UNSUPPORTED = -2,   /* valid request outside what this build implements    */
+    SPCONV_ERR_OOM = -3,           /* device allocation failed                             */
+    SPCONV_ERR_CUDA = -4,          /* a CUDA runtime call failed                            */
+    SPCONV_ERR_DUPLICATE_COORD = -5,
+    SPCONV_ERR_COORD_RANGE = -6,   /* b, x, y or z outside [0, batch) x [0, shape)          */
+    SPCONV_ERR_ALIAS = -7,         /* out overlaps feats                                     */
+    SPCONV_ERR_TIMEOUT = -8        /* a bounded wait inside a kernel ran out                 */
+} spconv_status_t;
+
+typedef enum { SPCONV_BF16 = 0, SPCONV_FP32 = 1 } spconv_dtype_t;
+
+typedef enum {
+    SPCONV_MAPPER_AUTO = 0,   /* dense grid iff padded cells <= dense_max_cells, else sorted keys */
+    SPCONV_MAPPER_DENSE = 1,  /* presence grid over the padded bounding box                       */
+    SPCONV_MAPPER_SORTED = 2  /* sorted 64-bit keys + binary search, memory O(N)                   */
+} spconv_mapper_t;
+
+typedef enum {
+    SPCONV_ORDER_CALIBRATED = 0, /* sort key bits by descending tap frequency (rarest tap = MSB) */
+    SPCONV_ORDER_PLAIN = 1       /* sort key = the 27-bit mask itself                             */
+} spconv_bit_order_t;
+
+/* Options of spconv_build_map.  Pass NULL for the defaults. */
+typedef struct {
+    int32_t mapper;          /* spconv_mapper_t, default AUTO                          */
+    int32_t bit_order;       /* spconv_bit_order_t, default CALIBRATED                 */
+    int64_t dense_max_cells; /* AUTO threshold on B*(X+2)*(Y+2)*(Z+2); default 1<<24   */
+} spconv_options_t;
+
+typedef struct spconv_map_s* spconv_map_t;
+typedef struct spconv_wpack_s* spconv_wpack_t;
+
+/* Summary of a built map.  Filling it synchronises the map's stream. */
+typedef struct {
+    int64_t n;           /* active voxels (rows)                                  */
+    int64_t pairs;       /* P = number of (row, tap) with a neighbour (>= n)      */
+    int64_t n_tiles;     /* 128-row tiles of the mask-sorted order                */
+    int64_t tile_taps;   /* sum over tiles of the taps in the tile's mask union   */
+    int32_t mapper;      /* spconv_mapper_t actually used (DENSE or SORTED)       */
+    int32_t key_bits;    /* live bits of the packed coordinate key                */
+    int32_t shape[3];    /* spatial shape used                                    */
+    int32_t batch_size;  /* batch size used                                       */
+} spconv_map_info_t;
+
+/*
+ * Build the kernel map of a coordinate set (FlyDSL PR #942, "Two mappers, both
+ * required"; "Sparse convolution in FP32", "Neighbour masks and sorted rows";
+ * FlyDSL PR #942, "Compaction is the largest single win").
+ *
+ *   coords_dev     int32 [n][4] rows (b, x, y, z), device, row-major.  Must stay
+ *                  valid until the stream has passed this call; the handle
+ *                  keeps what it needs.
+ *   n              number of rows, 0 <= n < 2^30.
+ *   spatial_shape  host int32[3] {X, Y, Z}, each >= 1; NULL derives max+1 per
+ *                  axis on the device (synchronises the stream).
+ *   batch_size     frames, >= 1; 0 derives max(b)+1 (synchronises the stream).
+ *   kernel_size    3 (the only size this build implements; others return
+ *                  SPCONV_ERR_UNSUPPORTED).
+ *   opt            options, NULL for defaults.
+ *   stream         CUDA stream (cudaStream_t) the work is enqueued on.
+ *   out_map        receives the handle; free it with spconv_map_destroy.
+ *
+ * Device-side results (all in the handle): the kernel map nbr[n][27], the
+ * 27-bit masks, perm (rows in ascending sort-key order, ties by row), the
+ * per-tap pair lists in perm order, and the 128-row tile work list.
+ */
+int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatial_shape,
+                     int32_t batch_size, int32_t kernel_size, const spconv_options_t* opt,
+                     void* stream, spconv_map_t* out_map);
+
+/*
+ * out = subm_conv(feats, weights) over the map's sites (the definition at the
+ * top of this file).
+ *
+ *   feats_dev    [n][c_in] row-major, dtype elements, 16-byte aligned.
+ *   weights_dev  [27][c_in][c_out] row-major, dtype elements.
+ *   out_dev      [n][c_out] row-major, dtype elements, 16-byte aligned; must
+ *                not overlap feats (SPCONV_ERR_ALIAS).
+ *   dtype        SPCONV_BF16: bf16 in/out, fp32 accumulation, one rounding to
+ *                bf16 at the store (tensor cores when c_in % 8 == 0 and
+ *                c_out % 16 == 0, else a SIMT kernel).  SPCONV_FP32: fp32
+ *                in/out with fp32 FMA on the SIMT path (exact mode).
+ * Packs the weights into a workspace owned by the map on every call; use
+ * spconv_wpack_create + spconv_subm_forward_packed to pack once.
+ */
+int spconv_subm_forward(spconv_map_t map, const void* feats_dev, const void* weights_dev,
+                        void* out_dev, int32_t c_in, int32_t c_out, int32_t dtype, void* stream);
+
+/*
+ * Pre-pack weights [27][c_in][c_out] for repeated forwards (FlyDSL PR #942,
+ * "Weight layout is [kv, t, k_outer, u, k_inner]": a packed tile layout; here
+ * the tensor-core shared-memory image).  The handle owns a copy; the source
+ * may be freed once the stream has passed this call.
+ */
+int spconv_wpack_create(const void* weights_dev, int32_t c_in, int32_t c_out, int32_t dtype,
+                        void* stream, spconv_wpack_t* out_wpack);
+int spconv_subm_forward_packed(spconv_map_t map, const void* feats_dev, spconv_wpack_t wpack,
+                               void* out_dev, void* stream);
+void spconv_wpack_destroy(spconv_wpack_t wpack);
+
+/* Synchronise the map's stream and return the first device-detected error
+ * (duplicate or out-of-range coordinates, kernel timeouts), else SPCONV_OK. */
+int spconv_map_status(spconv_map_t map);
+
+/* Fill *info (synchronises the map's stream). */
+int spconv_map_info(spconv_map_t map, spconv_map_info_t* info);
+
+/*
+ * Copy the map's arrays into caller device buffers (any may be NULL):
+ *   nbr_dev int32 [n][27]; mask_dev uint32 [n]; perm_dev int32 [n];
+ *   tap_off_dev int32 [28]; in_rows_dev, out_rows_dev int32 [pairs].
+ * Enqueued on stream; no synchronisation.
+ */
+int spconv_map_export(spconv_map_t map, int32_t* nbr_dev, uint32_t* mask_dev, int32_t* perm_dev,
+                      int32_t* tap_off_dev, int32_t* in_rows_dev, int32_t* out_rows_dev,
+                      void* stream);
+
+/* Free the handle (stream-ordered on the stream of the build). */
+void spconv_map_destroy(spconv_map_t map);
+
+/* Number of kernel launches enqueued by the last call on this thread. */
+int32_t spconv_last_launch_count(void);
+
+const char* spconv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPCONV_H_ */

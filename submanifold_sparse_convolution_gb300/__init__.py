@@ -1,0 +1,244 @@
+"""GB300 (sm_103a) submanifold sparse 3x3x3 convolution.
+
+A thin Python binding over the C ABI of ``libspconv.so`` (include/spconv.h):
+the functions below only check and marshal arguments; every step of the path
+(mapper, masks, sort, compaction, GEMM) runs in the library's CUDA kernels.
+PyTorch supplies device memory and streams.
+
+    m = build_map(coords)                       # int32 [N, 4] (b, x, y, z), CUDA
+    out = subm_forward(m, feats, weights)       # bf16 [N, C_in] x [27, C_in, C_out]
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _native
+
+__all__ = ["SpconvError", "Map", "WPack", "build_map", "subm_forward", "wpack_create",
+           "subm_forward_packed", "map_status", "map_info", "map_export", "map_destroy",
+           "last_launch_count", "status_string", "MAPPERS", "BIT_ORDERS", "library"]
+
+MAPPERS = {"auto": 0, "dense": 1, "sorted": 2}
+BIT_ORDERS = {"calibrated": 0, "plain": 1}
+_DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+
+
+def library():
+    """The loaded ctypes library (raises if it has not been built)."""
+    return _native.load()
+
+
+def status_string(code: int) -> str:
+    return library().spconv_status_string(int(code)).decode()
+
+
+class SpconvError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        super().__init__(f"{where}: {status_string(code)} ({code})" if where else status_string(code))
+        self.code = code
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SpconvError(code, where)
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _require_cuda(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class Map:
+    """A kernel map (handle ``spconv_map_t``); shared by every layer on these sites."""
+
+    def __init__(self, handle: ctypes.c_void_p, n: int, coords: torch.Tensor):
+        self._h = handle
+        self.n = n
+        self._coords = coords      # kept alive while the build may still read it
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._h is None:
+            raise ValueError("map has been destroyed")
+        return self._h
+
+    def destroy(self):
+        if getattr(self, "_h", None) is not None:
+            library().spconv_map_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+class WPack:
+    """Pre-packed weights (handle ``spconv_wpack_t``)."""
+
+    def __init__(self, handle, c_in, c_out, dtype, src):
+        self._h = handle
+        self.c_in, self.c_out, self.dtype = c_in, c_out, dtype
+        self._src = src
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("weight pack has been destroyed")
+        return self._h
+
+    def destroy(self):
+        if getattr(self, "_h", None) is not None:
+            library().spconv_wpack_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def build_map(coords: torch.Tensor, spatial_shape: Optional[Sequence[int]] = None,
+              batch_size: int = 0, kernel_size: int = 3, mapper: str = "auto",
+              bit_order: str = "calibrated", dense_max_cells: int = 0,
+              stream: Optional[torch.cuda.Stream] = None) -> Map:
+    """``spconv_build_map``: kernel map of ``coords`` (int32 [N, 4] (b, x, y, z) on the GPU).
+
+    ``spatial_shape`` None and ``batch_size`` 0 derive them on the device
+    (this synchronises the stream).
+    """
+    lib = library()
+    _require_cuda(coords, "coords")
+    if coords.dtype != torch.int32 or coords.dim() != 2 or coords.shape[1] != 4:
+        raise ValueError("coords must be int32 [N, 4]")
+    shape_arr = None
+    if spatial_shape is not None:
+        shape_arr = (ctypes.c_int32 * 3)(*[int(v) for v in spatial_shape])
+    opt = _native.Options(MAPPERS[mapper], BIT_ORDERS[bit_order], int(dense_max_cells))
+    h = ctypes.c_void_p()
+    rc = lib.spconv_build_map(_ptr(coords), int(coords.shape[0]),
+                              ctypes.cast(shape_arr, _native.c_int32_p) if shape_arr is not None else None,
+                              int(batch_size), int(kernel_size), ctypes.byref(opt), _stream_ptr(stream),
+                              ctypes.byref(h))
+    _check(rc, "spconv_build_map")
+    return Map(h, int(coords.shape[0]), coords)
+
+
+def subm_forward(m: Map, feats: torch.Tensor, weights: torch.Tensor,
+                 out: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """``spconv_subm_forward``: feats [N, C_in] x weights [27, C_in, C_out] -> [N, C_out].
+
+    bf16 inputs use fp32 accumulation and one rounding at the store; fp32
+    inputs take the exact fp32 path.
+    """
+    lib = library()
+    _require_cuda(feats, "feats")
+    _require_cuda(weights, "weights")
+    if feats.dtype not in _DTYPES or weights.dtype != feats.dtype:
+        raise ValueError("feats and weights must both be bf16 or both fp32")
+    if feats.dim() != 2 or feats.shape[0] != m.n:
+        raise ValueError(f"feats must be [{m.n}, C_in]")
+    if weights.dim() != 3 or weights.shape[0] != 27 or weights.shape[1] != feats.shape[1]:
+        raise ValueError("weights must be [27, C_in, C_out]")
+    c_in, c_out = int(weights.shape[1]), int(weights.shape[2])
+    if out is None:
+        out = torch.empty((m.n, c_out), dtype=feats.dtype, device=feats.device)
+    else:
+        _require_cuda(out, "out")
+        if out.dtype != feats.dtype or tuple(out.shape) != (m.n, c_out):
+            raise ValueError(f"out must be {feats.dtype} [{m.n}, {c_out}]")
+    rc = lib.spconv_subm_forward(m.handle, _ptr(feats), _ptr(weights), _ptr(out), c_in, c_out,
+                                 _DTYPES[feats.dtype], _stream_ptr(stream))
+    _check(rc, "spconv_subm_forward")
+    return out
+
+
+def wpack_create(weights: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> WPack:
+    """``spconv_wpack_create``: pack [27, C_in, C_out] weights once for many forwards."""
+    lib = library()
+    _require_cuda(weights, "weights")
+    if weights.dtype not in _DTYPES or weights.dim() != 3 or weights.shape[0] != 27:
+        raise ValueError("weights must be bf16 or fp32 [27, C_in, C_out]")
+    c_in, c_out = int(weights.shape[1]), int(weights.shape[2])
+    h = ctypes.c_void_p()
+    rc = lib.spconv_wpack_create(_ptr(weights), c_in, c_out, _DTYPES[weights.dtype],
+                                 _stream_ptr(stream), ctypes.byref(h))
+    _check(rc, "spconv_wpack_create")
+    return WPack(h, c_in, c_out, weights.dtype, weights)
+
+
+def subm_forward_packed(m: Map, feats: torch.Tensor, wp: WPack, out: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """``spconv_subm_forward_packed``: forward with weights from ``wpack_create``."""
+    lib = library()
+    _require_cuda(feats, "feats")
+    if feats.dtype != wp.dtype or feats.dim() != 2 or feats.shape != (m.n, wp.c_in):
+        raise ValueError(f"feats must be {wp.dtype} [{m.n}, {wp.c_in}]")
+    if out is None:
+        out = torch.empty((m.n, wp.c_out), dtype=feats.dtype, device=feats.device)
+    else:
+        _require_cuda(out, "out")
+        if out.dtype != feats.dtype or tuple(out.shape) != (m.n, wp.c_out):
+            raise ValueError(f"out must be {feats.dtype} [{m.n}, {wp.c_out}]")
+    rc = lib.spconv_subm_forward_packed(m.handle, _ptr(feats), wp.handle, _ptr(out), _stream_ptr(stream))
+    _check(rc, "spconv_subm_forward_packed")
+    return out
+
+
+def map_status(m: Map) -> int:
+    """``spconv_map_status``: 0, or the first device-detected error code (synchronises)."""
+    return int(library().spconv_map_status(m.handle))
+
+
+def map_info(m: Map) -> dict:
+    """``spconv_map_info`` as a dict (synchronises)."""
+    info = _native.MapInfo()
+    _check(library().spconv_map_info(m.handle, ctypes.byref(info)), "spconv_map_info")
+    return dict(n=info.n, pairs=info.pairs, n_tiles=info.n_tiles, tile_taps=info.tile_taps,
+                mapper={1: "dense", 2: "sorted"}.get(info.mapper, str(info.mapper)),
+                key_bits=info.key_bits, shape=tuple(info.shape), batch_size=info.batch_size)
+
+
+def map_export(m: Map, stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """``spconv_map_export``: nbr [N,27], mask [N], perm [N], tap_off [28], in_rows/out_rows [P]."""
+    info = map_info(m)
+    n, p = info["n"], info["pairs"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    nbr = torch.empty((n, 27), dtype=torch.int32, device=dev)
+    mask = torch.empty((n,), dtype=torch.int32, device=dev)
+    perm = torch.empty((n,), dtype=torch.int32, device=dev)
+    tap_off = torch.empty((28,), dtype=torch.int32, device=dev)
+    ins = torch.empty((max(p, 1),), dtype=torch.int32, device=dev)
+    outs = torch.empty((max(p, 1),), dtype=torch.int32, device=dev)
+    rc = library().spconv_map_export(m.handle, _ptr(nbr), _ptr(mask), _ptr(perm), _ptr(tap_off),
+                                     _ptr(ins), _ptr(outs), _stream_ptr(stream))
+    _check(rc, "spconv_map_export")
+    return dict(nbr=nbr, mask=mask, perm=perm, tap_off=tap_off, in_rows=ins[:p], out_rows=outs[:p],
+                info=info)
+
+
+def map_destroy(m: Map):
+    """``spconv_map_destroy``."""
+    m.destroy()
+
+
+def last_launch_count() -> int:
+    """Kernels the library launched in its last call on this thread."""
+    return int(library().spconv_last_launch_count())

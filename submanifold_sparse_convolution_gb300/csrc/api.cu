@@ -1,0 +1,271 @@
+// C ABI of libspconv (declared in include/spconv.h): argument checks, handle
+// lifetime, dispatch between the tensor-core and SIMT paths.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+
+namespace spconv {
+
+namespace {
+thread_local int g_launches = 0;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+int read_status(const MapHandle* h) {
+    int32_t st = 0;
+    SPCONV_CHECK_CUDA(cudaStreamSynchronize(h->stream));
+    SPCONV_CHECK_CUDA(cudaMemcpy(&st, h->status, sizeof(st), cudaMemcpyDeviceToHost));
+    if (st & kStatusRange) return SPCONV_ERR_COORD_RANGE;
+    if (st & kStatusDuplicate) return SPCONV_ERR_DUPLICATE_COORD;
+    if (st & kStatusTimeout) return SPCONV_ERR_TIMEOUT;
+    return SPCONV_OK;
+}
+
+int check_forward_args(const MapHandle* h, const void* feats, const void* out, int32_t c_in,
+                       int32_t c_out, int32_t dtype) {
+    if (!h) return SPCONV_ERR_INVALID_ARG;
+    if (dtype != SPCONV_BF16 && dtype != SPCONV_FP32) return SPCONV_ERR_INVALID_ARG;
+    if (c_in < 1 || c_out < 1 || c_in > 65536 || c_out > 65536) return SPCONV_ERR_INVALID_ARG;
+    if (h->n == 0) return SPCONV_OK;
+    if (!feats || !out) return SPCONV_ERR_INVALID_ARG;
+    const size_t es = dtype == SPCONV_FP32 ? 4 : 2;
+    if (!aligned(feats, es) || !aligned(out, es)) return SPCONV_ERR_INVALID_ARG;
+    if (overlaps(feats, static_cast<size_t>(h->n) * c_in * es, out, static_cast<size_t>(h->n) * c_out * es))
+        return SPCONV_ERR_ALIAS;
+    return SPCONV_OK;
+}
+
+bool use_tensor_path(int32_t c_in, int32_t c_out, int32_t dtype, const void* feats, const void* out) {
+    return dtype == SPCONV_BF16 && tc_supported(c_in, c_out) && aligned(feats, 16) && aligned(out, 16);
+}
+
+}  // namespace
+
+void count_launch(int n) { g_launches += n; }
+void reset_launch_count() { g_launches = 0; }
+
+}  // namespace spconv
+
+using namespace spconv;
+
+struct spconv_map_s : MapHandle {};
+struct spconv_wpack_s : WPackHandle {};
+
+extern "C" {
+
+int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatial_shape,
+                     int32_t batch_size, int32_t kernel_size, const spconv_options_t* opt,
+                     void* stream, spconv_map_t* out_map) {
+    reset_launch_count();
+    if (!out_map) return SPCONV_ERR_INVALID_ARG;
+    *out_map = nullptr;
+    if (n < 0 || n >= (int64_t(1) << 30)) return SPCONV_ERR_INVALID_ARG;
+    if (n > 0 && (!coords_dev || !aligned(coords_dev, 16))) return SPCONV_ERR_INVALID_ARG;
+    if (kernel_size != 3) return SPCONV_ERR_UNSUPPORTED;
+    if (batch_size < 0) return SPCONV_ERR_INVALID_ARG;
+    if (opt) {
+        if (opt->mapper < SPCONV_MAPPER_AUTO || opt->mapper > SPCONV_MAPPER_SORTED) return SPCONV_ERR_INVALID_ARG;
+        if (opt->bit_order != SPCONV_ORDER_CALIBRATED && opt->bit_order != SPCONV_ORDER_PLAIN)
+            return SPCONV_ERR_INVALID_ARG;
+        if (opt->dense_max_cells < 0) return SPCONV_ERR_INVALID_ARG;
+    }
+    int32_t shape[3] = {1, 1, 1};
+    int32_t batch = batch_size;
+    if (spatial_shape) {
+        for (int a = 0; a < 3; ++a) {
+            if (spatial_shape[a] < 1 || spatial_shape[a] >= (1 << 30)) return SPCONV_ERR_INVALID_ARG;
+            shape[a] = spatial_shape[a];
+        }
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!spatial_shape || batch <= 0) {
+        int32_t dshape[3], dbatch = 1;
+        SPCONV_CHECK(derive_shape(coords_dev, n, s, dshape, &dbatch));
+        if (!spatial_shape) std::memcpy(shape, dshape, sizeof(shape));
+        if (batch <= 0) batch = dbatch;
+    }
+    spconv_map_s* h = new (std::nothrow) spconv_map_s();
+    if (!h) return SPCONV_ERR_OOM;
+    h->stream = s;
+    cudaGetDevice(&h->device);
+    h->n = n;
+    std::memcpy(h->shape, shape, sizeof(shape));
+    h->batch = batch;
+    const int rc = build_map_impl(h, coords_dev, opt);
+    if (rc != SPCONV_OK) {
+        if (h->arena) cudaFreeAsync(h->arena, s);
+        delete h;
+        return rc;
+    }
+    *out_map = h;
+    return SPCONV_OK;
+}
+
+int spconv_subm_forward(spconv_map_t map, const void* feats_dev, const void* weights_dev, void* out_dev,
+                        int32_t c_in, int32_t c_out, int32_t dtype, void* stream) {
+    reset_launch_count();
+    SPCONV_CHECK(check_forward_args(map, feats_dev, out_dev, c_in, c_out, dtype));
+    if (map->n == 0) return SPCONV_OK;
+    if (!weights_dev) return SPCONV_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (use_tensor_path(c_in, c_out, dtype, feats_dev, out_dev) && aligned(weights_dev, 2)) {
+        const size_t need = tc_pack_bytes(c_in, c_out);
+        if (map->wspace_bytes < need) {
+            if (map->wspace) cudaFreeAsync(map->wspace, s);
+            map->wspace = nullptr;
+            map->wspace_bytes = 0;
+            if (cudaMallocAsync(&map->wspace, need, s) != cudaSuccess) {
+                cudaGetLastError();
+                map->wspace = nullptr;
+                return SPCONV_ERR_OOM;
+            }
+            map->wspace_bytes = need;
+        }
+        SPCONV_CHECK(tc_pack_weights(weights_dev, c_in, c_out, map->wspace, s));
+        return tc_forward(map, feats_dev, map->wspace, out_dev, c_in, c_out, s);
+    }
+    return simt_forward(map, feats_dev, weights_dev, out_dev, c_in, c_out, dtype, s);
+}
+
+int spconv_wpack_create(const void* weights_dev, int32_t c_in, int32_t c_out, int32_t dtype, void* stream,
+                        spconv_wpack_t* out_wpack) {
+    reset_launch_count();
+    if (!out_wpack) return SPCONV_ERR_INVALID_ARG;
+    *out_wpack = nullptr;
+    if (!weights_dev || c_in < 1 || c_out < 1 || c_in > 65536 || c_out > 65536) return SPCONV_ERR_INVALID_ARG;
+    if (dtype != SPCONV_BF16 && dtype != SPCONV_FP32) return SPCONV_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    spconv_wpack_s* w = new (std::nothrow) spconv_wpack_s();
+    if (!w) return SPCONV_ERR_OOM;
+    w->c_in = c_in;
+    w->c_out = c_out;
+    w->dtype = dtype;
+    w->stream = s;
+    w->tensor_path = (dtype == SPCONV_BF16 && tc_supported(c_in, c_out)) ? 1 : 0;
+    const size_t es = dtype == SPCONV_FP32 ? 4 : 2;
+    w->bytes = w->tensor_path ? tc_pack_bytes(c_in, c_out) : static_cast<size_t>(kTaps) * c_in * c_out * es;
+    if (cudaMallocAsync(&w->data, w->bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        delete w;
+        return SPCONV_ERR_OOM;
+    }
+    int rc = SPCONV_OK;
+    if (w->tensor_path) {
+        w->n_tile = tc_tile_n(c_out);
+        rc = tc_pack_weights(weights_dev, c_in, c_out, w->data, s);
+    } else {
+        rc = cuda_status(cudaMemcpyAsync(w->data, weights_dev, w->bytes, cudaMemcpyDeviceToDevice, s));
+    }
+    if (rc != SPCONV_OK) {
+        cudaFreeAsync(w->data, s);
+        delete w;
+        return rc;
+    }
+    *out_wpack = w;
+    return SPCONV_OK;
+}
+
+int spconv_subm_forward_packed(spconv_map_t map, const void* feats_dev, spconv_wpack_t wpack, void* out_dev,
+                               void* stream) {
+    reset_launch_count();
+    if (!wpack) return SPCONV_ERR_INVALID_ARG;
+    SPCONV_CHECK(check_forward_args(map, feats_dev, out_dev, wpack->c_in, wpack->c_out, wpack->dtype));
+    if (map->n == 0) return SPCONV_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (wpack->tensor_path) {
+        if (!aligned(feats_dev, 16) || !aligned(out_dev, 16)) return SPCONV_ERR_INVALID_ARG;
+        return tc_forward(map, feats_dev, wpack->data, out_dev, wpack->c_in, wpack->c_out, s);
+    }
+    return simt_forward(map, feats_dev, wpack->data, out_dev, wpack->c_in, wpack->c_out, wpack->dtype, s);
+}
+
+void spconv_wpack_destroy(spconv_wpack_t wpack) {
+    if (!wpack) return;
+    if (wpack->data) cudaFreeAsync(wpack->data, wpack->stream);
+    delete wpack;
+}
+
+int spconv_map_status(spconv_map_t map) {
+    if (!map) return SPCONV_ERR_INVALID_ARG;
+    return read_status(map);
+}
+
+int spconv_map_info(spconv_map_t map, spconv_map_info_t* info) {
+    if (!map || !info) return SPCONV_ERR_INVALID_ARG;
+    int32_t totals[2] = {0, 0};
+    SPCONV_CHECK_CUDA(cudaStreamSynchronize(map->stream));
+    SPCONV_CHECK_CUDA(cudaMemcpy(totals, map->totals, sizeof(totals), cudaMemcpyDeviceToHost));
+    info->n = map->n;
+    info->pairs = totals[0];
+    info->n_tiles = map->n_tiles;
+    info->tile_taps = totals[1];
+    info->mapper = map->mapper;
+    info->key_bits = map->key_bits;
+    std::memcpy(info->shape, map->shape, sizeof(info->shape));
+    info->batch_size = map->batch;
+    return SPCONV_OK;
+}
+
+int spconv_map_export(spconv_map_t map, int32_t* nbr_dev, uint32_t* mask_dev, int32_t* perm_dev,
+                      int32_t* tap_off_dev, int32_t* in_rows_dev, int32_t* out_rows_dev, void* stream) {
+    reset_launch_count();
+    if (!map) return SPCONV_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t n = map->n;
+    if (n > 0 && nbr_dev)
+        SPCONV_CHECK_CUDA(cudaMemcpy2DAsync(nbr_dev, kTaps * sizeof(int32_t), map->nbr, kNbrStride * sizeof(int32_t),
+                                            kTaps * sizeof(int32_t), static_cast<size_t>(n), cudaMemcpyDeviceToDevice, s));
+    if (n > 0 && mask_dev)
+        SPCONV_CHECK_CUDA(cudaMemcpyAsync(mask_dev, map->mask, n * sizeof(uint32_t), cudaMemcpyDeviceToDevice, s));
+    if (n > 0 && perm_dev)
+        SPCONV_CHECK_CUDA(cudaMemcpyAsync(perm_dev, map->perm, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+    if (tap_off_dev)
+        SPCONV_CHECK_CUDA(cudaMemcpyAsync(tap_off_dev, map->tap_off, (kTaps + 1) * sizeof(int32_t),
+                                          cudaMemcpyDeviceToDevice, s));
+    if (in_rows_dev || out_rows_dev) {
+        spconv_map_info_t info;
+        SPCONV_CHECK(spconv_map_info(map, &info));
+        if (info.pairs > 0 && in_rows_dev)
+            SPCONV_CHECK_CUDA(cudaMemcpyAsync(in_rows_dev, map->in_rows, info.pairs * sizeof(int32_t),
+                                              cudaMemcpyDeviceToDevice, s));
+        if (info.pairs > 0 && out_rows_dev)
+            SPCONV_CHECK_CUDA(cudaMemcpyAsync(out_rows_dev, map->out_rows, info.pairs * sizeof(int32_t),
+                                              cudaMemcpyDeviceToDevice, s));
+    }
+    return SPCONV_OK;
+}
+
+void spconv_map_destroy(spconv_map_t map) {
+    if (!map) return;
+    if (map->arena) cudaFreeAsync(map->arena, map->stream);
+    if (map->wspace) cudaFreeAsync(map->wspace, map->stream);
+    delete map;
+}
+
+int32_t spconv_last_launch_count(void) { return g_launches; }
+
+const char* spconv_status_string(int status) {
+    switch (status) {
+        case SPCONV_OK: return "ok";
+        case SPCONV_ERR_INVALID_ARG: return "invalid argument";
+        case SPCONV_ERR_UNSUPPORTED: return "unsupported";
+        case SPCONV_ERR_OOM: return "out of device memory";
+        case SPCONV_ERR_CUDA: return "CUDA runtime error";
+        case SPCONV_ERR_DUPLICATE_COORD: return "duplicate coordinate";
+        case SPCONV_ERR_COORD_RANGE: return "coordinate out of range";
+        case SPCONV_ERR_ALIAS: return "output overlaps input";
+        case SPCONV_ERR_TIMEOUT: return "kernel wait timed out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

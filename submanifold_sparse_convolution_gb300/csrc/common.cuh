@@ -1,0 +1,106 @@
+// Internal declarations shared by the translation units of libspconv.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/spconv.h"
+
+namespace spconv {
+
+constexpr int kTaps = 27;
+constexpr int kTileRows = 128;      // rows per output tile (tensor-core M)
+constexpr int kNbrStride = 32;      // padded width of the internal kernel-map rows
+
+// Device status word bits (set with atomicOr by kernels).
+enum : int32_t {
+    kStatusDuplicate = 1,
+    kStatusRange = 2,
+    kStatusTimeout = 4,
+};
+
+// Counts launches of the current host thread (reported by
+// spconv_last_launch_count).
+void count_launch(int n = 1);
+void reset_launch_count();
+
+// A stream-ordered device buffer.
+struct DevBuf {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+
+struct MapHandle {
+    cudaStream_t stream = nullptr;
+    int device = 0;
+    int64_t n = 0;
+    int64_t n_tiles = 0;
+    int64_t n_pad = 0;        // n_tiles * kTileRows
+    int32_t shape[3] = {0, 0, 0};
+    int32_t batch = 0;
+    int32_t mapper = 0;       // spconv_mapper_t used
+    int32_t bit_order = 0;
+    int32_t key_bits = 0;
+    // device arrays
+    int32_t* status = nullptr;     // [1]
+    int32_t* nbr = nullptr;        // [n][kNbrStride], original row order
+    uint32_t* mask = nullptr;      // [n]
+    int32_t* perm = nullptr;       // [n_pad] (rows >= n: -1)
+    int32_t* tap_count = nullptr;  // [27]
+    int32_t* tap_pos = nullptr;    // [27] key bit of each tap
+    int32_t* tap_off = nullptr;    // [28]
+    int32_t* in_rows = nullptr;    // [27 n]
+    int32_t* out_rows = nullptr;   // [27 n]
+    int32_t* gtab = nullptr;       // [27][n_pad]: nbr[perm[s]][k] or -1
+    uint32_t* tile_union = nullptr;  // [n_tiles]
+    int32_t* tile_order = nullptr;   // [n_tiles], tiles by descending union size
+    int32_t* seg_off = nullptr;      // [27][n_tiles] pair offset of (tap, tile)
+    int32_t* totals = nullptr;       // [2]: pairs, sum of union sizes
+    void* arena = nullptr;           // one allocation holding the arrays above
+    size_t arena_bytes = 0;
+    // weight workspace for spconv_subm_forward
+    void* wspace = nullptr;
+    size_t wspace_bytes = 0;
+};
+
+struct WPackHandle {
+    int32_t c_in = 0, c_out = 0, dtype = 0;
+    int32_t tensor_path = 0;   // 1: tcgen05 shared-memory image, 0: row-major copy for SIMT
+    int32_t n_tile = 0;        // output channels per tensor-core tile
+    int32_t k_chunks = 0;      // 64-wide input-channel chunks
+    void* data = nullptr;
+    size_t bytes = 0;
+    cudaStream_t stream = nullptr;
+};
+
+// ---- map building (map.cu) -----------------------------------------------
+int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* opt);
+int derive_shape(const int32_t* coords, int64_t n, cudaStream_t stream, int32_t shape[3],
+                 int32_t* batch);
+
+// ---- tensor-core GEMM (gemm_tc.cu) ------------------------------------------
+bool tc_supported(int32_t c_in, int32_t c_out);
+int tc_tile_n(int32_t c_out);
+size_t tc_pack_bytes(int32_t c_in, int32_t c_out);
+int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, void* dst, cudaStream_t s);
+int tc_forward(const MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
+               int32_t c_out, cudaStream_t s);
+
+// ---- SIMT path (gemm_simt.cu) ----------------------------------------------
+int simt_forward(const MapHandle* h, const void* feats, const void* w, void* out, int32_t c_in,
+                 int32_t c_out, int32_t dtype, cudaStream_t s);
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPCONV_OK : SPCONV_ERR_CUDA; }
+
+}  // namespace spconv
+
+#define SPCONV_CHECK_CUDA(call)                             \
+    do {                                                    \
+        cudaError_t e_ = (call);                            \
+        if (e_ != cudaSuccess) return SPCONV_ERR_CUDA;      \
+    } while (0)
+
+#define SPCONV_CHECK(call)                                  \
+    do {                                                    \
+        int s_ = (call);                                    \
+        if (s_ != SPCONV_OK) return s_;                     \
+    } while (0)

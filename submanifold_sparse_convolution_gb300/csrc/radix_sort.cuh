@@ -1,0 +1,155 @@
+// Stable LSD radix sort of (key, value) pairs on the device, 8 bits per pass.
+//
+// Each pass is reduce-then-scan with no atomics on global memory and no
+// inter-block waiting: an upsweep writes per-tile digit counts, one block
+// scans them (digit-major, so the scan yields every tile's output offset for
+// every digit), and a downsweep ranks each tile's keys stably and scatters
+// them.  Used for the packed coordinate keys (mapper) and for the 27-bit mask
+// keys (row order for the output tiles).
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace spconv {
+namespace rsort {
+
+constexpr int kThreads = 256;
+constexpr int kItems = 8;
+constexpr int kTile = kThreads * kItems;  // 2048 keys per block
+constexpr int kBins = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kScanThreads = 1024;
+
+inline int64_t num_tiles(int64_t n) { return (n + kTile - 1) / kTile; }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+template <typename K>
+__global__ void __launch_bounds__(kThreads) upsweep(const K* __restrict__ keys, int64_t n, int shift,
+                                                   int32_t* __restrict__ hist, int64_t nb) {
+    __shared__ int32_t h[kBins];
+    for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0;
+    __syncthreads();
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kTile;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+        const int64_t idx = base + j * kThreads + threadIdx.x;
+        const bool valid = idx < n;
+        const int d = valid ? static_cast<int>((keys[idx] >> shift) & 0xFF) : kBins;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d);
+        if (valid && lane == __ffs(peers) - 1) atomicAdd(&h[d], __popc(peers));
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kBins; i += kThreads) hist[static_cast<int64_t>(i) * nb + blockIdx.x] = h[i];
+}
+
+// Exclusive scan, in place, of m int32 values (one block).
+__global__ void __launch_bounds__(kScanThreads) scan_exclusive(int32_t* __restrict__ a, int64_t m) {
+    __shared__ int32_t part[kScanThreads];
+    const int64_t chunk = (m + kScanThreads - 1) / kScanThreads;
+    const int64_t lo = threadIdx.x * chunk;
+    const int64_t hi = lo + chunk < m ? lo + chunk : m;
+    int32_t s = 0;
+    for (int64_t i = lo; i < hi; ++i) s += a[i];
+    part[threadIdx.x] = s;
+    __syncthreads();
+    // Hillis-Steele inclusive scan of the partial sums
+    for (int off = 1; off < kScanThreads; off <<= 1) {
+        int32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
+    for (int64_t i = lo; i < hi; ++i) {
+        const int32_t v = a[i];
+        a[i] = run;
+        run += v;
+    }
+}
+
+template <typename K>
+__global__ void __launch_bounds__(kThreads) downsweep(const K* __restrict__ keys_in,
+                                                     const uint32_t* __restrict__ vals_in,
+                                                     K* __restrict__ keys_out,
+                                                     uint32_t* __restrict__ vals_out, int64_t n,
+                                                     int shift, const int32_t* __restrict__ hist,
+                                                     int64_t nb) {
+    // cnt[j][w][d]: keys of item slot j in warp w with digit d; then the
+    // exclusive prefix of those counts in tile order (j, w, lane).
+    __shared__ uint16_t cnt[kItems][kWarps][kBins];
+    __shared__ int32_t gbase[kBins];
+    uint32_t* cz = reinterpret_cast<uint32_t*>(&cnt[0][0][0]);
+    for (int i = threadIdx.x; i < kItems * kWarps * kBins / 2; i += kThreads) cz[i] = 0;
+    for (int i = threadIdx.x; i < kBins; i += kThreads) gbase[i] = hist[static_cast<int64_t>(i) * nb + blockIdx.x];
+    __syncthreads();
+
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kTile;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    K key[kItems];
+    uint32_t val[kItems];
+    int dig[kItems];
+    int rank[kItems];
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+        const int64_t idx = base + j * kThreads + threadIdx.x;
+        const bool valid = idx < n;
+        key[j] = valid ? keys_in[idx] : K(0);
+        val[j] = valid ? vals_in[idx] : 0u;
+        dig[j] = valid ? static_cast<int>((key[j] >> shift) & 0xFF) : kBins;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dig[j]);
+        rank[j] = __popc(peers & lanemask_lt());
+        if (valid && lane == __ffs(peers) - 1) cnt[j][warp][dig[j]] = static_cast<uint16_t>(__popc(peers));
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < kBins; d += kThreads) {
+        uint32_t run = 0;
+        for (int j = 0; j < kItems; ++j)
+            for (int w = 0; w < kWarps; ++w) {
+                const uint32_t c = cnt[j][w][d];
+                cnt[j][w][d] = static_cast<uint16_t>(run);
+                run += c;
+            }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+        if (dig[j] < kBins) {
+            const int64_t dst = static_cast<int64_t>(gbase[dig[j]]) + cnt[j][warp][dig[j]] + rank[j];
+            keys_out[dst] = key[j];
+            vals_out[dst] = val[j];
+        }
+    }
+}
+
+// Sort (keys, vals) of length n on the live low `bits` of the key.  Returns
+// true if the result ended in (keys_b, vals_b), false if in (keys_a, vals_a).
+// hist needs kBins * num_tiles(n) int32.
+template <typename K>
+bool sort_pairs(K* keys_a, uint32_t* vals_a, K* keys_b, uint32_t* vals_b, int64_t n, int bits,
+                int32_t* hist, cudaStream_t s, int* launches) {
+    if (n <= 1 || bits <= 0) return false;
+    const int64_t nb = num_tiles(n);
+    const int passes = (bits + 7) / 8;
+    bool in_b = false;
+    for (int p = 0; p < passes; ++p) {
+        const K* kin = in_b ? keys_b : keys_a;
+        const uint32_t* vin = in_b ? vals_b : vals_a;
+        K* kout = in_b ? keys_a : keys_b;
+        uint32_t* vout = in_b ? vals_a : vals_b;
+        upsweep<K><<<static_cast<unsigned>(nb), kThreads, 0, s>>>(kin, n, 8 * p, hist, nb);
+        scan_exclusive<<<1, kScanThreads, 0, s>>>(hist, kBins * nb);
+        downsweep<K><<<static_cast<unsigned>(nb), kThreads, 0, s>>>(kin, vin, kout, vout, n, 8 * p, hist, nb);
+        *launches += 3;
+        in_b = !in_b;
+    }
+    return in_b;
+}
+
+}  // namespace rsort
+}  // namespace spconv

@@ -1,0 +1,268 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Kernel maps, masks, row order and pair lists must match bit for bit.  bf16
+outputs (fp32 accumulation, one rounding) must satisfy
+|out - ref| <= 2e-2 * (1 + |ref|) against the fp64 oracle; fp32 exact-mode
+outputs |out - ref| <= 1e-5.  Small cases compare every output; the full-size
+workloads compare every integer output and a seeded sample of feature rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import submanifold_sparse_convolution_gb300 as sc
+from submanifold_sparse_convolution_gb300 import build as build_mod
+from submanifold_sparse_convolution_gb300 import synthetic as S
+
+pytestmark = pytest.mark.gpu
+
+BF16_RTOL = 2e-2
+FP32_ATOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_mod.build()
+    oracle.build()
+
+
+def oracle_map(coords, shape, batch, calibrated=True):
+    nbr = oracle.kernel_map(coords, shape, batch)
+    m = oracle.masks(nbr)
+    p = oracle.perm(oracle.sort_keys(m, oracle.tap_order(m, calibrated)))
+    tap_off, ins, outs = oracle.pair_lists(nbr, p)
+    return dict(nbr=nbr, mask=m, perm=p, tap_off=tap_off, in_rows=ins, out_rows=outs)
+
+
+def assert_map_equal(ex, ref):
+    assert np.array_equal(ex["nbr"].cpu().numpy(), ref["nbr"])
+    assert np.array_equal(ex["mask"].cpu().numpy().view(np.uint32), ref["mask"])
+    assert np.array_equal(ex["perm"].cpu().numpy(), ref["perm"])
+    assert np.array_equal(ex["tap_off"].cpu().numpy(), ref["tap_off"])
+    assert np.array_equal(ex["in_rows"].cpu().numpy(), ref["in_rows"])
+    assert np.array_equal(ex["out_rows"].cpu().numpy(), ref["out_rows"])
+
+
+def check_bf16(out, ref):
+    got = out.double().cpu().numpy()
+    err = np.abs(got - ref)
+    bound = BF16_RTOL * (1.0 + np.abs(ref))
+    worst = float((err / bound).max()) if err.size else 0.0
+    assert np.all(err <= bound), f"max err/bound {worst:.3f}"
+    return worst
+
+
+def check_fp32(out, ref):
+    err = np.abs(out.double().cpu().numpy() - ref)
+    assert err.size == 0 or err.max() <= FP32_ATOL, f"max abs err {err.max():.3e}"
+
+
+def build(wl, mapper="auto", bit_order="calibrated"):
+    coords = wl.coords.cuda()
+    m = sc.build_map(coords, wl.spatial_shape, wl.batch_size, mapper=mapper, bit_order=bit_order)
+    assert sc.map_status(m) == 0
+    return m
+
+
+# ---------------------------------------------------------------------------
+# kernel map and pair lists
+# ---------------------------------------------------------------------------
+
+SMALL = [(1, 1, (4, 4, 4), 1), (2, 7, (5, 5, 5), 1), (3, 127, (8, 8, 8), 1), (4, 128, (8, 8, 8), 1),
+         (5, 129, (8, 8, 8), 2), (6, 1000, (12, 12, 12), 3), (7, 5000, (24, 24, 24), 2),
+         (8, 27, (3, 3, 3), 1), (9, 4096, (16, 16, 16), 1)]
+
+
+@pytest.mark.parametrize("seed,n,shape,batch", SMALL)
+@pytest.mark.parametrize("mapper", ["dense", "sorted"])
+@pytest.mark.parametrize("bit_order", ["calibrated", "plain"])
+def test_map_small(seed, n, shape, batch, mapper, bit_order):
+    wl = S.random_cloud(seed, n, shape=shape, batch_size=batch)
+    m = build(wl, mapper, bit_order)
+    ref = oracle_map(wl.coords.numpy(), shape, batch, bit_order == "calibrated")
+    assert_map_equal(sc.map_export(m), ref)
+    info = sc.map_info(m)
+    assert info["mapper"] == mapper and info["pairs"] == int(ref["tap_off"][27])
+
+
+@pytest.mark.parametrize("name", ["tiny", "outdoor", "deep", "large", "stage"])
+def test_map_workloads(name):
+    coords, shape, batch, _ = S.make_coords(name)
+    wl = S.Workload(name, torch.from_numpy(coords), shape, batch, 1, 1, None, [], 0)
+    m = build(wl)
+    ref = oracle_map(coords, shape, batch)
+    ex = sc.map_export(m)
+    assert_map_equal(ex, ref)
+    info = ex["info"]
+    assert info["mapper"] == ("dense" if name in ("tiny", "deep") else "sorted")
+
+
+@pytest.mark.parametrize("name", ["tiny", "deep"])
+def test_dense_and_sorted_mappers_agree(name):
+    coords, shape, batch, _ = S.make_coords(name)
+    wl = S.Workload(name, torch.from_numpy(coords), shape, batch, 1, 1, None, [], 0)
+    a = sc.map_export(build(wl, "dense"))
+    b = sc.map_export(build(wl, "sorted"))
+    for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_derived_shape_and_batch():
+    wl = S.random_cloud(21, 900, shape=(10, 11, 12), batch_size=3)
+    explicit = sc.map_export(build(wl))
+    m = sc.build_map(wl.coords.cuda())          # shape and batch derived on the device
+    info = sc.map_info(m)
+    c = wl.coords.numpy()
+    assert info["batch_size"] == int(c[:, 0].max()) + 1
+    assert info["shape"] == tuple(int(v) + 1 for v in c[:, 1:].max(0))
+    derived = sc.map_export(m)
+    for key in ("nbr", "mask", "in_rows", "out_rows"):
+        assert torch.equal(explicit[key], derived[key]), key
+
+
+def test_empty_input():
+    coords = torch.zeros((0, 4), dtype=torch.int32, device="cuda")
+    m = sc.build_map(coords, (4, 4, 4), 1)
+    assert sc.map_status(m) == 0
+    assert sc.map_info(m)["pairs"] == 0
+    out = sc.subm_forward(m, torch.zeros((0, 16), dtype=torch.bfloat16, device="cuda"),
+                          torch.zeros((27, 16, 16), dtype=torch.bfloat16, device="cuda"))
+    assert out.shape == (0, 16)
+
+
+def test_duplicate_and_range_errors():
+    dup = torch.tensor([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=torch.int32, device="cuda")
+    for mapper in ("dense", "sorted"):
+        m = sc.build_map(dup, (4, 4, 4), 1, mapper=mapper)
+        assert sc.map_status(m) == -5
+    bad = torch.tensor([[0, 1, 1, 1], [0, 4, 0, 0]], dtype=torch.int32, device="cuda")
+    for mapper in ("dense", "sorted"):
+        m = sc.build_map(bad, (4, 4, 4), 1, mapper=mapper)
+        assert sc.map_status(m) == -6
+    neg = torch.tensor([[0, 1, 1, 1], [0, -1, 0, 0]], dtype=torch.int32, device="cuda")
+    with pytest.raises(sc.SpconvError):
+        sc.build_map(neg)                       # derived shape sees the negative coordinate
+
+
+def test_alias_rejected():
+    wl = S.random_cloud(22, 300, shape=(8, 8, 8), c_in=16, c_out=16)
+    m = build(wl)
+    buf = torch.zeros((300, 16), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sc.SpconvError) as e:
+        sc.subm_forward(m, buf, wl.weights[0].cuda(), out=buf)
+    assert e.value.code == -7
+
+
+# ---------------------------------------------------------------------------
+# features
+# ---------------------------------------------------------------------------
+
+CHANNELS = [(16, 16), (64, 64), (128, 128), (24, 48), (8, 32), (256, 512), (512, 512), (3, 5), (1, 1),
+            (16, 20)]
+
+
+@pytest.mark.parametrize("c_in,c_out", CHANNELS)
+def test_bf16_forward_small(c_in, c_out):
+    wl = S.random_cloud(100 + c_in + c_out, 1500, shape=(14, 14, 14), batch_size=2, c_in=c_in, c_out=c_out)
+    m = build(wl)
+    out = sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
+    assert sc.map_status(m) == 0
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    ref = oracle.conv_f64(nbr, wl.feats.double().numpy(), wl.weights[0].double().numpy())
+    check_bf16(out, ref)
+
+
+@pytest.mark.parametrize("c_in,c_out", [(64, 64), (16, 16), (5, 7), (128, 128)])
+def test_fp32_exact_small(c_in, c_out):
+    wl = S.random_cloud(200 + c_in, 2000, shape=(14, 14, 14), c_in=c_in, c_out=c_out)
+    rng = np.random.default_rng(201)
+    f = torch.from_numpy(rng.standard_normal((wl.n, c_in)).astype(np.float32))
+    w = torch.from_numpy((rng.standard_normal((27, c_in, c_out)) * S.weights_std(c_in)).astype(np.float32))
+    m = build(wl)
+    out = sc.subm_forward(m, f.cuda(), w.cuda())
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1)
+    check_fp32(out, oracle.conv_f64(nbr, f.double().numpy(), w.double().numpy()))
+
+
+def test_packed_weights_match_unpacked():
+    wl = S.random_cloud(31, 3000, shape=(16, 16, 16), c_in=128, c_out=128)
+    m = build(wl)
+    f, w = wl.feats.cuda(), wl.weights[0].cuda()
+    a = sc.subm_forward(m, f, w)
+    wp = sc.wpack_create(w)
+    b = sc.subm_forward_packed(m, f, wp)
+    c = sc.subm_forward_packed(m, f, wp)
+    assert torch.equal(a, b) and torch.equal(b, c)
+
+
+def test_row_permutation_equivariance():
+    wl = S.random_cloud(41, 2500, shape=(16, 16, 16), c_in=64, c_out=64)
+    q = torch.from_numpy(np.random.default_rng(42).permutation(wl.n))
+    m1, m2 = build(wl), None
+    out1 = sc.subm_forward(m1, wl.feats.cuda(), wl.weights[0].cuda())
+    coords2 = wl.coords[q].contiguous().cuda()
+    m2 = sc.build_map(coords2, wl.spatial_shape, 1)
+    out2 = sc.subm_forward(m2, wl.feats[q].contiguous().cuda(), wl.weights[0].cuda())
+    torch.testing.assert_close(out2.float(), out1[q.cuda()].float(), rtol=1e-2, atol=1e-2)
+
+
+def test_isolated_voxels_use_centre_tap_only():
+    coords = torch.tensor([[0, 0, 0, 0], [0, 5, 5, 5], [0, 9, 2, 7], [1, 3, 3, 3]], dtype=torch.int32)
+    rng = np.random.default_rng(43)
+    f = torch.from_numpy(rng.standard_normal((4, 128)).astype(np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy((rng.standard_normal((27, 128, 128)) * 0.05).astype(np.float32)).to(torch.bfloat16)
+    m = sc.build_map(coords.cuda(), (10, 10, 10), 2)
+    out = sc.subm_forward(m, f.cuda(), w.cuda())
+    ref = f.double().numpy() @ w[13].double().numpy()
+    check_bf16(out, ref)
+
+
+def sample_rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(n, size=min(n, k), replace=False)
+    return np.unique(np.concatenate([rows, [0, n - 1]])).astype(np.int32)
+
+
+@pytest.mark.parametrize("name", ["tiny", "outdoor", "deep", "large"])
+def test_bf16_workloads(name):
+    wl = S.make_workload(name)
+    m = build(wl)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    f, w = wl.feats.cuda(), wl.weights[0].cuda()
+    wp = sc.wpack_create(w)
+    out = sc.subm_forward_packed(m, f, wp)
+    assert sc.map_status(m) == 0
+    rows = None if name == "tiny" else sample_rows(wl.n, 3000, 7)
+    ref = oracle.conv_f64(nbr, wl.feats.double().numpy(), wl.weights[0].double().numpy(), rows=rows)
+    check_bf16(out if rows is None else out[torch.from_numpy(rows).long().cuda()], ref)
+    # the unpacked entry point gives the same bits
+    assert torch.equal(out, sc.subm_forward(m, f, w))
+
+
+def test_stage_six_layers_and_fp32_layer():
+    wl = S.make_workload("stage")
+    m = build(wl)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    rows = sample_rows(wl.n, 2000, 11)
+    rows_t = torch.from_numpy(rows).long().cuda()
+    x = wl.feats.cuda()
+    for layer, w in enumerate(wl.weights):
+        y = sc.subm_forward(m, x, w.cuda())
+        ref = oracle.conv_f64(nbr, x.double().cpu().numpy(), w.double().numpy(), rows=rows)
+        check_bf16(y[rows_t], ref)
+        x = torch.relu(y)
+    # the first layer again in exact fp32
+    f32 = wl.feats.float().cuda()
+    w32 = wl.weights[0].float().cuda()
+    y32 = sc.subm_forward(m, f32, w32)
+    ref = oracle.conv_f64(nbr, wl.feats.double().numpy(), wl.weights[0].double().numpy(), rows=rows)
+    check_fp32(y32[rows_t], ref)
+
+
+def test_launch_count_reported():
+    wl = S.random_cloud(51, 3000, shape=(16, 16, 16), c_in=64, c_out=64)
+    m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1)
+    assert sc.last_launch_count() > 5
+    sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
+    assert sc.last_launch_count() == 2          # weight pack + GEMM
