@@ -48,7 +48,8 @@ typedef enum {
     SPCONV_ERR_DUPLICATE_COORD = -5,
     SPCONV_ERR_COORD_RANGE = -6,   /* b, x, y or z outside [0, batch) x [0, shape)          */
     SPCONV_ERR_ALIAS = -7,         /* out overlaps feats                                     */
-    SPCONV_ERR_TIMEOUT = -8        /* a bounded wait inside a kernel ran out                 */
+    SPCONV_ERR_TIMEOUT = -8,       /* a bounded wait inside a kernel ran out                 */
+    SPCONV_ERR_INTERNAL = -9       /* a kernel's consistency guard fired (a library bug)     */
 } spconv_status_t;
 
 typedef enum { SPCONV_BF16 = 0, SPCONV_FP32 = 1 } spconv_dtype_t;
@@ -64,11 +65,20 @@ typedef enum {
     SPCONV_ORDER_PLAIN = 1       /* sort key = the 27-bit mask itself                             */
 } spconv_bit_order_t;
 
-/* Options of spconv_build_map.  Pass NULL for the defaults. */
+typedef enum {
+    SPCONV_PIPELINE_AUTO = 0,  /* single launch when it applies, else one kernel per step        */
+    SPCONV_PIPELINE_FUSED = 1, /* whole build in one thread-block-cluster launch (n <= 2^20)     */
+    SPCONV_PIPELINE_MULTI = 2  /* one kernel per step (any n)                                     */
+} spconv_pipeline_t;
+
+/* Options of spconv_build_map.  Pass NULL for the defaults.  None of them
+ * changes any result; they select how the same map is built. */
 typedef struct {
     int32_t mapper;          /* spconv_mapper_t, default AUTO                          */
     int32_t bit_order;       /* spconv_bit_order_t, default CALIBRATED                 */
     int64_t dense_max_cells; /* AUTO threshold on B*(X+2)*(Y+2)*(Z+2); default 1<<24   */
+    int32_t pipeline;        /* spconv_pipeline_t, default AUTO                        */
+    int32_t reserved;        /* must be 0                                              */
 } spconv_options_t;
 
 typedef struct spconv_map_s* spconv_map_t;
@@ -81,6 +91,7 @@ typedef struct {
     int64_t n_tiles;     /* 128-row tiles of the mask-sorted order                */
     int64_t tile_taps;   /* sum over tiles of the taps in the tile's mask union   */
     int32_t mapper;      /* spconv_mapper_t actually used (DENSE or SORTED)       */
+    int32_t pipeline;    /* spconv_pipeline_t actually used (FUSED or MULTI)      */
     int32_t key_bits;    /* live bits of the packed coordinate key                */
     int32_t shape[3];    /* spatial shape used                                    */
     int32_t batch_size;  /* batch size used                                       */

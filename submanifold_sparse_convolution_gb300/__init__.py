@@ -19,9 +19,10 @@ from . import _native
 
 __all__ = ["SpconvError", "Map", "WPack", "build_map", "subm_forward", "wpack_create",
            "subm_forward_packed", "map_status", "map_info", "map_export", "map_destroy",
-           "last_launch_count", "status_string", "MAPPERS", "BIT_ORDERS", "library"]
+           "last_launch_count", "status_string", "MAPPERS", "BIT_ORDERS", "PIPELINES", "library"]
 
 MAPPERS = {"auto": 0, "dense": 1, "sorted": 2}
+PIPELINES = {"auto": 0, "fused": 1, "multi": 2}
 BIT_ORDERS = {"calibrated": 0, "plain": 1}
 _DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
@@ -116,7 +117,7 @@ class WPack:
 
 def build_map(coords: torch.Tensor, spatial_shape: Optional[Sequence[int]] = None,
               batch_size: int = 0, kernel_size: int = 3, mapper: str = "auto",
-              bit_order: str = "calibrated", dense_max_cells: int = 0,
+              bit_order: str = "calibrated", dense_max_cells: int = 0, pipeline: str = "auto",
               stream: Optional[torch.cuda.Stream] = None) -> Map:
     """``spconv_build_map``: kernel map of ``coords`` (int32 [N, 4] (b, x, y, z) on the GPU).
 
@@ -130,7 +131,8 @@ def build_map(coords: torch.Tensor, spatial_shape: Optional[Sequence[int]] = Non
     shape_arr = None
     if spatial_shape is not None:
         shape_arr = (ctypes.c_int32 * 3)(*[int(v) for v in spatial_shape])
-    opt = _native.Options(MAPPERS[mapper], BIT_ORDERS[bit_order], int(dense_max_cells))
+    opt = _native.Options(MAPPERS[mapper], BIT_ORDERS[bit_order], int(dense_max_cells),
+                          PIPELINES[pipeline], 0)
     h = ctypes.c_void_p()
     rc = lib.spconv_build_map(_ptr(coords), int(coords.shape[0]),
                               ctypes.cast(shape_arr, _native.c_int32_p) if shape_arr is not None else None,
@@ -213,6 +215,7 @@ def map_info(m: Map) -> dict:
     _check(library().spconv_map_info(m.handle, ctypes.byref(info)), "spconv_map_info")
     return dict(n=info.n, pairs=info.pairs, n_tiles=info.n_tiles, tile_taps=info.tile_taps,
                 mapper={1: "dense", 2: "sorted"}.get(info.mapper, str(info.mapper)),
+                pipeline={1: "fused", 2: "multi"}.get(info.pipeline, str(info.pipeline)),
                 key_bits=info.key_bits, shape=tuple(info.shape), batch_size=info.batch_size)
 
 

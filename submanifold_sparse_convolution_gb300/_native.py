@@ -16,12 +16,14 @@ c_int32_p = ctypes.POINTER(ctypes.c_int32)
 
 class Options(ctypes.Structure):
     _fields_ = [("mapper", ctypes.c_int32), ("bit_order", ctypes.c_int32),
-                ("dense_max_cells", ctypes.c_int64)]
+                ("dense_max_cells", ctypes.c_int64), ("pipeline", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class MapInfo(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("pairs", ctypes.c_int64), ("n_tiles", ctypes.c_int64),
                 ("tile_taps", ctypes.c_int64), ("mapper", ctypes.c_int32),
+                ("pipeline", ctypes.c_int32),
                 ("key_bits", ctypes.c_int32), ("shape", ctypes.c_int32 * 3),
                 ("batch_size", ctypes.c_int32)]
 

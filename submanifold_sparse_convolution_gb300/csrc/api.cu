@@ -27,6 +27,7 @@ int read_status(const MapHandle* h) {
     if (st & kStatusRange) return SPCONV_ERR_COORD_RANGE;
     if (st & kStatusDuplicate) return SPCONV_ERR_DUPLICATE_COORD;
     if (st & kStatusTimeout) return SPCONV_ERR_TIMEOUT;
+    if (st & kStatusInternal) return SPCONV_ERR_INTERNAL;
     return SPCONV_OK;
 }
 
@@ -49,6 +50,28 @@ bool use_tensor_path(int32_t c_in, int32_t c_out, int32_t dtype, const void* fea
 }
 
 }  // namespace
+
+cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t s) {
+    constexpr int kMaxDevices = 64;
+    static cudaMemPool_t pools[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaMallocAsync(p, bytes, s);
+    if (pools[dev] == nullptr) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = ~0ull;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        pools[dev] = pool;
+    }
+    return cudaMallocFromPoolAsync(p, bytes, pools[dev], s);
+}
 
 void count_launch(int n) { g_launches += n; }
 void reset_launch_count() { g_launches = 0; }
@@ -77,6 +100,8 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
         if (opt->bit_order != SPCONV_ORDER_CALIBRATED && opt->bit_order != SPCONV_ORDER_PLAIN)
             return SPCONV_ERR_INVALID_ARG;
         if (opt->dense_max_cells < 0) return SPCONV_ERR_INVALID_ARG;
+        if (opt->pipeline < SPCONV_PIPELINE_AUTO || opt->pipeline > SPCONV_PIPELINE_MULTI) return SPCONV_ERR_INVALID_ARG;
+        if (opt->reserved != 0) return SPCONV_ERR_INVALID_ARG;
     }
     int32_t shape[3] = {1, 1, 1};
     int32_t batch = batch_size;
@@ -123,7 +148,7 @@ int spconv_subm_forward(spconv_map_t map, const void* feats_dev, const void* wei
             if (map->wspace) cudaFreeAsync(map->wspace, s);
             map->wspace = nullptr;
             map->wspace_bytes = 0;
-            if (cudaMallocAsync(&map->wspace, need, s) != cudaSuccess) {
+            if (pool_alloc(&map->wspace, need, s) != cudaSuccess) {
                 cudaGetLastError();
                 map->wspace = nullptr;
                 return SPCONV_ERR_OOM;
@@ -153,7 +178,7 @@ int spconv_wpack_create(const void* weights_dev, int32_t c_in, int32_t c_out, in
     w->tensor_path = (dtype == SPCONV_BF16 && tc_supported(c_in, c_out)) ? 1 : 0;
     const size_t es = dtype == SPCONV_FP32 ? 4 : 2;
     w->bytes = w->tensor_path ? tc_pack_bytes(c_in, c_out) : static_cast<size_t>(kTaps) * c_in * c_out * es;
-    if (cudaMallocAsync(&w->data, w->bytes, s) != cudaSuccess) {
+    if (pool_alloc(&w->data, w->bytes, s) != cudaSuccess) {
         cudaGetLastError();
         delete w;
         return SPCONV_ERR_OOM;
@@ -209,6 +234,7 @@ int spconv_map_info(spconv_map_t map, spconv_map_info_t* info) {
     info->n_tiles = map->n_tiles;
     info->tile_taps = totals[1];
     info->mapper = map->mapper;
+    info->pipeline = map->pipeline;
     info->key_bits = map->key_bits;
     std::memcpy(info->shape, map->shape, sizeof(info->shape));
     info->batch_size = map->batch;
@@ -264,6 +290,7 @@ const char* spconv_status_string(int status) {
         case SPCONV_ERR_COORD_RANGE: return "coordinate out of range";
         case SPCONV_ERR_ALIAS: return "output overlaps input";
         case SPCONV_ERR_TIMEOUT: return "kernel wait timed out";
+        case SPCONV_ERR_INTERNAL: return "internal consistency check failed";
         default: return "unknown status";
     }
 }

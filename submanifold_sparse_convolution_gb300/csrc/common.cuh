@@ -16,6 +16,7 @@ enum : int32_t {
     kStatusDuplicate = 1,
     kStatusRange = 2,
     kStatusTimeout = 4,
+    kStatusInternal = 8,   // an internal consistency guard fired (a would-be out-of-range store was skipped)
 };
 
 // Counts launches of the current host thread (reported by
@@ -38,6 +39,7 @@ struct MapHandle {
     int32_t shape[3] = {0, 0, 0};
     int32_t batch = 0;
     int32_t mapper = 0;       // spconv_mapper_t used
+    int32_t pipeline = 0;     // spconv_pipeline_t used
     int32_t bit_order = 0;
     int32_t key_bits = 0;
     // device arrays
@@ -90,6 +92,11 @@ int simt_forward(const MapHandle* h, const void* feats, const void* w, void* out
                  int32_t c_out, int32_t dtype, cudaStream_t s);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPCONV_OK : SPCONV_ERR_CUDA; }
+
+// Stream-ordered allocation from the library's memory pool on the current
+// device.  The pool keeps freed memory for reuse (no release threshold), so
+// a map rebuilt every frame does not map and unmap device memory each time.
+cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t s);
 
 }  // namespace spconv
 

@@ -14,8 +14,10 @@
 //   warps 0-3   epilogue: tcgen05.ld of the accumulator, bf16 convert, store
 //   warp 4      TMEM allocation + MMA issue (one thread)
 //   warps 5..   one producer warp per pipeline stage: cp.async 16-byte row
-//               gathers of A into the 128-byte-swizzled layout, plus one bulk
-//               async copy of the pre-packed weight tile B
+//               gathers of A into the 128-byte-swizzled layout (a row
+//               without the neighbour is written as zeros, with no memory
+//               request), plus one bulk async copy of the pre-packed weight
+//               tile B
 // The accumulator is double-buffered in TMEM so the epilogue of one tile
 // overlaps the main loop of the next.
 #include <cuda_bf16.h>
@@ -158,10 +160,11 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                     for (int i = 0; i < 32; ++i) {
                         const int row = 4 * i + (lane >> 3);
                         const int32_t src_row = __shfl_sync(0xFFFFFFFFu, gr[i >> 3], row & 31);
-                        const bool ok = src_row >= 0 && kcol < p.c_in;
-                        const __nv_bfloat16* src = ok ? p.feats + static_cast<int64_t>(src_row) * p.c_in + kcol : p.feats;
                         const uint32_t dst = a_smem + row * 128 + ((chunk ^ (row & 7)) << 4);
-                        ptx::cp_async_16(dst, src, ok ? 16u : 0u);
+                        if (src_row >= 0 && kcol < p.c_in)
+                            ptx::cp_async_16(dst, p.feats + static_cast<int64_t>(src_row) * p.c_in + kcol, 16u);
+                        else
+                            ptx::st_shared_zero16(dst);   // absent neighbour: no memory request
                     }
                     ptx::cp_async_commit();
                     ptx::cp_async_wait_all();

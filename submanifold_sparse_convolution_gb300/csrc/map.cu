@@ -21,6 +21,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "map_internal.cuh"
 #include "radix_sort.cuh"
 
 namespace spconv {
@@ -502,11 +503,25 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
     h->mapper = mapper;
     h->bit_order = opt ? opt->bit_order : SPCONV_ORDER_CALIBRATED;
 
+    // ---- pipeline: one cluster launch when the rows fit, else one kernel per step
+    const int row_bits = std::max(1, bit_length(static_cast<uint64_t>(n > 0 ? n - 1 : 0)));
+    const int want = opt ? opt->pipeline : SPCONV_PIPELINE_AUTO;
+    bool fused_ok = n <= kFusedMaxRows && (mapper != SPCONV_MAPPER_SORTED || key_bits + row_bits <= 64);
+    int cluster = 0;
+    if (fused_ok && want != SPCONV_PIPELINE_MULTI && n > 0) {
+        cluster = fused_cluster_size(s);
+        fused_ok = cluster > 0;
+    }
+    if (want == SPCONV_PIPELINE_FUSED && !fused_ok) return SPCONV_ERR_UNSUPPORTED;
+    const bool fused = want != SPCONV_PIPELINE_MULTI && fused_ok;
+    h->pipeline = fused ? SPCONV_PIPELINE_FUSED : SPCONV_PIPELINE_MULTI;
+
     // ---- one arena for everything the map keeps or needs while building
     const int64_t nb = std::max<int64_t>(1, rsort::num_tiles(n));
     const int64_t np = std::max<int64_t>(1, h->n_pad);
     const int64_t n1 = std::max<int64_t>(1, n);
     const int64_t t1 = std::max<int64_t>(1, T);
+    const int64_t cl = std::max(1, cluster);
     size_t bytes = 0;
     auto add = [&](size_t count, size_t elem) { bytes += (count * elem + 255) / 256 * 256; };
     add(4, 4);                          // status (+ pad)
@@ -517,15 +532,19 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
     add(kTaps * np, 4);                 // gtab
     add(t1, 4); add(t1, 4); add(kTaps * t1, 4); add(kTaps * t1, 4);  // union, order, counts, seg_off
     add(np, 4); add(np, 4);             // perm ping-pong
-    add(n1, 4); add(n1, 4);             // mask-sort keys ping-pong
-    add(rsort::kBins * nb, 4);          // radix histograms
-    if (mapper == SPCONV_MAPPER_SORTED) {
-        add(n1, 8); add(n1, 8); add(n1, 4); add(n1, 4);  // coordinate keys, row ids (ping-pong)
+    if (fused) {
+        add(n1, 8); add(n1, 8);         // packed (key, row) ping-pong
+        add(3 * cl * rsort::kBins, 4); add(cl * kTaps, 4); add(cl * (kTaps + 1), 4);
     } else {
-        add(static_cast<size_t>(cells), 4);              // presence grid
+        add(n1, 4); add(n1, 4);         // mask-sort keys ping-pong
+        add(rsort::kBins * nb, 4);      // radix histograms
+        if (mapper == SPCONV_MAPPER_SORTED) {
+            add(n1, 8); add(n1, 8); add(n1, 4); add(n1, 4);  // coordinate keys, row ids (ping-pong)
+        }
     }
+    if (mapper == SPCONV_MAPPER_DENSE) add(static_cast<size_t>(cells), 4);   // presence grid
     void* arena = nullptr;
-    if (cudaMallocAsync(&arena, bytes, s) != cudaSuccess) {
+    if (pool_alloc(&arena, bytes, s) != cudaSuccess) {
         cudaGetLastError();
         return SPCONV_ERR_OOM;
     }
@@ -548,6 +567,59 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
     h->seg_off = carve<int32_t>(p, kTaps * t1);
     int32_t* perm_a = carve<int32_t>(p, np);
     int32_t* perm_b = carve<int32_t>(p, np);
+
+    if (fused) {
+        FusedArgs fa;
+        fa.va = carve<uint64_t>(p, n1);
+        fa.vb = carve<uint64_t>(p, n1);
+        fa.hist = carve<int32_t>(p, 3 * cl * rsort::kBins);
+        fa.cta_tot = carve<int32_t>(p, cl * kTaps);
+        fa.cta_bkt = carve<int32_t>(p, cl * (kTaps + 1));
+        fa.grid = mapper == SPCONV_MAPPER_DENSE ? carve<int32_t>(p, static_cast<size_t>(cells)) : nullptr;
+        h->perm = perm_a;
+        if (n == 0) {
+            SPCONV_CHECK_CUDA(cudaMemsetAsync(h->status, 0, 256, s));
+            SPCONV_CHECK_CUDA(cudaMemsetAsync(h->tap_off, 0, 256, s));
+            SPCONV_CHECK_CUDA(cudaMemsetAsync(h->totals, 0, 256, s));
+            return cuda_status(cudaGetLastError());
+        }
+        fa.coords = reinterpret_cast<const int4*>(coords);
+        fa.n = n;
+        fa.shape = make_int3(X, Y, Z);
+        fa.batch = B;
+        fa.mapper = mapper;
+        fa.calibrated = h->bit_order == SPCONV_ORDER_CALIBRATED;
+        fa.wz = lay.wz;
+        fa.wy = lay.wy;
+        fa.wx = lay.wx;
+        fa.key_bits = key_bits;
+        fa.row_bits = row_bits;
+        for (int k = 0; k < kTaps; ++k) fa.koff[k] = lay.off[k];
+        fa.gsy = Z + 2;
+        fa.gsx = static_cast<int64_t>(Y + 2) * (Z + 2);
+        fa.gsb = static_cast<int64_t>(X + 2) * fa.gsx;
+        fa.cells = cells;
+        for (int dx = -1; dx <= 1; ++dx)
+            for (int dy = -1; dy <= 1; ++dy)
+                for (int dz = -1; dz <= 1; ++dz)
+                    fa.goff[9 * (dx + 1) + 3 * (dy + 1) + (dz + 1)] = dx * fa.gsx + dy * fa.gsy + dz;
+        fa.nbr = h->nbr;
+        fa.mask = h->mask;
+        fa.tap_count = h->tap_count;
+        fa.perm = h->perm;
+        fa.tap_off = h->tap_off;
+        fa.totals = h->totals;
+        fa.in_rows = h->in_rows;
+        fa.out_rows = h->out_rows;
+        fa.gtab = h->gtab;
+        fa.tile_union = h->tile_union;
+        fa.tile_order = h->tile_order;
+        fa.status = h->status;
+        fa.n_tiles = T;
+        fa.n_pad = h->n_pad;
+        return launch_map_fused(fa, cluster, s);
+    }
+
     uint32_t* mkey_a = carve<uint32_t>(p, n1);
     uint32_t* mkey_b = carve<uint32_t>(p, n1);
     int32_t* hist = carve<int32_t>(p, rsort::kBins * nb);

@@ -95,6 +95,10 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src, 
                  : "memory");
 }
 
+__device__ __forceinline__ void st_shared_zero16(uint32_t dst_smem) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst_smem), "r"(0u) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -119,6 +123,23 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst_smem, const void* src
             dst_smem),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Four-row gather through a 2D tensor map (box: one row x 64 bf16, 128-byte
+// swizzle): rows r0..r3 at column col land in 4 consecutive 128-byte rows at
+// dst_smem.  A row index outside the tensor is filled with zeros.  Completion
+// is counted in bytes (4 x 128) on *bar.
+__device__ __forceinline__ void tma_gather4(uint32_t dst_smem, const void* tmap, int32_t col, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst_smem),
+        "l"(tmap), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -43,7 +43,8 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     for code, text in [(0, "ok"), (-1, "invalid argument"), (-5, "duplicate coordinate"),
                        (-6, "coordinate out of range"), (-7, "output overlaps input"),
-                       (-8, "kernel wait timed out"), (-99, "unknown status")]:
+                       (-8, "kernel wait timed out"), (-9, "internal consistency check failed"),
+                       (-99, "unknown status")]:
         assert lib.spconv_status_string(code).decode() == text
 
 
@@ -62,10 +63,9 @@ def test_host_side_argument_errors(lib):
     # kernel size other than 3
     assert lib.spconv_build_map(None, 0, sp, 1, 5, None, None, ctypes.byref(h)) == -2
     # bad options
-    opt = _native.Options(7, 0, 0)
-    assert lib.spconv_build_map(None, 0, sp, 1, 3, ctypes.byref(opt), None, ctypes.byref(h)) == -1
-    opt = _native.Options(0, 3, 0)
-    assert lib.spconv_build_map(None, 0, sp, 1, 3, ctypes.byref(opt), None, ctypes.byref(h)) == -1
+    for bad in [(7, 0, 0, 0, 0), (0, 3, 0, 0, 0), (0, 0, -1, 0, 0), (0, 0, 0, 3, 0), (0, 0, 0, 0, 1)]:
+        opt = _native.Options(*bad)
+        assert lib.spconv_build_map(None, 0, sp, 1, 3, ctypes.byref(opt), None, ctypes.byref(h)) == -1
     # null handles everywhere else
     assert lib.spconv_subm_forward(None, None, None, None, 16, 16, 0, None) == -1
     assert lib.spconv_subm_forward_packed(None, None, None, None, None) == -1

@@ -58,9 +58,10 @@ def check_fp32(out, ref):
     assert err.size == 0 or err.max() <= FP32_ATOL, f"max abs err {err.max():.3e}"
 
 
-def build(wl, mapper="auto", bit_order="calibrated"):
+def build(wl, mapper="auto", bit_order="calibrated", pipeline="auto"):
     coords = wl.coords.cuda()
-    m = sc.build_map(coords, wl.spatial_shape, wl.batch_size, mapper=mapper, bit_order=bit_order)
+    m = sc.build_map(coords, wl.spatial_shape, wl.batch_size, mapper=mapper, bit_order=bit_order,
+                     pipeline=pipeline)
     assert sc.map_status(m) == 0
     return m
 
@@ -77,25 +78,38 @@ SMALL = [(1, 1, (4, 4, 4), 1), (2, 7, (5, 5, 5), 1), (3, 127, (8, 8, 8), 1), (4,
 @pytest.mark.parametrize("seed,n,shape,batch", SMALL)
 @pytest.mark.parametrize("mapper", ["dense", "sorted"])
 @pytest.mark.parametrize("bit_order", ["calibrated", "plain"])
-def test_map_small(seed, n, shape, batch, mapper, bit_order):
+@pytest.mark.parametrize("pipeline", ["fused", "multi"])
+def test_map_small(seed, n, shape, batch, mapper, bit_order, pipeline):
     wl = S.random_cloud(seed, n, shape=shape, batch_size=batch)
-    m = build(wl, mapper, bit_order)
+    m = build(wl, mapper, bit_order, pipeline)
     ref = oracle_map(wl.coords.numpy(), shape, batch, bit_order == "calibrated")
     assert_map_equal(sc.map_export(m), ref)
     info = sc.map_info(m)
     assert info["mapper"] == mapper and info["pairs"] == int(ref["tap_off"][27])
+    assert info["pipeline"] == pipeline
 
 
 @pytest.mark.parametrize("name", ["tiny", "outdoor", "deep", "large", "stage"])
-def test_map_workloads(name):
+@pytest.mark.parametrize("pipeline", ["auto", "multi"])
+def test_map_workloads(name, pipeline):
     coords, shape, batch, _ = S.make_coords(name)
     wl = S.Workload(name, torch.from_numpy(coords), shape, batch, 1, 1, None, [], 0)
-    m = build(wl)
+    m = build(wl, pipeline=pipeline)
     ref = oracle_map(coords, shape, batch)
     ex = sc.map_export(m)
     assert_map_equal(ex, ref)
     info = ex["info"]
     assert info["mapper"] == ("dense" if name in ("tiny", "deep") else "sorted")
+    assert info["pipeline"] == ("fused" if pipeline == "auto" else "multi")
+
+
+def test_map_many_rows_fused_and_multi_agree():
+    """Several ranking rounds per CTA and several tiles per CTA (N = 300k, 3 frames)."""
+    wl = S.random_cloud(61, 300000, shape=(200, 200, 60), batch_size=3)
+    a = sc.map_export(build(wl, "sorted", pipeline="fused"))
+    b = sc.map_export(build(wl, "sorted", pipeline="multi"))
+    for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
+        assert torch.equal(a[key], b[key]), key
 
 
 @pytest.mark.parametrize("name", ["tiny", "deep"])
@@ -131,14 +145,15 @@ def test_empty_input():
     assert out.shape == (0, 16)
 
 
-def test_duplicate_and_range_errors():
+@pytest.mark.parametrize("pipeline", ["fused", "multi"])
+def test_duplicate_and_range_errors(pipeline):
     dup = torch.tensor([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=torch.int32, device="cuda")
     for mapper in ("dense", "sorted"):
-        m = sc.build_map(dup, (4, 4, 4), 1, mapper=mapper)
+        m = sc.build_map(dup, (4, 4, 4), 1, mapper=mapper, pipeline=pipeline)
         assert sc.map_status(m) == -5
     bad = torch.tensor([[0, 1, 1, 1], [0, 4, 0, 0]], dtype=torch.int32, device="cuda")
     for mapper in ("dense", "sorted"):
-        m = sc.build_map(bad, (4, 4, 4), 1, mapper=mapper)
+        m = sc.build_map(bad, (4, 4, 4), 1, mapper=mapper, pipeline=pipeline)
         assert sc.map_status(m) == -6
     neg = torch.tensor([[0, 1, 1, 1], [0, -1, 0, 0]], dtype=torch.int32, device="cuda")
     with pytest.raises(sc.SpconvError):
@@ -263,6 +278,8 @@ def test_stage_six_layers_and_fp32_layer():
 def test_launch_count_reported():
     wl = S.random_cloud(51, 3000, shape=(16, 16, 16), c_in=64, c_out=64)
     m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1)
+    assert sc.last_launch_count() == 1                # the whole map in one cluster launch
+    sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, pipeline="multi")
     assert sc.last_launch_count() > 5
     sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
     assert sc.last_launch_count() == 2          # weight pack + GEMM
