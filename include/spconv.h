@@ -173,6 +173,35 @@ int spconv_map_export(spconv_map_t map, int32_t* nbr_dev, uint32_t* mask_dev, in
 /* Free the handle (stream-ordered on the stream of the build). */
 void spconv_map_destroy(spconv_map_t map);
 
+/*
+ * The kernel map nbr[n][27] of a coordinate set without allocating any device
+ * memory.  The pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate at the point where they run this code (a
+ * plugin's enqueue step in an inference runtime that plans all device memory
+ * up front, runtimes that forbid allocation after start-up, code running while
+ * its stream is captured into a graph).
+ *
+ *   coords_dev     int32 [n][4] rows (b, x, y, z), device, 16-byte aligned.
+ *   n              0 <= n <= 65536; larger n returns SPCONV_ERR_INVALID_ARG
+ *                  (the working buffers live in a fixed 1.6 MB device array).
+ *   spatial_shape  host int32[3] {X, Y, Z} (required).
+ *   batch_size     >= 1 (required).
+ *   nbr_dev        int32 [n][27] output, caller-owned: the same values as the
+ *                  nbr that spconv_map_export returns for this input.
+ *   stream         CUDA stream; the call synchronises it before returning and
+ *                  returns SPCONV_ERR_DUPLICATE_COORD / SPCONV_ERR_COORD_RANGE
+ *                  for bad coordinates.
+ *
+ * No cudaMalloc, cudaFree or allocating library routine is called.  The
+ * working buffers are one file-scope device array that every GPU loading this
+ * library holds until the process exits; the first call on a device looks up
+ * its address (make that first call before any stream capture).  All calls
+ * share the array, so calls whose work overlaps on the GPU (different streams
+ * or threads) race; serialise them.
+ */
+int spconv_kernel_map_static(const int32_t* coords_dev, int64_t n, const int32_t* spatial_shape,
+                             int32_t batch_size, int32_t* nbr_dev, void* stream);
+
 /* Number of kernel launches enqueued by the last call on this thread. */
 int32_t spconv_last_launch_count(void);
 

@@ -46,6 +46,8 @@ SIGNATURES = {
     "spconv_map_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(MapInfo)]),
     "spconv_map_export": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_void_p] * 6 + [ctypes.c_void_p]),
     "spconv_map_destroy": (None, [ctypes.c_void_p]),
+    "spconv_kernel_map_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, c_int32_p, ctypes.c_int32,
+                                                ctypes.c_void_p, ctypes.c_void_p]),
     "spconv_last_launch_count": (ctypes.c_int32, []),
     "spconv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }

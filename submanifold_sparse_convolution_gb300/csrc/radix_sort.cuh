@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kThreads) upsweep(const K* __restrict__ keys, 
 }
 
 // Exclusive scan, in place, of m int32 values (one block).
-__global__ void __launch_bounds__(kScanThreads) scan_exclusive(int32_t* __restrict__ a, int64_t m) {
+static __global__ void __launch_bounds__(kScanThreads) scan_exclusive(int32_t* __restrict__ a, int64_t m) {
     __shared__ int32_t part[kScanThreads];
     const int64_t chunk = (m + kScanThreads - 1) / kScanThreads;
     const int64_t lo = threadIdx.x * chunk;
