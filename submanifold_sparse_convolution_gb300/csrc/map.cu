@@ -534,7 +534,7 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
     add(np, 4); add(np, 4);             // perm ping-pong
     if (fused) {
         add(n1, 8); add(n1, 8);         // packed (key, row) ping-pong
-        add(3 * cl * rsort::kBins, 4); add(cl * kTaps, 4); add(cl * (kTaps + 1), 4);
+        add(3 * cl * kFusedBins, 4); add(cl * kTaps, 4); add(cl * (kTaps + 1), 4);
     } else {
         add(n1, 4); add(n1, 4);         // mask-sort keys ping-pong
         add(rsort::kBins * nb, 4);      // radix histograms
@@ -572,7 +572,7 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
         FusedArgs fa;
         fa.va = carve<uint64_t>(p, n1);
         fa.vb = carve<uint64_t>(p, n1);
-        fa.hist = carve<int32_t>(p, 3 * cl * rsort::kBins);
+        fa.hist = carve<int32_t>(p, 3 * cl * kFusedBins);
         fa.cta_tot = carve<int32_t>(p, cl * kTaps);
         fa.cta_bkt = carve<int32_t>(p, cl * (kTaps + 1));
         fa.grid = mapper == SPCONV_MAPPER_DENSE ? carve<int32_t>(p, static_cast<size_t>(cells)) : nullptr;
@@ -614,6 +614,7 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
         fa.gtab = h->gtab;
         fa.tile_union = h->tile_union;
         fa.tile_order = h->tile_order;
+        fa.seg_off = h->seg_off;
         fa.status = h->status;
         fa.n_tiles = T;
         fa.n_pad = h->n_pad;

@@ -29,12 +29,20 @@ constexpr int FT = 1024;          // threads per CTA
 constexpr int FW = FT / 32;       // warps per CTA
 constexpr int IPT = 4;            // items per thread per ranking round
 constexpr int RS = FT * IPT;      // elements per ranking round
-constexpr int BINS = 256;
+constexpr int kDigitMax = 10;                 // widest radix digit (bits)
+constexpr int BINS = 1 << kDigitMax;          // histogram capacity per CTA and pass
+static_assert(BINS == kFusedBins, "host and kernel agree on the histogram width");
 constexpr int kMaxCluster = 16;
 constexpr int kTilesPerRound = FW / 4;   // 4 warps (128 rows) per tile
+// Launch parts: the coordinate sort, then (after the whole-GPU neighbour
+// search) masks, mask sort and compaction.  The dense-grid mapper runs
+// everything in the second part.
+constexpr int kPartSort = 0;
+constexpr int kPartRest = 1;
+static_assert(FT == BINS && FW == 32, "one thread per digit value, 32 warps per CTA");
 
 struct FusedSmem {
-    uint16_t cnt[IPT][FW][BINS];   // ranking: per (item slot, warp, digit) counts, then offsets
+    uint16_t cnt[FW][BINS];        // ranking: per (warp, digit) counts of a round, then offsets
     int32_t base[BINS];
     int32_t run[BINS];
     int32_t scan[BINS];
@@ -45,6 +53,9 @@ struct FusedSmem {
     int32_t tap_base[kTaps];
     int32_t bkt_base[kTaps + 1];
     int32_t qcnt[kTilesPerRound][4][kTaps];
+    int32_t ctot[kMaxCluster * kTaps];             // every CTA's tap totals
+    int32_t ctab[kMaxCluster * (kTaps + 1)];       // every CTA's bucket counts
+    int32_t taps[kTaps];                           // this CTA's tap counts (then the global ones)
     int32_t err;
 };
 
@@ -60,84 +71,100 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-// Exclusive scan of a[0..255] in place (all threads call; uses the first 8 warps).
-__device__ int32_t block_scan256(int32_t* a, int32_t* tmp) {
+// Exclusive scan of a[0..count) in place, count <= FT (all threads call).
+__device__ void block_scan(int32_t* a, int count, int32_t* tmp) {
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    int32_t v = 0, incl = 0;
-    if (t < BINS) {
-        v = a[t];
-        incl = v;
+    const int32_t v = t < count ? a[t] : 0;
+    int32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) tmp[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        const int32_t x = tmp[lane];
+        int32_t y = x;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += x;
+            const int32_t z = __shfl_up_sync(0xFFFFFFFFu, y, o);
+            if (lane >= o) y += z;
         }
-        if (lane == 31) tmp[w] = incl;
+        tmp[lane] = y - x;     // exclusive prefix of the warp totals
     }
     __syncthreads();
-    int32_t total = 0;
-    for (int i = 0; i < BINS / 32; ++i) total += tmp[i];
-    if (t < BINS) {
-        int32_t wpre = 0;
-        for (int i = 0; i < w; ++i) wpre += tmp[i];
-        a[t] = wpre + incl - v;
-    }
+    if (t < count) a[t] = tmp[w] + incl - v;
     __syncthreads();
-    return total;
 }
 
 // One stable LSD pass over this CTA's part [c*chunk, min(n, (c+1)*chunk)) of
-// `in`, by digit (v >> shift) & 255.  hc: every CTA's digit counts of its
-// part ([C][256]).  When hn != nullptr the counts of the next digit
-// (v >> next_shift) of every element are accumulated into hn by the CTA
-// whose part the element lands in.
+// `in`, by the digit of `width` bits at `shift`.  hc: every CTA's digit counts
+// of its part ([C][BINS]).  When hn != nullptr the counts of the next digit
+// (next_width bits at next_shift) of every element are accumulated into hn by
+// the CTA whose part the element lands in.
 __device__ void radix_pass(const uint64_t* __restrict__ in, uint64_t* __restrict__ out, int64_t n,
-                           int64_t chunk, int C, int c, int shift, const int32_t* hc, int32_t* hn,
-                           int next_shift, FusedSmem& sm) {
+                           int64_t chunk, int C, int c, int shift, int width, const int32_t* hc,
+                           int32_t* hn, int next_shift, int next_width, FusedSmem& sm) {
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    if (t < BINS) {
+    const int bins = 1 << width;
+    const uint64_t dmask = static_cast<uint64_t>(bins - 1);
+    const uint64_t nmask = (uint64_t(1) << next_width) - 1;
+    if (t < bins) {
+        int32_t h[kMaxCluster];
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q) h[q] = q < C ? __ldcg(hc + q * BINS + t) : 0;   // loads in flight together
         int32_t tot = 0, pre = 0;
-        for (int q = 0; q < C; ++q) {
-            const int32_t h = __ldcg(hc + q * BINS + t);
-            tot += h;
-            if (q < c) pre += h;
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q) {
+            tot += h[q];
+            pre += q < c ? h[q] : 0;
         }
         sm.scan[t] = tot;
         sm.pre[t] = pre;
         sm.run[t] = 0;
     }
     __syncthreads();
-    block_scan256(sm.scan, sm.tmp);
-    if (t < BINS) sm.base[t] = sm.scan[t] + sm.pre[t];
+    block_scan(sm.scan, bins, sm.tmp);
+    if (t < bins) sm.base[t] = sm.scan[t] + sm.pre[t];
     const int64_t lo = static_cast<int64_t>(c) * chunk;
     const int64_t hi = lo + chunk < n ? lo + chunk : n;
     const uint32_t lt = lanemask_lt();
+    // A round is RS consecutive elements; warp w owns the 32*IPT of them
+    // starting at w*32*IPT (item j of lane l at w*32*IPT + 32*j + l), so the
+    // stable order inside a round is (warp, item, lane).
     for (int64_t r0 = lo; r0 < hi; r0 += RS) {
-        uint32_t* cz = reinterpret_cast<uint32_t*>(&sm.cnt[0][0][0]);
-        for (int i = t; i < IPT * FW * BINS / 2; i += FT) cz[i] = 0;
+        uint32_t* cz = reinterpret_cast<uint32_t*>(&sm.cnt[0][0]);
+        for (int i = t; i < FW * BINS / 2; i += FT) cz[i] = 0;
         __syncthreads();
         uint64_t v[IPT];
         int d[IPT], rk[IPT];
 #pragma unroll
+        for (int j = 0; j < IPT; ++j) {   // all loads first, so they are in flight together
+            const int64_t idx = r0 + static_cast<int64_t>(w) * 32 * IPT + 32 * j + lane;
+            v[j] = idx < hi ? __ldcg(in + idx) : 0ull;
+            d[j] = idx < hi ? 0 : BINS;
+        }
+#pragma unroll
         for (int j = 0; j < IPT; ++j) {
-            const int64_t idx = r0 + j * FT + t;
-            const bool valid = idx < hi;
-            v[j] = valid ? __ldcg(in + idx) : 0ull;
-            d[j] = valid ? static_cast<int>((v[j] >> shift) & 0xFF) : BINS;
+            const bool valid = d[j] < BINS;
+            d[j] = valid ? static_cast<int>((v[j] >> shift) & dmask) : BINS;
             const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d[j]);
-            rk[j] = __popc(peers & lt);
-            if (valid && lane == __ffs(peers) - 1) sm.cnt[j][w][d[j]] = static_cast<uint16_t>(__popc(peers));
+            const int prior = valid ? sm.cnt[w][d[j]] : 0;
+            rk[j] = prior + __popc(peers & lt);
+            __syncwarp();
+            if (valid && lane == __ffs(peers) - 1) sm.cnt[w][d[j]] = static_cast<uint16_t>(prior + __popc(peers));
+            __syncwarp();
         }
         __syncthreads();
-        if (t < BINS) {
-            uint32_t running = 0;
-            for (int j = 0; j < IPT; ++j)
-                for (int q = 0; q < FW; ++q) {
-                    const uint32_t x = sm.cnt[j][q][t];
-                    sm.cnt[j][q][t] = static_cast<uint16_t>(running);
-                    running += x;
-                }
-            sm.rtot[t] = static_cast<int32_t>(running);
+        if (t < bins) {   // exclusive prefix over the warps, per digit
+            int32_t pre = 0;
+            for (int q = 0; q < FW; ++q) {
+                const int32_t x = sm.cnt[q][t];
+                sm.cnt[q][t] = static_cast<uint16_t>(pre);
+                pre += x;
+            }
+            sm.rtot[t] = pre;
         }
         __syncthreads();
 #pragma unroll
@@ -146,7 +173,7 @@ __device__ void radix_pass(const uint64_t* __restrict__ in, uint64_t* __restrict
             int64_t dst = 0;
             bool ok = false;
             if (valid) {
-                dst = static_cast<int64_t>(sm.base[d[j]]) + sm.run[d[j]] + sm.cnt[j][w][d[j]] + rk[j];
+                dst = static_cast<int64_t>(sm.base[d[j]]) + sm.run[d[j]] + sm.cnt[w][d[j]] + rk[j];
                 ok = dst >= 0 && dst < n;
                 if (ok)
                     out[dst] = v[j];
@@ -155,40 +182,43 @@ __device__ void radix_pass(const uint64_t* __restrict__ in, uint64_t* __restrict
             }
             if (hn != nullptr) {
                 const int dc = ok ? static_cast<int>(dst / chunk) : 0;
-                const int key2 = ok ? dc * BINS + static_cast<int>((v[j] >> next_shift) & 0xFF) : -1;
+                const int key2 = ok ? dc * BINS + static_cast<int>((v[j] >> next_shift) & nmask) : -1;
                 const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key2);
                 if (ok && lane == __ffs(peers) - 1) atomicAdd(hn + key2, __popc(peers));
             }
         }
         __syncthreads();
-        if (t < BINS) sm.run[t] += sm.rtot[t];
+        if (t < bins) sm.run[t] += sm.rtot[t];
     }
     __syncthreads();
 }
 
-// Local (this CTA only) digit histogram of in[lo, hi) written to h[c][*].
-__device__ void local_hist(const uint64_t* __restrict__ in, int64_t lo, int64_t hi, int shift,
+// Local (this CTA only) histogram of the `width`-bit digit at `shift` of
+// in[lo, hi), written to h[0..BINS).
+__device__ void local_hist(const uint64_t* __restrict__ in, int64_t lo, int64_t hi, int shift, int width,
                            int32_t* h, FusedSmem& sm) {
     const int t = threadIdx.x, lane = t & 31;
-    if (t < BINS) sm.scan[t] = 0;
+    const uint64_t dmask = (uint64_t(1) << width) - 1;
+    sm.scan[t] = 0;
     __syncthreads();
     for (int64_t i0 = lo; i0 < hi; i0 += FT) {
         const int64_t i = i0 + t;
-        const int dg = i < hi ? static_cast<int>((__ldcg(in + i) >> shift) & 0xFF) : BINS;
+        const int dg = i < hi ? static_cast<int>((__ldcg(in + i) >> shift) & dmask) : BINS;
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dg);
         if (dg < BINS && lane == __ffs(peers) - 1) atomicAdd(&sm.scan[dg], __popc(peers));
     }
     __syncthreads();
-    if (t < BINS) h[t] = sm.scan[t];
+    h[t] = sm.scan[t];
     __syncthreads();
 }
 
-__device__ __forceinline__ void add_tap_counts(uint32_t m, int32_t* tap_count) {
+// Adds this warp's tap counts to the CTA's shared counters.
+__device__ __forceinline__ void add_tap_counts(uint32_t m, int32_t* cta_taps) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int k = 0; k < kTaps; ++k) {
         const uint32_t b = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
-        if (lane == 0 && b) atomicAdd(tap_count + k, __popc(b));
+        if (lane == 0 && b) atomicAdd(cta_taps + k, __popc(b));
     }
 }
 
@@ -198,7 +228,7 @@ __device__ __forceinline__ void store_row(int32_t* __restrict__ nbr, int64_t r, 
     for (int q = 0; q < kNbrStride / 4; ++q) dst[q] = make_int4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-__global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a) {
+__global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a, int part) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     FusedSmem& sm = *reinterpret_cast<FusedSmem*>(smem_raw);
     const int C = static_cast<int>(gridDim.x);
@@ -211,21 +241,26 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a) {
     const int rb = a.row_bits;
     const uint64_t rmask = (uint64_t(1) << rb) - 1;
     int32_t* H[3] = {a.hist, a.hist + C * BINS, a.hist + 2 * C * BINS};
+    // digit widths: the fewest passes of at most kDigitMax bits
+    const int key_passes = (a.key_bits + kDigitMax - 1) / kDigitMax;
+    const int key_w = (a.key_bits + key_passes - 1) / key_passes;
+    constexpr int kMaskPasses = (kTaps + kDigitMax - 1) / kDigitMax;
+    constexpr int kMaskW = (kTaps + kMaskPasses - 1) / kMaskPasses;
     if (t == 0) sm.err = 0;
+    if (t < kTaps) sm.taps[t] = 0;
 
     // ---------------- phase 0: reset counters, pack keys / clear the grid
-    if (c == 0 && t < kTaps) a.tap_count[t] = 0;
-    if (c == 0 && t == 0) {
+    const bool starts = part == kPartSort || a.mapper == SPCONV_MAPPER_DENSE;
+    if (starts && c == 0 && t < kTaps) a.tap_count[t] = 0;
+    if (starts && c == 0 && t == 0) {
         *a.status = 0;
         a.totals[0] = 0;
         a.totals[1] = 0;
     }
-    if (t < BINS) {
-        H[1][c * BINS + t] = 0;
-        H[2][c * BINS + t] = 0;
-    }
+    H[1][c * BINS + t] = 0;
+    H[2][c * BINS + t] = 0;
     __syncthreads();
-    if (a.mapper == SPCONV_MAPPER_SORTED) {
+    if (part == kPartSort) {
         const uint64_t invalid = ((uint64_t(1) << a.key_bits) - 1) << rb;
         for (int64_t i = lo + t; i < hi; i += FT) {
             const int4 q = a.coords[i];
@@ -243,8 +278,8 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a) {
             a.va[i] = key | static_cast<uint64_t>(i);
         }
         __syncthreads();
-        local_hist(a.va, lo, hi, rb, H[0] + c * BINS, sm);
-    } else {
+        local_hist(a.va, lo, hi, rb, key_w, H[0] + c * BINS, sm);
+    } else if (a.mapper == SPCONV_MAPPER_DENSE) {
         const int64_t per = (a.cells + C - 1) / C;
         const int64_t g0 = static_cast<int64_t>(c) * per;
         const int64_t g1 = g0 + per < a.cells ? g0 + per : a.cells;
@@ -252,87 +287,19 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a) {
     }
     cluster_sync_all();
 
-    if (a.mapper == SPCONV_MAPPER_SORTED) {
-        // ---------------- coordinate sort: one barrier per 8-bit pass
-        const int passes = (a.key_bits + 7) / 8;
-        for (int p = 0; p < passes; ++p) {
+    if (part == kPartSort) {
+        // ---------------- coordinate sort: one barrier per pass
+        for (int p = 0; p < key_passes; ++p) {
             const uint64_t* in = (p & 1) ? a.vb : a.va;
             uint64_t* out = (p & 1) ? a.va : a.vb;
-            if (t < BINS) H[(p + 2) % 3][c * BINS + t] = 0;
-            radix_pass(in, out, n, chunk, C, c, rb + 8 * p, H[p % 3], p + 1 < passes ? H[(p + 1) % 3] : nullptr,
-                       rb + 8 * (p + 1), sm);
+            H[(p + 2) % 3][c * BINS + t] = 0;
+            radix_pass(in, out, n, chunk, C, c, rb + key_w * p, key_w, H[p % 3],
+                       p + 1 < key_passes ? H[(p + 1) % 3] : nullptr, rb + key_w * (p + 1), key_w, sm);
             cluster_sync_all();
         }
-        const uint64_t* sv = (passes & 1) ? a.vb : a.va;
-        const uint64_t invalid_key = (uint64_t(1) << a.key_bits) - 1;
-        // ---------------- neighbour search: one lower_bound per (dx, dy) column
-        // Each thread takes a contiguous run of sorted positions.  The first
-        // is searched in lockstep over the whole array; later ones gallop
-        // forward from the previous bounds, since every column's target grows
-        // with the key.  The sorted array is read through L1: no thread has
-        // read it through L1 before, so no stale line can be there.
-        const int64_t per = (hi - lo + FT - 1) / FT;
-        const int64_t sa = lo + static_cast<int64_t>(t) * per;
-        const int64_t sb = sa + per < hi ? sa + per : hi;
-        int64_t pos[9];
-        bool have = false;
-        for (int64_t e = 0; e < per; ++e) {
-            const int64_t s = sa + e;
-            uint32_t m = 0;
-            if (s < sb) {
-                const uint64_t vs = __ldg(sv + s);
-                const uint64_t q = vs >> rb;
-                int64_t r = static_cast<int64_t>(vs & rmask);
-                if (r >= n) {
-                    atomicOr(&sm.err, kStatusInternal);
-                    r = -1;
-                }
-                int32_t v[kNbrStride];
-#pragma unroll
-                for (int k = 0; k < kNbrStride; ++k) v[k] = -1;
-                if (q != invalid_key) {
-                    if (s > 0 && (__ldg(sv + s - 1) >> rb) == q) atomicOr(&sm.err, kStatusDuplicate);
-                    uint64_t tl[9];
-#pragma unroll
-                    for (int cc = 0; cc < 9; ++cc) tl[cc] = (q + a.koff[3 * cc]) << rb;
-                    if (!have) {
-                        lower_bound9(sv, n, tl, pos);
-                        have = true;
-                    } else {
-#pragma unroll
-                        for (int cc = 0; cc < 9; ++cc) pos[cc] = lower_bound_from(sv, n, pos[cc], tl[cc]);
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < 9; ++cc) {
-                        const uint64_t hi_k = q + a.koff[3 * cc + 2];
-#pragma unroll
-                        for (int j = 0; j < 3; ++j) {
-                            const int64_t pp = pos[cc] + j;
-                            if (pp < n) {
-                                const uint64_t vv = __ldg(sv + pp);
-                                const uint64_t kk = vv >> rb;
-                                if (kk <= hi_k) {
-                                    const uint64_t dz = kk - (tl[cc] >> rb);
-                                    const int32_t row = static_cast<int32_t>(vv & rmask) < n
-                                                            ? static_cast<int32_t>(vv & rmask) : -1;
-                                    if (dz == 0) v[3 * cc] = row;
-                                    if (dz == 1) v[3 * cc + 1] = row;
-                                    if (dz == 2) v[3 * cc + 2] = row;
-                                }
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int k = 0; k < kTaps; ++k) m |= (v[k] >= 0 ? 1u : 0u) << k;
-                }
-                if (r >= 0) {
-                    store_row(a.nbr, r, v);
-                    a.mask[r] = m;
-                }
-            }
-            add_tap_counts(m, a.tap_count);
-        }
-    } else {
+        if (t == 0 && sm.err) atomicOr(a.status, sm.err);
+        return;   // the neighbour search runs next on the whole GPU (k_search_sorted)
+    } else if (a.mapper == SPCONV_MAPPER_DENSE) {
         // ---------------- dense grid: scatter row ids, then 27 lookups per row
         for (int64_t i = lo + t; i < hi; i += FT) {
             const int4 q = a.coords[i];
@@ -367,48 +334,59 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a) {
                 store_row(a.nbr, i, v);
                 a.mask[i] = m;
             }
-            add_tap_counts(m, a.tap_count);
+            add_tap_counts(m, sm.taps);
         }
     }
-    cluster_sync_all();
+    __syncthreads();
+    if (t < kTaps && sm.taps[t]) atomicAdd(a.tap_count + t, sm.taps[t]);
+    if (a.mapper == SPCONV_MAPPER_DENSE) cluster_sync_all();
 
     // ---------------- mask sort keys (tap order from the counts) + first histogram
+    if (t < kTaps) sm.taps[t] = __ldcg(a.tap_count + t);
+    __syncthreads();
     if (t < kTaps) {
         int32_t rank = t;
         if (a.calibrated) {
-            const int32_t ck = __ldcg(a.tap_count + t);
+            const int32_t ck = sm.taps[t];
             rank = 0;
             for (int j = 0; j < kTaps; ++j) {
-                const int32_t cj = __ldcg(a.tap_count + j);
+                const int32_t cj = sm.taps[j];
                 rank += (cj > ck || (cj == ck && j < t)) ? 1 : 0;
             }
         }
         sm.tap_pos[t] = rank;
     }
-    if (t < BINS) {
-        H[1][c * BINS + t] = 0;
-        H[2][c * BINS + t] = 0;
-    }
+    H[1][c * BINS + t] = 0;
+    H[2][c * BINS + t] = 0;
     __syncthreads();
-    for (int64_t i = lo + t; i < hi; i += FT) {
-        const uint32_t m = __ldcg(a.mask + i);
-        uint32_t key = 0;
+    sm.scan[t] = 0;
+    __syncthreads();
+    for (int64_t i0 = lo; i0 < hi; i0 += FT) {   // keys and their first-digit histogram in one pass
+        const int64_t i = i0 + t;
+        int dg = BINS;
+        if (i < hi) {
+            const uint32_t m = __ldcg(a.mask + i);
+            uint32_t key = 0;
 #pragma unroll
-        for (int k = 0; k < kTaps; ++k) key |= ((m >> k) & 1u) << sm.tap_pos[k];
-        a.va[i] = (static_cast<uint64_t>(key) << rb) | static_cast<uint64_t>(i);
+            for (int k = 0; k < kTaps; ++k) key |= ((m >> k) & 1u) << sm.tap_pos[k];
+            a.va[i] = (static_cast<uint64_t>(key) << rb) | static_cast<uint64_t>(i);
+            dg = static_cast<int>(key & ((1u << kMaskW) - 1));
+        }
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dg);
+        if (dg < BINS && lane == __ffs(peers) - 1) atomicAdd(&sm.scan[dg], __popc(peers));
     }
     __syncthreads();
-    local_hist(a.va, lo, hi, rb, H[0] + c * BINS, sm);
+    H[0][c * BINS + t] = sm.scan[t];
     cluster_sync_all();
-    for (int p = 0; p < 4; ++p) {
+    for (int p = 0; p < kMaskPasses; ++p) {
         const uint64_t* in = (p & 1) ? a.vb : a.va;
         uint64_t* out = (p & 1) ? a.va : a.vb;
-        if (t < BINS) H[(p + 2) % 3][c * BINS + t] = 0;
-        radix_pass(in, out, n, chunk, C, c, rb + 8 * p, H[p % 3], p + 1 < 4 ? H[(p + 1) % 3] : nullptr,
-                   rb + 8 * (p + 1), sm);
+        H[(p + 2) % 3][c * BINS + t] = 0;
+        radix_pass(in, out, n, chunk, C, c, rb + kMaskW * p, kMaskW, H[p % 3],
+                   p + 1 < kMaskPasses ? H[(p + 1) % 3] : nullptr, rb + kMaskW * (p + 1), kMaskW, sm);
         cluster_sync_all();
     }
-    const uint64_t* ms = a.va;   // 4 passes: the sorted (key, row) pairs are back in va
+    const uint64_t* ms = (kMaskPasses & 1) ? a.vb : a.va;   // where the last pass left the pairs
 
     // ---------------- compaction, count: per tile and tap, CTA totals, bucket counts
     const int64_t T = a.n_tiles;
@@ -418,6 +396,7 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a) {
     const int nt = static_cast<int>(tb > ta ? tb - ta : 0);
     int32_t* tcnt = reinterpret_cast<int32_t*>(smem_raw + sizeof(FusedSmem));   // [nt][27]
     int32_t* tbkt = tcnt + static_cast<int64_t>(nt) * kTaps;                    // [nt]
+    uint32_t* tuni = reinterpret_cast<uint32_t*>(tbkt + nt);                     // [nt]
     for (int i = t; i < nt * kTaps; i += FT) tcnt[i] = 0;
     if (t <= kTaps) sm.scan[t] = 0;   // bucket counts of this CTA's tiles
     __syncthreads();
@@ -442,8 +421,10 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a) {
     }
     __syncthreads();
     for (int i = t; i < nt; i += FT) {
-        int u = 0;
-        for (int k = 0; k < kTaps; ++k) u += tcnt[i * kTaps + k] > 0 ? 1 : 0;
+        uint32_t uni = 0;
+        for (int k = 0; k < kTaps; ++k) uni |= (tcnt[i * kTaps + k] > 0 ? 1u : 0u) << k;
+        const int u = __popc(uni);
+        tuni[i] = uni;
         tbkt[i] = kTaps - u;
         atomicAdd(&sm.scan[kTaps - u], 1);
     }
@@ -469,33 +450,60 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a) {
     cluster_sync_all();
 
     // ---------------- compaction, write
+    for (int i = t; i < C * kTaps; i += FT) sm.ctot[i] = __ldcg(a.cta_tot + i);
+    for (int i = t; i < C * (kTaps + 1); i += FT) sm.ctab[i] = __ldcg(a.cta_bkt + i);
+    __syncthreads();
+    // per tap: total over all CTAs and this CTA's offset among them; per
+    // bucket likewise (one thread each, C steps), then short scans
     if (t < kTaps) {
-        int32_t before = 0, mine = 0;
-        for (int k = 0; k < t; ++k)
-            for (int q = 0; q < C; ++q) before += __ldcg(a.cta_tot + q * kTaps + k);
-        for (int q = 0; q < c; ++q) mine += __ldcg(a.cta_tot + q * kTaps + t);
-        sm.tap_base[t] = before + mine;
-        if (c == 0) a.tap_off[t] = before;
-        if (c == 0 && t == kTaps - 1) {
-            int32_t all = before;
-            for (int q = 0; q < C; ++q) all += __ldcg(a.cta_tot + q * kTaps + t);
-            a.tap_off[kTaps] = all;
-            a.totals[0] = all;
+        int32_t all_k = 0, mine = 0;
+        for (int q = 0; q < C; ++q) {
+            const int32_t x = sm.ctot[q * kTaps + t];
+            all_k += x;
+            if (q < c) mine += x;
         }
+        sm.scan[t] = all_k;
+        sm.pre[t] = mine;
     }
     if (t >= 32 && t < 32 + kTaps + 1) {
         const int b = t - 32;
-        int32_t before = 0, mine = 0;
-        for (int bb = 0; bb < b; ++bb)
-            for (int q = 0; q < C; ++q) before += __ldcg(a.cta_bkt + q * (kTaps + 1) + bb);
-        for (int q = 0; q < c; ++q) mine += __ldcg(a.cta_bkt + q * (kTaps + 1) + b);
-        sm.bkt_base[b] = before + mine;
-        if (c == 0 && b == 0) {
-            int32_t taps = 0;
-            for (int bb = 0; bb <= kTaps; ++bb)
-                for (int q = 0; q < C; ++q) taps += (kTaps - bb) * __ldcg(a.cta_bkt + q * (kTaps + 1) + bb);
-            a.totals[1] = taps;
+        int32_t all_b = 0, mine = 0;
+        for (int q = 0; q < C; ++q) {
+            const int32_t x = sm.ctab[q * (kTaps + 1) + b];
+            all_b += x;
+            if (q < c) mine += x;
         }
+        sm.scan[64 + b] = all_b;
+        sm.pre[64 + b] = mine;
+    }
+    __syncthreads();
+    if (w == 0) {   // exclusive scans over the 27 taps and over the 28 buckets
+        const int32_t xt = lane < kTaps ? sm.scan[lane] : 0;
+        const int32_t xb = lane <= kTaps ? sm.scan[64 + lane] : 0;
+        int32_t it = xt, ib = xb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t yt = __shfl_up_sync(0xFFFFFFFFu, it, o);
+            const int32_t yb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+            if (lane >= o) {
+                it += yt;
+                ib += yb;
+            }
+        }
+        if (lane < kTaps) {
+            sm.tap_base[lane] = it - xt + sm.pre[lane];
+            if (c == 0) a.tap_off[lane] = it - xt;
+        }
+        if (lane == kTaps - 1 && c == 0) {
+            a.tap_off[kTaps] = it;
+            a.totals[0] = it;
+        }
+        if (lane <= kTaps) sm.bkt_base[lane] = ib - xb + sm.pre[64 + lane];
+        // sum of union sizes over all tiles: bucket b holds tiles with 27 - b taps
+        int32_t taps = lane <= kTaps ? (kTaps - lane) * xb : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) taps += __shfl_xor_sync(0xFFFFFFFFu, taps, o);
+        if (lane == 0 && c == 0) a.totals[1] = taps;
     }
     __syncthreads();
     // tiles by descending union size, stable in the tile index
@@ -508,73 +516,175 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a) {
         else
             atomicOr(&sm.err, kStatusInternal);
     }
-    const uint32_t lt = lanemask_lt();
-    for (int tr = 0; tr < nt; tr += kTilesPerRound) {
-        const int tl = tr + (w >> 2);
-        const int quarter = w & 3;
-        const int64_t s = (ta + tl) * kTileRows + quarter * 32 + lane;
-        const bool in_tile = tl < nt;
-        const bool valid = in_tile && s < n;
-        int32_t r = valid ? static_cast<int32_t>(__ldcg(ms + s) & rmask) : -1;
-        if (r >= n) r = -1;
-        const uint32_t m = r >= 0 ? __ldcg(a.mask + r) : 0u;
-        uint32_t ball[kTaps];
-#pragma unroll
-        for (int k = 0; k < kTaps; ++k) {
-            ball[k] = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
-            if (lane == 0) sm.qcnt[w >> 2][quarter][k] = __popc(ball[k]);
+    // offsets of every (tap, tile) pair run and the tile unions, for the
+    // whole-GPU write kernel that follows (k_tile_write_packed)
+    for (int i = t; i < nt * kTaps; i += FT) {
+        const int tl = i / kTaps, k = i % kTaps;
+        a.seg_off[static_cast<int64_t>(k) * T + ta + tl] = sm.tap_base[k] + tcnt[i];
+    }
+    for (int i = t; i < nt; i += FT) a.tile_union[ta + i] = tuni[i];
+    if (t == 0 && sm.err) atomicOr(a.status, sm.err);
+}
+
+// One thread per sorted position of the packed (key << rb | row) array: the
+// 27 neighbours of the voxel there, by one lower_bound per (dx, dy) column
+// (all 9 in lockstep) and a look at the next three keys for dz = -1, 0, +1.
+// Runs on the whole GPU between the two cluster launches.
+struct SearchArgs {
+    const uint64_t* sv;
+    int64_t n;
+    int rb, key_bits;
+    uint64_t koff[kTaps];
+    int32_t* nbr;
+    uint32_t* mask;
+    int32_t* tap_count;
+    int32_t* status;
+};
+
+__global__ void __launch_bounds__(256) k_search_sorted(const SearchArgs a) {
+    __shared__ int32_t cnt[kTaps];
+    __shared__ int32_t err;
+    if (threadIdx.x < kTaps) cnt[threadIdx.x] = 0;
+    if (threadIdx.x == 0) err = 0;
+    __syncthreads();
+    const int64_t s = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+    const int64_t n = a.n;
+    const int rb = a.rb;
+    const uint64_t rmask = (uint64_t(1) << rb) - 1;
+    const uint64_t invalid_key = (uint64_t(1) << a.key_bits) - 1;
+    uint32_t m = 0;
+    if (s < n) {
+        const uint64_t vs = __ldg(a.sv + s);
+        const uint64_t q = vs >> rb;
+        int64_t r = static_cast<int64_t>(vs & rmask);
+        if (r >= n) {
+            atomicOr(&err, kStatusInternal);
+            r = -1;
         }
-        __syncthreads();
-        if (in_tile) {
-            int32_t v[kNbrStride];
-            if (r >= 0) {
-                const int4* src = reinterpret_cast<const int4*>(a.nbr + static_cast<int64_t>(r) * kNbrStride);
+        int32_t* row = r >= 0 ? a.nbr + r * kNbrStride : nullptr;
+        if (q != invalid_key) {
+            if (s > 0 && (__ldg(a.sv + s - 1) >> rb) == q) atomicOr(&err, kStatusDuplicate);
+            uint64_t tl[9];
 #pragma unroll
-                for (int q = 0; q < kNbrStride / 4; ++q) {
-                    const int4 x = __ldcg(src + q);
-                    v[4 * q] = x.x;
-                    v[4 * q + 1] = x.y;
-                    v[4 * q + 2] = x.z;
-                    v[4 * q + 3] = x.w;
-                }
-            } else {
+            for (int cc = 0; cc < 9; ++cc) tl[cc] = (q + a.koff[3 * cc]) << rb;
+            int64_t pos[9];
+            lower_bound9(a.sv, n, tl, pos);
 #pragma unroll
-                for (int k = 0; k < kNbrStride; ++k) v[k] = -1;
-            }
-            uint32_t uni = 0;
+            for (int cc = 0; cc < 9; ++cc) {
+                const uint64_t hi_k = q + a.koff[3 * cc + 2];
+                int32_t x[3] = {-1, -1, -1};
 #pragma unroll
-            for (int k = 0; k < kTaps; ++k) {
-                const bool present = (m >> k) & 1u;
-                int32_t tile_k = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) tile_k += sm.qcnt[w >> 2][q][k];
-                uni |= (tile_k > 0 ? 1u : 0u) << k;
-                if (present) {
-                    int64_t off = sm.tap_base[k] + tcnt[tl * kTaps + k] + __popc(ball[k] & lt);
-                    for (int q = 0; q < quarter; ++q) off += sm.qcnt[w >> 2][q][k];
-                    if (off >= 0 && off < kTaps * n) {
-                        a.in_rows[off] = v[k];
-                        a.out_rows[off] = r;
-                    } else {
-                        atomicOr(&sm.err, kStatusInternal);
+                for (int j = 0; j < 3; ++j) {
+                    const int64_t pp = pos[cc] + j;
+                    if (pp < n) {
+                        const uint64_t vv = __ldg(a.sv + pp);
+                        const uint64_t kk = vv >> rb;
+                        if (kk <= hi_k) {
+                            const uint64_t dz = kk - (tl[cc] >> rb);
+                            const int64_t rr = static_cast<int64_t>(vv & rmask);
+                            const int32_t nr = rr < n ? static_cast<int32_t>(rr) : -1;
+                            if (dz == 0) x[0] = nr;
+                            if (dz == 1) x[1] = nr;
+                            if (dz == 2) x[2] = nr;
+                        }
                     }
                 }
-                a.gtab[k * a.n_pad + s] = present ? v[k] : -1;
+                m |= ((x[0] >= 0 ? 1u : 0u) | (x[1] >= 0 ? 2u : 0u) | (x[2] >= 0 ? 4u : 0u)) << (3 * cc);
+                if (row) {
+                    row[3 * cc] = x[0];
+                    row[3 * cc + 1] = x[1];
+                    row[3 * cc + 2] = x[2];
+                }
             }
-            a.perm[s] = r;
-            if (quarter == 0 && lane == 0) a.tile_union[ta + tl] = uni;
+            if (row) {
+                row[27] = -1;
+                reinterpret_cast<int4*>(row)[7] = make_int4(-1, -1, -1, -1);
+            }
+        } else if (row) {
+#pragma unroll
+            for (int qq = 0; qq < kNbrStride / 4; ++qq) reinterpret_cast<int4*>(row)[qq] = make_int4(-1, -1, -1, -1);
         }
-        __syncthreads();
+        if (r >= 0) a.mask[r] = m;
     }
-    if (t == 0 && sm.err) atomicOr(a.status, sm.err);
+    add_tap_counts(m, cnt);
+    __syncthreads();
+    if (threadIdx.x < kTaps && cnt[threadIdx.x]) atomicAdd(a.tap_count + threadIdx.x, cnt[threadIdx.x]);
+    if (threadIdx.x == 0 && err) atomicOr(a.status, err);
+}
+
+// One block of 128 threads per tile of the mask-sorted order: perm, the
+// per-tap pair lists and the GEMM gather table.  Reads the sorted packed
+// (mask key << rb | row) array, the masks, the kernel map and the (tap, tile)
+// offsets published by the cluster part; only the taps of the tile's union
+// get gather-table entries (the GEMM reads no others).
+__global__ void __launch_bounds__(kTileRows) k_tile_write_packed(const FusedArgs a, const uint64_t* __restrict__ ms) {
+    __shared__ int32_t wc[kTileRows / 32][kTaps];
+    __shared__ int32_t err;
+    const int64_t t = blockIdx.x;
+    const int64_t T = a.n_tiles;
+    const int64_t n = a.n;
+    const int rb = a.row_bits;
+    const uint64_t rmask = (uint64_t(1) << rb) - 1;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) err = 0;
+    const int64_t s = t * kTileRows + threadIdx.x;
+    int32_t r = s < n ? static_cast<int32_t>(ms[s] & rmask) : -1;
+    if (r >= n) {
+        r = -1;
+        atomicOr(&err, kStatusInternal);
+    }
+    const uint32_t m = r >= 0 ? a.mask[r] : 0u;
+    const uint32_t uni = a.tile_union[t];
+    int32_t v[kNbrStride];
+    if (r >= 0) {
+        const int4* src = reinterpret_cast<const int4*>(a.nbr + static_cast<int64_t>(r) * kNbrStride);
+#pragma unroll
+        for (int q = 0; q < kNbrStride / 4; ++q) {
+            const int4 x = src[q];
+            v[4 * q] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kNbrStride; ++k) v[k] = -1;
+    }
+    uint32_t ball[kTaps];
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) {
+        ball[k] = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
+        if (lane == 0) wc[warp][k] = __popc(ball[k]);
+    }
+    __syncthreads();
+    a.perm[s] = r;
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) {
+        if (!((uni >> k) & 1u)) continue;
+        const bool present = (m >> k) & 1u;
+        if (present) {
+            int64_t off = a.seg_off[static_cast<int64_t>(k) * T + t] + __popc(ball[k] & lt);
+            for (int q = 0; q < warp; ++q) off += wc[q][k];
+            if (off >= 0 && off < kTaps * n) {
+                a.in_rows[off] = v[k];
+                a.out_rows[off] = r;
+            } else {
+                atomicOr(&err, kStatusInternal);
+            }
+        }
+        a.gtab[static_cast<int64_t>(k) * a.n_pad + s] = present ? v[k] : -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && err) atomicOr(a.status, err);
 }
 
 }  // namespace
 
 // Tiles per CTA are bounded by kFusedMaxRows / kTileRows / (smallest cluster).
-constexpr int kMinCluster = 8;
+constexpr int kMinCluster = 16;
 constexpr size_t kFusedSmem = sizeof(FusedSmem) +
-    static_cast<size_t>(kFusedMaxRows / kTileRows / kMinCluster) * (kTaps + 1) * sizeof(int32_t);
+    static_cast<size_t>(kFusedMaxRows / kTileRows / kMinCluster) * (kTaps + 2) * sizeof(int32_t);
 
 int fused_cluster_size(cudaStream_t s) {
     static int cached = -1;
@@ -624,8 +734,29 @@ int launch_map_fused(const FusedArgs& a, int cluster, cudaStream_t s) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    SPCONV_CHECK_CUDA(cudaLaunchKernelEx(&cfg, k_map_fused, a));
-    count_launch();
+    if (a.mapper == SPCONV_MAPPER_SORTED) {
+        SPCONV_CHECK_CUDA(cudaLaunchKernelEx(&cfg, k_map_fused, a, static_cast<int>(kPartSort)));
+        SearchArgs sa;
+        const int key_passes = (a.key_bits + kDigitMax - 1) / kDigitMax;
+        sa.sv = (key_passes & 1) ? a.vb : a.va;
+        sa.n = a.n;
+        sa.rb = a.row_bits;
+        sa.key_bits = a.key_bits;
+        for (int k = 0; k < kTaps; ++k) sa.koff[k] = a.koff[k];
+        sa.nbr = a.nbr;
+        sa.mask = a.mask;
+        sa.tap_count = a.tap_count;
+        sa.status = a.status;
+        k_search_sorted<<<static_cast<unsigned>((a.n + 255) / 256), 256, 0, s>>>(sa);
+        SPCONV_CHECK_CUDA(cudaGetLastError());
+        count_launch(2);
+    }
+    SPCONV_CHECK_CUDA(cudaLaunchKernelEx(&cfg, k_map_fused, a, static_cast<int>(kPartRest)));
+    // the mask sort has an odd or even number of passes: the packed pairs end in vb or va
+    constexpr int kMaskPasses = (kTaps + kDigitMax - 1) / kDigitMax;
+    k_tile_write_packed<<<static_cast<unsigned>(a.n_tiles), kTileRows, 0, s>>>(a, (kMaskPasses & 1) ? a.vb : a.va);
+    SPCONV_CHECK_CUDA(cudaGetLastError());
+    count_launch(2);
     return SPCONV_OK;
 }
 

@@ -9,8 +9,10 @@
 
 namespace spconv {
 
-// Largest row count the single-launch pipeline takes.
+// Largest row count the single-launch pipeline takes, and the per-CTA radix
+// histogram width it uses (digits of up to 10 bits).
 constexpr int64_t kFusedMaxRows = int64_t(1) << 20;
+constexpr int kFusedBins = 1024;
 
 struct FusedArgs {
     const int4* coords;
@@ -30,7 +32,7 @@ struct FusedArgs {
     // scratch
     uint64_t* va;               // [n]
     uint64_t* vb;               // [n]
-    int32_t* hist;              // [3][cluster][256]
+    int32_t* hist;              // [3][cluster][kFusedBins]
     int32_t* cta_tot;           // [cluster][27]
     int32_t* cta_bkt;           // [cluster][28]
     // outputs (see MapHandle)
@@ -45,6 +47,7 @@ struct FusedArgs {
     int32_t* gtab;
     uint32_t* tile_union;
     int32_t* tile_order;
+    int32_t* seg_off;           // [27][n_tiles] first pair of (tap, tile)
     int32_t* status;
     int64_t n_tiles, n_pad;
 };

@@ -277,8 +277,10 @@ def test_stage_six_layers_and_fp32_layer():
 
 def test_launch_count_reported():
     wl = S.random_cloud(51, 3000, shape=(16, 16, 16), c_in=64, c_out=64)
-    m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1)
-    assert sc.last_launch_count() == 1                # the whole map in one cluster launch
+    m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="dense")
+    assert sc.last_launch_count() == 2                # cluster build + whole-GPU compaction write
+    sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="sorted")
+    assert sc.last_launch_count() == 4                # cluster sort, search, cluster rest, write
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, pipeline="multi")
     assert sc.last_launch_count() > 5
     sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
