@@ -12,12 +12,23 @@
 //
 // Per CTA (persistent, one per SM), warp-specialised:
 //   warps 0-3   epilogue: tcgen05.ld of the accumulator, bf16 convert, store
-//   warp 4      TMEM allocation + MMA issue (one thread)
-//   warps 5..   one producer warp per pipeline stage: cp.async 16-byte row
+//   warp 4      TMEM allocation + MMA issue (the whole warp runs the loop,
+//               lane 0 issues)
+//   warp 5      scheduler: walks this CTA's work items (tile, output block)
+//               and bulk-copies each tile's gather indices for every tap of
+//               its union into shared memory, two items ahead of the
+//               producers.  Items come largest tap union first and are dealt
+//               to the CTAs in snake order (CTA c takes item c of the first
+//               round, item 2G-1-c of the second, ...), which keeps the
+//               largest and smallest items together and the SMs balanced.
+//   warps 6..   one producer warp per pipeline stage: cp.async 16-byte row
 //               gathers of A into the 128-byte-swizzled layout (a row
 //               without the neighbour is written as zeros, with no memory
 //               request), plus one bulk async copy of the pre-packed weight
-//               tile B
+//               tile B.  Warp w runs on scheduler partition w % 4; no
+//               producer is placed on partition 0, where the MMA warp runs,
+//               so the MMA issue never queues behind a burst of gathers
+//               (warps 8, 12 are left idle).
 // The accumulator is double-buffered in TMEM so the epilogue of one tile
 // overlaps the main loop of the next.
 #include <cuda_bf16.h>
@@ -35,8 +46,18 @@ constexpr int BM = 128;          // tile rows (MMA M)
 constexpr int BK = 64;           // input channels per stage (one 128-byte row)
 constexpr int kEpiWarps = 4;
 constexpr int kMmaWarp = 4;
-constexpr int kProdWarp0 = 5;
+constexpr int kSchedWarp = 5;
+constexpr int kProdWarp0 = 6;
+
+// Warp of producer slot s: the s-th warp id >= kProdWarp0 that is not a
+// multiple of 4, and the inverse (-1 for a warp that is not a producer).
+__host__ __device__ constexpr int producer_warp(int s) { return kProdWarp0 + s + (s + 1) / 3; }
+__device__ __forceinline__ int producer_slot(int w) {
+    return (w < kProdWarp0 || (w & 3) == 0) ? -1 : w - kProdWarp0 - ((w - 1) / 4 - 1);
+}
 constexpr int kStageA = BM * BK * 2;   // 16 KB
+constexpr int kIdxBytes = kTaps * BM * 4;   // one item's gather indices, 13.5 KB
+constexpr int kMetaRing = 4;                // items in flight between scheduler and epilogue
 
 struct TcParams {
     const __nv_bfloat16* feats;   // [n][c_in]
@@ -60,11 +81,22 @@ struct TcConfig {
     static constexpr int kStageB = NTMAX * 128;
     static constexpr int kStage = kStageA + kStageB;
     static constexpr int kStages = (NTMAX == 256) ? 4 : (NTMAX == 128 ? 6 : 8);
-    static constexpr int kThreads = 32 * (kProdWarp0 + kStages);
+    // The MMA thread waits once per group of kGroup stages: a barrier wait
+    // stalls its issue for ~100-200 cycles, which only hides behind at least
+    // ~500 cycles of queued MMA work (4 MMAs of N=256, or 8 of N=128).
+    static constexpr int kGroup = (NTMAX == 256) ? 1 : 2;
+    static_assert(kStages % kGroup == 0, "stages come in whole groups");
+    static constexpr int kThreads = 32 * (producer_warp(kStages - 1) + 1);   // one producer warp per stage
     static constexpr int kTmemCols = 2 * NTMAX < 32 ? 32 : 2 * NTMAX;
-    static constexpr int kBarBytes = 256;
-    static constexpr int kSmem = kStages * kStage + 1024 + kBarBytes;
+    static constexpr int kBarBytes = 512;
+    static constexpr int kSmem = kStages * kStage + 2 * kIdxBytes + 1024 + kBarBytes;
+    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
+
+// Item that CTA `cta` of `grid` takes in its round L (snake order).
+__device__ __forceinline__ int snake_item(int L, int cta, int grid) {
+    return L * grid + ((L & 1) ? grid - 1 - cta : cta);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -75,26 +107,41 @@ template <int NTMAX>
 __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const TcParams p) {
     using Cfg = TcConfig<NTMAX>;
     constexpr int S = Cfg::kStages;
+    constexpr int G = Cfg::kGroup;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStage);
-    uint64_t* full = bars;             // [S]
-    uint64_t* empty = bars + S;        // [S]
-    uint64_t* acc_full = bars + 2 * S; // [2]
-    uint64_t* acc_empty = acc_full + 2;// [2]
-    uint64_t* exit_bar = acc_empty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(exit_bar + 1);
+    int32_t* idx = reinterpret_cast<int32_t*>(smem + S * Cfg::kStage);   // [2][27][128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStage + 2 * kIdxBytes);
+    uint64_t* full = bars;                       // [S / G], one per group of G stages
+    uint64_t* empty = full + S;                  // [S]
+    uint64_t* acc_full = empty + S;              // [2]
+    uint64_t* acc_empty = acc_full + 2;          // [2]
+    uint64_t* idx_full = acc_empty + 2;          // [2] indices + item landed
+    uint64_t* idx_empty = idx_full + 2;          // [2] producers and MMA done with the item
+    uint64_t* meta_full = idx_empty + 2;         // [kMetaRing] item published (epilogue side)
+    uint64_t* meta_empty = meta_full + kMetaRing;// [kMetaRing] epilogue has read it
+    uint64_t* exit_bar = meta_empty + kMetaRing;
+    int32_t* m_item = reinterpret_cast<int32_t*>(exit_bar + 1);   // [kMetaRing], -1 = no more work
+    int32_t* m_tile = m_item + kMetaRing;
+    uint32_t* m_uni = reinterpret_cast<uint32_t*>(m_tile + kMetaRing);
+    uint32_t* tmem_slot = m_uni + kMetaRing;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(&full[s], 2);
+            if (s < S / G) ptx::mbar_init(&full[s], 2 * G);   // two arrivals per stage of the group
             ptx::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
             ptx::mbar_init(&acc_empty[b], kEpiWarps);
+            ptx::mbar_init(&idx_full[b], 1);
+            ptx::mbar_init(&idx_empty[b], S + 1);
+        }
+        for (int r = 0; r < kMetaRing; ++r) {
+            ptx::mbar_init(&meta_full[r], 1);
+            ptx::mbar_init(&meta_empty[r], kEpiWarps);
         }
         ptx::mbar_init(exit_bar, 1);
         *abort_flag = 0;
@@ -104,45 +151,129 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
         ptx::tmem_alloc(tmem_slot, Cfg::kTmemCols);
         ptx::tmem_relinquish();
     }
+    // the scheduler looks up its first item while the CTA sets up
+    int s_it = snake_item(0, blockIdx.x, gridDim.x), s_tile = 0;
+    uint32_t s_uni = 0;
+    if (warp == kSchedWarp && s_it < p.n_items) {
+        s_tile = p.tile_order[s_it / p.n_nb];
+        s_uni = p.tile_union[s_tile];
+    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t smem_base = ptx::smem_u32(smem);
+    const uint32_t idx_base = ptx::smem_u32(idx);
 
     auto fail = [&]() {
         atomicOr(p.status, kStatusTimeout);
         *abort_flag = 1;
     };
-    // lane 0 waits, the warp follows its verdict
+    // every lane polls (warp-uniform control flow); the warp goes on only if all saw the phase
     auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-        int ok = 1;
-        if (lane == 0) ok = ptx::mbar_wait(bar, parity, abort_flag) ? 1 : 0;
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        return ok != 0;
+        const bool ok = ptx::mbar_wait(bar, parity, abort_flag);
+        return __all_sync(0xFFFFFFFFu, ok);
     };
 
-    if (warp >= kProdWarp0) {
-        // ---------------- producers: warp (kProdWarp0 + s) owns stage s
-        const int slot = warp - kProdWarp0;
+    if (warp == kSchedWarp) {
+        // ---------------- scheduler: item L goes to index buffer L % 2 and
+        // meta slot L % kMetaRing
+        int pend[2] = {-1, -1};   // item issued into each index buffer, not yet known consumed
+        for (int L = 0;; ++L) {
+            const int b = L & 1, r = L % kMetaRing;
+            if (L >= kMetaRing && !warp_wait(&meta_empty[r], ((L / kMetaRing) - 1) & 1)) {
+                if (lane == 0) fail();
+                break;
+            }
+            if (L >= 2) {
+                if (!warp_wait(&idx_empty[b], ((L >> 1) - 1) & 1)) {
+                    if (lane == 0) fail();
+                    break;
+                }
+                pend[b] = -1;   // consumed, so its copies have landed
+            }
+            const int it = s_it;
+            const int tile = s_tile;
+            const uint32_t uni = s_uni;
+            if (it >= p.n_items) {   // no more work: publish the end marker
+                if (lane == 0) {
+                    m_item[r] = -1;
+                    ptx::mbar_arrive(&idx_full[b]);
+                    ptx::mbar_arrive(&meta_full[r]);
+                }
+                break;
+            }
+            if (lane == 0) {
+                m_item[r] = it;
+                m_tile[r] = tile;
+                m_uni[r] = uni;
+                ptx::mbar_arrive_expect_tx(&idx_full[b], static_cast<uint32_t>(__popc(uni)) * (BM * 4));
+            }
+            __syncwarp();
+            // lane k copies tap k's 128 indices to the tap's rank in the union
+            if (lane < kTaps && ((uni >> lane) & 1u)) {
+                const int rank = __popc(uni & ((1u << lane) - 1u));
+                ptx::bulk_copy_g2s(idx_base + static_cast<uint32_t>((b * kTaps + rank) * BM * 4),
+                                   p.gtab + static_cast<int64_t>(lane) * p.n_pad + static_cast<int64_t>(tile) * BM,
+                                   BM * 4, &idx_full[b]);
+            }
+            pend[b] = L;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&meta_full[r]);
+            // look up the next item now: the loads overlap the waits above
+            s_it = snake_item(L + 1, blockIdx.x, gridDim.x);
+            if (s_it < p.n_items) {
+                s_tile = p.tile_order[s_it / p.n_nb];
+                s_uni = p.tile_union[s_tile];
+            }
+        }
+        // copies still in flight (only after an abort) land before the CTA exits
+        if (lane == 0)
+            for (int b = 0; b < 2; ++b)
+                if (pend[b] >= 0 && !ptx::mbar_wait(&idx_full[b], (pend[b] >> 1) & 1, nullptr))
+                    atomicOr(p.status, kStatusTimeout);
+        __syncwarp();
+    } else if (producer_slot(warp) >= 0) {
+        // ---------------- producers: warp producer_warp(s) owns stage s and
+        // arrives on the barrier of its stage's group
+        const int slot = producer_slot(warp);
+        uint64_t* gfull = &full[slot / G];
         const uint32_t a_smem = smem_base + slot * Cfg::kStage;
         const uint32_t b_smem = a_smem + kStageA;
         const uint32_t b_bytes = static_cast<uint32_t>(p.n_tile) * 128u;
         uint32_t f = 0;
+        int64_t last = -1;   // last fill this warp issued
         bool stop = false;
-        for (int it = blockIdx.x; it < p.n_items && !stop; it += gridDim.x) {
-            const int tile = p.tile_order[it / p.n_nb];
+        // lane group g (8 lanes) gathers rows 32g .. 32g + 31, one 16-byte
+        // chunk per lane, so each instruction reads four whole 128-byte rows
+        const int grp = lane >> 3, chunk = lane & 7;
+        for (int L = 0; !stop; ++L) {
+            const int b = L & 1;
+            if (!warp_wait(&idx_full[b], (L >> 1) & 1)) {
+                if (lane == 0) fail();
+                break;
+            }
+            const int it = m_item[L % kMetaRing];
+            if (it < 0) break;
             const int nb = it % p.n_nb;
-            uint32_t uni = p.tile_union[tile];
-            while (uni && !stop) {
+            uint32_t uni = m_uni[L % kMetaRing];
+            const int32_t* gidx = idx + b * kTaps * BM;
+            for (int j = 0; uni && !stop; ++j) {
                 const int k = __ffs(uni) - 1;
                 uni &= uni - 1;
-                const int32_t* g = p.gtab + static_cast<int64_t>(k) * p.n_pad + static_cast<int64_t>(tile) * BM;
-                int32_t gr[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) gr[q] = g[lane + 32 * q];
                 for (int kc = 0; kc < p.k_chunks; ++kc, ++f) {
                     if (static_cast<int>(f % S) != slot) continue;
+                    // all 32 source rows of this lane group, read before any copy is issued
+                    int32_t sr[32];
+                    const int4* gsrc = reinterpret_cast<const int4*>(gidx + j * BM + 32 * grp);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int4 v4 = gsrc[q];
+                        sr[4 * q] = v4.x;
+                        sr[4 * q + 1] = v4.y;
+                        sr[4 * q + 2] = v4.z;
+                        sr[4 * q + 3] = v4.w;
+                    }
                     const uint32_t u = f / S;
                     if (u > 0 && !warp_wait(&empty[slot], (u - 1) & 1)) {
                         if (lane == 0) fail();
@@ -150,113 +281,152 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                         break;
                     }
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(&full[slot], b_bytes);
+                        ptx::mbar_arrive_expect_tx(gfull, b_bytes);
                         const uint8_t* src = p.wpack + (static_cast<int64_t>(nb * kTaps + k) * p.k_chunks + kc) * b_bytes;
-                        ptx::bulk_copy_g2s(b_smem, src, b_bytes, &full[slot]);
+                        ptx::bulk_copy_g2s(b_smem, src, b_bytes, gfull);
                     }
-                    const int chunk = lane & 7;
                     const int kcol = kc * BK + chunk * 8;
+                    const bool col_ok = kcol < p.c_in;
+                    const __nv_bfloat16* fcol = p.feats + kcol;
+                    const uint32_t dst0 = a_smem + static_cast<uint32_t>(32 * grp) * 128;
+                    bool bad = false;   // a row index past n: skipped, reported below
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int row = 4 * i + (lane >> 3);
-                        const int32_t src_row = __shfl_sync(0xFFFFFFFFu, gr[i >> 3], row & 31);
-                        const uint32_t dst = a_smem + row * 128 + ((chunk ^ (row & 7)) << 4);
-                        if (src_row >= 0 && kcol < p.c_in)
-                            ptx::cp_async_16(dst, p.feats + static_cast<int64_t>(src_row) * p.c_in + kcol, 16u);
+                        const int32_t src_row = sr[i];
+                        // row 32g + i; its swizzle phase is i & 7 since 32g is a multiple of 8
+                        const uint32_t dst = dst0 + i * 128 + ((chunk ^ (i & 7)) << 4);
+                        if (src_row >= 0 && src_row < p.n && col_ok)
+                            ptx::cp_async_16(dst, fcol + static_cast<int64_t>(src_row) * p.c_in, 16u);
                         else
                             ptx::st_shared_zero16(dst);   // absent neighbour: no memory request
+                        bad |= src_row >= p.n;
                     }
+                    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.status, kStatusInternal);
                     ptx::cp_async_commit();
                     ptx::cp_async_wait_all();
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&full[slot]);
+                    if (lane == 0) ptx::mbar_arrive(gfull);
+                    last = f;
                 }
             }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&idx_empty[b]);
         }
-        ptx::cp_async_wait_all();
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_bf16_f32(BM, static_cast<uint32_t>(p.n_tile));
-            uint32_t f = 0;
-            int local = 0;
-            bool stop = false;
-            for (int it = blockIdx.x; it < p.n_items && !stop; it += gridDim.x, ++local) {
-                const int tile = p.tile_order[it / p.n_nb];
-                const int buf = local & 1;
-                const uint32_t v = static_cast<uint32_t>(local >> 1);
-                if (v > 0 && !ptx::mbar_wait(&acc_empty[buf], (v - 1) & 1, abort_flag)) {
-                    fail();
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * NTMAX);
-                uint32_t uni = p.tile_union[tile];
-                bool first = true;
-                while (uni && !stop) {
-                    uni &= uni - 1;
-                    for (int kc = 0; kc < p.k_chunks; ++kc, ++f) {
-                        const int slot = static_cast<int>(f % S);
-                        if (!ptx::mbar_wait(&full[slot], (f / S) & 1, abort_flag)) {
-                            fail();
-                            stop = true;
-                            break;
-                        }
-                        ptx::tc_fence_after();
-                        const uint32_t a_addr = smem_base + slot * Cfg::kStage;
-                        const uint32_t b_addr = a_addr + kStageA;
-#pragma unroll
-                        for (int j = 0; j < BK / 16; ++j) {
-                            ptx::mma_bf16(d_tmem, ptx::sdesc_k128(a_addr + 32 * j),
-                                          ptx::sdesc_k128(b_addr + 32 * j), idesc,
-                                          (first && j == 0) ? 0u : 1u);
-                        }
-                        first = false;
-                        ptx::mma_commit(&empty[slot]);
-                    }
-                }
-                if (!stop) ptx::mma_commit(&acc_full[buf]);
+        // the last group may be incomplete: its remaining stages arrive empty
+        const uint32_t padded = (f + G - 1) / G * G;
+        for (uint32_t d = f; d < padded && !stop; ++d) {
+            if (static_cast<int>(d % S) != slot) continue;
+            const uint32_t u = d / S;
+            if (u > 0 && !warp_wait(&empty[slot], (u - 1) & 1)) {
+                if (lane == 0) fail();
+                break;
             }
-            // all MMAs issued by this thread have completed once exit_bar flips
-            ptx::mma_commit(exit_bar);
-            if (!ptx::mbar_wait(exit_bar, 0, nullptr)) atomicOr(p.status, kStatusTimeout);
+            if (lane == 0) {
+                ptx::mbar_arrive(gfull);
+                ptx::mbar_arrive(gfull);
+            }
+            last = d;
         }
+        // every copy this warp issued has landed before the CTA may exit
+        if (lane == 0 && last >= 0 && !ptx::mbar_wait(gfull, (static_cast<uint32_t>(last) / S) & 1, nullptr))
+            atomicOr(p.status, kStatusTimeout);
         __syncwarp();
-    } else {
-        // ---------------- epilogue: warp w reads TMEM lanes [32w, 32w + 32)
-        int local = 0;
-        for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++local) {
-            const int tile = p.tile_order[it / p.n_nb];
-            const int nb = it % p.n_nb;
-            const int buf = local & 1;
-            const uint32_t v = static_cast<uint32_t>(local >> 1);
-            if (!warp_wait(&acc_full[buf], v & 1)) {
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issuer: the warp runs the loop, lane 0 issues
+        const uint32_t leader = lane == 0;
+        const uint32_t idesc = ptx::idesc_bf16_f32(BM, static_cast<uint32_t>(p.n_tile));
+        uint32_t f = 0;
+        bool stop = false;
+        for (int L = 0; !stop; ++L) {
+            const int b = L & 1;
+            if (!warp_wait(&idx_full[b], (L >> 1) & 1)) {
+                if (lane == 0) fail();
+                break;
+            }
+            const int it = m_item[L % kMetaRing];
+            const int n_taps = __popc(m_uni[L % kMetaRing]);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&idx_empty[b]);
+            if (it < 0) break;
+            const int buf = L & 1;
+            const uint32_t v = static_cast<uint32_t>(L >> 1);
+            if (v > 0 && !warp_wait(&acc_empty[buf], (v - 1) & 1)) {
                 if (lane == 0) fail();
                 break;
             }
             ptx::tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * NTMAX);
+            bool first = true;
+            for (int t = 0; t < n_taps && !stop; ++t) {
+                for (int kc = 0; kc < p.k_chunks; ++kc, ++f) {
+                    const int slot = static_cast<int>(f % S);
+                    if (slot % G == 0 && !warp_wait(&full[slot / G], (f / S) & 1)) {
+                        if (lane == 0) fail();
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t a_addr = smem_base + slot * Cfg::kStage;
+                    const uint32_t b_addr = a_addr + kStageA;
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j) {
+                        ptx::mma_bf16_if(leader, d_tmem, ptx::sdesc_k128(a_addr + 32 * j),
+                                         ptx::sdesc_k128(b_addr + 32 * j), idesc, (first && j == 0) ? 0u : 1u);
+                    }
+                    first = false;
+                    ptx::mma_commit_if(leader, &empty[slot]);
+                }
+            }
+            if (!stop) ptx::mma_commit_if(leader, &acc_full[buf]);
+        }
+        // all MMAs issued by this warp have completed once exit_bar flips
+        ptx::mma_commit_if(leader, exit_bar);
+        // (no early exit on abort here: TMEM is freed only after this)
+        const bool done = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(exit_bar, 0, nullptr));
+        if (!done && lane == 0) atomicOr(p.status, kStatusTimeout);
+    } else if (warp < kEpiWarps) {
+        // ---------------- epilogue: warp w reads TMEM lanes [32w, 32w + 32)
+        for (int L = 0;; ++L) {
+            const int r = L % kMetaRing;
+            if (!warp_wait(&meta_full[r], (L / kMetaRing) & 1)) {
+                if (lane == 0) fail();
+                break;
+            }
+            const int it = m_item[r];
+            const int tile = m_tile[r];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&meta_empty[r]);
+            if (it < 0) break;
+            const int nb = it % p.n_nb;
             const int64_t s = static_cast<int64_t>(tile) * BM + warp * 32 + lane;
             const int32_t orig = s < p.n ? p.perm[s] : -1;
+            const int buf = L & 1;
+            if (!warp_wait(&acc_full[buf], (L >> 1) & 1)) {
+                if (lane == 0) fail();
+                break;
+            }
+            ptx::tc_fence_after();
             __nv_bfloat16* dst_row = orig >= 0 ? p.out + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile : nullptr;
             const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(buf * NTMAX);
-            for (int c = 0; c < p.n_tile; c += 16) {
-                uint32_t r[16];
-                ptx::tmem_ld_32x32b_x16(t_addr + c, r);
+            // n_tile is a multiple of 16; columns go 32 at a time (two loads per wait)
+            for (int c = 0; c < p.n_tile; c += 32) {
+                const bool two = c + 16 < p.n_tile;
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x16_at(t_addr + c, v);
+                if (two) ptx::tmem_ld_32x32b_x16_at(t_addr + c + 16, v + 16);
                 ptx::tmem_ld_wait();
                 if (dst_row) {
-                    uint4 lo, hi;
-                    lo.x = pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1]));
-                    lo.y = pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3]));
-                    lo.z = pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5]));
-                    lo.w = pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7]));
-                    hi.x = pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9]));
-                    hi.y = pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11]));
-                    hi.z = pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13]));
-                    hi.w = pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15]));
                     uint4* d = reinterpret_cast<uint4*>(dst_row + c);
-                    d[0] = lo;
-                    d[1] = hi;
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        if (h >= 2 && !two) break;
+                        uint4 q;
+                        q.x = pack_bf16x2(__uint_as_float(v[8 * h + 0]), __uint_as_float(v[8 * h + 1]));
+                        q.y = pack_bf16x2(__uint_as_float(v[8 * h + 2]), __uint_as_float(v[8 * h + 3]));
+                        q.z = pack_bf16x2(__uint_as_float(v[8 * h + 4]), __uint_as_float(v[8 * h + 5]));
+                        q.w = pack_bf16x2(__uint_as_float(v[8 * h + 6]), __uint_as_float(v[8 * h + 7]));
+                        d[h] = q;
+                    }
                 }
             }
             ptx::tc_fence_before();

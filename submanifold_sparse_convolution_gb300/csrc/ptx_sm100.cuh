@@ -125,6 +125,17 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst_smem, const void* src
         : "memory");
 }
 
+// Asynchronously pull [src, src + bytes) into L2 (16-byte aligned, bytes a
+// multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Barrier among the `count` threads (a multiple of 32) that use barrier `id`.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Four-row gather through a 2D tensor map (box: one row x 64 bf16, 128-byte
 // swizzle): rows r0..r3 at column col land in 4 consecutive 128-byte rows at
 // dst_smem.  A row index outside the tensor is filled with zeros.  Completion
@@ -205,12 +216,37 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// The same MMA issued only by threads whose `issue` is nonzero.  A whole warp
+// runs the issue loop and one lane carries the predicate, so the warp never
+// diverges around the issue (a long single-lane loop pays a branch-resolution
+// stall at every branch).
+__device__ __forceinline__ void mma_bf16_if(uint32_t issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+        : "memory");
+}
+
 // Arrive once on *bar when all previously issued tcgen05 async operations of
 // this thread have completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// mma_commit by the threads whose `issue` is nonzero (see mma_bf16_if).
+__device__ __forceinline__ void mma_commit_if(uint32_t issue, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(issue)
         : "memory");
 }
 
@@ -225,6 +261,11 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
+}
+
+// The same load into r[0..15] of a larger register array.
+__device__ __forceinline__ void tmem_ld_32x32b_x16_at(uint32_t taddr, uint32_t* r) {
+    tmem_ld_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
