@@ -159,11 +159,23 @@ def run_ours(args, rank, world, device):
     stream = torch.cuda.current_stream(device)
     launches = [0]
 
+    # events inside the timed steps: per step [start, map done, layer 0 done]
+    marks = []
+    recording = [False]
+
+    def mark():
+        if recording[0]:
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            marks[-1].append(e)
+
     def layers(m, x):
         y = None
         for li in range(L):
             y = sc.subm_forward_packed(m, x, wps[li])
             launches[0] += sc.last_launch_count()
+            if li == 0:
+                mark()
             if li + 1 < L:
                 x = torch.relu(y)
         return y
@@ -171,6 +183,7 @@ def run_ours(args, rank, world, device):
     def step():
         m = sc.build_map(coords, wl.spatial_shape, wl.batch_size)
         launches[0] += sc.last_launch_count()
+        mark()
         y = layers(m, feats)
         m.destroy()
         return y
@@ -189,6 +202,8 @@ def run_ours(args, rank, world, device):
         for i in range(reps):
             flush.zero_()
             ev[i][0].record(stream)
+            if recording[0]:
+                marks.append([ev[i][0]])
             fn()
             ev[i][1].record(stream)
         torch.cuda.synchronize(device)
@@ -208,9 +223,14 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize(device)
     launches[0] = 0
     t0 = time.time()
+    recording[0] = True
     step_ms = timed(step, args.steps)
+    recording[0] = False
     t1 = time.time()
     gpu_launches = launches[0]
+    # map and first-layer GEMM durations of every timed step, from the same events
+    map_ms = [mk[0].elapsed_time(mk[1]) for mk in marks]
+    gemm_ms = [mk[1].elapsed_time(mk[2]) for mk in marks]
     torch.cuda.synchronize(device)
     if world > 1:
         torch.distributed.barrier()
@@ -224,11 +244,6 @@ def run_ours(args, rank, world, device):
         sampler.stop()
     clocks = sampler.summary(t0, t1) if sampler else None
 
-    # ---- components (same flush discipline)
-    reps = max(5, min(50, args.steps))
-    map_ms = timed(lambda: sc.build_map(coords, wl.spatial_shape, wl.batch_size).destroy(), reps)
-    x = feats
-    gemm_ms = timed(lambda: sc.subm_forward_packed(m0, x, wps[0]), reps)
     map_launches = None
     m1 = sc.build_map(coords, wl.spatial_shape, wl.batch_size)
     map_launches = sc.last_launch_count()
