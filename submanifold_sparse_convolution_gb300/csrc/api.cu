@@ -52,7 +52,6 @@ bool use_tensor_path(int32_t c_in, int32_t c_out, int32_t dtype, const void* fea
 }  // namespace
 
 cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t s) {
-    constexpr int kMaxDevices = 64;
     static cudaMemPool_t pools[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

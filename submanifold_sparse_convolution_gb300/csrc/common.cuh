@@ -8,6 +8,7 @@
 namespace spconv {
 
 constexpr int kTaps = 27;
+constexpr int kMaxDevices = 64;    // per-device one-time settings are kept for device ids below this
 constexpr int kTileRows = 128;      // rows per output tile (tensor-core M)
 constexpr int kNbrStride = 32;      // padded width of the internal kernel-map rows
 

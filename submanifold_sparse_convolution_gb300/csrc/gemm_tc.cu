@@ -489,7 +489,14 @@ int num_sms() {
 template <int NTMAX>
 int launch_tc(const TcParams& p, cudaStream_t s) {
     using Cfg = TcConfig<NTMAX>;
-    SPCONV_CHECK_CUDA(cudaFuncSetAttribute(k_tc_gemm<NTMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem));
+    static bool smem_set[kMaxDevices] = {};   // once per device
+    int dev = 0;
+    SPCONV_CHECK_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return SPCONV_ERR_UNSUPPORTED;
+    if (!smem_set[dev]) {
+        SPCONV_CHECK_CUDA(cudaFuncSetAttribute(k_tc_gemm<NTMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem));
+        smem_set[dev] = true;
+    }
     const int grid = p.n_items < num_sms() ? p.n_items : num_sms();
     k_tc_gemm<NTMAX><<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(p);
     count_launch();

@@ -52,53 +52,6 @@ struct FusedArgs {
     int64_t n_tiles, n_pad;
 };
 
-// Lower bounds of 9 targets in a sorted array a[0..n) (first index with
-// a[i] >= t[c], n if none), searched in lockstep: the branch-free halving
-// below takes the same steps for every target, so each step issues 9
-// independent loads instead of one.
-__device__ __forceinline__ void lower_bound9(const uint64_t* __restrict__ a, int64_t n, const uint64_t (&t)[9],
-                                             int64_t (&out)[9]) {
-    int64_t base[9];
-#pragma unroll
-    for (int c = 0; c < 9; ++c) base[c] = 0;
-    int64_t len = n;
-    while (len > 1) {
-        const int64_t half = len >> 1;
-#pragma unroll
-        for (int c = 0; c < 9; ++c) base[c] += __ldg(a + base[c] + half - 1) < t[c] ? half : 0;
-        len -= half;
-    }
-#pragma unroll
-    for (int c = 0; c < 9; ++c) out[c] = n == 0 ? 0 : base[c] + (__ldg(a + base[c]) < t[c] ? 1 : 0);
-}
-
-// Lower bound of t in a[0..n) given that it is >= from: probe from, from+1,
-// from+2, from+4, ... then halve inside the bracket.
-__device__ __forceinline__ int64_t lower_bound_from(const uint64_t* __restrict__ a, int64_t n, int64_t from,
-                                                    uint64_t t) {
-    if (from >= n || __ldg(a + from) >= t) return from;
-    int64_t lo = from;          // a[lo] < t
-    int64_t step = 1;
-    int64_t hi = from + 1;
-    while (hi < n && __ldg(a + hi) < t) {
-        lo = hi;
-        step <<= 1;
-        hi = from + step;
-    }
-    if (hi > n) hi = n;         // answer in (lo, hi]
-    int64_t first = lo + 1, count = hi - first;
-    while (count > 0) {
-        const int64_t st = count >> 1;
-        if (__ldg(a + first + st) < t) {
-            first += st + 1;
-            count -= st + 1;
-        } else {
-            count = st;
-        }
-    }
-    return first;
-}
-
 // Cluster size the fused kernel can be launched with on this device (16 or
 // 8), or 0 if none.
 int fused_cluster_size(cudaStream_t s);
