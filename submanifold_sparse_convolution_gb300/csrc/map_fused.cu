@@ -110,6 +110,21 @@ __device__ void radix_pass(const uint64_t* __restrict__ in, uint64_t* __restrict
     const int bins = 1 << width;
     const uint64_t dmask = static_cast<uint64_t>(bins - 1);
     const uint64_t nmask = (uint64_t(1) << next_width) - 1;
+    const int64_t lo = static_cast<int64_t>(c) * chunk;
+    const int64_t hi = lo + chunk < n ? lo + chunk : n;
+    // A round is RS consecutive elements; warp w owns the 32*IPT of them
+    // starting at w*32*IPT (item j of lane l at w*32*IPT + 32*j + l), so the
+    // stable order inside a round is (warp, item, lane).
+    uint64_t v[IPT];
+    auto load_round = [&](int64_t r0) {
+#pragma unroll
+        for (int j = 0; j < IPT; ++j) {
+            const int64_t idx = r0 + static_cast<int64_t>(w) * 32 * IPT + 32 * j + lane;
+            v[j] = idx < hi ? __ldcg(in + idx) : 0ull;
+        }
+    };
+    // the first round's keys are requested before the counts are read, so the two waits overlap
+    load_round(lo);
     if (t < bins) {
         int32_t h[kMaxCluster];
 #pragma unroll
@@ -127,27 +142,17 @@ __device__ void radix_pass(const uint64_t* __restrict__ in, uint64_t* __restrict
     __syncthreads();
     block_scan(sm.scan, bins, sm.tmp);
     if (t < bins) sm.base[t] = sm.scan[t] + sm.pre[t];
-    const int64_t lo = static_cast<int64_t>(c) * chunk;
-    const int64_t hi = lo + chunk < n ? lo + chunk : n;
     const uint32_t lt = lanemask_lt();
-    // A round is RS consecutive elements; warp w owns the 32*IPT of them
-    // starting at w*32*IPT (item j of lane l at w*32*IPT + 32*j + l), so the
-    // stable order inside a round is (warp, item, lane).
     for (int64_t r0 = lo; r0 < hi; r0 += RS) {
+        if (r0 != lo) load_round(r0);
         uint32_t* cz = reinterpret_cast<uint32_t*>(&sm.cnt[0][0]);
         for (int i = t; i < FW * BINS / 2; i += FT) cz[i] = 0;
         __syncthreads();
-        uint64_t v[IPT];
         int d[IPT], rk[IPT];
 #pragma unroll
-        for (int j = 0; j < IPT; ++j) {   // all loads first, so they are in flight together
-            const int64_t idx = r0 + static_cast<int64_t>(w) * 32 * IPT + 32 * j + lane;
-            v[j] = idx < hi ? __ldcg(in + idx) : 0ull;
-            d[j] = idx < hi ? 0 : BINS;
-        }
-#pragma unroll
         for (int j = 0; j < IPT; ++j) {
-            const bool valid = d[j] < BINS;
+            const int64_t idx = r0 + static_cast<int64_t>(w) * 32 * IPT + 32 * j + lane;
+            const bool valid = idx < hi;
             d[j] = valid ? static_cast<int>((v[j] >> shift) & dmask) : BINS;
             const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d[j]);
             const int prior = valid ? sm.cnt[w][d[j]] : 0;
@@ -157,12 +162,18 @@ __device__ void radix_pass(const uint64_t* __restrict__ in, uint64_t* __restrict
             __syncwarp();
         }
         __syncthreads();
-        if (t < bins) {   // exclusive prefix over the warps, per digit
+        if (t < bins) {   // exclusive prefix over the warps, per digit (loads batched ahead of the stores)
             int32_t pre = 0;
-            for (int q = 0; q < FW; ++q) {
-                const int32_t x = sm.cnt[q][t];
-                sm.cnt[q][t] = static_cast<uint16_t>(pre);
-                pre += x;
+#pragma unroll
+            for (int q0 = 0; q0 < FW; q0 += 16) {
+                int32_t x[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) x[q] = sm.cnt[q0 + q][t];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    sm.cnt[q0 + q][t] = static_cast<uint16_t>(pre);
+                    pre += x[q];
+                }
             }
             sm.rtot[t] = pre;
         }
@@ -190,25 +201,6 @@ __device__ void radix_pass(const uint64_t* __restrict__ in, uint64_t* __restrict
         __syncthreads();
         if (t < bins) sm.run[t] += sm.rtot[t];
     }
-    __syncthreads();
-}
-
-// Local (this CTA only) histogram of the `width`-bit digit at `shift` of
-// in[lo, hi), written to h[0..BINS).
-__device__ void local_hist(const uint64_t* __restrict__ in, int64_t lo, int64_t hi, int shift, int width,
-                           int32_t* h, FusedSmem& sm) {
-    const int t = threadIdx.x, lane = t & 31;
-    const uint64_t dmask = (uint64_t(1) << width) - 1;
-    sm.scan[t] = 0;
-    __syncthreads();
-    for (int64_t i0 = lo; i0 < hi; i0 += FT) {
-        const int64_t i = i0 + t;
-        const int dg = i < hi ? static_cast<int>((__ldcg(in + i) >> shift) & dmask) : BINS;
-        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dg);
-        if (dg < BINS && lane == __ffs(peers) - 1) atomicAdd(&sm.scan[dg], __popc(peers));
-    }
-    __syncthreads();
-    h[t] = sm.scan[t];
     __syncthreads();
 }
 
@@ -261,24 +253,35 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a, int part
     H[2][c * BINS + t] = 0;
     __syncthreads();
     if (part == kPartSort) {
+        // packed keys, and the first digit's counts of this CTA's part
         const uint64_t invalid = ((uint64_t(1) << a.key_bits) - 1) << rb;
-        for (int64_t i = lo + t; i < hi; i += FT) {
-            const int4 q = a.coords[i];
-            uint64_t key = invalid;
-            if (q.x >= 0 && q.x < a.batch && q.y >= 0 && q.y < a.shape.x && q.z >= 0 && q.z < a.shape.y &&
-                q.w >= 0 && q.w < a.shape.z) {
-                key = (((((static_cast<uint64_t>(q.x) << a.wx) | static_cast<uint64_t>(q.y + 1)) << a.wy) |
-                        static_cast<uint64_t>(q.z + 1))
-                       << a.wz |
-                       static_cast<uint64_t>(q.w + 1))
-                      << rb;
-            } else {
-                atomicOr(&sm.err, kStatusRange);
+        const uint64_t dmask0 = (uint64_t(1) << key_w) - 1;
+        sm.scan[t] = 0;
+        __syncthreads();
+        for (int64_t i0 = lo; i0 < hi; i0 += FT) {
+            const int64_t i = i0 + t;
+            int dg = BINS;
+            if (i < hi) {
+                const int4 q = a.coords[i];
+                uint64_t key = invalid;
+                if (q.x >= 0 && q.x < a.batch && q.y >= 0 && q.y < a.shape.x && q.z >= 0 && q.z < a.shape.y &&
+                    q.w >= 0 && q.w < a.shape.z) {
+                    key = (((((static_cast<uint64_t>(q.x) << a.wx) | static_cast<uint64_t>(q.y + 1)) << a.wy) |
+                            static_cast<uint64_t>(q.z + 1))
+                           << a.wz |
+                           static_cast<uint64_t>(q.w + 1))
+                          << rb;
+                } else {
+                    atomicOr(&sm.err, kStatusRange);
+                }
+                a.va[i] = key | static_cast<uint64_t>(i);
+                dg = static_cast<int>((key >> rb) & dmask0);
             }
-            a.va[i] = key | static_cast<uint64_t>(i);
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dg);
+            if (dg < BINS && lane == __ffs(peers) - 1) atomicAdd(&sm.scan[dg], __popc(peers));
         }
         __syncthreads();
-        local_hist(a.va, lo, hi, rb, key_w, H[0] + c * BINS, sm);
+        H[0][c * BINS + t] = sm.scan[t];
     } else if (a.mapper == SPCONV_MAPPER_DENSE) {
         const int64_t per = (a.cells + C - 1) / C;
         const int64_t g0 = static_cast<int64_t>(c) * per;
