@@ -71,14 +71,28 @@ typedef enum {
     SPCONV_PIPELINE_MULTI = 2  /* one kernel per step (any n)                                     */
 } spconv_pipeline_t;
 
+/* Work decomposition of the bf16 tensor-core forward ("Compaction is the
+ * largest single win", FlyDSL PR #942; "Offset-group partitioning", "Sparse
+ * convolution in FP32").  Both give the same sums up to fp32 rounding order. */
+typedef enum {
+    SPCONV_GEMM_AUTO = 0,        /* TILE_UNION (measured faster on every tested workload)      */
+    SPCONV_GEMM_TILE_UNION = 1,  /* output-stationary: 128 mask-sorted rows per tile, all taps of
+                                    the tile's mask union accumulated on chip, one bf16 store;
+                                    deterministic                                             */
+    SPCONV_GEMM_TAP_MAJOR = 2    /* 128 pairs of one tap per tile (compacted pair lists, no
+                                    zero rows), fp32 sums added in an [n][c_out] workspace,
+                                    then rounded to bf16; summation order varies run to run   */
+} spconv_gemm_t;
+
 /* Options of spconv_build_map.  Pass NULL for the defaults.  None of them
- * changes any result; they select how the same map is built. */
+ * changes any result beyond fp32 rounding order; they select how the same
+ * map is built and used. */
 typedef struct {
     int32_t mapper;          /* spconv_mapper_t, default AUTO                          */
     int32_t bit_order;       /* spconv_bit_order_t, default CALIBRATED                 */
     int64_t dense_max_cells; /* AUTO threshold on B*(X+2)*(Y+2)*(Z+2); default 1<<24   */
     int32_t pipeline;        /* spconv_pipeline_t, default AUTO                        */
-    int32_t reserved;        /* must be 0                                              */
+    int32_t gemm;            /* spconv_gemm_t for the bf16 forward on this map, default AUTO */
 } spconv_options_t;
 
 typedef struct spconv_map_s* spconv_map_t;
@@ -95,6 +109,7 @@ typedef struct {
     int32_t key_bits;    /* live bits of the packed coordinate key                */
     int32_t shape[3];    /* spatial shape used                                    */
     int32_t batch_size;  /* batch size used                                       */
+    int32_t gemm;        /* spconv_gemm_t the bf16 forward uses (TILE_UNION or TAP_MAJOR) */
 } spconv_map_info_t;
 
 /*

@@ -19,10 +19,11 @@ from . import _native
 
 __all__ = ["SpconvError", "Map", "WPack", "build_map", "subm_forward", "wpack_create",
            "subm_forward_packed", "map_status", "map_info", "map_export", "map_destroy",
-           "last_launch_count", "status_string", "MAPPERS", "BIT_ORDERS", "PIPELINES", "library"]
+           "last_launch_count", "status_string", "MAPPERS", "BIT_ORDERS", "PIPELINES", "GEMMS", "library"]
 
 MAPPERS = {"auto": 0, "dense": 1, "sorted": 2}
 PIPELINES = {"auto": 0, "fused": 1, "multi": 2}
+GEMMS = {"auto": 0, "tile_union": 1, "tap_major": 2}
 BIT_ORDERS = {"calibrated": 0, "plain": 1}
 _DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
@@ -118,11 +119,12 @@ class WPack:
 def build_map(coords: torch.Tensor, spatial_shape: Optional[Sequence[int]] = None,
               batch_size: int = 0, kernel_size: int = 3, mapper: str = "auto",
               bit_order: str = "calibrated", dense_max_cells: int = 0, pipeline: str = "auto",
-              stream: Optional[torch.cuda.Stream] = None) -> Map:
+              gemm: str = "auto", stream: Optional[torch.cuda.Stream] = None) -> Map:
     """``spconv_build_map``: kernel map of ``coords`` (int32 [N, 4] (b, x, y, z) on the GPU).
 
     ``spatial_shape`` None and ``batch_size`` 0 derive them on the device
-    (this synchronises the stream).
+    (this synchronises the stream).  ``gemm`` picks the bf16 forward's work
+    decomposition on this map (``GEMMS``).
     """
     lib = library()
     _require_cuda(coords, "coords")
@@ -132,7 +134,7 @@ def build_map(coords: torch.Tensor, spatial_shape: Optional[Sequence[int]] = Non
     if spatial_shape is not None:
         shape_arr = (ctypes.c_int32 * 3)(*[int(v) for v in spatial_shape])
     opt = _native.Options(MAPPERS[mapper], BIT_ORDERS[bit_order], int(dense_max_cells),
-                          PIPELINES[pipeline], 0)
+                          PIPELINES[pipeline], GEMMS[gemm])
     h = ctypes.c_void_p()
     rc = lib.spconv_build_map(_ptr(coords), int(coords.shape[0]),
                               ctypes.cast(shape_arr, _native.c_int32_p) if shape_arr is not None else None,
@@ -216,7 +218,8 @@ def map_info(m: Map) -> dict:
     return dict(n=info.n, pairs=info.pairs, n_tiles=info.n_tiles, tile_taps=info.tile_taps,
                 mapper={1: "dense", 2: "sorted"}.get(info.mapper, str(info.mapper)),
                 pipeline={1: "fused", 2: "multi"}.get(info.pipeline, str(info.pipeline)),
-                key_bits=info.key_bits, shape=tuple(info.shape), batch_size=info.batch_size)
+                key_bits=info.key_bits, shape=tuple(info.shape), batch_size=info.batch_size,
+                gemm={1: "tile_union", 2: "tap_major"}.get(info.gemm, str(info.gemm)))
 
 
 def map_export(m: Map, stream: Optional[torch.cuda.Stream] = None) -> dict:

@@ -17,7 +17,7 @@ c_int32_p = ctypes.POINTER(ctypes.c_int32)
 class Options(ctypes.Structure):
     _fields_ = [("mapper", ctypes.c_int32), ("bit_order", ctypes.c_int32),
                 ("dense_max_cells", ctypes.c_int64), ("pipeline", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("gemm", ctypes.c_int32)]
 
 
 class MapInfo(ctypes.Structure):
@@ -25,7 +25,7 @@ class MapInfo(ctypes.Structure):
                 ("tile_taps", ctypes.c_int64), ("mapper", ctypes.c_int32),
                 ("pipeline", ctypes.c_int32),
                 ("key_bits", ctypes.c_int32), ("shape", ctypes.c_int32 * 3),
-                ("batch_size", ctypes.c_int32)]
+                ("batch_size", ctypes.c_int32), ("gemm", ctypes.c_int32)]
 
 
 # name -> (restype, argtypes)

@@ -100,7 +100,7 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
             return SPCONV_ERR_INVALID_ARG;
         if (opt->dense_max_cells < 0) return SPCONV_ERR_INVALID_ARG;
         if (opt->pipeline < SPCONV_PIPELINE_AUTO || opt->pipeline > SPCONV_PIPELINE_MULTI) return SPCONV_ERR_INVALID_ARG;
-        if (opt->reserved != 0) return SPCONV_ERR_INVALID_ARG;
+        if (opt->gemm < SPCONV_GEMM_AUTO || opt->gemm > SPCONV_GEMM_TAP_MAJOR) return SPCONV_ERR_INVALID_ARG;
     }
     int32_t shape[3] = {1, 1, 1};
     int32_t batch = batch_size;
@@ -237,6 +237,7 @@ int spconv_map_info(spconv_map_t map, spconv_map_info_t* info) {
     info->key_bits = map->key_bits;
     std::memcpy(info->shape, map->shape, sizeof(info->shape));
     info->batch_size = map->batch;
+    info->gemm = map->gemm;
     return SPCONV_OK;
 }
 
@@ -273,6 +274,7 @@ void spconv_map_destroy(spconv_map_t map) {
     if (!map) return;
     if (map->arena) cudaFreeAsync(map->arena, map->stream);
     if (map->wspace) cudaFreeAsync(map->wspace, map->stream);
+    if (map->acc) cudaFreeAsync(map->acc, map->stream);
     delete map;
 }
 

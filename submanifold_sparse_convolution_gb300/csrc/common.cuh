@@ -42,6 +42,7 @@ struct MapHandle {
     int32_t mapper = 0;       // spconv_mapper_t used
     int32_t pipeline = 0;     // spconv_pipeline_t used
     int32_t bit_order = 0;
+    int32_t gemm = 0;         // spconv_gemm_t used by the bf16 forward (TILE_UNION or TAP_MAJOR)
     int32_t key_bits = 0;
     // device arrays
     int32_t* status = nullptr;     // [1]
@@ -63,6 +64,9 @@ struct MapHandle {
     // weight workspace for spconv_subm_forward
     void* wspace = nullptr;
     size_t wspace_bytes = 0;
+    // fp32 sums of the tap-major forward ([n][c_out])
+    void* acc = nullptr;
+    size_t acc_bytes = 0;
 };
 
 struct WPackHandle {
@@ -85,7 +89,7 @@ bool tc_supported(int32_t c_in, int32_t c_out);
 int tc_tile_n(int32_t c_out);
 size_t tc_pack_bytes(int32_t c_in, int32_t c_out);
 int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, void* dst, cudaStream_t s);
-int tc_forward(const MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
+int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
                int32_t c_out, cudaStream_t s);
 
 // ---- SIMT path (gemm_simt.cu) ----------------------------------------------

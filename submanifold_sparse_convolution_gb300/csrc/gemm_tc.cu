@@ -31,6 +31,20 @@
 //               (warps 8, 12 are left idle).
 // The accumulator is double-buffered in TMEM so the epilogue of one tile
 // overlaps the main loop of the next.
+//
+// Two work decompositions share this kernel ("Compaction is the largest
+// single win", FlyDSL PR #942; "Offset-group partitioning", "Sparse
+// convolution in FP32"):
+//   tile-union (TM = false)  an item is a 128-row tile of the mask-sorted
+//       rows and one output block; it visits every tap of the tile's union,
+//       accumulates them all in TMEM and stores each row once, in bf16.
+//       Rows lacking a tap of the union multiply zeros.
+//   tap-major (TM = true)    an item is 128 consecutive pairs of one tap's
+//       compacted pair list (the last item of a tap is ragged), so no MMA
+//       row is wasted; each row's product is added in fp32 into an
+//       accumulation buffer (vector red.global.add), which a final pass
+//       rounds to bf16.  It trades the zero rows for reduction traffic of
+//       4 bytes per pair and output channel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -67,6 +81,10 @@ struct TcParams {
     const uint32_t* tile_union;   // [n_tiles]
     const int32_t* tile_order;    // [n_tiles]
     const int32_t* perm;          // [n_pad]
+    const int32_t* tap_off;       // [28]  tap-major: CSR offsets of the pair lists
+    const int32_t* in_rows;       // [P]   tap-major: input row of each pair
+    const int32_t* out_rows;      // [P]   tap-major: output row of each pair
+    float* acc;                   // [n][c_out] tap-major: fp32 sums (zero at launch)
     int32_t* status;
     int64_t n, n_pad;
     int32_t n_items;              // n_tiles * n_nb
@@ -103,7 +121,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int NTMAX>
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+template <int NTMAX, bool TM>
 __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const TcParams p) {
     using Cfg = TcConfig<NTMAX>;
     constexpr int S = Cfg::kStages;
@@ -126,6 +149,10 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
     uint32_t* m_uni = reinterpret_cast<uint32_t*>(m_tile + kMetaRing);
     uint32_t* tmem_slot = m_uni + kMetaRing;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // tap-major: the output rows of the items in the meta ring, in the last
+    // kMetaRing x 128 entries of the index area (only rank 0 of each index
+    // buffer is used in that mode)
+    int32_t* m_orow = idx + 2 * kTaps * BM - kMetaRing * BM;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -151,13 +178,46 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
         ptx::tmem_alloc(tmem_slot, Cfg::kTmemCols);
         ptx::tmem_relinquish();
     }
-    // the scheduler looks up its first item while the CTA sets up
-    int s_it = snake_item(0, blockIdx.x, gridDim.x), s_tile = 0;
-    uint32_t s_uni = 0;
-    if (warp == kSchedWarp && s_it < p.n_items) {
-        s_tile = p.tile_order[s_it / p.n_nb];
-        s_uni = p.tile_union[s_tile];
+    // Scheduler state.  Tile-union items come from the tile order; tap-major
+    // items are numbered tap by tap: lane k < 27 holds t_excl, the number of
+    // 128-pair tiles of taps before k, and the item count is derived here.
+    int n_items = p.n_items;
+    int32_t t_excl = 0, t_off = 0, t_end = 0;
+    if (TM && warp == kSchedWarp) {
+        t_off = lane <= kTaps ? p.tap_off[lane] : 0;
+        const int32_t nxt = __shfl_down_sync(0xFFFFFFFFu, t_off, 1);
+        const int32_t tiles = lane < kTaps ? (nxt - t_off + BM - 1) / BM : 0;
+        int32_t incl = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        t_excl = incl - tiles;
+        t_end = nxt;
+        n_items = __shfl_sync(0xFFFFFFFFu, incl, kTaps - 1) * p.n_nb;
     }
+    // the scheduler looks up its first item while the CTA sets up:
+    // tile-union (tile, union); tap-major (pair base, pair count in s_tile, tap bit in s_uni)
+    int s_it = snake_item(0, blockIdx.x, gridDim.x), s_tile = 0, s_cnt = 0;
+    uint32_t s_uni = 0;
+    auto lookup = [&](int it) {
+        if (TM) {
+            const int pt = it / p.n_nb;
+            const uint32_t le = __ballot_sync(0xFFFFFFFFu, lane < kTaps && t_excl <= pt);
+            const int k = __popc(le) - 1;
+            const int32_t ex = __shfl_sync(0xFFFFFFFFu, t_excl, k);
+            const int32_t off = __shfl_sync(0xFFFFFFFFu, t_off, k);
+            const int32_t end = __shfl_sync(0xFFFFFFFFu, t_end, k);
+            s_tile = off + (pt - ex) * BM;
+            s_cnt = end - s_tile < BM ? end - s_tile : BM;
+            s_uni = 1u << k;
+        } else {
+            s_tile = p.tile_order[it / p.n_nb];
+            s_uni = p.tile_union[s_tile];
+        }
+    };
+    if (warp == kSchedWarp && s_it < n_items) lookup(s_it);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -195,7 +255,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
             const int it = s_it;
             const int tile = s_tile;
             const uint32_t uni = s_uni;
-            if (it >= p.n_items) {   // no more work: publish the end marker
+            if (it >= n_items) {   // no more work: publish the end marker
                 if (lane == 0) {
                     m_item[r] = -1;
                     ptx::mbar_arrive(&idx_full[b]);
@@ -203,29 +263,45 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                 }
                 break;
             }
-            if (lane == 0) {
-                m_item[r] = it;
-                m_tile[r] = tile;
-                m_uni[r] = uni;
-                ptx::mbar_arrive_expect_tx(&idx_full[b], static_cast<uint32_t>(__popc(uni)) * (BM * 4));
+            if (TM) {
+                // the item's input rows (rank 0 of index buffer b) and output rows
+                // (meta slot r), -1 past the end of the tap's list
+                const int32_t cnt = s_cnt;
+#pragma unroll
+                for (int q = 0; q < BM / 32; ++q) {
+                    const int i = lane + 32 * q;
+                    idx[b * kTaps * BM + i] = i < cnt ? p.in_rows[tile + i] : -1;
+                    m_orow[r * BM + i] = i < cnt ? p.out_rows[tile + i] : -1;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    m_item[r] = it;
+                    m_tile[r] = tile;
+                    m_uni[r] = uni;
+                    ptx::mbar_arrive(&idx_full[b]);
+                }
+            } else {
+                if (lane == 0) {
+                    m_item[r] = it;
+                    m_tile[r] = tile;
+                    m_uni[r] = uni;
+                    ptx::mbar_arrive_expect_tx(&idx_full[b], static_cast<uint32_t>(__popc(uni)) * (BM * 4));
+                }
+                __syncwarp();
+                // lane k copies tap k's 128 indices to the tap's rank in the union
+                if (lane < kTaps && ((uni >> lane) & 1u)) {
+                    const int rank = __popc(uni & ((1u << lane) - 1u));
+                    ptx::bulk_copy_g2s(idx_base + static_cast<uint32_t>((b * kTaps + rank) * BM * 4),
+                                       p.gtab + static_cast<int64_t>(lane) * p.n_pad + static_cast<int64_t>(tile) * BM,
+                                       BM * 4, &idx_full[b]);
+                }
+                pend[b] = L;
             }
-            __syncwarp();
-            // lane k copies tap k's 128 indices to the tap's rank in the union
-            if (lane < kTaps && ((uni >> lane) & 1u)) {
-                const int rank = __popc(uni & ((1u << lane) - 1u));
-                ptx::bulk_copy_g2s(idx_base + static_cast<uint32_t>((b * kTaps + rank) * BM * 4),
-                                   p.gtab + static_cast<int64_t>(lane) * p.n_pad + static_cast<int64_t>(tile) * BM,
-                                   BM * 4, &idx_full[b]);
-            }
-            pend[b] = L;
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&meta_full[r]);
             // look up the next item now: the loads overlap the waits above
             s_it = snake_item(L + 1, blockIdx.x, gridDim.x);
-            if (s_it < p.n_items) {
-                s_tile = p.tile_order[s_it / p.n_nb];
-                s_uni = p.tile_union[s_tile];
-            }
+            if (s_it < n_items) lookup(s_it);
         }
         // copies still in flight (only after an abort) land before the CTA exits
         if (lane == 0)
@@ -394,19 +470,27 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
             }
             const int it = m_item[r];
             const int tile = m_tile[r];
+            // the row this thread writes: tile-union, perm of the sorted position;
+            // tap-major, the pair's output row
+            int32_t orig = -1;
+            if (TM) {
+                orig = m_orow[r * BM + warp * 32 + lane];
+            } else if (it >= 0) {
+                const int64_t s = static_cast<int64_t>(tile) * BM + warp * 32 + lane;
+                orig = s < p.n ? p.perm[s] : -1;
+            }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&meta_empty[r]);
             if (it < 0) break;
             const int nb = it % p.n_nb;
-            const int64_t s = static_cast<int64_t>(tile) * BM + warp * 32 + lane;
-            const int32_t orig = s < p.n ? p.perm[s] : -1;
             const int buf = L & 1;
             if (!warp_wait(&acc_full[buf], (L >> 1) & 1)) {
                 if (lane == 0) fail();
                 break;
             }
             ptx::tc_fence_after();
-            __nv_bfloat16* dst_row = orig >= 0 ? p.out + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile : nullptr;
+            __nv_bfloat16* dst_row =
+                (!TM && orig >= 0) ? p.out + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile : nullptr;
             const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(buf * NTMAX);
             // n_tile is a multiple of 16; columns go 32 at a time (two loads per wait)
             for (int c = 0; c < p.n_tile; c += 32) {
@@ -415,7 +499,17 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                 ptx::tmem_ld_32x32b_x16_at(t_addr + c, v);
                 if (two) ptx::tmem_ld_32x32b_x16_at(t_addr + c + 16, v + 16);
                 ptx::tmem_ld_wait();
-                if (dst_row) {
+                if (TM) {
+                    if (orig >= 0) {
+                        float* dacc = p.acc + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile + c;
+#pragma unroll
+                        for (int h = 0; h < 8; ++h) {
+                            if (h >= 4 && !two) break;
+                            red_add_v4(dacc + 4 * h, __uint_as_float(v[4 * h]), __uint_as_float(v[4 * h + 1]),
+                                       __uint_as_float(v[4 * h + 2]), __uint_as_float(v[4 * h + 3]));
+                        }
+                    }
+                } else if (dst_row) {
                     uint4* d = reinterpret_cast<uint4*>(dst_row + c);
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
@@ -486,21 +580,40 @@ int num_sms() {
     return sms > 0 ? sms : 1;
 }
 
-template <int NTMAX>
-int launch_tc(const TcParams& p, cudaStream_t s) {
+// fp32 sums of the tap-major variant -> bf16 output (round to nearest even),
+// four values per thread and step.
+__global__ void __launch_bounds__(256) k_acc_to_bf16(const float4* __restrict__ acc, uint2* __restrict__ out,
+                                                     int64_t count4) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < count4;
+         i += static_cast<int64_t>(gridDim.x) * 256) {
+        const float4 v = acc[i];
+        out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
+}
+
+// grid: one persistent CTA per SM, or fewer when the item count is known and smaller
+template <int NTMAX, bool TM>
+int launch_tc(const TcParams& p, int grid, cudaStream_t s) {
     using Cfg = TcConfig<NTMAX>;
     static bool smem_set[kMaxDevices] = {};   // once per device
     int dev = 0;
     SPCONV_CHECK_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return SPCONV_ERR_UNSUPPORTED;
     if (!smem_set[dev]) {
-        SPCONV_CHECK_CUDA(cudaFuncSetAttribute(k_tc_gemm<NTMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem));
+        SPCONV_CHECK_CUDA(
+            cudaFuncSetAttribute(k_tc_gemm<NTMAX, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem));
         smem_set[dev] = true;
     }
-    const int grid = p.n_items < num_sms() ? p.n_items : num_sms();
-    k_tc_gemm<NTMAX><<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(p);
+    k_tc_gemm<NTMAX, TM><<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(p);
     count_launch();
     return cuda_status(cudaGetLastError());
+}
+
+template <bool TM>
+int launch_tc_n(const TcParams& p, int grid, cudaStream_t s) {
+    if (p.n_tile > 128) return launch_tc<256, TM>(p, grid, s);
+    if (p.n_tile > 64) return launch_tc<128, TM>(p, grid, s);
+    return launch_tc<64, TM>(p, grid, s);
 }
 
 }  // namespace
@@ -538,7 +651,7 @@ int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, void* dst, cudaS
     return cuda_status(cudaGetLastError());
 }
 
-int tc_forward(const MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
+int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
                int32_t c_out, cudaStream_t s) {
     if (h->n == 0) return SPCONV_OK;
     TcParams p;
@@ -549,6 +662,10 @@ int tc_forward(const MapHandle* h, const void* feats, const void* wpack, void* o
     p.tile_union = h->tile_union;
     p.tile_order = h->tile_order;
     p.perm = h->perm;
+    p.tap_off = h->tap_off;
+    p.in_rows = h->in_rows;
+    p.out_rows = h->out_rows;
+    p.acc = nullptr;
     p.status = h->status;
     p.n = h->n;
     p.n_pad = h->n_pad;
@@ -560,9 +677,33 @@ int tc_forward(const MapHandle* h, const void* feats, const void* wpack, void* o
     const int64_t items = h->n_tiles * p.n_nb;
     if (items > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
     p.n_items = static_cast<int32_t>(items);
-    if (p.n_tile > 128) return launch_tc<256>(p, s);
-    if (p.n_tile > 64) return launch_tc<128>(p, s);
-    return launch_tc<64>(p, s);
+    const int sms = num_sms();
+    if (h->gemm != SPCONV_GEMM_TAP_MAJOR) return launch_tc_n<false>(p, p.n_items < sms ? p.n_items : sms, s);
+
+    // tap-major: zeroed fp32 sums, the GEMM adds every pair's product, one rounding pass
+    // (at most 27n pairs: the item count fits in int32 when 27n/128 * n_nb does)
+    if (static_cast<int64_t>(kTaps) * h->n / BM * p.n_nb > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
+    const size_t need = static_cast<size_t>(h->n) * c_out * sizeof(float);
+    if (h->acc_bytes < need) {
+        if (h->acc) cudaFreeAsync(h->acc, s);
+        h->acc = nullptr;
+        h->acc_bytes = 0;
+        if (pool_alloc(&h->acc, need, s) != cudaSuccess) {
+            cudaGetLastError();
+            h->acc = nullptr;
+            return SPCONV_ERR_OOM;
+        }
+        h->acc_bytes = need;
+    }
+    p.acc = static_cast<float*>(h->acc);
+    SPCONV_CHECK_CUDA(cudaMemsetAsync(p.acc, 0, need, s));
+    SPCONV_CHECK(launch_tc_n<true>(p, sms, s));
+    const int64_t count4 = static_cast<int64_t>(h->n) * c_out / 4;
+    const int64_t blocks = (count4 + 255) / 256;
+    k_acc_to_bf16<<<static_cast<unsigned>(blocks < 8 * sms ? blocks : 8 * sms), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(p.acc), reinterpret_cast<uint2*>(out), count4);
+    count_launch();
+    return cuda_status(cudaGetLastError());
 }
 
 }  // namespace spconv

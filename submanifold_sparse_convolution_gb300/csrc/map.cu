@@ -502,6 +502,7 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
     if (mapper == SPCONV_MAPPER_DENSE && (cells_overflow || cells > (int64_t(1) << 34))) return SPCONV_ERR_UNSUPPORTED;
     h->mapper = mapper;
     h->bit_order = opt ? opt->bit_order : SPCONV_ORDER_CALIBRATED;
+    h->gemm = (opt && opt->gemm == SPCONV_GEMM_TAP_MAJOR) ? SPCONV_GEMM_TAP_MAJOR : SPCONV_GEMM_TILE_UNION;
 
     // ---- pipeline: one cluster launch when the rows fit, else one kernel per step
     const int row_bits = std::max(1, bit_length(static_cast<uint64_t>(n > 0 ? n - 1 : 0)));

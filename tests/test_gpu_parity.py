@@ -58,10 +58,10 @@ def check_fp32(out, ref):
     assert err.size == 0 or err.max() <= FP32_ATOL, f"max abs err {err.max():.3e}"
 
 
-def build(wl, mapper="auto", bit_order="calibrated", pipeline="auto"):
+def build(wl, mapper="auto", bit_order="calibrated", pipeline="auto", gemm="auto"):
     coords = wl.coords.cuda()
     m = sc.build_map(coords, wl.spatial_shape, wl.batch_size, mapper=mapper, bit_order=bit_order,
-                     pipeline=pipeline)
+                     pipeline=pipeline, gemm=gemm)
     assert sc.map_status(m) == 0
     return m
 
@@ -188,6 +188,21 @@ def test_bf16_forward_small(c_in, c_out):
     check_bf16(out, ref)
 
 
+@pytest.mark.parametrize("c_in,c_out", CHANNELS)
+def test_bf16_tap_major_small(c_in, c_out):
+    # the tap-major decomposition: same sums, fp32 atomics, one rounding
+    wl = S.random_cloud(300 + c_in + c_out, 1500, shape=(14, 14, 14), batch_size=2, c_in=c_in, c_out=c_out)
+    m = build(wl, gemm="tap_major")
+    assert sc.map_info(m)["gemm"] == "tap_major"
+    out = sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
+    assert sc.map_status(m) == 0
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    ref = oracle.conv_f64(nbr, wl.feats.double().numpy(), wl.weights[0].double().numpy())
+    check_bf16(out, ref)
+    # a second call on the same map (the fp32 workspace is reused and cleared)
+    check_bf16(sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda()), ref)
+
+
 @pytest.mark.parametrize("c_in,c_out", [(64, 64), (16, 16), (5, 7), (128, 128)])
 def test_fp32_exact_small(c_in, c_out):
     wl = S.random_cloud(200 + c_in, 2000, shape=(14, 14, 14), c_in=c_in, c_out=c_out)
@@ -255,6 +270,18 @@ def test_bf16_workloads(name):
     assert torch.equal(out, sc.subm_forward(m, f, w))
 
 
+@pytest.mark.parametrize("name", ["outdoor", "deep", "large"])
+def test_bf16_workloads_tap_major(name):
+    wl = S.make_workload(name)
+    m = build(wl, gemm="tap_major")
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    out = sc.subm_forward_packed(m, wl.feats.cuda(), sc.wpack_create(wl.weights[0].cuda()))
+    assert sc.map_status(m) == 0
+    rows = sample_rows(wl.n, 3000, 8)
+    ref = oracle.conv_f64(nbr, wl.feats.double().numpy(), wl.weights[0].double().numpy(), rows=rows)
+    check_bf16(out[torch.from_numpy(rows).long().cuda()], ref)
+
+
 def test_stage_six_layers_and_fp32_layer():
     wl = S.make_workload("stage")
     m = build(wl)
@@ -285,3 +312,6 @@ def test_launch_count_reported():
     assert sc.last_launch_count() > 5
     sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
     assert sc.last_launch_count() == 2          # weight pack + GEMM
+    mt = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, gemm="tap_major")
+    sc.subm_forward(mt, wl.feats.cuda(), wl.weights[0].cuda())
+    assert sc.last_launch_count() == 3          # weight pack + GEMM + bf16 rounding pass
