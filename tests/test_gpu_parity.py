@@ -188,6 +188,21 @@ def test_bf16_forward_small(c_in, c_out):
     check_bf16(out, ref)
 
 
+@pytest.mark.parametrize("n", [1, 50, 1300, 4100])
+def test_bf16_c128_tile_pairs(n):
+    # ragged and single-tile inputs at C_out = 128 (one output block of the
+    # tensor-core kernel): a lone voxel, a short tile, odd tile counts
+    wl = S.random_cloud(400 + n, n, shape=(20, 20, 20), batch_size=1, c_in=128, c_out=128)
+    m = build(wl)
+    f, w = wl.feats.cuda(), wl.weights[0].cuda()
+    out = sc.subm_forward(m, f, w)
+    assert sc.map_status(m) == 0
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    check_bf16(out, oracle.conv_f64(nbr, wl.feats.double().numpy(), wl.weights[0].double().numpy()))
+    # a second call on the same map gives the same bits
+    assert torch.equal(out, sc.subm_forward(m, f, w))
+
+
 @pytest.mark.parametrize("c_in,c_out", CHANNELS)
 def test_bf16_tap_major_small(c_in, c_out):
     # the tap-major decomposition: same sums, fp32 atomics, one rounding
