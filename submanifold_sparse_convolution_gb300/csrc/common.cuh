@@ -20,6 +20,21 @@ enum : int32_t {
     kStatusInternal = 8,   // an internal consistency guard fired (a would-be out-of-range store was skipped)
 };
 
+// Programmatic dependent launch.  A kernel launched with
+// pdl_attr() may start while the previous kernel of its stream is finishing;
+// before its first read of anything an earlier kernel wrote it must call
+// pdl_wait(), which returns once every earlier kernel has completed and its
+// writes are visible.  pdl_trigger() lets the next such kernel be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+inline cudaLaunchAttribute pdl_attr() {
+    cudaLaunchAttribute at = {};
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    return at;
+}
+
 // Counts launches of the current host thread (reported by
 // spconv_last_launch_count).
 void count_launch(int n = 1);

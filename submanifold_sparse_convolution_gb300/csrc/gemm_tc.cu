@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
         ptx::tmem_alloc(tmem_slot, Cfg::kTmemCols);
         ptx::tmem_relinquish();
     }
+    // launched early (programmatic dependent launch): the map and inputs are
+    // read only after the kernels before this one have finished
+    pdl_wait();
     // Scheduler state.  Tile-union items come from the tile order; tap-major
     // items are numbered tap by tap: lane k < 27 holds t_excl, the number of
     // 128-pair tiles of taps before k, and the item count is derived here.
@@ -532,6 +535,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
     __syncthreads();
     ptx::tc_fence_after();
     if (warp == kMmaWarp) ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    pdl_trigger();
 }
 
 // Packed weight image: for each (output block nb, tap k, 64-channel input
@@ -604,9 +608,17 @@ int launch_tc(const TcParams& p, int grid, cudaStream_t s) {
             cudaFuncSetAttribute(k_tc_gemm<NTMAX, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem));
         smem_set[dev] = true;
     }
-    k_tc_gemm<NTMAX, TM><<<grid, Cfg::kThreads, Cfg::kSmem, s>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    SPCONV_CHECK_CUDA(cudaLaunchKernelEx(&cfg, k_tc_gemm<NTMAX, TM>, p));
     count_launch();
-    return cuda_status(cudaGetLastError());
+    return SPCONV_OK;
 }
 
 template <bool TM>

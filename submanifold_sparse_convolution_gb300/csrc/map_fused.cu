@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a, int part
     constexpr int kMaskW = (kTaps + kMaskPasses - 1) / kMaskPasses;
     if (t == 0) sm.err = 0;
     if (t < kTaps) sm.taps[t] = 0;
+    if (part == kPartRest) pdl_wait();   // launched early: the neighbour search must have finished
 
     // ---------------- phase 0: reset counters, pack keys / clear the grid
     const bool starts = part == kPartSort || a.mapper == SPCONV_MAPPER_DENSE;
@@ -301,6 +302,7 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a, int part
             cluster_sync_all();
         }
         if (t == 0 && sm.err) atomicOr(a.status, sm.err);
+        pdl_trigger();
         return;   // the neighbour search runs next on the whole GPU (k_search_window)
     } else if (a.mapper == SPCONV_MAPPER_DENSE) {
         // ---------------- dense grid: scatter row ids, then 27 lookups per row
@@ -527,6 +529,7 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a, int part
     }
     for (int i = t; i < nt; i += FT) a.tile_union[ta + i] = tuni[i];
     if (t == 0 && sm.err) atomicOr(a.status, sm.err);
+    pdl_trigger();
 }
 
 // Neighbour search on the whole GPU, between the two cluster launches.  One
@@ -593,7 +596,8 @@ __global__ void __launch_bounds__(kSearchRows) k_search_window(const SearchArgs 
     const int64_t s_end = s0 + kSearchRows < n ? s0 + kSearchRows : n;
     if (t < kTaps) cnt[t] = 0;
     if (t == 0) err = 0;
-    for (int64_t j = t; j < ns; j += kSearchRows) samp[j] = __ldg(a.sv + (j << a.sample_shift));
+    pdl_wait();   // the coordinate sort must have finished
+    for (int64_t j = t; j < ns; j += kSearchRows) samp[j] = __ldcg(a.sv + (j << a.sample_shift));
     const int64_t s = s0 + t;
     const uint64_t vs = s < n ? __ldg(a.sv + s) : ~uint64_t(0);
     __syncthreads();
@@ -754,6 +758,7 @@ __global__ void __launch_bounds__(kSearchRows) k_search_window(const SearchArgs 
     __syncthreads();
     if (t < kTaps && cnt[t]) atomicAdd(a.tap_count + t, cnt[t]);
     if (t == 0 && err) atomicOr(a.status, err);
+    pdl_trigger();
 }
 
 // One block of 128 threads per tile of the mask-sorted order: perm, the
@@ -771,6 +776,7 @@ __global__ void __launch_bounds__(kTileRows) k_tile_write_packed(const FusedArgs
     const uint64_t rmask = (uint64_t(1) << rb) - 1;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) err = 0;
+    pdl_wait();   // the mask sort and the (tap, tile) offsets must be complete
     const int64_t s = t * kTileRows + threadIdx.x;
     int32_t r = s < n ? static_cast<int32_t>(ms[s] & rmask) : -1;
     if (r >= n) {
@@ -821,6 +827,7 @@ __global__ void __launch_bounds__(kTileRows) k_tile_write_packed(const FusedArgs
     }
     __syncthreads();
     if (threadIdx.x == 0 && err) atomicOr(a.status, err);
+    pdl_trigger();
 }
 
 }  // namespace
@@ -911,15 +918,35 @@ int launch_map_fused(const FusedArgs& a, int cluster, cudaStream_t s) {
             SPCONV_CHECK_CUDA(cudaFuncSetAttribute(k_search_window, cudaFuncAttributeMaxDynamicSharedMemorySize, most));
             smem_set[dev] = true;
         }
-        k_search_window<<<static_cast<unsigned>((a.n + kSearchRows - 1) / kSearchRows), kSearchRows, smem, s>>>(sa);
-        SPCONV_CHECK_CUDA(cudaGetLastError());
+        cudaLaunchConfig_t scfg = {};
+        scfg.gridDim = dim3(static_cast<unsigned>((a.n + kSearchRows - 1) / kSearchRows));
+        scfg.blockDim = dim3(kSearchRows);
+        scfg.dynamicSmemBytes = smem;
+        scfg.stream = s;
+        cudaLaunchAttribute sattr[1] = {pdl_attr()};
+        scfg.attrs = sattr;
+        scfg.numAttrs = 1;
+        SPCONV_CHECK_CUDA(cudaLaunchKernelEx(&scfg, k_search_window, sa));
         count_launch(2);
     }
-    SPCONV_CHECK_CUDA(cudaLaunchKernelEx(&cfg, k_map_fused, a, static_cast<int>(kPartRest)));
+    {   // after the search: may start while it finishes (the dense mapper has no search before it)
+        cudaLaunchAttribute rattr[2] = {attr[0], pdl_attr()};
+        cudaLaunchConfig_t rcfg = cfg;
+        rcfg.attrs = rattr;
+        rcfg.numAttrs = a.mapper == SPCONV_MAPPER_SORTED ? 2 : 1;
+        SPCONV_CHECK_CUDA(cudaLaunchKernelEx(&rcfg, k_map_fused, a, static_cast<int>(kPartRest)));
+    }
     // the mask sort has an odd or even number of passes: the packed pairs end in vb or va
     constexpr int kMaskPasses = (kTaps + kDigitMax - 1) / kDigitMax;
-    k_tile_write_packed<<<static_cast<unsigned>(a.n_tiles), kTileRows, 0, s>>>(a, (kMaskPasses & 1) ? a.vb : a.va);
-    SPCONV_CHECK_CUDA(cudaGetLastError());
+    cudaLaunchConfig_t wcfg = {};
+    wcfg.gridDim = dim3(static_cast<unsigned>(a.n_tiles));
+    wcfg.blockDim = dim3(kTileRows);
+    wcfg.stream = s;
+    cudaLaunchAttribute wattr[1] = {pdl_attr()};
+    wcfg.attrs = wattr;
+    wcfg.numAttrs = 1;
+    const uint64_t* ms = (kMaskPasses & 1) ? a.vb : a.va;
+    SPCONV_CHECK_CUDA(cudaLaunchKernelEx(&wcfg, k_tile_write_packed, a, ms));
     count_launch(2);
     return SPCONV_OK;
 }
