@@ -140,6 +140,24 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# ranks: independent replicas (weak scaling), one timing for the whole job
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's ``value`` (the job takes as long as its slowest rank)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_layer(total_ms: float, steps: int, layers: int, world: int) -> float:
+    """µs per layer of the whole job: every rank ran ``steps`` steps of ``layers`` layers in ``total_ms``."""
+    return total_ms * 1e3 / (steps * layers * world)
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
@@ -241,11 +259,7 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize(device)
     if world > 1:
         torch.distributed.barrier()
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), device)
     if sampler:
         time.sleep(0.3)
         sampler.stop()
@@ -280,7 +294,7 @@ def run_ours(args, rank, world, device):
         return None
 
     layers_total = args.steps * L * world
-    us_per_layer = total_ms * 1e3 / layers_total
+    us_per_layer = job_us_per_layer(total_ms, args.steps, L, world)
     useful_tflops = useful_flops_layer * layers_total / (total_ms * 1e-3) / 1e12
     gemm_avg_s = statistics.mean(gemm_ms) * 1e-3
     gemm_tflops = useful_flops_layer / gemm_avg_s / 1e12
