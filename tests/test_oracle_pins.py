@@ -224,6 +224,30 @@ def test_order_and_pair_lists(calibrated):
     assert pairs_follow_perm(p, tap_off, outs)
 
 
+def test_calibrated_key_compares_rows_rarest_tap_first():
+    # "Calibrated bit order" (Sparse convolution in FP32): taps ranked by descending
+    # frequency, the rarest in the most significant key bit.  Restated independently:
+    # the tap order is a lexsort of (-count, tap), and two rows compare like their
+    # tap sets read from the rarest tap to the commonest, the first difference deciding.
+    wl = S.random_cloud(33, 1800, shape=(12, 12, 12), batch_size=1)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1)
+    m = oracle.masks(nbr).astype(np.int64)
+    counts = (nbr >= 0).sum(0)
+    order = oracle.tap_order(oracle.masks(nbr), True)
+    assert order.tolist() == np.lexsort((np.arange(27), -counts)).tolist()
+    key = oracle.sort_keys(oracle.masks(nbr), order).astype(np.int64)
+    rng = np.random.default_rng(34)
+    rare_first = order[::-1].tolist()
+    for i, j in rng.integers(0, len(m), size=(3000, 2)):
+        expect = 0
+        for tap in rare_first:
+            a, b = (m[i] >> tap) & 1, (m[j] >> tap) & 1
+            if a != b:
+                expect = 1 if a > b else -1
+                break
+        assert np.sign(key[i] - key[j]) == expect
+
+
 def test_mutated_pair_lists_are_caught():
     wl = S.random_cloud(32, 800, shape=(10, 10, 10))
     nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1)
