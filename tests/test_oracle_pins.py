@@ -229,7 +229,7 @@ def test_calibrated_key_compares_rows_rarest_tap_first():
     # frequency, the rarest in the most significant key bit.  Restated independently:
     # the tap order is a lexsort of (-count, tap), and two rows compare like their
     # tap sets read from the rarest tap to the commonest, the first difference deciding.
-    wl = S.random_cloud(33, 1800, shape=(12, 12, 12), batch_size=1)
+    wl = S.random_cloud(33, 1800, shape=(14, 14, 14), batch_size=1)
     nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1)
     m = oracle.masks(nbr).astype(np.int64)
     counts = (nbr >= 0).sum(0)
