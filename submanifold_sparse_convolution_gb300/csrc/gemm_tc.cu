@@ -104,7 +104,13 @@ struct TcConfig {
     // ~500 cycles of queued MMA work (4 MMAs of N=256, or 8 of N=128).
     static constexpr int kGroup = (NTMAX == 256) ? 1 : 2;
     static_assert(kStages % kGroup == 0, "stages come in whole groups");
-    static constexpr int kThreads = 32 * (producer_warp(kStages - 1) + 1);   // one producer warp per stage
+    // Producer warps per stage.  With N = 256 the tensor pipe spends 512 cycles
+    // on a stage, and one warp's ~1,600-cycle gather round trip across four
+    // stages cannot keep up, so two warps share each stage (64 rows each).
+    static constexpr int kProdPerStage = (NTMAX == 256) ? 2 : 1;
+    static_assert(kProdPerStage == 1 || kGroup == 1, "shared stages are not grouped");
+    static constexpr int kProducers = kStages * kProdPerStage;
+    static constexpr int kThreads = 32 * (producer_warp(kProducers - 1) + 1);
     static constexpr int kTmemCols = 2 * NTMAX < 32 ? 32 : 2 * NTMAX;
     static constexpr int kBarBytes = 512;
     static constexpr int kSmem = kStages * kStage + 2 * kIdxBytes + 1024 + kBarBytes;
@@ -131,6 +137,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
     using Cfg = TcConfig<NTMAX>;
     constexpr int S = Cfg::kStages;
     constexpr int G = Cfg::kGroup;
+    constexpr int P = Cfg::kProdPerStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int32_t* idx = reinterpret_cast<int32_t*>(smem + S * Cfg::kStage);   // [2][27][128]
@@ -157,14 +164,14 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            if (s < S / G) ptx::mbar_init(&full[s], 2 * G);   // two arrivals per stage of the group
+            if (s < S / G) ptx::mbar_init(&full[s], 2 * G * P);   // two arrivals per producer warp of the group
             ptx::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
             ptx::mbar_init(&acc_empty[b], kEpiWarps);
             ptx::mbar_init(&idx_full[b], 1);
-            ptx::mbar_init(&idx_empty[b], S + 1);
+            ptx::mbar_init(&idx_empty[b], Cfg::kProducers + 1);
         }
         for (int r = 0; r < kMetaRing; ++r) {
             ptx::mbar_init(&meta_full[r], 1);
@@ -313,9 +320,10 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                     atomicOr(p.status, kStatusTimeout);
         __syncwarp();
     } else if (producer_slot(warp) >= 0) {
-        // ---------------- producers: warp producer_warp(s) owns stage s and
-        // arrives on the barrier of its stage's group
-        const int slot = producer_slot(warp);
+        // ---------------- producers: warp producer_warp(P s + h) fills rows
+        // [h 128/P, (h + 1) 128/P) of stage s and arrives on the barrier of the
+        // stage's group; part h = 0 also brings the stage's weight tile
+        const int slot = producer_slot(warp) / P, part = producer_slot(warp) % P;
         uint64_t* gfull = &full[slot / G];
         const uint32_t a_smem = smem_base + slot * Cfg::kStage;
         const uint32_t b_smem = a_smem + kStageA;
@@ -323,9 +331,11 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
         uint32_t f = 0;
         int64_t last = -1;   // last fill this warp issued
         bool stop = false;
-        // lane group g (8 lanes) gathers rows 32g .. 32g + 31, one 16-byte
-        // chunk per lane, so each instruction reads four whole 128-byte rows
+        // lane group g (8 lanes) gathers RG consecutive rows of this warp's part,
+        // one 16-byte chunk per lane, so each instruction reads four whole 128-byte rows
+        constexpr int RG = BM / P / 4;
         const int grp = lane >> 3, chunk = lane & 7;
+        const int row0 = part * (BM / P) + grp * RG;   // a multiple of 8: the swizzle phase of row0 + i is i & 7
         for (int L = 0; !stop; ++L) {
             const int b = L & 1;
             if (!warp_wait(&idx_full[b], (L >> 1) & 1)) {
@@ -342,11 +352,11 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                 uni &= uni - 1;
                 for (int kc = 0; kc < p.k_chunks; ++kc, ++f) {
                     if (static_cast<int>(f % S) != slot) continue;
-                    // all 32 source rows of this lane group, read before any copy is issued
-                    int32_t sr[32];
-                    const int4* gsrc = reinterpret_cast<const int4*>(gidx + j * BM + 32 * grp);
+                    // all RG source rows of this lane group, read before any copy is issued
+                    int32_t sr[RG];
+                    const int4* gsrc = reinterpret_cast<const int4*>(gidx + j * BM + row0);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int q = 0; q < RG / 4; ++q) {
                         const int4 v4 = gsrc[q];
                         sr[4 * q] = v4.x;
                         sr[4 * q + 1] = v4.y;
@@ -360,19 +370,23 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                         break;
                     }
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(gfull, b_bytes);
-                        const uint8_t* src = p.wpack + (static_cast<int64_t>(nb * kTaps + k) * p.k_chunks + kc) * b_bytes;
-                        ptx::bulk_copy_g2s(b_smem, src, b_bytes, gfull);
+                        if (part == 0) {
+                            ptx::mbar_arrive_expect_tx(gfull, b_bytes);
+                            const uint8_t* src =
+                                p.wpack + (static_cast<int64_t>(nb * kTaps + k) * p.k_chunks + kc) * b_bytes;
+                            ptx::bulk_copy_g2s(b_smem, src, b_bytes, gfull);
+                        } else {
+                            ptx::mbar_arrive(gfull);
+                        }
                     }
                     const int kcol = kc * BK + chunk * 8;
                     const bool col_ok = kcol < p.c_in;
                     const __nv_bfloat16* fcol = p.feats + kcol;
-                    const uint32_t dst0 = a_smem + static_cast<uint32_t>(32 * grp) * 128;
+                    const uint32_t dst0 = a_smem + static_cast<uint32_t>(row0) * 128;
                     bool bad = false;   // a row index past n: skipped, reported below
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                    for (int i = 0; i < RG; ++i) {
                         const int32_t src_row = sr[i];
-                        // row 32g + i; its swizzle phase is i & 7 since 32g is a multiple of 8
                         const uint32_t dst = dst0 + i * 128 + ((chunk ^ (i & 7)) << 4);
                         if (src_row >= 0 && src_row < p.n && col_ok)
                             ptx::cp_async_16(dst, fcol + static_cast<int64_t>(src_row) * p.c_in, 16u);
