@@ -199,7 +199,7 @@ def run_ours(args, rank, world, device):
         return y
 
     def step():
-        m = sc.build_map(coords, wl.spatial_shape, wl.batch_size, gemm=args.gemm)
+        m = sc.build_map(coords, wl.spatial_shape, wl.batch_size, gemm=args.gemm, pipeline=args.pipeline)
         launches[0] += sc.last_launch_count()
         mark()
         y = layers(m, feats)
@@ -207,7 +207,7 @@ def run_ours(args, rank, world, device):
         return y
 
     # map statistics (one synchronising call, outside any timing)
-    m0 = sc.build_map(coords, wl.spatial_shape, wl.batch_size, gemm=args.gemm)
+    m0 = sc.build_map(coords, wl.spatial_shape, wl.batch_size, gemm=args.gemm, pipeline=args.pipeline)
     if sc.map_status(m0) != 0:
         raise RuntimeError("map build reported " + sc.status_string(sc.map_status(m0)))
     info = sc.map_info(m0)
@@ -266,7 +266,7 @@ def run_ours(args, rank, world, device):
     clocks = sampler.summary(t0, t1) if sampler else None
 
     map_launches = None
-    m1 = sc.build_map(coords, wl.spatial_shape, wl.batch_size)
+    m1 = sc.build_map(coords, wl.spatial_shape, wl.batch_size, pipeline=args.pipeline)
     map_launches = sc.last_launch_count()
     m1.destroy()
 
@@ -280,7 +280,7 @@ def run_ours(args, rank, world, device):
     def e2e_step():
         coords_d2.copy_(coords_h, non_blocking=True)
         feats_d2.copy_(feats_h, non_blocking=True)
-        m = sc.build_map(coords_d2, wl.spatial_shape, wl.batch_size, gemm=args.gemm)
+        m = sc.build_map(coords_d2, wl.spatial_shape, wl.batch_size, gemm=args.gemm, pipeline=args.pipeline)
         y = layers(m, feats_d2)
         out_h.copy_(y, non_blocking=True)
         m.destroy()
@@ -315,7 +315,7 @@ def run_ours(args, rank, world, device):
         "dtype": "bf16", "data": DATA,
         "config": {"workload": f"{args.workload}: N={wl.n}, C_in={wl.c_in}, C_out={wl.c_out}, "
                                f"layers={L}, batch={wl.batch_size}, grid={'x'.join(map(str, wl.spatial_shape))}",
-                   "pairs": P, "pairs_per_row": round(P / n, 3), "mapper": info["mapper"], "gemm": info["gemm"],
+                   "pairs": P, "pairs_per_row": round(P / n, 3), "mapper": info["mapper"], "pipeline": info["pipeline"], "gemm": info["gemm"],
                    "tile_taps": info["tile_taps"], "l2": "flushed (256 MB write) before every timed step",
                    "weights": "packed once per layer (outside the step)"},
         "useful_tflops": round(useful_tflops, 3),
@@ -419,6 +419,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="outdoor",
                     choices=["tiny", "outdoor", "deep", "large", "stage"])
+    ap.add_argument("--pipeline", default="auto", choices=["auto", "wide", "fused", "multi"],
+                    help="kernel-map build pipeline (auto: wide when the keys fit it)")
     ap.add_argument("--gemm", default="auto", choices=["auto", "tile_union", "tap_major"],
                     help="work decomposition of the bf16 GEMM")
     ap.add_argument("--cpu-budget", type=float, default=10.0,

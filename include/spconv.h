@@ -66,9 +66,11 @@ typedef enum {
 } spconv_bit_order_t;
 
 typedef enum {
-    SPCONV_PIPELINE_AUTO = 0,  /* single launch when it applies, else one kernel per step        */
+    SPCONV_PIPELINE_AUTO = 0,  /* WIDE when it applies, else FUSED when it applies, else MULTI    */
     SPCONV_PIPELINE_FUSED = 1, /* whole build in one thread-block-cluster launch (n <= 2^20)     */
-    SPCONV_PIPELINE_MULTI = 2  /* one kernel per step (any n)                                     */
+    SPCONV_PIPELINE_MULTI = 2, /* one kernel per step, three per 8-bit sort pass (any n)          */
+    SPCONV_PIPELINE_WIDE = 3   /* one kernel per step on the whole GPU, look-back sort passes     */
+                               /* (n <= 2^26; sorted mapper: coordinate keys of at most 40 bits) */
 } spconv_pipeline_t;
 
 /* Work decomposition of the bf16 tensor-core forward ("Compaction is the
@@ -105,7 +107,7 @@ typedef struct {
     int64_t n_tiles;     /* 128-row tiles of the mask-sorted order                */
     int64_t tile_taps;   /* sum over tiles of the taps in the tile's mask union   */
     int32_t mapper;      /* spconv_mapper_t actually used (DENSE or SORTED)       */
-    int32_t pipeline;    /* spconv_pipeline_t actually used (FUSED or MULTI)      */
+    int32_t pipeline;    /* spconv_pipeline_t actually used (FUSED, MULTI, WIDE)  */
     int32_t key_bits;    /* live bits of the packed coordinate key                */
     int32_t shape[3];    /* spatial shape used                                    */
     int32_t batch_size;  /* batch size used                                       */

@@ -99,7 +99,7 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
         if (opt->bit_order != SPCONV_ORDER_CALIBRATED && opt->bit_order != SPCONV_ORDER_PLAIN)
             return SPCONV_ERR_INVALID_ARG;
         if (opt->dense_max_cells < 0) return SPCONV_ERR_INVALID_ARG;
-        if (opt->pipeline < SPCONV_PIPELINE_AUTO || opt->pipeline > SPCONV_PIPELINE_MULTI) return SPCONV_ERR_INVALID_ARG;
+        if (opt->pipeline < SPCONV_PIPELINE_AUTO || opt->pipeline > SPCONV_PIPELINE_WIDE) return SPCONV_ERR_INVALID_ARG;
         if (opt->gemm < SPCONV_GEMM_AUTO || opt->gemm > SPCONV_GEMM_TAP_MAJOR) return SPCONV_ERR_INVALID_ARG;
     }
     int32_t shape[3] = {1, 1, 1};

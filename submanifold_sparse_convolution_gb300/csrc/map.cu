@@ -504,18 +504,24 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
     h->bit_order = opt ? opt->bit_order : SPCONV_ORDER_CALIBRATED;
     h->gemm = (opt && opt->gemm == SPCONV_GEMM_TAP_MAJOR) ? SPCONV_GEMM_TAP_MAJOR : SPCONV_GEMM_TILE_UNION;
 
-    // ---- pipeline: one cluster launch when the rows fit, else one kernel per step
+    // ---- pipeline: the whole-GPU one when the keys fit it, else one cluster
+    // launch when the rows fit, else the plain one kernel per step
     const int row_bits = std::max(1, bit_length(static_cast<uint64_t>(n > 0 ? n - 1 : 0)));
     const int want = opt ? opt->pipeline : SPCONV_PIPELINE_AUTO;
-    bool fused_ok = n <= kFusedMaxRows && (mapper != SPCONV_MAPPER_SORTED || key_bits + row_bits <= 64);
+    const bool packs = mapper != SPCONV_MAPPER_SORTED || key_bits + row_bits <= 64;
+    const bool wide_ok = n <= kWideMaxRows && packs &&
+                         (mapper != SPCONV_MAPPER_SORTED || wide_key_passes(key_bits) <= kWideKeyPassesMax);
+    bool fused_ok = n <= kFusedMaxRows && packs;
     int cluster = 0;
-    if (fused_ok && want != SPCONV_PIPELINE_MULTI && n > 0) {
+    if (fused_ok && (want == SPCONV_PIPELINE_FUSED || (want == SPCONV_PIPELINE_AUTO && !wide_ok)) && n > 0) {
         cluster = fused_cluster_size(s);
         fused_ok = cluster > 0;
     }
     if (want == SPCONV_PIPELINE_FUSED && !fused_ok) return SPCONV_ERR_UNSUPPORTED;
-    const bool fused = want != SPCONV_PIPELINE_MULTI && fused_ok;
-    h->pipeline = fused ? SPCONV_PIPELINE_FUSED : SPCONV_PIPELINE_MULTI;
+    if (want == SPCONV_PIPELINE_WIDE && !wide_ok) return SPCONV_ERR_UNSUPPORTED;
+    const bool wide = want == SPCONV_PIPELINE_WIDE || (want == SPCONV_PIPELINE_AUTO && wide_ok);
+    const bool fused = !wide && want != SPCONV_PIPELINE_MULTI && fused_ok;
+    h->pipeline = wide ? SPCONV_PIPELINE_WIDE : fused ? SPCONV_PIPELINE_FUSED : SPCONV_PIPELINE_MULTI;
 
     // ---- one arena for everything the map keeps or needs while building
     const int64_t nb = std::max<int64_t>(1, rsort::num_tiles(n));
@@ -533,7 +539,12 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
     add(kTaps * np, 4);                 // gtab
     add(t1, 4); add(t1, 4); add(kTaps * t1, 4); add(kTaps * t1, 4);  // union, order, counts, seg_off
     add(np, 4); add(np, 4);             // perm ping-pong
-    if (fused) {
+    const int64_t parts = std::max<int64_t>(1, (n + kWideKeysPerCta - 1) / kWideKeysPerCta);
+    if (wide) {
+        add(n1, 8); add(n1, 8);         // packed (key, row) ping-pong
+        add((kWideKeyPassesMax + kWideMaskPasses) * kWideBins, 4); add(kWideCounters, 4);
+        add(parts * kWideBins, 8);      // look-back states
+    } else if (fused) {
         add(n1, 8); add(n1, 8);         // packed (key, row) ping-pong
         add(3 * cl * kFusedBins, 4); add(cl * kTaps, 4); add(cl * (kTaps + 1), 4);
     } else {
@@ -568,6 +579,61 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
     h->seg_off = carve<int32_t>(p, kTaps * t1);
     int32_t* perm_a = carve<int32_t>(p, np);
     int32_t* perm_b = carve<int32_t>(p, np);
+
+    if (wide) {
+        WideArgs wa;
+        wa.va = carve<uint64_t>(p, n1);
+        wa.vb = carve<uint64_t>(p, n1);
+        wa.gh = carve<int32_t>(p, (kWideKeyPassesMax + kWideMaskPasses) * kWideBins);
+        wa.tickets = carve<int32_t>(p, kWideCounters);
+        wa.look = carve<uint64_t>(p, parts * kWideBins);
+        wa.grid = mapper == SPCONV_MAPPER_DENSE ? carve<int32_t>(p, static_cast<size_t>(cells)) : nullptr;
+        h->perm = perm_a;
+        if (n == 0) {
+            SPCONV_CHECK_CUDA(cudaMemsetAsync(h->status, 0, 256, s));
+            SPCONV_CHECK_CUDA(cudaMemsetAsync(h->tap_off, 0, 256, s));
+            SPCONV_CHECK_CUDA(cudaMemsetAsync(h->totals, 0, 256, s));
+            return cuda_status(cudaGetLastError());
+        }
+        wa.coords = reinterpret_cast<const int4*>(coords);
+        wa.n = n;
+        wa.shape = make_int3(X, Y, Z);
+        wa.batch = B;
+        wa.mapper = mapper;
+        wa.calibrated = h->bit_order == SPCONV_ORDER_CALIBRATED;
+        wa.wz = lay.wz;
+        wa.wy = lay.wy;
+        wa.wx = lay.wx;
+        wa.key_bits = key_bits;
+        wa.row_bits = row_bits;
+        for (int k = 0; k < kTaps; ++k) wa.koff[k] = lay.off[k];
+        wa.gsy = Z + 2;
+        wa.gsx = static_cast<int64_t>(Y + 2) * (Z + 2);
+        wa.gsb = static_cast<int64_t>(X + 2) * wa.gsx;
+        wa.cells = cells;
+        for (int dx = -1; dx <= 1; ++dx)
+            for (int dy = -1; dy <= 1; ++dy)
+                for (int dz = -1; dz <= 1; ++dz)
+                    wa.goff[9 * (dx + 1) + 3 * (dy + 1) + (dz + 1)] = dx * wa.gsx + dy * wa.gsy + dz;
+        wa.nbr = h->nbr;
+        wa.mask = h->mask;
+        wa.tap_count = h->tap_count;
+        wa.perm = h->perm;
+        wa.tap_off = h->tap_off;
+        wa.totals = h->totals;
+        wa.in_rows = h->in_rows;
+        wa.out_rows = h->out_rows;
+        wa.gtab = h->gtab;
+        wa.tile_union = h->tile_union;
+        wa.tile_order = h->tile_order;
+        wa.seg_off = h->seg_off;
+        wa.status = h->status;
+        wa.n_tiles = T;
+        wa.n_pad = h->n_pad;
+        int sms = 0;
+        SPCONV_CHECK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device));
+        return launch_map_wide(wa, sms, s);
+    }
 
     if (fused) {
         FusedArgs fa;

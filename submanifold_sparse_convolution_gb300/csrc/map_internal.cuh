@@ -57,4 +57,63 @@ struct FusedArgs {
 int fused_cluster_size(cudaStream_t s);
 int launch_map_fused(const FusedArgs& a, int cluster, cudaStream_t s);
 
+// ---- whole-GPU pipeline (map_wide.cu) --------------------------------------
+constexpr int kWideKeysPerCta = 1024;    // keys per CTA (look-back partition) of a sort pass
+constexpr int kWideBins = 1024;          // histogram width: digits of up to 10 bits
+constexpr int kDigitBitsWide = 10;
+constexpr int kWideKeyPassesMax = 4;     // coordinate keys of up to 40 bits
+constexpr int kWideMaskPasses = 3;       // 27-bit mask keys, 9-bit digits
+constexpr int kWideTickets = kWideKeyPassesMax + kWideMaskPasses;   // one per sort pass
+constexpr int kWideBarrierInts = 33;                // a grid barrier: 32 arrival counters + a release counter
+// the tickets, then a grid barrier per sort pass
+constexpr int kWideCounters = kWideTickets + kWideTickets * kWideBarrierInts;
+constexpr int64_t kWideMaxRows = int64_t(1) << 26;
+
+struct WideArgs {
+    const int4* coords;
+    int64_t n;
+    int3 shape;
+    int batch;
+    int mapper;
+    int calibrated;
+    int wz, wy, wx, key_bits, row_bits;   // as in FusedArgs
+    uint64_t koff[kTaps];
+    int64_t gsb, gsx, gsy, cells;         // dense grid layout
+    int64_t goff[kTaps];
+    int32_t* grid;
+    // scratch
+    uint64_t* va;          // [n] packed (key << row_bits | row), ping-pong
+    uint64_t* vb;          // [n]
+    int32_t* gh;           // [kWideKeyPassesMax + kWideMaskPasses][kWideBins] digit totals
+    int32_t* tickets;      // [kWideCounters]
+    uint64_t* look;        // [ceil(n / kWideKeysPerCta)][kWideBins] look-back states (or counts) of a sort pass
+    // outputs (see MapHandle)
+    int32_t* nbr;
+    uint32_t* mask;
+    int32_t* tap_count;
+    int32_t* perm;
+    int32_t* tap_off;
+    int32_t* totals;
+    int32_t* in_rows;
+    int32_t* out_rows;
+    int32_t* gtab;
+    uint32_t* tile_union;
+    int32_t* tile_order;
+    int32_t* seg_off;
+    int32_t* status;
+    int64_t n_tiles, n_pad;
+};
+
+// Coordinate sort passes the whole-GPU pipeline takes for a key width.
+int wide_key_passes(int key_bits);
+// The whole build on stream s; sms = multiprocessors of the device.
+int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s);
+
+// Neighbour search (map_search.cu) over sv, the n packed values (key <<
+// row_bits | row) in ascending order: writes nbr (original row order), mask
+// and adds the per-tap counts to tap_count.  Launched with programmatic
+// dependent launch: it waits for the kernels before it.
+int launch_search_window(const uint64_t* sv, int64_t n, int row_bits, int key_bits, const uint64_t* koff,
+                         int32_t* nbr, uint32_t* mask, int32_t* tap_count, int32_t* status, cudaStream_t s);
+
 }  // namespace spconv

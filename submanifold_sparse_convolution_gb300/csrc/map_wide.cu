@@ -1,0 +1,922 @@
+// The kernel-map build on the whole GPU, one kernel per step.
+//
+// The cluster pipeline (map_fused.cu) runs every sort pass on the 16 SMs of
+// one thread-block cluster; a pass then costs ~8 us at 32k rows and grows
+// with the rows per SM (~40 us at 240k rows).  Here each stable LSD radix
+// pass is one kernel over all SMs, 1024 keys per CTA, with decoupled
+// look-back: a CTA ranks its keys, publishes its per-digit counts, sums the
+// counts of the CTAs before it (stopping at the first that has published its
+// inclusive prefix), publishes its own inclusive prefix and scatters.  The
+// digit totals of every pass come from one histogram kernel that reads the
+// keys once.  Kernels follow each other with programmatic dependent launch.
+//
+// When every partition of a pass is resident at once (up to ~300 CTAs), the
+// look-back is replaced by two grid barriers: partitions publish their
+// counts, each CTA scans a few digits across all partitions, partitions read
+// their prefixes back -- about seven memory round trips whatever the number
+// of partitions, where a look-back chain grows with it.
+//
+// Steps (sorted-key mapper):  pack keys + histograms of all key digits ->
+// key passes -> neighbour search (map_search.cu) -> mask keys + histograms
+// of the mask digits -> mask passes -> per-tile pair counts -> one-CTA scan
+// of the (tap, tile) offsets and the tile order -> pair lists, gather table
+// and row order.  The dense mapper replaces the first three steps by a
+// presence-grid scatter and a 27-lookup pass.  Results are bit-identical to
+// the other pipelines: the same packed keys, the same stable order, the same
+// outputs.  Every kernel lets the next one launch as soon as all of its CTAs
+// run (the next waits for its completion before reading anything).
+//
+// Look-back state words are (epoch << 32 | flag << 30 | count): every launch
+// that publishes states takes a fresh epoch, so a state left by an earlier
+// launch in the same memory never reads as ready and the buffers need no
+// clearing.  A CTA whose grid may not be resident at once takes its
+// partition from a ticket counter, so it only ever waits on CTAs that are
+// already running.  Every wait is bounded in time.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "common.cuh"
+#include "map_internal.cuh"
+#include "ptx_sm100.cuh"
+
+namespace spconv {
+namespace {
+
+constexpr int WT = 256;                        // threads per CTA
+constexpr int WI = kWideKeysPerCta / WT;       // keys per thread in a sort pass
+constexpr int WW = WT / 32;                    // warps per CTA
+constexpr int kBinsPerThread = kWideBins / WT;
+constexpr int kMaskWidth = (kTaps + kWideMaskPasses - 1) / kWideMaskPasses;
+constexpr int kRowsPerThread = 4;              // key and mask-key kernels (loads issued together)
+static_assert(kBinsPerThread * WT == kWideBins, "digit values split evenly over the threads");
+static_assert(WI * WT == kWideKeysPerCta, "keys split evenly over the threads");
+static_assert((1 << kMaskWidth) <= kWideBins, "mask digits fit the histogram");
+
+constexpr uint64_t kAgg = 1ull << 30;      // the partition's own count
+constexpr uint64_t kPre = 2ull << 30;      // the inclusive prefix up to and including the partition
+constexpr uint64_t kFlags = 3ull << 30;
+constexpr uint64_t kCount = (1ull << 30) - 1;
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t state(uint32_t epoch, uint64_t flag, int32_t count) {
+    return (static_cast<uint64_t>(epoch) << 32) | flag | (static_cast<uint64_t>(count) & kCount);
+}
+
+// Decoupled look-back for Q counters of partition c at once: ex[i] = sum of
+// counter q[i] over partitions [0, c).  States are look[part * stride + q].
+// Each step loads the states of the W partitions below the current one for
+// every counter (Q * W independent loads in flight), adds them from the
+// nearest down to the first inclusive prefix, and continues below the window
+// only if all W were aggregates; a state not yet published ends the step
+// early and is read again.  Partitions all publish their aggregates at about
+// the same time, so a CTA reaches an inclusive prefix in about c / W steps at
+// worst instead of c.  A predecessor that does not publish within the wait
+// limit records a timeout and the chain stops (the result is then wrong but
+// the kernel ends).
+template <int Q, int W>
+__device__ void look_back(const uint64_t* look, int64_t stride, int64_t c, const int (&q)[Q], const bool (&act)[Q],
+                          uint32_t epoch, int32_t (&ex)[Q], int32_t* status) {
+    int64_t j[Q];   // next partition to read, per counter (-1: done)
+    bool all = true;
+#pragma unroll
+    for (int i = 0; i < Q; ++i) {
+        ex[i] = 0;
+        j[i] = (act[i] && c > 0) ? c - 1 : -1;
+        all &= j[i] < 0;
+    }
+    if (all) return;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint64_t v[Q][W];
+#pragma unroll
+        for (int i = 0; i < Q; ++i)
+#pragma unroll
+            for (int k = 0; k < W; ++k)
+                v[i][k] = (j[i] - k >= 0) ? ld_relaxed(look + (j[i] - k) * stride + q[i]) : 0ull;
+        all = true;
+#pragma unroll
+        for (int i = 0; i < Q; ++i) {
+            bool go = j[i] >= 0;
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                if (!go || j[i] < 0) break;
+                const uint64_t x = v[i][k];
+                if ((x >> 32) != epoch || (x & kFlags) == 0) {
+                    go = false;   // not published yet: read again from here
+                    break;
+                }
+                ex[i] += static_cast<int32_t>(x & kCount);
+                j[i] = (x & kFlags) == kPre ? -1 : j[i] - 1;
+            }
+            all &= j[i] < 0;
+        }
+        if (all) return;
+        if (it == 0) t0 = ptx::globaltimer();
+        if ((it & 15u) == 15u && ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+            atomicOr(status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+// Exclusive scan over the threads of the CTA (all WT threads call).
+__device__ __forceinline__ int32_t block_exclusive(int32_t x, int32_t* wsum) {
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    int32_t incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    int32_t before = 0;
+#pragma unroll
+    for (int i = 0; i < WW; ++i) before += i < w ? wsum[i] : 0;
+    __syncthreads();
+    return before + incl - x;
+}
+
+// Barrier over all P CTAs of the grid (every CTA must be resident), for the
+// round-th time (0, 1, ...).  bar: kWideBarrierInts counters, zero before
+// round 0.  CTA c arrives at counter c % 32; the arrival that completes a
+// counter's share of the round bumps the release counter, which every CTA
+// polls (with a short sleep between polls) until all used counters have
+// completed the round.  Arrivals spread over 32 addresses instead of one.
+// Bounded in time.
+__device__ void grid_barrier(int32_t* bar, int64_t P, int round, int32_t* status) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int nsub = P < 32 ? static_cast<int>(P) : 32;
+        const int j = static_cast<int>(blockIdx.x % 32);
+        const int share = static_cast<int>(P / 32 + (j < P % 32 ? 1 : 0));
+        __threadfence();
+        const int old = atomicAdd(bar + j, 1);
+        if ((old + 1) % share == 0) {
+            __threadfence();
+            atomicAdd(bar + 32, 1);
+        }
+        const int32_t target = (round + 1) * nsub;
+        uint64_t t0 = 0;
+        for (uint32_t it = 0;; ++it) {
+            int32_t v;
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(bar + 32) : "memory");
+            if (v >= target) break;
+            if (it == 0) t0 = ptx::globaltimer();
+            __nanosleep(32);
+            if ((it & 63u) == 63u && ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+                atomicOr(status, kStatusTimeout);
+                break;
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ bool coord_ok(int4 q, int3 shape, int batch) {
+    return q.x >= 0 && q.x < batch && q.y >= 0 && q.y < shape.x && q.z >= 0 && q.z < shape.y && q.w >= 0 &&
+           q.w < shape.z;
+}
+
+// First kernel of a build: clears the status word, every digit histogram,
+// the tickets and barrier counters, the tap counts and totals, and (dense
+// mapper) the presence grid to -1.  The kernel after it overlaps it and waits
+// for it only before its first write to any of these.
+__global__ void __launch_bounds__(WT) k_wide_clear(const WideArgs a) {
+    pdl_trigger();
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * WT + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * WT;
+    if (i0 == 0) *a.status = 0;
+    for (int64_t i = i0; i < (kWideKeyPassesMax + kWideMaskPasses) * kWideBins; i += stride) a.gh[i] = 0;
+    for (int64_t i = i0; i < kWideCounters; i += stride) a.tickets[i] = 0;
+    if (i0 < kTaps) a.tap_count[i0] = 0;
+    if (i0 < 2) a.totals[i0] = 0;
+    if (a.mapper == SPCONV_MAPPER_DENSE) {
+        int4* g4 = reinterpret_cast<int4*>(a.grid);
+        const int64_t c4 = a.cells / 4;
+        for (int64_t i = i0; i < c4; i += stride) g4[i] = make_int4(-1, -1, -1, -1);
+        for (int64_t i = 4 * c4 + i0; i < a.cells; i += stride) a.grid[i] = -1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// sorted-key mapper: packed keys and the digit counts of every key pass
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(WT) k_wide_keys(const WideArgs a, int passes, int width) {
+    __shared__ int32_t h[kWideKeyPassesMax][kWideBins];
+    const int t = threadIdx.x, lane = t & 31;
+    const int bins = 1 << width;
+    pdl_trigger();
+    for (int i = t; i < kWideKeyPassesMax * kWideBins; i += WT) (&h[0][0])[i] = 0;
+    __syncthreads();
+    const int rb = a.row_bits;
+    const uint64_t invalid = (uint64_t(1) << a.key_bits) - 1;
+    const uint64_t dmask = static_cast<uint64_t>(bins - 1);
+    int32_t err = 0;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * WT * kRowsPerThread + t;
+    int4 qs[kRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) {
+        const int64_t i = row0 + r * WT;
+        qs[r] = i < a.n ? a.coords[i] : make_int4(-1, -1, -1, -1);
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) {
+        const int64_t i = row0 + r * WT;
+        const bool valid = i < a.n;
+        uint64_t key = invalid;
+        if (valid) {
+            const int4 q = qs[r];
+            if (coord_ok(q, a.shape, a.batch)) {
+                key = (((((static_cast<uint64_t>(q.x) << a.wx) | static_cast<uint64_t>(q.y + 1)) << a.wy) |
+                        static_cast<uint64_t>(q.z + 1))
+                       << a.wz) |
+                      static_cast<uint64_t>(q.w + 1);
+            } else {
+                err |= kStatusRange;
+            }
+            a.va[i] = (key << rb) | static_cast<uint64_t>(i);
+        }
+        for (int p = 0; p < passes; ++p) {
+            const int dg = valid ? static_cast<int>((key >> (width * p)) & dmask) : kWideBins;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dg);
+            if (valid && lane == __ffs(peers) - 1) atomicAdd(&h[p][dg], __popc(peers));
+        }
+    }
+    __syncthreads();
+    pdl_wait();   // the histograms and the status word are cleared
+    for (int i = t; i < passes * bins; i += WT) {
+        const int p = i / bins, b = i % bins;
+        const int32_t x = h[p][b];
+        if (x) atomicAdd(a.gh + p * kWideBins + b, x);
+    }
+    if (err) atomicOr(a.status, err);
+}
+
+// ---------------------------------------------------------------------------
+// dense mapper: presence grid (cleared to -1 before), then 27 lookups per row
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(WT) k_wide_grid_scatter(const WideArgs a) {
+    pdl_trigger();
+    pdl_wait();   // the grid is cleared
+    int32_t err = 0;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * WT + threadIdx.x; i < a.n;
+         i += static_cast<int64_t>(gridDim.x) * WT) {
+        const int4 q = a.coords[i];
+        if (coord_ok(q, a.shape, a.batch)) {
+            const int64_t cell = q.x * a.gsb + static_cast<int64_t>(q.y + 1) * a.gsx +
+                                 static_cast<int64_t>(q.z + 1) * a.gsy + (q.w + 1);
+            if (atomicCAS(a.grid + cell, -1, static_cast<int32_t>(i)) != -1) err |= kStatusDuplicate;
+        } else {
+            err |= kStatusRange;
+        }
+    }
+    if (err) atomicOr(a.status, err);
+}
+
+__global__ void __launch_bounds__(WT) k_wide_grid_lookup(const WideArgs a) {
+    __shared__ int32_t cnt[kTaps];
+    const int t = threadIdx.x, lane = t & 31;
+    if (t < kTaps) cnt[t] = 0;
+    __syncthreads();
+    pdl_wait();   // the grid scatter has finished
+    pdl_trigger();
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * WT; i0 < a.n; i0 += static_cast<int64_t>(gridDim.x) * WT) {
+        const int64_t i = i0 + t;
+        uint32_t m = 0;
+        if (i < a.n) {
+            const int4 q = a.coords[i];
+            int32_t v[kNbrStride];
+#pragma unroll
+            for (int k = 0; k < kNbrStride; ++k) v[k] = -1;
+            if (coord_ok(q, a.shape, a.batch)) {
+                const int64_t cell = q.x * a.gsb + static_cast<int64_t>(q.y + 1) * a.gsx +
+                                     static_cast<int64_t>(q.z + 1) * a.gsy + (q.w + 1);
+#pragma unroll
+                for (int k = 0; k < kTaps; ++k) {
+                    v[k] = __ldcg(a.grid + cell + a.goff[k]);
+                    m |= (v[k] >= 0 ? 1u : 0u) << k;
+                }
+            }
+            int4* dst = reinterpret_cast<int4*>(a.nbr + i * kNbrStride);
+#pragma unroll
+            for (int qq = 0; qq < kNbrStride / 4; ++qq)
+                dst[qq] = make_int4(v[4 * qq], v[4 * qq + 1], v[4 * qq + 2], v[4 * qq + 3]);
+            a.mask[i] = m;
+        }
+#pragma unroll
+        for (int k = 0; k < kTaps; ++k) {
+            const uint32_t b = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
+            if (lane == 0 && b) atomicAdd(&cnt[k], __popc(b));
+        }
+    }
+    __syncthreads();
+    if (t < kTaps && cnt[t]) atomicAdd(a.tap_count + t, cnt[t]);
+}
+
+// ---------------------------------------------------------------------------
+// mask sort keys: the mask's bits in the tap order (rarest tap in the top bit
+// with the calibrated order), packed with the row; digit counts of the passes
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(WT) k_wide_mask_keys(const WideArgs a) {
+    __shared__ int32_t h[kWideMaskPasses][1 << kMaskWidth];
+    __shared__ int32_t taps[kTaps];
+    __shared__ int32_t pos[kTaps];
+    const int t = threadIdx.x, lane = t & 31;
+    constexpr int bins = 1 << kMaskWidth;
+    for (int i = t; i < kWideMaskPasses * bins; i += WT) (&h[0][0])[i] = 0;
+    pdl_wait();   // masks and tap counts are complete
+    pdl_trigger();
+    if (t < kTaps) taps[t] = __ldcg(a.tap_count + t);
+    __syncthreads();
+    if (t < kTaps) {
+        int32_t rank = t;
+        if (a.calibrated) {
+            const int32_t ck = taps[t];
+            rank = 0;
+            for (int j = 0; j < kTaps; ++j) {
+                const int32_t cj = taps[j];
+                rank += (cj > ck || (cj == ck && j < t)) ? 1 : 0;
+            }
+        }
+        pos[t] = rank;
+    }
+    __syncthreads();
+    const int rb = a.row_bits;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * WT * kRowsPerThread + t;
+    uint32_t ms[kRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) {
+        const int64_t i = row0 + r * WT;
+        ms[r] = i < a.n ? __ldcg(a.mask + i) : 0u;
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) {
+        const int64_t i = row0 + r * WT;
+        const bool valid = i < a.n;
+        uint32_t key = 0;
+        if (valid) {
+            const uint32_t m = ms[r];
+#pragma unroll
+            for (int k = 0; k < kTaps; ++k) key |= ((m >> k) & 1u) << pos[k];
+            a.va[i] = (static_cast<uint64_t>(key) << rb) | static_cast<uint64_t>(i);
+        }
+#pragma unroll
+        for (int p = 0; p < kWideMaskPasses; ++p) {
+            const int dg = valid ? static_cast<int>((key >> (kMaskWidth * p)) & (bins - 1)) : kWideBins;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dg);
+            if (valid && lane == __ffs(peers) - 1) atomicAdd(&h[p][dg], __popc(peers));
+        }
+    }
+    __syncthreads();
+    for (int i = t; i < kWideMaskPasses * bins; i += WT) {
+        const int p = i / bins, b = i % bins;
+        const int32_t x = h[p][b];
+        if (x) atomicAdd(a.gh + (kWideKeyPassesMax + p) * kWideBins + b, x);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// one stable LSD pass by the digit of `width` bits at bit `shift` of the
+// packed values
+// ---------------------------------------------------------------------------
+struct PassArgs {
+    const uint64_t* in;
+    uint64_t* out;
+    int64_t n;
+    int shift, width;
+    const int32_t* gh;     // [kWideBins] digit totals of this pass
+    uint64_t* look;        // [partitions][kWideBins] look-back states
+    uint32_t epoch;
+    int32_t* ticket;       // partition counter, or null: partition = blockIdx.x (the whole grid is resident)
+    int32_t* bar;          // non-null: prefixes by two grid barriers instead of look-back (see below)
+    int32_t* status;
+};
+
+// Partitions a CTA scans per digit in the barrier form (consecutive, one lane
+// each group), and digits a warp scans at once.
+constexpr int kScanPerLane = 8;
+constexpr int kScanDigitsPerWarp = 4;
+
+__global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
+    // cnt[w][d]: keys of warp w with digit d, then the warp's offset within
+    // the CTA's keys of digit d (stable order inside the CTA: warp, item, lane)
+    __shared__ uint16_t cnt[WW][kWideBins];
+    __shared__ int32_t gbase[kWideBins];   // first output position of each digit
+    __shared__ int32_t excl[kWideBins];    // keys of each digit in the partitions before this one
+    __shared__ int32_t wsum[WW];
+    __shared__ int32_t part_sh, err;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int bins = 1 << a.width;
+    const uint64_t dmask = static_cast<uint64_t>(bins - 1);
+    uint32_t* cz = reinterpret_cast<uint32_t*>(&cnt[0][0]);
+    for (int i = t; i < WW * kWideBins / 2; i += WT) cz[i] = 0;
+    if (t == 0) err = 0;
+    pdl_wait();   // the keys and the digit totals are complete
+    pdl_trigger();
+    int64_t c = blockIdx.x;
+    if (a.ticket) {
+        if (t == 0) part_sh = atomicAdd(a.ticket, 1);
+        __syncthreads();
+        c = part_sh;
+    }
+    // this partition's keys (requested first: their latency overlaps the scan below)
+    const int64_t base = c * kWideKeysPerCta;
+    uint64_t v[WI];
+    int d[WI], rk[WI];
+#pragma unroll
+    for (int j = 0; j < WI; ++j) {
+        const int64_t idx = base + static_cast<int64_t>(w) * 32 * WI + 32 * j + lane;
+        v[j] = idx < a.n ? __ldcg(a.in + idx) : 0ull;
+    }
+    // digit totals -> first output position of every digit (thread t: digits 4t .. 4t+3)
+    int32_t g[kBinsPerThread];
+    int32_t gs = 0;
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) {
+        const int d = kBinsPerThread * t + q;
+        g[q] = d < bins ? __ldcg(a.gh + d) : 0;
+        gs += g[q];
+    }
+    int32_t run = block_exclusive(gs, wsum);   // (synchronises the CTA: cnt is cleared after it)
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) {
+        gbase[kBinsPerThread * t + q] = run;
+        run += g[q];
+    }
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int j = 0; j < WI; ++j) {
+        const int64_t idx = base + static_cast<int64_t>(w) * 32 * WI + 32 * j + lane;
+        d[j] = idx < a.n ? static_cast<int>((v[j] >> a.shift) & dmask) : kWideBins;
+    }
+#pragma unroll
+    for (int j = 0; j < WI; ++j) {
+        const bool valid = d[j] < kWideBins;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d[j]);
+        const int prior = valid ? cnt[w][d[j]] : 0;
+        rk[j] = prior + __popc(peers & lt);
+        __syncwarp();
+        if (valid && lane == __ffs(peers) - 1) cnt[w][d[j]] = static_cast<uint16_t>(prior + __popc(peers));
+        __syncwarp();
+    }
+    __syncthreads();
+    // per digit (thread t: digits t, t + WT, ...): offsets of the warps, the
+    // CTA's count, published as this partition's aggregate
+    int qd[kBinsPerThread];
+    bool act[kBinsPerThread];
+    int32_t tot[kBinsPerThread];
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q) {
+        const int dd = t + q * WT;
+        qd[q] = dd;
+        act[q] = dd < bins;
+        int32_t x[WW];
+#pragma unroll
+        for (int ww = 0; ww < WW; ++ww) x[ww] = act[q] ? cnt[ww][dd] : 0;
+        int32_t pre = 0;
+#pragma unroll
+        for (int ww = 0; ww < WW; ++ww) {
+            if (act[q]) cnt[ww][dd] = static_cast<uint16_t>(pre);
+            pre += x[ww];
+        }
+        tot[q] = pre;
+    }
+    int32_t ex[kBinsPerThread];
+    if (a.bar != nullptr) {
+        // Every partition is resident.  Counts go to pc[digit][partition];
+        // after a grid barrier each CTA turns the rows of its own few digits
+        // into exclusive prefixes over the partitions (a warp per digit, lane
+        // l holding partitions [l K, l K + K)), and after a second barrier
+        // each partition reads its prefix of every digit.  About seven
+        // dependent memory round trips, whatever the number of partitions.
+        const int64_t P = gridDim.x;
+        int32_t* pc = reinterpret_cast<int32_t*>(a.look);
+#pragma unroll
+        for (int q = 0; q < kBinsPerThread; ++q)
+            if (act[q]) pc[qd[q] * P + c] = tot[q];
+        grid_barrier(a.bar, P, 0, a.status);
+        const int per = static_cast<int>((bins + P - 1) / P);       // digits of this CTA
+        const int K = static_cast<int>((P + 31) / 32);              // partitions per lane (<= kScanPerLane)
+        const int d0 = static_cast<int>(c) * per;
+        const int d1 = d0 + per < bins ? d0 + per : bins;
+        int32_t x[kScanDigitsPerWarp][kScanPerLane];
+#pragma unroll
+        for (int i = 0; i < kScanDigitsPerWarp; ++i) {
+            const int dd = d0 + w + WW * i;
+#pragma unroll
+            for (int k = 0; k < kScanPerLane; ++k) {
+                const int64_t j = static_cast<int64_t>(lane) * K + k;
+                x[i][k] = (dd < d1 && k < K && j < P) ? __ldcg(pc + dd * P + j) : 0;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kScanDigitsPerWarp; ++i) {
+            const int dd = d0 + w + WW * i;
+            int32_t sum = 0;
+#pragma unroll
+            for (int k = 0; k < kScanPerLane; ++k) sum += x[i][k];
+            int32_t inc = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            int32_t run = inc - sum;
+#pragma unroll
+            for (int k = 0; k < kScanPerLane; ++k) {
+                const int64_t j = static_cast<int64_t>(lane) * K + k;
+                if (dd < d1 && k < K && j < P) pc[dd * P + j] = run;
+                run += x[i][k];
+            }
+        }
+        grid_barrier(a.bar, P, 1, a.status);
+#pragma unroll
+        for (int q = 0; q < kBinsPerThread; ++q) ex[q] = act[q] ? __ldcg(pc + qd[q] * P + c) : 0;
+    } else {
+#pragma unroll
+        for (int q = 0; q < kBinsPerThread; ++q)
+            if (act[q]) st_relaxed(a.look + c * kWideBins + qd[q], state(a.epoch, c == 0 ? kPre : kAgg, tot[q]));
+        look_back<kBinsPerThread, 8>(a.look, kWideBins, c, qd, act, a.epoch, ex, a.status);
+#pragma unroll
+        for (int q = 0; q < kBinsPerThread; ++q)
+            if (act[q] && c > 0) st_relaxed(a.look + c * kWideBins + qd[q], state(a.epoch, kPre, ex[q] + tot[q]));
+    }
+#pragma unroll
+    for (int q = 0; q < kBinsPerThread; ++q)
+        if (act[q]) excl[qd[q]] = ex[q];
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < WI; ++j) {
+        if (d[j] >= kWideBins) continue;
+        const int64_t dst = static_cast<int64_t>(gbase[d[j]]) + excl[d[j]] + cnt[w][d[j]] + rk[j];
+        if (dst >= 0 && dst < a.n)
+            a.out[dst] = v[j];
+        else
+            atomicOr(&err, kStatusInternal);
+    }
+    __syncthreads();
+    if (t == 0 && err) atomicOr(a.status, err);
+}
+
+// ---------------------------------------------------------------------------
+// per 128-row tile of the mask-sorted order: pair counts per tap (into
+// seg_off, tap-major [27][T]) and the union of the tile's masks
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kTileRows) k_wide_tile_count(const WideArgs a, const uint64_t* __restrict__ ms) {
+    __shared__ int32_t wc[kTileRows / 32][kTaps];
+    __shared__ int32_t err;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int64_t T = a.n_tiles, n = a.n;
+    const int64_t tile = blockIdx.x;
+    const uint64_t rmask = (uint64_t(1) << a.row_bits) - 1;
+    if (t == 0) err = 0;
+    pdl_wait();   // the mask sort is complete
+    pdl_trigger();
+    const int64_t s = tile * kTileRows + t;
+    int64_t r = s < n ? static_cast<int64_t>(__ldcg(ms + s) & rmask) : -1;
+    if (r >= n) {
+        atomicOr(&err, kStatusInternal);
+        r = -1;
+    }
+    const uint32_t m = r >= 0 ? __ldcg(a.mask + r) : 0u;
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) {
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
+        if (lane == 0) wc[warp][k] = __popc(b);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int32_t x = 0;
+        if (lane < kTaps) {
+#pragma unroll
+            for (int q = 0; q < kTileRows / 32; ++q) x += wc[q][lane];
+            a.seg_off[static_cast<int64_t>(lane) * T + tile] = x;
+        }
+        const uint32_t uni = __ballot_sync(0xFFFFFFFFu, x > 0);
+        if (lane == 0) a.tile_union[tile] = uni;
+    }
+    if (t == 0 && err) atomicOr(a.status, err);
+}
+
+// One CTA: the exclusive scan of the (tap, tile) counts in tap-major order
+// (each tap's list starts where the previous tap's ends) in place, the tap
+// offsets and totals, and the tiles in descending order of union size,
+// stable in the tile index (a counting sort over the 28 sizes: warp w takes
+// a contiguous range of tiles, 32 at a time).
+constexpr int kScanThreads = 1024;
+constexpr int kScanWarps = kScanThreads / 32;
+constexpr int kScanPer = 8;                          // values per thread and round
+constexpr int kScanRound = kScanThreads * kScanPer;
+
+__global__ void __launch_bounds__(kScanThreads) k_wide_tile_scan(const WideArgs a) {
+    __shared__ int32_t wsum[kScanWarps];
+    __shared__ __align__(16) int32_t buf[kScanRound];
+    __shared__ int32_t wcnt[kScanWarps][kTaps + 1];
+    __shared__ int32_t bbase[kTaps + 1];
+    __shared__ int32_t tap_sum;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int64_t T = a.n_tiles;
+    const int64_t m = kTaps * T;
+    if (t < kScanWarps * (kTaps + 1)) (&wcnt[0][0])[t] = 0;
+    if (t == 0) tap_sum = 0;
+    pdl_wait();   // counts and unions of every tile are complete
+    pdl_trigger();
+    // ---- pair offsets, in rounds of kScanRound values: coalesced loads into
+    // shared memory, each thread scans kScanPer consecutive values there,
+    // a block scan of the thread sums, coalesced stores
+    int32_t carry = 0;
+    for (int64_t r0 = 0; r0 < m; r0 += kScanRound) {
+#pragma unroll
+        for (int k = 0; k < kScanPer; ++k) {
+            const int64_t i = r0 + static_cast<int64_t>(k) * kScanThreads + t;
+            buf[k * kScanThreads + t] = i < m ? __ldcg(a.seg_off + i) : 0;
+        }
+        __syncthreads();
+        int4 v[kScanPer / 4];
+#pragma unroll
+        for (int k = 0; k < kScanPer / 4; ++k) v[k] = reinterpret_cast<const int4*>(buf)[t * (kScanPer / 4) + k];
+        int32_t sum = 0;
+#pragma unroll
+        for (int k = 0; k < kScanPer / 4; ++k) sum += v[k].x + v[k].y + v[k].z + v[k].w;
+        int32_t inc = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane == 31) wsum[w] = inc;
+        __syncthreads();
+        int32_t before = 0, total = 0;
+        for (int i = 0; i < kScanWarps; ++i) {
+            const int32_t x = wsum[i];
+            before += i < w ? x : 0;
+            total += x;
+        }
+        int32_t run = carry + before + inc - sum;
+#pragma unroll
+        for (int k = 0; k < kScanPer / 4; ++k) {
+            int4 o4;
+            o4.x = run; run += v[k].x;
+            o4.y = run; run += v[k].y;
+            o4.z = run; run += v[k].z;
+            o4.w = run; run += v[k].w;
+            reinterpret_cast<int4*>(buf)[t * (kScanPer / 4) + k] = o4;
+        }
+        carry += total;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kScanPer; ++k) {
+            const int64_t i = r0 + static_cast<int64_t>(k) * kScanThreads + t;
+            if (i < m) a.seg_off[i] = buf[k * kScanThreads + t];
+        }
+        __syncthreads();   // buf and wsum are reused
+    }
+    if (t < kTaps) a.tap_off[t] = __ldcg(a.seg_off + static_cast<int64_t>(t) * T);   // (block-visible after the barrier)
+    if (t == 0) {
+        a.tap_off[kTaps] = carry;
+        a.totals[0] = carry;
+    }
+    // ---- tile order
+    const int64_t tw = (T + kScanWarps - 1) / kScanWarps;
+    const int64_t t0 = w * tw < T ? w * tw : T;
+    const int64_t t1 = t0 + tw < T ? t0 + tw : T;
+    const uint32_t lt = lanemask_lt();
+    int32_t my_taps = 0;
+    for (int64_t i0 = t0; i0 < t1; i0 += 32) {
+        const int64_t tt = i0 + lane;
+        const int c = tt < t1 ? __popc(__ldcg(a.tile_union + tt)) : -1;
+        const int b = c >= 0 ? kTaps - c : kTaps + 1;
+        my_taps += c > 0 ? c : 0;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, b);
+        if (b <= kTaps && lane == __ffs(peers) - 1) wcnt[w][b] += __popc(peers);
+        __syncwarp();
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) my_taps += __shfl_xor_sync(0xFFFFFFFFu, my_taps, o);
+    if (lane == 0) atomicAdd(&tap_sum, my_taps);
+    __syncthreads();
+    if (t <= kTaps) {   // per size: offsets of the warps, total
+        int32_t r = 0;
+        for (int q = 0; q < kScanWarps; ++q) {
+            const int32_t x = wcnt[q][t];
+            wcnt[q][t] = r;
+            r += x;
+        }
+        bbase[t] = r;
+    }
+    __syncthreads();
+    if (t == 0) {
+        int32_t r = 0;
+        for (int b = 0; b <= kTaps; ++b) {
+            const int32_t x = bbase[b];
+            bbase[b] = r;
+            r += x;
+        }
+        a.totals[1] = tap_sum;
+    }
+    __syncthreads();
+    for (int64_t i0 = t0; i0 < t1; i0 += 32) {
+        const int64_t tt = i0 + lane;
+        const int b = tt < t1 ? kTaps - __popc(__ldcg(a.tile_union + tt)) : kTaps + 1;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, b);
+        if (b <= kTaps) {
+            const int64_t at = static_cast<int64_t>(bbase[b]) + wcnt[w][b] + __popc(peers & lt);
+            if (at >= 0 && at < T) a.tile_order[at] = static_cast<int32_t>(tt);
+        }
+        __syncwarp();
+        if (b <= kTaps && lane == __ffs(peers) - 1) wcnt[w][b] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// One block of 128 threads per tile: perm, the per-tap pair lists (from the
+// (tap, tile) offsets) and the GEMM gather table (only the taps of the
+// tile's union).
+__global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a, const uint64_t* __restrict__ ms) {
+    __shared__ int32_t wc[kTileRows / 32][kTaps];
+    __shared__ int32_t err;
+    const int64_t tile = blockIdx.x;
+    const int64_t T = a.n_tiles, n = a.n;
+    const uint64_t rmask = (uint64_t(1) << a.row_bits) - 1;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) err = 0;
+    pdl_wait();   // the pair offsets are complete
+    pdl_trigger();
+    const int64_t s = tile * kTileRows + threadIdx.x;
+    int32_t r = s < n ? static_cast<int32_t>(__ldcg(ms + s) & rmask) : -1;
+    if (r >= n) {
+        r = -1;
+        atomicOr(&err, kStatusInternal);
+    }
+    const uint32_t m = r >= 0 ? __ldcg(a.mask + r) : 0u;
+    const uint32_t uni = __ldcg(a.tile_union + tile);
+    int32_t v[kNbrStride];
+    if (r >= 0) {
+        const int4* src = reinterpret_cast<const int4*>(a.nbr + static_cast<int64_t>(r) * kNbrStride);
+#pragma unroll
+        for (int q = 0; q < kNbrStride / 4; ++q) {
+            const int4 x = __ldcg(src + q);
+            v[4 * q] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kNbrStride; ++k) v[k] = -1;
+    }
+    uint32_t ball[kTaps];
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) {
+        ball[k] = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
+        if (lane == 0) wc[warp][k] = __popc(ball[k]);
+    }
+    __syncthreads();
+    a.perm[s] = r;
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) {
+        if (!((uni >> k) & 1u)) continue;
+        const bool present = (m >> k) & 1u;
+        if (present) {
+            int64_t off = static_cast<int64_t>(__ldcg(a.seg_off + static_cast<int64_t>(k) * T + tile)) +
+                          __popc(ball[k] & lt);
+            for (int q = 0; q < warp; ++q) off += wc[q][k];
+            if (off >= 0 && off < kTaps * n) {
+                a.in_rows[off] = v[k];
+                a.out_rows[off] = r;
+            } else {
+                atomicOr(&err, kStatusInternal);
+            }
+        }
+        a.gtab[static_cast<int64_t>(k) * a.n_pad + s] = present ? v[k] : -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && err) atomicOr(a.status, err);
+}
+
+// A fresh nonzero epoch for every launch that publishes look-back states.
+uint32_t next_epoch() {
+    static std::atomic<uint32_t> counter{0};
+    uint32_t e = ++counter;
+    if (e == 0) e = ++counter;
+    return e;
+}
+
+// CTAs of `kernel` (block threads, no dynamic shared memory) the device holds at once.
+template <typename Kernel>
+int64_t resident_ctas(Kernel kernel, int block, int sms) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return static_cast<int64_t>(per_sm) * sms;
+}
+
+template <typename Kernel, typename... Args>
+int launch_pdl(Kernel kernel, unsigned grid, unsigned block, cudaStream_t s, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    SPCONV_CHECK_CUDA(cudaLaunchKernelEx(&cfg, kernel, args...));
+    count_launch();
+    return SPCONV_OK;
+}
+
+}  // namespace
+
+int wide_key_passes(int key_bits) { return (key_bits + kDigitBitsWide - 1) / kDigitBitsWide; }
+
+int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
+    const int64_t n = a.n;
+    const unsigned parts = static_cast<unsigned>((n + kWideKeysPerCta - 1) / kWideKeysPerCta);
+    const unsigned key_blocks = static_cast<unsigned>((n + WT * kRowsPerThread - 1) / (WT * kRowsPerThread));
+    const unsigned row_blocks = static_cast<unsigned>((n + WT - 1) / WT);
+    // a look-back kernel numbers its partitions by blockIdx when all of its
+    // CTAs fit on the device at once (each waits only on lower ones), else
+    // takes them from a ticket counter in the order the CTAs start
+    static int64_t cap_pass[kMaxDevices] = {};
+    int dev = 0;
+    SPCONV_CHECK_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return SPCONV_ERR_UNSUPPORTED;
+    if (cap_pass[dev] == 0) {
+        cap_pass[dev] = resident_ctas(k_wide_pass, WT, sms);
+    }
+    const bool pass_ticket = static_cast<int64_t>(parts) > cap_pass[dev];
+    int64_t clear_blocks = a.mapper == SPCONV_MAPPER_DENSE ? (a.cells / 4 + WT * 8 - 1) / (WT * 8) : 8;
+    if (clear_blocks > 4 * sms) clear_blocks = 4 * sms;
+    SPCONV_CHECK(launch_pdl(k_wide_clear, static_cast<unsigned>(clear_blocks < 1 ? 1 : clear_blocks), WT, s, false, a));
+    auto pass = [&](const uint64_t* in, uint64_t* out, int shift, int width, const int32_t* gh, int ticket) {
+        PassArgs pa;
+        pa.in = in;
+        pa.out = out;
+        pa.n = n;
+        pa.shift = shift;
+        pa.width = width;
+        pa.gh = gh;
+        pa.look = a.look;
+        pa.epoch = next_epoch();
+        pa.ticket = pass_ticket ? a.tickets + ticket : nullptr;
+        // the barrier form when every partition is resident, each warp scans at
+        // most kScanDigitsPerWarp digits and each lane at most kScanPerLane partitions
+        const int64_t bins = int64_t(1) << width;
+        // (below ~64 partitions a windowed look-back chain is as short and has no barrier)
+        const bool barrier = !pass_ticket && parts > 64 &&
+                             bins <= static_cast<int64_t>(parts) * WW * kScanDigitsPerWarp &&
+                             static_cast<int64_t>(parts) <= 32 * kScanPerLane;
+        pa.bar = barrier ? a.tickets + kWideTickets + ticket * kWideBarrierInts : nullptr;
+        pa.status = a.status;
+        return launch_pdl(k_wide_pass, parts, WT, s, true, pa);
+    };
+    if (a.mapper == SPCONV_MAPPER_SORTED) {
+        const int passes = wide_key_passes(a.key_bits);
+        const int width = (a.key_bits + passes - 1) / passes;
+        if (passes > kWideKeyPassesMax) return SPCONV_ERR_UNSUPPORTED;
+        SPCONV_CHECK(launch_pdl(k_wide_keys, key_blocks, WT, s, true, a, passes, width));
+        for (int p = 0; p < passes; ++p)
+            SPCONV_CHECK(pass((p & 1) ? a.vb : a.va, (p & 1) ? a.va : a.vb, a.row_bits + width * p, width,
+                              a.gh + p * kWideBins, p));
+        SPCONV_CHECK(launch_search_window((passes & 1) ? a.vb : a.va, n, a.row_bits, a.key_bits, a.koff, a.nbr, a.mask,
+                                          a.tap_count, a.status, s));
+        count_launch();
+    } else {
+        SPCONV_CHECK(launch_pdl(k_wide_grid_scatter, row_blocks, WT, s, true, a));
+        SPCONV_CHECK(launch_pdl(k_wide_grid_lookup, row_blocks, WT, s, true, a));
+    }
+    SPCONV_CHECK(launch_pdl(k_wide_mask_keys, key_blocks, WT, s, true, a));
+    for (int p = 0; p < kWideMaskPasses; ++p)
+        SPCONV_CHECK(pass((p & 1) ? a.vb : a.va, (p & 1) ? a.va : a.vb, a.row_bits + kMaskWidth * p, kMaskWidth,
+                          a.gh + (kWideKeyPassesMax + p) * kWideBins, kWideKeyPassesMax + p));
+    const uint64_t* ms = (kWideMaskPasses & 1) ? a.vb : a.va;
+    const unsigned tiles = static_cast<unsigned>(a.n_tiles);
+    SPCONV_CHECK(launch_pdl(k_wide_tile_count, tiles, kTileRows, s, true, a, ms));
+    SPCONV_CHECK(launch_pdl(k_wide_tile_scan, 1u, static_cast<unsigned>(kScanThreads), s, true, a));
+    SPCONV_CHECK(launch_pdl(k_wide_tile_write, tiles, kTileRows, s, true, a, ms));
+    return SPCONV_OK;
+}
+
+}  // namespace spconv

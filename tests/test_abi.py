@@ -63,7 +63,7 @@ def test_host_side_argument_errors(lib):
     # kernel size other than 3
     assert lib.spconv_build_map(None, 0, sp, 1, 5, None, None, ctypes.byref(h)) == -2
     # bad options
-    for bad in [(7, 0, 0, 0, 0), (0, 3, 0, 0, 0), (0, 0, -1, 0, 0), (0, 0, 0, 3, 0), (0, 0, 0, 0, 3),
+    for bad in [(7, 0, 0, 0, 0), (0, 3, 0, 0, 0), (0, 0, -1, 0, 0), (0, 0, 0, 4, 0), (0, 0, 0, 0, 3),
                 (0, 0, 0, 0, -1)]:
         opt = _native.Options(*bad)
         assert lib.spconv_build_map(None, 0, sp, 1, 3, ctypes.byref(opt), None, ctypes.byref(h)) == -1

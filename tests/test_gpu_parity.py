@@ -78,7 +78,7 @@ SMALL = [(1, 1, (4, 4, 4), 1), (2, 7, (5, 5, 5), 1), (3, 127, (8, 8, 8), 1), (4,
 @pytest.mark.parametrize("seed,n,shape,batch", SMALL)
 @pytest.mark.parametrize("mapper", ["dense", "sorted"])
 @pytest.mark.parametrize("bit_order", ["calibrated", "plain"])
-@pytest.mark.parametrize("pipeline", ["fused", "multi"])
+@pytest.mark.parametrize("pipeline", ["fused", "multi", "wide"])
 def test_map_small(seed, n, shape, batch, mapper, bit_order, pipeline):
     wl = S.random_cloud(seed, n, shape=shape, batch_size=batch)
     m = build(wl, mapper, bit_order, pipeline)
@@ -90,7 +90,7 @@ def test_map_small(seed, n, shape, batch, mapper, bit_order, pipeline):
 
 
 @pytest.mark.parametrize("name", ["tiny", "outdoor", "deep", "large", "stage"])
-@pytest.mark.parametrize("pipeline", ["auto", "multi"])
+@pytest.mark.parametrize("pipeline", ["auto", "fused", "multi"])
 def test_map_workloads(name, pipeline):
     coords, shape, batch, _ = S.make_coords(name)
     wl = S.Workload(name, torch.from_numpy(coords), shape, batch, 1, 1, None, [], 0)
@@ -100,16 +100,19 @@ def test_map_workloads(name, pipeline):
     assert_map_equal(ex, ref)
     info = ex["info"]
     assert info["mapper"] == ("dense" if name in ("tiny", "deep") else "sorted")
-    assert info["pipeline"] == ("fused" if pipeline == "auto" else "multi")
+    assert info["pipeline"] == ("wide" if pipeline == "auto" else pipeline)
 
 
-def test_map_many_rows_fused_and_multi_agree():
-    """Several ranking rounds per CTA and several tiles per CTA (N = 300k, 3 frames)."""
+@pytest.mark.parametrize("mapper", ["sorted", "dense"])
+def test_map_many_rows_pipelines_agree(mapper):
+    """Several ranking rounds and tiles per CTA in the cluster pipeline, hundreds of
+    look-back partitions in the whole-GPU one (N = 300k, 3 frames)."""
     wl = S.random_cloud(61, 300000, shape=(200, 200, 60), batch_size=3)
-    a = sc.map_export(build(wl, "sorted", pipeline="fused"))
-    b = sc.map_export(build(wl, "sorted", pipeline="multi"))
-    for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
-        assert torch.equal(a[key], b[key]), key
+    b = sc.map_export(build(wl, mapper, pipeline="multi"))
+    for pipeline in ("fused", "wide"):
+        a = sc.map_export(build(wl, mapper, pipeline=pipeline))
+        for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
+            assert torch.equal(a[key], b[key]), (pipeline, key)
 
 
 @pytest.mark.parametrize("name", ["tiny", "deep"])
@@ -145,7 +148,7 @@ def test_empty_input():
     assert out.shape == (0, 16)
 
 
-@pytest.mark.parametrize("pipeline", ["fused", "multi"])
+@pytest.mark.parametrize("pipeline", ["fused", "multi", "wide"])
 def test_duplicate_and_range_errors(pipeline):
     dup = torch.tensor([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=torch.int32, device="cuda")
     for mapper in ("dense", "sorted"):
@@ -319,10 +322,16 @@ def test_stage_six_layers_and_fp32_layer():
 
 def test_launch_count_reported():
     wl = S.random_cloud(51, 3000, shape=(16, 16, 16), c_in=64, c_out=64)
-    m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="dense")
+    m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="dense", pipeline="fused")
     assert sc.last_launch_count() == 2                # cluster build + whole-GPU compaction write
-    sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="sorted")
+    sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="sorted", pipeline="fused")
     assert sc.last_launch_count() == 4                # cluster sort, search, cluster rest, write
+    sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="dense", pipeline="wide")
+    assert sc.last_launch_count() == 10               # clear, scatter, lookup, mask keys, 3 passes,
+                                                      # tile count/scan/write
+    sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="sorted", pipeline="wide")
+    assert sc.last_launch_count() == 12               # clear, keys, 2 passes (15-bit keys), search, mask keys,
+                                                      # 3 passes, tile count/scan/write
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, pipeline="multi")
     assert sc.last_launch_count() > 5
     sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
