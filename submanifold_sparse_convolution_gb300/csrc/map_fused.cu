@@ -539,6 +539,7 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a, int part
 // get gather-table entries (the GEMM reads no others).
 __global__ void __launch_bounds__(kTileRows) k_tile_write_packed(const FusedArgs a, const uint64_t* __restrict__ ms) {
     __shared__ int32_t wc[kTileRows / 32][kTaps];
+    __shared__ int32_t seg[kTaps];   // the tile's first pair in every tap's list
     __shared__ int32_t err;
     const int64_t t = blockIdx.x;
     const int64_t T = a.n_tiles;
@@ -548,6 +549,8 @@ __global__ void __launch_bounds__(kTileRows) k_tile_write_packed(const FusedArgs
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) err = 0;
     pdl_wait();   // the mask sort and the (tap, tile) offsets must be complete
+    // read once here, not in the per-tap loop behind the pair stores
+    if (threadIdx.x < kTaps) seg[threadIdx.x] = a.seg_off[static_cast<int64_t>(threadIdx.x) * T + t];
     const int64_t s = t * kTileRows + threadIdx.x;
     int32_t r = s < n ? static_cast<int32_t>(ms[s] & rmask) : -1;
     if (r >= n) {
@@ -585,7 +588,7 @@ __global__ void __launch_bounds__(kTileRows) k_tile_write_packed(const FusedArgs
         if (!((uni >> k) & 1u)) continue;
         const bool present = (m >> k) & 1u;
         if (present) {
-            int64_t off = a.seg_off[static_cast<int64_t>(k) * T + t] + __popc(ball[k] & lt);
+            int64_t off = seg[k] + __popc(ball[k] & lt);
             for (int q = 0; q < warp; ++q) off += wc[q][k];
             if (off >= 0 && off < kTaps * n) {
                 a.in_rows[off] = v[k];

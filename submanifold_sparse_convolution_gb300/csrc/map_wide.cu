@@ -217,19 +217,28 @@ __global__ void __launch_bounds__(WT) k_wide_clear(const WideArgs a) {
     }
 }
 
+// The digits of the coordinate sort: the live key bits split into the fewest
+// passes of at most kDigitBitsWide bits, as evenly as possible (28 bits:
+// 10 + 9 + 9; a 9-bit pass looks back over half the digit values of a
+// 10-bit one).
+struct KeyDigits {
+    int passes;
+    int shift[kWideKeyPassesMax];
+    int width[kWideKeyPassesMax];
+};
+
 // ---------------------------------------------------------------------------
 // sorted-key mapper: packed keys and the digit counts of every key pass
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(WT) k_wide_keys(const WideArgs a, int passes, int width) {
+__global__ void __launch_bounds__(WT) k_wide_keys(const WideArgs a, const KeyDigits kd) {
     __shared__ int32_t h[kWideKeyPassesMax][kWideBins];
     const int t = threadIdx.x, lane = t & 31;
-    const int bins = 1 << width;
+    const int passes = kd.passes;
     pdl_trigger();
     for (int i = t; i < kWideKeyPassesMax * kWideBins; i += WT) (&h[0][0])[i] = 0;
     __syncthreads();
     const int rb = a.row_bits;
     const uint64_t invalid = (uint64_t(1) << a.key_bits) - 1;
-    const uint64_t dmask = static_cast<uint64_t>(bins - 1);
     int32_t err = 0;
     const int64_t row0 = static_cast<int64_t>(blockIdx.x) * WT * kRowsPerThread + t;
     int4 qs[kRowsPerThread];
@@ -256,16 +265,17 @@ __global__ void __launch_bounds__(WT) k_wide_keys(const WideArgs a, int passes, 
             a.va[i] = (key << rb) | static_cast<uint64_t>(i);
         }
         for (int p = 0; p < passes; ++p) {
-            const int dg = valid ? static_cast<int>((key >> (width * p)) & dmask) : kWideBins;
+            const uint64_t dmask = (uint64_t(1) << kd.width[p]) - 1;
+            const int dg = valid ? static_cast<int>((key >> kd.shift[p]) & dmask) : kWideBins;
             const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dg);
             if (valid && lane == __ffs(peers) - 1) atomicAdd(&h[p][dg], __popc(peers));
         }
     }
     __syncthreads();
     pdl_wait();   // the histograms and the status word are cleared
-    for (int i = t; i < passes * bins; i += WT) {
-        const int p = i / bins, b = i % bins;
-        const int32_t x = h[p][b];
+    for (int i = t; i < passes * kWideBins; i += WT) {
+        const int p = i / kWideBins, b = i % kWideBins;
+        const int32_t x = b < (1 << kd.width[p]) ? h[p][b] : 0;
         if (x) atomicAdd(a.gh + p * kWideBins + b, x);
     }
     if (err) atomicOr(a.status, err);
@@ -753,6 +763,7 @@ __global__ void __launch_bounds__(kScanThreads) k_wide_tile_scan(const WideArgs 
 // tile's union).
 __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a, const uint64_t* __restrict__ ms) {
     __shared__ int32_t wc[kTileRows / 32][kTaps];
+    __shared__ int32_t seg[kTaps];   // the tile's first pair in every tap's list
     __shared__ int32_t err;
     const int64_t tile = blockIdx.x;
     const int64_t T = a.n_tiles, n = a.n;
@@ -761,6 +772,9 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a,
     if (threadIdx.x == 0) err = 0;
     pdl_wait();   // the pair offsets are complete
     pdl_trigger();
+    // the offsets are read once, with the row ids, not inside the per-tap loop
+    // (there they would wait one round trip per tap behind the pair stores)
+    if (threadIdx.x < kTaps) seg[threadIdx.x] = __ldcg(a.seg_off + static_cast<int64_t>(threadIdx.x) * T + tile);
     const int64_t s = tile * kTileRows + threadIdx.x;
     int32_t r = s < n ? static_cast<int32_t>(__ldcg(ms + s) & rmask) : -1;
     if (r >= n) {
@@ -798,8 +812,7 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a,
         if (!((uni >> k) & 1u)) continue;
         const bool present = (m >> k) & 1u;
         if (present) {
-            int64_t off = static_cast<int64_t>(__ldcg(a.seg_off + static_cast<int64_t>(k) * T + tile)) +
-                          __popc(ball[k] & lt);
+            int64_t off = static_cast<int64_t>(seg[k]) + __popc(ball[k] & lt);
             for (int q = 0; q < warp; ++q) off += wc[q][k];
             if (off >= 0 && off < kTaps * n) {
                 a.in_rows[off] = v[k];
@@ -894,11 +907,17 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     };
     if (a.mapper == SPCONV_MAPPER_SORTED) {
         const int passes = wide_key_passes(a.key_bits);
-        const int width = (a.key_bits + passes - 1) / passes;
         if (passes > kWideKeyPassesMax) return SPCONV_ERR_UNSUPPORTED;
-        SPCONV_CHECK(launch_pdl(k_wide_keys, key_blocks, WT, s, true, a, passes, width));
+        KeyDigits kd = {};
+        kd.passes = passes;
+        for (int p = 0, at = 0; p < passes; ++p) {
+            kd.width[p] = a.key_bits / passes + (p < a.key_bits % passes ? 1 : 0);
+            kd.shift[p] = at;
+            at += kd.width[p];
+        }
+        SPCONV_CHECK(launch_pdl(k_wide_keys, key_blocks, WT, s, true, a, kd));
         for (int p = 0; p < passes; ++p)
-            SPCONV_CHECK(pass((p & 1) ? a.vb : a.va, (p & 1) ? a.va : a.vb, a.row_bits + width * p, width,
+            SPCONV_CHECK(pass((p & 1) ? a.vb : a.va, (p & 1) ? a.va : a.vb, a.row_bits + kd.shift[p], kd.width[p],
                               a.gh + p * kWideBins, p));
         SPCONV_CHECK(launch_search_window((passes & 1) ? a.vb : a.va, n, a.row_bits, a.key_bits, a.koff, a.nbr, a.mask,
                                           a.tap_count, a.status, s));
