@@ -115,6 +115,36 @@ def test_map_many_rows_pipelines_agree(mapper):
             assert torch.equal(a[key], b[key]), (pipeline, key)
 
 
+@pytest.mark.parametrize("y_extent", [1024, 2048])
+@pytest.mark.parametrize("pipeline", ["wide", "fused"])
+def test_map_sparse_line_beside_dense_slab(y_extent, pipeline):
+    """A line of voxels at x = 10 next to a full (y, z) slab at x = 11: the sorted
+    search's run for the slab column is y-range x 40 keys long, far beyond its
+    shared-memory window, so it takes the in-place global search; 42k rows use
+    the small-array block shape, 84k rows the large one."""
+    rng = np.random.default_rng(71)
+    line = np.stack([np.zeros(y_extent), np.full(y_extent, 10), np.arange(y_extent), np.zeros(y_extent)], 1)
+    yy, zz = np.meshgrid(np.arange(y_extent), np.arange(40), indexing="ij")
+    slab = np.stack([np.zeros(yy.size), np.full(yy.size, 11), yy.ravel(), zz.ravel()], 1)
+    coords = np.concatenate([line, slab], 0).astype(np.int32)
+    coords = coords[rng.permutation(len(coords))]
+    shape = (16, y_extent, 40)
+    m = sc.build_map(torch.from_numpy(coords).cuda(), shape, 1, mapper="sorted", pipeline=pipeline)
+    assert sc.map_status(m) == 0
+    assert_map_equal(sc.map_export(m), oracle_map(coords, shape, 1))
+
+
+def test_map_ticketed_sort_passes_agree():
+    """420k rows: more sort-pass CTAs (1024 keys each) than the GPU holds at once,
+    so the whole-GPU passes take their partitions from ticket counters and use
+    the look-back (not the grid barriers)."""
+    wl = S.random_cloud(62, 420000, shape=(240, 240, 60), batch_size=2)
+    a = sc.map_export(build(wl, "sorted", pipeline="wide"))
+    b = sc.map_export(build(wl, "sorted", pipeline="multi"))
+    for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
+        assert torch.equal(a[key], b[key]), key
+
+
 @pytest.mark.parametrize("name", ["tiny", "deep"])
 def test_dense_and_sorted_mappers_agree(name):
     coords, shape, batch, _ = S.make_coords(name)
