@@ -49,7 +49,11 @@ constexpr int WI = kWideKeysPerCta / WT;       // keys per thread in a sort pass
 constexpr int WW = WT / 32;                    // warps per CTA
 constexpr int kBinsPerThread = kWideBins / WT;
 constexpr int kMaskWidth = (kTaps + kWideMaskPasses - 1) / kWideMaskPasses;
-constexpr int kRowsPerThread = 4;              // key and mask-key kernels (loads issued together)
+// Rows per thread of the key and mask-key kernels (their loads issued
+// together): 1 up to kFewRows rows, for parallelism (outdoor 84 -> 80 us per
+// build); 4 above, where more CTAs would mean more global atomics for the
+// digit counts (stage, 240k rows: 203 vs 210 us).
+constexpr int64_t kFewRows = 131072;
 static_assert(kBinsPerThread * WT == kWideBins, "digit values split evenly over the threads");
 static_assert(WI * WT == kWideKeysPerCta, "keys split evenly over the threads");
 static_assert((1 << kMaskWidth) <= kWideBins, "mask digits fit the histogram");
@@ -230,6 +234,7 @@ struct KeyDigits {
 // ---------------------------------------------------------------------------
 // sorted-key mapper: packed keys and the digit counts of every key pass
 // ---------------------------------------------------------------------------
+template <int kRowsPerThread>
 __global__ void __launch_bounds__(WT) k_wide_keys(const WideArgs a, const KeyDigits kd) {
     __shared__ int32_t h[kWideKeyPassesMax][kWideBins];
     const int t = threadIdx.x, lane = t & 31;
@@ -346,6 +351,7 @@ __global__ void __launch_bounds__(WT) k_wide_grid_lookup(const WideArgs a) {
 // mask sort keys: the mask's bits in the tap order (rarest tap in the top bit
 // with the calibrated order), packed with the row; digit counts of the passes
 // ---------------------------------------------------------------------------
+template <int kRowsPerThread>
 __global__ void __launch_bounds__(WT) k_wide_mask_keys(const WideArgs a) {
     __shared__ int32_t h[kWideMaskPasses][1 << kMaskWidth];
     __shared__ int32_t taps[kTaps];
@@ -867,7 +873,9 @@ int wide_key_passes(int key_bits) { return (key_bits + kDigitBitsWide - 1) / kDi
 int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     const int64_t n = a.n;
     const unsigned parts = static_cast<unsigned>((n + kWideKeysPerCta - 1) / kWideKeysPerCta);
-    const unsigned key_blocks = static_cast<unsigned>((n + WT * kRowsPerThread - 1) / (WT * kRowsPerThread));
+    const bool few = n <= kFewRows;
+    const int rpt = few ? 1 : 4;
+    const unsigned key_blocks = static_cast<unsigned>((n + WT * rpt - 1) / (WT * rpt));
     const unsigned row_blocks = static_cast<unsigned>((n + WT - 1) / WT);
     // a look-back kernel numbers its partitions by blockIdx when all of its
     // CTAs fit on the device at once (each waits only on lower ones), else
@@ -915,7 +923,8 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
             kd.shift[p] = at;
             at += kd.width[p];
         }
-        SPCONV_CHECK(launch_pdl(k_wide_keys, key_blocks, WT, s, true, a, kd));
+        SPCONV_CHECK(few ? launch_pdl(k_wide_keys<1>, key_blocks, WT, s, true, a, kd)
+                         : launch_pdl(k_wide_keys<4>, key_blocks, WT, s, true, a, kd));
         for (int p = 0; p < passes; ++p)
             SPCONV_CHECK(pass((p & 1) ? a.vb : a.va, (p & 1) ? a.va : a.vb, a.row_bits + kd.shift[p], kd.width[p],
                               a.gh + p * kWideBins, p));
@@ -926,7 +935,8 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
         SPCONV_CHECK(launch_pdl(k_wide_grid_scatter, row_blocks, WT, s, true, a));
         SPCONV_CHECK(launch_pdl(k_wide_grid_lookup, row_blocks, WT, s, true, a));
     }
-    SPCONV_CHECK(launch_pdl(k_wide_mask_keys, key_blocks, WT, s, true, a));
+    SPCONV_CHECK(few ? launch_pdl(k_wide_mask_keys<1>, key_blocks, WT, s, true, a)
+                     : launch_pdl(k_wide_mask_keys<4>, key_blocks, WT, s, true, a));
     for (int p = 0; p < kWideMaskPasses; ++p)
         SPCONV_CHECK(pass((p & 1) ? a.vb : a.va, (p & 1) ? a.va : a.vb, a.row_bits + kMaskWidth * p, kMaskWidth,
                           a.gh + (kWideKeyPassesMax + p) * kWideBins, kWideKeyPassesMax + p));
