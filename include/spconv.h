@@ -100,6 +100,34 @@ typedef struct {
 typedef struct spconv_map_s* spconv_map_t;
 typedef struct spconv_wpack_s* spconv_wpack_t;
 
+/*
+ * Epilogue of a forward: what happens to each fp32 sum of output row i,
+ * channel o before its one rounding to the output dtype.  The inference form
+ * of a layer's batch norm (a per-channel scale and shift), its bias, a
+ * residual branch and the ReLU between layers, fused into the store so that
+ * they cost no extra pass over [n][c_out].  The pages' networks are stacks of
+ * such layers (FlyDSL PR #942, "Open questions": a layer stack with
+ * normalisation and residuals; "Sparse convolution in FP32", "Offset-group
+ * partitioning": the convolution's last launch applies the ReLU to every row):
+ *
+ *   y = sum * scale[o] + bias[o] + residual[i][o];   out[i][o] = relu ? max(y, 0) : y
+ *
+ *   scale_dev     fp32 [c_out], device, 16-byte aligned; NULL means 1.
+ *   bias_dev      fp32 [c_out], device, 16-byte aligned; NULL means 0.
+ *   residual_dev  [n][c_out] in the forward's dtype, device, 16-byte aligned,
+ *                 row-major in the original row order; NULL means 0.  It may
+ *                 be out_dev itself (an in-place add) or feats_dev, but must
+ *                 not partly overlap out_dev (SPCONV_ERR_ALIAS).
+ *   relu          0: none, 1: max(y, 0).  Other values: SPCONV_ERR_INVALID_ARG.
+ * The caller owns every buffer; the library only reads them, in stream order.
+ */
+typedef struct {
+    const float* scale_dev;
+    const float* bias_dev;
+    const void* residual_dev;
+    int32_t relu;
+} spconv_epilogue_t;
+
 /* Summary of a built map.  Filling it synchronises the map's stream. */
 typedef struct {
     int64_t n;           /* active voxels (rows)                                  */
@@ -158,6 +186,12 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
 int spconv_subm_forward(spconv_map_t map, const void* feats_dev, const void* weights_dev,
                         void* out_dev, int32_t c_in, int32_t c_out, int32_t dtype, void* stream);
 
+/* spconv_subm_forward with an epilogue (spconv_epilogue_t above; NULL is the
+ * plain forward).  Same arguments, layouts and errors otherwise. */
+int spconv_subm_forward_ex(spconv_map_t map, const void* feats_dev, const void* weights_dev,
+                           void* out_dev, int32_t c_in, int32_t c_out, int32_t dtype,
+                           const spconv_epilogue_t* epi, void* stream);
+
 /*
  * Pre-pack weights [27][c_in][c_out] for repeated forwards (FlyDSL PR #942,
  * "Weight layout is [kv, t, k_outer, u, k_inner]": a packed tile layout; here
@@ -168,6 +202,9 @@ int spconv_wpack_create(const void* weights_dev, int32_t c_in, int32_t c_out, in
                         void* stream, spconv_wpack_t* out_wpack);
 int spconv_subm_forward_packed(spconv_map_t map, const void* feats_dev, spconv_wpack_t wpack,
                                void* out_dev, void* stream);
+/* spconv_subm_forward_packed with an epilogue (NULL: none). */
+int spconv_subm_forward_packed_ex(spconv_map_t map, const void* feats_dev, spconv_wpack_t wpack,
+                                  void* out_dev, const spconv_epilogue_t* epi, void* stream);
 void spconv_wpack_destroy(spconv_wpack_t wpack);
 
 /* Synchronise the map's stream and return the first device-detected error

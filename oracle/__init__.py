@@ -161,6 +161,30 @@ def conv_f64(nbr: np.ndarray, feats, weights, rows=None, threads: int = 0) -> np
     return out
 
 
+def epilogue_f64(conv, scale=None, bias=None, residual=None, relu=False, rows=None) -> np.ndarray:
+    """The layer epilogue on fp64 convolution sums ``conv`` [R, C_out]:
+    ``y = conv * scale[o] + bias[o] + residual[row][o]``, then ``max(y, 0)``
+    when ``relu`` -- a layer's inference-form batch norm (per-channel scale
+    and shift), bias, residual branch and the ReLU that follows it ("Sparse
+    convolution in FP32", "Offset-group partitioning": the ReLU applied to
+    every output row; FlyDSL PR #942, "Open questions": layer stacks with
+    normalisation and residuals).  ``residual`` is [N, C_out] in original row
+    order; ``rows`` names the rows of ``conv`` (all N when None).  Missing
+    terms are 1, 0 and 0.
+    """
+    y = np.array(conv, dtype=np.float64)
+    if scale is not None:
+        y = y * np.asarray(scale, dtype=np.float64)[None, :]
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float64)[None, :]
+    if residual is not None:
+        r = np.asarray(residual, dtype=np.float64)
+        y = y + (r if rows is None else r[np.asarray(rows)])
+    if relu:
+        y = np.maximum(y, 0.0)
+    return y
+
+
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
 

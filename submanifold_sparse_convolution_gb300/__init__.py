@@ -144,13 +144,48 @@ def build_map(coords: torch.Tensor, spatial_shape: Optional[Sequence[int]] = Non
     return Map(h, int(coords.shape[0]), coords)
 
 
+def _epilogue(n: int, c_out: int, dtype: torch.dtype, device, scale, bias, residual, relu):
+    """The ``spconv_epilogue_t`` of a forward, or None when it is the identity.
+
+    Returns (struct or None, tensors to keep alive until the call returns)."""
+    if scale is None and bias is None and residual is None and not relu:
+        return None, ()
+    keep = []
+
+    def vec(t, name):
+        if t is None:
+            return None
+        _require_cuda(t, name)
+        if t.dtype != torch.float32 or t.dim() != 1 or t.shape[0] != c_out or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 [{c_out}] tensor")
+        keep.append(t)
+        return t.data_ptr()
+
+    e = _native.Epilogue()
+    e.scale_dev = vec(scale, "scale")
+    e.bias_dev = vec(bias, "bias")
+    if residual is not None:
+        _require_cuda(residual, "residual")
+        if residual.dtype != dtype or tuple(residual.shape) != (n, c_out):
+            raise ValueError(f"residual must be {dtype} [{n}, {c_out}]")
+        keep.append(residual)
+        e.residual_dev = residual.data_ptr()
+    e.relu = 1 if relu else 0
+    return e, tuple(keep)
+
+
 def subm_forward(m: Map, feats: torch.Tensor, weights: torch.Tensor,
                  out: Optional[torch.Tensor] = None,
-                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                 stream: Optional[torch.cuda.Stream] = None, *,
+                 scale: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
+                 residual: Optional[torch.Tensor] = None, relu: bool = False) -> torch.Tensor:
     """``spconv_subm_forward``: feats [N, C_in] x weights [27, C_in, C_out] -> [N, C_out].
 
     bf16 inputs use fp32 accumulation and one rounding at the store; fp32
-    inputs take the exact fp32 path.
+    inputs take the exact fp32 path.  ``scale``/``bias`` (fp32 [C_out]),
+    ``residual`` ([N, C_out], the output dtype; may be ``out``) and ``relu``
+    are applied to each fp32 sum before that rounding
+    (``spconv_subm_forward_ex``): y = sum*scale + bias + residual, then max(y, 0).
     """
     lib = library()
     _require_cuda(feats, "feats")
@@ -168,9 +203,15 @@ def subm_forward(m: Map, feats: torch.Tensor, weights: torch.Tensor,
         _require_cuda(out, "out")
         if out.dtype != feats.dtype or tuple(out.shape) != (m.n, c_out):
             raise ValueError(f"out must be {feats.dtype} [{m.n}, {c_out}]")
-    rc = lib.spconv_subm_forward(m.handle, _ptr(feats), _ptr(weights), _ptr(out), c_in, c_out,
-                                 _DTYPES[feats.dtype], _stream_ptr(stream))
-    _check(rc, "spconv_subm_forward")
+    epi, _keep = _epilogue(m.n, c_out, feats.dtype, feats.device, scale, bias, residual, relu)
+    if epi is None:
+        rc = lib.spconv_subm_forward(m.handle, _ptr(feats), _ptr(weights), _ptr(out), c_in, c_out,
+                                     _DTYPES[feats.dtype], _stream_ptr(stream))
+        _check(rc, "spconv_subm_forward")
+    else:
+        rc = lib.spconv_subm_forward_ex(m.handle, _ptr(feats), _ptr(weights), _ptr(out), c_in, c_out,
+                                        _DTYPES[feats.dtype], ctypes.byref(epi), _stream_ptr(stream))
+        _check(rc, "spconv_subm_forward_ex")
     return out
 
 
@@ -189,8 +230,11 @@ def wpack_create(weights: torch.Tensor, stream: Optional[torch.cuda.Stream] = No
 
 
 def subm_forward_packed(m: Map, feats: torch.Tensor, wp: WPack, out: Optional[torch.Tensor] = None,
-                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """``spconv_subm_forward_packed``: forward with weights from ``wpack_create``."""
+                        stream: Optional[torch.cuda.Stream] = None, *,
+                        scale: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
+                        residual: Optional[torch.Tensor] = None, relu: bool = False) -> torch.Tensor:
+    """``spconv_subm_forward_packed``: forward with weights from ``wpack_create``;
+    the epilogue arguments are those of ``subm_forward``."""
     lib = library()
     _require_cuda(feats, "feats")
     if feats.dtype != wp.dtype or feats.dim() != 2 or feats.shape != (m.n, wp.c_in):
@@ -201,8 +245,14 @@ def subm_forward_packed(m: Map, feats: torch.Tensor, wp: WPack, out: Optional[to
         _require_cuda(out, "out")
         if out.dtype != feats.dtype or tuple(out.shape) != (m.n, wp.c_out):
             raise ValueError(f"out must be {feats.dtype} [{m.n}, {wp.c_out}]")
-    rc = lib.spconv_subm_forward_packed(m.handle, _ptr(feats), wp.handle, _ptr(out), _stream_ptr(stream))
-    _check(rc, "spconv_subm_forward_packed")
+    epi, _keep = _epilogue(m.n, wp.c_out, feats.dtype, feats.device, scale, bias, residual, relu)
+    if epi is None:
+        rc = lib.spconv_subm_forward_packed(m.handle, _ptr(feats), wp.handle, _ptr(out), _stream_ptr(stream))
+        _check(rc, "spconv_subm_forward_packed")
+    else:
+        rc = lib.spconv_subm_forward_packed_ex(m.handle, _ptr(feats), wp.handle, _ptr(out), ctypes.byref(epi),
+                                               _stream_ptr(stream))
+        _check(rc, "spconv_subm_forward_packed_ex")
     return out
 
 

@@ -28,6 +28,11 @@ class MapInfo(ctypes.Structure):
                 ("batch_size", ctypes.c_int32), ("gemm", ctypes.c_int32)]
 
 
+class Epilogue(ctypes.Structure):
+    _fields_ = [("scale_dev", ctypes.c_void_p), ("bias_dev", ctypes.c_void_p),
+                ("residual_dev", ctypes.c_void_p), ("relu", ctypes.c_int32)]
+
+
 # name -> (restype, argtypes)
 SIGNATURES = {
     "spconv_build_map": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, c_int32_p, ctypes.c_int32,
@@ -36,11 +41,18 @@ SIGNATURES = {
     "spconv_subm_forward": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.c_void_p]),
+    "spconv_subm_forward_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.POINTER(Epilogue),
+                                              ctypes.c_void_p]),
     "spconv_wpack_create": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.c_void_p,
                                            ctypes.POINTER(ctypes.c_void_p)]),
     "spconv_subm_forward_packed": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                   ctypes.c_void_p, ctypes.c_void_p]),
+    "spconv_subm_forward_packed_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_void_p, ctypes.POINTER(Epilogue),
+                                                     ctypes.c_void_p]),
     "spconv_wpack_destroy": (None, [ctypes.c_void_p]),
     "spconv_map_status": (ctypes.c_int, [ctypes.c_void_p]),
     "spconv_map_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(MapInfo)]),

@@ -45,6 +45,25 @@ int check_forward_args(const MapHandle* h, const void* feats, const void* out, i
     return SPCONV_OK;
 }
 
+// Validates an epilogue against the forward's output and fills *e.
+int check_epilogue(const MapHandle* h, const spconv_epilogue_t* epi, const void* out, int32_t c_out,
+                   int32_t dtype, Epilogue* e) {
+    *e = Epilogue();
+    if (!epi) return SPCONV_OK;
+    if (epi->relu != 0 && epi->relu != 1) return SPCONV_ERR_INVALID_ARG;
+    if (!aligned(epi->scale_dev, 16) || !aligned(epi->bias_dev, 16) || !aligned(epi->residual_dev, 16))
+        return SPCONV_ERR_INVALID_ARG;
+    if (epi->residual_dev && epi->residual_dev != out) {
+        const size_t bytes = static_cast<size_t>(h->n) * c_out * (dtype == SPCONV_FP32 ? 4 : 2);
+        if (overlaps(epi->residual_dev, bytes, out, bytes)) return SPCONV_ERR_ALIAS;
+    }
+    e->scale = epi->scale_dev;
+    e->bias = epi->bias_dev;
+    e->residual = epi->residual_dev;
+    e->relu = epi->relu;
+    return SPCONV_OK;
+}
+
 bool use_tensor_path(int32_t c_in, int32_t c_out, int32_t dtype, const void* feats, const void* out) {
     return dtype == SPCONV_BF16 && tc_supported(c_in, c_out) && aligned(feats, 16) && aligned(out, 16);
 }
@@ -136,8 +155,16 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
 
 int spconv_subm_forward(spconv_map_t map, const void* feats_dev, const void* weights_dev, void* out_dev,
                         int32_t c_in, int32_t c_out, int32_t dtype, void* stream) {
+    return spconv_subm_forward_ex(map, feats_dev, weights_dev, out_dev, c_in, c_out, dtype, nullptr, stream);
+}
+
+int spconv_subm_forward_ex(spconv_map_t map, const void* feats_dev, const void* weights_dev, void* out_dev,
+                           int32_t c_in, int32_t c_out, int32_t dtype, const spconv_epilogue_t* epi,
+                           void* stream) {
     reset_launch_count();
     SPCONV_CHECK(check_forward_args(map, feats_dev, out_dev, c_in, c_out, dtype));
+    Epilogue e;
+    SPCONV_CHECK(check_epilogue(map, epi, out_dev, c_out, dtype, &e));
     if (map->n == 0) return SPCONV_OK;
     if (!weights_dev) return SPCONV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -155,9 +182,9 @@ int spconv_subm_forward(spconv_map_t map, const void* feats_dev, const void* wei
             map->wspace_bytes = need;
         }
         SPCONV_CHECK(tc_pack_weights(weights_dev, c_in, c_out, map->wspace, s));
-        return tc_forward(map, feats_dev, map->wspace, out_dev, c_in, c_out, s);
+        return tc_forward(map, feats_dev, map->wspace, out_dev, c_in, c_out, e, s);
     }
-    return simt_forward(map, feats_dev, weights_dev, out_dev, c_in, c_out, dtype, s);
+    return simt_forward(map, feats_dev, weights_dev, out_dev, c_in, c_out, dtype, e, s);
 }
 
 int spconv_wpack_create(const void* weights_dev, int32_t c_in, int32_t c_out, int32_t dtype, void* stream,
@@ -200,16 +227,23 @@ int spconv_wpack_create(const void* weights_dev, int32_t c_in, int32_t c_out, in
 
 int spconv_subm_forward_packed(spconv_map_t map, const void* feats_dev, spconv_wpack_t wpack, void* out_dev,
                                void* stream) {
+    return spconv_subm_forward_packed_ex(map, feats_dev, wpack, out_dev, nullptr, stream);
+}
+
+int spconv_subm_forward_packed_ex(spconv_map_t map, const void* feats_dev, spconv_wpack_t wpack, void* out_dev,
+                                  const spconv_epilogue_t* epi, void* stream) {
     reset_launch_count();
     if (!wpack) return SPCONV_ERR_INVALID_ARG;
     SPCONV_CHECK(check_forward_args(map, feats_dev, out_dev, wpack->c_in, wpack->c_out, wpack->dtype));
+    Epilogue e;
+    SPCONV_CHECK(check_epilogue(map, epi, out_dev, wpack->c_out, wpack->dtype, &e));
     if (map->n == 0) return SPCONV_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (wpack->tensor_path) {
         if (!aligned(feats_dev, 16) || !aligned(out_dev, 16)) return SPCONV_ERR_INVALID_ARG;
-        return tc_forward(map, feats_dev, wpack->data, out_dev, wpack->c_in, wpack->c_out, s);
+        return tc_forward(map, feats_dev, wpack->data, out_dev, wpack->c_in, wpack->c_out, e, s);
     }
-    return simt_forward(map, feats_dev, wpack->data, out_dev, wpack->c_in, wpack->c_out, wpack->dtype, s);
+    return simt_forward(map, feats_dev, wpack->data, out_dev, wpack->c_in, wpack->c_out, wpack->dtype, e, s);
 }
 
 void spconv_wpack_destroy(spconv_wpack_t wpack) {

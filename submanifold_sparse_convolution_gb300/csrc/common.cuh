@@ -94,6 +94,18 @@ struct WPackHandle {
     cudaStream_t stream = nullptr;
 };
 
+// What the forward does to each fp32 sum before its one rounding to the
+// output dtype: y = sum * scale[o] + bias[o] + residual[row][o], then
+// max(y, 0) if relu.  Null pointers stand for 1, 0 and 0.  Device pointers;
+// residual is in the output dtype with the output's [n][c_out] layout.
+struct Epilogue {
+    const float* scale = nullptr;
+    const float* bias = nullptr;
+    const void* residual = nullptr;
+    int32_t relu = 0;
+    bool active() const { return scale || bias || residual || relu; }
+};
+
 // ---- map building (map.cu) -----------------------------------------------
 int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* opt);
 int derive_shape(const int32_t* coords, int64_t n, cudaStream_t stream, int32_t shape[3],
@@ -105,11 +117,11 @@ int tc_tile_n(int32_t c_out);
 size_t tc_pack_bytes(int32_t c_in, int32_t c_out);
 int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, void* dst, cudaStream_t s);
 int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
-               int32_t c_out, cudaStream_t s);
+               int32_t c_out, const Epilogue& epi, cudaStream_t s);
 
 // ---- SIMT path (gemm_simt.cu) ----------------------------------------------
 int simt_forward(const MapHandle* h, const void* feats, const void* w, void* out, int32_t c_in,
-                 int32_t c_out, int32_t dtype, cudaStream_t s);
+                 int32_t c_out, int32_t dtype, const Epilogue& epi, cudaStream_t s);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPCONV_OK : SPCONV_ERR_CUDA; }
 

@@ -6,7 +6,9 @@
 // element is a plain FMA chain in fp32 over taps 0..26 and input channels in
 // ascending order, skipping absent taps ("Sparse convolution in FP32":
 // weights read as [offset][input][output] with consecutive output channels per
-// thread), so the result does not depend on the launch shape.
+// thread), so the result does not depend on the launch shape.  The optional
+// epilogue (scale, bias, residual, ReLU) is applied to the fp32 sum before
+// the store.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,7 +33,7 @@ __global__ void __launch_bounds__(256) k_simt(const T* __restrict__ feats, const
                                               T* __restrict__ out, const int32_t* __restrict__ perm,
                                               const int32_t* __restrict__ nbr,
                                               const uint32_t* __restrict__ mask, int64_t n, int c_in,
-                                              int c_out) {
+                                              int c_out, Epilogue epi) {
     const int groups = (c_out + VEC - 1) / VEC;
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t s = idx / groups;
@@ -57,14 +59,22 @@ __global__ void __launch_bounds__(256) k_simt(const T* __restrict__ feats, const
         }
     }
     T* dst = out + static_cast<int64_t>(r) * c_out + o0;
+    const T* res = epi.residual ? static_cast<const T*>(epi.residual) + static_cast<int64_t>(r) * c_out + o0 : nullptr;
 #pragma unroll
-    for (int v = 0; v < VEC; ++v)
-        if (o0 + v < c_out) dst[v] = from_f<T>(acc[v]);
+    for (int v = 0; v < VEC; ++v) {
+        if (o0 + v >= c_out) continue;
+        float y = acc[v];
+        if (epi.scale) y *= epi.scale[o0 + v];
+        if (epi.bias) y += epi.bias[o0 + v];
+        if (res) y += to_f(res[v]);
+        if (epi.relu) y = fmaxf(y, 0.0f);
+        dst[v] = from_f<T>(y);
+    }
 }
 
 template <typename T>
 int launch(const MapHandle* h, const void* feats, const void* w, void* out, int32_t c_in,
-           int32_t c_out, cudaStream_t s) {
+           int32_t c_out, const Epilogue& epi, cudaStream_t s) {
     const int vec = c_out % 4 == 0 ? 4 : 1;
     const int64_t groups = (c_out + vec - 1) / vec;
     const int64_t threads = h->n * groups;
@@ -73,11 +83,11 @@ int launch(const MapHandle* h, const void* feats, const void* w, void* out, int3
     if (vec == 4)
         k_simt<T, 4><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
             static_cast<const T*>(feats), static_cast<const T*>(w), static_cast<T*>(out), h->perm, h->nbr,
-            h->mask, h->n, c_in, c_out);
+            h->mask, h->n, c_in, c_out, epi);
     else
         k_simt<T, 1><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
             static_cast<const T*>(feats), static_cast<const T*>(w), static_cast<T*>(out), h->perm, h->nbr,
-            h->mask, h->n, c_in, c_out);
+            h->mask, h->n, c_in, c_out, epi);
     count_launch();
     return cuda_status(cudaGetLastError());
 }
@@ -85,10 +95,10 @@ int launch(const MapHandle* h, const void* feats, const void* w, void* out, int3
 }  // namespace
 
 int simt_forward(const MapHandle* h, const void* feats, const void* w, void* out, int32_t c_in,
-                 int32_t c_out, int32_t dtype, cudaStream_t s) {
+                 int32_t c_out, int32_t dtype, const Epilogue& epi, cudaStream_t s) {
     if (h->n == 0) return SPCONV_OK;
-    if (dtype == SPCONV_FP32) return launch<float>(h, feats, w, out, c_in, c_out, s);
-    return launch<__nv_bfloat16>(h, feats, w, out, c_in, c_out, s);
+    if (dtype == SPCONV_FP32) return launch<float>(h, feats, w, out, c_in, c_out, epi, s);
+    return launch<__nv_bfloat16>(h, feats, w, out, c_in, c_out, epi, s);
 }
 
 }  // namespace spconv

@@ -11,7 +11,8 @@
 // position (FlyDSL PR #942: fp32 accumulation, gather fused into the GEMM).
 //
 // Per CTA (persistent, one per SM), warp-specialised:
-//   warps 0-3   epilogue: tcgen05.ld of the accumulator, bf16 convert, store
+//   warps 0-3   epilogue: tcgen05.ld of the accumulator, the optional
+//               scale / bias / residual / ReLU in fp32, bf16 convert, store
 //   warp 4      TMEM allocation + MMA issue (the whole warp runs the loop,
 //               lane 0 issues)
 //   warp 5      scheduler: walks this CTA's work items (tile, output block)
@@ -92,6 +93,8 @@ struct TcParams {
     int32_t k_chunks;             // ceil(c_in / 64)
     int32_t n_tile;               // output channels per item (multiple of 16, <= NTMAX)
     int32_t n_nb;                 // c_out / n_tile
+    Epilogue epi;                 // applied to each fp32 sum before the rounding
+    int32_t epi_on;               // epi.active()
 };
 
 template <int NTMAX>
@@ -125,6 +128,42 @@ __device__ __forceinline__ int snake_item(int L, int cta, int grid) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The epilogue on 8 consecutive sums v[0..7] of output row `row`, channels
+// o .. o+7 (o a multiple of 8; scale, bias and residual 16-byte aligned).
+__device__ __forceinline__ void epilogue8(uint32_t* v, const Epilogue& e, int64_t row, int c_out, int o) {
+    float y[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[j] = __uint_as_float(v[j]);
+    if (e.scale) {
+        const float4 a = *reinterpret_cast<const float4*>(e.scale + o);
+        const float4 b = *reinterpret_cast<const float4*>(e.scale + o + 4);
+        y[0] *= a.x; y[1] *= a.y; y[2] *= a.z; y[3] *= a.w;
+        y[4] *= b.x; y[5] *= b.y; y[6] *= b.z; y[7] *= b.w;
+    }
+    if (e.bias) {
+        const float4 a = *reinterpret_cast<const float4*>(e.bias + o);
+        const float4 b = *reinterpret_cast<const float4*>(e.bias + o + 4);
+        y[0] += a.x; y[1] += a.y; y[2] += a.z; y[3] += a.w;
+        y[4] += b.x; y[5] += b.y; y[6] += b.z; y[7] += b.w;
+    }
+    if (e.residual) {
+        const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(e.residual) +
+                                                        row * c_out + o);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            y[2 * j] += __uint_as_float(w[j] << 16);
+            y[2 * j + 1] += __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+    if (e.relu) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) y[j] = fmaxf(y[j], 0.0f);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __float_as_uint(y[j]);
 }
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
@@ -527,6 +566,13 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                         }
                     }
                 } else if (dst_row) {
+                    if (p.epi_on) {
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            if (h >= 2 && !two) break;
+                            epilogue8(v + 8 * h, p.epi, orig, p.c_out, nb * p.n_tile + c + 8 * h);
+                        }
+                    }
                     uint4* d = reinterpret_cast<uint4*>(dst_row + c);
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
@@ -600,12 +646,23 @@ int num_sms() {
 
 // fp32 sums of the tap-major variant -> bf16 output (round to nearest even),
 // four values per thread and step.
-__global__ void __launch_bounds__(256) k_acc_to_bf16(const float4* __restrict__ acc, uint2* __restrict__ out,
-                                                     int64_t count4) {
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < count4;
+// Rounds the tap-major sums to bf16, 8 channels per thread, applying the
+// epilogue on the way (c_out is a multiple of 16, so 8 never straddle rows).
+__global__ void __launch_bounds__(256) k_acc_to_bf16(const float4* __restrict__ acc, uint4* __restrict__ out,
+                                                     int64_t count8, int c_out, Epilogue epi, int epi_on) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < count8;
          i += static_cast<int64_t>(gridDim.x) * 256) {
-        const float4 v = acc[i];
-        out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+        const float4 a = acc[2 * i], b = acc[2 * i + 1];
+        uint32_t v[8] = {__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z), __float_as_uint(a.w),
+                         __float_as_uint(b.x), __float_as_uint(b.y), __float_as_uint(b.z), __float_as_uint(b.w)};
+        if (epi_on) {
+            const int64_t e0 = 8 * i;
+            epilogue8(v, epi, e0 / c_out, c_out, static_cast<int>(e0 % c_out));
+        }
+        out[i] = make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                            pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                            pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                            pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
     }
 }
 
@@ -678,7 +735,7 @@ int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, void* dst, cudaS
 }
 
 int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
-               int32_t c_out, cudaStream_t s) {
+               int32_t c_out, const Epilogue& epi, cudaStream_t s) {
     if (h->n == 0) return SPCONV_OK;
     TcParams p;
     p.feats = static_cast<const __nv_bfloat16*>(feats);
@@ -700,6 +757,8 @@ int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, in
     p.k_chunks = (c_in + BK - 1) / BK;
     p.n_tile = tc_tile_n(c_out);
     p.n_nb = c_out / p.n_tile;
+    p.epi = epi;
+    p.epi_on = epi.active() ? 1 : 0;
     const int64_t items = h->n_tiles * p.n_nb;
     if (items > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
     p.n_items = static_cast<int32_t>(items);
@@ -724,10 +783,10 @@ int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, in
     p.acc = static_cast<float*>(h->acc);
     SPCONV_CHECK_CUDA(cudaMemsetAsync(p.acc, 0, need, s));
     SPCONV_CHECK(launch_tc_n<true>(p, sms, s));
-    const int64_t count4 = static_cast<int64_t>(h->n) * c_out / 4;
-    const int64_t blocks = (count4 + 255) / 256;
+    const int64_t count8 = static_cast<int64_t>(h->n) * c_out / 8;
+    const int64_t blocks = (count8 + 255) / 256;
     k_acc_to_bf16<<<static_cast<unsigned>(blocks < 8 * sms ? blocks : 8 * sms), 256, 0, s>>>(
-        reinterpret_cast<const float4*>(p.acc), reinterpret_cast<uint2*>(out), count4);
+        reinterpret_cast<const float4*>(p.acc), reinterpret_cast<uint4*>(out), count8, c_out, epi, p.epi_on);
     count_launch();
     return cuda_status(cudaGetLastError());
 }

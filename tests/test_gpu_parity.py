@@ -338,16 +338,127 @@ def test_stage_six_layers_and_fp32_layer():
     rows_t = torch.from_numpy(rows).long().cuda()
     x = wl.feats.cuda()
     for layer, w in enumerate(wl.weights):
-        y = sc.subm_forward(m, x, w.cuda())
-        ref = oracle.conv_f64(nbr, x.double().cpu().numpy(), w.double().numpy(), rows=rows)
+        relu = layer + 1 < len(wl.weights)   # the ReLU between layers, fused into the store
+        y = sc.subm_forward(m, x, w.cuda(), relu=relu)
+        ref = oracle.epilogue_f64(oracle.conv_f64(nbr, x.double().cpu().numpy(), w.double().numpy(), rows=rows),
+                                  relu=relu)
         check_bf16(y[rows_t], ref)
-        x = torch.relu(y)
+        x = y
     # the first layer again in exact fp32
     f32 = wl.feats.float().cuda()
     w32 = wl.weights[0].float().cuda()
     y32 = sc.subm_forward(m, f32, w32)
     ref = oracle.conv_f64(nbr, wl.feats.double().numpy(), wl.weights[0].double().numpy(), rows=rows)
     check_fp32(y32[rows_t], ref)
+
+
+# ---------------------------------------------------------------------------
+# fused epilogue (scale, bias, residual, ReLU)
+# ---------------------------------------------------------------------------
+
+EPI_CASES = [  # (c_in, c_out, dtype, gemm): tensor-core tile-union and tap-major, SIMT bf16, fp32
+    (64, 64, torch.bfloat16, "tile_union"), (128, 128, torch.bfloat16, "tile_union"),
+    (32, 256, torch.bfloat16, "tile_union"), (128, 128, torch.bfloat16, "tap_major"),
+    (5, 7, torch.bfloat16, "tile_union"), (16, 16, torch.float32, "tile_union")]
+EPI_TERMS = [dict(relu=True), dict(bias=True), dict(scale=True, bias=True),
+             dict(residual=True), dict(scale=True, bias=True, residual=True, relu=True)]
+
+
+def epilogue_inputs(n, c_out, dtype, terms, seed):
+    rng = np.random.default_rng(seed)
+    scale = torch.from_numpy(rng.uniform(0.5, 1.5, c_out).astype(np.float32)) if terms.get("scale") else None
+    bias = torch.from_numpy((rng.standard_normal(c_out) * 0.5).astype(np.float32)) if terms.get("bias") else None
+    res = (torch.from_numpy(rng.standard_normal((n, c_out)).astype(np.float32)).to(dtype)
+           if terms.get("residual") else None)
+    return scale, bias, res
+
+
+@pytest.mark.parametrize("c_in,c_out,dtype,gemm", EPI_CASES)
+@pytest.mark.parametrize("ti", range(len(EPI_TERMS)))
+def test_epilogue_forward(c_in, c_out, dtype, gemm, ti):
+    terms = EPI_TERMS[ti]
+    wl = S.random_cloud(600 + c_in + ti, 1700, shape=(14, 14, 14), batch_size=2, c_in=c_in, c_out=c_out)
+    f, w = wl.feats.to(dtype), wl.weights[0].to(dtype)
+    scale, bias, res = epilogue_inputs(wl.n, c_out, dtype, terms, 601 + ti)
+    m = build(wl, gemm=gemm)
+    cu = lambda t: None if t is None else t.cuda()
+    out = sc.subm_forward(m, f.cuda(), w.cuda(), scale=cu(scale), bias=cu(bias), residual=cu(res),
+                          relu=terms.get("relu", False))
+    assert sc.map_status(m) == 0
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    conv = oracle.conv_f64(nbr, f.double().numpy(), w.double().numpy())
+    d = lambda t: None if t is None else t.double().numpy()
+    ref = oracle.epilogue_f64(conv, d(scale), d(bias), d(res), terms.get("relu", False))
+    (check_fp32 if dtype == torch.float32 else check_bf16)(out, ref)
+    # the packed-weight entry point applies the same epilogue to the same bits
+    wp = sc.wpack_create(w.cuda())
+    out2 = sc.subm_forward_packed(m, f.cuda(), wp, scale=cu(scale), bias=cu(bias), residual=cu(res),
+                                  relu=terms.get("relu", False))
+    if gemm == "tap_major":
+        (check_fp32 if dtype == torch.float32 else check_bf16)(out2, ref)
+    else:
+        assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("gemm", ["tile_union", "tap_major"])
+def test_epilogue_relu_equals_relu_of_output(gemm):
+    # max(., 0) commutes with the rounding to bf16, so the fused ReLU gives
+    # exactly the bits of a ReLU applied to the plain output
+    wl = S.random_cloud(611, 5000, shape=(24, 24, 24), c_in=64, c_out=64)
+    m = build(wl, gemm=gemm)
+    f, w = wl.feats.cuda(), wl.weights[0].cuda()
+    wp = sc.wpack_create(w)
+    plain = sc.subm_forward_packed(m, f, wp)
+    fused = sc.subm_forward_packed(m, f, wp, relu=True)
+    if gemm == "tile_union":
+        assert torch.equal(fused, torch.relu(plain))
+    else:
+        # tap-major sums in a run-dependent order; compare with the tolerance
+        ref = oracle.epilogue_f64(oracle.conv_f64(oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1),
+                                                  wl.feats.double().numpy(), wl.weights[0].double().numpy()),
+                                  relu=True)
+        check_bf16(fused, ref)
+    assert (fused == 0).any() and (fused > 0).any()
+
+
+def test_epilogue_residual_in_place():
+    # residual == out: each element is read, then overwritten by the same thread
+    wl = S.random_cloud(621, 3000, shape=(16, 16, 16), c_in=128, c_out=128)
+    m = build(wl)
+    rng = np.random.default_rng(622)
+    r = torch.from_numpy(rng.standard_normal((wl.n, 128)).astype(np.float32)).to(torch.bfloat16)
+    buf = r.cuda().clone()
+    out = sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda(), out=buf, residual=buf, relu=True)
+    assert out.data_ptr() == buf.data_ptr()
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1)
+    ref = oracle.epilogue_f64(oracle.conv_f64(nbr, wl.feats.double().numpy(), wl.weights[0].double().numpy()),
+                              residual=r.double().numpy(), relu=True)
+    check_bf16(out, ref)
+
+
+def test_epilogue_argument_errors():
+    wl = S.random_cloud(631, 500, shape=(10, 10, 10), c_in=16, c_out=16)
+    m = build(wl)
+    f, w = wl.feats.cuda(), wl.weights[0].cuda()
+    lib = sc.library()
+    out = torch.empty((wl.n, 16), dtype=torch.bfloat16, device="cuda")
+    import ctypes
+    from submanifold_sparse_convolution_gb300 import _native
+
+    def call(e):
+        return lib.spconv_subm_forward_ex(m.handle, f.data_ptr(), w.data_ptr(), out.data_ptr(), 16, 16, 0,
+                                          ctypes.byref(e), None)
+
+    bias = torch.zeros(17, dtype=torch.float32, device="cuda")
+    assert call(_native.Epilogue(None, None, None, 2)) == -1            # relu must be 0 or 1
+    assert call(_native.Epilogue(None, bias.data_ptr() + 4, None, 0)) == -1   # bias not 16-byte aligned
+    big = torch.empty((wl.n + 8, 16), dtype=torch.bfloat16, device="cuda")
+    out = big[:wl.n]
+    assert call(_native.Epilogue(None, None, big[8:].data_ptr(), 0)) == -7  # residual partly overlaps out
+    assert call(_native.Epilogue(None, None, out.data_ptr(), 0)) == 0       # in place is allowed
+    assert lib.spconv_subm_forward_ex(m.handle, f.data_ptr(), w.data_ptr(), out.data_ptr(), 16, 16, 0,
+                                      None, None) == 0                     # NULL: the plain forward
+    assert sc.map_status(m) == 0
 
 
 def test_launch_count_reported():

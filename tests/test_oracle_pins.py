@@ -342,3 +342,76 @@ def test_conv_row_subset_matches_full():
     w = wl.weights[0].double().numpy()
     rows = np.array([7, 3, 499, 0, 3], dtype=np.int32)
     assert np.array_equal(oracle.conv_f64(nbr, f, w, rows=rows), oracle.conv_f64(nbr, f, w)[rows])
+
+
+# ---------------------------------------------------------------------------
+# layer epilogue (scale, bias, residual, ReLU)
+# ---------------------------------------------------------------------------
+
+def dense_layer_reference(coords, shape, batch, feats, weights, scale, bias, residual, relu):
+    """A dense layer through torch on a zero-filled grid (fp64, CPU): conv3d with
+    the per-channel scale folded into the weights and its own bias argument,
+    plus the residual, then torch's ReLU."""
+    w = np.asarray(weights, dtype=np.float64) * np.asarray(scale, dtype=np.float64)[None, None, :]
+    X, Y, Z = shape
+    f = torch.as_tensor(np.asarray(feats, dtype=np.float64))
+    wt = torch.as_tensor(w)
+    c_in, c_out = wt.shape[1], wt.shape[2]
+    grid = torch.zeros(batch, c_in, X, Y, Z, dtype=torch.float64)
+    c = torch.as_tensor(np.asarray(coords, dtype=np.int64))
+    grid[c[:, 0], :, c[:, 1], c[:, 2], c[:, 3]] = f
+    wd = torch.zeros(c_out, c_in, 3, 3, 3, dtype=torch.float64)
+    for k, (dx, dy, dz) in enumerate(OFFSETS):
+        wd[:, :, dx + 1, dy + 1, dz + 1] = wt[k].T
+    out = torch.nn.functional.conv3d(grid, wd, bias=torch.as_tensor(np.asarray(bias, dtype=np.float64)),
+                                     padding=1)
+    y = out[c[:, 0], :, c[:, 1], c[:, 2], c[:, 3]] + torch.as_tensor(np.asarray(residual, dtype=np.float64))
+    return (torch.relu(y) if relu else y).numpy()
+
+
+@pytest.mark.parametrize("relu", [False, True])
+def test_epilogue_matches_dense_layer(relu):
+    wl = S.random_cloud(81, 500, shape=(9, 8, 10), batch_size=2, c_in=6, c_out=5)
+    c = wl.coords.numpy()
+    rng = np.random.default_rng(82)
+    f = wl.feats.double().numpy()
+    w = wl.weights[0].double().numpy()
+    scale = rng.uniform(0.5, 2.0, 5)
+    bias = rng.standard_normal(5)
+    res = rng.standard_normal((c.shape[0], 5))
+    nbr = oracle.kernel_map(c, wl.spatial_shape, 2)
+    got = oracle.epilogue_f64(oracle.conv_f64(nbr, f, w), scale, bias, res, relu)
+    ref = dense_layer_reference(c, wl.spatial_shape, 2, f, w, scale, bias, res, relu)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    if relu:
+        assert (got == 0).any() and (got > 0).any()
+    # the row subset form reads the residual rows it is given
+    rows = np.array([3, 0, 499, 42], dtype=np.int32)
+    sub = oracle.epilogue_f64(oracle.conv_f64(nbr, f, w, rows=rows), scale, bias, res, relu, rows=rows)
+    np.testing.assert_allclose(sub, got[rows], rtol=1e-13, atol=1e-13)
+
+
+def test_mutated_epilogue_is_caught():
+    """Scaling after the bias, or the ReLU before the residual, both fail the dense layer."""
+    wl = S.random_cloud(83, 400, shape=(9, 9, 9), c_in=4, c_out=4)
+    c = wl.coords.numpy()
+    rng = np.random.default_rng(84)
+    f = wl.feats.double().numpy()
+    w = wl.weights[0].double().numpy()
+    scale, bias = rng.uniform(0.5, 2.0, 4), rng.standard_normal(4)
+    res = rng.standard_normal((c.shape[0], 4))
+    conv = oracle.conv_f64(oracle.kernel_map(c, wl.spatial_shape, 1), f, w)
+    ref = dense_layer_reference(c, wl.spatial_shape, 1, f, w, scale, bias, res, True)
+    wrong_order = np.maximum((conv + bias) * scale + res, 0.0)
+    relu_first = np.maximum(conv * scale + bias, 0.0) + res
+    assert not np.allclose(wrong_order, ref, atol=1e-6)
+    assert not np.allclose(relu_first, ref, atol=1e-6)
+    np.testing.assert_allclose(oracle.epilogue_f64(conv, scale, bias, res, True), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_epilogue_identity_and_defaults():
+    rng = np.random.default_rng(85)
+    conv = rng.standard_normal((7, 3))
+    assert np.array_equal(oracle.epilogue_f64(conv), conv)
+    assert np.array_equal(oracle.epilogue_f64(conv, relu=True), np.where(conv > 0, conv, 0.0))
+    assert np.array_equal(oracle.epilogue_f64(conv, scale=np.ones(3), bias=np.zeros(3)), conv)
