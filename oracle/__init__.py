@@ -1,4 +1,4 @@
-"""CPU oracle for submanifold sparse 3x3x3 convolution (test infrastructure).
+"""CPU oracle for submanifold sparse convolution, K = 3 and 5 (test infrastructure).
 
 Only the tests, the smoke check in ``__graft_entry__`` and the CPU-baseline leg
 of ``bench.py`` may import this package.  The library's product path never
@@ -6,7 +6,7 @@ does: it shares no code, header or helper with the CUDA implementation.
 
 The arithmetic lives in ``spconv_oracle.cpp`` (plain C++17: a hash-map
 neighbour lookup, ``std::stable_sort`` for the mask order, and an fp64 sum over
-the 27 taps).  This module compiles it with the host C++ compiler and wraps it
+the K^3 taps).  This module compiles it with the host C++ compiler and wraps it
 with numpy arrays.  See the C++ file for the conventions and the passages each
 function follows.
 """
@@ -54,19 +54,19 @@ def _load():
         lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
         i64, i32 = ctypes.c_int64, ctypes.c_int32
-        lib.oracle_kernel_map.argtypes = [P, i64, P, i32, P]
+        lib.oracle_kernel_map.argtypes = [P, i64, P, i32, i32, P]
         lib.oracle_kernel_map.restype = ctypes.c_int
-        lib.oracle_masks.argtypes = [P, i64, P]
+        lib.oracle_masks.argtypes = [P, i64, i32, i32, i32, P]
         lib.oracle_masks.restype = None
-        lib.oracle_tap_order.argtypes = [P, i64, ctypes.c_int, P]
+        lib.oracle_tap_order.argtypes = [P, i64, i32, ctypes.c_int, P]
         lib.oracle_tap_order.restype = None
-        lib.oracle_sort_keys.argtypes = [P, i64, P, P]
+        lib.oracle_sort_keys.argtypes = [P, i64, i32, P, P]
         lib.oracle_sort_keys.restype = None
         lib.oracle_perm.argtypes = [P, i64, P]
         lib.oracle_perm.restype = None
-        lib.oracle_pair_lists.argtypes = [P, P, i64, P, P, P]
+        lib.oracle_pair_lists.argtypes = [P, P, i64, i32, i32, P, P, P]
         lib.oracle_pair_lists.restype = i64
-        lib.oracle_conv_f64.argtypes = [P, P, i64, P, P, i32, i32, P, i32]
+        lib.oracle_conv_f64.argtypes = [P, i32, P, i64, P, P, i32, i32, P, i32]
         lib.oracle_conv_f64.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -85,28 +85,35 @@ class OracleError(RuntimeError):
         self.code = code
 
 
-def kernel_map(coords, spatial_shape, batch_size: int) -> np.ndarray:
-    """``nbr[N, 27]`` int32: row of the neighbour at tap k, or -1."""
+def kernel_map(coords, spatial_shape, batch_size: int, kernel_size: int = 3) -> np.ndarray:
+    """``nbr[N, K^3]`` int32: row of the neighbour at tap k, or -1."""
     c = np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 4))
     shape = np.ascontiguousarray(np.asarray(spatial_shape, dtype=np.int32))
-    nbr = np.empty((c.shape[0], 27), dtype=np.int32)
-    rc = _load().oracle_kernel_map(_ptr(c), c.shape[0], _ptr(shape), int(batch_size), _ptr(nbr))
+    K = int(kernel_size)
+    assert K >= 1 and K % 2 == 1
+    nbr = np.empty((c.shape[0], K ** 3), dtype=np.int32)
+    rc = _load().oracle_kernel_map(_ptr(c), c.shape[0], _ptr(shape), int(batch_size), K, _ptr(nbr))
     if rc != 0:
         raise OracleError(rc)
     return nbr
 
 
-def masks(nbr: np.ndarray) -> np.ndarray:
+def masks(nbr: np.ndarray, k0: int = 0, kg: int = None) -> np.ndarray:
+    """Masks over the taps ``[k0, k0 + kg)`` (all taps when ``kg`` is None; at most 32)."""
     nbr = np.ascontiguousarray(nbr, dtype=np.int32)
+    V = nbr.shape[1]
+    kg = V - k0 if kg is None else int(kg)
+    assert 0 < kg <= 32 and 0 <= k0 and k0 + kg <= V
     m = np.empty(nbr.shape[0], dtype=np.uint32)
-    _load().oracle_masks(_ptr(nbr), nbr.shape[0], _ptr(m))
+    _load().oracle_masks(_ptr(nbr), nbr.shape[0], V, int(k0), kg, _ptr(m))
     return m
 
 
-def tap_order(mask: np.ndarray, calibrated: bool = True) -> np.ndarray:
+def tap_order(mask: np.ndarray, calibrated: bool = True, taps: int = 27) -> np.ndarray:
+    """Key bit order of a group of ``taps`` taps (masks from ``masks``)."""
     mask = np.ascontiguousarray(mask, dtype=np.uint32)
-    order = np.empty(27, dtype=np.int32)
-    _load().oracle_tap_order(_ptr(mask), mask.shape[0], int(bool(calibrated)), _ptr(order))
+    order = np.empty(int(taps), dtype=np.int32)
+    _load().oracle_tap_order(_ptr(mask), mask.shape[0], int(taps), int(bool(calibrated)), _ptr(order))
     return order
 
 
@@ -114,7 +121,7 @@ def sort_keys(mask: np.ndarray, order: np.ndarray) -> np.ndarray:
     mask = np.ascontiguousarray(mask, dtype=np.uint32)
     order = np.ascontiguousarray(order, dtype=np.int32)
     key = np.empty(mask.shape[0], dtype=np.uint32)
-    _load().oracle_sort_keys(_ptr(mask), mask.shape[0], _ptr(order), _ptr(key))
+    _load().oracle_sort_keys(_ptr(mask), mask.shape[0], order.shape[0], _ptr(order), _ptr(key))
     return key
 
 
@@ -125,23 +132,45 @@ def perm(key: np.ndarray) -> np.ndarray:
     return p
 
 
+def group_orders(nbr: np.ndarray, groups: int = 1, calibrated: bool = True):
+    """Per group of ``V / groups`` consecutive taps: its masks, key bit order
+    and row order (each group orders the rows by its own masks).  Returns
+    ``(masks[G, N], orders[G, V/G], perms[G, N])``."""
+    V = nbr.shape[1]
+    assert V % groups == 0 and V // groups <= 32
+    kg = V // groups
+    ms, os_, ps = [], [], []
+    for g in range(groups):
+        m = masks(nbr, g * kg, kg)
+        o = tap_order(m, calibrated, kg)
+        ms.append(m)
+        os_.append(o)
+        ps.append(perm(sort_keys(m, o)))
+    return np.stack(ms), np.stack(os_), np.stack(ps)
+
+
 def pair_lists(nbr: np.ndarray, perm_: np.ndarray):
-    """``(tap_off[28], in_rows[P], out_rows[P])`` per tap in ``perm_`` order."""
+    """``(tap_off[V+1], in_rows[P], out_rows[P])``: the pairs of tap k in the
+    row order of its group.  ``perm_`` is one order [N] (one group) or
+    [G, N], one per group of V / G consecutive taps."""
     nbr = np.ascontiguousarray(nbr, dtype=np.int32)
-    perm_ = np.ascontiguousarray(perm_, dtype=np.int32)
-    n = nbr.shape[0]
-    tap_off = np.empty(28, dtype=np.int32)
-    cap = max(1, 27 * n)
+    perm_ = np.ascontiguousarray(np.atleast_2d(perm_), dtype=np.int32)
+    n, V = nbr.shape
+    G = perm_.shape[0]
+    assert V % G == 0 and perm_.shape[1] == n
+    tap_off = np.empty(V + 1, dtype=np.int32)
+    cap = max(1, V * n)
     ins = np.empty(cap, dtype=np.int32)
     outs = np.empty(cap, dtype=np.int32)
-    p = _load().oracle_pair_lists(_ptr(nbr), _ptr(perm_), n, _ptr(tap_off), _ptr(ins), _ptr(outs))
+    p = _load().oracle_pair_lists(_ptr(nbr), _ptr(perm_), n, V, G, _ptr(tap_off), _ptr(ins), _ptr(outs))
     return tap_off, ins[:p].copy(), outs[:p].copy()
 
 
 def conv_f64(nbr: np.ndarray, feats, weights, rows=None, threads: int = 0) -> np.ndarray:
     """fp64 ``out[r] = sum_k sum_c feats[nbr[r][k]][c] * weights[k][c][:]``.
 
-    ``feats`` [N, C_in] and ``weights`` [27, C_in, C_out] are taken as exact
+    ``feats`` [N, C_in] and ``weights`` [V, C_in, C_out] (V = K^3, the width
+    of ``nbr``) are taken as exact
     fp64 values (bf16 and fp32 inputs convert exactly).  ``rows`` selects the
     output rows to evaluate (all when None); the result follows its order.
     """
@@ -149,14 +178,15 @@ def conv_f64(nbr: np.ndarray, feats, weights, rows=None, threads: int = 0) -> np
     f = np.ascontiguousarray(np.asarray(feats, dtype=np.float64))
     w = np.ascontiguousarray(np.asarray(weights, dtype=np.float64))
     c_in, c_out = int(w.shape[1]), int(w.shape[2])
-    assert w.shape[0] == 27 and f.shape[1] == c_in
+    V = nbr.shape[1]
+    assert w.shape[0] == V and f.shape[1] == c_in
     if rows is None:
         r_arr, n_rows, rp = None, nbr.shape[0], None
     else:
         r_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
         n_rows, rp = r_arr.shape[0], _ptr(r_arr)
     out = np.empty((n_rows, c_out), dtype=np.float64)
-    _load().oracle_conv_f64(_ptr(nbr), rp, n_rows, _ptr(f), _ptr(w), c_in, c_out, _ptr(out),
+    _load().oracle_conv_f64(_ptr(nbr), V, rp, n_rows, _ptr(f), _ptr(w), c_in, c_out, _ptr(out),
                             int(threads))
     return out
 
@@ -190,13 +220,15 @@ def max_threads() -> int:
 
 
 def subm_conv(coords, spatial_shape, batch_size, feats, weights, calibrated=True, rows=None,
-              threads: int = 0):
-    """The whole path: kernel map, masks, order, pair lists and fp64 output."""
-    nbr = kernel_map(coords, spatial_shape, batch_size)
-    m = masks(nbr)
-    order = tap_order(m, calibrated)
-    p = perm(sort_keys(m, order))
+              threads: int = 0, kernel_size: int = 3, groups: int = 1):
+    """The whole path: kernel map, masks, order, pair lists and fp64 output.
+    With one group, ``mask``/``order``/``perm`` are one array each; with
+    ``groups`` > 1 they carry a leading group axis."""
+    nbr = kernel_map(coords, spatial_shape, batch_size, kernel_size)
+    m, order, p = group_orders(nbr, groups, calibrated)
     lists = pair_lists(nbr, p)
     out = conv_f64(nbr, feats, weights, rows=rows, threads=threads)
+    if groups == 1:
+        m, order, p = m[0], order[0], p[0]
     return dict(nbr=nbr, mask=m, order=order, perm=p, tap_off=lists[0], in_rows=lists[1],
                 out_rows=lists[2], out=out)

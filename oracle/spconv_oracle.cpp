@@ -1,29 +1,37 @@
-// Plain, slow CPU oracle for submanifold sparse 3x3x3 convolution.
+// Plain, slow CPU oracle for submanifold sparse convolution (K x K x K
+// kernels, K odd: 3 and 5).
 //
 // TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check of the
 // build entry module and the CPU-baseline leg of the benchmark may load or
 // call this code.  The product path never does, and the two share no code.
 //
 // What it computes (each function names the passage it follows):
-//   * the kernel map: for every active voxel and each of the 27 offsets, the
+//   * the kernel map: for every active voxel and each of the K^3 offsets, the
 //     row of the neighbour at that offset, or -1 -- an exact set lookup
 //     through a hash map ("Sparse convolution in FP32", section "The starting
 //     point": the work is finding which neighbours exist);
-//   * the 27-bit neighbour mask of each row and the rows sorted by it
-//     (same page, "Neighbour masks and sorted rows"; the bit order may be the
-//     plain one or calibrated, same page, "Calibrated bit order");
-//   * the per-tap pair lists in that sorted order (FlyDSL PR #942 summary,
-//     "Compaction is the largest single win": only the valid pairs, grouped
-//     by tap);
+//   * the neighbour mask of each row over a group of taps and the rows
+//     sorted by it (same page, "Neighbour masks and sorted rows"; the bit
+//     order may be the plain one or calibrated, same page, "Calibrated bit
+//     order").  With one group (K = 3) the mask has all 27 bits; with the
+//     taps partitioned into groups, each group has its own masks and its own
+//     row order (same page, "Offset-group partitioning");
+//   * the per-tap pair lists, each in the row order of its tap's group
+//     (FlyDSL PR #942 summary, "Compaction is the largest single win": only
+//     the valid pairs, grouped by tap);
 //   * the convolution itself, out[i][o] = sum_k sum_c f[nbr[i][k]][c] W[k][c][o],
 //     in fp64 ("Sparse convolution in FP32", "The starting point").
 //
 // Conventions (the pages leave them open; this is the reading used
 // throughout):
-//   tap k = 9*(dx+1) + 3*(dy+1) + (dz+1), offset d = (dx,dy,dz) in {-1,0,1}^3;
+//   r = (K-1)/2, tap k = K*K*(dx+r) + K*(dy+r) + (dz+r), offset
+//   d = (dx,dy,dz) in {-r..r}^3, V = K^3 taps (k = 9(dx+1) + 3(dy+1) + (dz+1)
+//   for K = 3);
 //   nbr[i][k] = row of the voxel at coords[i] + d_k in the same batch, else -1;
-//   weights are [27][C_in][C_out]; out = sum_k W[k]^T f(p + d_k)
-//   (cross-correlation, as torch conv3d with padding 1).
+//   weights are [V][C_in][C_out]; out = sum_k W[k]^T f(p + d_k)
+//   (cross-correlation, as torch conv3d with padding r);
+//   a group is a run of consecutive taps [k0, k0 + kg): with G groups of
+//   V / G taps, group g holds the taps with dx = g - r when G = K.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
@@ -55,7 +63,10 @@ struct VoxelHash {
     }
 };
 
-inline int tap_index(int dx, int dy, int dz) { return 9 * (dx + 1) + 3 * (dy + 1) + (dz + 1); }
+inline int tap_index(int K, int dx, int dy, int dz) {
+    const int r = (K - 1) / 2;
+    return K * K * (dx + r) + K * (dy + r) + (dz + r);
+}
 
 }  // namespace
 
@@ -66,9 +77,11 @@ enum { ORACLE_OK = 0, ORACLE_ERR_DUPLICATE = -5, ORACLE_ERR_RANGE = -6 };
 
 // Kernel map by hash lookup.  coords: [n][4] (b,x,y,z).  shape: {X,Y,Z}.
 // A coordinate outside 0 <= b < batch_size, 0 <= x < X, ... is an error, and
-// so is a repeated coordinate.  nbr: [n][27].
+// so is a repeated coordinate.  K: odd kernel size.  nbr: [n][K^3].
 int oracle_kernel_map(const int32_t* coords, int64_t n, const int32_t* shape,
-                      int32_t batch_size, int32_t* nbr) {
+                      int32_t batch_size, int32_t K, int32_t* nbr) {
+    const int r = (K - 1) / 2;
+    const int64_t V = static_cast<int64_t>(K) * K * K;
     std::unordered_map<Voxel, int32_t, VoxelHash> where;
     where.reserve(static_cast<size_t>(n) * 2 + 1);
     for (int64_t i = 0; i < n; ++i) {
@@ -80,49 +93,51 @@ int oracle_kernel_map(const int32_t* coords, int64_t n, const int32_t* shape,
     }
     for (int64_t i = 0; i < n; ++i) {
         const int32_t* c = coords + 4 * i;
-        for (int dx = -1; dx <= 1; ++dx)
-            for (int dy = -1; dy <= 1; ++dy)
-                for (int dz = -1; dz <= 1; ++dz) {
+        for (int dx = -r; dx <= r; ++dx)
+            for (int dy = -r; dy <= r; ++dy)
+                for (int dz = -r; dz <= r; ++dz) {
                     Voxel q{c[0], c[1] + dx, c[2] + dy, c[3] + dz};
                     auto it = where.find(q);
-                    nbr[27 * i + tap_index(dx, dy, dz)] = it == where.end() ? -1 : it->second;
+                    nbr[V * i + tap_index(K, dx, dy, dz)] = it == where.end() ? -1 : it->second;
                 }
     }
     return ORACLE_OK;
 }
 
-// mask[i] bit k set iff nbr[i][k] >= 0.
-void oracle_masks(const int32_t* nbr, int64_t n, uint32_t* mask) {
+// Mask over the group of taps [k0, k0 + kg) (kg <= 32): mask[i] bit j set
+// iff nbr[i][k0 + j] >= 0.  nbr rows have V entries.
+void oracle_masks(const int32_t* nbr, int64_t n, int32_t V, int32_t k0, int32_t kg, uint32_t* mask) {
     for (int64_t i = 0; i < n; ++i) {
         uint32_t m = 0;
-        for (int k = 0; k < 27; ++k)
-            if (nbr[27 * i + k] >= 0) m |= 1u << k;
+        for (int j = 0; j < kg; ++j)
+            if (nbr[V * i + k0 + j] >= 0) m |= 1u << j;
         mask[i] = m;
     }
 }
 
-// Bit order of the sort key.  order[j] is the tap whose presence sets key bit j.
+// Bit order of the sort key of one group of kg taps (masks as above).
+// order[j] is the group's tap (bit of the mask) whose presence sets key bit j.
 // calibrated == 0: plain order, order[j] = j.
 // calibrated != 0: taps by descending number of rows that have them (ties by
 // ascending tap index), so the rarest tap is the most significant key bit and
 // rows that share rare taps end up next to each other.
-void oracle_tap_order(const uint32_t* mask, int64_t n, int calibrated, int32_t* order) {
-    int64_t count[27] = {0};
+void oracle_tap_order(const uint32_t* mask, int64_t n, int32_t kg, int calibrated, int32_t* order) {
+    std::vector<int64_t> count(static_cast<size_t>(kg), 0);
     for (int64_t i = 0; i < n; ++i)
-        for (int k = 0; k < 27; ++k) count[k] += (mask[i] >> k) & 1u;
-    std::vector<int32_t> taps(27);
-    for (int k = 0; k < 27; ++k) taps[k] = k;
+        for (int k = 0; k < kg; ++k) count[k] += (mask[i] >> k) & 1u;
+    std::vector<int32_t> taps(static_cast<size_t>(kg));
+    for (int k = 0; k < kg; ++k) taps[k] = k;
     if (calibrated)
         std::stable_sort(taps.begin(), taps.end(),
                          [&](int32_t a, int32_t b) { return count[a] > count[b]; });
-    for (int j = 0; j < 27; ++j) order[j] = taps[j];
+    for (int j = 0; j < kg; ++j) order[j] = taps[j];
 }
 
-// key[i] = sum_j [tap order[j] present in row i] << j.
-void oracle_sort_keys(const uint32_t* mask, int64_t n, const int32_t* order, uint32_t* key) {
+// key[i] = sum_j [tap order[j] present in row i] << j, j < kg.
+void oracle_sort_keys(const uint32_t* mask, int64_t n, int32_t kg, const int32_t* order, uint32_t* key) {
     for (int64_t i = 0; i < n; ++i) {
         uint32_t k = 0;
-        for (int j = 0; j < 27; ++j)
+        for (int j = 0; j < kg; ++j)
             if ((mask[i] >> order[j]) & 1u) k |= 1u << j;
         key[i] = k;
     }
@@ -137,16 +152,19 @@ void oracle_perm(const uint32_t* key, int64_t n, int32_t* perm) {
     std::memcpy(perm, rows.data(), sizeof(int32_t) * static_cast<size_t>(n));
 }
 
-// Per-tap pair lists in perm order.  tap_off: [28], CSR offsets.  in_rows /
-// out_rows: room for every pair (27 n at most).  Returns the pair count P.
-int64_t oracle_pair_lists(const int32_t* nbr, const int32_t* perm, int64_t n, int32_t* tap_off,
-                          int32_t* in_rows, int32_t* out_rows) {
+// Per-tap pair lists, tap k in the row order of its group: perms holds G
+// orders of n rows ([G][n]), the taps split into G groups of V / G
+// consecutive taps.  tap_off: [V + 1], CSR offsets.  in_rows / out_rows: room
+// for every pair (V n at most).  Returns the pair count P.
+int64_t oracle_pair_lists(const int32_t* nbr, const int32_t* perms, int64_t n, int32_t V, int32_t G,
+                          int32_t* tap_off, int32_t* in_rows, int32_t* out_rows) {
     int64_t p = 0;
-    for (int k = 0; k < 27; ++k) {
+    for (int k = 0; k < V; ++k) {
         tap_off[k] = static_cast<int32_t>(p);
+        const int32_t* perm = perms + static_cast<int64_t>(k / (V / G)) * n;
         for (int64_t s = 0; s < n; ++s) {
             int32_t r = perm[s];
-            int32_t j = nbr[27 * static_cast<int64_t>(r) + k];
+            int32_t j = nbr[static_cast<int64_t>(V) * r + k];
             if (j >= 0) {
                 in_rows[p] = j;
                 out_rows[p] = r;
@@ -154,14 +172,14 @@ int64_t oracle_pair_lists(const int32_t* nbr, const int32_t* perm, int64_t n, in
             }
         }
     }
-    tap_off[27] = static_cast<int32_t>(p);
+    tap_off[V] = static_cast<int32_t>(p);
     return p;
 }
 
-// out[r][o] = sum_k sum_c feats[nbr[r][k]][c] * weights[k][c][o] in fp64, for
+// out[r][o] = sum_{k<V} sum_c feats[nbr[r][k]][c] * weights[k][c][o] in fp64, for
 // the rows listed in rows[0..n_rows) (all rows when rows == NULL, then
 // n_rows == n).  out is [n_rows][c_out], in the order of rows.
-void oracle_conv_f64(const int32_t* nbr, const int32_t* rows, int64_t n_rows,
+void oracle_conv_f64(const int32_t* nbr, int32_t V, const int32_t* rows, int64_t n_rows,
                      const double* feats, const double* weights, int32_t c_in, int32_t c_out,
                      double* out, int32_t threads) {
 #ifdef _OPENMP
@@ -172,8 +190,8 @@ void oracle_conv_f64(const int32_t* nbr, const int32_t* rows, int64_t n_rows,
         int64_t r = rows ? rows[t] : t;
         double* o = out + t * c_out;
         for (int32_t q = 0; q < c_out; ++q) o[q] = 0.0;
-        for (int k = 0; k < 27; ++k) {
-            int32_t j = nbr[27 * r + k];
+        for (int k = 0; k < V; ++k) {
+            int32_t j = nbr[static_cast<int64_t>(V) * r + k];
             if (j < 0) continue;
             const double* f = feats + static_cast<int64_t>(j) * c_in;
             const double* w = weights + static_cast<int64_t>(k) * c_in * c_out;

@@ -415,3 +415,171 @@ def test_epilogue_identity_and_defaults():
     assert np.array_equal(oracle.epilogue_f64(conv), conv)
     assert np.array_equal(oracle.epilogue_f64(conv, relu=True), np.where(conv > 0, conv, 0.0))
     assert np.array_equal(oracle.epilogue_f64(conv, scale=np.ones(3), bias=np.zeros(3)), conv)
+
+
+# ---------------------------------------------------------------------------
+# kernel size 5 and offset groups
+# ---------------------------------------------------------------------------
+
+def offsets_k(K):
+    r = (K - 1) // 2
+    return [(dx, dy, dz) for dx in range(-r, r + 1) for dy in range(-r, r + 1) for dz in range(-r, r + 1)]
+
+
+def brute_force_nbr_k(coords, K):
+    """All-pairs search for a K x K x K kernel (taps in the order of offsets_k)."""
+    c = np.asarray(coords, dtype=np.int64)
+    n = c.shape[0]
+    offs = offsets_k(K)
+    nbr = np.full((n, len(offs)), -1, dtype=np.int64)
+    diff = c[None, :, :] - c[:, None, :]
+    same_b = diff[:, :, 0] == 0
+    for k, (dx, dy, dz) in enumerate(offs):
+        hit = same_b & (diff[:, :, 1] == dx) & (diff[:, :, 2] == dy) & (diff[:, :, 3] == dz)
+        i_idx, j_idx = np.nonzero(hit)
+        nbr[i_idx, k] = j_idx
+    return nbr
+
+
+def dense_conv_reference_k(coords, shape, batch, feats, weights, K):
+    """torch conv3d (padding (K-1)/2, fp64) on a zero-filled grid, read at active sites."""
+    X, Y, Z = shape
+    r = (K - 1) // 2
+    f = torch.as_tensor(np.asarray(feats, dtype=np.float64))
+    w = torch.as_tensor(np.asarray(weights, dtype=np.float64))
+    c_in, c_out = w.shape[1], w.shape[2]
+    grid = torch.zeros(batch, c_in, X, Y, Z, dtype=torch.float64)
+    c = torch.as_tensor(np.asarray(coords, dtype=np.int64))
+    grid[c[:, 0], :, c[:, 1], c[:, 2], c[:, 3]] = f
+    wd = torch.zeros(c_out, c_in, K, K, K, dtype=torch.float64)
+    for k, (dx, dy, dz) in enumerate(offsets_k(K)):
+        wd[:, :, dx + r, dy + r, dz + r] = w[k].T
+    out = torch.nn.functional.conv3d(grid, wd, padding=r)
+    return out[c[:, 0], :, c[:, 1], c[:, 2], c[:, 3]].numpy()
+
+
+def check_group_golden(name):
+    g = read_golden(name)
+    K, G = g["kernel"][0], g["groups"][0]
+    V = K ** 3
+    coords = np.array(g["coords"], dtype=np.int32).reshape(-1, 4)
+    n = coords.shape[0]
+    nbr = oracle.kernel_map(coords, g["shape"], g["batch"][0], K)
+    m, _, p = oracle.group_orders(nbr, G)
+    assert m.reshape(-1).tolist() == g["masks"]
+    assert p.reshape(-1).tolist() == g["perms"]
+    tap_off, ins, outs = oracle.pair_lists(nbr, p)
+    assert ins.tolist() == g["in_rows"] and outs.tolist() == g["out_rows"]
+    counts = np.diff(tap_off)
+    want = dict(zip(g["tap_counts"][0::2], g["tap_counts"][1::2]))
+    assert counts.tolist() == [want.get(k, 0) for k in range(V)]
+    if "out" in g:
+        feats = np.array(g["feats"], dtype=np.float64).reshape(-1, 1)
+        weights = (np.arange(V, dtype=np.float64) + 1).reshape(V, 1, 1)
+        res = oracle.subm_conv(coords, g["shape"], g["batch"][0], feats, weights, kernel_size=K, groups=G)
+        assert res["out"][:, 0].tolist() == g["out"]
+        assert res["perm"].shape == (G, n)
+
+
+def test_golden_k3_three_groups():
+    check_group_golden("line_k3_three_groups.txt")
+
+
+def test_golden_k5_five_groups():
+    check_group_golden("line_k5_five_groups.txt")
+
+
+@pytest.mark.parametrize("seed,n,shape,batch", [(91, 300, (9, 8, 7), 2), (92, 700, (10, 10, 10), 1),
+                                                (93, 1, (4, 4, 4), 1)])
+def test_kernel_map_k5_matches_brute_force(seed, n, shape, batch):
+    wl = S.random_cloud(seed, n, shape=shape, batch_size=batch)
+    nbr = oracle.kernel_map(wl.coords.numpy(), shape, batch, 5)
+    assert nbr.shape == (n, 125)
+    assert np.array_equal(nbr, brute_force_nbr_k(wl.coords.numpy(), 5))
+
+
+def test_kernel_map_k5_invariants_and_cube():
+    wl = S.random_cloud(94, 2000, shape=(14, 14, 14), batch_size=2)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 2, 5)
+    n = nbr.shape[0]
+    assert np.array_equal(nbr[:, 62], np.arange(n))
+    for k in range(125):
+        rows = np.nonzero(nbr[:, k] >= 0)[0]
+        assert np.array_equal(nbr[nbr[rows, k], 124 - k], rows)
+    # the 3x3x3 taps of the 5x5x5 map are the K = 3 map
+    nbr3 = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 2, 3)
+    inner = [25 * (dx + 2) + 5 * (dy + 2) + (dz + 2) for dx, dy, dz in OFFSETS]
+    assert np.array_equal(nbr[:, inner], nbr3)
+    # a full 5x5x5 cube: per-axis neighbour counts 3 4 5 4 3, 19^3 pairs
+    cells = np.array([(0, x, y, z) for x in range(5) for y in range(5) for z in range(5)], dtype=np.int32)
+    cube = oracle.kernel_map(cells, (5, 5, 5), 1, 5)
+    per_axis = [3, 4, 5, 4, 3]
+    for i, (_, x, y, z) in enumerate(cells):
+        assert (cube[i] >= 0).sum() == per_axis[x] * per_axis[y] * per_axis[z]
+    assert (cube >= 0).sum() == 19 ** 3
+
+
+@pytest.mark.parametrize("seed,n,shape,batch,c_in,c_out", [(95, 300, (9, 8, 7), 2, 5, 3),
+                                                            (96, 600, (11, 11, 11), 1, 8, 8)])
+def test_conv_k5_matches_dense_conv3d(seed, n, shape, batch, c_in, c_out):
+    wl = S.random_cloud(seed, n, shape=shape, batch_size=batch, c_in=c_in, c_out=c_out)
+    rng = np.random.default_rng(seed)
+    nbr = oracle.kernel_map(wl.coords.numpy(), shape, batch, 5)
+    f = wl.feats.double().numpy()
+    w = rng.standard_normal((125, c_in, c_out)) * 0.05
+    got = oracle.conv_f64(nbr, f, w)
+    ref = dense_conv_reference_k(wl.coords.numpy(), shape, batch, f, w, 5)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # a mirrored kernel (convolution instead of correlation) is caught
+    assert not np.allclose(oracle.conv_f64(nbr, f, w[::-1].copy()), ref, atol=1e-6)
+
+
+@pytest.mark.parametrize("K,G", [(3, 3), (5, 5), (3, 1)])
+@pytest.mark.parametrize("calibrated", [False, True])
+def test_group_orders_and_pair_lists(K, G, calibrated):
+    wl = S.random_cloud(97 + K + G, 1500, shape=(13, 13, 13), batch_size=2)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 2, K)
+    V, kg = K ** 3, K ** 3 // G
+    m, orders, p = oracle.group_orders(nbr, G, calibrated)
+    assert m.shape == (G, nbr.shape[0]) and p.shape == (G, nbr.shape[0])
+    present = nbr >= 0
+    for g in range(G):
+        bits = present[:, g * kg:(g + 1) * kg]
+        assert np.array_equal(m[g], (bits * (1 << np.arange(kg, dtype=np.int64))).sum(1).astype(np.uint32))
+        counts = bits.sum(0)
+        if calibrated:
+            assert orders[g].tolist() == np.lexsort((np.arange(kg), -counts)).tolist()
+        else:
+            assert orders[g].tolist() == list(range(kg))
+        key = oracle.sort_keys(m[g], orders[g]).astype(np.int64)
+        ks = key[p[g]]
+        assert sorted(p[g].tolist()) == list(range(nbr.shape[0]))
+        assert np.all(np.diff(ks) >= 0)
+        assert np.all(np.diff(p[g])[np.diff(ks) == 0] > 0)
+    tap_off, ins, outs = oracle.pair_lists(nbr, p)
+    assert tap_off[V] == present.sum() and np.all(np.diff(tap_off) == present.sum(0))
+    for k in range(V):
+        seg = slice(tap_off[k], tap_off[k + 1])
+        got = set(zip(ins[seg].tolist(), outs[seg].tolist()))
+        rows = np.nonzero(present[:, k])[0]
+        assert got == set(zip(nbr[rows, k].tolist(), rows.tolist()))
+        pos = np.empty(nbr.shape[0], dtype=np.int64)
+        pos[p[k // kg]] = np.arange(nbr.shape[0])
+        assert np.all(np.diff(pos[outs[seg]]) > 0)
+    if G == 1:
+        # one group is the plain K = 3 order
+        assert np.array_equal(p[0], oracle.perm(oracle.sort_keys(oracle.masks(nbr),
+                                                                 oracle.tap_order(oracle.masks(nbr), calibrated))))
+
+
+def test_mutated_group_order_is_caught():
+    """Pair lists laid out in one order for all taps (the groups' orders
+    ignored) break the property that each tap follows its own group's order."""
+    wl = S.random_cloud(99, 1200, shape=(12, 12, 12))
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1, 3)
+    _, _, p = oracle.group_orders(nbr, 3)
+    tap_off, _, outs = oracle.pair_lists(nbr, p[1])
+    pos = np.empty(nbr.shape[0], dtype=np.int64)
+    pos[p[0]] = np.arange(nbr.shape[0])
+    follows = [np.all(np.diff(pos[outs[tap_off[k]:tap_off[k + 1]]]) > 0) for k in range(9)]
+    assert not all(follows)
