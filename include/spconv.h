@@ -1,19 +1,23 @@
 /*
- * spconv.h -- C ABI of the GB300 (sm_103a) submanifold sparse 3x3x3 convolution.
+ * spconv.h -- C ABI of the GB300 (sm_103a) submanifold sparse convolution
+ * (3x3x3 and 5x5x5 kernels, stride 1).
  *
  * The operation (FlyDSL PR #942, "Add submanifold sparse 3D convolution",
  * Summary: raw voxel coordinates in, output features out, the kernel map built
  * internally; "Sparse convolution in FP32", section "The starting point": for
  * every active voxel, the sum over its 27 neighbours of the neighbour's
- * features times the weights of that kernel offset):
+ * features times the weights of that kernel offset; FlyDSL PR #942, "Test
+ * plan": kernel sizes 3 and 5):
  *
- *     out[i][o] = sum_{k=0..26} sum_{c} f[nbr[i][k]][c] * W[k][c][o]
+ *     out[i][o] = sum_{k=0..V-1} sum_{c} f[nbr[i][k]][c] * W[k][c][o]
  *
  * over the rows i of the input, where nbr[i][k] is the row of the voxel at
  * coords[i] + d_k (same batch index), the term skipped when there is none.
- * Tap order: k = 9*(dx+1) + 3*(dy+1) + (dz+1) for d = (dx,dy,dz) in {-1,0,1}^3
- * (cross-correlation, as torch conv3d with padding 1).  Outputs live at the
- * input sites, in the input row order.
+ * Kernel size K (3 or 5), radius r = (K-1)/2, V = K^3 taps; tap order
+ * k = K*K*(dx+r) + K*(dy+r) + (dz+r) for d = (dx,dy,dz) in {-r..r}^3, i.e.
+ * k = 9*(dx+1) + 3*(dy+1) + (dz+1) for K = 3 (cross-correlation, as torch
+ * conv3d with padding r).  Outputs live at the input sites, in the input row
+ * order.
  *
  * Memory: every pointer argument named *_dev is a device pointer that the
  * caller owns; host pointers are marked host.  The library allocates only map
@@ -62,7 +66,7 @@ typedef enum {
 
 typedef enum {
     SPCONV_ORDER_CALIBRATED = 0, /* sort key bits by descending tap frequency (rarest tap = MSB) */
-    SPCONV_ORDER_PLAIN = 1       /* sort key = the 27-bit mask itself                             */
+    SPCONV_ORDER_PLAIN = 1       /* sort key = the mask itself                                    */
 } spconv_bit_order_t;
 
 typedef enum {
@@ -95,6 +99,14 @@ typedef struct {
     int64_t dense_max_cells; /* AUTO threshold on B*(X+2)*(Y+2)*(Z+2); default 1<<24   */
     int32_t pipeline;        /* spconv_pipeline_t, default AUTO                        */
     int32_t gemm;            /* spconv_gemm_t for the bf16 forward on this map, default AUTO */
+    int32_t groups;          /* offset groups ("Sparse convolution in FP32", "Offset-group
+                                partitioning"): the V taps split into G runs of V/G
+                                consecutive taps (G = K: the taps of one dx each), every
+                                group with its own masks, row order and tiles, the forward
+                                one GEMM pass per group.  0: default (1 for K = 3, 5 for
+                                K = 5); 1 (K = 3 only) or K.  G > 1 builds with the MULTI
+                                pipeline and the TILE_UNION forward; other choices of
+                                pipeline or gemm return SPCONV_ERR_UNSUPPORTED.           */
 } spconv_options_t;
 
 typedef struct spconv_map_s* spconv_map_t;
@@ -132,14 +144,16 @@ typedef struct {
 typedef struct {
     int64_t n;           /* active voxels (rows)                                  */
     int64_t pairs;       /* P = number of (row, tap) with a neighbour (>= n)      */
-    int64_t n_tiles;     /* 128-row tiles of the mask-sorted order                */
-    int64_t tile_taps;   /* sum over tiles of the taps in the tile's mask union   */
+    int64_t n_tiles;     /* 128-row tiles of the mask-sorted order (per group)    */
+    int64_t tile_taps;   /* sum over tiles (all groups) of the taps in the tile's mask union */
     int32_t mapper;      /* spconv_mapper_t actually used (DENSE or SORTED)       */
     int32_t pipeline;    /* spconv_pipeline_t actually used (FUSED, MULTI, WIDE)  */
     int32_t key_bits;    /* live bits of the packed coordinate key                */
     int32_t shape[3];    /* spatial shape used                                    */
     int32_t batch_size;  /* batch size used                                       */
     int32_t gemm;        /* spconv_gemm_t the bf16 forward uses (TILE_UNION or TAP_MAJOR) */
+    int32_t kernel_size; /* K                                                     */
+    int32_t groups;      /* G offset groups                                       */
 } spconv_map_info_t;
 
 /*
@@ -154,15 +168,15 @@ typedef struct {
  *   spatial_shape  host int32[3] {X, Y, Z}, each >= 1; NULL derives max+1 per
  *                  axis on the device (synchronises the stream).
  *   batch_size     frames, >= 1; 0 derives max(b)+1 (synchronises the stream).
- *   kernel_size    3 (the only size this build implements; others return
- *                  SPCONV_ERR_UNSUPPORTED).
+ *   kernel_size    3 or 5 (others return SPCONV_ERR_UNSUPPORTED).
  *   opt            options, NULL for defaults.
  *   stream         CUDA stream (cudaStream_t) the work is enqueued on.
  *   out_map        receives the handle; free it with spconv_map_destroy.
  *
- * Device-side results (all in the handle): the kernel map nbr[n][27], the
- * 27-bit masks, perm (rows in ascending sort-key order, ties by row), the
- * per-tap pair lists in perm order, and the 128-row tile work list.
+ * Device-side results (all in the handle): the kernel map nbr[n][V]; per
+ * offset group its masks (bit j: the group's tap j present), perm (rows in
+ * ascending sort-key order, ties by row) and 128-row tile work list; the
+ * per-tap pair lists, each in the order of its tap's group.
  */
 int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatial_shape,
                      int32_t batch_size, int32_t kernel_size, const spconv_options_t* opt,
@@ -173,7 +187,7 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
  * top of this file).
  *
  *   feats_dev    [n][c_in] row-major, dtype elements, 16-byte aligned.
- *   weights_dev  [27][c_in][c_out] row-major, dtype elements.
+ *   weights_dev  [V][c_in][c_out] row-major, dtype elements (V = K^3 of the map).
  *   out_dev      [n][c_out] row-major, dtype elements, 16-byte aligned; must
  *                not overlap feats (SPCONV_ERR_ALIAS).
  *   dtype        SPCONV_BF16: bf16 in/out, fp32 accumulation, one rounding to
@@ -193,7 +207,7 @@ int spconv_subm_forward_ex(spconv_map_t map, const void* feats_dev, const void* 
                            const spconv_epilogue_t* epi, void* stream);
 
 /*
- * Pre-pack weights [27][c_in][c_out] for repeated forwards (FlyDSL PR #942,
+ * Pre-pack weights [27][c_in][c_out] of a 3x3x3 kernel for repeated forwards (FlyDSL PR #942,
  * "Weight layout is [kv, t, k_outer, u, k_inner]": a packed tile layout; here
  * the tensor-core shared-memory image).  The handle owns a copy; the source
  * may be freed once the stream has passed this call.
@@ -205,6 +219,11 @@ int spconv_subm_forward_packed(spconv_map_t map, const void* feats_dev, spconv_w
 /* spconv_subm_forward_packed with an epilogue (NULL: none). */
 int spconv_subm_forward_packed_ex(spconv_map_t map, const void* feats_dev, spconv_wpack_t wpack,
                                   void* out_dev, const spconv_epilogue_t* epi, void* stream);
+/* spconv_wpack_create for a kernel of size kernel_size (3 or 5): weights
+ * [K^3][c_in][c_out].  A packed forward on a map of another kernel size returns
+ * SPCONV_ERR_INVALID_ARG. */
+int spconv_wpack_create_ex(const void* weights_dev, int32_t kernel_size, int32_t c_in, int32_t c_out,
+                           int32_t dtype, void* stream, spconv_wpack_t* out_wpack);
 void spconv_wpack_destroy(spconv_wpack_t wpack);
 
 /* Synchronise the map's stream and return the first device-detected error
@@ -216,8 +235,8 @@ int spconv_map_info(spconv_map_t map, spconv_map_info_t* info);
 
 /*
  * Copy the map's arrays into caller device buffers (any may be NULL):
- *   nbr_dev int32 [n][27]; mask_dev uint32 [n]; perm_dev int32 [n];
- *   tap_off_dev int32 [28]; in_rows_dev, out_rows_dev int32 [pairs].
+ *   nbr_dev int32 [n][V]; mask_dev uint32 [G][n]; perm_dev int32 [G][n];
+ *   tap_off_dev int32 [V + 1]; in_rows_dev, out_rows_dev int32 [pairs].
  * Enqueued on stream; no synchronisation.
  */
 int spconv_map_export(spconv_map_t map, int32_t* nbr_dev, uint32_t* mask_dev, int32_t* perm_dev,

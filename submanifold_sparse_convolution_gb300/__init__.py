@@ -67,9 +67,11 @@ def _require_cuda(t: torch.Tensor, name: str):
 class Map:
     """A kernel map (handle ``spconv_map_t``); shared by every layer on these sites."""
 
-    def __init__(self, handle: ctypes.c_void_p, n: int, coords: torch.Tensor):
+    def __init__(self, handle: ctypes.c_void_p, n: int, coords: torch.Tensor, kernel_size: int = 3):
         self._h = handle
         self.n = n
+        self.kernel_size = kernel_size
+        self.taps = kernel_size ** 3
         self._coords = coords      # kept alive while the build may still read it
 
     @property
@@ -93,9 +95,9 @@ class Map:
 class WPack:
     """Pre-packed weights (handle ``spconv_wpack_t``)."""
 
-    def __init__(self, handle, c_in, c_out, dtype, src):
+    def __init__(self, handle, c_in, c_out, dtype, src, taps=27):
         self._h = handle
-        self.c_in, self.c_out, self.dtype = c_in, c_out, dtype
+        self.c_in, self.c_out, self.dtype, self.taps = c_in, c_out, dtype, taps
         self._src = src
 
     @property
@@ -119,12 +121,13 @@ class WPack:
 def build_map(coords: torch.Tensor, spatial_shape: Optional[Sequence[int]] = None,
               batch_size: int = 0, kernel_size: int = 3, mapper: str = "auto",
               bit_order: str = "calibrated", dense_max_cells: int = 0, pipeline: str = "auto",
-              gemm: str = "auto", stream: Optional[torch.cuda.Stream] = None) -> Map:
+              gemm: str = "auto", stream: Optional[torch.cuda.Stream] = None, groups: int = 0) -> Map:
     """``spconv_build_map``: kernel map of ``coords`` (int32 [N, 4] (b, x, y, z) on the GPU).
 
     ``spatial_shape`` None and ``batch_size`` 0 derive them on the device
     (this synchronises the stream).  ``gemm`` picks the bf16 forward's work
-    decomposition on this map (``GEMMS``).
+    decomposition on this map (``GEMMS``).  ``kernel_size`` 3 or 5;
+    ``groups`` the offset groups (0: 1 for K = 3, 5 for K = 5; or K).
     """
     lib = library()
     _require_cuda(coords, "coords")
@@ -134,14 +137,14 @@ def build_map(coords: torch.Tensor, spatial_shape: Optional[Sequence[int]] = Non
     if spatial_shape is not None:
         shape_arr = (ctypes.c_int32 * 3)(*[int(v) for v in spatial_shape])
     opt = _native.Options(MAPPERS[mapper], BIT_ORDERS[bit_order], int(dense_max_cells),
-                          PIPELINES[pipeline], GEMMS[gemm])
+                          PIPELINES[pipeline], GEMMS[gemm], int(groups))
     h = ctypes.c_void_p()
     rc = lib.spconv_build_map(_ptr(coords), int(coords.shape[0]),
                               ctypes.cast(shape_arr, _native.c_int32_p) if shape_arr is not None else None,
                               int(batch_size), int(kernel_size), ctypes.byref(opt), _stream_ptr(stream),
                               ctypes.byref(h))
     _check(rc, "spconv_build_map")
-    return Map(h, int(coords.shape[0]), coords)
+    return Map(h, int(coords.shape[0]), coords, int(kernel_size))
 
 
 def _epilogue(n: int, c_out: int, dtype: torch.dtype, device, scale, bias, residual, relu):
@@ -179,7 +182,7 @@ def subm_forward(m: Map, feats: torch.Tensor, weights: torch.Tensor,
                  stream: Optional[torch.cuda.Stream] = None, *,
                  scale: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
                  residual: Optional[torch.Tensor] = None, relu: bool = False) -> torch.Tensor:
-    """``spconv_subm_forward``: feats [N, C_in] x weights [27, C_in, C_out] -> [N, C_out].
+    """``spconv_subm_forward``: feats [N, C_in] x weights [V, C_in, C_out] -> [N, C_out], V = K^3.
 
     bf16 inputs use fp32 accumulation and one rounding at the store; fp32
     inputs take the exact fp32 path.  ``scale``/``bias`` (fp32 [C_out]),
@@ -194,8 +197,8 @@ def subm_forward(m: Map, feats: torch.Tensor, weights: torch.Tensor,
         raise ValueError("feats and weights must both be bf16 or both fp32")
     if feats.dim() != 2 or feats.shape[0] != m.n:
         raise ValueError(f"feats must be [{m.n}, C_in]")
-    if weights.dim() != 3 or weights.shape[0] != 27 or weights.shape[1] != feats.shape[1]:
-        raise ValueError("weights must be [27, C_in, C_out]")
+    if weights.dim() != 3 or weights.shape[0] != m.taps or weights.shape[1] != feats.shape[1]:
+        raise ValueError(f"weights must be [{m.taps}, C_in, C_out]")
     c_in, c_out = int(weights.shape[1]), int(weights.shape[2])
     if out is None:
         out = torch.empty((m.n, c_out), dtype=feats.dtype, device=feats.device)
@@ -216,17 +219,19 @@ def subm_forward(m: Map, feats: torch.Tensor, weights: torch.Tensor,
 
 
 def wpack_create(weights: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> WPack:
-    """``spconv_wpack_create``: pack [27, C_in, C_out] weights once for many forwards."""
+    """``spconv_wpack_create_ex``: pack [K^3, C_in, C_out] weights (K = 3 or 5,
+    from the first dimension) once for many forwards."""
     lib = library()
     _require_cuda(weights, "weights")
-    if weights.dtype not in _DTYPES or weights.dim() != 3 or weights.shape[0] != 27:
-        raise ValueError("weights must be bf16 or fp32 [27, C_in, C_out]")
+    sizes = {27: 3, 125: 5}
+    if weights.dtype not in _DTYPES or weights.dim() != 3 or int(weights.shape[0]) not in sizes:
+        raise ValueError("weights must be bf16 or fp32 [27 or 125, C_in, C_out]")
     c_in, c_out = int(weights.shape[1]), int(weights.shape[2])
     h = ctypes.c_void_p()
-    rc = lib.spconv_wpack_create(_ptr(weights), c_in, c_out, _DTYPES[weights.dtype],
-                                 _stream_ptr(stream), ctypes.byref(h))
-    _check(rc, "spconv_wpack_create")
-    return WPack(h, c_in, c_out, weights.dtype, weights)
+    rc = lib.spconv_wpack_create_ex(_ptr(weights), sizes[int(weights.shape[0])], c_in, c_out,
+                                    _DTYPES[weights.dtype], _stream_ptr(stream), ctypes.byref(h))
+    _check(rc, "spconv_wpack_create_ex")
+    return WPack(h, c_in, c_out, weights.dtype, weights, int(weights.shape[0]))
 
 
 def subm_forward_packed(m: Map, feats: torch.Tensor, wp: WPack, out: Optional[torch.Tensor] = None,
@@ -239,6 +244,8 @@ def subm_forward_packed(m: Map, feats: torch.Tensor, wp: WPack, out: Optional[to
     _require_cuda(feats, "feats")
     if feats.dtype != wp.dtype or feats.dim() != 2 or feats.shape != (m.n, wp.c_in):
         raise ValueError(f"feats must be {wp.dtype} [{m.n}, {wp.c_in}]")
+    if wp.taps != m.taps:
+        raise ValueError(f"weights pack has {wp.taps} taps, the map {m.taps}")
     if out is None:
         out = torch.empty((m.n, wp.c_out), dtype=feats.dtype, device=feats.device)
     else:
@@ -269,18 +276,22 @@ def map_info(m: Map) -> dict:
                 mapper={1: "dense", 2: "sorted"}.get(info.mapper, str(info.mapper)),
                 pipeline={1: "fused", 2: "multi", 3: "wide"}.get(info.pipeline, str(info.pipeline)),
                 key_bits=info.key_bits, shape=tuple(info.shape), batch_size=info.batch_size,
-                gemm={1: "tile_union", 2: "tap_major"}.get(info.gemm, str(info.gemm)))
+                gemm={1: "tile_union", 2: "tap_major"}.get(info.gemm, str(info.gemm)),
+                kernel_size=info.kernel_size, groups=info.groups)
 
 
 def map_export(m: Map, stream: Optional[torch.cuda.Stream] = None) -> dict:
-    """``spconv_map_export``: nbr [N,27], mask [N], perm [N], tap_off [28], in_rows/out_rows [P]."""
+    """``spconv_map_export``: nbr [N, V], tap_off [V+1], in_rows/out_rows [P];
+    mask and perm [N] with one offset group, [G, N] with G > 1."""
     info = map_info(m)
     n, p = info["n"], info["pairs"]
+    V, G = info["kernel_size"] ** 3, info["groups"]
     dev = torch.device("cuda", torch.cuda.current_device())
-    nbr = torch.empty((n, 27), dtype=torch.int32, device=dev)
-    mask = torch.empty((n,), dtype=torch.int32, device=dev)
-    perm = torch.empty((n,), dtype=torch.int32, device=dev)
-    tap_off = torch.empty((28,), dtype=torch.int32, device=dev)
+    nbr = torch.empty((n, V), dtype=torch.int32, device=dev)
+    gshape = (n,) if G == 1 else (G, n)
+    mask = torch.empty(gshape, dtype=torch.int32, device=dev)
+    perm = torch.empty(gshape, dtype=torch.int32, device=dev)
+    tap_off = torch.empty((V + 1,), dtype=torch.int32, device=dev)
     ins = torch.empty((max(p, 1),), dtype=torch.int32, device=dev)
     outs = torch.empty((max(p, 1),), dtype=torch.int32, device=dev)
     rc = library().spconv_map_export(m.handle, _ptr(nbr), _ptr(mask), _ptr(perm), _ptr(tap_off),

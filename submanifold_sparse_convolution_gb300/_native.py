@@ -17,7 +17,7 @@ c_int32_p = ctypes.POINTER(ctypes.c_int32)
 class Options(ctypes.Structure):
     _fields_ = [("mapper", ctypes.c_int32), ("bit_order", ctypes.c_int32),
                 ("dense_max_cells", ctypes.c_int64), ("pipeline", ctypes.c_int32),
-                ("gemm", ctypes.c_int32)]
+                ("gemm", ctypes.c_int32), ("groups", ctypes.c_int32)]
 
 
 class MapInfo(ctypes.Structure):
@@ -25,7 +25,8 @@ class MapInfo(ctypes.Structure):
                 ("tile_taps", ctypes.c_int64), ("mapper", ctypes.c_int32),
                 ("pipeline", ctypes.c_int32),
                 ("key_bits", ctypes.c_int32), ("shape", ctypes.c_int32 * 3),
-                ("batch_size", ctypes.c_int32), ("gemm", ctypes.c_int32)]
+                ("batch_size", ctypes.c_int32), ("gemm", ctypes.c_int32),
+                ("kernel_size", ctypes.c_int32), ("groups", ctypes.c_int32)]
 
 
 class Epilogue(ctypes.Structure):
@@ -48,6 +49,9 @@ SIGNATURES = {
     "spconv_wpack_create": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.c_void_p,
                                            ctypes.POINTER(ctypes.c_void_p)]),
+    "spconv_wpack_create_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                              ctypes.POINTER(ctypes.c_void_p)]),
     "spconv_subm_forward_packed": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                   ctypes.c_void_p, ctypes.c_void_p]),
     "spconv_subm_forward_packed_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,

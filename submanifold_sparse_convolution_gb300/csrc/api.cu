@@ -111,7 +111,7 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
     *out_map = nullptr;
     if (n < 0 || n >= (int64_t(1) << 30)) return SPCONV_ERR_INVALID_ARG;
     if (n > 0 && (!coords_dev || !aligned(coords_dev, 16))) return SPCONV_ERR_INVALID_ARG;
-    if (kernel_size != 3) return SPCONV_ERR_UNSUPPORTED;
+    if (kernel_size != 3 && kernel_size != 5) return SPCONV_ERR_UNSUPPORTED;
     if (batch_size < 0) return SPCONV_ERR_INVALID_ARG;
     if (opt) {
         if (opt->mapper < SPCONV_MAPPER_AUTO || opt->mapper > SPCONV_MAPPER_SORTED) return SPCONV_ERR_INVALID_ARG;
@@ -120,6 +120,15 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
         if (opt->dense_max_cells < 0) return SPCONV_ERR_INVALID_ARG;
         if (opt->pipeline < SPCONV_PIPELINE_AUTO || opt->pipeline > SPCONV_PIPELINE_WIDE) return SPCONV_ERR_INVALID_ARG;
         if (opt->gemm < SPCONV_GEMM_AUTO || opt->gemm > SPCONV_GEMM_TAP_MAJOR) return SPCONV_ERR_INVALID_ARG;
+    }
+    // offset groups: one (K = 3 only: 27 taps fit one mask) or K (the taps of each dx)
+    int32_t groups = (opt && opt->groups > 0) ? opt->groups : (kernel_size == 3 ? 1 : kernel_size);
+    if (opt && opt->groups < 0) return SPCONV_ERR_INVALID_ARG;
+    if (groups != kernel_size && !(groups == 1 && kernel_size == 3)) return SPCONV_ERR_UNSUPPORTED;
+    if (groups > 1 && opt) {
+        if (opt->pipeline != SPCONV_PIPELINE_AUTO && opt->pipeline != SPCONV_PIPELINE_MULTI)
+            return SPCONV_ERR_UNSUPPORTED;
+        if (opt->gemm == SPCONV_GEMM_TAP_MAJOR) return SPCONV_ERR_UNSUPPORTED;
     }
     int32_t shape[3] = {1, 1, 1};
     int32_t batch = batch_size;
@@ -143,6 +152,9 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
     h->n = n;
     std::memcpy(h->shape, shape, sizeof(shape));
     h->batch = batch;
+    h->kernel_size = kernel_size;
+    h->taps = kernel_size * kernel_size * kernel_size;
+    h->groups = groups;
     const int rc = build_map_impl(h, coords_dev, opt);
     if (rc != SPCONV_OK) {
         if (h->arena) cudaFreeAsync(h->arena, s);
@@ -169,7 +181,7 @@ int spconv_subm_forward_ex(spconv_map_t map, const void* feats_dev, const void* 
     if (!weights_dev) return SPCONV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (use_tensor_path(c_in, c_out, dtype, feats_dev, out_dev) && aligned(weights_dev, 2)) {
-        const size_t need = tc_pack_bytes(c_in, c_out);
+        const size_t need = tc_pack_bytes(c_in, c_out, map->taps);
         if (map->wspace_bytes < need) {
             if (map->wspace) cudaFreeAsync(map->wspace, s);
             map->wspace = nullptr;
@@ -181,7 +193,7 @@ int spconv_subm_forward_ex(spconv_map_t map, const void* feats_dev, const void* 
             }
             map->wspace_bytes = need;
         }
-        SPCONV_CHECK(tc_pack_weights(weights_dev, c_in, c_out, map->wspace, s));
+        SPCONV_CHECK(tc_pack_weights(weights_dev, c_in, c_out, map->taps, map->wspace, s));
         return tc_forward(map, feats_dev, map->wspace, out_dev, c_in, c_out, e, s);
     }
     return simt_forward(map, feats_dev, weights_dev, out_dev, c_in, c_out, dtype, e, s);
@@ -189,9 +201,16 @@ int spconv_subm_forward_ex(spconv_map_t map, const void* feats_dev, const void* 
 
 int spconv_wpack_create(const void* weights_dev, int32_t c_in, int32_t c_out, int32_t dtype, void* stream,
                         spconv_wpack_t* out_wpack) {
+    return spconv_wpack_create_ex(weights_dev, 3, c_in, c_out, dtype, stream, out_wpack);
+}
+
+int spconv_wpack_create_ex(const void* weights_dev, int32_t kernel_size, int32_t c_in, int32_t c_out,
+                           int32_t dtype, void* stream, spconv_wpack_t* out_wpack) {
     reset_launch_count();
     if (!out_wpack) return SPCONV_ERR_INVALID_ARG;
     *out_wpack = nullptr;
+    if (kernel_size != 3 && kernel_size != 5) return SPCONV_ERR_UNSUPPORTED;
+    const int32_t taps = kernel_size * kernel_size * kernel_size;
     if (!weights_dev || c_in < 1 || c_out < 1 || c_in > 65536 || c_out > 65536) return SPCONV_ERR_INVALID_ARG;
     if (dtype != SPCONV_BF16 && dtype != SPCONV_FP32) return SPCONV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -200,10 +219,11 @@ int spconv_wpack_create(const void* weights_dev, int32_t c_in, int32_t c_out, in
     w->c_in = c_in;
     w->c_out = c_out;
     w->dtype = dtype;
+    w->taps = taps;
     w->stream = s;
     w->tensor_path = (dtype == SPCONV_BF16 && tc_supported(c_in, c_out)) ? 1 : 0;
     const size_t es = dtype == SPCONV_FP32 ? 4 : 2;
-    w->bytes = w->tensor_path ? tc_pack_bytes(c_in, c_out) : static_cast<size_t>(kTaps) * c_in * c_out * es;
+    w->bytes = w->tensor_path ? tc_pack_bytes(c_in, c_out, taps) : static_cast<size_t>(taps) * c_in * c_out * es;
     if (pool_alloc(&w->data, w->bytes, s) != cudaSuccess) {
         cudaGetLastError();
         delete w;
@@ -212,7 +232,7 @@ int spconv_wpack_create(const void* weights_dev, int32_t c_in, int32_t c_out, in
     int rc = SPCONV_OK;
     if (w->tensor_path) {
         w->n_tile = tc_tile_n(c_out);
-        rc = tc_pack_weights(weights_dev, c_in, c_out, w->data, s);
+        rc = tc_pack_weights(weights_dev, c_in, c_out, taps, w->data, s);
     } else {
         rc = cuda_status(cudaMemcpyAsync(w->data, weights_dev, w->bytes, cudaMemcpyDeviceToDevice, s));
     }
@@ -235,6 +255,7 @@ int spconv_subm_forward_packed_ex(spconv_map_t map, const void* feats_dev, spcon
     reset_launch_count();
     if (!wpack) return SPCONV_ERR_INVALID_ARG;
     SPCONV_CHECK(check_forward_args(map, feats_dev, out_dev, wpack->c_in, wpack->c_out, wpack->dtype));
+    if (wpack->taps != map->taps) return SPCONV_ERR_INVALID_ARG;
     Epilogue e;
     SPCONV_CHECK(check_epilogue(map, epi, out_dev, wpack->c_out, wpack->dtype, &e));
     if (map->n == 0) return SPCONV_OK;
@@ -272,6 +293,8 @@ int spconv_map_info(spconv_map_t map, spconv_map_info_t* info) {
     std::memcpy(info->shape, map->shape, sizeof(info->shape));
     info->batch_size = map->batch;
     info->gemm = map->gemm;
+    info->kernel_size = map->kernel_size;
+    info->groups = map->groups;
     return SPCONV_OK;
 }
 
@@ -281,15 +304,16 @@ int spconv_map_export(spconv_map_t map, int32_t* nbr_dev, uint32_t* mask_dev, in
     if (!map) return SPCONV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t n = map->n;
+    const size_t V = static_cast<size_t>(map->taps), G = static_cast<size_t>(map->groups);
     if (n > 0 && nbr_dev)
-        SPCONV_CHECK_CUDA(cudaMemcpy2DAsync(nbr_dev, kTaps * sizeof(int32_t), map->nbr, kNbrStride * sizeof(int32_t),
-                                            kTaps * sizeof(int32_t), static_cast<size_t>(n), cudaMemcpyDeviceToDevice, s));
+        SPCONV_CHECK_CUDA(cudaMemcpy2DAsync(nbr_dev, V * sizeof(int32_t), map->nbr, map->nbr_stride * sizeof(int32_t),
+                                            V * sizeof(int32_t), static_cast<size_t>(n), cudaMemcpyDeviceToDevice, s));
     if (n > 0 && mask_dev)
-        SPCONV_CHECK_CUDA(cudaMemcpyAsync(mask_dev, map->mask, n * sizeof(uint32_t), cudaMemcpyDeviceToDevice, s));
+        SPCONV_CHECK_CUDA(cudaMemcpyAsync(mask_dev, map->mask, G * n * sizeof(uint32_t), cudaMemcpyDeviceToDevice, s));
     if (n > 0 && perm_dev)
-        SPCONV_CHECK_CUDA(cudaMemcpyAsync(perm_dev, map->perm, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+        SPCONV_CHECK_CUDA(cudaMemcpyAsync(perm_dev, map->perm, G * n * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
     if (tap_off_dev)
-        SPCONV_CHECK_CUDA(cudaMemcpyAsync(tap_off_dev, map->tap_off, (kTaps + 1) * sizeof(int32_t),
+        SPCONV_CHECK_CUDA(cudaMemcpyAsync(tap_off_dev, map->tap_off, (V + 1) * sizeof(int32_t),
                                           cudaMemcpyDeviceToDevice, s));
     if (in_rows_dev || out_rows_dev) {
         spconv_map_info_t info;

@@ -7,7 +7,10 @@
 
 namespace spconv {
 
-constexpr int kTaps = 27;
+constexpr int kTaps = 27;           // taps of a 3x3x3 kernel
+constexpr int kMaxKernel = 5;       // largest kernel size (5x5x5, 125 taps)
+constexpr int kMaxTaps = kMaxKernel * kMaxKernel * kMaxKernel;
+constexpr int kMaxGroupTaps = 27;   // taps of one offset group (mask bits, GEMM index buffer)
 constexpr int kMaxDevices = 64;    // per-device one-time settings are kept for device ids below this
 constexpr int kTileRows = 128;      // rows per output tile (tensor-core M)
 constexpr int kNbrStride = 32;      // padded width of the internal kernel-map rows
@@ -59,20 +62,27 @@ struct MapHandle {
     int32_t bit_order = 0;
     int32_t gemm = 0;         // spconv_gemm_t used by the bf16 forward (TILE_UNION or TAP_MAJOR)
     int32_t key_bits = 0;
+    int32_t kernel_size = 3;  // K: the kernel is K x K x K
+    int32_t taps = kTaps;     // V = K^3
+    int32_t groups = 1;       // G offset groups of V / G consecutive taps, each with its own row order
+    int32_t group_taps = kTaps;     // V / G
+    int32_t nbr_stride = kNbrStride;   // width of an nbr row (>= V, a multiple of 4)
     // device arrays
     int32_t* status = nullptr;     // [1]
-    int32_t* nbr = nullptr;        // [n][kNbrStride], original row order
-    uint32_t* mask = nullptr;      // [n]
-    int32_t* perm = nullptr;       // [n_pad] (rows >= n: -1)
-    int32_t* tap_count = nullptr;  // [27]
-    int32_t* tap_pos = nullptr;    // [27] key bit of each tap
-    int32_t* tap_off = nullptr;    // [28]
-    int32_t* in_rows = nullptr;    // [27 n]
-    int32_t* out_rows = nullptr;   // [27 n]
-    int32_t* gtab = nullptr;       // [27][n_pad]: nbr[perm[s]][k] or -1
-    uint32_t* tile_union = nullptr;  // [n_tiles]
-    int32_t* tile_order = nullptr;   // [n_tiles], tiles by descending union size
-    int32_t* seg_off = nullptr;      // [27][n_tiles] pair offset of (tap, tile)
+    // (with G groups: masks, orders, unions and tile orders per group, group-major)
+    int32_t* nbr = nullptr;        // [n][nbr_stride], original row order
+    uint32_t* mask = nullptr;      // [G][n] bit j: tap g V/G + j present
+    int32_t* perm = nullptr;       // one group: [n_pad] (rows >= n: -1); G groups: [G][n]
+    int32_t* tap_count = nullptr;  // [V]
+    int32_t* tap_pos = nullptr;    // [V] key bit of each tap within its group
+    int32_t* tap_off = nullptr;    // [V + 1]
+    int32_t* in_rows = nullptr;    // [V n]
+    int32_t* out_rows = nullptr;   // [V n]
+    int32_t* gtab = nullptr;       // [V][n_pad]: nbr[perm_g[s]][k] or -1 (g the group of tap k)
+    uint32_t* tile_union = nullptr;  // [G][n_tiles]
+    int32_t* tile_order = nullptr;   // [G][n_tiles], each group's tiles by descending union size
+    int32_t* seg_off = nullptr;      // [V][n_tiles] pair offset of (tap, tile)
+    int32_t* tile_nonempty = nullptr;  // [G] tiles with a nonempty union (the first ones of each tile order)
     int32_t* totals = nullptr;       // [2]: pairs, sum of union sizes
     void* arena = nullptr;           // one allocation holding the arrays above
     size_t arena_bytes = 0;
@@ -86,6 +96,7 @@ struct MapHandle {
 
 struct WPackHandle {
     int32_t c_in = 0, c_out = 0, dtype = 0;
+    int32_t taps = kTaps;      // kernel volume the weights are for
     int32_t tensor_path = 0;   // 1: tcgen05 shared-memory image, 0: row-major copy for SIMT
     int32_t n_tile = 0;        // output channels per tensor-core tile
     int32_t k_chunks = 0;      // 64-wide input-channel chunks
@@ -108,14 +119,16 @@ struct Epilogue {
 
 // ---- map building (map.cu) -----------------------------------------------
 int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* opt);
+// K != 3 or more than one offset group (map_groups.cu)
+int build_map_grouped(MapHandle* h, const int32_t* coords, const spconv_options_t* opt);
 int derive_shape(const int32_t* coords, int64_t n, cudaStream_t stream, int32_t shape[3],
                  int32_t* batch);
 
 // ---- tensor-core GEMM (gemm_tc.cu) ------------------------------------------
 bool tc_supported(int32_t c_in, int32_t c_out);
 int tc_tile_n(int32_t c_out);
-size_t tc_pack_bytes(int32_t c_in, int32_t c_out);
-int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, void* dst, cudaStream_t s);
+size_t tc_pack_bytes(int32_t c_in, int32_t c_out, int32_t taps);
+int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, int32_t taps, void* dst, cudaStream_t s);
 int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
                int32_t c_out, const Epilogue& epi, cudaStream_t s);
 

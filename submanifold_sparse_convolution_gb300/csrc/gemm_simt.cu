@@ -3,7 +3,7 @@
 //
 // One thread per (row, group of VEC output channels), rows visited in the
 // mask-sorted order so that a warp's rows share their taps.  Each output
-// element is a plain FMA chain in fp32 over taps 0..26 and input channels in
+// element is a plain FMA chain in fp32 over taps 0..V-1 and input channels in
 // ascending order, skipping absent taps ("Sparse convolution in FP32":
 // weights read as [offset][input][output] with consecutive output channels per
 // thread), so the result does not depend on the launch shape.  The optional
@@ -31,9 +31,8 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return
 template <typename T, int VEC>
 __global__ void __launch_bounds__(256) k_simt(const T* __restrict__ feats, const T* __restrict__ w,
                                               T* __restrict__ out, const int32_t* __restrict__ perm,
-                                              const int32_t* __restrict__ nbr,
-                                              const uint32_t* __restrict__ mask, int64_t n, int c_in,
-                                              int c_out, Epilogue epi) {
+                                              const int32_t* __restrict__ nbr, int taps, int stride,
+                                              int64_t n, int c_in, int c_out, Epilogue epi) {
     const int groups = (c_out + VEC - 1) / VEC;
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t s = idx / groups;
@@ -41,13 +40,13 @@ __global__ void __launch_bounds__(256) k_simt(const T* __restrict__ feats, const
     const int g = static_cast<int>(idx % groups);
     const int o0 = g * VEC;
     const int32_t r = perm[s];
-    const uint32_t m = mask[r];
     float acc[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) acc[v] = 0.0f;
-    for (int k = 0; k < kTaps; ++k) {
-        if (!((m >> k) & 1u)) continue;
-        const int32_t j = nbr[static_cast<int64_t>(r) * kNbrStride + k];
+    const int32_t* nrow = nbr + static_cast<int64_t>(r) * stride;
+    for (int k = 0; k < taps; ++k) {
+        const int32_t j = nrow[k];
+        if (j < 0) continue;
         const T* f = feats + static_cast<int64_t>(j) * c_in;
         const T* wk = w + static_cast<int64_t>(k) * c_in * c_out + o0;
         for (int c = 0; c < c_in; ++c) {
@@ -83,11 +82,11 @@ int launch(const MapHandle* h, const void* feats, const void* w, void* out, int3
     if (vec == 4)
         k_simt<T, 4><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
             static_cast<const T*>(feats), static_cast<const T*>(w), static_cast<T*>(out), h->perm, h->nbr,
-            h->mask, h->n, c_in, c_out, epi);
+            h->taps, h->nbr_stride, h->n, c_in, c_out, epi);
     else
         k_simt<T, 1><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
             static_cast<const T*>(feats), static_cast<const T*>(w), static_cast<T*>(out), h->perm, h->nbr,
-            h->mask, h->n, c_in, c_out, epi);
+            h->taps, h->nbr_stride, h->n, c_in, c_out, epi);
     count_launch();
     return cuda_status(cudaGetLastError());
 }

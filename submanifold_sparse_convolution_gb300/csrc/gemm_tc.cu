@@ -95,7 +95,23 @@ struct TcParams {
     int32_t n_nb;                 // c_out / n_tile
     Epilogue epi;                 // applied to each fp32 sum before the rounding
     int32_t epi_on;               // epi.active()
+    // offset groups: this launch covers the group's taps [k0, k0 + taps of the
+    // union bits); gtab, tile_union, tile_order and perm point at the group's
+    // slices, the packed weights hold taps_w taps per output block
+    int32_t k0, taps_w;
+    int32_t mode;                 // kModeStore, or the partial-sum modes of a grouped forward
+    float* ws;                    // [n][c_out] fp32 partial sums of the groups before the last
+    const int32_t* tiles_dev;     // device count of the leading tiles of tile_order to visit, or null (all)
 };
+
+// Output modes.  One group: the tile's sum, rounded once, to out.  G groups,
+// one launch each, ws zeroed first: every group but the centre one adds its
+// sums to ws, visiting only the tiles whose union is not empty; the centre
+// group (every row has the centre tap, so every tile is visited) goes last,
+// adds ws to its own sums and rounds once to out.  Items with no tap are
+// never scheduled: two of them in a row could stall the stage ring, whose
+// MMA waits span consecutive items.
+enum : int32_t { kModeStore = 0, kModeWsAdd = 2, kModeWsFinish = 3 };
 
 template <int NTMAX>
 struct TcConfig {
@@ -231,6 +247,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
     // items are numbered tap by tap: lane k < 27 holds t_excl, the number of
     // 128-pair tiles of taps before k, and the item count is derived here.
     int n_items = p.n_items;
+    if (p.tiles_dev && warp == kSchedWarp) n_items = *p.tiles_dev * p.n_nb;
     int32_t t_excl = 0, t_off = 0, t_end = 0;
     if (TM && warp == kSchedWarp) {
         t_off = lane <= kTaps ? p.tap_off[lane] : 0;
@@ -412,7 +429,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                         if (part == 0) {
                             ptx::mbar_arrive_expect_tx(gfull, b_bytes);
                             const uint8_t* src =
-                                p.wpack + (static_cast<int64_t>(nb * kTaps + k) * p.k_chunks + kc) * b_bytes;
+                                p.wpack + (static_cast<int64_t>(nb * p.taps_w + p.k0 + k) * p.k_chunks + kc) * b_bytes;
                             ptx::bulk_copy_g2s(b_smem, src, b_bytes, gfull);
                         } else {
                             ptx::mbar_arrive(gfull);
@@ -526,6 +543,8 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
             }
             const int it = m_item[r];
             const int tile = m_tile[r];
+            // a tile none of whose rows has a tap of this group: no MMA ran, the sums are zero
+            const bool none = m_uni[r] == 0u;
             // the row this thread writes: tile-union, perm of the sorted position;
             // tap-major, the pair's output row
             int32_t orig = -1;
@@ -545,16 +564,50 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                 break;
             }
             ptx::tc_fence_after();
-            __nv_bfloat16* dst_row =
-                (!TM && orig >= 0) ? p.out + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile : nullptr;
+            const bool to_out = p.mode == kModeStore || p.mode == kModeWsFinish;
+            __nv_bfloat16* dst_row = (!TM && orig >= 0 && to_out)
+                                         ? p.out + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile
+                                         : nullptr;
+            float* ws_row = (!TM && orig >= 0 && p.mode != kModeStore)
+                                ? p.ws + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile
+                                : nullptr;
             const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(buf * NTMAX);
             // n_tile is a multiple of 16; columns go 32 at a time (two loads per wait)
             for (int c = 0; c < p.n_tile; c += 32) {
                 const bool two = c + 16 < p.n_tile;
                 uint32_t v[32];
-                ptx::tmem_ld_32x32b_x16_at(t_addr + c, v);
-                if (two) ptx::tmem_ld_32x32b_x16_at(t_addr + c + 16, v + 16);
-                ptx::tmem_ld_wait();
+                if (!none) {
+                    ptx::tmem_ld_32x32b_x16_at(t_addr + c, v);
+                    if (two) ptx::tmem_ld_32x32b_x16_at(t_addr + c + 16, v + 16);
+                    ptx::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0u;
+                }
+                if (ws_row) {
+                    // partial sums of a grouped forward (one thread per row: no races)
+                    float4* w4 = reinterpret_cast<float4*>(ws_row + c);
+#pragma unroll
+                    for (int h = 0; h < 8; ++h) {
+                        if (h >= 4 && !two) break;
+                        float4 a = make_float4(__uint_as_float(v[4 * h]), __uint_as_float(v[4 * h + 1]),
+                                               __uint_as_float(v[4 * h + 2]), __uint_as_float(v[4 * h + 3]));
+                        if (none && p.mode == kModeWsAdd) continue;
+                        const float4 b = w4[h];
+                        a.x += b.x;
+                        a.y += b.y;
+                        a.z += b.z;
+                        a.w += b.w;
+                        if (p.mode == kModeWsAdd) {
+                            w4[h] = a;
+                        } else {
+                            v[4 * h] = __float_as_uint(a.x);
+                            v[4 * h + 1] = __float_as_uint(a.y);
+                            v[4 * h + 2] = __float_as_uint(a.z);
+                            v[4 * h + 3] = __float_as_uint(a.w);
+                        }
+                    }
+                }
                 if (TM) {
                     if (orig >= 0) {
                         float* dacc = p.acc + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile + c;
@@ -603,9 +656,9 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
 // W[k][kc*64 .. kc*64+63][nb*n_tile + n] (zero past c_in), its 16-byte chunk c
 // stored at chunk position c ^ (n & 7) -- the K-major 128-byte-swizzled
 // shared-memory layout that the MMA reads directly after one bulk copy.
-__global__ void k_pack_weights(const __nv_bfloat16* __restrict__ w, int c_in, int c_out, int n_tile,
+__global__ void k_pack_weights(const __nv_bfloat16* __restrict__ w, int c_in, int c_out, int taps, int n_tile,
                                int k_chunks, int n_nb, uint4* __restrict__ dst) {
-    const int64_t total = static_cast<int64_t>(n_nb) * kTaps * k_chunks * n_tile * 8;
+    const int64_t total = static_cast<int64_t>(n_nb) * taps * k_chunks * n_tile * 8;
     for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         // idx enumerates (nb, k, kc, c, n) with n fastest so reads of W rows coalesce
@@ -616,8 +669,8 @@ __global__ void k_pack_weights(const __nv_bfloat16* __restrict__ w, int c_in, in
         q /= 8;
         const int kc = static_cast<int>(q % k_chunks);
         q /= k_chunks;
-        const int k = static_cast<int>(q % kTaps);
-        const int nb = static_cast<int>(q / kTaps);
+        const int k = static_cast<int>(q % taps);
+        const int nb = static_cast<int>(q / taps);
         const int o = nb * n_tile + n;
         uint32_t h[4];
 #pragma unroll
@@ -631,7 +684,7 @@ __global__ void k_pack_weights(const __nv_bfloat16* __restrict__ w, int c_in, in
             v.y = b;
             h[e / 2] = *reinterpret_cast<uint32_t*>(&v);
         }
-        const int64_t blk = (static_cast<int64_t>(nb) * kTaps + k) * k_chunks + kc;
+        const int64_t blk = (static_cast<int64_t>(nb) * taps + k) * k_chunks + kc;
         const int64_t off16 = blk * n_tile * 8 + static_cast<int64_t>(n) * 8 + (c ^ (n & 7));
         dst[off16] = make_uint4(h[0], h[1], h[2], h[3]);
     }
@@ -714,21 +767,21 @@ bool tc_supported(int32_t c_in, int32_t c_out) {
     return c_in > 0 && c_in % 8 == 0 && c_in <= 65536 && tc_tile_n(c_out) > 0;
 }
 
-size_t tc_pack_bytes(int32_t c_in, int32_t c_out) {
+size_t tc_pack_bytes(int32_t c_in, int32_t c_out, int32_t taps) {
     const int nt = tc_tile_n(c_out);
     const int kcs = (c_in + BK - 1) / BK;
-    return static_cast<size_t>(c_out / nt) * kTaps * kcs * nt * 128;
+    return static_cast<size_t>(c_out / nt) * taps * kcs * nt * 128;
 }
 
-int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, void* dst, cudaStream_t s) {
+int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, int32_t taps, void* dst, cudaStream_t s) {
     const int nt = tc_tile_n(c_out);
     const int kcs = (c_in + BK - 1) / BK;
     const int n_nb = c_out / nt;
-    const int64_t total = static_cast<int64_t>(n_nb) * kTaps * kcs * nt * 8;
+    const int64_t total = static_cast<int64_t>(n_nb) * taps * kcs * nt * 8;
     const int threads = 256;
     const int64_t blocks64 = (total + threads - 1) / threads;
     const unsigned blocks = static_cast<unsigned>(blocks64 < 65535 * 16 ? blocks64 : 65535 * 16);
-    k_pack_weights<<<blocks, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(w), c_in, c_out, nt, kcs,
+    k_pack_weights<<<blocks, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(w), c_in, c_out, taps, nt, kcs,
                                               n_nb, static_cast<uint4*>(dst));
     count_launch();
     return cuda_status(cudaGetLastError());
@@ -759,17 +812,18 @@ int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, in
     p.n_nb = c_out / p.n_tile;
     p.epi = epi;
     p.epi_on = epi.active() ? 1 : 0;
+    p.k0 = 0;
+    p.taps_w = h->taps;
+    p.mode = kModeStore;
+    p.ws = nullptr;
+    p.tiles_dev = nullptr;
     const int64_t items = h->n_tiles * p.n_nb;
     if (items > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
     p.n_items = static_cast<int32_t>(items);
     const int sms = num_sms();
-    if (h->gemm != SPCONV_GEMM_TAP_MAJOR) return launch_tc_n<false>(p, p.n_items < sms ? p.n_items : sms, s);
-
-    // tap-major: zeroed fp32 sums, the GEMM adds every pair's product, one rounding pass
-    // (at most 27n pairs: the item count fits in int32 when 27n/128 * n_nb does)
-    if (static_cast<int64_t>(kTaps) * h->n / BM * p.n_nb > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
-    const size_t need = static_cast<size_t>(h->n) * c_out * sizeof(float);
-    if (h->acc_bytes < need) {
+    const int grid = p.n_items < sms ? p.n_items : sms;
+    auto ensure_acc = [&](size_t need) -> int {
+        if (h->acc_bytes >= need) return SPCONV_OK;
         if (h->acc) cudaFreeAsync(h->acc, s);
         h->acc = nullptr;
         h->acc_bytes = 0;
@@ -779,7 +833,37 @@ int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, in
             return SPCONV_ERR_OOM;
         }
         h->acc_bytes = need;
+        return SPCONV_OK;
+    };
+    if (h->groups > 1) {
+        // offset groups ("Offset-group partitioning", "Sparse convolution in FP32"):
+        // one tile-union pass per group over that group's row order, the
+        // partial sums carried in fp32 between the passes, one rounding at the end
+        const size_t ws_bytes = static_cast<size_t>(h->n) * c_out * sizeof(float);
+        SPCONV_CHECK(ensure_acc(ws_bytes));
+        p.ws = static_cast<float*>(h->acc);
+        SPCONV_CHECK_CUDA(cudaMemsetAsync(p.ws, 0, ws_bytes, s));
+        const int centre = (h->groups - 1) / 2;   // the group of the centre tap
+        for (int j = 0; j < h->groups; ++j) {
+            const int g = j < centre ? j : (j + 1 < h->groups ? j + 1 : centre);
+            p.k0 = g * h->group_taps;
+            p.gtab = h->gtab + static_cast<int64_t>(p.k0) * h->n_pad;
+            p.tile_union = h->tile_union + g * h->n_tiles;
+            p.tile_order = h->tile_order + g * h->n_tiles;
+            p.perm = h->perm + g * h->n;
+            p.mode = g == centre ? kModeWsFinish : kModeWsAdd;
+            p.tiles_dev = g == centre ? nullptr : h->tile_nonempty + g;
+            SPCONV_CHECK(launch_tc_n<false>(p, grid, s));
+        }
+        return SPCONV_OK;
     }
+    if (h->gemm != SPCONV_GEMM_TAP_MAJOR) return launch_tc_n<false>(p, grid, s);
+
+    // tap-major: zeroed fp32 sums, the GEMM adds every pair's product, one rounding pass
+    // (at most 27n pairs: the item count fits in int32 when 27n/128 * n_nb does)
+    if (static_cast<int64_t>(kTaps) * h->n / BM * p.n_nb > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
+    const size_t need = static_cast<size_t>(h->n) * c_out * sizeof(float);
+    SPCONV_CHECK(ensure_acc(need));
     p.acc = static_cast<float*>(h->acc);
     SPCONV_CHECK_CUDA(cudaMemsetAsync(p.acc, 0, need, s));
     SPCONV_CHECK(launch_tc_n<true>(p, sms, s));

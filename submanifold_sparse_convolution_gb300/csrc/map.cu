@@ -470,6 +470,7 @@ int derive_shape(const int32_t* coords, int64_t n, cudaStream_t stream, int32_t 
 }
 
 int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* opt) {
+    if (h->kernel_size != 3 || h->groups != 1) return build_map_grouped(h, coords, opt);
     cudaStream_t s = h->stream;
     const int64_t n = h->n;
     const int64_t T = (n + kTileRows - 1) / kTileRows;

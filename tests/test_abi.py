@@ -60,13 +60,21 @@ def test_host_side_argument_errors(lib):
     # n > 0 with null or misaligned coordinates
     assert lib.spconv_build_map(None, 5, sp, 1, 3, None, None, ctypes.byref(h)) == -1
     assert lib.spconv_build_map(ctypes.c_void_p(8), 5, sp, 1, 3, None, None, ctypes.byref(h)) == -1
-    # kernel size other than 3
-    assert lib.spconv_build_map(None, 0, sp, 1, 5, None, None, ctypes.byref(h)) == -2
+    # kernel sizes other than 3 and 5
+    for k in (1, 2, 4, 7):
+        assert lib.spconv_build_map(None, 0, sp, 1, k, None, None, ctypes.byref(h)) == -2
     # bad options
     for bad in [(7, 0, 0, 0, 0), (0, 3, 0, 0, 0), (0, 0, -1, 0, 0), (0, 0, 0, 4, 0), (0, 0, 0, 0, 3),
-                (0, 0, 0, 0, -1)]:
+                (0, 0, 0, 0, -1), (0, 0, 0, 0, 0, -1)]:
         opt = _native.Options(*bad)
         assert lib.spconv_build_map(None, 0, sp, 1, 3, ctypes.byref(opt), None, ctypes.byref(h)) == -1
+    # offset groups: 1 or K; more than one only with the MULTI pipeline and the TILE_UNION forward
+    for k, extra in [(3, (0, 0, 0, 0, 0, 2)), (5, (0, 0, 0, 0, 0, 1)), (5, (0, 0, 0, 3, 0, 0)),
+                     (5, (0, 0, 0, 1, 0, 5)), (3, (0, 0, 0, 0, 2, 3))]:
+        opt = _native.Options(*extra)
+        assert lib.spconv_build_map(None, 0, sp, 1, k, ctypes.byref(opt), None, ctypes.byref(h)) == -2
+    assert lib.spconv_wpack_create_ex(None, 5, 16, 16, 0, None, ctypes.byref(h)) == -1
+    assert lib.spconv_wpack_create_ex(ctypes.c_void_p(256), 7, 16, 16, 0, None, ctypes.byref(h)) == -2
     # null handles everywhere else
     assert lib.spconv_subm_forward(None, None, None, None, 16, 16, 0, None) == -1
     assert lib.spconv_subm_forward_packed(None, None, None, None, None) == -1

@@ -461,6 +461,185 @@ def test_epilogue_argument_errors():
     assert sc.map_status(m) == 0
 
 
+# ---------------------------------------------------------------------------
+# kernel size 5 and offset groups
+# ---------------------------------------------------------------------------
+
+def oracle_groups(coords, shape, batch, K, G, calibrated=True):
+    nbr = oracle.kernel_map(coords, shape, batch, K)
+    m, _, p = oracle.group_orders(nbr, G, calibrated)
+    tap_off, ins, outs = oracle.pair_lists(nbr, p)
+    if G == 1:
+        m, p = m[0], p[0]
+    return dict(nbr=nbr, mask=m, perm=p, tap_off=tap_off, in_rows=ins, out_rows=outs)
+
+
+def weights_k(K, c_in, c_out, seed, dtype=torch.bfloat16):
+    rng = np.random.default_rng(seed)
+    w = rng.standard_normal((K ** 3, c_in, c_out)) / np.sqrt(K ** 3 * c_in)
+    return torch.from_numpy(w.astype(np.float32)).to(dtype)
+
+
+GROUP_CASES = [(3, 3), (5, 5)]
+GROUP_SMALL = [(1, 1, (4, 4, 4), 1), (2, 7, (5, 5, 5), 1), (3, 128, (8, 8, 8), 1), (4, 129, (8, 8, 8), 2),
+               (5, 1500, (14, 13, 12), 2), (6, 4000, (30, 30, 6), 1)]
+
+
+@pytest.mark.parametrize("K,G", GROUP_CASES)
+@pytest.mark.parametrize("seed,n,shape,batch", GROUP_SMALL)
+@pytest.mark.parametrize("mapper", ["dense", "sorted"])
+@pytest.mark.parametrize("bit_order", ["calibrated", "plain"])
+def test_map_groups_small(K, G, seed, n, shape, batch, mapper, bit_order):
+    wl = S.random_cloud(700 + seed, n, shape=shape, batch_size=batch)
+    m = sc.build_map(wl.coords.cuda(), shape, batch, kernel_size=K, groups=G, mapper=mapper, bit_order=bit_order)
+    assert sc.map_status(m) == 0
+    info = sc.map_info(m)
+    assert info["kernel_size"] == K and info["groups"] == G and info["mapper"] == mapper
+    ex = sc.map_export(m)
+    ref = oracle_groups(wl.coords.numpy(), shape, batch, K, G, bit_order == "calibrated")
+    assert_map_equal(ex, ref)
+    assert info["pairs"] == ref["tap_off"][-1]
+
+
+@pytest.mark.parametrize("K,G", GROUP_CASES)
+def test_map_groups_dense_and_sorted_agree_on_outdoor(K, G):
+    wl = S.make_workload("outdoor")
+    ref = oracle_groups(wl.coords.numpy(), wl.spatial_shape, wl.batch_size, K, G)
+    for mapper in ("sorted", "dense"):
+        m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, wl.batch_size, kernel_size=K, groups=G,
+                         mapper=mapper, dense_max_cells=1 << 30)
+        assert sc.map_status(m) == 0
+        assert_map_equal(sc.map_export(m), ref)
+
+
+FWD_GROUP = [(64, 64, torch.bfloat16), (128, 128, torch.bfloat16), (32, 256, torch.bfloat16),
+             (16, 16, torch.bfloat16), (5, 7, torch.bfloat16), (16, 16, torch.float32)]
+
+
+@pytest.mark.parametrize("K,G", GROUP_CASES)
+@pytest.mark.parametrize("c_in,c_out,dtype", FWD_GROUP)
+def test_forward_groups(K, G, c_in, c_out, dtype):
+    wl = S.random_cloud(800 + c_in + K, 2500, shape=(16, 16, 16), batch_size=2, c_in=c_in, c_out=c_out)
+    f = wl.feats.to(dtype)
+    w = weights_k(K, c_in, c_out, 801 + c_out, dtype)
+    m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, wl.batch_size, kernel_size=K, groups=G)
+    out = sc.subm_forward(m, f.cuda(), w.cuda())
+    assert sc.map_status(m) == 0
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size, K)
+    ref = oracle.conv_f64(nbr, f.double().numpy(), w.double().numpy())
+    (check_fp32 if dtype == torch.float32 else check_bf16)(out, ref)
+    # packed weights: the same bits; a pack for another kernel size is refused
+    wp = sc.wpack_create(w.cuda())
+    assert torch.equal(sc.subm_forward_packed(m, f.cuda(), wp), out)
+    other = sc.wpack_create(weights_k(8 - K, c_in, c_out, 5, dtype).cuda())
+    with pytest.raises(ValueError):
+        sc.subm_forward_packed(m, f.cuda(), other)
+    rc = sc.library().spconv_subm_forward_packed(m.handle, f.cuda().data_ptr(), other.handle,
+                                                 out.data_ptr(), None)
+    assert rc == -1
+
+
+@pytest.mark.parametrize("K,G", GROUP_CASES)
+def test_forward_groups_epilogue(K, G):
+    # the epilogue is applied once, by the last group's pass, to every row
+    wl = S.random_cloud(811 + K, 3000, shape=(18, 18, 18), c_in=64, c_out=64)
+    w = weights_k(K, 64, 64, 812)
+    scale, bias, res = epilogue_inputs(wl.n, 64, torch.bfloat16, dict(scale=1, bias=1, residual=1), 813)
+    m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, kernel_size=K, groups=G)
+    out = sc.subm_forward(m, wl.feats.cuda(), w.cuda(), scale=scale.cuda(), bias=bias.cuda(),
+                          residual=res.cuda(), relu=True)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1, K)
+    ref = oracle.epilogue_f64(oracle.conv_f64(nbr, wl.feats.double().numpy(), w.double().numpy()),
+                              scale.double().numpy(), bias.double().numpy(), res.double().numpy(), True)
+    check_bf16(out, ref)
+
+
+def test_three_groups_match_one_group():
+    # K = 3 in one group or in three: the same sums up to fp32 rounding order
+    wl = S.random_cloud(821, 6000, shape=(24, 24, 24), c_in=128, c_out=128)
+    f, w = wl.feats.cuda(), wl.weights[0].cuda()
+    m1 = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1)
+    m3 = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, groups=3)
+    a, b = sc.subm_forward(m1, f, w), sc.subm_forward(m3, f, w)
+    torch.testing.assert_close(a.float(), b.float(), rtol=2e-2, atol=2e-2)
+    i1, i3 = sc.map_info(m1), sc.map_info(m3)
+    assert i1["pairs"] == i3["pairs"]
+    # each group's tiles cover only its own taps: fewer executed tile-taps than 3 x one group
+    assert i3["tile_taps"] < 3 * i1["tile_taps"]
+
+
+@pytest.mark.parametrize("name", ["outdoor", "stage"])
+def test_k5_workload(name):
+    wl = S.make_workload(name)
+    K = 5
+    w = weights_k(K, wl.c_in, wl.c_out, 831)
+    m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, wl.batch_size, kernel_size=K)
+    out = sc.subm_forward(m, wl.feats.cuda(), w.cuda())
+    assert sc.map_status(m) == 0
+    ex = sc.map_export(m)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size, K)
+    assert np.array_equal(ex["nbr"].cpu().numpy(), nbr)
+    ref = oracle_groups(wl.coords.numpy(), wl.spatial_shape, wl.batch_size, K, K)
+    assert_map_equal(ex, ref)
+    rows = sample_rows(wl.n, 1500, 832)
+    check_bf16(out[torch.from_numpy(rows).long().cuda()],
+               oracle.conv_f64(nbr, wl.feats.double().numpy(), w.double().numpy(), rows=rows))
+
+
+@pytest.mark.parametrize("K,G", GROUP_CASES)
+def test_groups_with_empty_tiles(K, G):
+    # voxels on even x only: no row has a dx = +-1 neighbour, so those groups
+    # have no tile to visit at all, and a sparse tail gives runs of empty tiles
+    rng = np.random.default_rng(851)
+    lattice = np.array([(0, x, y, z) for x in range(0, 24, 2) for y in range(10) for z in range(10)], np.int32)
+    tail = np.array([(0, 40 + 6 * i, 3 * (i % 3), 5) for i in range(300)], np.int32)
+    coords = np.concatenate([lattice, tail])[rng.permutation(lattice.shape[0] + 300)]
+    shape = (40 + 6 * 300, 10, 10)
+    f = torch.from_numpy(rng.standard_normal((coords.shape[0], 64)).astype(np.float32)).to(torch.bfloat16)
+    w = weights_k(K, 64, 64, 852)
+    m = sc.build_map(torch.from_numpy(coords).cuda(), shape, 1, kernel_size=K, groups=G)
+    out = sc.subm_forward(m, f.cuda(), w.cuda(), relu=True)
+    assert sc.map_status(m) == 0
+    ref_map = oracle_groups(coords, shape, 1, K, G)
+    assert_map_equal(sc.map_export(m), ref_map)
+    nbr = ref_map["nbr"]
+    assert (nbr[:, K * K * ((K - 1) // 2 - 1):K * K * ((K - 1) // 2)] < 0).all()   # the dx = -1 group is empty
+    check_bf16(out, oracle.epilogue_f64(oracle.conv_f64(nbr, f.double().numpy(), w.double().numpy()), relu=True))
+
+
+def test_groups_argument_errors():
+    wl = S.random_cloud(841, 300, shape=(8, 8, 8))
+    c = wl.coords.cuda()
+    for kw in (dict(kernel_size=5, groups=1), dict(kernel_size=3, groups=2), dict(kernel_size=7),
+               dict(kernel_size=5, pipeline="wide"), dict(kernel_size=5, pipeline="fused"),
+               dict(kernel_size=3, groups=3, gemm="tap_major"), dict(kernel_size=5, gemm="tap_major")):
+        with pytest.raises(sc.SpconvError) as e:
+            sc.build_map(c, wl.spatial_shape, 1, **kw)
+        assert e.value.code == -2, kw
+    with pytest.raises(sc.SpconvError) as e:
+        sc.build_map(c, wl.spatial_shape, 1, groups=-1)
+    assert e.value.code == -1
+
+
+def test_groups_duplicate_and_range_errors():
+    for mapper in ("dense", "sorted"):
+        dup = torch.tensor([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=torch.int32).cuda()
+        m = sc.build_map(dup, (8, 8, 8), 1, kernel_size=5, mapper=mapper)
+        assert sc.map_status(m) == -5
+        bad = torch.tensor([[0, 1, 1, 1], [0, 8, 2, 2]], dtype=torch.int32).cuda()
+        m = sc.build_map(bad, (8, 8, 8), 1, kernel_size=5, mapper=mapper)
+        assert sc.map_status(m) == -6
+
+
+def test_groups_empty_input():
+    c = torch.empty((0, 4), dtype=torch.int32, device="cuda")
+    m = sc.build_map(c, (4, 4, 4), 1, kernel_size=5)
+    assert sc.map_status(m) == 0 and sc.map_info(m)["pairs"] == 0
+    out = sc.subm_forward(m, torch.empty((0, 16), dtype=torch.bfloat16, device="cuda"),
+                          weights_k(5, 16, 16, 1).cuda())
+    assert out.shape == (0, 16)
+
+
 def test_launch_count_reported():
     wl = S.random_cloud(51, 3000, shape=(16, 16, 16), c_in=64, c_out=64)
     m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="dense", pipeline="fused")
