@@ -169,7 +169,7 @@ def run_ours(args, rank, world, device):
 
     build_mod.build()
     peaks = load_peaks()
-    wl = S.make_workload(args.workload)
+    wl = S.make_workload(args.workload, kernel_size=args.kernel_size)
     L = wl.layers
     coords = wl.coords.to(device)
     feats = wl.feats.to(device)
@@ -199,8 +199,12 @@ def run_ours(args, rank, world, device):
             x = y
         return y
 
+    def build(c):
+        return sc.build_map(c, wl.spatial_shape, wl.batch_size, kernel_size=args.kernel_size,
+                            groups=args.groups, gemm=args.gemm, pipeline=args.pipeline)
+
     def step():
-        m = sc.build_map(coords, wl.spatial_shape, wl.batch_size, gemm=args.gemm, pipeline=args.pipeline)
+        m = build(coords)
         launches[0] += sc.last_launch_count()
         mark()
         y = layers(m, feats)
@@ -208,7 +212,7 @@ def run_ours(args, rank, world, device):
         return y
 
     # map statistics (one synchronising call, outside any timing)
-    m0 = sc.build_map(coords, wl.spatial_shape, wl.batch_size, gemm=args.gemm, pipeline=args.pipeline)
+    m0 = build(coords)
     if sc.map_status(m0) != 0:
         raise RuntimeError("map build reported " + sc.status_string(sc.map_status(m0)))
     info = sc.map_info(m0)
@@ -267,7 +271,7 @@ def run_ours(args, rank, world, device):
     clocks = sampler.summary(t0, t1) if sampler else None
 
     map_launches = None
-    m1 = sc.build_map(coords, wl.spatial_shape, wl.batch_size, pipeline=args.pipeline)
+    m1 = build(coords)
     map_launches = sc.last_launch_count()
     m1.destroy()
 
@@ -288,7 +292,7 @@ def run_ours(args, rank, world, device):
         with torch.cuda.stream(side):
             feats_d2.copy_(feats_h, non_blocking=True)
             feats_ready.record(side)
-        m = sc.build_map(coords_d2, wl.spatial_shape, wl.batch_size, gemm=args.gemm, pipeline=args.pipeline)
+        m = build(coords_d2)
         stream.wait_event(feats_ready)
         y = layers(m, feats_d2)
         out_h.copy_(y, non_blocking=True)
@@ -308,22 +312,27 @@ def run_ours(args, rank, world, device):
     gemm_avg_s = statistics.mean(gemm_ms) * 1e-3
     gemm_tflops = useful_flops_layer / gemm_avg_s / 1e12
     n, P = wl.n, pairs
-    map_bytes = 16 * n + 108 * n + 8 * n + 8 * P
+    V, G = info["kernel_size"] ** 3, info["groups"]
+    # coordinates read, nbr [n][V] written, masks and row order per group, pair lists
+    map_bytes = 16 * n + 4 * V * n + 8 * G * n + 8 * P
     map_avg_s = statistics.mean(map_ms) * 1e-3
     kernel_name = (f"k_tc_gemm<{256 if wl.c_out > 256 else (128 if wl.c_out > 64 else 64)}, "
                    f"{'tap-major' if tap_major else 'tile-union'}>")
-    traffic = ncu_traffic("k_tc_gemm", args.workload)
+    plain = info["kernel_size"] == 3 and G == 1
+    traffic = ncu_traffic("k_tc_gemm", args.workload if plain else f"{args.workload}-k{info['kernel_size']}-g{G}")
+    pages_us = PAGES_US.get(args.workload) if plain else None
     out = {
         "metric": METRIC, "value": round(us_per_layer, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": False,
         "scaling": "weak",
-        "vs_baseline": round(us_per_layer / PAGES_US[args.workload], 4) if args.workload in PAGES_US else None,
+        "vs_baseline": round(us_per_layer / pages_us, 4) if pages_us else None,
         "vs_baseline_note": ("value / the pages' µs on an AMD gfx950 for the same N and C "
-                             "(context: other hardware, real scans)") if args.workload in PAGES_US else None,
+                             "(context: other hardware, real scans)") if pages_us else None,
         "dtype": "bf16", "data": DATA,
         "config": {"workload": f"{args.workload}: N={wl.n}, C_in={wl.c_in}, C_out={wl.c_out}, "
                                f"layers={L}, batch={wl.batch_size}, grid={'x'.join(map(str, wl.spatial_shape))}",
+                   "kernel_size": info["kernel_size"], "groups": G,
                    "pairs": P, "pairs_per_row": round(P / n, 3), "mapper": info["mapper"], "pipeline": info["pipeline"], "gemm": info["gemm"],
                    "tile_taps": info["tile_taps"], "l2": "flushed (256 MB write) before every timed step",
                    "weights": "packed once per layer (outside the step)",
@@ -335,6 +344,7 @@ def run_ours(args, rank, world, device):
                      "peak": peaks["bf16"], "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / peaks["bf16"], 4), "traffic": traffic,
                      "peak_source": f"{peaks['source']} bf16 dense (burst, kernel timed alone)",
+                     "launches_per_layer": G,
                      "executed_over_useful": round(executed_rows / P, 3)},
         "roofline_map": {"bound": "hbm", "achieved": round(map_bytes / map_avg_s / 1e9, 2),
                          "peak": peaks["hbm"], "unit": "GB/s",
@@ -352,14 +362,15 @@ def run_ours(args, rank, world, device):
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def prepare_oracle(workload):
+def prepare_oracle(workload, kernel_size=3, groups=0):
     import oracle
     from submanifold_sparse_convolution_gb300 import synthetic as S
 
     oracle.build()
-    wl = S.make_workload(workload)
+    wl = S.make_workload(workload, kernel_size=kernel_size)
+    G = groups if groups > 0 else (1 if kernel_size == 3 else kernel_size)
     return dict(wl=wl, c=wl.coords.numpy(), f=wl.feats.double().numpy(),
-                w=wl.weights[0].double().numpy())
+                w=wl.weights[0].double().numpy(), K=kernel_size, G=G)
 
 
 def time_oracle(prep, budget_s):
@@ -368,9 +379,8 @@ def time_oracle(prep, budget_s):
 
     wl, c, f, w = prep["wl"], prep["c"], prep["f"], prep["w"]
     t = time.perf_counter()
-    nbr = oracle.kernel_map(c, wl.spatial_shape, wl.batch_size)
-    m = oracle.masks(nbr)
-    p = oracle.perm(oracle.sort_keys(m, oracle.tap_order(m, True)))
+    nbr = oracle.kernel_map(c, wl.spatial_shape, wl.batch_size, prep["K"])
+    _, _, p = oracle.group_orders(nbr, prep["G"], True)
     oracle.pair_lists(nbr, p)
     t_map = time.perf_counter() - t
     # calibrate the conv sample on 256 rows, then size it to the budget
@@ -384,18 +394,18 @@ def time_oracle(prep, budget_s):
     oracle.conv_f64(nbr, f, w, rows=rows)
     t_conv = (time.perf_counter() - t) / k * wl.n
     us_per_layer = (t_map + wl.layers * t_conv) / wl.layers * 1e6
-    sample = (f"full kernel map, masks, order and pair lists of N={wl.n}; fp64 conv on {k} of "
-              f"{wl.n} rows (evenly spaced) scaled to N; {wl.layers} layer(s)")
+    sample = (f"full kernel map (K={prep['K']}), masks, order and pair lists ({prep['G']} group(s)) of "
+              f"N={wl.n}; fp64 conv on {k} of {wl.n} rows (evenly spaced) scaled to N; {wl.layers} layer(s)")
     return us_per_layer, oracle.max_threads(), sample
 
 
-def cpu_baseline(workload, budget_s):
-    us, cores, sample = time_oracle(prepare_oracle(workload), budget_s)
+def cpu_baseline(workload, budget_s, kernel_size=3, groups=0):
+    us, cores, sample = time_oracle(prepare_oracle(workload, kernel_size, groups), budget_s)
     return {"value": round(us, 3), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
 
 
 def run_reference(args):
-    prep = prepare_oracle(args.workload)
+    prep = prepare_oracle(args.workload, args.kernel_size, args.groups)
     wl = prep["wl"]
     # the whole run stays within about two minutes of oracle work
     budget = max(0.05, min(args.ref_budget, 120.0 / (args.steps + args.warmup)))
@@ -413,7 +423,8 @@ def run_reference(args):
         "data": DATA,
         "config": {"workload": f"{args.workload}: N={wl.n}, C_in={wl.c_in}, C_out={wl.c_out}, "
                                f"layers={wl.layers}, batch={wl.batch_size}, "
-                               f"grid={'x'.join(map(str, wl.spatial_shape))}"},
+                               f"grid={'x'.join(map(str, wl.spatial_shape))}",
+                   "kernel_size": prep["K"], "groups": prep["G"]},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -433,6 +444,10 @@ def main():
                     help="kernel-map build pipeline (auto: wide when the keys fit it)")
     ap.add_argument("--gemm", default="auto", choices=["auto", "tile_union", "tap_major"],
                     help="work decomposition of the bf16 GEMM")
+    ap.add_argument("--kernel-size", type=int, default=3, choices=[3, 5],
+                    help="K of the K x K x K kernel (the workloads are quoted for 3)")
+    ap.add_argument("--groups", type=int, default=0,
+                    help="offset groups (0: 1 for K = 3, K for K = 5; or K)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle conv work for the cpu_baseline leg (0 disables)")
     ap.add_argument("--ref-budget", type=float, default=2.0,
@@ -460,7 +475,7 @@ def main():
         torch.distributed.destroy_process_group()
     if rank == 0 and out is not None:
         if world == 1 and args.cpu_budget > 0:
-            out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget)
+            out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget, args.kernel_size, args.groups)
         print(json.dumps(out), flush=True)
 
 

@@ -193,13 +193,13 @@ def bf16_normal(rng: np.random.Generator, shape, std: float = 1.0) -> torch.Tens
     return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
 
 
-def weights_std(c_in: int) -> float:
-    return 1.0 / float(np.sqrt(27.0 * c_in))
+def weights_std(c_in: int, taps: int = 27) -> float:
+    return 1.0 / float(np.sqrt(float(taps) * c_in))
 
 
-def make_weights(rng, c_in, c_out) -> torch.Tensor:
-    """``[27, C_in, C_out]`` bf16, std 1/sqrt(27*C_in) (fan-in scaling)."""
-    return bf16_normal(rng, (27, c_in, c_out), weights_std(c_in))
+def make_weights(rng, c_in, c_out, taps: int = 27) -> torch.Tensor:
+    """``[taps, C_in, C_out]`` bf16, std 1/sqrt(taps*C_in) (fan-in scaling)."""
+    return bf16_normal(rng, (taps, c_in, c_out), weights_std(c_in, taps))
 
 
 # ---------------------------------------------------------------------------
@@ -252,14 +252,17 @@ _CHANNELS = {"tiny": (16, 16, 1), "outdoor": (128, 128, 1), "deep": (512, 512, 1
              "large": (128, 128, 1), "stage": (64, 64, 6)}
 
 
-def make_workload(name: str, seed: Optional[int] = None, layers: Optional[int] = None) -> Workload:
-    """Workload ``name`` with its coordinates, bf16 features and per-layer weights."""
+def make_workload(name: str, seed: Optional[int] = None, layers: Optional[int] = None,
+                  kernel_size: int = 3) -> Workload:
+    """Workload ``name`` with its coordinates, bf16 features and per-layer
+    weights ([K^3, C_in, C_out] for kernel size K; the coordinates and
+    features do not depend on K)."""
     coords, shape, batch, rng = make_coords(name, seed)
     c_in, c_out, n_layers = _CHANNELS[name]
     if layers is not None:
         n_layers = layers
     feats = bf16_normal(rng, (coords.shape[0], c_in))
-    weights = [make_weights(rng, c_in, c_out) for _ in range(n_layers)]
+    weights = [make_weights(rng, c_in, c_out, kernel_size ** 3) for _ in range(n_layers)]
     return Workload(name=name, coords=torch.from_numpy(coords), spatial_shape=shape,
                     batch_size=batch, c_in=c_in, c_out=c_out, feats=feats,
                     weights=weights, seed=BASE_SEED + CONFIG_NAMES.index(name) + 1
