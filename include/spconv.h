@@ -59,9 +59,13 @@ typedef enum {
 typedef enum { SPCONV_BF16 = 0, SPCONV_FP32 = 1 } spconv_dtype_t;
 
 typedef enum {
-    SPCONV_MAPPER_AUTO = 0,   /* dense grid iff padded cells <= dense_max_cells, else sorted keys */
+    SPCONV_MAPPER_AUTO = 0,   /* dense grid iff padded cells <= dense_max_cells, else HASH when
+                                 the WIDE pipeline builds the map, else SORTED                   */
     SPCONV_MAPPER_DENSE = 1,  /* presence grid over the padded bounding box                       */
-    SPCONV_MAPPER_SORTED = 2  /* sorted 64-bit keys + binary search, memory O(N)                   */
+    SPCONV_MAPPER_SORTED = 2, /* sorted 64-bit keys + binary search, memory O(N)                   */
+    SPCONV_MAPPER_HASH = 3    /* the same packed keys in an open-addressing hash table, one probe
+                                 per tap; memory O(N).  WIDE pipeline only (other pipelines:
+                                 SPCONV_ERR_UNSUPPORTED), one offset group                         */
 } spconv_mapper_t;
 
 typedef enum {

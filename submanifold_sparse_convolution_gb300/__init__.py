@@ -21,7 +21,7 @@ __all__ = ["SpconvError", "Map", "WPack", "build_map", "subm_forward", "wpack_cr
            "subm_forward_packed", "map_status", "map_info", "map_export", "map_destroy",
            "last_launch_count", "status_string", "MAPPERS", "BIT_ORDERS", "PIPELINES", "GEMMS", "library"]
 
-MAPPERS = {"auto": 0, "dense": 1, "sorted": 2}
+MAPPERS = {"auto": 0, "dense": 1, "sorted": 2, "hash": 3}
 PIPELINES = {"auto": 0, "fused": 1, "multi": 2, "wide": 3}
 GEMMS = {"auto": 0, "tile_union": 1, "tap_major": 2}
 BIT_ORDERS = {"calibrated": 0, "plain": 1}
@@ -273,7 +273,7 @@ def map_info(m: Map) -> dict:
     info = _native.MapInfo()
     _check(library().spconv_map_info(m.handle, ctypes.byref(info)), "spconv_map_info")
     return dict(n=info.n, pairs=info.pairs, n_tiles=info.n_tiles, tile_taps=info.tile_taps,
-                mapper={1: "dense", 2: "sorted"}.get(info.mapper, str(info.mapper)),
+                mapper={1: "dense", 2: "sorted", 3: "hash"}.get(info.mapper, str(info.mapper)),
                 pipeline={1: "fused", 2: "multi", 3: "wide"}.get(info.pipeline, str(info.pipeline)),
                 key_bits=info.key_bits, shape=tuple(info.shape), batch_size=info.batch_size,
                 gemm={1: "tile_union", 2: "tap_major"}.get(info.gemm, str(info.gemm)),

@@ -114,7 +114,7 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
     if (kernel_size != 3 && kernel_size != 5) return SPCONV_ERR_UNSUPPORTED;
     if (batch_size < 0) return SPCONV_ERR_INVALID_ARG;
     if (opt) {
-        if (opt->mapper < SPCONV_MAPPER_AUTO || opt->mapper > SPCONV_MAPPER_SORTED) return SPCONV_ERR_INVALID_ARG;
+        if (opt->mapper < SPCONV_MAPPER_AUTO || opt->mapper > SPCONV_MAPPER_HASH) return SPCONV_ERR_INVALID_ARG;
         if (opt->bit_order != SPCONV_ORDER_CALIBRATED && opt->bit_order != SPCONV_ORDER_PLAIN)
             return SPCONV_ERR_INVALID_ARG;
         if (opt->dense_max_cells < 0) return SPCONV_ERR_INVALID_ARG;

@@ -498,10 +498,12 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
     const bool cells_overflow = static_cast<double>(B) * (X + 2) * (Y + 2) * (Z + 2) > 9.0e18;
     int mapper = opt ? opt->mapper : SPCONV_MAPPER_AUTO;
     const int64_t dense_max = (opt && opt->dense_max_cells > 0) ? opt->dense_max_cells : (int64_t(1) << 24);
-    if (mapper == SPCONV_MAPPER_AUTO) mapper = (!cells_overflow && cells <= dense_max) ? SPCONV_MAPPER_DENSE : SPCONV_MAPPER_SORTED;
-    if (mapper == SPCONV_MAPPER_SORTED && key_bits > 63) return SPCONV_ERR_UNSUPPORTED;
+    // AUTO: the dense grid on small boxes, else packed keys -- in a hash table
+    // when the whole-GPU pipeline builds the map, else sorted (decided below)
+    const bool auto_keys = mapper == SPCONV_MAPPER_AUTO && !(!cells_overflow && cells <= dense_max);
+    if (mapper == SPCONV_MAPPER_AUTO) mapper = auto_keys ? SPCONV_MAPPER_SORTED : SPCONV_MAPPER_DENSE;
+    if ((mapper == SPCONV_MAPPER_SORTED || mapper == SPCONV_MAPPER_HASH) && key_bits > 63) return SPCONV_ERR_UNSUPPORTED;
     if (mapper == SPCONV_MAPPER_DENSE && (cells_overflow || cells > (int64_t(1) << 34))) return SPCONV_ERR_UNSUPPORTED;
-    h->mapper = mapper;
     h->bit_order = opt ? opt->bit_order : SPCONV_ORDER_CALIBRATED;
     h->gemm = (opt && opt->gemm == SPCONV_GEMM_TAP_MAJOR) ? SPCONV_GEMM_TAP_MAJOR : SPCONV_GEMM_TILE_UNION;
 
@@ -509,7 +511,12 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
     // launch when the rows fit, else the plain one kernel per step
     const int row_bits = std::max(1, bit_length(static_cast<uint64_t>(n > 0 ? n - 1 : 0)));
     const int want = opt ? opt->pipeline : SPCONV_PIPELINE_AUTO;
-    const bool packs = mapper != SPCONV_MAPPER_SORTED || key_bits + row_bits <= 64;
+    const bool packs = mapper == SPCONV_MAPPER_DENSE || key_bits + row_bits <= 64;
+    const bool hash_ok = n <= kWideMaxRows && key_bits + row_bits <= 64 &&
+                         (want == SPCONV_PIPELINE_AUTO || want == SPCONV_PIPELINE_WIDE);
+    if (auto_keys && hash_ok) mapper = SPCONV_MAPPER_HASH;
+    if (mapper == SPCONV_MAPPER_HASH && !hash_ok) return SPCONV_ERR_UNSUPPORTED;
+    h->mapper = mapper;
     const bool wide_ok = n <= kWideMaxRows && packs &&
                          (mapper != SPCONV_MAPPER_SORTED || wide_key_passes(key_bits) <= kWideKeyPassesMax);
     bool fused_ok = n <= kFusedMaxRows && packs;
@@ -556,6 +563,8 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
         }
     }
     if (mapper == SPCONV_MAPPER_DENSE) add(static_cast<size_t>(cells), 4);   // presence grid
+    const int table_log2 = mapper == SPCONV_MAPPER_HASH ? hash_table_log2(n) : 0;
+    if (mapper == SPCONV_MAPPER_HASH) add(size_t(1) << table_log2, 8);       // hash table
     void* arena = nullptr;
     if (pool_alloc(&arena, bytes, s) != cudaSuccess) {
         cudaGetLastError();
@@ -589,6 +598,8 @@ int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* 
         wa.tickets = carve<int32_t>(p, kWideCounters);
         wa.look = carve<uint64_t>(p, parts * kWideBins);
         wa.grid = mapper == SPCONV_MAPPER_DENSE ? carve<int32_t>(p, static_cast<size_t>(cells)) : nullptr;
+        wa.table = mapper == SPCONV_MAPPER_HASH ? carve<uint64_t>(p, size_t(1) << table_log2) : nullptr;
+        wa.table_log2 = table_log2;
         h->perm = perm_a;
         if (n == 0) {
             SPCONV_CHECK_CUDA(cudaMemsetAsync(h->status, 0, 256, s));

@@ -442,6 +442,7 @@ int build_map_grouped(MapHandle* h, const int32_t* coords, const spconv_options_
     const double cells_d = static_cast<double>(B) * (X + 2 * r) * (Y + 2 * r) * (Z + 2 * r);
     const int64_t cells = cells_d > 9.0e18 ? 0 : static_cast<int64_t>(B) * L.gsb;
     int mapper = opt ? opt->mapper : SPCONV_MAPPER_AUTO;
+    if (mapper == SPCONV_MAPPER_HASH) return SPCONV_ERR_UNSUPPORTED;
     const int64_t dense_max = (opt && opt->dense_max_cells > 0) ? opt->dense_max_cells : (int64_t(1) << 24);
     if (mapper == SPCONV_MAPPER_AUTO)
         mapper = (cells_d <= 9.0e18 && cells <= dense_max) ? SPCONV_MAPPER_DENSE : SPCONV_MAPPER_SORTED;

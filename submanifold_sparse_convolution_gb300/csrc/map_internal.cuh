@@ -68,6 +68,14 @@ constexpr int kWideBarrierInts = 33;                // a grid barrier: 32 arriva
 // the tickets, then a grid barrier per sort pass
 constexpr int kWideCounters = kWideTickets + kWideTickets * kWideBarrierInts;
 constexpr int64_t kWideMaxRows = int64_t(1) << 26;
+// Hash mapper table: the smallest power of two >= kHashSlotsPerRow * n
+// entries, in buckets of kHashBucket (one 32-byte sector).  At a load of at
+// most 1/16 a bucket is almost never full, so nearly every probe ends in the
+// first bucket: one round trip per lookup.
+constexpr int kHashSlotsPerRow = 16;
+constexpr int kHashBucket = 4;
+constexpr int kHashMinLog2 = 11;
+int hash_table_log2(int64_t n);
 
 struct WideArgs {
     const int4* coords;
@@ -81,6 +89,9 @@ struct WideArgs {
     int64_t gsb, gsx, gsy, cells;         // dense grid layout
     int64_t goff[kTaps];
     int32_t* grid;
+    // hash mapper: open-addressing table of (key << row_bits | row), 0 = empty
+    uint64_t* table;       // [1 << table_log2]
+    int table_log2;
     // scratch
     uint64_t* va;          // [n] packed (key << row_bits | row), ping-pong
     uint64_t* vb;          // [n]

@@ -213,6 +213,11 @@ __global__ void __launch_bounds__(WT) k_wide_clear(const WideArgs a) {
     for (int64_t i = i0; i < kWideCounters; i += stride) a.tickets[i] = 0;
     if (i0 < kTaps) a.tap_count[i0] = 0;
     if (i0 < 2) a.totals[i0] = 0;
+    if (a.mapper == SPCONV_MAPPER_HASH) {
+        ulonglong2* t2 = reinterpret_cast<ulonglong2*>(a.table);
+        const int64_t slots2 = (int64_t(1) << a.table_log2) / 2;
+        for (int64_t i = i0; i < slots2; i += stride) t2[i] = make_ulonglong2(0ull, 0ull);
+    }
     if (a.mapper == SPCONV_MAPPER_DENSE) {
         int4* g4 = reinterpret_cast<int4*>(a.grid);
         const int64_t c4 = a.cells / 4;
@@ -284,6 +289,149 @@ __global__ void __launch_bounds__(WT) k_wide_keys(const WideArgs a, const KeyDig
         if (x) atomicAdd(a.gh + p * kWideBins + b, x);
     }
     if (err) atomicOr(a.status, err);
+}
+
+// ---------------------------------------------------------------------------
+// hash mapper: the packed coordinate keys in an open-addressing table of
+// 4-slot buckets (bucketed linear probing), then 27 probes per row.  The
+// packed key's arithmetic is the sorted mapper's (neighbour key = key +
+// packed(d)); only the lookup structure differs: a probe is one 32-byte
+// bucket read instead of a binary search after a sort.  Within a bucket the
+// slots fill in order and never empty again, so a lookup that meets an empty
+// slot without a match knows the key is absent; only a full bucket sends it
+// on to the next one.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t hash_bucket(uint64_t key, int log2_buckets) {
+    return (key * 0x9E3779B97F4A7C15ull) >> (64 - log2_buckets);   // multiplicative (Fibonacci) hashing
+}
+
+__device__ __forceinline__ uint64_t packed_key(int4 q, const WideArgs& a) {
+    return (((((static_cast<uint64_t>(q.x) << a.wx) | static_cast<uint64_t>(q.y + 1)) << a.wy) |
+             static_cast<uint64_t>(q.z + 1))
+            << a.wz) |
+           static_cast<uint64_t>(q.w + 1);
+}
+
+__global__ void __launch_bounds__(WT) k_wide_hash_insert(const WideArgs a) {
+    pdl_trigger();
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * WT + threadIdx.x;
+    const bool valid = i < a.n;
+    const int4 q = valid ? a.coords[i] : make_int4(-1, -1, -1, -1);
+    const bool ok = valid && coord_ok(q, a.shape, a.batch);
+    const uint64_t key = ok ? packed_key(q, a) : 0ull;
+    pdl_wait();   // the table is cleared
+    int32_t err = (valid && !ok) ? kStatusRange : 0;
+    if (ok) {
+        // key >= 1 (every field is offset by one), so an entry is never 0 (empty)
+        const uint64_t entry = (key << a.row_bits) | static_cast<uint64_t>(i);
+        const int lb = a.table_log2 - 2;
+        const uint64_t bmask = (uint64_t(1) << lb) - 1;
+        uint64_t b = hash_bucket(key, lb);
+        bool placed = false;
+        for (uint64_t probe = 0; probe <= bmask && !placed; ++probe, b = (b + 1) & bmask) {
+            for (int j = 0; j < kHashBucket; ++j) {
+                const unsigned long long prev = atomicCAS(
+                    reinterpret_cast<unsigned long long*>(a.table + b * kHashBucket + j), 0ull,
+                    static_cast<unsigned long long>(entry));
+                if (prev == 0ull || (prev >> a.row_bits) == key) {   // placed, or the same voxel twice
+                    if (prev != 0ull) err |= kStatusDuplicate;
+                    placed = true;
+                    break;
+                }
+            }
+        }
+        if (!placed) err |= kStatusInternal;   // a full table: cannot happen at load <= 1/16
+    }
+    if (err) atomicOr(a.status, err);
+}
+
+// Looks key kk up in bucket b (slots lo.x, lo.y, hi.x, hi.y): 1 found (*row
+// set), 0 absent, -1 the bucket is full without it (go on to the next).
+__device__ __forceinline__ int bucket_find(ulonglong2 lo, ulonglong2 hi, uint64_t kk, int row_bits, int32_t* row) {
+    const uint64_t s[4] = {lo.x, lo.y, hi.x, hi.y};
+    const uint64_t row_mask = (uint64_t(1) << row_bits) - 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (s[j] == 0ull) return 0;
+        if ((s[j] >> row_bits) == kk) {
+            *row = static_cast<int32_t>(s[j] & row_mask);
+            return 1;
+        }
+    }
+    return -1;
+}
+
+__global__ void __launch_bounds__(WT) k_wide_hash_lookup(const WideArgs a) {
+    __shared__ int32_t cnt[kTaps];
+    const int t = threadIdx.x, lane = t & 31;
+    if (t < kTaps) cnt[t] = 0;
+    __syncthreads();
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * WT + t;
+    const bool valid = i < a.n;
+    const int4 q = valid ? a.coords[i] : make_int4(-1, -1, -1, -1);
+    const bool ok = valid && coord_ok(q, a.shape, a.batch);
+    const uint64_t key = ok ? packed_key(q, a) : 0ull;
+    pdl_wait();   // every key is in the table
+    pdl_trigger();
+    int32_t v[kNbrStride];
+#pragma unroll
+    for (int k = 0; k < kNbrStride; ++k) v[k] = -1;
+    const int lb = a.table_log2 - 2;
+    const uint64_t bmask = (uint64_t(1) << lb) - 1;
+    const ulonglong2* tab = reinterpret_cast<const ulonglong2*>(a.table);
+    // one dx plane (9 taps) per round: its 9 bucket reads in flight together;
+    // the rare lookups that meet a full bucket go on, all of the warp's in
+    // the same extra round
+#pragma unroll
+    for (int k0 = 0; k0 < kTaps; k0 += 9) {
+        ulonglong2 lo[9], hi[9];
+        uint32_t pending = 0;
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+            if (ok) {
+                const uint64_t b = hash_bucket(key + a.koff[k0 + j], lb);
+                lo[j] = __ldcg(tab + 2 * b);
+                hi[j] = __ldcg(tab + 2 * b + 1);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+            if (ok && bucket_find(lo[j], hi[j], key + a.koff[k0 + j], a.row_bits, &v[k0 + j]) < 0) pending |= 1u << j;
+        }
+        for (uint64_t r = 1; __any_sync(0xFFFFFFFFu, pending != 0u) && r <= bmask; ++r) {
+#pragma unroll
+            for (int j = 0; j < 9; ++j) {
+                if ((pending >> j) & 1u) {
+                    const uint64_t b = (hash_bucket(key + a.koff[k0 + j], lb) + r) & bmask;
+                    lo[j] = __ldcg(tab + 2 * b);
+                    hi[j] = __ldcg(tab + 2 * b + 1);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 9; ++j) {
+                if (((pending >> j) & 1u) &&
+                    bucket_find(lo[j], hi[j], key + a.koff[k0 + j], a.row_bits, &v[k0 + j]) >= 0)
+                    pending &= ~(1u << j);
+            }
+        }
+    }
+    uint32_t m = 0;
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) m |= (v[k] >= 0 ? 1u : 0u) << k;
+    if (valid) {
+        int4* dst = reinterpret_cast<int4*>(a.nbr + i * kNbrStride);
+#pragma unroll
+        for (int qq = 0; qq < kNbrStride / 4; ++qq)
+            dst[qq] = make_int4(v[4 * qq], v[4 * qq + 1], v[4 * qq + 2], v[4 * qq + 3]);
+        a.mask[i] = m;
+    }
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) {
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
+        if (lane == 0 && b) atomicAdd(&cnt[k], __popc(b));
+    }
+    __syncthreads();
+    if (t < kTaps && cnt[t]) atomicAdd(a.tap_count + t, cnt[t]);
 }
 
 // ---------------------------------------------------------------------------
@@ -870,6 +1018,12 @@ int launch_pdl(Kernel kernel, unsigned grid, unsigned block, cudaStream_t s, boo
 
 int wide_key_passes(int key_bits) { return (key_bits + kDigitBitsWide - 1) / kDigitBitsWide; }
 
+int hash_table_log2(int64_t n) {
+    int l = kHashMinLog2;   // >= 2: whole buckets
+    while ((int64_t(1) << l) < kHashSlotsPerRow * n) ++l;
+    return l;
+}
+
 int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     const int64_t n = a.n;
     const unsigned parts = static_cast<unsigned>((n + kWideKeysPerCta - 1) / kWideKeysPerCta);
@@ -888,7 +1042,9 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
         cap_pass[dev] = resident_ctas(k_wide_pass, WT, sms);
     }
     const bool pass_ticket = static_cast<int64_t>(parts) > cap_pass[dev];
-    int64_t clear_blocks = a.mapper == SPCONV_MAPPER_DENSE ? (a.cells / 4 + WT * 8 - 1) / (WT * 8) : 8;
+    int64_t clear_blocks = a.mapper == SPCONV_MAPPER_DENSE ? (a.cells / 4 + WT * 8 - 1) / (WT * 8)
+                         : a.mapper == SPCONV_MAPPER_HASH ? ((int64_t(1) << a.table_log2) / 2 + WT * 8 - 1) / (WT * 8)
+                                                          : 8;
     if (clear_blocks > 4 * sms) clear_blocks = 4 * sms;
     SPCONV_CHECK(launch_pdl(k_wide_clear, static_cast<unsigned>(clear_blocks < 1 ? 1 : clear_blocks), WT, s, false, a));
     auto pass = [&](const uint64_t* in, uint64_t* out, int shift, int width, const int32_t* gh, int ticket) {
@@ -913,7 +1069,10 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
         pa.status = a.status;
         return launch_pdl(k_wide_pass, parts, WT, s, true, pa);
     };
-    if (a.mapper == SPCONV_MAPPER_SORTED) {
+    if (a.mapper == SPCONV_MAPPER_HASH) {
+        SPCONV_CHECK(launch_pdl(k_wide_hash_insert, row_blocks, WT, s, true, a));
+        SPCONV_CHECK(launch_pdl(k_wide_hash_lookup, row_blocks, WT, s, true, a));
+    } else if (a.mapper == SPCONV_MAPPER_SORTED) {
         const int passes = wide_key_passes(a.key_bits);
         if (passes > kWideKeyPassesMax) return SPCONV_ERR_UNSUPPORTED;
         KeyDigits kd = {};

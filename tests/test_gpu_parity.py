@@ -99,8 +99,46 @@ def test_map_workloads(name, pipeline):
     ex = sc.map_export(m)
     assert_map_equal(ex, ref)
     info = ex["info"]
-    assert info["mapper"] == ("dense" if name in ("tiny", "deep") else "sorted")
+    # AUTO: the dense grid on the small boxes; keys elsewhere, hashed by the whole-GPU pipeline
+    assert info["mapper"] == ("dense" if name in ("tiny", "deep") else ("hash" if pipeline == "auto" else "sorted"))
     assert info["pipeline"] == ("wide" if pipeline == "auto" else pipeline)
+
+
+@pytest.mark.parametrize("name", ["outdoor", "large", "stage"])
+def test_map_workloads_wide_sorted(name):
+    # the sorted mapper on the whole-GPU pipeline (AUTO hashes these workloads)
+    coords, shape, batch, _ = S.make_coords(name)
+    wl = S.Workload(name, torch.from_numpy(coords), shape, batch, 1, 1, None, [], 0)
+    ex = sc.map_export(build(wl, "sorted", pipeline="wide"))
+    assert_map_equal(ex, oracle_map(coords, shape, batch))
+    assert ex["info"]["mapper"] == "sorted" and ex["info"]["pipeline"] == "wide"
+
+
+@pytest.mark.parametrize("seed,n,shape,batch", SMALL)
+@pytest.mark.parametrize("bit_order", ["calibrated", "plain"])
+def test_map_small_hash(seed, n, shape, batch, bit_order):
+    wl = S.random_cloud(seed, n, shape=shape, batch_size=batch)
+    m = build(wl, "hash", bit_order, "wide")
+    ref = oracle_map(wl.coords.numpy(), shape, batch, bit_order == "calibrated")
+    assert_map_equal(sc.map_export(m), ref)
+    assert sc.map_info(m)["mapper"] == "hash"
+
+
+def test_map_hash_many_rows_and_unsupported_pipelines():
+    """300k rows in 3 frames (a 2M-slot table): the hash and sorted mappers give the same map;
+    the hash mapper exists only in the whole-GPU pipeline."""
+    wl = S.random_cloud(63, 300000, shape=(200, 200, 60), batch_size=3)
+    a = sc.map_export(build(wl, "hash", pipeline="wide"))
+    b = sc.map_export(build(wl, "sorted", pipeline="wide"))
+    for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
+        assert torch.equal(a[key], b[key]), key
+    for pipeline in ("fused", "multi"):
+        with pytest.raises(sc.SpconvError) as e:
+            sc.build_map(wl.coords.cuda(), wl.spatial_shape, 3, mapper="hash", pipeline=pipeline)
+        assert e.value.code == -2
+    with pytest.raises(sc.SpconvError) as e:
+        sc.build_map(wl.coords.cuda(), wl.spatial_shape, 3, mapper="hash", kernel_size=5)
+    assert e.value.code == -2
 
 
 @pytest.mark.parametrize("mapper", ["sorted", "dense"])
@@ -150,9 +188,10 @@ def test_dense_and_sorted_mappers_agree(name):
     coords, shape, batch, _ = S.make_coords(name)
     wl = S.Workload(name, torch.from_numpy(coords), shape, batch, 1, 1, None, [], 0)
     a = sc.map_export(build(wl, "dense"))
-    b = sc.map_export(build(wl, "sorted"))
-    for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
-        assert torch.equal(a[key], b[key]), key
+    for mapper in ("sorted", "hash"):
+        b = sc.map_export(build(wl, mapper))
+        for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
+            assert torch.equal(a[key], b[key]), (mapper, key)
 
 
 def test_derived_shape_and_batch():
@@ -181,11 +220,12 @@ def test_empty_input():
 @pytest.mark.parametrize("pipeline", ["fused", "multi", "wide"])
 def test_duplicate_and_range_errors(pipeline):
     dup = torch.tensor([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=torch.int32, device="cuda")
-    for mapper in ("dense", "sorted"):
+    mappers = ("dense", "sorted", "hash") if pipeline == "wide" else ("dense", "sorted")
+    for mapper in mappers:
         m = sc.build_map(dup, (4, 4, 4), 1, mapper=mapper, pipeline=pipeline)
         assert sc.map_status(m) == -5
     bad = torch.tensor([[0, 1, 1, 1], [0, 4, 0, 0]], dtype=torch.int32, device="cuda")
-    for mapper in ("dense", "sorted"):
+    for mapper in mappers:
         m = sc.build_map(bad, (4, 4, 4), 1, mapper=mapper, pipeline=pipeline)
         assert sc.map_status(m) == -6
     neg = torch.tensor([[0, 1, 1, 1], [0, -1, 0, 0]], dtype=torch.int32, device="cuda")
@@ -652,6 +692,9 @@ def test_launch_count_reported():
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="sorted", pipeline="wide")
     assert sc.last_launch_count() == 12               # clear, keys, 2 passes (15-bit keys), search, mask keys,
                                                       # 3 passes, tile count/scan/write
+    sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="hash", pipeline="wide")
+    assert sc.last_launch_count() == 10               # clear, insert, lookup, mask keys, 3 passes,
+                                                      # tile count/scan/write
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, pipeline="multi")
     assert sc.last_launch_count() > 5
     sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
