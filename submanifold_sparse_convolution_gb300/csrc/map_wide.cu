@@ -293,13 +293,15 @@ __global__ void __launch_bounds__(WT) k_wide_keys(const WideArgs a, const KeyDig
 
 // ---------------------------------------------------------------------------
 // hash mapper: the packed coordinate keys in an open-addressing table of
-// 4-slot buckets (bucketed linear probing), then 27 probes per row.  The
-// packed key's arithmetic is the sorted mapper's (neighbour key = key +
-// packed(d)); only the lookup structure differs: a probe is one 32-byte
-// bucket read instead of a binary search after a sort.  Within a bucket the
-// slots fill in order and never empty again, so a lookup that meets an empty
-// slot without a match knows the key is absent; only a full bucket sends it
-// on to the next one.
+// 4-slot buckets (bucketed linear probing), hashed by key >> 1 so that the
+// two voxels of a z pair share a bucket; then per row and (dx, dy) column
+// two bucket reads cover the three keys of dz = -1, 0, +1.  The packed key's
+// arithmetic is the sorted mapper's (neighbour key = key + packed(d)); only
+// the lookup structure differs: a probe is a 32-byte bucket read instead of
+// a binary search after a sort.  Within a bucket the slots fill in order and
+// never empty again, and a pair's entries go to its bucket or the ones after
+// it, so a bucket with an empty slot holds every entry of the pairs hashed to
+// it; only a full bucket sends a lookup on to the next one.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint64_t hash_bucket(uint64_t key, int log2_buckets) {
     return (key * 0x9E3779B97F4A7C15ull) >> (64 - log2_buckets);   // multiplicative (Fibonacci) hashing
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__(WT) k_wide_hash_insert(const WideArgs a) {
         const uint64_t entry = (key << a.row_bits) | static_cast<uint64_t>(i);
         const int lb = a.table_log2 - 2;
         const uint64_t bmask = (uint64_t(1) << lb) - 1;
-        uint64_t b = hash_bucket(key, lb);
+        uint64_t b = hash_bucket(key >> 1, lb);
         bool placed = false;
         for (uint64_t probe = 0; probe <= bmask && !placed; ++probe, b = (b + 1) & bmask) {
             for (int j = 0; j < kHashBucket; ++j) {
@@ -345,92 +347,112 @@ __global__ void __launch_bounds__(WT) k_wide_hash_insert(const WideArgs a) {
     if (err) atomicOr(a.status, err);
 }
 
-// Looks key kk up in bucket b (slots lo.x, lo.y, hi.x, hi.y): 1 found (*row
-// set), 0 absent, -1 the bucket is full without it (go on to the next).
-__device__ __forceinline__ int bucket_find(ulonglong2 lo, ulonglong2 hi, uint64_t kk, int row_bits, int32_t* row) {
+// Scans one bucket (slots lo.x, lo.y, hi.x, hi.y) for the keys kc - 1, kc,
+// kc + 1 of a column, recording the rows found in v0, v1, v2; returns whether
+// the bucket has an empty slot (then it holds every entry of its pairs).
+__device__ __forceinline__ bool bucket_scan(ulonglong2 lo, ulonglong2 hi, uint64_t kc, int row_bits, int32_t& v0,
+                                            int32_t& v1, int32_t& v2) {
     const uint64_t s[4] = {lo.x, lo.y, hi.x, hi.y};
     const uint64_t row_mask = (uint64_t(1) << row_bits) - 1;
+    bool open = false;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        if (s[j] == 0ull) return 0;
-        if ((s[j] >> row_bits) == kk) {
-            *row = static_cast<int32_t>(s[j] & row_mask);
-            return 1;
+        open |= s[j] == 0ull;
+        const uint64_t d = (s[j] >> row_bits) - (kc - 1);   // 0, 1, 2 for the column's keys
+        const int32_t row = static_cast<int32_t>(s[j] & row_mask);
+        if (s[j] != 0ull) {
+            v0 = d == 0 ? row : v0;
+            v1 = d == 1 ? row : v1;
+            v2 = d == 2 ? row : v2;
         }
     }
-    return -1;
+    return open;
 }
 
-__global__ void __launch_bounds__(WT) k_wide_hash_lookup(const WideArgs a) {
+// Three threads per row, one dx plane each, 128 rows per block: every
+// thread's 6 bucket reads are in flight at once (a thread per row with the
+// planes in turn had only a third of the reads in flight and waited three
+// times as long).  The rows are assembled in shared memory and written whole,
+// coalesced.
+constexpr int kHashLookupRows = 128;
+
+__global__ void __launch_bounds__(kHashLookupRows * 3) k_wide_hash_lookup(const WideArgs a) {
+    __shared__ int32_t rows_s[kHashLookupRows][kNbrStride + 1];   // +1: conflict-free row and column access
+    __shared__ uint32_t mask_s[kHashLookupRows];
     __shared__ int32_t cnt[kTaps];
     const int t = threadIdx.x, lane = t & 31;
+    const int p = t / kHashLookupRows;   // this thread's dx plane (warp-uniform)
+    const int rl = t % kHashLookupRows;  // its row within the block
     if (t < kTaps) cnt[t] = 0;
-    __syncthreads();
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * WT + t;
+    if (t < kHashLookupRows) mask_s[t] = 0;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kHashLookupRows;
+    const int64_t i = row0 + rl;
     const bool valid = i < a.n;
     const int4 q = valid ? a.coords[i] : make_int4(-1, -1, -1, -1);
     const bool ok = valid && coord_ok(q, a.shape, a.batch);
     const uint64_t key = ok ? packed_key(q, a) : 0ull;
     pdl_wait();   // every key is in the table
     pdl_trigger();
-    int32_t v[kNbrStride];
+    int32_t v[9];
 #pragma unroll
-    for (int k = 0; k < kNbrStride; ++k) v[k] = -1;
+    for (int k = 0; k < 9; ++k) v[k] = -1;
     const int lb = a.table_log2 - 2;
     const uint64_t bmask = (uint64_t(1) << lb) - 1;
     const ulonglong2* tab = reinterpret_cast<const ulonglong2*>(a.table);
-    // one dx plane (9 taps) per round: its 9 bucket reads in flight together;
-    // the rare lookups that meet a full bucket go on, all of the warp's in
-    // the same extra round
+    // the plane's 3 columns, 6 bucket reads (the pairs of kc - 1 and kc + 1);
+    // the rare reads that meet a full bucket go on, all of the warp's in the
+    // same extra round
+    ulonglong2 lo[6], hi[6];
+    uint64_t kc[3];
+    uint32_t pending = 0;
 #pragma unroll
-    for (int k0 = 0; k0 < kTaps; k0 += 9) {
-        ulonglong2 lo[9], hi[9];
-        uint32_t pending = 0;
+    for (int c = 0; c < 3; ++c) kc[c] = key + a.koff[9 * p + 3 * c + 1];   // the column's dz = 0 key
 #pragma unroll
-        for (int j = 0; j < 9; ++j) {
-            if (ok) {
-                const uint64_t b = hash_bucket(key + a.koff[k0 + j], lb);
-                lo[j] = __ldcg(tab + 2 * b);
-                hi[j] = __ldcg(tab + 2 * b + 1);
+    for (int r = 0; r < 6; ++r) {
+        if (ok) {
+            const uint64_t b = hash_bucket((kc[r >> 1] + ((r & 1) ? 1 : -1)) >> 1, lb);
+            lo[r] = __ldcg(tab + 2 * b);
+            hi[r] = __ldcg(tab + 2 * b + 1);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 6; ++r)
+        if (ok && !bucket_scan(lo[r], hi[r], kc[r >> 1], a.row_bits, v[3 * (r >> 1)], v[3 * (r >> 1) + 1],
+                               v[3 * (r >> 1) + 2]))
+            pending |= 1u << r;
+    for (uint64_t step = 1; __any_sync(0xFFFFFFFFu, pending != 0u) && step <= bmask; ++step) {
+#pragma unroll
+        for (int r = 0; r < 6; ++r) {
+            if ((pending >> r) & 1u) {
+                const uint64_t b = (hash_bucket((kc[r >> 1] + ((r & 1) ? 1 : -1)) >> 1, lb) + step) & bmask;
+                lo[r] = __ldcg(tab + 2 * b);
+                hi[r] = __ldcg(tab + 2 * b + 1);
             }
         }
 #pragma unroll
-        for (int j = 0; j < 9; ++j) {
-            if (ok && bucket_find(lo[j], hi[j], key + a.koff[k0 + j], a.row_bits, &v[k0 + j]) < 0) pending |= 1u << j;
-        }
-        for (uint64_t r = 1; __any_sync(0xFFFFFFFFu, pending != 0u) && r <= bmask; ++r) {
-#pragma unroll
-            for (int j = 0; j < 9; ++j) {
-                if ((pending >> j) & 1u) {
-                    const uint64_t b = (hash_bucket(key + a.koff[k0 + j], lb) + r) & bmask;
-                    lo[j] = __ldcg(tab + 2 * b);
-                    hi[j] = __ldcg(tab + 2 * b + 1);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 9; ++j) {
-                if (((pending >> j) & 1u) &&
-                    bucket_find(lo[j], hi[j], key + a.koff[k0 + j], a.row_bits, &v[k0 + j]) >= 0)
-                    pending &= ~(1u << j);
-            }
-        }
+        for (int r = 0; r < 6; ++r)
+            if (((pending >> r) & 1u) && bucket_scan(lo[r], hi[r], kc[r >> 1], a.row_bits, v[3 * (r >> 1)],
+                                                     v[3 * (r >> 1) + 1], v[3 * (r >> 1) + 2]))
+                pending &= ~(1u << r);
     }
     uint32_t m = 0;
 #pragma unroll
-    for (int k = 0; k < kTaps; ++k) m |= (v[k] >= 0 ? 1u : 0u) << k;
-    if (valid) {
-        int4* dst = reinterpret_cast<int4*>(a.nbr + i * kNbrStride);
-#pragma unroll
-        for (int qq = 0; qq < kNbrStride / 4; ++qq)
-            dst[qq] = make_int4(v[4 * qq], v[4 * qq + 1], v[4 * qq + 2], v[4 * qq + 3]);
-        a.mask[i] = m;
+    for (int k = 0; k < 9; ++k) {
+        rows_s[rl][9 * p + k] = v[k];
+        m |= (v[k] >= 0 ? 1u : 0u) << k;
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, v[k] >= 0);
+        if (lane == 0 && b) atomicAdd(&cnt[9 * p + k], __popc(b));
     }
-#pragma unroll
-    for (int k = 0; k < kTaps; ++k) {
-        const uint32_t b = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
-        if (lane == 0 && b) atomicAdd(&cnt[k], __popc(b));
-    }
+    if (p == 0)
+        for (int k = kTaps; k < kNbrStride; ++k) rows_s[rl][k] = -1;
+    __syncthreads();   // mask_s is cleared
+    if (m) atomicOr(&mask_s[rl], m << (9 * p));
     __syncthreads();
+    // the block's rows, whole and coalesced
+    const int64_t rows = a.n - row0 < kHashLookupRows ? a.n - row0 : kHashLookupRows;
+    for (int idx = t; idx < rows * kNbrStride; idx += kHashLookupRows * 3)
+        a.nbr[row0 * kNbrStride + idx] = rows_s[idx / kNbrStride][idx % kNbrStride];
+    if (t < rows) a.mask[row0 + t] = mask_s[t];
     if (t < kTaps && cnt[t]) atomicAdd(a.tap_count + t, cnt[t]);
 }
 
@@ -785,25 +807,33 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_count(const WideArgs a,
 // (each tap's list starts where the previous tap's ends) in place, the tap
 // offsets and totals, and the tiles in descending order of union size,
 // stable in the tile index (a counting sort over the 28 sizes: warp w takes
-// a contiguous range of tiles, 32 at a time).
+// a contiguous range of tiles, 32 at a time).  It is a chain of dependent
+// steps on one SM, so its global reads are issued together up front: the
+// first round of counts and (up to kUnionCache tiles) every tile's union.
 constexpr int kScanThreads = 1024;
 constexpr int kScanWarps = kScanThreads / 32;
 constexpr int kScanPer = 8;                          // values per thread and round
 constexpr int kScanRound = kScanThreads * kScanPer;
+constexpr int kUnionCache = 2048;                    // unions kept in shared memory
 
 __global__ void __launch_bounds__(kScanThreads) k_wide_tile_scan(const WideArgs a) {
-    __shared__ int32_t wsum[kScanWarps];
     __shared__ __align__(16) int32_t buf[kScanRound];
+    __shared__ uint32_t uc[kUnionCache];
+    __shared__ int32_t wsum[kScanWarps];
     __shared__ int32_t wcnt[kScanWarps][kTaps + 1];
     __shared__ int32_t bbase[kTaps + 1];
     __shared__ int32_t tap_sum;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const int64_t T = a.n_tiles;
     const int64_t m = kTaps * T;
+    const bool cached = T <= kUnionCache;
     if (t < kScanWarps * (kTaps + 1)) (&wcnt[0][0])[t] = 0;
     if (t == 0) tap_sum = 0;
     pdl_wait();   // counts and unions of every tile are complete
     pdl_trigger();
+    // the unions, in flight together with the first round of counts
+    if (cached)
+        for (int64_t i = t; i < T; i += kScanThreads) uc[i] = __ldcg(a.tile_union + i);
     // ---- pair offsets, in rounds of kScanRound values: coalesced loads into
     // shared memory, each thread scans kScanPer consecutive values there,
     // a block scan of the thread sums, coalesced stores
@@ -852,9 +882,12 @@ __global__ void __launch_bounds__(kScanThreads) k_wide_tile_scan(const WideArgs 
             const int64_t i = r0 + static_cast<int64_t>(k) * kScanThreads + t;
             if (i < m) a.seg_off[i] = buf[k * kScanThreads + t];
         }
+        if (t < kTaps) {   // the taps whose first pair falls in this round
+            const int64_t at = static_cast<int64_t>(t) * T - r0;
+            if (at >= 0 && at < kScanRound) a.tap_off[t] = buf[at];
+        }
         __syncthreads();   // buf and wsum are reused
     }
-    if (t < kTaps) a.tap_off[t] = __ldcg(a.seg_off + static_cast<int64_t>(t) * T);   // (block-visible after the barrier)
     if (t == 0) {
         a.tap_off[kTaps] = carry;
         a.totals[0] = carry;
@@ -867,7 +900,7 @@ __global__ void __launch_bounds__(kScanThreads) k_wide_tile_scan(const WideArgs 
     int32_t my_taps = 0;
     for (int64_t i0 = t0; i0 < t1; i0 += 32) {
         const int64_t tt = i0 + lane;
-        const int c = tt < t1 ? __popc(__ldcg(a.tile_union + tt)) : -1;
+        const int c = tt < t1 ? __popc(cached ? uc[tt] : __ldcg(a.tile_union + tt)) : -1;
         const int b = c >= 0 ? kTaps - c : kTaps + 1;
         my_taps += c > 0 ? c : 0;
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, b);
@@ -900,7 +933,7 @@ __global__ void __launch_bounds__(kScanThreads) k_wide_tile_scan(const WideArgs 
     __syncthreads();
     for (int64_t i0 = t0; i0 < t1; i0 += 32) {
         const int64_t tt = i0 + lane;
-        const int b = tt < t1 ? kTaps - __popc(__ldcg(a.tile_union + tt)) : kTaps + 1;
+        const int b = tt < t1 ? kTaps - __popc(cached ? uc[tt] : __ldcg(a.tile_union + tt)) : kTaps + 1;
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, b);
         if (b <= kTaps) {
             const int64_t at = static_cast<int64_t>(bbase[b]) + wcnt[w][b] + __popc(peers & lt);
@@ -1071,7 +1104,8 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     };
     if (a.mapper == SPCONV_MAPPER_HASH) {
         SPCONV_CHECK(launch_pdl(k_wide_hash_insert, row_blocks, WT, s, true, a));
-        SPCONV_CHECK(launch_pdl(k_wide_hash_lookup, row_blocks, WT, s, true, a));
+        SPCONV_CHECK(launch_pdl(k_wide_hash_lookup, static_cast<unsigned>((n + kHashLookupRows - 1) / kHashLookupRows),
+                                3 * kHashLookupRows, s, true, a));
     } else if (a.mapper == SPCONV_MAPPER_SORTED) {
         const int passes = wide_key_passes(a.key_bits);
         if (passes > kWideKeyPassesMax) return SPCONV_ERR_UNSUPPORTED;
