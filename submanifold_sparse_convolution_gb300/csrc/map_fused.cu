@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(FT, 1) k_map_fused(const FusedArgs a, int part
                                          static_cast<int64_t>(q.z + 1) * a.gsy + (q.w + 1);
 #pragma unroll
                     for (int k = 0; k < kTaps; ++k) {
-                        v[k] = __ldg(a.grid + cell + a.goff[k]);
+                        v[k] = __ldcg(a.grid + cell + a.goff[k]);
                         m |= (v[k] >= 0 ? 1u : 0u) << k;
                     }
                 }

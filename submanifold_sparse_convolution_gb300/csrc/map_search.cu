@@ -86,6 +86,18 @@ __device__ __forceinline__ int64_t lower_bound_in(const uint64_t* a, int64_t len
     return len == 1 && a[base] < t ? base + 1 : base;
 }
 
+// The same over global memory written by the kernel before this one (which
+// may still have been running when this kernel started): L2 loads only.
+__device__ __forceinline__ int64_t lower_bound_global(const uint64_t* a, int64_t len, uint64_t t) {
+    int64_t base = 0;
+    while (len > 1) {
+        const int64_t half = len >> 1;
+        base += __ldcg(a + base + half - 1) < t ? half : 0;
+        len -= half;
+    }
+    return len == 1 && __ldcg(a + base) < t ? base + 1 : base;
+}
+
 template <int kSearchRows, int kSearchGroups>
 __global__ void __launch_bounds__(kSearchRows * kSearchGroups) k_search_window(const SearchArgs a) {
     constexpr int kSearchThreads = kSearchRows * kSearchGroups;
@@ -128,8 +140,8 @@ __global__ void __launch_bounds__(kSearchRows * kSearchGroups) k_search_window(c
         sv8[u] = j < ns ? __ldcg(a.sv + (j << a.sample_shift)) : 0ull;
     }
     const int64_t s = s0 + i;
-    const uint64_t vs = (g == 0 && s < n) ? __ldg(a.sv + s) : ~uint64_t(0);
-    const uint64_t before = (t == 0 && s0 > 0) ? __ldg(a.sv + s0 - 1) : ~uint64_t(0);
+    const uint64_t vs = (g == 0 && s < n) ? __ldcg(a.sv + s) : ~uint64_t(0);
+    const uint64_t before = (t == 0 && s0 > 0) ? __ldcg(a.sv + s0 - 1) : ~uint64_t(0);
 #pragma unroll
     for (int u = 0; u < kSampPerThread; ++u) {
         const int64_t j = t + static_cast<int64_t>(u) * kSearchThreads;
@@ -189,7 +201,7 @@ __global__ void __launch_bounds__(kSearchRows * kSearchGroups) k_search_window(c
             for (int q = 1; q < 9; ++q) c += e >= wofs[q] ? 1 : 0;
             const int32_t i = e - wofs[c];
             slot[u] = e < total ? c * wst + pad_idx(i) : -1;
-            v[u] = e < total ? __ldg(a.sv + wlo[c] + i) : 0ull;
+            v[u] = e < total ? __ldcg(a.sv + wlo[c] + i) : 0ull;
         }
 #pragma unroll
         for (int u = 0; u < kCopyBatch; ++u)
@@ -252,10 +264,10 @@ __global__ void __launch_bounds__(kSearchRows * kSearchGroups) k_search_window(c
                         cand[j] = win[cc * wst + pad_idx(pp)];
                     }
                 } else {   // a run too long for shared memory: search it in global memory
-                    const int64_t gp = wlo[cc] + lower_bound_in(a.sv + wlo[cc], glen[cc], tl[c]);
+                    const int64_t gp = wlo[cc] + lower_bound_global(a.sv + wlo[cc], glen[cc], tl[c]);
                     avail = static_cast<int32_t>(n - gp < 3 ? n - gp : 3);
 #pragma unroll
-                    for (int j = 0; j < 3; ++j) cand[j] = gp + j < n ? __ldg(a.sv + gp + j) : 0ull;
+                    for (int j = 0; j < 3; ++j) cand[j] = gp + j < n ? __ldcg(a.sv + gp + j) : 0ull;
                 }
 #pragma unroll
                 for (int j = 0; j < 3; ++j) {

@@ -201,9 +201,12 @@ __device__ __forceinline__ bool coord_ok(int4 q, int3 shape, int batch) {
 }
 
 // First kernel of a build: clears the status word, every digit histogram,
-// the tickets and barrier counters, the tap counts and totals, and (dense
-// mapper) the presence grid to -1.  The kernel after it overlaps it and waits
-// for it only before its first write to any of these.
+// the tickets and barrier counters, the tap counts and totals, the look-back
+// states, and the hash table (hash mapper) or the presence grid to -1 (dense
+// mapper).  The kernel after it overlaps it and waits for it only before its
+// first write to any of these.  The look-back states must start cleared: the
+// arena is recycled memory, and a stale word (an old hash entry or packed key)
+// can carry the current epoch in its top half and nonzero flag bits.
 __global__ void __launch_bounds__(WT) k_wide_clear(const WideArgs a) {
     pdl_trigger();
     const int64_t i0 = static_cast<int64_t>(blockIdx.x) * WT + threadIdx.x;
@@ -213,6 +216,11 @@ __global__ void __launch_bounds__(WT) k_wide_clear(const WideArgs a) {
     for (int64_t i = i0; i < kWideCounters; i += stride) a.tickets[i] = 0;
     if (i0 < kTaps) a.tap_count[i0] = 0;
     if (i0 < 2) a.totals[i0] = 0;
+    {
+        ulonglong2* l2 = reinterpret_cast<ulonglong2*>(a.look);
+        const int64_t parts = (a.n + kWideKeysPerCta - 1) / kWideKeysPerCta;
+        for (int64_t i = i0; i < parts * kWideBins / 2; i += stride) l2[i] = make_ulonglong2(0ull, 0ull);
+    }
     if (a.mapper == SPCONV_MAPPER_HASH) {
         ulonglong2* t2 = reinterpret_cast<ulonglong2*>(a.table);
         const int64_t slots2 = (int64_t(1) << a.table_log2) / 2;
@@ -769,21 +777,47 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kTileRows) k_wide_tile_count(const WideArgs a, const uint64_t* __restrict__ ms) {
     __shared__ int32_t wc[kTileRows / 32][kTaps];
+    __shared__ int32_t taps[kTaps];
+    __shared__ int32_t pos[kTaps];
     __shared__ int32_t err;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int64_t T = a.n_tiles, n = a.n;
     const int64_t tile = blockIdx.x;
-    const uint64_t rmask = (uint64_t(1) << a.row_bits) - 1;
+    const int rb = a.row_bits;
+    const uint64_t rmask = (uint64_t(1) << rb) - 1;
     if (t == 0) err = 0;
     pdl_wait();   // the mask sort is complete
     pdl_trigger();
+    // the row's mask comes back out of its sort key (the key is the mask in
+    // the tap order: tap k at bit pos[k]), not from a second dependent load
+    if (t < kTaps) taps[t] = __ldcg(a.tap_count + t);
     const int64_t s = tile * kTileRows + t;
-    int64_t r = s < n ? static_cast<int64_t>(__ldcg(ms + s) & rmask) : -1;
+    const uint64_t sv = s < n ? __ldcg(ms + s) : 0ull;
+    __syncthreads();
+    if (t < kTaps) {
+        int32_t rank = t;
+        if (a.calibrated) {
+            const int32_t ck = taps[t];
+            rank = 0;
+            for (int j = 0; j < kTaps; ++j) {
+                const int32_t cj = taps[j];
+                rank += (cj > ck || (cj == ck && j < t)) ? 1 : 0;
+            }
+        }
+        pos[t] = rank;
+    }
+    __syncthreads();
+    int64_t r = s < n ? static_cast<int64_t>(sv & rmask) : -1;
     if (r >= n) {
         atomicOr(&err, kStatusInternal);
         r = -1;
     }
-    const uint32_t m = r >= 0 ? __ldcg(a.mask + r) : 0u;
+    uint32_t m = 0;
+    if (r >= 0) {
+        const uint32_t key = static_cast<uint32_t>(sv >> rb);
+#pragma unroll
+        for (int k = 0; k < kTaps; ++k) m |= ((key >> pos[k]) & 1u) << k;
+    }
 #pragma unroll
     for (int k = 0; k < kTaps; ++k) {
         const uint32_t b = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
@@ -1075,9 +1109,13 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
         cap_pass[dev] = resident_ctas(k_wide_pass, WT, sms);
     }
     const bool pass_ticket = static_cast<int64_t>(parts) > cap_pass[dev];
-    int64_t clear_blocks = a.mapper == SPCONV_MAPPER_DENSE ? (a.cells / 4 + WT * 8 - 1) / (WT * 8)
-                         : a.mapper == SPCONV_MAPPER_HASH ? ((int64_t(1) << a.table_log2) / 2 + WT * 8 - 1) / (WT * 8)
-                                                          : 8;
+    // every thread clears ~8 16-byte words of the largest array
+    const int64_t look16 = static_cast<int64_t>(parts) * kWideBins / 2;
+    int64_t clear16 = a.mapper == SPCONV_MAPPER_DENSE ? a.cells / 4
+                    : a.mapper == SPCONV_MAPPER_HASH ? (int64_t(1) << a.table_log2) / 2
+                                                     : 0;
+    if (look16 > clear16) clear16 = look16;
+    int64_t clear_blocks = (clear16 + WT * 8 - 1) / (WT * 8);
     if (clear_blocks > 4 * sms) clear_blocks = 4 * sms;
     SPCONV_CHECK(launch_pdl(k_wide_clear, static_cast<unsigned>(clear_blocks < 1 ? 1 : clear_blocks), WT, s, false, a));
     auto pass = [&](const uint64_t* in, uint64_t* out, int shift, int width, const int32_t* gh, int ticket) {

@@ -124,6 +124,49 @@ def test_map_small_hash(seed, n, shape, batch, bit_order):
     assert sc.map_info(m)["mapper"] == "hash"
 
 
+def _hash_bucket_of_pairs(keys, lb):
+    """The library's bucket of each key's z pair (multiplicative hashing of key >> 1), restated
+    here to build a cloud that overfills buckets."""
+    phi = np.uint64(0x9E3779B97F4A7C15)
+    with np.errstate(over="ignore"):
+        return ((keys >> np.uint64(1)) * phi) >> np.uint64(64 - lb)
+
+
+def test_map_hash_full_buckets():
+    """Pairs of voxels chosen so that many hash to one bucket: insertion overflows into the
+    following buckets and lookups take the extra rounds; the map must still be exact."""
+    shape, n_target = (64, 64, 64), 480
+    X, Y, Z = shape
+    wz, wy, wx = (Z + 1).bit_length(), (Y + 1).bit_length(), (X + 1).bit_length()
+    log2 = 11
+    while (1 << log2) < 16 * n_target:
+        log2 += 1
+    lb = log2 - 2
+    g = np.stack(np.meshgrid(np.arange(X), np.arange(Y), np.arange(0, Z, 2), indexing="ij"), -1).reshape(-1, 3)
+    g = g.astype(np.uint64)
+    keys = (((g[:, 0] + 1) << np.uint64(wy) | (g[:, 1] + 1)) << np.uint64(wz)) | (g[:, 2] + 1)
+    buckets = _hash_bucket_of_pairs(keys, lb)
+    target = np.bincount(buckets.astype(np.int64)).argmax()
+    hot = g[buckets == target][:16].astype(np.int64)          # 16 distinct pairs in one bucket
+    assert hot.shape[0] == 16
+    rng = np.random.default_rng(861)
+    cells = {tuple(v) for v in hot}
+    cells |= {(x, y, z + 1) for x, y, z in hot if z + 1 < Z}   # a voxel above each
+    for x, y, z in hot:                                        # neighbours that look them up
+        for d in rng.integers(-1, 2, size=(6, 3)):
+            c = (x + d[0], y + d[1], z + d[2])
+            if all(0 <= c[i] < shape[i] for i in range(3)):
+                cells.add(tuple(int(v) for v in c))
+    while len(cells) < n_target:
+        cells.add(tuple(int(v) for v in rng.integers(0, 64, size=3)))
+    coords = np.array([(0,) + c for c in sorted(cells)], dtype=np.int32)
+    coords = coords[rng.permutation(len(coords))]
+    assert 16 * len(coords) <= (1 << log2) and 16 * len(coords) > (1 << (log2 - 1))
+    m = sc.build_map(torch.from_numpy(coords).cuda(), shape, 1, mapper="hash")
+    assert sc.map_status(m) == 0
+    assert_map_equal(sc.map_export(m), oracle_map(coords, shape, 1))
+
+
 def test_map_hash_many_rows_and_unsupported_pipelines():
     """300k rows in 3 frames (a 2M-slot table): the hash and sorted mappers give the same map;
     the hash mapper exists only in the whole-GPU pipeline."""
@@ -181,6 +224,21 @@ def test_map_ticketed_sort_passes_agree():
     b = sc.map_export(build(wl, "sorted", pipeline="multi"))
     for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
         assert torch.equal(a[key], b[key]), key
+
+
+def test_map_recycled_arena():
+    """Map memory is recycled between builds.  Look-back states of a sort pass left in it by
+    earlier builds (or hash-table entries, whose top half can equal a pass's epoch) must not be
+    taken for published ones: a 300k-row hash build, freed, then a 420k-row ticketed sorted build
+    in the same memory, three times over, against the one-kernel-per-step pipeline."""
+    big = S.random_cloud(64, 300000, shape=(200, 200, 60), batch_size=3)
+    wl = S.random_cloud(62, 420000, shape=(240, 240, 60), batch_size=2)
+    ref = sc.map_export(build(wl, "sorted", pipeline="multi"))
+    for _ in range(3):
+        build(big, "hash", pipeline="wide").destroy()
+        a = sc.map_export(build(wl, "sorted", pipeline="wide"))
+        for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
+            assert torch.equal(a[key], ref[key]), key
 
 
 @pytest.mark.parametrize("name", ["tiny", "deep"])
