@@ -81,7 +81,7 @@ struct MapHandle {
     int32_t* gtab = nullptr;       // [V][n_pad]: nbr[perm_g[s]][k] or -1 (g the group of tap k)
     uint32_t* tile_union = nullptr;  // [G][n_tiles]
     int32_t* tile_order = nullptr;   // [G][n_tiles], each group's tiles by descending union size
-    int32_t* seg_off = nullptr;      // [V][n_tiles] pair offset of (tap, tile)
+    int32_t* seg_off = nullptr;      // [V][n_tiles] pair count of (tap, tile), scanned into offsets where a scan runs
     int32_t* tile_nonempty = nullptr;  // [G] tiles with a nonempty union (the first ones of each tile order)
     int32_t* totals = nullptr;       // [2]: pairs, sum of union sizes
     void* arena = nullptr;           // one allocation holding the arrays above

@@ -539,6 +539,13 @@ __global__ void __launch_bounds__(WT) k_wide_mask_keys(const WideArgs a) {
     for (int i = t; i < kWideMaskPasses * bins; i += WT) (&h[0][0])[i] = 0;
     pdl_wait();   // masks and tap counts are complete
     pdl_trigger();
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * WT * kRowsPerThread + t;
+    uint32_t ms[kRowsPerThread];   // requested with the tap counts: one round trip for both
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) {
+        const int64_t i = row0 + r * WT;
+        ms[r] = i < a.n ? __ldcg(a.mask + i) : 0u;
+    }
     if (t < kTaps) taps[t] = __ldcg(a.tap_count + t);
     __syncthreads();
     if (t < kTaps) {
@@ -555,13 +562,6 @@ __global__ void __launch_bounds__(WT) k_wide_mask_keys(const WideArgs a) {
     }
     __syncthreads();
     const int rb = a.row_bits;
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * WT * kRowsPerThread + t;
-    uint32_t ms[kRowsPerThread];
-#pragma unroll
-    for (int r = 0; r < kRowsPerThread; ++r) {
-        const int64_t i = row0 + r * WT;
-        ms[r] = i < a.n ? __ldcg(a.mask + i) : 0u;
-    }
 #pragma unroll
     for (int r = 0; r < kRowsPerThread; ++r) {
         const int64_t i = row0 + r * WT;
@@ -982,20 +982,116 @@ __global__ void __launch_bounds__(kScanThreads) k_wide_tile_scan(const WideArgs 
 // One block of 128 threads per tile: perm, the per-tap pair lists (from the
 // (tap, tile) offsets) and the GEMM gather table (only the taps of the
 // tile's union).
+// With kPrefix (up to kPrefixTiles tiles) it also does the tile scan's work,
+// so that kernel is not launched: the tile's offset in tap k's list is the
+// tap's start (the exclusive sum of the per-tap totals the lookup counted)
+// plus the counts of tap k in the tiles before it, which the CTA sums itself
+// (the counts are still raw in seg_off); its place in the tile order is the
+// number of tiles with a larger union plus those before it with an equal
+// one.  CTA 0 writes the tap offsets and totals.
+constexpr int64_t kPrefixTiles = 1024;
+
+template <bool kPrefix>
 __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a, const uint64_t* __restrict__ ms) {
     __shared__ int32_t wc[kTileRows / 32][kTaps];
     __shared__ int32_t seg[kTaps];   // the tile's first pair in every tap's list
+    __shared__ int32_t tapc[kTaps];
+    __shared__ int32_t red[3][kTileRows / 32];
     __shared__ int32_t err;
     const int64_t tile = blockIdx.x;
     const int64_t T = a.n_tiles, n = a.n;
     const uint64_t rmask = (uint64_t(1) << a.row_bits) - 1;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) err = 0;
-    pdl_wait();   // the pair offsets are complete
+    pdl_wait();   // the pair offsets (kPrefix: counts) are complete
     pdl_trigger();
     // the offsets are read once, with the row ids, not inside the per-tap loop
     // (there they would wait one round trip per tap behind the pair stores)
-    if (threadIdx.x < kTaps) seg[threadIdx.x] = __ldcg(a.seg_off + static_cast<int64_t>(threadIdx.x) * T + tile);
+    if (!kPrefix && threadIdx.x < kTaps)
+        seg[threadIdx.x] = __ldcg(a.seg_off + static_cast<int64_t>(threadIdx.x) * T + tile);
+    const uint32_t uni = __ldcg(a.tile_union + tile);
+    if (kPrefix) {
+        if (threadIdx.x < kTaps) tapc[threadIdx.x] = __ldcg(a.tap_count + threadIdx.x);
+        // counts of the earlier tiles: warp w sums taps w, w + 4, ...; lanes stride over the tiles
+        constexpr int kPerWarp = (kTaps + kTileRows / 32 - 1) / (kTileRows / 32);
+        int32_t acc[kPerWarp];
+#pragma unroll
+        for (int j = 0; j < kPerWarp; ++j) acc[j] = 0;
+        for (int64_t b0 = 0; b0 < tile; b0 += 32 * 4) {
+#pragma unroll
+            for (int j = 0; j < kPerWarp; ++j) {
+                const int k = warp + (kTileRows / 32) * j;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t tt = b0 + 32 * u + lane;
+                    if (k < kTaps && tt < tile) acc[j] += __ldcg(a.seg_off + static_cast<int64_t>(k) * T + tt);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPerWarp; ++j) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
+            const int k = warp + (kTileRows / 32) * j;
+            if (lane == 0 && k < kTaps) seg[k] = acc[j];
+        }
+        // place in the tile order, and (for CTA 0) the sum of all union sizes
+        const int c = __popc(uni);
+        int32_t greater = 0, equal_before = 0, taps_all = 0;
+        for (int64_t b0 = 0; b0 < T; b0 += kTileRows * 4) {
+            uint32_t u4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t tt = b0 + kTileRows * u + threadIdx.x;
+                u4[u] = tt < T ? __ldcg(a.tile_union + tt) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t tt = b0 + kTileRows * u + threadIdx.x;
+                if (tt < T) {
+                    const int cu = __popc(u4[u]);
+                    greater += cu > c ? 1 : 0;
+                    equal_before += (cu == c && tt < tile) ? 1 : 0;
+                    taps_all += cu;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            greater += __shfl_xor_sync(0xFFFFFFFFu, greater, o);
+            equal_before += __shfl_xor_sync(0xFFFFFFFFu, equal_before, o);
+            taps_all += __shfl_xor_sync(0xFFFFFFFFu, taps_all, o);
+        }
+        if (lane == 0) {
+            red[0][warp] = greater;
+            red[1][warp] = equal_before;
+            red[2][warp] = taps_all;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int32_t g2 = 0, e2 = 0, s2 = 0;
+            for (int w2 = 0; w2 < kTileRows / 32; ++w2) {
+                g2 += red[0][w2];
+                e2 += red[1][w2];
+                s2 += red[2][w2];
+            }
+            const int64_t at = static_cast<int64_t>(g2) + e2;
+            if (at >= 0 && at < T) a.tile_order[at] = static_cast<int32_t>(tile);
+            else atomicOr(&err, kStatusInternal);
+            // the tap starts; CTA 0 publishes them with the totals
+            int32_t run = 0;
+            for (int k = 0; k < kTaps; ++k) {
+                if (tile == 0) a.tap_off[k] = run;
+                seg[k] += run;
+                run += tapc[k];
+            }
+            if (tile == 0) {
+                a.tap_off[kTaps] = run;
+                a.totals[0] = run;
+                a.totals[1] = s2;
+            }
+        }
+    }
     const int64_t s = tile * kTileRows + threadIdx.x;
     int32_t r = s < n ? static_cast<int32_t>(__ldcg(ms + s) & rmask) : -1;
     if (r >= n) {
@@ -1003,7 +1099,6 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a,
         atomicOr(&err, kStatusInternal);
     }
     const uint32_t m = r >= 0 ? __ldcg(a.mask + r) : 0u;
-    const uint32_t uni = __ldcg(a.tile_union + tile);
     int32_t v[kNbrStride];
     if (r >= 0) {
         const int4* src = reinterpret_cast<const int4*>(a.nbr + static_cast<int64_t>(r) * kNbrStride);
@@ -1174,8 +1269,12 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     const uint64_t* ms = (kWideMaskPasses & 1) ? a.vb : a.va;
     const unsigned tiles = static_cast<unsigned>(a.n_tiles);
     SPCONV_CHECK(launch_pdl(k_wide_tile_count, tiles, kTileRows, s, true, a, ms));
-    SPCONV_CHECK(launch_pdl(k_wide_tile_scan, 1u, static_cast<unsigned>(kScanThreads), s, true, a));
-    SPCONV_CHECK(launch_pdl(k_wide_tile_write, tiles, kTileRows, s, true, a, ms));
+    if (a.n_tiles <= kPrefixTiles) {
+        SPCONV_CHECK(launch_pdl(k_wide_tile_write<true>, tiles, kTileRows, s, true, a, ms));
+    } else {
+        SPCONV_CHECK(launch_pdl(k_wide_tile_scan, 1u, static_cast<unsigned>(kScanThreads), s, true, a));
+        SPCONV_CHECK(launch_pdl(k_wide_tile_write<false>, tiles, kTileRows, s, true, a, ms));
+    }
     return SPCONV_OK;
 }
 

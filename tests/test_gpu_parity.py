@@ -744,15 +744,19 @@ def test_launch_count_reported():
     assert sc.last_launch_count() == 2                # cluster build + whole-GPU compaction write
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="sorted", pipeline="fused")
     assert sc.last_launch_count() == 4                # cluster sort, search, cluster rest, write
+    # (up to 1024 tiles the tile write also does the tile scan's work: no scan launch)
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="dense", pipeline="wide")
-    assert sc.last_launch_count() == 10               # clear, scatter, lookup, mask keys, 3 passes,
-                                                      # tile count/scan/write
+    assert sc.last_launch_count() == 9                # clear, scatter, lookup, mask keys, 3 passes,
+                                                      # tile count/write
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="sorted", pipeline="wide")
-    assert sc.last_launch_count() == 12               # clear, keys, 2 passes (15-bit keys), search, mask keys,
-                                                      # 3 passes, tile count/scan/write
+    assert sc.last_launch_count() == 11               # clear, keys, 2 passes (15-bit keys), search, mask keys,
+                                                      # 3 passes, tile count/write
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="hash", pipeline="wide")
-    assert sc.last_launch_count() == 10               # clear, insert, lookup, mask keys, 3 passes,
-                                                      # tile count/scan/write
+    assert sc.last_launch_count() == 9                # clear, insert, lookup, mask keys, 3 passes,
+                                                      # tile count/write
+    big = S.random_cloud(52, 140000, shape=(100, 100, 40))
+    sc.build_map(big.coords.cuda(), big.spatial_shape, 1, mapper="hash", pipeline="wide")
+    assert sc.last_launch_count() == 10               # 1094 tiles: the tile scan runs
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, pipeline="multi")
     assert sc.last_launch_count() > 5
     sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
