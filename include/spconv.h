@@ -60,12 +60,14 @@ typedef enum { SPCONV_BF16 = 0, SPCONV_FP32 = 1 } spconv_dtype_t;
 
 typedef enum {
     SPCONV_MAPPER_AUTO = 0,   /* dense grid iff padded cells <= dense_max_cells, else HASH when
-                                 the WIDE pipeline builds the map, else SORTED                   */
+                                 the WIDE pipeline or a grouped K = 3 build makes the map, else
+                                 SORTED                                                           */
     SPCONV_MAPPER_DENSE = 1,  /* presence grid over the padded bounding box                       */
     SPCONV_MAPPER_SORTED = 2, /* sorted 64-bit keys + binary search, memory O(N)                   */
-    SPCONV_MAPPER_HASH = 3    /* the same packed keys in an open-addressing hash table, one probe
-                                 per tap; memory O(N).  WIDE pipeline only (other pipelines:
-                                 SPCONV_ERR_UNSUPPORTED), one offset group                         */
+    SPCONV_MAPPER_HASH = 3    /* the same packed keys in an open-addressing hash table, one
+                                 bucket read per pair of z neighbours; memory O(N).  The WIDE
+                                 pipeline and grouped builds only (the FUSED and MULTI
+                                 pipelines with one group: SPCONV_ERR_UNSUPPORTED)                 */
 } spconv_mapper_t;
 
 typedef enum {

@@ -179,9 +179,7 @@ def test_map_hash_many_rows_and_unsupported_pipelines():
         with pytest.raises(sc.SpconvError) as e:
             sc.build_map(wl.coords.cuda(), wl.spatial_shape, 3, mapper="hash", pipeline=pipeline)
         assert e.value.code == -2
-    with pytest.raises(sc.SpconvError) as e:
-        sc.build_map(wl.coords.cuda(), wl.spatial_shape, 3, mapper="hash", kernel_size=5)
-    assert e.value.code == -2
+
 
 
 @pytest.mark.parametrize("mapper", ["sorted", "dense"])
@@ -585,7 +583,7 @@ GROUP_SMALL = [(1, 1, (4, 4, 4), 1), (2, 7, (5, 5, 5), 1), (3, 128, (8, 8, 8), 1
 
 @pytest.mark.parametrize("K,G", GROUP_CASES)
 @pytest.mark.parametrize("seed,n,shape,batch", GROUP_SMALL)
-@pytest.mark.parametrize("mapper", ["dense", "sorted"])
+@pytest.mark.parametrize("mapper", ["dense", "sorted", "hash"])
 @pytest.mark.parametrize("bit_order", ["calibrated", "plain"])
 def test_map_groups_small(K, G, seed, n, shape, batch, mapper, bit_order):
     wl = S.random_cloud(700 + seed, n, shape=shape, batch_size=batch)
@@ -603,7 +601,7 @@ def test_map_groups_small(K, G, seed, n, shape, batch, mapper, bit_order):
 def test_map_groups_dense_and_sorted_agree_on_outdoor(K, G):
     wl = S.make_workload("outdoor")
     ref = oracle_groups(wl.coords.numpy(), wl.spatial_shape, wl.batch_size, K, G)
-    for mapper in ("sorted", "dense"):
+    for mapper in ("sorted", "dense", "hash"):
         m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, wl.batch_size, kernel_size=K, groups=G,
                          mapper=mapper, dense_max_cells=1 << 30)
         assert sc.map_status(m) == 0
@@ -720,7 +718,7 @@ def test_groups_argument_errors():
 
 
 def test_groups_duplicate_and_range_errors():
-    for mapper in ("dense", "sorted"):
+    for mapper in ("dense", "sorted", "hash"):
         dup = torch.tensor([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=torch.int32).cuda()
         m = sc.build_map(dup, (8, 8, 8), 1, kernel_size=5, mapper=mapper)
         assert sc.map_status(m) == -5
