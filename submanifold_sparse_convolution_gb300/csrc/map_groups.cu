@@ -169,6 +169,14 @@ __device__ __forceinline__ uint64_t g_bucket(uint64_t pair, int lb) {
     return (pair * 0x9E3779B97F4A7C15ull) >> (64 - lb);   // multiplicative (Fibonacci) hashing
 }
 
+// One bucket (4 slots, 32 bytes, 32-byte aligned) in a single 256-bit load
+// through L2 (the table was written by the kernel before this one).
+__device__ __forceinline__ void g_load_bucket(const uint64_t* b, ulonglong2& lo, ulonglong2& hi) {
+    asm volatile("ld.global.cg.v4.u64 {%0, %1, %2, %3}, [%4];"
+                 : "=l"(lo.x), "=l"(lo.y), "=l"(hi.x), "=l"(hi.y)
+                 : "l"(b));
+}
+
 __device__ __forceinline__ uint64_t g_key(int4 c, const GLayout& L) {
     return ((((static_cast<uint64_t>(c.x) << L.wx) | static_cast<uint64_t>(c.y + L.r)) << L.wy |
              static_cast<uint64_t>(c.z + L.r))
@@ -226,7 +234,6 @@ __global__ void __launch_bounds__(kGBlock) kg_hash_lookup(const int4* __restrict
     const int lb = log2 - 2;
     const uint64_t bmask = (uint64_t(1) << lb) - 1;
     const uint64_t rmask = (uint64_t(1) << row_bits) - 1;
-    const ulonglong2* tab = reinterpret_cast<const ulonglong2*>(table);
     for (int p = 0; p < K; ++p) {   // dx plane
         ulonglong2 lo[K * NP], hi[K * NP];
         uint64_t first_pair[K];
@@ -237,8 +244,7 @@ __global__ void __launch_bounds__(kGBlock) kg_hash_lookup(const int4* __restrict
         for (int q = 0; q < K * NP; ++q) {
             if (ok) {
                 const uint64_t b = g_bucket(first_pair[q / NP] + q % NP, lb);
-                lo[q] = __ldcg(tab + 2 * b);
-                hi[q] = __ldcg(tab + 2 * b + 1);
+                g_load_bucket(table + b * kGHashBucket, lo[q], hi[q]);
             }
         }
         for (uint64_t step = 0;; ++step) {
@@ -269,8 +275,7 @@ __global__ void __launch_bounds__(kGBlock) kg_hash_lookup(const int4* __restrict
             for (int q = 0; q < K * NP; ++q) {
                 if ((pending >> q) & 1u) {
                     const uint64_t b = (g_bucket(first_pair[q / NP] + q % NP, lb) + step + 1) & bmask;
-                    lo[q] = __ldcg(tab + 2 * b);
-                    hi[q] = __ldcg(tab + 2 * b + 1);
+                    g_load_bucket(table + b * kGHashBucket, lo[q], hi[q]);
                 }
             }
         }

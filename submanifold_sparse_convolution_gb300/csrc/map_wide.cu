@@ -315,6 +315,14 @@ __device__ __forceinline__ uint64_t hash_bucket(uint64_t key, int log2_buckets) 
     return (key * 0x9E3779B97F4A7C15ull) >> (64 - log2_buckets);   // multiplicative (Fibonacci) hashing
 }
 
+// One bucket (4 slots, 32 bytes, 32-byte aligned) in a single 256-bit load
+// through L2 (the table was written by the kernel before this one).
+__device__ __forceinline__ void load_bucket(const uint64_t* b, ulonglong2& lo, ulonglong2& hi) {
+    asm volatile("ld.global.cg.v4.u64 {%0, %1, %2, %3}, [%4];"
+                 : "=l"(lo.x), "=l"(lo.y), "=l"(hi.x), "=l"(hi.y)
+                 : "l"(b));
+}
+
 __device__ __forceinline__ uint64_t packed_key(int4 q, const WideArgs& a) {
     return (((((static_cast<uint64_t>(q.x) << a.wx) | static_cast<uint64_t>(q.y + 1)) << a.wy) |
              static_cast<uint64_t>(q.z + 1))
@@ -406,7 +414,6 @@ __global__ void __launch_bounds__(kHashLookupRows * 3) k_wide_hash_lookup(const 
     for (int k = 0; k < 9; ++k) v[k] = -1;
     const int lb = a.table_log2 - 2;
     const uint64_t bmask = (uint64_t(1) << lb) - 1;
-    const ulonglong2* tab = reinterpret_cast<const ulonglong2*>(a.table);
     // the plane's 3 columns, 6 bucket reads (the pairs of kc - 1 and kc + 1);
     // the rare reads that meet a full bucket go on, all of the warp's in the
     // same extra round
@@ -419,8 +426,7 @@ __global__ void __launch_bounds__(kHashLookupRows * 3) k_wide_hash_lookup(const 
     for (int r = 0; r < 6; ++r) {
         if (ok) {
             const uint64_t b = hash_bucket((kc[r >> 1] + ((r & 1) ? 1 : -1)) >> 1, lb);
-            lo[r] = __ldcg(tab + 2 * b);
-            hi[r] = __ldcg(tab + 2 * b + 1);
+            load_bucket(a.table + b * kHashBucket, lo[r], hi[r]);
         }
     }
 #pragma unroll
@@ -433,8 +439,7 @@ __global__ void __launch_bounds__(kHashLookupRows * 3) k_wide_hash_lookup(const 
         for (int r = 0; r < 6; ++r) {
             if ((pending >> r) & 1u) {
                 const uint64_t b = (hash_bucket((kc[r >> 1] + ((r & 1) ? 1 : -1)) >> 1, lb) + step) & bmask;
-                lo[r] = __ldcg(tab + 2 * b);
-                hi[r] = __ldcg(tab + 2 * b + 1);
+                load_bucket(a.table + b * kHashBucket, lo[r], hi[r]);
             }
         }
 #pragma unroll
