@@ -68,6 +68,10 @@ def _load():
         lib.oracle_pair_lists.restype = i64
         lib.oracle_conv_f64.argtypes = [P, i32, P, i64, P, P, i32, i32, P, i32]
         lib.oracle_conv_f64.restype = None
+        lib.oracle_strided_map.argtypes = [P, i64, P, i32, P, P]
+        lib.oracle_strided_map.restype = i64
+        lib.oracle_inverse_map.argtypes = [P, i64, i64, P]
+        lib.oracle_inverse_map.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -189,6 +193,35 @@ def conv_f64(nbr: np.ndarray, feats, weights, rows=None, threads: int = 0) -> np
     _load().oracle_conv_f64(_ptr(nbr), V, rp, n_rows, _ptr(f), _ptr(w), c_in, c_out, _ptr(out),
                             int(threads))
     return out
+
+
+def strided_map(coords, spatial_shape, batch_size: int):
+    """Strided convolution (kernel 3, stride 2, padding 1): ``(out_coords[M, 4], nbr[M, 27])``,
+    the output sites in ascending (b, x, y, z) order and, per tap, the input row at 2o + d_k
+    or -1 (see ``oracle_strided_map``)."""
+    c = np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 4))
+    shape = np.ascontiguousarray(np.asarray(spatial_shape, dtype=np.int32))
+    cap = max(1, 8 * c.shape[0])
+    oc = np.empty((cap, 4), dtype=np.int32)
+    nbr = np.empty((cap, 27), dtype=np.int32)
+    m = _load().oracle_strided_map(_ptr(c), c.shape[0], _ptr(shape), int(batch_size), _ptr(oc), _ptr(nbr))
+    if m < 0:
+        raise OracleError(int(m))
+    return oc[:m].copy(), nbr[:m].copy()
+
+
+def strided_shape(spatial_shape):
+    """Output shape of the strided convolution: (X - 1) // 2 + 1 per axis."""
+    return tuple((int(v) - 1) // 2 + 1 for v in spatial_shape)
+
+
+def inverse_map(nbr: np.ndarray, n_in: int) -> np.ndarray:
+    """The map of the inverse (transposed) convolution: ``inv[n_in, 27]``, the output site o
+    of the strided map with 2o + d_k at input row i, or -1."""
+    nbr = np.ascontiguousarray(nbr, dtype=np.int32)
+    inv = np.empty((int(n_in), 27), dtype=np.int32)
+    _load().oracle_inverse_map(_ptr(nbr), nbr.shape[0], int(n_in), _ptr(inv))
+    return inv
 
 
 def epilogue_f64(conv, scale=None, bias=None, residual=None, relu=False, rows=None) -> np.ndarray:

@@ -33,6 +33,7 @@
 //   a group is a run of consecutive taps [k0, k0 + kg): with G groups of
 //   V / G taps, group g holds the taps with dx = g - r when G = K.
 #include <algorithm>
+#include <array>
 #include <cstdint>
 #include <cstring>
 #include <unordered_map>
@@ -202,6 +203,67 @@ void oracle_conv_f64(const int32_t* nbr, int32_t V, const int32_t* rows, int64_t
             }
         }
     }
+}
+
+// Strided (downsampling) convolution, kernel 3, stride 2, padding 1 ("Sparse
+// convolution in FP32", "Calibrated bit order": the strided kernels change
+// the coordinate set).  Output shape X' = (X - 1) / 2 + 1 per axis (torch
+// conv3d with kernel 3, stride 2, padding 1).  The output sites are every o
+// in [0, X') x [0, Y') x [0, Z') of a batch whose window {2o + d : d in
+// {-1,0,1}^3} holds an input site, in ascending (b, x, y, z) order;
+// nbr[o][k] = the input row at 2o + d_k, else -1 (tap k as above, K = 3).
+// out_coords: room for 8 n rows (an input site lies in at most 8 windows).
+// Returns the number of output sites.
+int64_t oracle_strided_map(const int32_t* coords, int64_t n, const int32_t* shape, int32_t batch_size,
+                           int32_t* out_coords, int32_t* nbr) {
+    std::unordered_map<Voxel, int32_t, VoxelHash> where;
+    where.reserve(static_cast<size_t>(n) * 2 + 1);
+    for (int64_t i = 0; i < n; ++i) {
+        Voxel v{coords[4 * i], coords[4 * i + 1], coords[4 * i + 2], coords[4 * i + 3]};
+        if (v.b < 0 || v.b >= batch_size || v.x < 0 || v.x >= shape[0] || v.y < 0 ||
+            v.y >= shape[1] || v.z < 0 || v.z >= shape[2])
+            return ORACLE_ERR_RANGE;
+        if (!where.emplace(v, static_cast<int32_t>(i)).second) return ORACLE_ERR_DUPLICATE;
+    }
+    const int32_t os[3] = {(shape[0] - 1) / 2 + 1, (shape[1] - 1) / 2 + 1, (shape[2] - 1) / 2 + 1};
+    // every output whose window holds an input: o = (c - d) / 2 with c - d even, inside the output shape
+    std::vector<std::array<int32_t, 4>> outs;
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t* c = coords + 4 * i;
+        for (int dx = -1; dx <= 1; ++dx)
+            for (int dy = -1; dy <= 1; ++dy)
+                for (int dz = -1; dz <= 1; ++dz) {
+                    const int32_t px = c[1] - dx, py = c[2] - dy, pz = c[3] - dz;
+                    if (px < 0 || py < 0 || pz < 0 || px % 2 || py % 2 || pz % 2) continue;
+                    const std::array<int32_t, 4> o = {c[0], px / 2, py / 2, pz / 2};
+                    if (o[1] < os[0] && o[2] < os[1] && o[3] < os[2]) outs.push_back(o);
+                }
+    }
+    std::sort(outs.begin(), outs.end());
+    outs.erase(std::unique(outs.begin(), outs.end()), outs.end());
+    for (size_t j = 0; j < outs.size(); ++j) {
+        for (int a = 0; a < 4; ++a) out_coords[4 * j + a] = outs[j][a];
+        for (int dx = -1; dx <= 1; ++dx)
+            for (int dy = -1; dy <= 1; ++dy)
+                for (int dz = -1; dz <= 1; ++dz) {
+                    Voxel q{outs[j][0], 2 * outs[j][1] + dx, 2 * outs[j][2] + dy, 2 * outs[j][3] + dz};
+                    auto it = where.find(q);
+                    nbr[27 * j + tap_index(3, dx, dy, dz)] = it == where.end() ? -1 : it->second;
+                }
+    }
+    return static_cast<int64_t>(outs.size());
+}
+
+// The map of the inverse (transposed) convolution of a strided map: rows are
+// the strided map's input sites, inv[i][k] = the output site o with
+// 2o + d_k = the site of row i (there is at most one), else -1.
+void oracle_inverse_map(const int32_t* nbr, int64_t n_out, int64_t n_in, int32_t* inv) {
+    for (int64_t i = 0; i < 27 * n_in; ++i) inv[i] = -1;
+    for (int64_t o = 0; o < n_out; ++o)
+        for (int k = 0; k < 27; ++k) {
+            const int32_t i = nbr[27 * o + k];
+            if (i >= 0) inv[27 * static_cast<int64_t>(i) + k] = static_cast<int32_t>(o);
+        }
 }
 
 int oracle_max_threads(void) {

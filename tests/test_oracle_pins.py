@@ -583,3 +583,92 @@ def test_mutated_group_order_is_caught():
     pos[p[0]] = np.arange(nbr.shape[0])
     follows = [np.all(np.diff(pos[outs[tap_off[k]:tap_off[k + 1]]]) > 0) for k in range(9)]
     assert not all(follows)
+
+
+# ---------------------------------------------------------------------------
+# strided convolution (kernel 3, stride 2, padding 1) and its inverse
+# ---------------------------------------------------------------------------
+
+def _dense_weights(w):
+    """[27, Cin, Cout] taps -> a torch [Cout, Cin, 3, 3, 3] conv3d weight."""
+    w = torch.as_tensor(np.asarray(w, dtype=np.float64))
+    wd = torch.zeros(w.shape[2], w.shape[1], 3, 3, 3, dtype=torch.float64)
+    for k, (dx, dy, dz) in enumerate(OFFSETS):
+        wd[:, :, dx + 1, dy + 1, dz + 1] = w[k].T
+    return wd
+
+
+def _grid(coords, values, batch, shape):
+    c = torch.as_tensor(np.asarray(coords, dtype=np.int64))
+    v = torch.as_tensor(np.asarray(values, dtype=np.float64))
+    g = torch.zeros(batch, v.shape[1], *shape, dtype=torch.float64)
+    g[c[:, 0], :, c[:, 1], c[:, 2], c[:, 3]] = v
+    return g
+
+
+@pytest.mark.parametrize("seed,n,shape,batch", [(111, 300, (9, 8, 7), 2), (112, 800, (12, 12, 12), 1),
+                                                (113, 1, (4, 4, 4), 1), (114, 400, (10, 11, 6), 3)])
+def test_strided_map_and_conv_match_dense_conv3d(seed, n, shape, batch):
+    wl = S.random_cloud(seed, n, shape=shape, batch_size=batch, c_in=5, c_out=4)
+    c = wl.coords.numpy()
+    oc, nbr = oracle.strided_map(c, shape, batch)
+    oshape = oracle.strided_shape(shape)
+    assert oshape == tuple(((np.asarray(shape) + 2 - 3) // 2 + 1).tolist())
+    # the output sites are where a stride-2 window holds any input site
+    ones = torch.nn.functional.conv3d(_grid(c, np.ones((n, 1)), batch, shape),
+                                      torch.ones(1, 1, 3, 3, 3, dtype=torch.float64), stride=2, padding=1)
+    assert tuple(ones.shape[2:]) == oshape
+    want = np.stack(np.nonzero(ones[:, 0].numpy() > 0), 1).astype(np.int32)   # ascending (b, x, y, z)
+    assert np.array_equal(oc, want)
+    # values
+    f = wl.feats.double().numpy()
+    w = np.random.default_rng(seed).standard_normal((27, 5, 4))
+    dense = torch.nn.functional.conv3d(_grid(c, f, batch, shape), _dense_weights(w), stride=2, padding=1)
+    ref = dense[oc[:, 0], :, oc[:, 1], oc[:, 2], oc[:, 3]].numpy()
+    np.testing.assert_allclose(oracle.conv_f64(nbr, f, w), ref, rtol=1e-12, atol=1e-12)
+    # every output site has at least one input; the pairs count every (input, window) incidence
+    assert (nbr >= 0).any(1).all()
+    assert (nbr >= 0).sum() == sum(1 for (b, x, y, z) in c for d in OFFSETS
+                                   if all((v - dd) % 2 == 0 and 0 <= (v - dd) // 2 < s
+                                          for v, dd, s in zip((x, y, z), d, oshape)))
+
+
+@pytest.mark.parametrize("seed,n,shape,batch", [(121, 300, (9, 8, 7), 2), (122, 700, (12, 12, 12), 1)])
+def test_inverse_map_and_conv_match_dense_conv_transpose3d(seed, n, shape, batch):
+    wl = S.random_cloud(seed, n, shape=shape, batch_size=batch)
+    c = wl.coords.numpy()
+    oc, nbr = oracle.strided_map(c, shape, batch)
+    inv = oracle.inverse_map(nbr, n)
+    oshape = oracle.strided_shape(shape)
+    rng = np.random.default_rng(seed)
+    y = rng.standard_normal((oc.shape[0], 3))
+    w = rng.standard_normal((27, 3, 6))           # [tap][C_in][C_out] of the inverse convolution
+    wt = torch.zeros(3, 6, 3, 3, 3, dtype=torch.float64)   # conv_transpose3d: [C_in, C_out, kx, ky, kz]
+    for k, (dx, dy, dz) in enumerate(OFFSETS):
+        wt[:, :, dx + 1, dy + 1, dz + 1] = torch.as_tensor(w[k])
+    pad = tuple(int(s % 2 == 0) for s in shape)   # output_padding recovers an even extent
+    dense = torch.nn.functional.conv_transpose3d(_grid(oc, y, batch, oshape), wt, stride=2, padding=1,
+                                                 output_padding=pad)
+    assert tuple(dense.shape[2:]) == tuple(shape)
+    ref = dense[c[:, 0], :, c[:, 1], c[:, 2], c[:, 3]].numpy()
+    np.testing.assert_allclose(oracle.conv_f64(inv, y, w), ref, rtol=1e-12, atol=1e-12)
+    # the inverse map is the strided map read backwards
+    for o, k in zip(*np.nonzero(nbr >= 0)):
+        assert inv[nbr[o, k], k] == o
+    assert (inv >= 0).sum() == (nbr >= 0).sum()
+
+
+def test_mutated_strided_map_is_caught():
+    """Windows at o + d (no stride) or at 2o - d (mirrored) both fail the dense conv."""
+    wl = S.random_cloud(131, 500, shape=(10, 10, 10), c_in=3, c_out=3)
+    c = wl.coords.numpy()
+    oc, nbr = oracle.strided_map(c, (10, 10, 10), 1)
+    f = wl.feats.double().numpy()
+    w = np.random.default_rng(132).standard_normal((27, 3, 3))
+    dense = torch.nn.functional.conv3d(_grid(c, f, 1, (10, 10, 10)), _dense_weights(w), stride=2, padding=1)
+    ref = dense[oc[:, 0], :, oc[:, 1], oc[:, 2], oc[:, 3]].numpy()
+    assert not np.allclose(oracle.conv_f64(nbr[:, ::-1].copy(), f, w), ref, atol=1e-6)
+    where = {tuple(v): i for i, v in enumerate(c.tolist())}
+    nbr_plain = np.array([[where.get((o[0], o[1] + dx, o[2] + dy, o[3] + dz), -1) for dx, dy, dz in OFFSETS]
+                          for o in oc.tolist()], dtype=np.int32)
+    assert not np.allclose(oracle.conv_f64(nbr_plain, f, w), ref, atol=1e-6)
