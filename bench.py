@@ -170,7 +170,9 @@ def run_ours(args, rank, world, device):
     build_mod.build()
     peaks = load_peaks()
     wl = S.make_workload(args.workload, kernel_size=args.kernel_size)
-    L = wl.layers
+    strided = args.conv == "strided"
+    # a strided convolution changes the sites: one layer (the workload's first weights)
+    L = 1 if strided else wl.layers
     coords = wl.coords.to(device)
     feats = wl.feats.to(device)
     wps = [sc.wpack_create(w.to(device)) for w in wl.weights]
@@ -200,6 +202,8 @@ def run_ours(args, rank, world, device):
         return y
 
     def build(c):
+        if strided:
+            return sc.build_map_strided(c, wl.spatial_shape, wl.batch_size)
         return sc.build_map(c, wl.spatial_shape, wl.batch_size, kernel_size=args.kernel_size,
                             groups=args.groups, gemm=args.gemm, pipeline=args.pipeline)
 
@@ -278,7 +282,8 @@ def run_ours(args, rank, world, device):
     # ---- end to end from pinned host buffers
     coords_h = wl.coords.pin_memory()
     feats_h = wl.feats.pin_memory()
-    out_h = torch.empty((wl.n, wl.c_out), dtype=torch.bfloat16).pin_memory()
+    n_rows = info["n"]   # output sites (the input sites but for a strided convolution)
+    out_h = torch.empty((n_rows, wl.c_out), dtype=torch.bfloat16).pin_memory()
     coords_d2 = torch.empty_like(coords)
     feats_d2 = torch.empty_like(feats)
     # the map needs only the coordinates: the features travel on a side stream
@@ -300,7 +305,7 @@ def run_ours(args, rank, world, device):
 
     e2e_ms = timed(e2e_step, max(args.steps, 5))
     h2d = coords.numel() * 4 + feats.numel() * 2
-    d2h = wl.n * wl.c_out * 2
+    d2h = n_rows * wl.c_out * 2
 
     m0.destroy()
     if rank != 0:
@@ -313,13 +318,14 @@ def run_ours(args, rank, world, device):
     gemm_tflops = useful_flops_layer / gemm_avg_s / 1e12
     n, P = wl.n, pairs
     V, G = info["kernel_size"] ** 3, info["groups"]
-    # coordinates read, nbr [n][V] written, masks and row order per group, pair lists
-    map_bytes = 16 * n + 4 * V * n + 8 * G * n + 8 * P
+    # coordinates read, nbr [rows][V] written, masks and row order per group, pair lists
+    map_bytes = 16 * n + 4 * V * n_rows + 8 * G * n_rows + 8 * P
     map_avg_s = statistics.mean(map_ms) * 1e-3
     kernel_name = (f"k_tc_gemm<{256 if wl.c_out > 256 else (128 if wl.c_out > 64 else 64)}, "
                    f"{'tap-major' if tap_major else 'tile-union'}>")
-    plain = info["kernel_size"] == 3 and G == 1
-    traffic = ncu_traffic("k_tc_gemm", args.workload if plain else f"{args.workload}-k{info['kernel_size']}-g{G}")
+    plain = info["kernel_size"] == 3 and G == 1 and not strided
+    traffic = ncu_traffic("k_tc_gemm", args.workload if plain else
+                          f"{args.workload}-strided" if strided else f"{args.workload}-k{info['kernel_size']}-g{G}")
     pages_us = PAGES_US.get(args.workload) if plain else None
     out = {
         "metric": METRIC, "value": round(us_per_layer, 3), "unit": UNIT, "n_gpus": world,
@@ -332,8 +338,9 @@ def run_ours(args, rank, world, device):
         "dtype": "bf16", "data": DATA,
         "config": {"workload": f"{args.workload}: N={wl.n}, C_in={wl.c_in}, C_out={wl.c_out}, "
                                f"layers={L}, batch={wl.batch_size}, grid={'x'.join(map(str, wl.spatial_shape))}",
+                   "conv": args.conv, "output_sites": n_rows,
                    "kernel_size": info["kernel_size"], "groups": G,
-                   "pairs": P, "pairs_per_row": round(P / n, 3), "mapper": info["mapper"], "pipeline": info["pipeline"], "gemm": info["gemm"],
+                   "pairs": P, "pairs_per_row": round(P / n_rows, 3) if n_rows else None, "mapper": info["mapper"], "pipeline": info["pipeline"], "gemm": info["gemm"],
                    "tile_taps": info["tile_taps"], "l2": "flushed (256 MB write) before every timed step",
                    "weights": "packed once per layer (outside the step)",
                    "relu": "between layers, fused into the GEMM store" if L > 1 else None},
@@ -362,7 +369,7 @@ def run_ours(args, rank, world, device):
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def prepare_oracle(workload, kernel_size=3, groups=0):
+def prepare_oracle(workload, kernel_size=3, groups=0, conv="submanifold"):
     import oracle
     from submanifold_sparse_convolution_gb300 import synthetic as S
 
@@ -370,7 +377,7 @@ def prepare_oracle(workload, kernel_size=3, groups=0):
     wl = S.make_workload(workload, kernel_size=kernel_size)
     G = groups if groups > 0 else (1 if kernel_size == 3 else kernel_size)
     return dict(wl=wl, c=wl.coords.numpy(), f=wl.feats.double().numpy(),
-                w=wl.weights[0].double().numpy(), K=kernel_size, G=G)
+                w=wl.weights[0].double().numpy(), K=kernel_size, G=G, conv=conv)
 
 
 def time_oracle(prep, budget_s):
@@ -379,33 +386,39 @@ def time_oracle(prep, budget_s):
 
     wl, c, f, w = prep["wl"], prep["c"], prep["f"], prep["w"]
     t = time.perf_counter()
-    nbr = oracle.kernel_map(c, wl.spatial_shape, wl.batch_size, prep["K"])
+    if prep["conv"] == "strided":
+        _, nbr = oracle.strided_map(c, wl.spatial_shape, wl.batch_size)
+    else:
+        nbr = oracle.kernel_map(c, wl.spatial_shape, wl.batch_size, prep["K"])
     _, _, p = oracle.group_orders(nbr, prep["G"], True)
     oracle.pair_lists(nbr, p)
+    n_rows = nbr.shape[0]                   # output sites (strided: fewer than the inputs)
+    layers = 1 if prep["conv"] == "strided" else wl.layers
     t_map = time.perf_counter() - t
     # calibrate the conv sample on 256 rows, then size it to the budget
-    rows = np.arange(min(256, wl.n), dtype=np.int32)
+    rows = np.arange(min(256, n_rows), dtype=np.int32)
     t = time.perf_counter()
     oracle.conv_f64(nbr, f, w, rows=rows)
-    t_cal = max(time.perf_counter() - t, 1e-6) / rows.shape[0]
-    k = int(min(wl.n, max(256, budget_s / t_cal)))
-    rows = np.linspace(0, wl.n - 1, k).astype(np.int32)
+    t_cal = max(time.perf_counter() - t, 1e-6) / max(1, rows.shape[0])
+    k = int(min(n_rows, max(256, budget_s / t_cal)))
+    rows = np.linspace(0, n_rows - 1, k).astype(np.int32)
     t = time.perf_counter()
     oracle.conv_f64(nbr, f, w, rows=rows)
-    t_conv = (time.perf_counter() - t) / k * wl.n
-    us_per_layer = (t_map + wl.layers * t_conv) / wl.layers * 1e6
-    sample = (f"full kernel map (K={prep['K']}), masks, order and pair lists ({prep['G']} group(s)) of "
-              f"N={wl.n}; fp64 conv on {k} of {wl.n} rows (evenly spaced) scaled to N; {wl.layers} layer(s)")
+    t_conv = (time.perf_counter() - t) / max(1, k) * n_rows
+    us_per_layer = (t_map + layers * t_conv) / layers * 1e6
+    what = "strided map (kernel 3, stride 2)" if prep["conv"] == "strided" else f"full kernel map (K={prep['K']})"
+    sample = (f"{what}, masks, order and pair lists ({prep['G']} group(s)) of N={wl.n}; fp64 conv on {k} of "
+              f"{n_rows} output rows (evenly spaced) scaled to all; {layers} layer(s)")
     return us_per_layer, oracle.max_threads(), sample
 
 
-def cpu_baseline(workload, budget_s, kernel_size=3, groups=0):
-    us, cores, sample = time_oracle(prepare_oracle(workload, kernel_size, groups), budget_s)
+def cpu_baseline(workload, budget_s, kernel_size=3, groups=0, conv="submanifold"):
+    us, cores, sample = time_oracle(prepare_oracle(workload, kernel_size, groups, conv), budget_s)
     return {"value": round(us, 3), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
 
 
 def run_reference(args):
-    prep = prepare_oracle(args.workload, args.kernel_size, args.groups)
+    prep = prepare_oracle(args.workload, args.kernel_size, args.groups, args.conv)
     wl = prep["wl"]
     # the whole run stays within about two minutes of oracle work
     budget = max(0.05, min(args.ref_budget, 120.0 / (args.steps + args.warmup)))
@@ -416,15 +429,16 @@ def run_reference(args):
         if i >= args.warmup:
             per_step.append(us)
     value = statistics.mean(per_step)
+    layers = 1 if args.conv == "strided" else wl.layers
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value * wl.layers / 1e3, 4),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value * layers / 1e3, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": DATA,
         "config": {"workload": f"{args.workload}: N={wl.n}, C_in={wl.c_in}, C_out={wl.c_out}, "
-                               f"layers={wl.layers}, batch={wl.batch_size}, "
+                               f"layers={layers}, batch={wl.batch_size}, "
                                f"grid={'x'.join(map(str, wl.spatial_shape))}",
-                   "kernel_size": prep["K"], "groups": prep["G"]},
+                   "kernel_size": prep["K"], "groups": prep["G"], "conv": prep["conv"]},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -448,6 +462,9 @@ def main():
                     help="K of the K x K x K kernel (the workloads are quoted for 3)")
     ap.add_argument("--groups", type=int, default=0,
                     help="offset groups (0: 1 for K = 3, K for K = 5; or K)")
+    ap.add_argument("--conv", default="submanifold", choices=["submanifold", "strided"],
+                    help="submanifold convolution (the workloads' layers), or one strided layer "
+                         "(kernel 3, stride 2, padding 1) on the workload's sites")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle conv work for the cpu_baseline leg (0 disables)")
     ap.add_argument("--ref-budget", type=float, default=2.0,
@@ -475,7 +492,8 @@ def main():
         torch.distributed.destroy_process_group()
     if rank == 0 and out is not None:
         if world == 1 and args.cpu_budget > 0:
-            out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget, args.kernel_size, args.groups)
+            out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget, args.kernel_size, args.groups,
+                                               args.conv)
         print(json.dumps(out), flush=True)
 
 

@@ -160,6 +160,9 @@ typedef struct {
     int32_t gemm;        /* spconv_gemm_t the bf16 forward uses (TILE_UNION or TAP_MAJOR) */
     int32_t kernel_size; /* K                                                     */
     int32_t groups;      /* G offset groups                                       */
+    int64_t n_in;        /* rows of the features a forward reads (n but for strided and inverse maps) */
+    int32_t conv;        /* 0 submanifold, 1 strided, 2 inverse of a strided map  */
+    int32_t out_shape[3];/* spatial shape of the map's rows (a strided map: the output grid) */
 } spconv_map_info_t;
 
 /*
@@ -189,10 +192,50 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
                      void* stream, spconv_map_t* out_map);
 
 /*
+ * The map of a strided (downsampling) sparse convolution: kernel 3, stride 2,
+ * padding 1 per axis ("Sparse convolution in FP32", "Calibrated bit order":
+ * the strided kernels, which change the coordinate set).  Its rows are the
+ * output sites: every o of the output grid, X' = (X - 1) / 2 + 1 per axis,
+ * whose window {2o + d : d in {-1,0,1}^3} holds an input site of the same
+ * batch, in ascending (b, x, y, z) order; tap k of row o is the input row at
+ * 2o + d_k.  A forward on it computes out[o] = sum_k W[k]^T f(2o + d_k):
+ * feats [n][c_in] on the input sites, out [n_out][c_out] (torch conv3d with
+ * stride 2 and padding 1, read at the output sites).
+ *
+ *   coords_dev, n, spatial_shape, batch_size: as spconv_build_map (n < 2^27).
+ *   kernel_size 3 and stride 2 only (else SPCONV_ERR_UNSUPPORTED).
+ *   opt: mapper AUTO or HASH, pipeline AUTO or MULTI, gemm not TAP_MAJOR,
+ *        groups 0 or 1 (else SPCONV_ERR_UNSUPPORTED).
+ * Synchronises the stream once: the number of output sites sizes the map.
+ * spconv_map_info gives n (output sites), n_in and out_shape;
+ * spconv_map_out_coords copies the output sites' coordinates.
+ */
+int spconv_build_map_strided(const int32_t* coords_dev, int64_t n, const int32_t* spatial_shape,
+                             int32_t batch_size, int32_t kernel_size, int32_t stride, const spconv_options_t* opt,
+                             void* stream, spconv_map_t* out_map);
+
+/*
+ * The map of the inverse (transposed) convolution of a strided map: rows are
+ * the strided map's input sites (its n_in), tap k of row i is the output site
+ * o with 2o + d_k at site i, or none.  A forward on it computes
+ * out[i] = sum_k W[k]^T g(o_k(i)) with g [n_out][c_in] on the strided map's
+ * output sites and out [n_in][c_out] (torch conv_transpose3d, stride 2,
+ * padding 1, read at the input sites).  Enqueued on the strided map's stream,
+ * which the strided map must outlive until then; no synchronisation.
+ * opt: bit_order and gemm (not TAP_MAJOR) are used; NULL for defaults.
+ */
+int spconv_build_map_inverse(spconv_map_t strided, const spconv_options_t* opt, spconv_map_t* out_map);
+
+/* Copy a strided map's output sites, int32 [n][4] (b, x, y, z), to caller
+ * device memory, enqueued on stream.  SPCONV_ERR_INVALID_ARG for other maps. */
+int spconv_map_out_coords(spconv_map_t map, int32_t* out_coords_dev, void* stream);
+
+/*
  * out = subm_conv(feats, weights) over the map's sites (the definition at the
  * top of this file).
  *
- *   feats_dev    [n][c_in] row-major, dtype elements, 16-byte aligned.
+ *   feats_dev    [n_in][c_in] row-major, dtype elements, 16-byte aligned
+ *                (n_in = n but for strided and inverse maps, spconv_map_info).
  *   weights_dev  [V][c_in][c_out] row-major, dtype elements (V = K^3 of the map).
  *   out_dev      [n][c_out] row-major, dtype elements, 16-byte aligned; must
  *                not overlap feats (SPCONV_ERR_ALIAS).

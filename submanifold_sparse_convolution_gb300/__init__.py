@@ -67,12 +67,15 @@ def _require_cuda(t: torch.Tensor, name: str):
 class Map:
     """A kernel map (handle ``spconv_map_t``); shared by every layer on these sites."""
 
-    def __init__(self, handle: ctypes.c_void_p, n: int, coords: torch.Tensor, kernel_size: int = 3):
+    def __init__(self, handle: ctypes.c_void_p, n: int, coords: torch.Tensor, kernel_size: int = 3,
+                 n_in: Optional[int] = None, keep=None):
         self._h = handle
-        self.n = n
+        self.n = n                 # rows: the sites the output lives on
+        self.n_in = n if n_in is None else n_in   # rows of the features a forward reads
         self.kernel_size = kernel_size
         self.taps = kernel_size ** 3
         self._coords = coords      # kept alive while the build may still read it
+        self._keep = keep          # (an inverse map: the strided map it reads)
 
     @property
     def handle(self) -> ctypes.c_void_p:
@@ -177,6 +180,48 @@ def _epilogue(n: int, c_out: int, dtype: torch.dtype, device, scale, bias, resid
     return e, tuple(keep)
 
 
+def build_map_strided(coords: torch.Tensor, spatial_shape: Optional[Sequence[int]] = None,
+                      batch_size: int = 0, kernel_size: int = 3, stride: int = 2, bit_order: str = "calibrated",
+                      stream: Optional[torch.cuda.Stream] = None) -> Map:
+    """``spconv_build_map_strided``: the map of a strided convolution (kernel 3, stride 2,
+    padding 1) from the input sites ``coords``; its rows are the output sites
+    (``map_out_coords``).  Synchronises the stream once."""
+    lib = library()
+    _require_cuda(coords, "coords")
+    if coords.dtype != torch.int32 or coords.dim() != 2 or coords.shape[1] != 4:
+        raise ValueError("coords must be int32 [N, 4]")
+    shape_arr = None
+    if spatial_shape is not None:
+        shape_arr = (ctypes.c_int32 * 3)(*[int(v) for v in spatial_shape])
+    opt = _native.Options(0, BIT_ORDERS[bit_order], 0, 0, 0, 0)
+    h = ctypes.c_void_p()
+    rc = lib.spconv_build_map_strided(_ptr(coords), int(coords.shape[0]),
+                                      ctypes.cast(shape_arr, _native.c_int32_p) if shape_arr is not None else None,
+                                      int(batch_size), int(kernel_size), int(stride), ctypes.byref(opt),
+                                      _stream_ptr(stream), ctypes.byref(h))
+    _check(rc, "spconv_build_map_strided")
+    info = _native.MapInfo()
+    _check(lib.spconv_map_info(h, ctypes.byref(info)), "spconv_map_info")
+    return Map(h, int(info.n), coords, 3, n_in=int(coords.shape[0]))
+
+
+def build_map_inverse(m: Map, bit_order: str = "calibrated") -> Map:
+    """``spconv_build_map_inverse``: the map of the transposed convolution of strided map
+    ``m``, from its output sites back onto its input sites."""
+    opt = _native.Options(0, BIT_ORDERS[bit_order], 0, 0, 0, 0)
+    h = ctypes.c_void_p()
+    _check(library().spconv_build_map_inverse(m.handle, ctypes.byref(opt), ctypes.byref(h)),
+           "spconv_build_map_inverse")
+    return Map(h, m.n_in, m._coords, 3, n_in=m.n, keep=m)
+
+
+def map_out_coords(m: Map, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """``spconv_map_out_coords``: a strided map's output sites, int32 [n, 4]."""
+    out = torch.empty((m.n, 4), dtype=torch.int32, device=torch.device("cuda", torch.cuda.current_device()))
+    _check(library().spconv_map_out_coords(m.handle, _ptr(out), _stream_ptr(stream)), "spconv_map_out_coords")
+    return out
+
+
 def subm_forward(m: Map, feats: torch.Tensor, weights: torch.Tensor,
                  out: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None, *,
@@ -195,8 +240,8 @@ def subm_forward(m: Map, feats: torch.Tensor, weights: torch.Tensor,
     _require_cuda(weights, "weights")
     if feats.dtype not in _DTYPES or weights.dtype != feats.dtype:
         raise ValueError("feats and weights must both be bf16 or both fp32")
-    if feats.dim() != 2 or feats.shape[0] != m.n:
-        raise ValueError(f"feats must be [{m.n}, C_in]")
+    if feats.dim() != 2 or feats.shape[0] != m.n_in:
+        raise ValueError(f"feats must be [{m.n_in}, C_in]")
     if weights.dim() != 3 or weights.shape[0] != m.taps or weights.shape[1] != feats.shape[1]:
         raise ValueError(f"weights must be [{m.taps}, C_in, C_out]")
     c_in, c_out = int(weights.shape[1]), int(weights.shape[2])
@@ -242,8 +287,8 @@ def subm_forward_packed(m: Map, feats: torch.Tensor, wp: WPack, out: Optional[to
     the epilogue arguments are those of ``subm_forward``."""
     lib = library()
     _require_cuda(feats, "feats")
-    if feats.dtype != wp.dtype or feats.dim() != 2 or feats.shape != (m.n, wp.c_in):
-        raise ValueError(f"feats must be {wp.dtype} [{m.n}, {wp.c_in}]")
+    if feats.dtype != wp.dtype or feats.dim() != 2 or feats.shape != (m.n_in, wp.c_in):
+        raise ValueError(f"feats must be {wp.dtype} [{m.n_in}, {wp.c_in}]")
     if wp.taps != m.taps:
         raise ValueError(f"weights pack has {wp.taps} taps, the map {m.taps}")
     if out is None:
@@ -277,7 +322,9 @@ def map_info(m: Map) -> dict:
                 pipeline={1: "fused", 2: "multi", 3: "wide"}.get(info.pipeline, str(info.pipeline)),
                 key_bits=info.key_bits, shape=tuple(info.shape), batch_size=info.batch_size,
                 gemm={1: "tile_union", 2: "tap_major"}.get(info.gemm, str(info.gemm)),
-                kernel_size=info.kernel_size, groups=info.groups)
+                kernel_size=info.kernel_size, groups=info.groups, n_in=info.n_in,
+                conv={0: "submanifold", 1: "strided", 2: "inverse"}.get(info.conv, str(info.conv)),
+                out_shape=tuple(info.out_shape))
 
 
 def map_export(m: Map, stream: Optional[torch.cuda.Stream] = None) -> dict:

@@ -26,7 +26,8 @@ class MapInfo(ctypes.Structure):
                 ("pipeline", ctypes.c_int32),
                 ("key_bits", ctypes.c_int32), ("shape", ctypes.c_int32 * 3),
                 ("batch_size", ctypes.c_int32), ("gemm", ctypes.c_int32),
-                ("kernel_size", ctypes.c_int32), ("groups", ctypes.c_int32)]
+                ("kernel_size", ctypes.c_int32), ("groups", ctypes.c_int32),
+                ("n_in", ctypes.c_int64), ("conv", ctypes.c_int32), ("out_shape", ctypes.c_int32 * 3)]
 
 
 class Epilogue(ctypes.Structure):
@@ -39,6 +40,12 @@ SIGNATURES = {
     "spconv_build_map": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, c_int32_p, ctypes.c_int32,
                                         ctypes.c_int32, ctypes.POINTER(Options), ctypes.c_void_p,
                                         ctypes.POINTER(ctypes.c_void_p)]),
+    "spconv_build_map_strided": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, c_int32_p, ctypes.c_int32,
+                                                ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Options),
+                                                ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
+    "spconv_build_map_inverse": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(Options),
+                                                ctypes.POINTER(ctypes.c_void_p)]),
+    "spconv_map_out_coords": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "spconv_subm_forward": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.c_void_p]),

@@ -40,7 +40,8 @@ int check_forward_args(const MapHandle* h, const void* feats, const void* out, i
     if (!feats || !out) return SPCONV_ERR_INVALID_ARG;
     const size_t es = dtype == SPCONV_FP32 ? 4 : 2;
     if (!aligned(feats, es) || !aligned(out, es)) return SPCONV_ERR_INVALID_ARG;
-    if (overlaps(feats, static_cast<size_t>(h->n) * c_in * es, out, static_cast<size_t>(h->n) * c_out * es))
+    const int64_t n_in = h->n_in >= 0 ? h->n_in : h->n;
+    if (overlaps(feats, static_cast<size_t>(n_in) * c_in * es, out, static_cast<size_t>(h->n) * c_out * es))
         return SPCONV_ERR_ALIAS;
     return SPCONV_OK;
 }
@@ -163,6 +164,96 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
     }
     *out_map = h;
     return SPCONV_OK;
+}
+
+int spconv_build_map_strided(const int32_t* coords_dev, int64_t n, const int32_t* spatial_shape,
+                             int32_t batch_size, int32_t kernel_size, int32_t stride, const spconv_options_t* opt,
+                             void* stream, spconv_map_t* out_map) {
+    reset_launch_count();
+    if (!out_map) return SPCONV_ERR_INVALID_ARG;
+    *out_map = nullptr;
+    if (n < 0 || n >= (int64_t(1) << 27)) return SPCONV_ERR_INVALID_ARG;   // 8 n candidates in int32 ranks
+    if (n > 0 && (!coords_dev || !aligned(coords_dev, 16))) return SPCONV_ERR_INVALID_ARG;
+    if (kernel_size != 3 || stride != 2) return SPCONV_ERR_UNSUPPORTED;
+    if (batch_size < 0) return SPCONV_ERR_INVALID_ARG;
+    if (opt) {
+        if (opt->mapper != SPCONV_MAPPER_AUTO && opt->mapper != SPCONV_MAPPER_HASH) return SPCONV_ERR_UNSUPPORTED;
+        if (opt->bit_order != SPCONV_ORDER_CALIBRATED && opt->bit_order != SPCONV_ORDER_PLAIN)
+            return SPCONV_ERR_INVALID_ARG;
+        if (opt->pipeline != SPCONV_PIPELINE_AUTO && opt->pipeline != SPCONV_PIPELINE_MULTI)
+            return SPCONV_ERR_UNSUPPORTED;
+        if (opt->gemm == SPCONV_GEMM_TAP_MAJOR) return SPCONV_ERR_UNSUPPORTED;
+        if (opt->gemm < SPCONV_GEMM_AUTO || opt->gemm > SPCONV_GEMM_TAP_MAJOR) return SPCONV_ERR_INVALID_ARG;
+        if (opt->groups != 0 && opt->groups != 1) return SPCONV_ERR_UNSUPPORTED;
+    }
+    int32_t shape[3] = {1, 1, 1};
+    int32_t batch = batch_size;
+    if (spatial_shape) {
+        for (int a = 0; a < 3; ++a) {
+            if (spatial_shape[a] < 1 || spatial_shape[a] >= (1 << 30)) return SPCONV_ERR_INVALID_ARG;
+            shape[a] = spatial_shape[a];
+        }
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!spatial_shape || batch <= 0) {
+        int32_t dshape[3], dbatch = 1;
+        SPCONV_CHECK(derive_shape(coords_dev, n, s, dshape, &dbatch));
+        if (!spatial_shape) std::memcpy(shape, dshape, sizeof(shape));
+        if (batch <= 0) batch = dbatch;
+    }
+    spconv_map_s* h = new (std::nothrow) spconv_map_s();
+    if (!h) return SPCONV_ERR_OOM;
+    h->stream = s;
+    cudaGetDevice(&h->device);
+    std::memcpy(h->shape, shape, sizeof(shape));
+    h->batch = batch;
+    h->kernel_size = 3;
+    h->taps = kTaps;
+    h->groups = 1;
+    const int rc = build_map_strided(h, coords_dev, n, opt);
+    if (rc != SPCONV_OK) {
+        if (h->arena) cudaFreeAsync(h->arena, s);
+        if (h->out_alloc) cudaFreeAsync(h->out_alloc, s);
+        delete h;
+        return rc;
+    }
+    *out_map = h;
+    return SPCONV_OK;
+}
+
+int spconv_build_map_inverse(spconv_map_t strided, const spconv_options_t* opt, spconv_map_t* out_map) {
+    reset_launch_count();
+    if (!out_map) return SPCONV_ERR_INVALID_ARG;
+    *out_map = nullptr;
+    if (!strided || strided->conv != kConvStrided) return SPCONV_ERR_INVALID_ARG;
+    if (opt) {
+        if (opt->bit_order != SPCONV_ORDER_CALIBRATED && opt->bit_order != SPCONV_ORDER_PLAIN)
+            return SPCONV_ERR_INVALID_ARG;
+        if (opt->gemm == SPCONV_GEMM_TAP_MAJOR) return SPCONV_ERR_UNSUPPORTED;
+    }
+    spconv_map_s* h = new (std::nothrow) spconv_map_s();
+    if (!h) return SPCONV_ERR_OOM;
+    h->stream = strided->stream;
+    h->device = strided->device;
+    h->kernel_size = 3;
+    h->taps = kTaps;
+    h->groups = 1;
+    const int rc = build_map_inverse(h, strided, opt);
+    if (rc != SPCONV_OK) {
+        if (h->arena) cudaFreeAsync(h->arena, h->stream);
+        delete h;
+        return rc;
+    }
+    *out_map = h;
+    return SPCONV_OK;
+}
+
+int spconv_map_out_coords(spconv_map_t map, int32_t* out_coords_dev, void* stream) {
+    if (!map || !map->out_coords) return SPCONV_ERR_INVALID_ARG;
+    if (map->n == 0) return SPCONV_OK;
+    if (!out_coords_dev) return SPCONV_ERR_INVALID_ARG;
+    return cuda_status(cudaMemcpyAsync(out_coords_dev, map->out_coords, static_cast<size_t>(map->n) * 16,
+                                       cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)));
 }
 
 int spconv_subm_forward(spconv_map_t map, const void* feats_dev, const void* weights_dev, void* out_dev,
@@ -295,6 +386,9 @@ int spconv_map_info(spconv_map_t map, spconv_map_info_t* info) {
     info->gemm = map->gemm;
     info->kernel_size = map->kernel_size;
     info->groups = map->groups;
+    info->n_in = map->n_in >= 0 ? map->n_in : map->n;
+    info->conv = map->conv;
+    std::memcpy(info->out_shape, map->conv == kConvStrided ? map->out_shape : map->shape, sizeof(info->out_shape));
     return SPCONV_OK;
 }
 
@@ -333,6 +427,7 @@ void spconv_map_destroy(spconv_map_t map) {
     if (map->arena) cudaFreeAsync(map->arena, map->stream);
     if (map->wspace) cudaFreeAsync(map->wspace, map->stream);
     if (map->acc) cudaFreeAsync(map->acc, map->stream);
+    if (map->out_alloc) cudaFreeAsync(map->out_alloc, map->stream);
     delete map;
 }
 

@@ -49,10 +49,22 @@ struct DevBuf {
     size_t bytes = 0;
 };
 
+// What a map's rows and neighbours are: a submanifold map (rows and
+// neighbours are the same sites), a strided map (rows are the output sites of
+// a kernel-3, stride-2, padding-1 convolution, neighbours the input sites), or
+// the inverse of a strided map (rows the strided map's input sites,
+// neighbours its output sites).
+enum : int32_t { kConvSubmanifold = 0, kConvStrided = 1, kConvInverse = 2 };
+
 struct MapHandle {
     cudaStream_t stream = nullptr;
     int device = 0;
-    int64_t n = 0;
+    int64_t n = 0;            // rows (output sites)
+    int64_t n_in = -1;        // sites the neighbours index (feature rows of a forward); -1: n
+    int32_t conv = kConvSubmanifold;
+    int32_t out_shape[3] = {0, 0, 0};   // spatial shape of the row sites (strided: the output grid)
+    int32_t* out_coords = nullptr;      // strided and inverse maps: [n][4] (b, x, y, z) of the rows
+    void* out_alloc = nullptr;          // the allocation holding out_coords
     int64_t n_tiles = 0;
     int64_t n_pad = 0;        // n_tiles * kTileRows
     int32_t shape[3] = {0, 0, 0};
@@ -121,6 +133,11 @@ struct Epilogue {
 int build_map_impl(MapHandle* h, const int32_t* coords, const spconv_options_t* opt);
 // K != 3 or more than one offset group (map_groups.cu)
 int build_map_grouped(MapHandle* h, const int32_t* coords, const spconv_options_t* opt);
+// strided (kernel 3, stride 2, padding 1) map of coords [n_in][4]; synchronises once (the
+// number of output sites sizes the map); h->shape is the input shape
+int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const spconv_options_t* opt);
+// the inverse of strided map src, into h (same device and stream)
+int build_map_inverse(MapHandle* h, const MapHandle* src, const spconv_options_t* opt);
 int derive_shape(const int32_t* coords, int64_t n, cudaStream_t stream, int32_t shape[3],
                  int32_t* batch);
 

@@ -88,6 +88,7 @@ struct TcParams {
     float* acc;                   // [n][c_out] tap-major: fp32 sums (zero at launch)
     int32_t* status;
     int64_t n, n_pad;
+    int64_t n_in;                 // rows of feats (gather bound)
     int32_t n_items;              // n_tiles * n_nb
     int32_t c_in, c_out;
     int32_t k_chunks;             // ceil(c_in / 64)
@@ -444,11 +445,11 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                     for (int i = 0; i < RG; ++i) {
                         const int32_t src_row = sr[i];
                         const uint32_t dst = dst0 + i * 128 + ((chunk ^ (i & 7)) << 4);
-                        if (src_row >= 0 && src_row < p.n && col_ok)
+                        if (src_row >= 0 && src_row < p.n_in && col_ok)
                             ptx::cp_async_16(dst, fcol + static_cast<int64_t>(src_row) * p.c_in, 16u);
                         else
                             ptx::st_shared_zero16(dst);   // absent neighbour: no memory request
-                        bad |= src_row >= p.n;
+                        bad |= src_row >= p.n_in;
                     }
                     if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.status, kStatusInternal);
                     ptx::cp_async_commit();
@@ -805,6 +806,7 @@ int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, in
     p.status = h->status;
     p.n = h->n;
     p.n_pad = h->n_pad;
+    p.n_in = h->n_in >= 0 ? h->n_in : h->n;
     p.c_in = c_in;
     p.c_out = c_out;
     p.k_chunks = (c_in + BK - 1) / BK;

@@ -528,9 +528,111 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write(const int32_t* __rest
     }
 }
 
+// ---------------------------------------------------------------------------
+// strided maps: the output sites and the query sites 2o
+// ---------------------------------------------------------------------------
+// Output key of site (b, x, y, z) of the strided grid: fields of widths
+// ow[0..2] (x, y, z), the batch above them; ~0 for no site.
+struct OutLayout {
+    int wx, wy, wz;
+    int3 shape;   // output shape
+};
+
+__device__ __forceinline__ uint64_t out_key(int b, int x, int y, int z, const OutLayout& O) {
+    return ((((static_cast<uint64_t>(b) << O.wx) | static_cast<uint64_t>(x)) << O.wy | static_cast<uint64_t>(y))
+            << O.wz) |
+           static_cast<uint64_t>(z);
+}
+
+// Per input site, the up to 8 output sites whose window {2o + d} holds it:
+// o = (c - d) / 2 for the d of matching parity on each axis, inside the
+// output shape.  cand[8 i + j] (~0 where there is none).
+__global__ void __launch_bounds__(kGBlock) kst_candidates(const int4* __restrict__ coords, int64_t n, int3 shape,
+                                                          int batch, const OutLayout O, uint64_t* __restrict__ cand,
+                                                          uint32_t* __restrict__ vals) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
+    if (i >= n) return;
+    const int4 c = coords[i];
+    const bool ok = in_range(c, shape, batch);
+    int j = 0;
+    for (int dx = -1; dx <= 1; ++dx)
+        for (int dy = -1; dy <= 1; ++dy)
+            for (int dz = -1; dz <= 1; ++dz) {
+                const int px = c.y - dx, py = c.z - dy, pz = c.w - dz;
+                if (!ok || px < 0 || py < 0 || pz < 0 || (px & 1) || (py & 1) || (pz & 1)) continue;
+                const int ox = px >> 1, oy = py >> 1, oz = pz >> 1;
+                if (ox >= O.shape.x || oy >= O.shape.y || oz >= O.shape.z) continue;
+                cand[8 * i + j] = out_key(c.x, ox, oy, oz, O);
+                vals[8 * i + j] = 0;
+                ++j;
+            }
+    for (; j < 8; ++j) {
+        cand[8 * i + j] = kNoKey;
+        vals[8 * i + j] = 0;
+    }
+}
+
+// flags[j] = 1 for the first of each run of equal sorted keys (not ~0).
+__global__ void __launch_bounds__(kGBlock) kst_first(const uint64_t* __restrict__ keys, int64_t m,
+                                                     int32_t* __restrict__ flags) {
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
+    if (j >= m) return;
+    const uint64_t k = keys[j];
+    flags[j] = (k != kNoKey && (j == 0 || keys[j - 1] != k)) ? 1 : 0;
+}
+
+// After the exclusive scan of the flags: output row rank[j] is site keys[j];
+// writes its coordinates, its query site 2o in input coordinates, and the
+// count of sites (into *count, by the last entry).
+__global__ void __launch_bounds__(kGBlock) kst_outputs(const uint64_t* __restrict__ keys,
+                                                       const int32_t* __restrict__ flags_first,
+                                                       const int32_t* __restrict__ rank, int64_t m, const OutLayout O,
+                                                       int4* __restrict__ out_coords, int4* __restrict__ query,
+                                                       int64_t cap, int64_t* __restrict__ count) {
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
+    if (j >= m) return;
+    if (j == m - 1) *count = static_cast<int64_t>(rank[j]) + flags_first[j];
+    if (!flags_first[j]) return;
+    const uint64_t k = keys[j];
+    const int z = static_cast<int>(k & ((uint64_t(1) << O.wz) - 1));
+    const int y = static_cast<int>((k >> O.wz) & ((uint64_t(1) << O.wy) - 1));
+    const int x = static_cast<int>((k >> (O.wz + O.wy)) & ((uint64_t(1) << O.wx) - 1));
+    const int b = static_cast<int>(k >> (O.wz + O.wy + O.wx));
+    const int64_t r = rank[j];
+    if (r < cap) {
+        out_coords[r] = make_int4(b, x, y, z);
+        query[r] = make_int4(b, 2 * x, 2 * y, 2 * z);
+    }
+}
+
+// Inverse map: for every (o, k) of the strided map with input row i,
+// inv[i][k] = o (one writer per entry: o is fixed by i and k).
+__global__ void __launch_bounds__(kGBlock) kg_inverse_scatter(const int32_t* __restrict__ nbr, int stride, int64_t n,
+                                                              int32_t* __restrict__ inv, int inv_stride) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
+    if (idx >= n * kTaps) return;
+    const int64_t o = idx / kTaps;
+    const int k = static_cast<int>(idx % kTaps);
+    const int32_t i = nbr[o * stride + k];
+    if (i >= 0) inv[static_cast<int64_t>(i) * inv_stride + k] = static_cast<int32_t>(o);
+}
+
+// The whole grouped build for one of three sources of the neighbours: the
+// sites themselves (coords, n_table = h->n rows), the input sites of a
+// strided map (table coords [n_table], query sites [h->n], hash mapper), or
+// the inverse of strided map src.
+int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coords, int64_t n_table,
+                 const int32_t* query, const MapHandle* src);
+
 }  // namespace
 
 int build_map_grouped(MapHandle* h, const int32_t* coords, const spconv_options_t* opt) {
+    return grouped_core(h, opt, coords, h->n, nullptr, nullptr);
+}
+
+namespace {
+int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coords, int64_t n_table,
+                 const int32_t* query, const MapHandle* src) {
     cudaStream_t s = h->stream;
     const int64_t n = h->n;
     const int64_t T = (n + kTileRows - 1) / kTileRows;
@@ -574,11 +676,16 @@ int build_map_grouped(MapHandle* h, const int32_t* coords, const spconv_options_
     const int64_t cells = cells_d > 9.0e18 ? 0 : static_cast<int64_t>(B) * L.gsb;
     int mapper = opt ? opt->mapper : SPCONV_MAPPER_AUTO;
     const int64_t dense_max = (opt && opt->dense_max_cells > 0) ? opt->dense_max_cells : (int64_t(1) << 24);
-    const int row_bits = std::max(1, bit_len(static_cast<uint64_t>(n > 0 ? n - 1 : 0)));
+    const int row_bits = std::max(1, bit_len(static_cast<uint64_t>(n_table > 0 ? n_table - 1 : 0)));
     // AUTO: the dense grid on small boxes; else, for K = 3, hashed keys when they
     // pack with the row (outdoor in 3 groups: map 197 -> 130 us), and sorted keys
     // for K = 5, where the per-row hash lookup of 125 taps measured slower (outdoor
     // 339 vs 354 us, 240k rows 1364 vs 1747 us)
+    if (query) {   // strided: the input sites go in a hash table
+        if (mapper != SPCONV_MAPPER_AUTO && mapper != SPCONV_MAPPER_HASH) return SPCONV_ERR_UNSUPPORTED;
+        mapper = SPCONV_MAPPER_HASH;
+    }
+    if (src) mapper = src->mapper;   // inverse: read off the strided map (reported as its mapper)
     if (mapper == SPCONV_MAPPER_AUTO)
         mapper = (cells_d <= 9.0e18 && cells <= dense_max) ? SPCONV_MAPPER_DENSE
                  : (K == 3 && key_bits + row_bits <= 64) ? SPCONV_MAPPER_HASH : SPCONV_MAPPER_SORTED;
@@ -596,6 +703,7 @@ int build_map_grouped(MapHandle* h, const int32_t* coords, const spconv_options_
     const int64_t np = std::max<int64_t>(1, h->n_pad);
     const int64_t t1 = std::max<int64_t>(1, T);
     const int64_t nb = std::max<int64_t>(1, rsort::num_tiles(std::max(G * n, mapper == SPCONV_MAPPER_SORTED ? n : 0)));
+    const int64_t nt1 = std::max<int64_t>(1, n_table);
     size_t bytes = 0;
     auto add = [&](size_t count, size_t elem) { bytes += (count * elem + 255) / 256 * 256; };
     add(4, 4);                                        // status
@@ -610,8 +718,10 @@ int build_map_grouped(MapHandle* h, const int32_t* coords, const spconv_options_
     add(gn, 4); add(gn, 4); add(gn, 4); add(gn, 4);   // mask keys and row ids, ping-pong
     add(rsort::kBins * nb, 4);                        // radix histograms
     int table_log2 = 11;
-    while ((int64_t(1) << table_log2) < kGHashSlotsPerRow * n) ++table_log2;
-    if (mapper == SPCONV_MAPPER_SORTED) {
+    while ((int64_t(1) << table_log2) < kGHashSlotsPerRow * nt1) ++table_log2;
+    if (src) {
+        // the neighbours come from the strided map
+    } else if (mapper == SPCONV_MAPPER_SORTED) {
         add(n1, 8); add(n1, 8); add(n1, 4); add(n1, 4);   // coordinate keys and rows, ping-pong
     } else if (mapper == SPCONV_MAPPER_HASH) {
         add(size_t(1) << table_log2, 8);                 // hash table
@@ -660,7 +770,15 @@ int build_map_grouped(MapHandle* h, const int32_t* coords, const spconv_options_
     const int4* c4 = reinterpret_cast<const int4*>(coords);
     const int3 shape3 = make_int3(X, Y, Z);
     int launches = 0;
-    if (mapper == SPCONV_MAPPER_SORTED) {
+    if (src) {
+        // the strided map read backwards; the tap counts are the same incidences
+        kg_inverse_scatter<<<blocks(src->n * kTaps, kGBlock), kGBlock, 0, s>>>(src->nbr, src->nbr_stride, src->n,
+                                                                              h->nbr, h->nbr_stride);
+        SPCONV_CHECK_CUDA(cudaMemcpyAsync(h->tap_count, src->tap_count, V * sizeof(int32_t),
+                                          cudaMemcpyDeviceToDevice, s));
+        SPCONV_CHECK_CUDA(cudaMemcpyAsync(h->status, src->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+        ++launches;
+    } else if (mapper == SPCONV_MAPPER_SORTED) {
         uint64_t* ck_a = take<uint64_t>(p, n1);
         uint64_t* ck_b = take<uint64_t>(p, n1);
         uint32_t* cv_a = take<uint32_t>(p, n1);
@@ -676,13 +794,14 @@ int build_map_grouped(MapHandle* h, const int32_t* coords, const spconv_options_
     } else if (mapper == SPCONV_MAPPER_HASH) {
         uint64_t* table = take<uint64_t>(p, size_t(1) << table_log2);
         SPCONV_CHECK_CUDA(cudaMemsetAsync(table, 0, (size_t(1) << table_log2) * 8, s));
-        kg_hash_insert<<<blocks(n, kGBlock), kGBlock, 0, s>>>(c4, n, shape3, B, L, table, table_log2, row_bits,
-                                                              h->status);
+        kg_hash_insert<<<blocks(n_table, kGBlock), kGBlock, 0, s>>>(c4, n_table, shape3, B, L, table, table_log2,
+                                                                    row_bits, h->status);
+        const int4* q4 = query ? reinterpret_cast<const int4*>(query) : c4;
         if (K == 3)
-            kg_hash_lookup<3><<<blocks(n, kGBlock), kGBlock, 0, s>>>(c4, n, shape3, B, L, table, table_log2, row_bits,
+            kg_hash_lookup<3><<<blocks(n, kGBlock), kGBlock, 0, s>>>(q4, n, shape3, B, L, table, table_log2, row_bits,
                                                                      h->nbr, h->tap_count);
         else
-            kg_hash_lookup<5><<<blocks(n, kGBlock), kGBlock, 0, s>>>(c4, n, shape3, B, L, table, table_log2, row_bits,
+            kg_hash_lookup<5><<<blocks(n, kGBlock), kGBlock, 0, s>>>(q4, n, shape3, B, L, table, table_log2, row_bits,
                                                                      h->nbr, h->tap_count);
         launches += 2;
     } else {
@@ -708,6 +827,90 @@ int build_map_grouped(MapHandle* h, const int32_t* coords, const spconv_options_
     launches += 3;
     count_launch(launches);
     return cuda_status(cudaGetLastError());
+}
+}  // namespace
+
+int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const spconv_options_t* opt) {
+    cudaStream_t s = h->stream;
+    OutLayout O;
+    O.shape = make_int3((h->shape[0] - 1) / 2 + 1, (h->shape[1] - 1) / 2 + 1, (h->shape[2] - 1) / 2 + 1);
+    O.wx = std::max(1, bit_len(static_cast<uint64_t>(O.shape.x - 1)));
+    O.wy = std::max(1, bit_len(static_cast<uint64_t>(O.shape.y - 1)));
+    O.wz = std::max(1, bit_len(static_cast<uint64_t>(O.shape.z - 1)));
+    const int okey_bits = O.wx + O.wy + O.wz + bit_len(static_cast<uint64_t>(h->batch) - 1);
+    if (okey_bits > 62) return SPCONV_ERR_UNSUPPORTED;
+    h->conv = kConvStrided;
+    h->n_in = n_in;
+    h->out_shape[0] = O.shape.x;
+    h->out_shape[1] = O.shape.y;
+    h->out_shape[2] = O.shape.z;
+    // ---- the output sites: 8 candidates per input site, sorted, the first of each run kept
+    const int64_t m = 8 * std::max<int64_t>(1, n_in);
+    size_t bytes = 0;
+    auto add = [&](size_t count, size_t elem) { bytes += (count * elem + 255) / 256 * 256; };
+    const int64_t nb = rsort::num_tiles(m);
+    add(m, 8); add(m, 8); add(m, 4); add(m, 4);   // candidate keys and (unused) values, ping-pong
+    add(m, 4); add(m, 4);                         // first-of-run flags, their exclusive scan
+    add(rsort::kBins * std::max<int64_t>(1, nb), 4);
+    add(m, 16); add(1, 8);                        // query sites, the output count
+    void* scratch = nullptr;
+    if (pool_alloc(&scratch, bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return SPCONV_ERR_OOM;
+    }
+    char* p = static_cast<char*>(scratch);
+    uint64_t* ka = take<uint64_t>(p, m);
+    uint64_t* kb = take<uint64_t>(p, m);
+    uint32_t* va = take<uint32_t>(p, m);
+    uint32_t* vb = take<uint32_t>(p, m);
+    int32_t* flags = take<int32_t>(p, m);
+    int32_t* rank = take<int32_t>(p, m);
+    int32_t* hist = take<int32_t>(p, rsort::kBins * std::max<int64_t>(1, nb));
+    int4* query = take<int4>(p, m);
+    int64_t* count = take<int64_t>(p, 1);
+    void* outs = nullptr;
+    if (pool_alloc(&outs, static_cast<size_t>(m) * 16, s) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFreeAsync(scratch, s);
+        return SPCONV_ERR_OOM;
+    }
+    h->out_alloc = outs;
+    h->out_coords = static_cast<int32_t*>(outs);
+    int launches = 0;
+    int64_t n_out = 0;
+    SPCONV_CHECK_CUDA(cudaMemsetAsync(count, 0, 8, s));
+    if (n_in > 0) {
+        kst_candidates<<<blocks(n_in, kGBlock), kGBlock, 0, s>>>(reinterpret_cast<const int4*>(coords), n_in,
+                                                                  make_int3(h->shape[0], h->shape[1], h->shape[2]),
+                                                                  h->batch, O, ka, va);
+        ++launches;
+        const bool in_b = rsort::sort_pairs<uint64_t>(ka, va, kb, vb, m, okey_bits + 1, hist, s, &launches);
+        const uint64_t* sk = in_b ? kb : ka;
+        kst_first<<<blocks(m, kGBlock), kGBlock, 0, s>>>(sk, m, flags);
+        SPCONV_CHECK_CUDA(cudaMemcpyAsync(rank, flags, m * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+        rsort::scan_exclusive<<<1, rsort::kScanThreads, 0, s>>>(rank, m);
+        kst_outputs<<<blocks(m, kGBlock), kGBlock, 0, s>>>(sk, flags, rank, m, O,
+                                                           reinterpret_cast<int4*>(h->out_coords), query, m, count);
+        launches += 3;
+        // the one synchronisation: the output count sizes the map
+        SPCONV_CHECK_CUDA(cudaMemcpyAsync(&n_out, count, 8, cudaMemcpyDeviceToHost, s));
+        SPCONV_CHECK_CUDA(cudaStreamSynchronize(s));
+    }
+    count_launch(launches);
+    h->n = n_out;
+    const int rc = grouped_core(h, opt, coords, n_in, reinterpret_cast<const int32_t*>(query), nullptr);
+    cudaFreeAsync(scratch, s);   // stream-ordered: after the kernels that read it
+    return rc;
+}
+
+int build_map_inverse(MapHandle* h, const MapHandle* src, const spconv_options_t* opt) {
+    h->conv = kConvInverse;
+    h->n = src->n_in;
+    h->n_in = src->n;
+    std::memcpy(h->out_shape, src->shape, sizeof(h->out_shape));
+    std::memcpy(h->shape, src->shape, sizeof(h->shape));
+    h->batch = src->batch;
+    return grouped_core(h, opt, nullptr, src->n, nullptr, src);
 }
 
 }  // namespace spconv

@@ -736,6 +736,107 @@ def test_groups_empty_input():
     assert out.shape == (0, 16)
 
 
+# ---------------------------------------------------------------------------
+# strided convolution (kernel 3, stride 2, padding 1) and its inverse
+# ---------------------------------------------------------------------------
+
+def oracle_strided(coords, shape, batch, calibrated=True):
+    oc, nbr = oracle.strided_map(coords, shape, batch)
+    m = oracle.masks(nbr)
+    p = oracle.perm(oracle.sort_keys(m, oracle.tap_order(m, calibrated)))
+    tap_off, ins, outs = oracle.pair_lists(nbr, p)
+    return oc, dict(nbr=nbr, mask=m, perm=p, tap_off=tap_off, in_rows=ins, out_rows=outs)
+
+
+def oracle_inverse(nbr_s, n_in, calibrated=True):
+    inv = oracle.inverse_map(nbr_s, n_in)
+    m = oracle.masks(inv)
+    p = oracle.perm(oracle.sort_keys(m, oracle.tap_order(m, calibrated)))
+    tap_off, ins, outs = oracle.pair_lists(inv, p)
+    return dict(nbr=inv, mask=m, perm=p, tap_off=tap_off, in_rows=ins, out_rows=outs)
+
+
+STRIDED_SMALL = [(1, 1, (4, 4, 4), 1), (2, 7, (5, 5, 5), 1), (3, 129, (8, 9, 10), 2), (4, 1500, (14, 13, 12), 2),
+                 (5, 3000, (31, 30, 7), 1)]
+
+
+@pytest.mark.parametrize("seed,n,shape,batch", STRIDED_SMALL)
+@pytest.mark.parametrize("bit_order", ["calibrated", "plain"])
+def test_strided_and_inverse_maps_small(seed, n, shape, batch, bit_order):
+    wl = S.random_cloud(900 + seed, n, shape=shape, batch_size=batch)
+    m = sc.build_map_strided(wl.coords.cuda(), shape, batch, bit_order=bit_order)
+    assert sc.map_status(m) == 0
+    oc, ref = oracle_strided(wl.coords.numpy(), shape, batch, bit_order == "calibrated")
+    info = sc.map_info(m)
+    assert info["conv"] == "strided" and info["n"] == oc.shape[0] and info["n_in"] == n
+    assert info["out_shape"] == oracle.strided_shape(shape)
+    assert np.array_equal(sc.map_out_coords(m).cpu().numpy(), oc)
+    assert_map_equal(sc.map_export(m), ref)
+    mi = sc.build_map_inverse(m, bit_order=bit_order)
+    assert sc.map_status(mi) == 0
+    assert sc.map_info(mi)["conv"] == "inverse" and sc.map_info(mi)["n_in"] == oc.shape[0]
+    assert_map_equal(sc.map_export(mi), oracle_inverse(ref["nbr"], n, bit_order == "calibrated"))
+
+
+STRIDED_FWD = [(64, 64, torch.bfloat16), (128, 128, torch.bfloat16), (32, 256, torch.bfloat16),
+               (5, 7, torch.bfloat16), (16, 16, torch.float32)]
+
+
+@pytest.mark.parametrize("c_in,c_out,dtype", STRIDED_FWD)
+def test_strided_and_inverse_forward(c_in, c_out, dtype):
+    wl = S.random_cloud(950 + c_in, 2500, shape=(16, 17, 15), batch_size=2, c_in=c_in, c_out=c_out)
+    f = wl.feats.to(dtype)
+    w = wl.weights[0].to(dtype)
+    m = sc.build_map_strided(wl.coords.cuda(), wl.spatial_shape, 2)
+    y = sc.subm_forward(m, f.cuda(), w.cuda())
+    assert sc.map_status(m) == 0 and y.shape == (m.n, c_out)
+    oc, nbr = oracle.strided_map(wl.coords.numpy(), wl.spatial_shape, 2)
+    check = check_fp32 if dtype == torch.float32 else check_bf16
+    check(y, oracle.conv_f64(nbr, f.double().numpy(), w.double().numpy()))
+    # the inverse convolution back onto the input sites, with its own weights and a fused ReLU
+    rng = np.random.default_rng(951)
+    w2 = torch.from_numpy((rng.standard_normal((27, c_out, c_in)) / np.sqrt(27 * c_out)).astype(np.float32)).to(dtype)
+    mi = sc.build_map_inverse(m)
+    z = sc.subm_forward(mi, y, w2.cuda(), relu=True)
+    assert z.shape == (wl.n, c_in)
+    inv = oracle.inverse_map(nbr, wl.n)
+    check(z, oracle.epilogue_f64(oracle.conv_f64(inv, y.double().cpu().numpy(), w2.double().numpy()), relu=True))
+
+
+@pytest.mark.parametrize("name", ["outdoor", "stage"])
+def test_strided_workload(name):
+    wl = S.make_workload(name)
+    m = sc.build_map_strided(wl.coords.cuda(), wl.spatial_shape, wl.batch_size)
+    y = sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
+    assert sc.map_status(m) == 0
+    oc, ref = oracle_strided(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    assert np.array_equal(sc.map_out_coords(m).cpu().numpy(), oc)
+    assert_map_equal(sc.map_export(m), ref)
+    rows = sample_rows(m.n, 1500, 961)
+    check_bf16(y[torch.from_numpy(rows).long().cuda()],
+               oracle.conv_f64(ref["nbr"], wl.feats.double().numpy(), wl.weights[0].double().numpy(), rows=rows))
+
+
+def test_strided_errors():
+    c = torch.tensor([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=torch.int32).cuda()
+    m = sc.build_map_strided(c, (8, 8, 8), 1)
+    assert sc.map_status(m) == -5                     # duplicates, found at insertion
+    bad = torch.tensor([[0, 1, 1, 1], [0, 8, 2, 2]], dtype=torch.int32).cuda()
+    assert sc.map_status(sc.build_map_strided(bad, (8, 8, 8), 1)) == -6
+    for kw in (dict(kernel_size=5), dict(stride=1)):
+        with pytest.raises(sc.SpconvError) as e:
+            sc.build_map_strided(c[:2].contiguous(), (8, 8, 8), 1, **kw)
+        assert e.value.code == -2
+    sub = sc.build_map(c[:2].contiguous(), (8, 8, 8), 1)
+    with pytest.raises(sc.SpconvError) as e:
+        sc.build_map_inverse(sub)                     # only a strided map has an inverse
+    assert e.value.code == -1
+    with pytest.raises(sc.SpconvError):
+        sc.map_out_coords(sub)
+    empty = sc.build_map_strided(torch.empty((0, 4), dtype=torch.int32, device="cuda"), (4, 4, 4), 1)
+    assert sc.map_status(empty) == 0 and empty.n == 0
+
+
 def test_launch_count_reported():
     wl = S.random_cloud(51, 3000, shape=(16, 16, 16), c_in=64, c_out=64)
     m = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="dense", pipeline="fused")
