@@ -581,6 +581,65 @@ __global__ void __launch_bounds__(kGBlock) kst_first(const uint64_t* __restrict_
     flags[j] = (k != kNoKey && (j == 0 || keys[j - 1] != k)) ? 1 : 0;
 }
 
+// Exclusive scan of the first-of-run flags over the whole grid, in three
+// steps: per 1024-entry block the number of flags, one CTA's scan of the
+// block counts, then each block's ranks (a single-CTA scan over 8 n entries
+// was a serial walk of thousands of values per thread).
+constexpr int kRankBlock = 1024;
+
+__global__ void __launch_bounds__(kRankBlock) kst_block_count(const int32_t* __restrict__ flags, int64_t m,
+                                                              int32_t* __restrict__ bcount) {
+    __shared__ int32_t ws[kRankBlock / 32];
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * kRankBlock + threadIdx.x;
+    const int f = j < m ? flags[j] : 0;
+    const int c = __syncthreads_count(f);
+    (void)ws;
+    if (threadIdx.x == 0) bcount[blockIdx.x] = c;
+}
+
+__global__ void __launch_bounds__(kRankBlock) kst_block_scan(int32_t* __restrict__ bcount, int64_t nb) {
+    __shared__ int32_t carry;
+    __shared__ int32_t wsum[kRankBlock / 32];
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    if (t == 0) carry = 0;
+    __syncthreads();
+    for (int64_t b0 = 0; b0 < nb; b0 += kRankBlock) {
+        const int64_t i = b0 + t;
+        const int32_t v = i < nb ? bcount[i] : 0;
+        int32_t inc = v;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane == 31) wsum[w] = inc;
+        __syncthreads();
+        int32_t before = 0, total = 0;
+        for (int q = 0; q < kRankBlock / 32; ++q) {
+            before += q < w ? wsum[q] : 0;
+            total += wsum[q];
+        }
+        if (i < nb) bcount[i] = carry + before + inc - v;
+        __syncthreads();
+        if (t == 0) carry += total;
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kRankBlock) kst_block_rank(const int32_t* __restrict__ flags, int64_t m,
+                                                             const int32_t* __restrict__ bbase,
+                                                             int32_t* __restrict__ rank) {
+    __shared__ int32_t wsum[kRankBlock / 32];
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * kRankBlock + t;
+    const int32_t f = j < m ? flags[j] : 0;
+    const uint32_t b = __ballot_sync(0xFFFFFFFFu, f != 0);
+    if (lane == 0) wsum[w] = __popc(b);
+    __syncthreads();
+    int32_t before = 0;
+    for (int q = 0; q < w; ++q) before += wsum[q];
+    if (j < m) rank[j] = bbase[blockIdx.x] + before + __popc(b & ((1u << lane) - 1u));
+}
+
 // After the exclusive scan of the flags: output row rank[j] is site keys[j];
 // writes its coordinates, its query site 2o in input coordinates, and the
 // count of sites (into *count, by the last entry).
@@ -851,6 +910,7 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
     const int64_t nb = rsort::num_tiles(m);
     add(m, 8); add(m, 8); add(m, 4); add(m, 4);   // candidate keys and (unused) values, ping-pong
     add(m, 4); add(m, 4);                         // first-of-run flags, their exclusive scan
+    add((m + kRankBlock - 1) / kRankBlock, 4);    // per-block flag counts
     add(rsort::kBins * std::max<int64_t>(1, nb), 4);
     add(m, 16); add(1, 8);                        // query sites, the output count
     void* scratch = nullptr;
@@ -865,6 +925,8 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
     uint32_t* vb = take<uint32_t>(p, m);
     int32_t* flags = take<int32_t>(p, m);
     int32_t* rank = take<int32_t>(p, m);
+    const int64_t rb = (m + kRankBlock - 1) / kRankBlock;
+    int32_t* bcount = take<int32_t>(p, rb);
     int32_t* hist = take<int32_t>(p, rsort::kBins * std::max<int64_t>(1, nb));
     int4* query = take<int4>(p, m);
     int64_t* count = take<int64_t>(p, 1);
@@ -887,8 +949,10 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
         const bool in_b = rsort::sort_pairs<uint64_t>(ka, va, kb, vb, m, okey_bits + 1, hist, s, &launches);
         const uint64_t* sk = in_b ? kb : ka;
         kst_first<<<blocks(m, kGBlock), kGBlock, 0, s>>>(sk, m, flags);
-        SPCONV_CHECK_CUDA(cudaMemcpyAsync(rank, flags, m * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
-        rsort::scan_exclusive<<<1, rsort::kScanThreads, 0, s>>>(rank, m);
+        kst_block_count<<<static_cast<unsigned>(rb), kRankBlock, 0, s>>>(flags, m, bcount);
+        kst_block_scan<<<1, kRankBlock, 0, s>>>(bcount, rb);
+        kst_block_rank<<<static_cast<unsigned>(rb), kRankBlock, 0, s>>>(flags, m, bcount, rank);
+        launches += 2;
         kst_outputs<<<blocks(m, kGBlock), kGBlock, 0, s>>>(sk, flags, rank, m, O,
                                                            reinterpret_cast<int4*>(h->out_coords), query, m, count);
         launches += 3;
