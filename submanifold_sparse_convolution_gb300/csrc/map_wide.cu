@@ -45,7 +45,7 @@ namespace spconv {
 namespace {
 
 constexpr int WT = 256;                        // threads per CTA
-constexpr int WI = kWideKeysPerCta / WT;       // keys per thread in a sort pass
+constexpr int WI = kWideKeysPerCta / WT;       // keys per thread in a sort pass (the smaller partition)
 constexpr int WW = WT / 32;                    // warps per CTA
 constexpr int kBinsPerThread = kWideBins / WT;
 constexpr int kMaskWidth = (kTaps + kWideMaskPasses - 1) / kWideMaskPasses;
@@ -615,6 +615,7 @@ struct PassArgs {
 constexpr int kScanPerLane = 8;
 constexpr int kScanDigitsPerWarp = 4;
 
+template <int WI>
 __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
     // cnt[w][d]: keys of warp w with digit d, then the warp's offset within
     // the CTA's keys of digit d (stable order inside the CTA: warp, item, lane)
@@ -638,7 +639,7 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
         c = part_sh;
     }
     // this partition's keys (requested first: their latency overlaps the scan below)
-    const int64_t base = c * kWideKeysPerCta;
+    const int64_t base = c * WT * WI;
     uint64_t v[WI];
     int d[WI], rk[WI];
 #pragma unroll
@@ -1193,7 +1194,11 @@ int hash_table_log2(int64_t n) {
 
 int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     const int64_t n = a.n;
-    const unsigned parts = static_cast<unsigned>((n + kWideKeysPerCta - 1) / kWideKeysPerCta);
+    // keys per sort CTA: 1024, or 2048 above kBigPassRows (fewer partitions to
+    // look back over: 94k rows 97 -> 90 us per build, 32k rows 57.6 vs 58.6)
+    const bool big_pass = n > kBigPassRows;
+    const int64_t keys_per_cta = big_pass ? 2 * kWideKeysPerCta : kWideKeysPerCta;
+    const unsigned parts = static_cast<unsigned>((n + keys_per_cta - 1) / keys_per_cta);
     const bool few = n <= kFewRows;
     const int rpt = few ? 1 : 4;
     const unsigned key_blocks = static_cast<unsigned>((n + WT * rpt - 1) / (WT * rpt));
@@ -1201,14 +1206,15 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     // a look-back kernel numbers its partitions by blockIdx when all of its
     // CTAs fit on the device at once (each waits only on lower ones), else
     // takes them from a ticket counter in the order the CTAs start
-    static int64_t cap_pass[kMaxDevices] = {};
+    static int64_t cap_pass[kMaxDevices][2] = {};
     int dev = 0;
     SPCONV_CHECK_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return SPCONV_ERR_UNSUPPORTED;
-    if (cap_pass[dev] == 0) {
-        cap_pass[dev] = resident_ctas(k_wide_pass, WT, sms);
+    if (cap_pass[dev][0] == 0) {
+        cap_pass[dev][0] = resident_ctas(k_wide_pass<WI>, WT, sms);
+        cap_pass[dev][1] = resident_ctas(k_wide_pass<2 * WI>, WT, sms);
     }
-    const bool pass_ticket = static_cast<int64_t>(parts) > cap_pass[dev];
+    const bool pass_ticket = static_cast<int64_t>(parts) > cap_pass[dev][big_pass ? 1 : 0];
     // every thread clears ~8 16-byte words of the largest array
     const int64_t look16 = static_cast<int64_t>(parts) * kWideBins / 2;
     int64_t clear16 = a.mapper == SPCONV_MAPPER_DENSE ? a.cells / 4
@@ -1238,7 +1244,8 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
                              static_cast<int64_t>(parts) <= 32 * kScanPerLane;
         pa.bar = barrier ? a.tickets + kWideTickets + ticket * kWideBarrierInts : nullptr;
         pa.status = a.status;
-        return launch_pdl(k_wide_pass, parts, WT, s, true, pa);
+        return big_pass ? launch_pdl(k_wide_pass<2 * WI>, parts, WT, s, true, pa)
+                        : launch_pdl(k_wide_pass<WI>, parts, WT, s, true, pa);
     };
     if (a.mapper == SPCONV_MAPPER_HASH) {
         SPCONV_CHECK(launch_pdl(k_wide_hash_insert, row_blocks, WT, s, true, a));
