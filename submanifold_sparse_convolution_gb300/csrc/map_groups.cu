@@ -589,11 +589,9 @@ constexpr int kRankBlock = 1024;
 
 __global__ void __launch_bounds__(kRankBlock) kst_block_count(const int32_t* __restrict__ flags, int64_t m,
                                                               int32_t* __restrict__ bcount) {
-    __shared__ int32_t ws[kRankBlock / 32];
     const int64_t j = static_cast<int64_t>(blockIdx.x) * kRankBlock + threadIdx.x;
     const int f = j < m ? flags[j] : 0;
     const int c = __syncthreads_count(f);
-    (void)ws;
     if (threadIdx.x == 0) bcount[blockIdx.x] = c;
 }
 
