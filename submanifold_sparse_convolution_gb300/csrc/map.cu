@@ -299,33 +299,17 @@ __global__ void __launch_bounds__(1024) k_scan_tiles(const int32_t* __restrict__
                                                      int32_t* __restrict__ tap_off,
                                                      int32_t* __restrict__ totals,
                                                      int32_t* __restrict__ tile_order) {
-    __shared__ int32_t part[1024];
     __shared__ int32_t hist[kTaps + 1];
-    const int64_t m = kTaps * n_tiles;
-    const int64_t chunk = (m + 1023) / 1024;
-    const int64_t lo = threadIdx.x * chunk;
-    const int64_t hi = lo + chunk < m ? lo + chunk : m;
-    int32_t sum = 0;
-    for (int64_t i = lo; i < hi; ++i) sum += counts[i];
-    part[threadIdx.x] = sum;
     if (threadIdx.x <= kTaps) hist[threadIdx.x] = 0;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-        const int32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
-    }
-    int32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
-    for (int64_t i = lo; i < hi; ++i) {
-        const int32_t v = counts[i];
-        seg_off[i] = run;
-        if (i % n_tiles == 0) tap_off[i / n_tiles] = run;
-        run += v;
-    }
-    if (threadIdx.x == 1023) {
-        tap_off[kTaps] = part[1023];
-        totals[0] = part[1023];
+    const int64_t m = kTaps * n_tiles;
+    // seg_off is the exclusive scan of counts; a tap's list starts at the
+    // offset of its first tile
+    const int32_t total = rsort::block_scan_exclusive(counts, seg_off, m, [&](int64_t i, int32_t v) {
+        if (i % n_tiles == 0) tap_off[i / n_tiles] = v;
+    });
+    if (threadIdx.x == 0) {
+        tap_off[kTaps] = total;
+        totals[0] = total;
     }
     if (n_tiles == 0 && threadIdx.x < kTaps) tap_off[threadIdx.x] = 0;
     __syncthreads();
@@ -347,12 +331,20 @@ __global__ void __launch_bounds__(1024) k_scan_tiles(const int32_t* __restrict__
         }
     }
     __syncthreads();
-    // stable scatter: one thread per bucket walks the tiles in order
-    if (threadIdx.x <= kTaps) {
-        const int bucket = threadIdx.x;
-        int32_t at = hist[bucket];
-        for (int64_t t = 0; t < n_tiles; ++t)
-            if (kTaps - __popc(tile_union[t]) == bucket) tile_order[at++] = static_cast<int32_t>(t);
+    // stable scatter by warp 0, 32 tiles at a time: each at its bucket's next
+    // free position, tiles of one bucket in t order
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const uint32_t lt = rsort::lanemask_lt();
+        for (int64_t t0 = 0; t0 < n_tiles; t0 += 32) {
+            const int64_t t = t0 + lane;
+            const int b = t < n_tiles ? kTaps - __popc(tile_union[t]) : kTaps + 1;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, b);
+            if (b <= kTaps) tile_order[hist[b] + __popc(peers & lt)] = static_cast<int32_t>(t);
+            __syncwarp();
+            if (b <= kTaps && lane == __ffs(peers) - 1) hist[b] += __popc(peers);
+            __syncwarp();
+        }
     }
 }
 

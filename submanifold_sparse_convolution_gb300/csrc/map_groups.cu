@@ -38,6 +38,7 @@ namespace {
 constexpr int kGBlock = 256;
 constexpr int kMaxCols = kMaxKernel * kMaxKernel;
 constexpr int kMaxGroups = kMaxKernel;
+static_assert(kMaxGroups <= 32, "the tile scan places one group per warp");
 constexpr uint64_t kNoKey = ~0ull;
 
 struct GLayout {
@@ -424,33 +425,17 @@ __global__ void __launch_bounds__(1024) kg_scan_tiles(const int32_t* __restrict_
                                                       int32_t* __restrict__ totals,
                                                       int32_t* __restrict__ tile_order,
                                                       int32_t* __restrict__ nonempty) {
-    __shared__ int32_t part[1024];
     __shared__ int32_t hist[kMaxGroups][kMaxGroupTaps + 1];
-    const int64_t m = V * n_tiles;
-    const int64_t chunk = (m + 1023) / 1024;
-    const int64_t lo = threadIdx.x * chunk;
-    const int64_t hi = lo + chunk < m ? lo + chunk : m;
-    int32_t sum = 0;
-    for (int64_t i = lo; i < hi; ++i) sum += counts[i];
-    part[threadIdx.x] = sum;
     for (int i = threadIdx.x; i < kMaxGroups * (kMaxGroupTaps + 1); i += 1024) (&hist[0][0])[i] = 0;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-        const int32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
-    }
-    int32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
-    for (int64_t i = lo; i < hi; ++i) {
-        const int32_t v = counts[i];
-        seg_off[i] = run;
-        if (i % n_tiles == 0) tap_off[i / n_tiles] = run;
-        run += v;
-    }
-    if (threadIdx.x == 1023) {
-        tap_off[V] = part[1023];
-        totals[0] = part[1023];
+    const int64_t m = V * n_tiles;
+    // seg_off is the exclusive scan of counts; a tap's list starts at the
+    // offset of its first tile
+    const int32_t total = rsort::block_scan_exclusive(counts, seg_off, m, [&](int64_t i, int32_t v) {
+        if (i % n_tiles == 0) tap_off[i / n_tiles] = v;
+    });
+    if (threadIdx.x == 0) {
+        tap_off[V] = total;
+        totals[0] = total;
     }
     if (n_tiles == 0)
         for (int k = threadIdx.x; k < V; k += 1024) tap_off[k] = 0;
@@ -474,14 +459,23 @@ __global__ void __launch_bounds__(1024) kg_scan_tiles(const int32_t* __restrict_
         }
     }
     __syncthreads();
-    // one thread per (group, bucket) walks the group's tiles in order
-    if (threadIdx.x < G * (kg + 1)) {
-        const int g = threadIdx.x / (kg + 1), bucket = threadIdx.x % (kg + 1);
-        int32_t at = hist[g][bucket];
-        const uint32_t* un = tile_union + g * n_tiles;
-        int32_t* ord = tile_order + g * n_tiles;
-        for (int64_t t = 0; t < n_tiles; ++t)
-            if (kg - __popc(un[t]) == bucket) ord[at++] = static_cast<int32_t>(t);
+    // warp g places group g's tiles, 32 at a time: each at its bucket's next
+    // free position, tiles of one bucket in t order (ranked among the lanes
+    // that share the bucket)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp < G) {
+        const uint32_t* un = tile_union + warp * n_tiles;
+        int32_t* ord = tile_order + warp * n_tiles;
+        const uint32_t lt = rsort::lanemask_lt();
+        for (int64_t t0 = 0; t0 < n_tiles; t0 += 32) {
+            const int64_t t = t0 + lane;
+            const int b = t < n_tiles ? kg - __popc(un[t]) : kg + 1;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, b);
+            if (b <= kg) ord[hist[warp][b] + __popc(peers & lt)] = static_cast<int32_t>(t);
+            __syncwarp();
+            if (b <= kg && lane == __ffs(peers) - 1) hist[warp][b] += __popc(peers);
+            __syncwarp();
+        }
     }
 }
 

@@ -48,29 +48,95 @@ __global__ void __launch_bounds__(kThreads) upsweep(const K* __restrict__ keys, 
     for (int i = threadIdx.x; i < kBins; i += kThreads) hist[static_cast<int64_t>(i) * nb + blockIdx.x] = h[i];
 }
 
+// Exclusive scan of m int32 values from src to dst (the same array or
+// disjoint ones) by one block of kScanThreads threads.  Each round takes 16
+// consecutive values per thread (four 16-byte loads where both arrays are
+// 16-byte aligned), scans them in registers, then across the warp and across
+// the block's 32 warp sums; every load of a round is issued before its first
+// barrier.  on(i, v) is called once per element after dst[i] = v.  Returns
+// the total, in every thread.
+constexpr int kScanPer = 16;
+static_assert(kScanThreads == 1024, "the block scan holds one warp sum per lane");
+
+template <typename F>
+__device__ __forceinline__ int32_t block_scan_exclusive(const int32_t* src, int32_t* dst, int64_t m, F on) {
+    __shared__ int32_t wsum[2][kScanThreads / 32];
+    constexpr int64_t kRound = static_cast<int64_t>(kScanPer) * kScanThreads;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const bool vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) == 0;
+    int32_t carry = 0;
+    int buf = 0;
+    for (int64_t base = 0; base < m; base += kRound, buf ^= 1) {
+        const int64_t i0 = base + static_cast<int64_t>(kScanPer) * t;
+        const bool whole = vec && i0 + kScanPer <= m;
+        int32_t v[kScanPer];
+        if (whole) {
+#pragma unroll
+            for (int q = 0; q < kScanPer / 4; ++q) {
+                const int4 x = reinterpret_cast<const int4*>(src + i0)[q];
+                v[4 * q] = x.x;
+                v[4 * q + 1] = x.y;
+                v[4 * q + 2] = x.z;
+                v[4 * q + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < kScanPer; ++j) v[j] = i0 + j < m ? src[i0 + j] : 0;
+        }
+        int32_t s = 0;
+#pragma unroll
+        for (int j = 0; j < kScanPer; ++j) s += v[j];
+        int32_t inc = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        // two buffers: a warp writes this round's sum only after every warp
+        // has passed the barrier that follows its reads of the same buffer
+        // two rounds back
+        if (lane == 31) wsum[buf][w] = inc;
+        __syncthreads();
+        const int32_t ws = wsum[buf][lane];
+        int32_t winc = ws;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, winc, o);
+            if (lane >= o) winc += y;
+        }
+        const int32_t before = __shfl_sync(0xFFFFFFFFu, winc - ws, w);
+        const int32_t total = __shfl_sync(0xFFFFFFFFu, winc, 31);
+        int32_t run = carry + before + inc - s;
+#pragma unroll
+        for (int j = 0; j < kScanPer; ++j) {
+            const int32_t x = v[j];
+            v[j] = run;
+            run += x;
+        }
+        if (whole) {
+#pragma unroll
+            for (int q = 0; q < kScanPer / 4; ++q)
+                reinterpret_cast<int4*>(dst + i0)[q] = make_int4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < kScanPer; ++j)
+                if (i0 + j < m) dst[i0 + j] = v[j];
+        }
+#pragma unroll
+        for (int j = 0; j < kScanPer; ++j)
+            if (i0 + j < m) on(i0 + j, v[j]);
+        carry += total;
+    }
+    return carry;
+}
+
+struct NoVisit {
+    __device__ void operator()(int64_t, int32_t) const {}
+};
+
 // Exclusive scan, in place, of m int32 values (one block).
 static __global__ void __launch_bounds__(kScanThreads) scan_exclusive(int32_t* __restrict__ a, int64_t m) {
-    __shared__ int32_t part[kScanThreads];
-    const int64_t chunk = (m + kScanThreads - 1) / kScanThreads;
-    const int64_t lo = threadIdx.x * chunk;
-    const int64_t hi = lo + chunk < m ? lo + chunk : m;
-    int32_t s = 0;
-    for (int64_t i = lo; i < hi; ++i) s += a[i];
-    part[threadIdx.x] = s;
-    __syncthreads();
-    // Hillis-Steele inclusive scan of the partial sums
-    for (int off = 1; off < kScanThreads; off <<= 1) {
-        int32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
-    }
-    int32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
-    for (int64_t i = lo; i < hi; ++i) {
-        const int32_t v = a[i];
-        a[i] = run;
-        run += v;
-    }
+    block_scan_exclusive(a, a, m, NoVisit());
 }
 
 template <typename K>
