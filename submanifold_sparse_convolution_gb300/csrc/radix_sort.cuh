@@ -6,9 +6,17 @@
 // every digit), and a downsweep ranks each tile's keys stably and scatters
 // them.  Used for the packed coordinate keys (mapper) and for the 27-bit mask
 // keys (row order for the output tiles).
+//
+// The three kernels of every pass are launched with programmatic dependent
+// launch: each lets its successor be scheduled as soon as it starts, then
+// waits for its predecessor before its first global access, so a kernel's
+// launch latency hides behind the tail of the one before.  Data an earlier
+// kernel wrote is read through L2 (ld.global.cg), never the read-only path.
 #pragma once
 #include <cuda_runtime.h>
 #include <cstdint>
+
+#include "common.cuh"
 
 namespace spconv {
 namespace rsort {
@@ -31,6 +39,8 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 template <typename K>
 __global__ void __launch_bounds__(kThreads) upsweep(const K* __restrict__ keys, int64_t n, int shift,
                                                    int32_t* __restrict__ hist, int64_t nb) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t h[kBins];
     for (int i = threadIdx.x; i < kBins; i += kThreads) h[i] = 0;
     __syncthreads();
@@ -40,7 +50,7 @@ __global__ void __launch_bounds__(kThreads) upsweep(const K* __restrict__ keys, 
     for (int j = 0; j < kItems; ++j) {
         const int64_t idx = base + j * kThreads + threadIdx.x;
         const bool valid = idx < n;
-        const int d = valid ? static_cast<int>((keys[idx] >> shift) & 0xFF) : kBins;
+        const int d = valid ? static_cast<int>((__ldcg(keys + idx) >> shift) & 0xFF) : kBins;
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d);
         if (valid && lane == __ffs(peers) - 1) atomicAdd(&h[d], __popc(peers));
     }
@@ -73,7 +83,7 @@ __device__ __forceinline__ int32_t block_scan_exclusive(const int32_t* src, int3
         if (whole) {
 #pragma unroll
             for (int q = 0; q < kScanPer / 4; ++q) {
-                const int4 x = reinterpret_cast<const int4*>(src + i0)[q];
+                const int4 x = __ldcg(reinterpret_cast<const int4*>(src + i0) + q);
                 v[4 * q] = x.x;
                 v[4 * q + 1] = x.y;
                 v[4 * q + 2] = x.z;
@@ -81,7 +91,7 @@ __device__ __forceinline__ int32_t block_scan_exclusive(const int32_t* src, int3
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < kScanPer; ++j) v[j] = i0 + j < m ? src[i0 + j] : 0;
+            for (int j = 0; j < kScanPer; ++j) v[j] = i0 + j < m ? __ldcg(src + i0 + j) : 0;
         }
         int32_t s = 0;
 #pragma unroll
@@ -136,6 +146,8 @@ struct NoVisit {
 
 // Exclusive scan, in place, of m int32 values (one block).
 static __global__ void __launch_bounds__(kScanThreads) scan_exclusive(int32_t* __restrict__ a, int64_t m) {
+    pdl_trigger();
+    pdl_wait();
     block_scan_exclusive(a, a, m, NoVisit());
 }
 
@@ -146,13 +158,15 @@ __global__ void __launch_bounds__(kThreads) downsweep(const K* __restrict__ keys
                                                      uint32_t* __restrict__ vals_out, int64_t n,
                                                      int shift, const int32_t* __restrict__ hist,
                                                      int64_t nb) {
+    pdl_trigger();
+    pdl_wait();
     // cnt[j][w][d]: keys of item slot j in warp w with digit d; then the
     // exclusive prefix of those counts in tile order (j, w, lane).
     __shared__ uint16_t cnt[kItems][kWarps][kBins];
     __shared__ int32_t gbase[kBins];
     uint32_t* cz = reinterpret_cast<uint32_t*>(&cnt[0][0][0]);
     for (int i = threadIdx.x; i < kItems * kWarps * kBins / 2; i += kThreads) cz[i] = 0;
-    for (int i = threadIdx.x; i < kBins; i += kThreads) gbase[i] = hist[static_cast<int64_t>(i) * nb + blockIdx.x];
+    for (int i = threadIdx.x; i < kBins; i += kThreads) gbase[i] = __ldcg(hist + static_cast<int64_t>(i) * nb + blockIdx.x);
     __syncthreads();
 
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kTile;
@@ -165,8 +179,8 @@ __global__ void __launch_bounds__(kThreads) downsweep(const K* __restrict__ keys
     for (int j = 0; j < kItems; ++j) {
         const int64_t idx = base + j * kThreads + threadIdx.x;
         const bool valid = idx < n;
-        key[j] = valid ? keys_in[idx] : K(0);
-        val[j] = valid ? vals_in[idx] : 0u;
+        key[j] = valid ? __ldcg(keys_in + idx) : K(0);
+        val[j] = valid ? __ldcg(vals_in + idx) : 0u;
         dig[j] = valid ? static_cast<int>((key[j] >> shift) & 0xFF) : kBins;
         const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dig[j]);
         rank[j] = __popc(peers & lanemask_lt());
@@ -193,6 +207,19 @@ __global__ void __launch_bounds__(kThreads) downsweep(const K* __restrict__ keys
     }
 }
 
+template <typename Kernel, typename... Args>
+void launch_chained(Kernel kernel, unsigned grid, unsigned block, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a failed launch stays in cudaGetLastError, which every caller checks
+    (void)cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Sort (keys, vals) of length n on the live low `bits` of the key.  Returns
 // true if the result ended in (keys_b, vals_b), false if in (keys_a, vals_a).
 // hist needs kBins * num_tiles(n) int32.
@@ -208,9 +235,10 @@ bool sort_pairs(K* keys_a, uint32_t* vals_a, K* keys_b, uint32_t* vals_b, int64_
         const uint32_t* vin = in_b ? vals_b : vals_a;
         K* kout = in_b ? keys_a : keys_b;
         uint32_t* vout = in_b ? vals_a : vals_b;
-        upsweep<K><<<static_cast<unsigned>(nb), kThreads, 0, s>>>(kin, n, 8 * p, hist, nb);
-        scan_exclusive<<<1, kScanThreads, 0, s>>>(hist, kBins * nb);
-        downsweep<K><<<static_cast<unsigned>(nb), kThreads, 0, s>>>(kin, vin, kout, vout, n, 8 * p, hist, nb);
+        launch_chained(upsweep<K>, static_cast<unsigned>(nb), kThreads, s, kin, n, 8 * p, hist, nb);
+        launch_chained(scan_exclusive, 1u, kScanThreads, s, hist, static_cast<int64_t>(kBins) * nb);
+        launch_chained(downsweep<K>, static_cast<unsigned>(nb), kThreads, s, kin, vin, kout, vout, n, 8 * p,
+                       static_cast<const int32_t*>(hist), nb);
         *launches += 3;
         in_b = !in_b;
     }
