@@ -429,10 +429,19 @@ __global__ void __launch_bounds__(1024) kg_scan_tiles(const int32_t* __restrict_
     for (int i = threadIdx.x; i < kMaxGroups * (kMaxGroupTaps + 1); i += 1024) (&hist[0][0])[i] = 0;
     const int64_t m = V * n_tiles;
     // seg_off is the exclusive scan of counts; a tap's list starts at the
-    // offset of its first tile
-    const int32_t total = rsort::block_scan_exclusive(counts, seg_off, m, [&](int64_t i, int32_t v) {
-        if (i % n_tiles == 0) tap_off[i / n_tiles] = v;
-    });
+    // offset of its first tile (one division per run of entries)
+    const int32_t total = rsort::block_scan_exclusive(
+        counts, seg_off, m, [&](int64_t i0, const int32_t (&v)[rsort::kScanPer]) {
+            int64_t k = i0 / n_tiles, t = i0 - k * n_tiles;
+#pragma unroll
+            for (int j = 0; j < rsort::kScanPer; ++j) {
+                if (t == 0 && i0 + j < m) tap_off[k] = v[j];
+                if (++t == n_tiles) {
+                    t = 0;
+                    ++k;
+                }
+            }
+        });
     if (threadIdx.x == 0) {
         tap_off[V] = total;
         totals[0] = total;
@@ -447,7 +456,10 @@ __global__ void __launch_bounds__(1024) kg_scan_tiles(const int32_t* __restrict_
         atomicAdd(&hist[i / n_tiles][kg - c], 1);
         tap_sum += c;
     }
-    atomicAdd(&totals[1], tap_sum);
+    // one atomic per warp
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tap_sum += __shfl_down_sync(0xFFFFFFFFu, tap_sum, o);
+    if ((threadIdx.x & 31) == 0 && tap_sum != 0) atomicAdd(&totals[1], tap_sum);
     __syncthreads();
     if (threadIdx.x < G) {
         nonempty[threadIdx.x] = static_cast<int32_t>(n_tiles) - hist[threadIdx.x][kg];

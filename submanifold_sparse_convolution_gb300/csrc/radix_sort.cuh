@@ -63,8 +63,9 @@ __global__ void __launch_bounds__(kThreads) upsweep(const K* __restrict__ keys, 
 // consecutive values per thread (four 16-byte loads where both arrays are
 // 16-byte aligned), scans them in registers, then across the warp and across
 // the block's 32 warp sums; every load of a round is issued before its first
-// barrier.  on(i, v) is called once per element after dst[i] = v.  Returns
-// the total, in every thread.
+// barrier.  on(i0, v) is called once per round by every thread whose run
+// starts inside the array, after it stored dst[i0 + j] = v[j] for the j with
+// i0 + j < m.  Returns the total, in every thread.
 constexpr int kScanPer = 16;
 static_assert(kScanThreads == 1024, "the block scan holds one warp sum per lane");
 
@@ -132,16 +133,14 @@ __device__ __forceinline__ int32_t block_scan_exclusive(const int32_t* src, int3
             for (int j = 0; j < kScanPer; ++j)
                 if (i0 + j < m) dst[i0 + j] = v[j];
         }
-#pragma unroll
-        for (int j = 0; j < kScanPer; ++j)
-            if (i0 + j < m) on(i0 + j, v[j]);
+        if (i0 < m) on(i0, v);
         carry += total;
     }
     return carry;
 }
 
 struct NoVisit {
-    __device__ void operator()(int64_t, int32_t) const {}
+    __device__ void operator()(int64_t, const int32_t (&)[kScanPer]) const {}
 };
 
 // Exclusive scan, in place, of m int32 values (one block).
