@@ -41,6 +41,10 @@ UNIT = "us/layer"
 # gfx950 for N=32,371, C=128 -- another machine's number, quoted as context.
 PAGES_US = {"outdoor": 47.0, "large": 178.0}
 L2_FLUSH_BYTES = 256 << 20
+# GB300 nominal figures, reported beside the measured peaks: HBM3e bandwidth and
+# dense bf16 tensor throughput
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
 DATA = ("synthetic, seeded: LiDAR-like scan-ring ground plane (2 jittered layers) plus "
         "box/cylinder surfaces, rows shuffled; features N(0,1), weights N(0,1/sqrt(27*C_in)), bf16")
 
@@ -350,12 +354,14 @@ def run_ours(args, rank, world, device):
         "roofline": {"bound": "tensor", "kernel": kernel_name, "achieved": round(gemm_tflops, 2),
                      "peak": peaks["bf16"], "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / peaks["bf16"], 4), "traffic": traffic,
+                     "frac_of_nominal": round(gemm_tflops / NOMINAL_BF16_TFLOPS, 4),
                      "peak_source": f"{peaks['source']} bf16 dense (burst, kernel timed alone)",
                      "launches_per_layer": G,
                      "executed_over_useful": round(executed_rows / P, 3)},
         "roofline_map": {"bound": "hbm", "achieved": round(map_bytes / map_avg_s / 1e9, 2),
                          "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": round(map_bytes / map_avg_s / 1e9 / peaks["hbm"], 4),
+                         "frac_of_nominal": round(map_bytes / map_avg_s / 1e9 / NOMINAL_HBM_GBS, 4),
                          "algorithmic_bytes": map_bytes},
         "e2e": {"value": round(statistics.mean(e2e_ms) * 1e3 / L, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
