@@ -7,6 +7,27 @@ PyTorch supplies device memory and streams.
 
     m = build_map(coords)                       # int32 [N, 4] (b, x, y, z), CUDA
     out = subm_forward(m, feats, weights)       # bf16 [N, C_in] x [27, C_in, C_out]
+
+One map serves every layer on the same sites; weights can be packed once, and
+a layer's batch norm (inference form), bias, residual and ReLU are applied to
+the fp32 sum before its single rounding:
+
+    wp = wpack_create(weights)                  # [27 or 125, C_in, C_out]
+    y = subm_forward_packed(m, x, wp, scale=s, bias=b, residual=x, relu=True)
+    y32 = subm_forward(m, x.float(), weights.float())   # exact fp32 mode
+
+Kernel size 5 and offset groups: ``build_map(coords, kernel_size=5)`` (125
+taps, always five groups), ``build_map(coords, groups=3)``.  Downsampling and
+its inverse, on the output sites of a stride-2 grid:
+
+    d = build_map_strided(coords)               # sites o with a site in {2o + d}
+    y = subm_forward(d, x, w)                   # [d.n, C_out] at map_out_coords(d)
+    u = build_map_inverse(d)                    # back onto the input sites
+    z = subm_forward(u, y, w2)                  # [N, C_out2]
+
+Errors raise ``SpconvError`` with the library's status code; errors found on
+the device (duplicate or out-of-range coordinates) surface through
+``map_status`` or the next call on the map.
 """
 from __future__ import annotations
 
@@ -34,10 +55,13 @@ def library():
 
 
 def status_string(code: int) -> str:
+    """The library's message for a status code (``spconv_status_string``)."""
     return library().spconv_status_string(int(code)).decode()
 
 
 class SpconvError(RuntimeError):
+    """A call into the library returned a status other than SPCONV_OK; ``code`` holds it."""
+
     def __init__(self, code: int, where: str = ""):
         super().__init__(f"{where}: {status_string(code)} ({code})" if where else status_string(code))
         self.code = code
