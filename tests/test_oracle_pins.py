@@ -658,6 +658,29 @@ def test_inverse_map_and_conv_match_dense_conv_transpose3d(seed, n, shape, batch
     assert (inv >= 0).sum() == (nbr >= 0).sum()
 
 
+def test_golden_strided_and_inverse():
+    g = read_golden("line_strided_and_inverse.txt")
+    coords = np.array(g["coords"], dtype=np.int32).reshape(-1, 4)
+    n = coords.shape[0]
+    assert oracle.strided_shape(g["shape"]) == tuple(g["out_shape"])
+    oc, nbr = oracle.strided_map(coords, g["shape"], g["batch"][0])
+    assert oc.reshape(-1).tolist() == g["out_coords"]
+    want = np.full((oc.shape[0], 27), -1, dtype=np.int32)
+    for o, k, i in zip(*[iter(g["nbr"])] * 3):
+        want[o, k] = i
+    assert np.array_equal(nbr, want)
+    inv = oracle.inverse_map(nbr, n)
+    want_inv = np.full((n, 27), -1, dtype=np.int32)
+    for i, k, o in zip(*[iter(g["inv"])] * 3):
+        want_inv[i, k] = o
+    assert np.array_equal(inv, want_inv)
+    w = (np.arange(27, dtype=np.float64) + 1).reshape(27, 1, 1)
+    f = np.array(g["feats"], dtype=np.float64).reshape(-1, 1)
+    assert oracle.conv_f64(nbr, f, w)[:, 0].tolist() == g["out"]
+    y = np.array(g["inv_feats"], dtype=np.float64).reshape(-1, 1)
+    assert oracle.conv_f64(inv, y, w)[:, 0].tolist() == g["inv_out"]
+
+
 def test_mutated_strided_map_is_caught():
     """Windows at o + d (no stride) or at 2o - d (mirrored) both fail the dense conv."""
     wl = S.random_cloud(131, 500, shape=(10, 10, 10), c_in=3, c_out=3)
