@@ -166,6 +166,193 @@ def job_us_per_layer(total_ms: float, steps: int, layers: int, world: int) -> fl
 # our arm
 # ---------------------------------------------------------------------------
 
+class StepTimer:
+    """Timed repetitions on one stream, the L2 flushed (a 256 MB write) before each;
+    ``mark()`` records an event inside the repetition being timed."""
+
+    def __init__(self, stream, flush):
+        self.stream = stream
+        self.flush = flush
+        self.marks = []
+        self.recording = False
+
+    def mark(self):
+        if self.recording:
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(self.stream)
+            self.marks[-1].append(e)
+
+    def run(self, fn, reps, record=False):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        self.marks = []
+        self.recording = record
+        for i in range(reps):
+            self.flush.zero_()
+            ev[i][0].record(self.stream)
+            if record:
+                self.marks.append([ev[i][0]])
+            fn()
+            ev[i][1].record(self.stream)
+        torch.cuda.synchronize(self.stream.device)
+        self.recording = False
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def spans(self, a, b):
+        """Milliseconds between marks a and b of every recorded repetition."""
+        return [mk[a].elapsed_time(mk[b]) for mk in self.marks]
+
+
+def gemm_bytes(n_in, n_out, c_in, c_out, taps, pairs, elem):
+    """Algorithmic bytes of one forward: input rows read once, output rows written once,
+    the weights once, and one gather and one scatter index per pair."""
+    return elem * (n_in * c_in + n_out * c_out + taps * c_in * c_out) + 8 * pairs
+
+
+def map_bytes(n_in, n_rows, taps, groups, pairs):
+    """Algorithmic bytes of one map build: coordinates read, nbr [rows][taps] written,
+    masks and row order per group, the pair lists."""
+    return 16 * n_in + 4 * taps * n_rows + 8 * groups * n_rows + 8 * pairs
+
+
+class Workbench:
+    """One workload on the device: its map build and layers, timed per step."""
+
+    def __init__(self, sc, wl, device, timer, build_kw, strided=False):
+        self.sc, self.wl, self.device, self.timer = sc, wl, device, timer
+        self.strided = strided
+        # a strided convolution changes the sites: one layer (the workload's first weights)
+        self.L = 1 if strided else wl.layers
+        self.coords = wl.coords.to(device)
+        self.feats = wl.feats.to(device)
+        self.wps = [sc.wpack_create(w.to(device)) for w in wl.weights[:self.L]]
+        self.build_kw = build_kw
+        self.launches = 0
+
+    def build(self, c, **over):
+        kw = dict(self.build_kw, **over)
+        if self.strided:
+            return self.sc.build_map_strided(c, self.wl.spatial_shape, self.wl.batch_size)
+        return self.sc.build_map(c, self.wl.spatial_shape, self.wl.batch_size, **kw)
+
+    def layers(self, m, x):
+        y = None
+        for li in range(self.L):
+            # the ReLU between layers is fused into the GEMM's store
+            y = self.sc.subm_forward_packed(m, x, self.wps[li], relu=li + 1 < self.L)
+            self.launches += self.sc.last_launch_count()
+            if li == 0:
+                self.timer.mark()
+            x = y
+        return y
+
+    def step(self):
+        m = self.build(self.coords)
+        self.launches += self.sc.last_launch_count()
+        self.timer.mark()
+        y = self.layers(m, self.feats)
+        m.destroy()
+        return y
+
+    def info(self):
+        """Map statistics (one synchronising call, outside any timing)."""
+        m0 = self.build(self.coords)
+        st = self.sc.map_status(m0)
+        if st != 0:
+            raise RuntimeError("map build reported " + self.sc.status_string(st))
+        info = self.sc.map_info(m0)
+        if info["gemm"] == "tap_major":
+            # 128-pair tiles per tap (only each tap's last is ragged)
+            tap_off = self.sc.map_export(m0)["tap_off"].cpu().numpy().astype(np.int64)
+            V = info["kernel_size"] ** 3
+            info["executed_rows"] = int(sum(-(-(tap_off[k + 1] - tap_off[k]) // 128) * 128 for k in range(V)))
+        else:
+            info["executed_rows"] = info["tile_taps"] * 128
+        self.map0 = m0
+        m1 = self.build(self.coords)
+        info["map_launches"] = self.sc.last_launch_count()
+        m1.destroy()
+        return info
+
+    def time_steps(self, steps, warmup):
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize(self.device)
+        self.launches = 0
+        step_ms = self.timer.run(self.step, steps, record=True)
+        return dict(step_ms=step_ms, map_ms=self.timer.spans(0, 1), gemm_ms=self.timer.spans(1, 2))
+
+    def time_map(self, reps, **over):
+        """Map build alone (e.g. another mapper), flushed L2, mean ms."""
+        for _ in range(3):
+            self.build(self.coords, **over).destroy()
+        ms = self.timer.run(lambda: self.build(self.coords, **over).destroy(), reps)
+        return statistics.mean(ms)
+
+    def time_fp32_layer(self, reps):
+        """The first layer in exact fp32 mode (SIMT FFMA) on the built map, mean ms."""
+        f32 = self.wl.feats.float().to(self.device)
+        w32 = self.wl.weights[0].float().to(self.device)
+        out = torch.empty((self.map0.n, self.wl.c_out), dtype=torch.float32, device=self.device)
+        for _ in range(3):
+            self.sc.subm_forward(self.map0, f32, w32, out=out)
+        return statistics.mean(self.timer.run(lambda: self.sc.subm_forward(self.map0, f32, w32, out=out), reps))
+
+    def close(self):
+        self.map0.destroy()
+
+
+def summarise(wb, info, t, peaks, L):
+    """µs/layer, component times and roofline fractions of one workload's timed steps."""
+    wl = wb.wl
+    P, n_rows = info["pairs"], info["n"]
+    V, G = info["kernel_size"] ** 3, info["groups"]
+    useful = 2.0 * P * wl.c_in * wl.c_out
+    map_s = statistics.mean(t["map_ms"]) * 1e-3
+    gemm_s = statistics.mean(t["gemm_ms"]) * 1e-3
+    us_layer = statistics.mean(t["step_ms"]) * 1e3 / L
+    tflops = useful / gemm_s / 1e12
+    gbytes = gemm_bytes(wl.n, n_rows, wl.c_in, wl.c_out, V, P, 2)
+    mbytes = map_bytes(wl.n, n_rows, V, G, P)
+    gather = P * wl.c_in * 2
+    return {
+        "us_per_layer": round(us_layer, 3), "layers": L,
+        "map_us": round(map_s * 1e6, 3), "gemm_us": round(gemm_s * 1e6, 3),
+        "useful_tflops_gemm": round(tflops, 2),
+        "useful_tflops_layer": round(useful * L / (statistics.mean(t["step_ms"]) * 1e-3) / 1e12, 3),
+        "gemm_tensor": {"frac": round(tflops / peaks["bf16"], 4), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                        "executed_over_useful": round(info["executed_rows"] / P, 3) if P else None},
+        # the same GEMM against HBM: what a memory-bound launch of this size would move
+        "gemm_hbm": {"algorithmic_bytes": gbytes, "achieved": round(gbytes / gemm_s / 1e9, 2),
+                     "peak": peaks["hbm"], "unit": "GB/s", "frac": round(gbytes / gemm_s / 1e9 / peaks["hbm"], 4)},
+        # feature rows the gather moves into shared memory (one C_in row per pair, zero rows not counted)
+        "gather": {"bytes": gather, "achieved": round(gather / gemm_s / 1e9, 2), "unit": "GB/s"},
+        "map_hbm": {"algorithmic_bytes": mbytes, "achieved": round(mbytes / map_s / 1e9, 2),
+                    "peak": peaks["hbm"], "unit": "GB/s", "frac": round(mbytes / map_s / 1e9 / peaks["hbm"], 4)},
+        "pairs": P, "pairs_per_row": round(P / n_rows, 3) if n_rows else None,
+        "mapper": info["mapper"], "pipeline": info["pipeline"], "gemm": info["gemm"],
+        "tile_taps": info["tile_taps"], "map_launches": info["map_launches"],
+    }
+
+
+def ffma_peak_tflops(device, sm_mhz):
+    """SIMT fp32 peak: SMs x 128 FP32 lanes x 2 FLOP (FFMA) x SM clock."""
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def workload_config(args, wl, n_rows, pairs, kernel_size, groups, L):
+    """The workload as both arms name it (no implementation detail)."""
+    return {"workload": f"{args.workload}: N={wl.n}, C_in={wl.c_in}, C_out={wl.c_out}, "
+                        f"layers={L}, batch={wl.batch_size}, grid={'x'.join(map(str, wl.spatial_shape))}",
+            "conv": args.conv, "output_sites": n_rows, "kernel_size": kernel_size, "groups": groups,
+            "pairs": pairs, "pairs_per_row": round(pairs / n_rows, 3) if n_rows else None,
+            "l2": "flushed (256 MB write) before every timed step"}
+
+
+PER_WORKLOAD = ["tiny", "outdoor", "deep", "large", "stage"]
+
+
 def run_ours(args, rank, world, device):
     import submanifold_sparse_convolution_gb300 as sc
     from submanifold_sparse_convolution_gb300 import build as build_mod
@@ -175,80 +362,18 @@ def run_ours(args, rank, world, device):
     peaks = load_peaks()
     wl = S.make_workload(args.workload, kernel_size=args.kernel_size)
     strided = args.conv == "strided"
-    # a strided convolution changes the sites: one layer (the workload's first weights)
-    L = 1 if strided else wl.layers
-    coords = wl.coords.to(device)
-    feats = wl.feats.to(device)
-    wps = [sc.wpack_create(w.to(device)) for w in wl.weights]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    launches = [0]
-
-    # events inside the timed steps: per step [start, map done, layer 0 done]
-    marks = []
-    recording = [False]
-
-    def mark():
-        if recording[0]:
-            e = torch.cuda.Event(enable_timing=True)
-            e.record(stream)
-            marks[-1].append(e)
-
-    def layers(m, x):
-        y = None
-        for li in range(L):
-            # the ReLU between layers is fused into the GEMM's store
-            y = sc.subm_forward_packed(m, x, wps[li], relu=li + 1 < L)
-            launches[0] += sc.last_launch_count()
-            if li == 0:
-                mark()
-            x = y
-        return y
-
-    def build(c):
-        if strided:
-            return sc.build_map_strided(c, wl.spatial_shape, wl.batch_size)
-        return sc.build_map(c, wl.spatial_shape, wl.batch_size, kernel_size=args.kernel_size,
-                            groups=args.groups, gemm=args.gemm, pipeline=args.pipeline)
-
-    def step():
-        m = build(coords)
-        launches[0] += sc.last_launch_count()
-        mark()
-        y = layers(m, feats)
-        m.destroy()
-        return y
-
-    # map statistics (one synchronising call, outside any timing)
-    m0 = build(coords)
-    if sc.map_status(m0) != 0:
-        raise RuntimeError("map build reported " + sc.status_string(sc.map_status(m0)))
-    info = sc.map_info(m0)
+    timer = StepTimer(stream, flush)
+    build_kw = dict(kernel_size=args.kernel_size, groups=args.groups, gemm=args.gemm, pipeline=args.pipeline)
+    wb = Workbench(sc, wl, device, timer, build_kw, strided)
+    L = wb.L
+    info = wb.info()
     pairs = info["pairs"]
     useful_flops_layer = 2.0 * pairs * wl.c_in * wl.c_out
-    # MMA rows the GEMM executes: mask-union tiles, or 128-pair tiles per tap (only each tap's last is ragged)
-    tap_major = info["gemm"] == "tap_major"
-    if tap_major:
-        tap_off = sc.map_export(m0)["tap_off"].cpu().numpy().astype(np.int64)
-        executed_rows = int(sum(-(-(tap_off[k + 1] - tap_off[k]) // 128) * 128 for k in range(27)))
-    else:
-        executed_rows = info["tile_taps"] * 128
-
-    def timed(fn, reps):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(reps)]
-        for i in range(reps):
-            flush.zero_()
-            ev[i][0].record(stream)
-            if recording[0]:
-                marks.append([ev[i][0]])
-            fn()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize(device)
-        return [a.elapsed_time(b) for a, b in ev]
 
     for _ in range(args.warmup):
-        step()
+        wb.step()
     torch.cuda.synchronize(device)
 
     # ---- the timed K steps
@@ -259,37 +384,26 @@ def run_ours(args, rank, world, device):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
-    launches[0] = 0
     t0 = time.time()
-    recording[0] = True
-    step_ms = timed(step, args.steps)
-    recording[0] = False
+    t = wb.time_steps(args.steps, 0)
     t1 = time.time()
-    gpu_launches = launches[0]
-    # map and first-layer GEMM durations of every timed step, from the same events
-    map_ms = [mk[0].elapsed_time(mk[1]) for mk in marks]
-    gemm_ms = [mk[1].elapsed_time(mk[2]) for mk in marks]
+    gpu_launches = wb.launches
     torch.cuda.synchronize(device)
     if world > 1:
         torch.distributed.barrier()
-    total_ms = max_over_ranks(sum(step_ms), device)
+    total_ms = max_over_ranks(sum(t["step_ms"]), device)
     if sampler:
         time.sleep(0.3)
         sampler.stop()
     clocks = sampler.summary(t0, t1) if sampler else None
-
-    map_launches = None
-    m1 = build(coords)
-    map_launches = sc.last_launch_count()
-    m1.destroy()
 
     # ---- end to end from pinned host buffers
     coords_h = wl.coords.pin_memory()
     feats_h = wl.feats.pin_memory()
     n_rows = info["n"]   # output sites (the input sites but for a strided convolution)
     out_h = torch.empty((n_rows, wl.c_out), dtype=torch.bfloat16).pin_memory()
-    coords_d2 = torch.empty_like(coords)
-    feats_d2 = torch.empty_like(feats)
+    coords_d2 = torch.empty_like(wb.coords)
+    feats_d2 = torch.empty_like(wb.feats)
     # the map needs only the coordinates: the features travel on a side stream
     # while it builds, and the first layer waits for them
     side = torch.cuda.Stream(device)
@@ -301,36 +415,38 @@ def run_ours(args, rank, world, device):
         with torch.cuda.stream(side):
             feats_d2.copy_(feats_h, non_blocking=True)
             feats_ready.record(side)
-        m = build(coords_d2)
+        m = wb.build(coords_d2)
         stream.wait_event(feats_ready)
-        y = layers(m, feats_d2)
+        y = wb.layers(m, feats_d2)
         out_h.copy_(y, non_blocking=True)
         m.destroy()
 
-    e2e_ms = timed(e2e_step, max(args.steps, 5))
-    h2d = coords.numel() * 4 + feats.numel() * 2
+    e2e_ms = timer.run(e2e_step, max(args.steps, 5))
+    h2d = wb.coords.numel() * 4 + wb.feats.numel() * 2
     d2h = n_rows * wl.c_out * 2
 
-    m0.destroy()
+    plain = info["kernel_size"] == 3 and info["groups"] == 1 and not strided
+    # the benchmark spec's sorted-key mapper, timed beside the shipped one
+    sorted_map_us = None
+    if plain and info["mapper"] == "hash" and rank == 0:
+        sorted_map_us = round(wb.time_map(max(10, min(args.steps, 50)), mapper="sorted") * 1e3, 3)
+    wb.close()
     if rank != 0:
         return None
 
-    layers_total = args.steps * L * world
+    summ = summarise(wb, info, t, peaks, L)
     us_per_layer = job_us_per_layer(total_ms, args.steps, L, world)
+    layers_total = args.steps * L * world
     useful_tflops = useful_flops_layer * layers_total / (total_ms * 1e-3) / 1e12
-    gemm_avg_s = statistics.mean(gemm_ms) * 1e-3
-    gemm_tflops = useful_flops_layer / gemm_avg_s / 1e12
-    n, P = wl.n, pairs
-    V, G = info["kernel_size"] ** 3, info["groups"]
-    # coordinates read, nbr [rows][V] written, masks and row order per group, pair lists
-    map_bytes = 16 * n + 4 * V * n_rows + 8 * G * n_rows + 8 * P
-    map_avg_s = statistics.mean(map_ms) * 1e-3
+    gemm_tflops = summ["useful_tflops_gemm"]
+    tap_major = info["gemm"] == "tap_major"
+    G = info["groups"]
     kernel_name = (f"k_tc_gemm<{256 if wl.c_out > 256 else (128 if wl.c_out > 64 else 64)}, "
                    f"{'tap-major' if tap_major else 'tile-union'}>")
-    plain = info["kernel_size"] == 3 and G == 1 and not strided
     traffic = ncu_traffic("k_tc_gemm", args.workload if plain else
                           f"{args.workload}-strided" if strided else f"{args.workload}-k{info['kernel_size']}-g{G}")
     pages_us = PAGES_US.get(args.workload) if plain else None
+    config = workload_config(args, wl, n_rows, pairs, info["kernel_size"], G, L)
     out = {
         "metric": METRIC, "value": round(us_per_layer, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -339,41 +455,93 @@ def run_ours(args, rank, world, device):
         "vs_baseline": round(us_per_layer / pages_us, 4) if pages_us else None,
         "vs_baseline_note": ("value / the pages' µs on an AMD gfx950 for the same N and C "
                              "(context: other hardware, real scans)") if pages_us else None,
-        "dtype": "bf16", "data": DATA,
-        "config": {"workload": f"{args.workload}: N={wl.n}, C_in={wl.c_in}, C_out={wl.c_out}, "
-                               f"layers={L}, batch={wl.batch_size}, grid={'x'.join(map(str, wl.spatial_shape))}",
-                   "conv": args.conv, "output_sites": n_rows,
-                   "kernel_size": info["kernel_size"], "groups": G,
-                   "pairs": P, "pairs_per_row": round(P / n_rows, 3) if n_rows else None, "mapper": info["mapper"], "pipeline": info["pipeline"], "gemm": info["gemm"],
-                   "tile_taps": info["tile_taps"], "l2": "flushed (256 MB write) before every timed step",
-                   "weights": "packed once per layer (outside the step)",
-                   "relu": "between layers, fused into the GEMM store" if L > 1 else None},
+        "dtype": "bf16", "data": DATA, "config": config,
+        "impl_config": {"mapper": info["mapper"], "pipeline": info["pipeline"], "gemm": info["gemm"],
+                        "tile_taps": info["tile_taps"],
+                        "weights": "packed once per layer (outside the step)",
+                        "relu": "between layers, fused into the GEMM store" if L > 1 else None},
         "useful_tflops": round(useful_tflops, 3),
-        "components_us": {"map": round(map_avg_s * 1e6, 3), "gemm_layer0": round(gemm_avg_s * 1e6, 3),
-                          "map_launches": map_launches},
-        "roofline": {"bound": "tensor", "kernel": kernel_name, "achieved": round(gemm_tflops, 2),
+        "components_us": {"map": summ["map_us"], "gemm_layer0": summ["gemm_us"],
+                          "map_launches": info["map_launches"], "map_sorted_mapper": sorted_map_us},
+        "roofline": {"bound": "tensor", "kernel": kernel_name, "achieved": gemm_tflops,
                      "peak": peaks["bf16"], "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / peaks["bf16"], 4), "traffic": traffic,
                      "frac_of_nominal": round(gemm_tflops / NOMINAL_BF16_TFLOPS, 4),
                      "peak_source": f"{peaks['source']} bf16 dense (burst, kernel timed alone)",
                      "launches_per_layer": G,
-                     "executed_over_useful": round(executed_rows / P, 3)},
-        "roofline_map": {"bound": "hbm", "achieved": round(map_bytes / map_avg_s / 1e9, 2),
-                         "peak": peaks["hbm"], "unit": "GB/s",
-                         "frac": round(map_bytes / map_avg_s / 1e9 / peaks["hbm"], 4),
-                         "frac_of_nominal": round(map_bytes / map_avg_s / 1e9 / NOMINAL_HBM_GBS, 4),
-                         "algorithmic_bytes": map_bytes},
+                     "executed_over_useful": summ["gemm_tensor"]["executed_over_useful"],
+                     "gather": summ["gather"], "hbm": summ["gemm_hbm"]},
+        "roofline_map": {"bound": "hbm", "achieved": summ["map_hbm"]["achieved"],
+                         "peak": peaks["hbm"], "unit": "GB/s", "frac": summ["map_hbm"]["frac"],
+                         "frac_of_nominal": round(summ["map_hbm"]["achieved"] / NOMINAL_HBM_GBS, 4),
+                         "algorithmic_bytes": summ["map_hbm"]["algorithmic_bytes"]},
         "e2e": {"value": round(statistics.mean(e2e_ms) * 1e3 / L, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
     }
+    if plain and args.per_workload and world == 1:
+        sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+        out["per_workload"] = per_workload(sc, S, args, device, timer, peaks, sm_mhz, {args.workload: summ})
     return out
+
+
+def per_workload(sc, S, args, device, timer, peaks, sm_mhz, done):
+    """Every workload of the metric, timed the same way in this run (fewer steps each)."""
+    res = {}
+    steps = max(5, min(args.steps, 30))
+    for name in PER_WORKLOAD:
+        if name in done:
+            res[name] = done[name]
+            continue
+        wl = S.make_workload(name)
+        wb = Workbench(sc, wl, device, timer, dict(pipeline=args.pipeline, gemm=args.gemm))
+        info = wb.info()
+        t = wb.time_steps(steps, 3)
+        r = summarise(wb, info, t, peaks, wb.L)
+        r["steps"] = steps
+        if name == "stage":
+            # the same first layer in exact fp32 (SIMT FFMA, plain ALUs)
+            ms = wb.time_fp32_layer(steps)
+            flops = 2.0 * info["pairs"] * wl.c_in * wl.c_out
+            peak = ffma_peak_tflops(device, sm_mhz)
+            b32 = gemm_bytes(wl.n, info["n"], wl.c_in, wl.c_out, 27, info["pairs"], 4)
+            r["fp32_layer"] = {"bound": "alu", "us": round(ms * 1e3, 3),
+                               "achieved": round(flops / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                               "peak": round(peak, 2), "frac": round(flops / (ms * 1e-3) / 1e12 / peak, 4),
+                               "peak_source": f"SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz (median SM clock "
+                                              "of the timed run)",
+                               "hbm_achieved": round(b32 / (ms * 1e-3) / 1e9, 2),
+                               "hbm_frac": round(b32 / (ms * 1e-3) / 1e9 / peaks["hbm"], 4)}
+        wb.close()
+        res[name] = r
+        del wb
+        torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        outp = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in outp.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
 
 def prepare_oracle(workload, kernel_size=3, groups=0, conv="submanifold"):
     import oracle
@@ -386,41 +554,62 @@ def prepare_oracle(workload, kernel_size=3, groups=0, conv="submanifold"):
                 w=wl.weights[0].double().numpy(), K=kernel_size, G=G, conv=conv)
 
 
-def time_oracle(prep, budget_s):
-    """Oracle µs/layer: full map build + fp64 conv on a row sample scaled to N."""
+def oracle_map(prep):
+    """The oracle's map build (single-threaded): kernel map, masks, order, pair lists."""
     import oracle
 
-    wl, c, f, w = prep["wl"], prep["c"], prep["f"], prep["w"]
-    t = time.perf_counter()
+    wl, c = prep["wl"], prep["c"]
     if prep["conv"] == "strided":
         _, nbr = oracle.strided_map(c, wl.spatial_shape, wl.batch_size)
     else:
         nbr = oracle.kernel_map(c, wl.spatial_shape, wl.batch_size, prep["K"])
     _, _, p = oracle.group_orders(nbr, prep["G"], True)
-    oracle.pair_lists(nbr, p)
+    lists = oracle.pair_lists(nbr, p)
+    return nbr, int(lists[0][-1])
+
+
+def time_oracle(prep, budget_s, threads=0, nbr=None):
+    """Oracle µs/layer: the full map build + the fp64 conv on ``threads`` threads (0: all),
+    on a row sample scaled to N.  Returns (µs/layer, threads used, sample, nbr, map s)."""
+    import oracle
+
+    wl, f, w = prep["wl"], prep["f"], prep["w"]
+    t = time.perf_counter()
+    if nbr is None:
+        nbr, _ = oracle_map(prep)
+        t_map = time.perf_counter() - t
+    else:
+        t_map = prep["t_map"]
     n_rows = nbr.shape[0]                   # output sites (strided: fewer than the inputs)
     layers = 1 if prep["conv"] == "strided" else wl.layers
-    t_map = time.perf_counter() - t
     # calibrate the conv sample on 256 rows, then size it to the budget
     rows = np.arange(min(256, n_rows), dtype=np.int32)
     t = time.perf_counter()
-    oracle.conv_f64(nbr, f, w, rows=rows)
+    oracle.conv_f64(nbr, f, w, rows=rows, threads=threads)
     t_cal = max(time.perf_counter() - t, 1e-6) / max(1, rows.shape[0])
     k = int(min(n_rows, max(256, budget_s / t_cal)))
     rows = np.linspace(0, n_rows - 1, k).astype(np.int32)
     t = time.perf_counter()
-    oracle.conv_f64(nbr, f, w, rows=rows)
+    oracle.conv_f64(nbr, f, w, rows=rows, threads=threads)
     t_conv = (time.perf_counter() - t) / max(1, k) * n_rows
     us_per_layer = (t_map + layers * t_conv) / layers * 1e6
+    used = threads if threads > 0 else oracle.max_threads()
     what = "strided map (kernel 3, stride 2)" if prep["conv"] == "strided" else f"full kernel map (K={prep['K']})"
-    sample = (f"{what}, masks, order and pair lists ({prep['G']} group(s)) of N={wl.n}; fp64 conv on {k} of "
-              f"{n_rows} output rows (evenly spaced) scaled to all; {layers} layer(s)")
-    return us_per_layer, oracle.max_threads(), sample
+    sample = (f"{what}, masks, order and pair lists ({prep['G']} group(s)) of N={wl.n} on one thread; "
+              f"fp64 conv on {k} of {n_rows} output rows (evenly spaced) on {used} thread(s), scaled to all; "
+              f"{layers} layer(s)")
+    return us_per_layer, used, sample, nbr, t_map
 
 
 def cpu_baseline(workload, budget_s, kernel_size=3, groups=0, conv="submanifold"):
-    us, cores, sample = time_oracle(prepare_oracle(workload, kernel_size, groups, conv), budget_s)
-    return {"value": round(us, 3), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    """The oracle on all host threads and on one, the map build timed once for both."""
+    prep = prepare_oracle(workload, kernel_size, groups, conv)
+    us, cores, sample, nbr, t_map = time_oracle(prep, budget_s)
+    prep["t_map"] = t_map
+    us1, _, sample1, _, _ = time_oracle(prep, budget_s / 2, threads=1, nbr=nbr)
+    return {"value": round(us, 3), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+            "value_1thread": round(us1, 3), "sample_1thread": sample1,
+            "map_build_s": round(t_map, 4), "cpu_model": cpu_model(), "host_threads": os.cpu_count()}
 
 
 def run_reference(args):
@@ -429,11 +618,13 @@ def run_reference(args):
     # the whole run stays within about two minutes of oracle work
     budget = max(0.05, min(args.ref_budget, 120.0 / (args.steps + args.warmup)))
     per_step = []
-    cores, sample = None, None
+    cores, sample, pairs, n_rows = None, None, 0, wl.n
     for i in range(args.warmup + args.steps):
-        us, cores, sample = time_oracle(prep, budget)
+        us, cores, sample, nbr, _ = time_oracle(prep, budget)
+        n_rows = nbr.shape[0]
         if i >= args.warmup:
             per_step.append(us)
+    _, pairs = oracle_map(prep)
     value = statistics.mean(per_step)
     layers = 1 if args.conv == "strided" else wl.layers
     return {
@@ -441,12 +632,9 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(value * layers / 1e3, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": DATA,
-        "config": {"workload": f"{args.workload}: N={wl.n}, C_in={wl.c_in}, C_out={wl.c_out}, "
-                               f"layers={layers}, batch={wl.batch_size}, "
-                               f"grid={'x'.join(map(str, wl.spatial_shape))}",
-                   "kernel_size": prep["K"], "groups": prep["G"], "conv": prep["conv"]},
+        "config": workload_config(args, wl, n_rows, pairs, prep["K"], prep["G"], layers),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -473,6 +661,8 @@ def main():
                          "(kernel 3, stride 2, padding 1) on the workload's sites")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle conv work for the cpu_baseline leg (0 disables)")
+    ap.add_argument("--per-workload", type=int, default=1,
+                    help="also time every other workload in the same run (per_workload key; 0 disables)")
     ap.add_argument("--ref-budget", type=float, default=2.0,
                     help="seconds of oracle conv work per reference step")
     args = ap.parse_args()

@@ -152,7 +152,7 @@ typedef struct {
     int64_t pairs;       /* P = number of (row, tap) with a neighbour (>= n)      */
     int64_t n_tiles;     /* 128-row tiles of the mask-sorted order (per group)    */
     int64_t tile_taps;   /* sum over tiles (all groups) of the taps in the tile's mask union */
-    int32_t mapper;      /* spconv_mapper_t actually used (DENSE or SORTED)       */
+    int32_t mapper;      /* spconv_mapper_t actually used (DENSE, SORTED or HASH) */
     int32_t pipeline;    /* spconv_pipeline_t actually used (FUSED, MULTI, WIDE)  */
     int32_t key_bits;    /* live bits of the packed coordinate key                */
     int32_t shape[3];    /* spatial shape used                                    */
@@ -300,8 +300,7 @@ void spconv_map_destroy(spconv_map_t map);
  * memory.  The pages have no counterpart to this entry point; it exists for
  * callers that cannot allocate at the point where they run this code (a
  * plugin's enqueue step in an inference runtime that plans all device memory
- * up front, runtimes that forbid allocation after start-up, code running while
- * its stream is captured into a graph).
+ * up front, runtimes that forbid allocation after start-up).
  *
  *   coords_dev     int32 [n][4] rows (b, x, y, z), device, 16-byte aligned.
  *   n              0 <= n <= 65536; larger n returns SPCONV_ERR_INVALID_ARG
@@ -326,6 +325,27 @@ int spconv_kernel_map_static(const int32_t* coords_dev, int64_t n, const int32_t
 
 /* Number of kernel launches enqueued by the last call on this thread. */
 int32_t spconv_last_launch_count(void);
+
+/*
+ * Diagnostics: runs one of the bounded device waits of the sort passes
+ * against a state that nothing will ever publish, so that it must give up.
+ * The pages have no counterpart; every device wait of the library ends after
+ * a time limit (2 s in the product path) with SPCONV_ERR_TIMEOUT instead of
+ * hanging the GPU, and this call shows that path working with a short limit.
+ *
+ *   which     0: the decoupled look-back of a sort pass, waiting for a
+ *             predecessor partition whose state stays unpublished;
+ *             1: the grid barrier of a two-CTA grid of which only one CTA
+ *             runs.
+ *   limit_ns  the wait's limit, 1 ms .. 100 ms.
+ *   stream    CUDA stream; the call allocates a few hundred bytes
+ *             stream-ordered, synchronises the stream and frees them.
+ *
+ * Returns SPCONV_ERR_TIMEOUT when the wait ran out as designed (the GPU
+ * context stays usable), SPCONV_ERR_INVALID_ARG for a bad argument, or
+ * SPCONV_ERR_CUDA.
+ */
+int spconv_selftest_wait_timeout(int32_t which, int64_t limit_ns, void* stream);
 
 const char* spconv_status_string(int status);
 

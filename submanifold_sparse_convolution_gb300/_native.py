@@ -72,6 +72,7 @@ SIGNATURES = {
     "spconv_kernel_map_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, c_int32_p, ctypes.c_int32,
                                                 ctypes.c_void_p, ctypes.c_void_p]),
     "spconv_last_launch_count": (ctypes.c_int32, []),
+    "spconv_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p]),
     "spconv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 

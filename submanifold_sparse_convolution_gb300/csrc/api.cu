@@ -24,11 +24,7 @@ int read_status(const MapHandle* h) {
     int32_t st = 0;
     SPCONV_CHECK_CUDA(cudaStreamSynchronize(h->stream));
     SPCONV_CHECK_CUDA(cudaMemcpy(&st, h->status, sizeof(st), cudaMemcpyDeviceToHost));
-    if (st & kStatusRange) return SPCONV_ERR_COORD_RANGE;
-    if (st & kStatusDuplicate) return SPCONV_ERR_DUPLICATE_COORD;
-    if (st & kStatusTimeout) return SPCONV_ERR_TIMEOUT;
-    if (st & kStatusInternal) return SPCONV_ERR_INTERNAL;
-    return SPCONV_OK;
+    return status_from_flags(st);
 }
 
 int check_forward_args(const MapHandle* h, const void* feats, const void* out, int32_t c_in,
@@ -432,6 +428,12 @@ void spconv_map_destroy(spconv_map_t map) {
 }
 
 int32_t spconv_last_launch_count(void) { return g_launches; }
+
+int spconv_selftest_wait_timeout(int32_t which, int64_t limit_ns, void* stream) {
+    reset_launch_count();
+    if ((which != 0 && which != 1) || limit_ns < 1000000 || limit_ns > 100000000) return SPCONV_ERR_INVALID_ARG;
+    return wait_probe(which, static_cast<uint64_t>(limit_ns), static_cast<cudaStream_t>(stream));
+}
 
 const char* spconv_status_string(int status) {
     switch (status) {

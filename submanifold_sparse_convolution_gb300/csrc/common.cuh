@@ -153,7 +153,20 @@ int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, in
 int simt_forward(const MapHandle* h, const void* feats, const void* w, void* out, int32_t c_in,
                  int32_t c_out, int32_t dtype, const Epilogue& epi, cudaStream_t s);
 
+// One bounded wait of the sort passes run against a state nothing publishes
+// (which = 0: look-back, 1: grid barrier); the status it ends with (map_wide.cu).
+int wait_probe(int which, uint64_t limit_ns, cudaStream_t s);
+
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPCONV_OK : SPCONV_ERR_CUDA; }
+
+// The status code of a device status word (kStatus* flags), the most specific first.
+inline int status_from_flags(int32_t st) {
+    if (st & kStatusRange) return SPCONV_ERR_COORD_RANGE;
+    if (st & kStatusDuplicate) return SPCONV_ERR_DUPLICATE_COORD;
+    if (st & kStatusTimeout) return SPCONV_ERR_TIMEOUT;
+    if (st & kStatusInternal) return SPCONV_ERR_INTERNAL;
+    return SPCONV_OK;
+}
 
 // Stream-ordered allocation from the library's memory pool on the current
 // device.  The pool keeps freed memory for reuse (no release threshold), so

@@ -3,9 +3,8 @@
 //
 // Some callers cannot allocate device memory when they run this code: a
 // plugin's enqueue step inside an inference runtime that plans every device
-// buffer at initialisation and forbids cudaMalloc afterwards, runtimes
-// certified to never allocate after start-up, or code that must not touch an
-// allocator while its stream is being captured into a graph.  For them this
+// buffer at initialisation and forbids cudaMalloc afterwards, or runtimes
+// certified to never allocate after start-up.  For them this
 // entry point keeps its working buffers (packed keys, row ids, radix
 // histograms, a status word) in one file-scope device array of fixed size,
 // kStaticScratchBytes, which every GPU that loads the library holds until the

@@ -96,7 +96,8 @@ __device__ __forceinline__ uint64_t state(uint32_t epoch, uint64_t flag, int32_t
 // the kernel ends).
 template <int Q, int W>
 __device__ void look_back(const uint64_t* look, int64_t stride, int64_t c, const int (&q)[Q], const bool (&act)[Q],
-                          uint32_t epoch, int32_t (&ex)[Q], int32_t* status) {
+                          uint32_t epoch, int32_t (&ex)[Q], int32_t* status,
+                          uint64_t limit_ns = ptx::kWaitLimitNs) {
     int64_t j[Q];   // next partition to read, per counter (-1: done)
     bool all = true;
 #pragma unroll
@@ -133,7 +134,7 @@ __device__ void look_back(const uint64_t* look, int64_t stride, int64_t c, const
         }
         if (all) return;
         if (it == 0) t0 = ptx::globaltimer();
-        if ((it & 15u) == 15u && ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+        if ((it & 15u) == 15u && ptx::globaltimer() - t0 > limit_ns) {
             atomicOr(status, kStatusTimeout);
             return;
         }
@@ -165,7 +166,8 @@ __device__ __forceinline__ int32_t block_exclusive(int32_t x, int32_t* wsum) {
 // polls (with a short sleep between polls) until all used counters have
 // completed the round.  Arrivals spread over 32 addresses instead of one.
 // Bounded in time.
-__device__ void grid_barrier(int32_t* bar, int64_t P, int round, int32_t* status) {
+__device__ void grid_barrier(int32_t* bar, int64_t P, int round, int32_t* status,
+                             uint64_t limit_ns = ptx::kWaitLimitNs) {
     __syncthreads();
     if (threadIdx.x == 0) {
         const int nsub = P < 32 ? static_cast<int>(P) : 32;
@@ -185,7 +187,7 @@ __device__ void grid_barrier(int32_t* bar, int64_t P, int round, int32_t* status
             if (v >= target) break;
             if (it == 0) t0 = ptx::globaltimer();
             __nanosleep(32);
-            if ((it & 63u) == 63u && ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+            if ((it & 63u) == 63u && ptx::globaltimer() - t0 > limit_ns) {
                 atomicOr(status, kStatusTimeout);
                 break;
             }
@@ -1149,6 +1151,23 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a,
     if (threadIdx.x == 0 && err) atomicOr(a.status, err);
 }
 
+// The two bounded waits of the sort passes, each against a state that nothing
+// will ever publish, with a short limit: which = 0, the look-back of
+// partition 1 over partition 0 (whose state words stay zero); which = 1, the
+// grid barrier of a two-CTA grid entered by the only CTA launched.  Both must
+// give up after limit_ns and set kStatusTimeout; nothing else is touched.
+__global__ void __launch_bounds__(WT) k_wait_probe(int which, const uint64_t* look, int32_t* bar, int32_t* status,
+                                                   uint64_t limit_ns) {
+    if (which == 0) {
+        const int q[1] = {static_cast<int>(threadIdx.x)};
+        const bool act[1] = {true};
+        int32_t ex[1];
+        look_back<1, 8>(look, kWideBins, 1, q, act, 1u, ex, status, limit_ns);
+    } else {
+        grid_barrier(bar, 2, 0, status, limit_ns);
+    }
+}
+
 // A fresh nonzero epoch for every launch that publishes look-back states.
 uint32_t next_epoch() {
     static std::atomic<uint32_t> counter{0};
@@ -1183,6 +1202,29 @@ int launch_pdl(Kernel kernel, unsigned grid, unsigned block, cudaStream_t s, boo
 }
 
 }  // namespace
+
+int wait_probe(int which, uint64_t limit_ns, cudaStream_t s) {
+    // look-back states of one partition (zero: never published), barrier counters, status
+    const size_t look_bytes = kWideBins * sizeof(uint64_t);
+    const size_t bytes = look_bytes + kWideBarrierInts * sizeof(int32_t) + 16;
+    void* buf = nullptr;
+    SPCONV_CHECK_CUDA(cudaMallocAsync(&buf, bytes, s));
+    uint64_t* look = static_cast<uint64_t*>(buf);
+    int32_t* bar = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(buf) + look_bytes);
+    int32_t* status = bar + kWideBarrierInts;
+    int rc = cuda_status(cudaMemsetAsync(buf, 0, bytes, s));
+    if (rc == SPCONV_OK) {
+        k_wait_probe<<<1, WT, 0, s>>>(which, look, bar, status, limit_ns);
+        count_launch();
+        rc = cuda_status(cudaGetLastError());
+    }
+    int32_t st = 0;
+    if (rc == SPCONV_OK) rc = cuda_status(cudaMemcpyAsync(&st, status, sizeof(st), cudaMemcpyDeviceToHost, s));
+    if (rc == SPCONV_OK) rc = cuda_status(cudaStreamSynchronize(s));
+    cudaFreeAsync(buf, s);
+    if (rc != SPCONV_OK) return rc;
+    return status_from_flags(st);
+}
 
 int wide_key_passes(int key_bits) { return (key_bits + kDigitBitsWide - 1) / kDigitBitsWide; }
 

@@ -136,23 +136,6 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) 
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Four-row gather through a 2D tensor map (box: one row x 64 bf16, 128-byte
-// swizzle): rows r0..r3 at column col land in 4 consecutive 128-byte rows at
-// dst_smem.  A row index outside the tensor is filled with zeros.  Completion
-// is counted in bytes (4 x 128) on *bar.
-__device__ __forceinline__ void tma_gather4(uint32_t dst_smem, const void* tmap, int32_t col, int32_t r0,
-                                            int32_t r1, int32_t r2, int32_t r3, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst_smem),
-        "l"(tmap), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation MMA
 // ---------------------------------------------------------------------------

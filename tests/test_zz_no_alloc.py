@@ -1,9 +1,9 @@
 """spconv_kernel_map_static: the kernel map without any device allocation.
 
 Callers that cannot allocate device memory where they run (a plugin's
-enqueue step in a runtime that plans all memory up front, code running while
-its stream is captured) use this entry point; its working buffers are a fixed
-file-scope device array.  Here it is called through the C ABI twice in a row
+enqueue step in a runtime that plans all memory up front, a runtime that
+forbids allocation after start-up) use this entry point; its working buffers
+are a fixed file-scope device array.  Here it is called through the C ABI twice in a row
 and must reproduce, bit for bit, the kernel map that the allocating entry
 point (spconv_build_map + spconv_map_export) gives for the same coordinates.
 This file is collected last so that a failure here leaves every other test run.
@@ -64,3 +64,53 @@ def test_static_map_limits_and_errors():
     assert rc == -5
     rc, nbr = static_map(lib, torch.tensor([[0, 3, 3, 3]], dtype=torch.int32, device="cuda"), (8, 8, 8), 1)
     assert rc == 0 and nbr.cpu().numpy()[0].tolist() == [-1] * 13 + [0] + [-1] * 13
+
+
+def test_static_map_at_the_row_limit_on_the_large_grid():
+    """n = 65536 exactly (the scratch limit), two frames on the 2095 x 2095 x 695 grid whose
+    dense volume overflows int32 (35-bit keys with the frame bit): bit for bit the allocating
+    map, twice in a row."""
+    build_mod.build()
+    lib = _native.load()
+    c, shape, _, _ = S.make_coords("large")
+    c = c[:65536].copy()
+    c[32768:, 0] = 1                            # the second half is frame 1
+    coords = torch.from_numpy(c).cuda()
+    ref = allocating_map(coords, shape, 2)
+    assert (ref[:, :13] >= 0).any()             # the frames have neighbours, not only isolated voxels
+    for _ in range(2):
+        rc, nbr = static_map(lib, coords, shape, 2)
+        assert rc == 0
+        assert torch.equal(nbr, ref)
+
+
+def test_static_map_63_bit_keys():
+    """A (2^20 - 1)^3 grid: 21 bits per axis, 63 key bits, the widest key the sort takes.  A
+    dense 12^3 block in the far corner (every top bit set) and scattered voxels."""
+    build_mod.build()
+    lib = _native.load()
+    X = (1 << 20) - 1
+    shape = (X, X, X)
+    rng = np.random.default_rng(871)
+    g = np.arange(X - 12, X)
+    block = np.stack(np.meshgrid(g, g, g, indexing="ij"), -1).reshape(-1, 3)
+    scatter = rng.integers(0, X, size=(500, 3))
+    cells = np.unique(np.concatenate([block, scatter]), axis=0)
+    c = np.concatenate([np.zeros((len(cells), 1), np.int64), cells], 1).astype(np.int32)
+    c = c[rng.permutation(len(c))]
+    coords = torch.from_numpy(c).cuda()
+    ref = allocating_map(coords, shape, 1)
+    rc, nbr = static_map(lib, coords, shape, 1)
+    assert rc == 0
+    assert torch.equal(nbr, ref)
+
+
+def test_static_map_coordinate_out_of_range():
+    """x = X (one past the last cell) is reported, not clamped or wrapped."""
+    build_mod.build()
+    lib = _native.load()
+    c = torch.tensor([[0, 1, 1, 1], [0, 8, 2, 2], [0, 2, 2, 2]], dtype=torch.int32, device="cuda")
+    rc, _ = static_map(lib, c, (8, 8, 8), 1)
+    assert rc == -6
+    rc, nbr = static_map(lib, c[:1].contiguous(), (8, 8, 8), 1)   # the status word was cleared again
+    assert rc == 0
