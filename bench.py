@@ -282,6 +282,25 @@ class Workbench:
         step_ms = self.timer.run(self.step, steps, record=True)
         return dict(step_ms=step_ms, map_ms=self.timer.spans(0, 1), gemm_ms=self.timer.spans(1, 2))
 
+    def fused_step(self):
+        """The map build and every layer in one fused launch (ReLU between layers)."""
+        m = self.build(self.coords)
+        self.timer.mark()
+        self.sc.subm_forward_layers(m, self.feats, self.wps, relu=[li + 1 < self.L for li in range(self.L)],
+                                    outs=self.fused_outs)
+        m.destroy()
+
+    def time_fused(self, steps, warmup):
+        """Steps with the layers fused into one launch: (step ms, map ms) per step."""
+        self.fused_outs = [torch.empty((self.map0.n, self.wl.c_out), dtype=torch.bfloat16, device=self.device)
+                           for _ in range(2)] * ((self.L + 1) // 2)
+        self.fused_outs = self.fused_outs[:self.L]
+        for _ in range(warmup):
+            self.fused_step()
+        torch.cuda.synchronize(self.device)
+        step_ms = self.timer.run(self.fused_step, steps, record=True)
+        return dict(step_ms=step_ms, map_ms=self.timer.spans(0, 1))
+
     def time_map(self, reps, **over):
         """Map build alone (e.g. another mapper), flushed L2, mean ms."""
         for _ in range(3):
@@ -500,6 +519,15 @@ def per_workload(sc, S, args, device, timer, peaks, sm_mhz, done):
         t = wb.time_steps(steps, 3)
         r = summarise(wb, info, t, peaks, wb.L)
         r["steps"] = steps
+        if wb.L > 1:
+            # the same layers as one launch over the shared map
+            tf = wb.time_fused(steps, 3)
+            fused_layers_ms = statistics.mean(a - b for a, b in zip(tf["step_ms"], tf["map_ms"]))
+            r["fused_layers"] = {"us_per_layer": round(statistics.mean(tf["step_ms"]) * 1e3 / wb.L, 3),
+                                 "layers_us_per_layer": round(fused_layers_ms * 1e3 / wb.L, 3),
+                                 "separate_layers_us_per_layer": round(
+                                     (statistics.mean(t["step_ms"]) - statistics.mean(t["map_ms"])) * 1e3 / wb.L, 3),
+                                 "launches_per_step": 1}
         if name == "stage":
             # the same first layer in exact fp32 (SIMT FFMA, plain ALUs)
             ms = wb.time_fp32_layer(steps)

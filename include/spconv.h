@@ -275,6 +275,37 @@ int spconv_wpack_create_ex(const void* weights_dev, int32_t kernel_size, int32_t
                            int32_t dtype, void* stream, spconv_wpack_t* out_wpack);
 void spconv_wpack_destroy(spconv_wpack_t wpack);
 
+/*
+ * A stack of n_layers submanifold convolutions over one kernel map in a single
+ * launch ("Sparse convolution in FP32", "Offset-group partitioning": the
+ * convolution's last step applies the ReLU to every output row; layers that
+ * share one coordinate set share one map, FlyDSL PR #942, "API style").
+ * Layer l computes out_l = epilogue_l(conv(in_l, W_l)) with in_0 = feats and
+ * in_l = out_{l-1}; every layer visits the same mask-sorted tiles and gather
+ * table.  A layer's gathers start only after every CTA has stored the layer
+ * before it, so each layer's result equals that of a separate
+ * spconv_subm_forward_packed_ex call, bit for bit.
+ *
+ *   map        a submanifold map with one offset group and the tile-union GEMM
+ *              (else SPCONV_ERR_UNSUPPORTED when n_layers > 1).
+ *   feats_dev  bf16 [n][c_in], 16-byte aligned.
+ *   wpacks     n_layers bf16 tensor-core weight packs (spconv_wpack_create),
+ *              all c_in -> c_out with c_in == c_out when n_layers > 1.
+ *   outs_dev   n_layers bf16 [n][c_out] outputs, 16-byte aligned, caller-owned;
+ *              outs_dev[l] must not overlap its own input (feats_dev for l = 0,
+ *              else outs_dev[l - 1]): SPCONV_ERR_ALIAS.  outs_dev[l] may equal
+ *              outs_dev[l - 2] (two buffers ping-pong).
+ *   n_layers   1 .. 8.
+ *   epis       n_layers epilogues (each as in spconv_subm_forward_ex), or NULL.
+ *   stream     CUDA stream; with n_layers > 1 the launch is cooperative (one
+ *              CTA per SM, all resident) and uses a small per-map counter array.
+ * Device-side waits between layers are bounded: a stall sets
+ * SPCONV_ERR_TIMEOUT in the map's status (spconv_map_status).
+ */
+int spconv_subm_forward_layers(spconv_map_t map, const void* feats_dev, const spconv_wpack_t* wpacks,
+                               void* const* outs_dev, int32_t n_layers, const spconv_epilogue_t* epis,
+                               void* stream);
+
 /* Synchronise the map's stream and return the first device-detected error
  * (duplicate or out-of-range coordinates, kernel timeouts), else SPCONV_OK. */
 int spconv_map_status(spconv_map_t map);

@@ -332,6 +332,46 @@ def subm_forward_packed(m: Map, feats: torch.Tensor, wp: WPack, out: Optional[to
     return out
 
 
+def subm_forward_layers(m: Map, feats: torch.Tensor, wps: Sequence[WPack], relu: Sequence[bool] = (),
+                        outs: Optional[Sequence[torch.Tensor]] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> list:
+    """``spconv_subm_forward_layers``: ``len(wps)`` layers over map ``m`` in one launch;
+    layer l reads layer l - 1's output (layer 0: ``feats``) and applies a ReLU
+    when ``relu[l]``.  ``outs`` gives one output per layer (consecutive ones may
+    not overlap; two buffers may alternate); by default two buffers alternate.
+    Returns the list of per-layer outputs (views of ``outs``)."""
+    lib = library()
+    _require_cuda(feats, "feats")
+    L = len(wps)
+    if L < 1:
+        raise ValueError("at least one layer")
+    wp0 = wps[0]
+    if feats.dtype != torch.bfloat16 or tuple(feats.shape) != (m.n_in, wp0.c_in):
+        raise ValueError(f"feats must be bf16 [{m.n_in}, {wp0.c_in}]")
+    relu = list(relu) + [False] * (L - len(relu))
+    if outs is None:
+        bufs = [torch.empty((m.n, wp0.c_out), dtype=feats.dtype, device=feats.device) for _ in range(min(L, 2))]
+        outs = [bufs[l % 2] for l in range(L)]
+    else:
+        outs = list(outs)
+        if len(outs) != L:
+            raise ValueError(f"{L} outputs expected")
+        for o in outs:
+            _require_cuda(o, "out")
+            if o.dtype != feats.dtype or tuple(o.shape) != (m.n, wp0.c_out):
+                raise ValueError(f"outputs must be bf16 [{m.n}, {wp0.c_out}]")
+    wh = (ctypes.c_void_p * L)(*[w.handle for w in wps])
+    oh = (ctypes.c_void_p * L)(*[_ptr(o) for o in outs])
+    epis = (_native.Epilogue * L)()
+    for l in range(L):
+        epis[l].relu = 1 if relu[l] else 0
+    rc = lib.spconv_subm_forward_layers(m.handle, _ptr(feats), ctypes.cast(wh, ctypes.POINTER(ctypes.c_void_p)),
+                                        ctypes.cast(oh, ctypes.POINTER(ctypes.c_void_p)), L, epis,
+                                        _stream_ptr(stream))
+    _check(rc, "spconv_subm_forward_layers")
+    return outs
+
+
 def map_status(m: Map) -> int:
     """``spconv_map_status``: 0, or the first device-detected error code (synchronises)."""
     return int(library().spconv_map_status(m.handle))

@@ -65,6 +65,9 @@ SIGNATURES = {
                                                      ctypes.c_void_p, ctypes.POINTER(Epilogue),
                                                      ctypes.c_void_p]),
     "spconv_wpack_destroy": (None, [ctypes.c_void_p]),
+    "spconv_subm_forward_layers": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
+                                                  ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
+                                                  ctypes.POINTER(Epilogue), ctypes.c_void_p]),
     "spconv_map_status": (ctypes.c_int, [ctypes.c_void_p]),
     "spconv_map_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(MapInfo)]),
     "spconv_map_export": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_void_p] * 6 + [ctypes.c_void_p]),

@@ -354,6 +354,37 @@ int spconv_subm_forward_packed_ex(spconv_map_t map, const void* feats_dev, spcon
     return simt_forward(map, feats_dev, wpack->data, out_dev, wpack->c_in, wpack->c_out, wpack->dtype, e, s);
 }
 
+int spconv_subm_forward_layers(spconv_map_t map, const void* feats_dev, const spconv_wpack_t* wpacks,
+                               void* const* outs_dev, int32_t n_layers, const spconv_epilogue_t* epis,
+                               void* stream) {
+    reset_launch_count();
+    if (!map || !wpacks || !outs_dev || n_layers < 1 || n_layers > kMaxFusedLayers) return SPCONV_ERR_INVALID_ARG;
+    for (int l = 0; l < n_layers; ++l)
+        if (!wpacks[l]) return SPCONV_ERR_INVALID_ARG;
+    const int32_t c_in = wpacks[0]->c_in, c_out = wpacks[0]->c_out;
+    for (int l = 0; l < n_layers; ++l) {
+        const WPackHandle* w = wpacks[l];
+        if (w->c_in != c_in || w->c_out != c_out || w->taps != map->taps) return SPCONV_ERR_INVALID_ARG;
+        if (!w->tensor_path || w->dtype != SPCONV_BF16) return SPCONV_ERR_UNSUPPORTED;
+    }
+    if (n_layers > 1 && c_in != c_out) return SPCONV_ERR_INVALID_ARG;
+    // later layers gather the previous output through the same map: its rows
+    // must be the sites it indexes (a submanifold map, one offset group)
+    if (n_layers > 1 && (map->conv != kConvSubmanifold || map->groups > 1 || map->gemm == SPCONV_GEMM_TAP_MAJOR))
+        return SPCONV_ERR_UNSUPPORTED;
+    Epilogue e[kMaxFusedLayers];
+    const void* wp[kMaxFusedLayers];
+    for (int l = 0; l < n_layers; ++l) {
+        const void* in = l == 0 ? feats_dev : outs_dev[l - 1];
+        SPCONV_CHECK(check_forward_args(map, in, outs_dev[l], c_in, c_out, SPCONV_BF16));
+        SPCONV_CHECK(check_epilogue(map, epis ? &epis[l] : nullptr, outs_dev[l], c_out, SPCONV_BF16, &e[l]));
+        if (map->n > 0 && (!aligned(in, 16) || !aligned(outs_dev[l], 16))) return SPCONV_ERR_INVALID_ARG;
+        wp[l] = wpacks[l]->data;
+    }
+    if (map->n == 0) return SPCONV_OK;
+    return tc_forward_layers(map, feats_dev, wp, outs_dev, e, n_layers, c_in, c_out, static_cast<cudaStream_t>(stream));
+}
+
 void spconv_wpack_destroy(spconv_wpack_t wpack) {
     if (!wpack) return;
     if (wpack->data) cudaFreeAsync(wpack->data, wpack->stream);
@@ -423,6 +454,7 @@ void spconv_map_destroy(spconv_map_t map) {
     if (map->arena) cudaFreeAsync(map->arena, map->stream);
     if (map->wspace) cudaFreeAsync(map->wspace, map->stream);
     if (map->acc) cudaFreeAsync(map->acc, map->stream);
+    if (map->layer_done) cudaFreeAsync(map->layer_done, map->stream);
     if (map->out_alloc) cudaFreeAsync(map->out_alloc, map->stream);
     delete map;
 }

@@ -14,6 +14,7 @@ constexpr int kMaxGroupTaps = 27;   // taps of one offset group (mask bits, GEMM
 constexpr int kMaxDevices = 64;    // per-device one-time settings are kept for device ids below this
 constexpr int kTileRows = 128;      // rows per output tile (tensor-core M)
 constexpr int kNbrStride = 32;      // padded width of the internal kernel-map rows
+constexpr int kMaxFusedLayers = 8;  // layers of one fused forward launch
 
 // Device status word bits (set with atomicOr by kernels).
 enum : int32_t {
@@ -104,6 +105,8 @@ struct MapHandle {
     // fp32 sums of the tap-major forward ([n][c_out])
     void* acc = nullptr;
     size_t acc_bytes = 0;
+    // per-layer CTA counters of a fused layer stack ([kMaxFusedLayers] int32)
+    int32_t* layer_done = nullptr;
 };
 
 struct WPackHandle {
@@ -148,6 +151,10 @@ size_t tc_pack_bytes(int32_t c_in, int32_t c_out, int32_t taps);
 int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, int32_t taps, void* dst, cudaStream_t s);
 int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
                int32_t c_out, const Epilogue& epi, cudaStream_t s);
+// n_layers layers of c_in -> c_out (c_in == c_out when n_layers > 1) in one
+// cooperative launch: layer l reads outs[l - 1] (layer 0: feats), stores outs[l]
+int tc_forward_layers(MapHandle* h, const void* feats, const void* const* wpacks, void* const* outs,
+                      const Epilogue* epis, int32_t n_layers, int32_t c_in, int32_t c_out, cudaStream_t s);
 
 // ---- SIMT path (gemm_simt.cu) ----------------------------------------------
 int simt_forward(const MapHandle* h, const void* feats, const void* w, void* out, int32_t c_in,

@@ -73,11 +73,10 @@ __device__ __forceinline__ int producer_slot(int w) {
 constexpr int kStageA = BM * BK * 2;   // 16 KB
 constexpr int kIdxBytes = kTaps * BM * 4;   // one item's gather indices, 13.5 KB
 constexpr int kMetaRing = 4;                // items in flight between scheduler and epilogue
+constexpr int kLayerMark = -2;              // a meta entry that closes a layer of a fused stack
 
 struct TcParams {
-    const __nv_bfloat16* feats;   // [n][c_in]
-    const uint8_t* wpack;         // packed weights, see k_pack_weights
-    __nv_bfloat16* out;           // [n][c_out]
+    const __nv_bfloat16* feats;   // [n][c_in], the input of layer 0
     const int32_t* gtab;          // [27][n_pad]
     const uint32_t* tile_union;   // [n_tiles]
     const int32_t* tile_order;    // [n_tiles]
@@ -94,8 +93,6 @@ struct TcParams {
     int32_t k_chunks;             // ceil(c_in / 64)
     int32_t n_tile;               // output channels per item (multiple of 16, <= NTMAX)
     int32_t n_nb;                 // c_out / n_tile
-    Epilogue epi;                 // applied to each fp32 sum before the rounding
-    int32_t epi_on;               // epi.active()
     // offset groups: this launch covers the group's taps [k0, k0 + taps of the
     // union bits); gtab, tile_union, tile_order and perm point at the group's
     // slices, the packed weights hold taps_w taps per output block
@@ -103,6 +100,19 @@ struct TcParams {
     int32_t mode;                 // kModeStore, or the partial-sum modes of a grouped forward
     float* ws;                    // [n][c_out] fp32 partial sums of the groups before the last
     const int32_t* tiles_dev;     // device count of the leading tiles of tile_order to visit, or null (all)
+    // Layer l multiplies the output of layer l - 1 (layer 0: feats) by its
+    // packed weights wpacks[l] (see k_pack_weights), applies epis[l] to each
+    // fp32 sum before the rounding (when epi_ons[l]) and stores outs[l]
+    // ([n][c_out]).  One layer is the plain forward.  A stack of layers over
+    // the same map runs in one launch (tile-union only): between two layers
+    // every CTA counts itself into layer_done[l] once its stores are visible,
+    // and no gather of layer l + 1 starts before all have.
+    int32_t n_layers;
+    const uint8_t* wpacks[kMaxFusedLayers];
+    __nv_bfloat16* outs[kMaxFusedLayers];
+    Epilogue epis[kMaxFusedLayers];
+    int32_t epi_ons[kMaxFusedLayers];
+    int32_t* layer_done;          // [kMaxFusedLayers], zero at launch
 };
 
 // Output modes.  One group: the tile's sum, rounded once, to out.  G groups,
@@ -207,10 +217,12 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
     uint64_t* meta_full = idx_empty + 2;         // [kMetaRing] item published (epilogue side)
     uint64_t* meta_empty = meta_full + kMetaRing;// [kMetaRing] epilogue has read it
     uint64_t* exit_bar = meta_empty + kMetaRing;
-    int32_t* m_item = reinterpret_cast<int32_t*>(exit_bar + 1);   // [kMetaRing], -1 = no more work
+    uint64_t* layer_bar = exit_bar + 1;          // the epilogue warps have stored a layer
+    int32_t* m_item = reinterpret_cast<int32_t*>(layer_bar + 1);   // [kMetaRing], -1 = no more work
     int32_t* m_tile = m_item + kMetaRing;
     uint32_t* m_uni = reinterpret_cast<uint32_t*>(m_tile + kMetaRing);
-    uint32_t* tmem_slot = m_uni + kMetaRing;
+    int32_t* m_layer = reinterpret_cast<int32_t*>(m_uni + kMetaRing);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(m_layer + kMetaRing);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // tap-major: the output rows of the items in the meta ring, in the last
     // kMetaRing x 128 entries of the index area (only rank 0 of each index
@@ -234,6 +246,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
             ptx::mbar_init(&meta_empty[r], kEpiWarps);
         }
         ptx::mbar_init(exit_bar, 1);
+        ptx::mbar_init(layer_bar, kEpiWarps);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -266,6 +279,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
     }
     // the scheduler looks up its first item while the CTA sets up:
     // tile-union (tile, union); tap-major (pair base, pair count in s_tile, tap bit in s_uni)
+    int s_layer = 0, s_round = 0;   // the scheduler's layer and its round in that layer
     int s_it = snake_item(0, blockIdx.x, gridDim.x), s_tile = 0, s_cnt = 0;
     uint32_t s_uni = 0;
     auto lookup = [&](int it) {
@@ -322,6 +336,47 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
             const int it = s_it;
             const int tile = s_tile;
             const uint32_t uni = s_uni;
+            if (it >= n_items && s_layer + 1 < p.n_layers) {
+                // this CTA's items of the layer are published: a marker tells the
+                // epilogue to count the CTA in once they are stored, and the next
+                // layer's items wait until every CTA has
+                if (lane == 0) {
+                    m_item[r] = kLayerMark;
+                    m_layer[r] = s_layer;
+                    ptx::mbar_arrive(&idx_full[b]);
+                    ptx::mbar_arrive(&meta_full[r]);
+                }
+                bool ok = true;
+                if (lane == 0) {
+                    const uint64_t t0 = ptx::globaltimer();
+                    for (uint32_t spin = 0;; ++spin) {
+                        int32_t v;
+                        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];"
+                                     : "=r"(v)
+                                     : "l"(p.layer_done + s_layer)
+                                     : "memory");
+                        if (v >= static_cast<int32_t>(gridDim.x)) break;
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                        if ((spin & 63u) == 63u && ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+                    if (lane == 0) fail();
+                    break;
+                }
+                ++s_layer;
+                s_round = 0;
+                s_it = snake_item(0, blockIdx.x, gridDim.x);
+                if (s_it < n_items) lookup(s_it);
+                continue;
+            }
             if (it >= n_items) {   // no more work: publish the end marker
                 if (lane == 0) {
                     m_item[r] = -1;
@@ -345,6 +400,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                     m_item[r] = it;
                     m_tile[r] = tile;
                     m_uni[r] = uni;
+                    m_layer[r] = s_layer;
                     ptx::mbar_arrive(&idx_full[b]);
                 }
             } else {
@@ -352,6 +408,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                     m_item[r] = it;
                     m_tile[r] = tile;
                     m_uni[r] = uni;
+                    m_layer[r] = s_layer;
                     ptx::mbar_arrive_expect_tx(&idx_full[b], static_cast<uint32_t>(__popc(uni)) * (BM * 4));
                 }
                 __syncwarp();
@@ -367,7 +424,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&meta_full[r]);
             // look up the next item now: the loads overlap the waits above
-            s_it = snake_item(L + 1, blockIdx.x, gridDim.x);
+            s_it = snake_item(++s_round, blockIdx.x, gridDim.x);
             if (s_it < n_items) lookup(s_it);
         }
         // copies still in flight (only after an abort) land before the CTA exits
@@ -393,6 +450,27 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
         constexpr int RG = BM / P / 4;
         const int grp = lane >> 3, chunk = lane & 7;
         const int row0 = part * (BM / P) + grp * RG;   // a multiple of 8: the swizzle phase of row0 + i is i & 7
+        // The MMA waits for whole groups of G stages: an incomplete group (at
+        // the end, or before a layer boundary, where the next stage waits for
+        // every CTA) is completed with empty stages, two arrivals each.
+        auto pad_group = [&]() {
+            const uint32_t padded = (f + G - 1) / G * G;
+            for (uint32_t d = f; d < padded && !stop; ++d) {
+                if (static_cast<int>(d % S) != slot) continue;
+                const uint32_t u = d / S;
+                if (u > 0 && !warp_wait(&empty[slot], (u - 1) & 1)) {
+                    if (lane == 0) fail();
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) {
+                    ptx::mbar_arrive(gfull);
+                    ptx::mbar_arrive(gfull);
+                }
+                last = d;
+            }
+            f = padded;
+        };
         for (int L = 0; !stop; ++L) {
             const int b = L & 1;
             if (!warp_wait(&idx_full[b], (L >> 1) & 1)) {
@@ -400,10 +478,19 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                 break;
             }
             const int it = m_item[L % kMetaRing];
+            if (it == kLayerMark) {   // a layer boundary: nothing to gather
+                pad_group();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&idx_empty[b]);
+                continue;
+            }
             if (it < 0) break;
             const int nb = it % p.n_nb;
+            const int layer = m_layer[L % kMetaRing];
             uint32_t uni = m_uni[L % kMetaRing];
             const int32_t* gidx = idx + b * kTaps * BM;
+            const __nv_bfloat16* lin = layer == 0 ? p.feats : p.outs[layer - 1];
+            const uint8_t* lw = p.wpacks[layer];
             for (int j = 0; uni && !stop; ++j) {
                 const int k = __ffs(uni) - 1;
                 uni &= uni - 1;
@@ -430,7 +517,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                         if (part == 0) {
                             ptx::mbar_arrive_expect_tx(gfull, b_bytes);
                             const uint8_t* src =
-                                p.wpack + (static_cast<int64_t>(nb * p.taps_w + p.k0 + k) * p.k_chunks + kc) * b_bytes;
+                                lw + (static_cast<int64_t>(nb * p.taps_w + p.k0 + k) * p.k_chunks + kc) * b_bytes;
                             ptx::bulk_copy_g2s(b_smem, src, b_bytes, gfull);
                         } else {
                             ptx::mbar_arrive(gfull);
@@ -438,7 +525,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                     }
                     const int kcol = kc * BK + chunk * 8;
                     const bool col_ok = kcol < p.c_in;
-                    const __nv_bfloat16* fcol = p.feats + kcol;
+                    const __nv_bfloat16* fcol = lin + kcol;
                     const uint32_t dst0 = a_smem + static_cast<uint32_t>(row0) * 128;
                     bool bad = false;   // a row index past n: skipped, reported below
 #pragma unroll
@@ -464,20 +551,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
             if (lane == 0) ptx::mbar_arrive(&idx_empty[b]);
         }
         // the last group may be incomplete: its remaining stages arrive empty
-        const uint32_t padded = (f + G - 1) / G * G;
-        for (uint32_t d = f; d < padded && !stop; ++d) {
-            if (static_cast<int>(d % S) != slot) continue;
-            const uint32_t u = d / S;
-            if (u > 0 && !warp_wait(&empty[slot], (u - 1) & 1)) {
-                if (lane == 0) fail();
-                break;
-            }
-            if (lane == 0) {
-                ptx::mbar_arrive(gfull);
-                ptx::mbar_arrive(gfull);
-            }
-            last = d;
-        }
+        if (!stop) pad_group();
         // every copy this warp issued has landed before the CTA may exit
         if (lane == 0 && last >= 0 && !ptx::mbar_wait(gfull, (static_cast<uint32_t>(last) / S) & 1, nullptr))
             atomicOr(p.status, kStatusTimeout);
@@ -487,6 +561,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
         const uint32_t leader = lane == 0;
         const uint32_t idesc = ptx::idesc_bf16_f32(BM, static_cast<uint32_t>(p.n_tile));
         uint32_t f = 0;
+        int ai = 0;   // items accumulated so far: item ai uses TMEM buffer ai & 1
         bool stop = false;
         for (int L = 0; !stop; ++L) {
             const int b = L & 1;
@@ -498,9 +573,16 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
             const int n_taps = __popc(m_uni[L % kMetaRing]);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&idx_empty[b]);
+            if (it == kLayerMark) {
+                // the producers completed the open group with empty stages (its
+                // barrier was waited for at its first stage): release them
+                for (; f % G != 0; ++f) ptx::mma_commit_if(leader, &empty[f % S]);
+                continue;
+            }
             if (it < 0) break;
-            const int buf = L & 1;
-            const uint32_t v = static_cast<uint32_t>(L >> 1);
+            const int buf = ai & 1;
+            const uint32_t v = static_cast<uint32_t>(ai >> 1);
+            ++ai;
             if (v > 0 && !warp_wait(&acc_empty[buf], (v - 1) & 1)) {
                 if (lane == 0) fail();
                 break;
@@ -536,6 +618,8 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
         if (!done && lane == 0) atomicOr(p.status, kStatusTimeout);
     } else if (warp < kEpiWarps) {
         // ---------------- epilogue: warp w reads TMEM lanes [32w, 32w + 32)
+        int ai = 0;      // items stored so far: item ai sits in TMEM buffer ai & 1
+        int marks = 0;   // layer markers seen
         for (int L = 0;; ++L) {
             const int r = L % kMetaRing;
             if (!warp_wait(&meta_full[r], (L / kMetaRing) & 1)) {
@@ -555,19 +639,42 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                 const int64_t s = static_cast<int64_t>(tile) * BM + warp * 32 + lane;
                 orig = s < p.n ? p.perm[s] : -1;
             }
+            const int layer = m_layer[r];
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&meta_empty[r]);
+            if (it == kLayerMark) {
+                // every store of this CTA's items of the layer has been issued:
+                // each thread makes its own visible GPU-wide, the warps meet on
+                // layer_bar, and warp 0 counts the CTA in
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(layer_bar);
+                if (warp == 0) {
+                    if (!warp_wait(layer_bar, static_cast<uint32_t>(marks) & 1u)) {
+                        if (lane == 0) fail();
+                        break;
+                    }
+                    if (lane == 0) atomicAdd(p.layer_done + layer, 1);
+                }
+                ++marks;
+                continue;
+            }
             if (it < 0) break;
             const int nb = it % p.n_nb;
-            const int buf = L & 1;
-            if (!warp_wait(&acc_full[buf], (L >> 1) & 1)) {
+            const int buf = ai & 1;
+            const uint32_t par = static_cast<uint32_t>(ai >> 1) & 1u;
+            ++ai;
+            __nv_bfloat16* lout = p.outs[layer];
+            const Epilogue& lepi = p.epis[layer];
+            const int32_t lepi_on = p.epi_ons[layer];
+            if (!warp_wait(&acc_full[buf], par)) {
                 if (lane == 0) fail();
                 break;
             }
             ptx::tc_fence_after();
             const bool to_out = p.mode == kModeStore || p.mode == kModeWsFinish;
             __nv_bfloat16* dst_row = (!TM && orig >= 0 && to_out)
-                                         ? p.out + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile
+                                         ? lout + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile
                                          : nullptr;
             float* ws_row = (!TM && orig >= 0 && p.mode != kModeStore)
                                 ? p.ws + static_cast<int64_t>(orig) * p.c_out + nb * p.n_tile
@@ -620,11 +727,11 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                         }
                     }
                 } else if (dst_row) {
-                    if (p.epi_on) {
+                    if (lepi_on) {
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
                             if (h >= 2 && !two) break;
-                            epilogue8(v + 8 * h, p.epi, orig, p.c_out, nb * p.n_tile + c + 8 * h);
+                            epilogue8(v + 8 * h, lepi, orig, p.c_out, nb * p.n_tile + c + 8 * h);
                         }
                     }
                     uint4* d = reinterpret_cast<uint4*>(dst_row + c);
@@ -721,8 +828,10 @@ __global__ void __launch_bounds__(256) k_acc_to_bf16(const float4* __restrict__ 
 }
 
 // grid: one persistent CTA per SM, or fewer when the item count is known and smaller
+// cooperative: every CTA resident at once (a fused stack waits across CTAs
+// between layers), launched without programmatic dependent launch
 template <int NTMAX, bool TM>
-int launch_tc(const TcParams& p, int grid, cudaStream_t s) {
+int launch_tc(const TcParams& p, int grid, cudaStream_t s, bool cooperative) {
     using Cfg = TcConfig<NTMAX>;
     static bool smem_set[kMaxDevices] = {};   // once per device
     int dev = 0;
@@ -739,6 +848,10 @@ int launch_tc(const TcParams& p, int grid, cudaStream_t s) {
     cfg.dynamicSmemBytes = Cfg::kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1] = {pdl_attr()};
+    if (cooperative) {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     SPCONV_CHECK_CUDA(cudaLaunchKernelEx(&cfg, k_tc_gemm<NTMAX, TM>, p));
@@ -747,10 +860,10 @@ int launch_tc(const TcParams& p, int grid, cudaStream_t s) {
 }
 
 template <bool TM>
-int launch_tc_n(const TcParams& p, int grid, cudaStream_t s) {
-    if (p.n_tile > 128) return launch_tc<256, TM>(p, grid, s);
-    if (p.n_tile > 64) return launch_tc<128, TM>(p, grid, s);
-    return launch_tc<64, TM>(p, grid, s);
+int launch_tc_n(const TcParams& p, int grid, cudaStream_t s, bool cooperative = false) {
+    if (p.n_tile > 128) return launch_tc<256, TM>(p, grid, s, cooperative);
+    if (p.n_tile > 64) return launch_tc<128, TM>(p, grid, s, cooperative);
+    return launch_tc<64, TM>(p, grid, s, cooperative);
 }
 
 }  // namespace
@@ -788,13 +901,13 @@ int tc_pack_weights(const void* w, int32_t c_in, int32_t c_out, int32_t taps, vo
     return cuda_status(cudaGetLastError());
 }
 
-int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
-               int32_t c_out, const Epilogue& epi, cudaStream_t s) {
-    if (h->n == 0) return SPCONV_OK;
-    TcParams p;
+namespace {
+
+// The launch parameters shared by every forward of map h (one layer, the
+// plain store mode, all tiles).
+TcParams base_params(const MapHandle* h, const void* feats, int32_t c_in, int32_t c_out) {
+    TcParams p = {};
     p.feats = static_cast<const __nv_bfloat16*>(feats);
-    p.wpack = static_cast<const uint8_t*>(wpack);
-    p.out = static_cast<__nv_bfloat16*>(out);
     p.gtab = h->gtab;
     p.tile_union = h->tile_union;
     p.tile_order = h->tile_order;
@@ -812,13 +925,26 @@ int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, in
     p.k_chunks = (c_in + BK - 1) / BK;
     p.n_tile = tc_tile_n(c_out);
     p.n_nb = c_out / p.n_tile;
-    p.epi = epi;
-    p.epi_on = epi.active() ? 1 : 0;
     p.k0 = 0;
     p.taps_w = h->taps;
     p.mode = kModeStore;
     p.ws = nullptr;
     p.tiles_dev = nullptr;
+    p.n_layers = 1;
+    p.layer_done = nullptr;
+    return p;
+}
+
+}  // namespace
+
+int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, int32_t c_in,
+               int32_t c_out, const Epilogue& epi, cudaStream_t s) {
+    if (h->n == 0) return SPCONV_OK;
+    TcParams p = base_params(h, feats, c_in, c_out);
+    p.wpacks[0] = static_cast<const uint8_t*>(wpack);
+    p.outs[0] = static_cast<__nv_bfloat16*>(out);
+    p.epis[0] = epi;
+    p.epi_ons[0] = epi.active() ? 1 : 0;
     const int64_t items = h->n_tiles * p.n_nb;
     if (items > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
     p.n_items = static_cast<int32_t>(items);
@@ -872,9 +998,42 @@ int tc_forward(MapHandle* h, const void* feats, const void* wpack, void* out, in
     const int64_t count8 = static_cast<int64_t>(h->n) * c_out / 8;
     const int64_t blocks = (count8 + 255) / 256;
     k_acc_to_bf16<<<static_cast<unsigned>(blocks < 8 * sms ? blocks : 8 * sms), 256, 0, s>>>(
-        reinterpret_cast<const float4*>(p.acc), reinterpret_cast<uint4*>(out), count8, c_out, epi, p.epi_on);
+        reinterpret_cast<const float4*>(p.acc), reinterpret_cast<uint4*>(out), count8, c_out, epi, p.epi_ons[0]);
     count_launch();
     return cuda_status(cudaGetLastError());
+}
+
+int tc_forward_layers(MapHandle* h, const void* feats, const void* const* wpacks, void* const* outs,
+                      const Epilogue* epis, int32_t n_layers, int32_t c_in, int32_t c_out, cudaStream_t s) {
+    if (h->n == 0) return SPCONV_OK;
+    if (n_layers < 1 || n_layers > kMaxFusedLayers) return SPCONV_ERR_INVALID_ARG;
+    if (h->groups > 1 || h->gemm == SPCONV_GEMM_TAP_MAJOR) return SPCONV_ERR_UNSUPPORTED;
+    TcParams p = base_params(h, feats, c_in, c_out);
+    p.n_layers = n_layers;
+    for (int l = 0; l < n_layers; ++l) {
+        p.wpacks[l] = static_cast<const uint8_t*>(wpacks[l]);
+        p.outs[l] = static_cast<__nv_bfloat16*>(outs[l]);
+        p.epis[l] = epis[l];
+        p.epi_ons[l] = epis[l].active() ? 1 : 0;
+    }
+    const int64_t items = h->n_tiles * p.n_nb;
+    if (items > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
+    p.n_items = static_cast<int32_t>(items);
+    const int sms = num_sms();
+    const int grid = p.n_items < sms ? p.n_items : sms;
+    if (n_layers == 1) return launch_tc_n<false>(p, grid, s);
+    if (!h->layer_done) {
+        void* buf = nullptr;
+        if (pool_alloc(&buf, kMaxFusedLayers * sizeof(int32_t), s) != cudaSuccess) {
+            cudaGetLastError();
+            return SPCONV_ERR_OOM;
+        }
+        h->layer_done = static_cast<int32_t*>(buf);
+    }
+    SPCONV_CHECK_CUDA(cudaMemsetAsync(h->layer_done, 0, kMaxFusedLayers * sizeof(int32_t), s));
+    p.layer_done = h->layer_done;
+    // one CTA per SM, all resident together: the kernel's shared memory admits one per SM
+    return launch_tc_n<false>(p, grid, s, true);
 }
 
 }  // namespace spconv

@@ -360,6 +360,28 @@ def test_fp32_exact_small(c_in, c_out):
     check_fp32(out, oracle.conv_f64(nbr, f.double().numpy(), w.double().numpy()))
 
 
+@pytest.mark.parametrize("c_in,c_out,n", [(64, 64, 3000), (128, 128, 2000), (64, 192, 700), (100, 64, 1500)])
+def test_fp32_tiled_matches_generic_bits(c_in, c_out, n):
+    """The tiled fp32 kernel (16-byte aligned buffers) and the one-thread-per-output kernel
+    (reached through a misaligned output view) run the same FMA chain: equal bits, with an
+    epilogue, and within 1e-5 of the oracle."""
+    wl = S.random_cloud(700 + c_in + n, n, shape=(16, 16, 16), batch_size=2, c_in=c_in, c_out=c_out)
+    rng = np.random.default_rng(701)
+    f = torch.from_numpy(rng.standard_normal((wl.n, c_in)).astype(np.float32)).cuda()
+    w = torch.from_numpy((rng.standard_normal((27, c_in, c_out)) * S.weights_std(c_in)).astype(np.float32)).cuda()
+    bias = torch.from_numpy(rng.standard_normal(c_out).astype(np.float32)).cuda()
+    m = build(wl)
+    a = sc.subm_forward(m, f, w, bias=bias, relu=True)
+    big = torch.empty(wl.n * c_out + 1, dtype=torch.float32, device="cuda")
+    b = sc.subm_forward(m, f, w, out=big[1:].view(wl.n, c_out), bias=bias, relu=True)
+    assert sc.map_status(m) == 0
+    assert torch.equal(a, b)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    ref = oracle.epilogue_f64(oracle.conv_f64(nbr, f.double().cpu().numpy(), w.double().cpu().numpy()),
+                              bias=bias.double().cpu().numpy(), relu=True)
+    check_fp32(a, ref)
+
+
 def test_packed_weights_match_unpacked():
     wl = S.random_cloud(31, 3000, shape=(16, 16, 16), c_in=128, c_out=128)
     m = build(wl)
@@ -784,7 +806,7 @@ def test_strided_and_inverse_maps_small(seed, n, shape, batch, bit_order):
 
 
 STRIDED_FWD = [(64, 64, torch.bfloat16), (128, 128, torch.bfloat16), (32, 256, torch.bfloat16),
-               (5, 7, torch.bfloat16), (16, 16, torch.float32)]
+               (5, 7, torch.bfloat16), (16, 16, torch.float32), (64, 128, torch.float32)]
 
 
 @pytest.mark.parametrize("c_in,c_out,dtype", STRIDED_FWD)
@@ -899,3 +921,75 @@ def test_bounded_wait_times_out_and_gpu_keeps_working(which):
     assert sc.map_status(m) == 0
     nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, 1)
     check_bf16(out, oracle.conv_f64(nbr, wl.feats.double().numpy(), wl.weights[0].double().numpy()))
+
+
+# ---------------------------------------------------------------------------
+# a stack of layers over one map in one launch
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("c,n,layers", [(64, 3000, 3), (128, 5000, 2), (64, 300, 4), (16, 1000, 2)])
+def test_fused_layers_match_separate_layers(c, n, layers):
+    """Every layer of the fused launch has the bits of the same layer run as its own launch
+    (fewer items than SMs for n = 300: a smaller cooperative grid)."""
+    wl = S.random_cloud(900 + c + n, n, shape=(20, 20, 20), batch_size=2, c_in=c, c_out=c)
+    m = build(wl)
+    rng = np.random.default_rng(901)
+    ws = [torch.from_numpy((rng.standard_normal((27, c, c)) * S.weights_std(c)).astype(np.float32))
+          .to(torch.bfloat16).cuda() for _ in range(layers)]
+    wps = [sc.wpack_create(w) for w in ws]
+    relu = [l + 1 < layers for l in range(layers)]
+    outs = [torch.empty((wl.n, c), dtype=torch.bfloat16, device="cuda") for _ in range(layers)]
+    fused = sc.subm_forward_layers(m, wl.feats.cuda(), wps, relu=relu, outs=outs)
+    assert sc.map_status(m) == 0
+    x = wl.feats.cuda()
+    for l in range(layers):
+        y = sc.subm_forward_packed(m, x, wps[l], relu=relu[l])
+        assert torch.equal(fused[l], y), l
+        x = y
+    # two alternating buffers (the default) give the same final layer
+    again = sc.subm_forward_layers(m, wl.feats.cuda(), wps, relu=relu)
+    assert torch.equal(again[-1], fused[-1])
+
+
+def test_fused_stage_six_layers_every_row():
+    """The stage workload's six layers (ReLU between them) in one launch: every row of every
+    layer against the oracle, each layer fed the GPU's input to it."""
+    wl = S.make_workload("stage")
+    m = build(wl)
+    nbr = oracle.kernel_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size)
+    wps = [sc.wpack_create(w.cuda()) for w in wl.weights]
+    L = len(wps)
+    relu = [l + 1 < L for l in range(L)]
+    outs = [torch.empty((wl.n, wl.c_out), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    ys = sc.subm_forward_layers(m, wl.feats.cuda(), wps, relu=relu, outs=outs)
+    assert sc.map_status(m) == 0
+    x = wl.feats
+    for l in range(L):
+        ref = oracle.epilogue_f64(oracle.conv_f64(nbr, x.double().numpy(), wl.weights[l].double().numpy()),
+                                  relu=relu[l])
+        check_bf16(ys[l], ref)
+        x = ys[l].cpu()
+
+
+def test_fused_layers_errors():
+    wl = S.random_cloud(911, 800, shape=(12, 12, 12), c_in=64, c_out=64)
+    f = wl.feats.cuda()
+    wp = sc.wpack_create(wl.weights[0].cuda())
+    wp2 = sc.wpack_create(torch.zeros((27, 64, 32), dtype=torch.bfloat16, device="cuda"))
+    m = build(wl)
+    with pytest.raises(sc.SpconvError) as e:                    # c_in != c_out in a stack
+        sc.subm_forward_layers(m, f, [wp2, wp2])
+    assert e.value.code == -1
+    mt = build(wl, gemm="tap_major")
+    with pytest.raises(sc.SpconvError) as e:                    # only the tile-union GEMM stacks
+        sc.subm_forward_layers(mt, f, [wp, wp])
+    assert e.value.code == -2
+    ms = sc.build_map_strided(wl.coords.cuda(), wl.spatial_shape, 1)
+    with pytest.raises(sc.SpconvError) as e:                    # a strided map's rows are not its inputs
+        sc.subm_forward_layers(ms, f, [wp, wp])
+    assert e.value.code in (-1, -2)
+    buf = torch.empty((wl.n, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sc.SpconvError) as e:                    # a layer's output overlaps its input
+        sc.subm_forward_layers(m, f, [wp, wp], outs=[buf, buf])
+    assert e.value.code == -7
+    assert sc.map_status(m) == 0
