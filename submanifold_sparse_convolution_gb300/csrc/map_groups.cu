@@ -30,6 +30,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "map_internal.cuh"
 #include "radix_sort.cuh"
 
 namespace spconv {
@@ -59,6 +60,27 @@ int bit_len(uint64_t v) {
 }
 
 inline unsigned blocks(int64_t n, int per) { return static_cast<unsigned>((n + per - 1) / per); }
+// Launch with programmatic dependent launch: the kernel may be scheduled
+// while the kernel before it finishes (that kernel's CTAs have all started);
+// every kernel launched this way begins with pdl_trigger(); pdl_wait(), so it
+// touches global memory only once the kernels before it have completed.
+template <typename Kernel, typename... Args>
+int launch_chained(Kernel kernel, unsigned grid, unsigned block, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kernel, args...));
+}
+
+// grid of a grid-stride kernel over n entries (kGBlock threads per CTA)
+inline unsigned capped_blocks(int64_t n) {
+    const unsigned b = blocks(n, kGBlock);
+    return b < 2048 ? (b < 1 ? 1 : b) : 2048;
+}
 
 template <typename T>
 T* take(char*& p, size_t count) {
@@ -78,6 +100,8 @@ __device__ __forceinline__ bool in_range(int4 c, int3 shape, int batch) {
 __global__ void __launch_bounds__(kGBlock) kg_pack_keys(const int4* __restrict__ coords, int64_t n, int3 shape,
                                                         int batch, const GLayout L, uint64_t* __restrict__ keys,
                                                         uint32_t* __restrict__ vals, int32_t* __restrict__ status) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
     if (i >= n) return;
     const int4 c = coords[i];
@@ -94,17 +118,45 @@ __global__ void __launch_bounds__(kGBlock) kg_pack_keys(const int4* __restrict__
     vals[i] = static_cast<uint32_t>(i);
 }
 
-// First index in [lo, hi) with keys[idx] >= t (hi if none).
-__device__ __forceinline__ int64_t first_not_less(const uint64_t* __restrict__ keys, int64_t lo, int64_t hi,
-                                                  uint64_t t) {
-    while (lo < hi) {
-        const int64_t mid = (lo + hi) >> 1;
-        if (__ldg(keys + mid) < t)
-            lo = mid + 1;
-        else
-            hi = mid;
+// The same keys packed with the row for the whole-GPU sort: (key << rbits) |
+// row, the key kb = key_bits + 1 bits wide (all ones for an out-of-range
+// row, which orders it last); counts every sort pass's digits.  Grid-stride,
+// so that whole warps take part in the digit counts.
+__global__ void __launch_bounds__(kGBlock) kg_pack_keys_packed(const int4* __restrict__ coords, int64_t n, int3 shape,
+                                                               int batch, const GLayout L, int kb, int rbits,
+                                                               const WideDigits d, uint64_t* __restrict__ packed,
+                                                               int32_t* __restrict__ gh,
+                                                               int32_t* __restrict__ status) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ int32_t h[kWideKeyPassesMax][kWideBins];
+    for (int i = threadIdx.x; i < kWideKeyPassesMax * kWideBins; i += kGBlock) (&h[0][0])[i] = 0;
+    __syncthreads();
+    const uint64_t none = (uint64_t(1) << kb) - 1;
+    int32_t err = 0;
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kGBlock; i0 < n; i0 += static_cast<int64_t>(gridDim.x) * kGBlock) {
+        const int64_t i = i0 + threadIdx.x;
+        const bool valid = i < n;
+        uint64_t v = 0;
+        if (valid) {
+            const int4 c = coords[i];
+            uint64_t key = none;
+            if (in_range(c, shape, batch)) {
+                key = ((((static_cast<uint64_t>(c.x) << L.wx) | static_cast<uint64_t>(c.y + L.r)) << L.wy |
+                        static_cast<uint64_t>(c.z + L.r))
+                       << L.wz) |
+                      static_cast<uint64_t>(c.w + L.r);
+            } else {
+                err |= kStatusRange;
+            }
+            v = (key << rbits) | static_cast<uint64_t>(i);
+            packed[i] = v;
+        }
+        wide_count_digits(v, valid, d, h);
     }
-    return lo;
+    if (err) atomicOr(status, err);
+    __syncthreads();
+    wide_flush_digits(d, h, gh);
 }
 
 // One thread per sorted position s: for each (dx, dy) column, the lower bound
@@ -112,20 +164,30 @@ __device__ __forceinline__ int64_t first_not_less(const uint64_t* __restrict__ k
 // hold smaller keys than the row's own, columns after it larger ones, so each
 // search runs on one side of s.  nbr is cleared to -1 beforehand; only the
 // present neighbours are written.
+// kPacked: skeys holds (key << rbits) | row (the whole-GPU sort's values),
+// no_key the key of an out-of-range row; else keys and rows are separate.
+template <bool kPacked>
 __global__ void __launch_bounds__(kGBlock) kg_search(const uint64_t* __restrict__ skeys,
-                                                     const uint32_t* __restrict__ svals, int64_t n,
-                                                     const GLayout L, int32_t* __restrict__ nbr,
+                                                     const uint32_t* __restrict__ svals, int64_t n, int rbits,
+                                                     uint64_t no_key, const GLayout L, int32_t* __restrict__ nbr,
                                                      int32_t* __restrict__ tap_count,
                                                      int32_t* __restrict__ status) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t cnt[kMaxTaps];
     for (int k = threadIdx.x; k < L.V; k += kGBlock) cnt[k] = 0;
     __syncthreads();
+    const uint64_t rmask = (uint64_t(1) << rbits) - 1;
+    auto key_at = [&](int64_t p) -> uint64_t { return kPacked ? (__ldcg(skeys + p) >> rbits) : __ldcg(skeys + p); };
+    auto row_at = [&](int64_t p) -> int64_t {
+        return kPacked ? static_cast<int64_t>(__ldcg(skeys + p) & rmask) : static_cast<int64_t>(__ldcg(svals + p));
+    };
     const int64_t s = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
     if (s < n) {
-        const uint64_t q = skeys[s];
-        const int64_t row = svals[s];
-        if (q != kNoKey) {
-            if (s > 0 && skeys[s - 1] == q) atomicOr(status, kStatusDuplicate);
+        const uint64_t q = key_at(s);
+        const int64_t row = row_at(s);
+        if (q != no_key) {
+            if (s > 0 && key_at(s - 1) == q) atomicOr(status, kStatusDuplicate);
             const int cols = L.K * L.K, centre = (cols - 1) / 2;
             for (int c = 0; c < cols; ++c) {
                 const uint64_t lo_t = q + L.col_off[c];
@@ -137,14 +199,21 @@ __global__ void __launch_bounds__(kGBlock) kg_search(const uint64_t* __restrict_
                     lo = s > L.r ? s - L.r : 0;
                     hi = s + L.r + 1 < n ? s + L.r + 1 : n;
                 }
-                const int64_t pos = first_not_less(skeys, lo, hi, lo_t);
+                int64_t pos = lo, top = hi;   // first position in [lo, hi) with key >= lo_t
+                while (pos < top) {
+                    const int64_t mid = (pos + top) >> 1;
+                    if (key_at(mid) < lo_t)
+                        pos = mid + 1;
+                    else
+                        top = mid;
+                }
                 for (int j = 0; j < L.K; ++j) {
                     const int64_t p = pos + j;
                     if (p >= n) break;
-                    const uint64_t kk = __ldg(skeys + p);
+                    const uint64_t kk = key_at(p);
                     if (kk > hi_t) break;
                     const int k = c * L.K + static_cast<int>(kk - lo_t);
-                    nbr[row * L.stride + k] = static_cast<int32_t>(__ldg(svals + p));
+                    nbr[row * L.stride + k] = static_cast<int32_t>(row_at(p));
                     atomicAdd(&cnt[k], 1);
                 }
             }
@@ -152,6 +221,91 @@ __global__ void __launch_bounds__(kGBlock) kg_search(const uint64_t* __restrict_
     }
     __syncthreads();
     for (int k = threadIdx.x; k < L.V; k += kGBlock)
+        if (cnt[k]) atomicAdd(&tap_count[k], cnt[k]);
+}
+
+// The same search over the packed values (key << rbits | row) for kernel size
+// K, with the K^2 column searches of a row in lockstep: every step of the
+// binary searches issues the probes of all columns still open at once, and
+// the K keys after every lower bound are read together, so a row waits
+// ~log2(n) memory round trips rather than K^2 log2(n).
+constexpr int kLockRows = 128;   // rows per block; K threads per row, one per dx plane
+
+template <int K>
+__global__ void __launch_bounds__(kLockRows * K) kg_search_lockstep(const uint64_t* __restrict__ sv, int64_t n,
+                                                                    int rbits, uint64_t no_key, const GLayout L,
+                                                                    int32_t* __restrict__ nbr,
+                                                                    int32_t* __restrict__ tap_count,
+                                                                    int32_t* __restrict__ status) {
+    pdl_trigger();
+    pdl_wait();
+    constexpr int R = (K - 1) / 2, V = K * K * K;
+    __shared__ int32_t cnt[V];
+    for (int k = threadIdx.x; k < V; k += kLockRows * K) cnt[k] = 0;
+    __syncthreads();
+    const int plane = threadIdx.x / kLockRows;   // dx = plane - R (warp-uniform)
+    const uint64_t rmask = (uint64_t(1) << rbits) - 1;
+    const int64_t s = static_cast<int64_t>(blockIdx.x) * kLockRows + threadIdx.x % kLockRows;
+    bool ok = s < n;
+    uint64_t q = 0;
+    int64_t row = 0;
+    if (ok) {
+        const uint64_t v = __ldcg(sv + s);
+        q = v >> rbits;
+        row = static_cast<int64_t>(v & rmask);
+        ok = q != no_key;
+        if (ok && plane == R && s > 0 && (__ldcg(sv + s - 1) >> rbits) == q) atomicOr(status, kStatusDuplicate);
+    }
+    if (ok) {
+        // the plane's K columns c = K plane + e; those before the row's own
+        // column hold smaller keys than its own, those after it larger ones
+        int32_t lo[K], hi[K];
+#pragma unroll
+        for (int e = 0; e < K; ++e) {
+            const int rel = (plane - R) * K + (e - R);   // sign of the column's offset from the row's own
+            lo[e] = rel < 0 ? 0 : (rel > 0 ? static_cast<int32_t>(s + 1) : static_cast<int32_t>(s > R ? s - R : 0));
+            hi[e] = rel < 0 ? static_cast<int32_t>(s)
+                            : (rel > 0 ? static_cast<int32_t>(n) : static_cast<int32_t>(s + R + 1 < n ? s + R + 1 : n));
+        }
+        for (int it = 0; it < 40; ++it) {
+            uint64_t kk[K];
+#pragma unroll
+            for (int e = 0; e < K; ++e) kk[e] = lo[e] < hi[e] ? (__ldcg(sv + ((lo[e] + hi[e]) >> 1)) >> rbits) : 0ull;
+            bool open = false;
+#pragma unroll
+            for (int e = 0; e < K; ++e) {
+                if (lo[e] < hi[e]) {
+                    const int32_t mid = (lo[e] + hi[e]) >> 1;
+                    if (kk[e] < q + L.col_off[plane * K + e])
+                        lo[e] = mid + 1;
+                    else
+                        hi[e] = mid;
+                    open |= lo[e] < hi[e];
+                }
+            }
+            if (!open) break;
+        }
+        // at most K keys from each lower bound lie in the column (keys are unique)
+#pragma unroll
+        for (int e = 0; e < K; ++e) {
+            const int c = plane * K + e;
+            const uint64_t lo_t = q + L.col_off[c];
+            uint64_t vv[K];
+#pragma unroll
+            for (int j = 0; j < K; ++j) vv[j] = lo[e] + j < n ? __ldcg(sv + lo[e] + j) : ~0ull;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const uint64_t d = (vv[j] >> rbits) - lo_t;
+                if (vv[j] != ~0ull && d <= static_cast<uint64_t>(2 * R)) {
+                    const int k = c * K + static_cast<int>(d);
+                    nbr[row * L.stride + k] = static_cast<int32_t>(vv[j] & rmask);
+                    atomicAdd(&cnt[k], 1);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < V; k += kLockRows * K)
         if (cnt[k]) atomicAdd(&tap_count[k], cnt[k]);
 }
 
@@ -188,6 +342,8 @@ __device__ __forceinline__ uint64_t g_key(int4 c, const GLayout& L) {
 __global__ void __launch_bounds__(kGBlock) kg_hash_insert(const int4* __restrict__ coords, int64_t n, int3 shape,
                                                           int batch, const GLayout L, uint64_t* __restrict__ table,
                                                           int log2, int row_bits, int32_t* __restrict__ status) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
     if (i >= n) return;
     const int4 c = coords[i];
@@ -215,27 +371,37 @@ __global__ void __launch_bounds__(kGBlock) kg_hash_insert(const int4* __restrict
     atomicOr(status, kStatusInternal);   // a full table: cannot happen at load <= 1/16
 }
 
-// One thread per row, one dx plane at a time: the plane's K columns' bucket
-// reads (r + 1 pairs each) in flight together; the rare reads that meet a
-// full bucket go on, all of the warp's in the same extra round.  nbr is
-// cleared to -1 beforehand; only present neighbours are written.
+// K threads per row, one per dx plane (kLookRows rows per block, each warp
+// in one plane): the plane's K columns' bucket reads (r + 1 pairs each) in
+// flight together; the rare reads that meet a full bucket go on, all of the
+// warp's in the same extra round.  nbr is cleared to -1 beforehand; only
+// present neighbours are written.
 template <int K>
-__global__ void __launch_bounds__(kGBlock) kg_hash_lookup(const int4* __restrict__ coords, int64_t n, int3 shape,
-                                                          int batch, const GLayout L,
-                                                          const uint64_t* __restrict__ table, int log2,
-                                                          int row_bits, int32_t* __restrict__ nbr,
-                                                          int32_t* __restrict__ tap_count) {
+struct LookRows {
+    static constexpr int value = K == 3 ? 128 : 64;   // 5 x 64 threads keep the 15 bucket reads in registers
+};
+
+template <int K>
+__global__ void __launch_bounds__(LookRows<K>::value * K) kg_hash_lookup(const int4* __restrict__ coords, int64_t n,
+                                                                         int3 shape, int batch, const GLayout L,
+                                                                         const uint64_t* __restrict__ table, int log2,
+                                                                         int row_bits, int32_t* __restrict__ nbr,
+                                                                         int32_t* __restrict__ tap_count) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int r = (K - 1) / 2, V = K * K * K, NP = r + 1;   // pairs per column
+    constexpr int kRows = LookRows<K>::value;
     __shared__ int32_t cnt[V];
-    for (int k = threadIdx.x; k < V; k += kGBlock) cnt[k] = 0;
+    for (int k = threadIdx.x; k < V; k += kRows * K) cnt[k] = 0;
     __syncthreads();
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
+    const int p = threadIdx.x / kRows;   // this thread's dx plane
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * kRows + threadIdx.x % kRows;
     const bool ok = i < n && in_range(coords[i], shape, batch);
     const uint64_t key = ok ? g_key(coords[i], L) : 0ull;
     const int lb = log2 - 2;
     const uint64_t bmask = (uint64_t(1) << lb) - 1;
     const uint64_t rmask = (uint64_t(1) << row_bits) - 1;
-    for (int p = 0; p < K; ++p) {   // dx plane
+    {
         ulonglong2 lo[K * NP], hi[K * NP];
         uint64_t first_pair[K];
         uint32_t pending = 0, found = 0;   // found: bit K c + dz of this plane (a bucket may be read twice)
@@ -282,7 +448,7 @@ __global__ void __launch_bounds__(kGBlock) kg_hash_lookup(const int4* __restrict
         }
     }
     __syncthreads();
-    for (int k = threadIdx.x; k < V; k += kGBlock)
+    for (int k = threadIdx.x; k < V; k += kRows * K)
         if (cnt[k]) atomicAdd(&tap_count[k], cnt[k]);
 }
 
@@ -297,6 +463,8 @@ __device__ __forceinline__ int64_t cell_of(int4 c, const GLayout& L) {
 __global__ void __launch_bounds__(kGBlock) kg_grid_scatter(const int4* __restrict__ coords, int64_t n, int3 shape,
                                                            int batch, const GLayout L, int32_t* __restrict__ grid,
                                                            int32_t* __restrict__ status) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
     if (i >= n) return;
     const int4 c = coords[i];
@@ -312,6 +480,8 @@ __global__ void __launch_bounds__(kGBlock) kg_grid_lookup(const int4* __restrict
                                                           const int32_t* __restrict__ grid,
                                                           int32_t* __restrict__ nbr,
                                                           int32_t* __restrict__ tap_count) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t cnt[kMaxTaps];
     for (int k = threadIdx.x; k < L.V; k += kGBlock) cnt[k] = 0;
     __syncthreads();
@@ -321,7 +491,7 @@ __global__ void __launch_bounds__(kGBlock) kg_grid_lookup(const int4* __restrict
         if (in_range(c, shape, batch)) {
             const int64_t cell = cell_of(c, L);
             for (int k = 0; k < L.V; ++k) {
-                const int32_t v = __ldg(grid + cell + L.goff[k]);
+                const int32_t v = __ldcg(grid + cell + L.goff[k]);
                 if (v >= 0) {
                     nbr[i * L.stride + k] = v;
                     atomicAdd(&cnt[k], 1);
@@ -342,6 +512,8 @@ __global__ void __launch_bounds__(kGBlock) kg_grid_lookup(const int4* __restrict
 // bit 0, so the rarest is the most significant ("Calibrated bit order").
 __global__ void kg_tap_order(const int32_t* __restrict__ tap_count, int V, int kg, int calibrated,
                              int32_t* __restrict__ tap_pos) {
+    pdl_trigger();
+    pdl_wait();
     for (int k = threadIdx.x; k < V; k += blockDim.x) {
         const int g0 = k / kg * kg;
         if (!calibrated) {
@@ -365,6 +537,8 @@ __global__ void __launch_bounds__(kGBlock) kg_mask_keys(const int32_t* __restric
                                                         int G, int kg, const int32_t* __restrict__ tap_pos,
                                                         uint32_t* __restrict__ mask, uint32_t* __restrict__ keys,
                                                         uint32_t* __restrict__ vals) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t pos[kMaxTaps];
     for (int k = threadIdx.x; k < G * kg; k += kGBlock) pos[k] = tap_pos[k];
     __syncthreads();
@@ -385,19 +559,151 @@ __global__ void __launch_bounds__(kGBlock) kg_mask_keys(const int32_t* __restric
     vals[idx] = static_cast<uint32_t>(i);
 }
 
+// The same keys packed with the row for the whole-GPU sort: entry g n + i is
+// (((g << kg) | key) << rbits) | i; counts every sort pass's digits.
+__global__ void __launch_bounds__(kGBlock) kg_mask_keys_packed(const int32_t* __restrict__ nbr, int64_t n, int stride,
+                                                               int G, int kg, int rbits,
+                                                               const int32_t* __restrict__ tap_pos,
+                                                               const WideDigits d, uint32_t* __restrict__ mask,
+                                                               uint64_t* __restrict__ packed,
+                                                               int32_t* __restrict__ gh) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ int32_t pos[kMaxTaps];
+    __shared__ int32_t h[kWideKeyPassesMax][kWideBins];
+    for (int k = threadIdx.x; k < G * kg; k += kGBlock) pos[k] = tap_pos[k];
+    for (int i = threadIdx.x; i < kWideKeyPassesMax * kWideBins; i += kGBlock) (&h[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t total = G * n;
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kGBlock; i0 < total;
+         i0 += static_cast<int64_t>(gridDim.x) * kGBlock) {
+        const int64_t idx = i0 + threadIdx.x;
+        const bool valid = idx < total;
+        uint64_t v = 0;
+        if (valid) {
+            const int g = static_cast<int>(idx / n);
+            const int64_t i = idx - g * n;
+            const int32_t* row = nbr + i * stride + g * kg;
+            uint32_t m = 0, key = 0;
+            for (int j = 0; j < kg; ++j) {
+                if (row[j] >= 0) {
+                    m |= 1u << j;
+                    key |= 1u << pos[g * kg + j];
+                }
+            }
+            mask[idx] = m;
+            v = (((static_cast<uint64_t>(g) << kg) | key) << rbits) | static_cast<uint64_t>(i);
+            packed[idx] = v;
+        }
+        wide_count_digits(v, valid, d, h);
+    }
+    __syncthreads();
+    wide_flush_digits(d, h, gh);
+}
+
+// The same, four lanes per row for kernel size K: the lanes read the row's
+// nbr entries with 16-byte loads (lane q the words q, q + 4, ...), combine
+// their presence bits (bit k: tap k) by shuffles, and lane q then writes the
+// mask and key of groups q, q + 4, ...; entry g n + i gets group g's.
+template <int K>
+__global__ void __launch_bounds__(kGBlock) kg_mask_keys_rows(const int32_t* __restrict__ nbr, int64_t n, int G,
+                                                             int kg, int rbits, const int32_t* __restrict__ tap_pos,
+                                                             const WideDigits d, uint32_t* __restrict__ mask,
+                                                             uint64_t* __restrict__ packed,
+                                                             int32_t* __restrict__ gh) {
+    pdl_trigger();
+    pdl_wait();
+    constexpr int V = K * K * K, NQ = (V + 3) / 4, NW = (V + 31) / 32;   // taps, 16-byte words of a row, bitmap words
+    __shared__ int32_t pos[V];
+    __shared__ int32_t h[kWideKeyPassesMax][kWideBins];
+    for (int k = threadIdx.x; k < V; k += kGBlock) pos[k] = tap_pos[k];
+    for (int i = threadIdx.x; i < kWideKeyPassesMax * kWideBins; i += kGBlock) (&h[0][0])[i] = 0;
+    __syncthreads();
+    const int q = threadIdx.x & 3;
+    for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kGBlock; t0 < 4 * n; t0 += static_cast<int64_t>(gridDim.x) * kGBlock) {
+        const int64_t i = (t0 + threadIdx.x) >> 2;
+        const bool valid = i < n;
+        uint32_t pres[NW];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) pres[w] = 0;
+        if (valid) {
+            const int4* row = reinterpret_cast<const int4*>(nbr + i * (4 * NQ));
+#pragma unroll
+            for (int u = 0; u < (NQ + 3) / 4; ++u) {
+                const int qd = q + 4 * u;
+                if (qd < NQ) {
+                    const int4 v = __ldcg(row + qd);
+                    const int32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        // tap 4 qd + b: word (4 qd + b) / 32, the same for the four b
+                        const uint32_t bit = (4 * qd + b < V && e[b] >= 0) ? 1u << ((4 * qd + b) & 31) : 0u;
+#pragma unroll
+                        for (int w = 0; w < NW; ++w) pres[w] |= ((4 * qd) >> 5) == w ? bit : 0u;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            pres[w] |= __shfl_xor_sync(0xFFFFFFFFu, pres[w], 1);
+            pres[w] |= __shfl_xor_sync(0xFFFFFFFFu, pres[w], 2);
+        }
+        // the presence bits as two 64-bit words (V <= 128)
+        uint64_t p0 = pres[0], p1 = 0;
+        if (NW > 1) p0 |= static_cast<uint64_t>(pres[NW > 1 ? 1 : 0]) << 32;
+        if (NW > 2) p1 = pres[NW > 2 ? 2 : 0];
+        if (NW > 3) p1 |= static_cast<uint64_t>(pres[NW > 3 ? 3 : 0]) << 32;
+        for (int gi = 0; gi < (G + 3) / 4; ++gi) {
+            const int g = q + 4 * gi;
+            const bool on = valid && g < G;
+            uint64_t v = 0;
+            if (on) {
+                const int a = g * kg;   // group g's taps are bits [a, a + kg)
+                const uint64_t w = a < 64 ? ((p0 >> a) | (a > 0 ? p1 << (64 - a) : 0ull)) : (p1 >> (a - 64));
+                const uint32_t m = static_cast<uint32_t>(w) & ((1u << kg) - 1u);
+                uint32_t key = 0;
+                for (uint32_t b = m; b; b &= b - 1) key |= 1u << pos[a + __ffs(b) - 1];
+                v = (((static_cast<uint64_t>(g) << kg) | key) << rbits) | static_cast<uint64_t>(i);
+                mask[g * n + i] = m;
+                packed[g * n + i] = v;
+            }
+            wide_count_digits(v, on, d, h);
+        }
+    }
+    __syncthreads();
+    wide_flush_digits(d, h, gh);
+}
+
 // ---------------------------------------------------------------------------
 // compaction: per-(tap, tile) counts -> scan -> pair lists, gather table
 // ---------------------------------------------------------------------------
 // Block (g, t): tile t of group g's order.  counts[k][t] for the group's taps
 // k; the tile's union (bit j: tap g kg + j) in tile_union[g][t].
-__global__ void __launch_bounds__(kTileRows) kg_tile_count(const int32_t* __restrict__ perm,
+// kPacked: the row order comes as the sorted packed values (row in the low
+// rbits bits) and is written out to perm here.
+template <bool kPacked>
+__global__ void __launch_bounds__(kTileRows) kg_tile_count(int32_t* __restrict__ perm,
+                                                           const uint64_t* __restrict__ sorted, int rbits,
                                                            const uint32_t* __restrict__ mask, int64_t n,
                                                            int64_t n_tiles, int kg, int32_t* __restrict__ counts,
                                                            uint32_t* __restrict__ tile_union) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t wc[kTileRows / 32][kMaxGroupTaps];
     const int64_t g = blockIdx.x / n_tiles, t = blockIdx.x % n_tiles;
     const int64_t s = t * kTileRows + threadIdx.x;
-    const uint32_t m = s < n ? mask[g * n + perm[g * n + s]] : 0u;
+    uint32_t m = 0;
+    if (s < n) {
+        int32_t r;
+        if (kPacked) {
+            r = static_cast<int32_t>(sorted[g * n + s] & ((uint64_t(1) << rbits) - 1));
+            perm[g * n + s] = r;
+        } else {
+            r = perm[g * n + s];
+        }
+        m = mask[g * n + r];
+    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int j = 0; j < kg; ++j) {
         const uint32_t b = __ballot_sync(0xFFFFFFFFu, (m >> j) & 1u);
@@ -425,6 +731,8 @@ __global__ void __launch_bounds__(1024) kg_scan_tiles(const int32_t* __restrict_
                                                       int32_t* __restrict__ totals,
                                                       int32_t* __restrict__ tile_order,
                                                       int32_t* __restrict__ nonempty) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t hist[kMaxGroups][kMaxGroupTaps + 1];
     for (int i = threadIdx.x; i < kMaxGroups * (kMaxGroupTaps + 1); i += 1024) (&hist[0][0])[i] = 0;
     const int64_t m = V * n_tiles;
@@ -503,6 +811,8 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write(const int32_t* __rest
                                                            int32_t* __restrict__ in_rows,
                                                            int32_t* __restrict__ out_rows,
                                                            int32_t* __restrict__ gtab) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int32_t wc[kTileRows / 32][kMaxGroupTaps];
     __shared__ int32_t seg[kMaxGroupTaps];
     const int64_t g = blockIdx.x / n_tiles, t = blockIdx.x % n_tiles;
@@ -512,6 +822,129 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write(const int32_t* __rest
     const uint32_t m = valid ? mask[g * n + r] : 0u;
     if (threadIdx.x < kg) seg[threadIdx.x] = seg_off[(g * kg + threadIdx.x) * n_tiles + t];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int j = 0; j < kg; ++j) {
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, (m >> j) & 1u);
+        if (lane == 0) wc[warp][j] = __popc(b);
+    }
+    __syncthreads();
+    const uint32_t lt = rsort::lanemask_lt();
+    for (int j = 0; j < kg; ++j) {
+        const int64_t k = g * kg + j;
+        const bool present = (m >> j) & 1u;
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, present);
+        int32_t v = -1;
+        if (present) {
+            v = nbr[static_cast<int64_t>(r) * stride + k];
+            int32_t off = seg[j] + __popc(b & lt);
+            for (int w = 0; w < warp; ++w) off += wc[w][j];
+            in_rows[off] = v;
+            out_rows[off] = r;
+        }
+        gtab[k * n_pad + s] = v;
+    }
+}
+
+// kg_scan_tiles and kg_tile_write in one, for groups of up to
+// kPrefixTilesG tiles: block (g, t) finds its own offsets.  Tap k's list
+// starts after the pairs of every earlier tap (their totals are the tap
+// counts of the lookup), and tile t's part of it after those of tiles
+// 0 .. t - 1 (summed here from the raw counts); the tile's place in its
+// group's order is the number of the group's tiles with a larger union plus
+// those before it with an equal one.  Block (g, 0) writes the group's count
+// of tiles with a nonempty union, block (0, 0) the tap offsets and totals.
+constexpr int64_t kPrefixTilesG = 512;
+
+__global__ void __launch_bounds__(kTileRows) kg_tile_write_prefix(
+    const int32_t* __restrict__ perm, const uint32_t* __restrict__ mask, const int32_t* __restrict__ nbr, int stride,
+    int64_t n, int64_t n_tiles, int64_t n_pad, int G, int kg, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ tap_count, const uint32_t* __restrict__ tile_union, int32_t* __restrict__ tap_off,
+    int32_t* __restrict__ totals, int32_t* __restrict__ tile_order, int32_t* __restrict__ nonempty,
+    int32_t* __restrict__ in_rows, int32_t* __restrict__ out_rows, int32_t* __restrict__ gtab) {
+    pdl_trigger();
+    pdl_wait();
+    constexpr int W = kTileRows / 32;
+    __shared__ int32_t wc[W][kMaxGroupTaps];
+    __shared__ int32_t seg[kMaxGroupTaps];
+    __shared__ int32_t tstart[kMaxTaps + 1];
+    __shared__ int32_t wsum[W];
+    __shared__ int32_t red[4][W];
+    const int64_t g = blockIdx.x / n_tiles, t = blockIdx.x % n_tiles;
+    const int V = G * kg;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // ---- tap starts: exclusive prefix of the tap counts (V <= kTileRows)
+    const int32_t tc = threadIdx.x < V ? tap_count[threadIdx.x] : 0;
+    int32_t inc = tc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    int32_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+        before += w < warp ? wsum[w] : 0;
+        total += wsum[w];
+    }
+    if (threadIdx.x <= V) tstart[threadIdx.x] = threadIdx.x < V ? before + inc - tc : total;
+    // ---- the counts of the group's taps in the tiles before t: warp w sums taps w, w + W, ...
+    for (int j = warp; j < kg; j += W) {
+        const int32_t* row = counts + (g * kg + j) * n_tiles;
+        int32_t acc = 0;
+        for (int64_t tt = lane; tt < t; tt += 32) acc += row[tt];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        if (lane == 0) wc[0][j] = acc;   // (wc is reused below)
+    }
+    // ---- place in the group's tile order; nonempty tiles; (block 0, 0) the sum of all union sizes
+    const int c = __popc(tile_union[g * n_tiles + t]);
+    int32_t greater = 0, equal_before = 0, nonzero = 0, taps_all = 0;
+    for (int64_t tt = threadIdx.x; tt < n_tiles; tt += kTileRows) {
+        const int cu = __popc(tile_union[g * n_tiles + tt]);
+        greater += cu > c ? 1 : 0;
+        equal_before += (cu == c && tt < t) ? 1 : 0;
+        nonzero += cu > 0 ? 1 : 0;
+    }
+    if (g == 0 && t == 0)
+        for (int64_t tt = threadIdx.x; tt < G * n_tiles; tt += kTileRows) taps_all += __popc(tile_union[tt]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        greater += __shfl_xor_sync(0xFFFFFFFFu, greater, o);
+        equal_before += __shfl_xor_sync(0xFFFFFFFFu, equal_before, o);
+        nonzero += __shfl_xor_sync(0xFFFFFFFFu, nonzero, o);
+        taps_all += __shfl_xor_sync(0xFFFFFFFFu, taps_all, o);
+    }
+    if (lane == 0) {
+        red[0][warp] = greater;
+        red[1][warp] = equal_before;
+        red[2][warp] = nonzero;
+        red[3][warp] = taps_all;
+    }
+    __syncthreads();
+    if (threadIdx.x < kg) seg[threadIdx.x] = tstart[g * kg + threadIdx.x] + wc[0][threadIdx.x];
+    if (threadIdx.x == 0) {
+        int32_t gs = 0, es = 0, nz = 0, ta = 0;
+        for (int w = 0; w < W; ++w) {
+            gs += red[0][w];
+            es += red[1][w];
+            nz += red[2][w];
+            ta += red[3][w];
+        }
+        tile_order[g * n_tiles + gs + es] = static_cast<int32_t>(t);
+        if (t == 0) nonempty[g] = nz;
+        if (g == 0 && t == 0) {
+            totals[0] = tstart[V];
+            totals[1] = ta;
+        }
+    }
+    if (g == 0 && t == 0 && threadIdx.x <= V) tap_off[threadIdx.x] = tstart[threadIdx.x];
+    __syncthreads();   // seg is complete; wc is rewritten below
+    // ---- the pairs and the gather table, as kg_tile_write
+    const int64_t s = t * kTileRows + threadIdx.x;
+    const bool valid = s < n;
+    const int32_t r = valid ? perm[g * n + s] : -1;
+    const uint32_t m = valid ? mask[g * n + r] : 0u;
     for (int j = 0; j < kg; ++j) {
         const uint32_t b = __ballot_sync(0xFFFFFFFFu, (m >> j) & 1u);
         if (lane == 0) wc[warp][j] = __popc(b);
@@ -578,13 +1011,137 @@ __global__ void __launch_bounds__(kGBlock) kst_candidates(const int4* __restrict
     }
 }
 
-// flags[j] = 1 for the first of each run of equal sorted keys (not ~0).
-__global__ void __launch_bounds__(kGBlock) kst_first(const uint64_t* __restrict__ keys, int64_t m,
+// The distinct candidates without sorting them all: each input site's up to
+// 8 output keys go into a hash set (slot = key + 1, 0 empty, linear probing
+// from a multiplicative hash); the thread whose insertion creates an entry
+// appends the key to uniq[] (the count in *n_uniq) and counts its digits for
+// the sort of the distinct keys.  The set has at least twice as many slots
+// as there can be candidates, so a probe always ends.
+__device__ __forceinline__ uint64_t set_slot(uint64_t key, int log2) {
+    return (key * 0x9E3779B97F4A7C15ull) >> (64 - log2);
+}
+
+__global__ void __launch_bounds__(kGBlock) kst_dedupe(const int4* __restrict__ coords, int64_t n, int3 shape,
+                                                      int batch, const OutLayout O, uint64_t* __restrict__ set,
+                                                      int set_log2, const WideDigits d, uint64_t* __restrict__ uniq,
+                                                      int64_t* __restrict__ n_uniq, int32_t* __restrict__ gh) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ int32_t h[kWideKeyPassesMax][kWideBins];
+    __shared__ uint64_t staged[8 * kGBlock];   // the block's new keys of one round
+    __shared__ int32_t n_staged;
+    __shared__ unsigned long long base_sh;
+    for (int i = threadIdx.x; i < kWideKeyPassesMax * kWideBins; i += kGBlock) (&h[0][0])[i] = 0;
+    if (threadIdx.x == 0) n_staged = 0;
+    __syncthreads();
+    const uint64_t smask = (uint64_t(1) << set_log2) - 1;
+    const int lane = threadIdx.x & 31;
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kGBlock; i0 < n; i0 += static_cast<int64_t>(gridDim.x) * kGBlock) {
+        const int64_t i = i0 + threadIdx.x;
+        int4 c = make_int4(-1, -1, -1, -1);
+        bool ok = false;
+        if (i < n) {
+            c = coords[i];
+            ok = in_range(c, shape, batch);
+        }
+        // the candidate of parity choice j (bit a: the second choice on axis a), if any:
+        // an even coordinate has o = c / 2 only, an odd one (c - 1) / 2 and (c + 1) / 2
+        uint64_t key[8];
+        uint32_t valid = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            bool v = ok;
+            int o[3];
+            const int cc[3] = {c.y, c.z, c.w};
+            const int lim[3] = {O.shape.x, O.shape.y, O.shape.z};
+#pragma unroll
+            for (int a = 0; a < 3; ++a) {
+                const int second = (j >> a) & 1;
+                const bool odd = cc[a] & 1;
+                if (!odd && second) v = false;
+                o[a] = odd ? (second ? (cc[a] + 1) >> 1 : (cc[a] - 1) >> 1) : cc[a] >> 1;
+                if (o[a] < 0 || o[a] >= lim[a]) v = false;
+            }
+            key[j] = v ? out_key(c.x, o[0], o[1], o[2], O) : 0ull;
+            valid |= (v ? 1u : 0u) << j;
+        }
+        // the first slot of every candidate, read together; most end there
+        uint64_t seen[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) seen[j] = ((valid >> j) & 1u) ? __ldcg(set + set_slot(key[j], set_log2)) : 0ull;
+        uint32_t fresh = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (!((valid >> j) & 1u) || seen[j] == key[j] + 1) continue;
+            uint64_t slot = set_slot(key[j], set_log2);
+            uint64_t cur = seen[j];
+            for (uint64_t probe = 0; probe <= smask; ++probe, slot = (slot + 1) & smask) {
+                if (probe > 0) cur = __ldcg(set + slot);
+                if (cur == key[j] + 1) break;
+                if (cur != 0ull) continue;
+                const unsigned long long prev = atomicCAS(reinterpret_cast<unsigned long long*>(set + slot), 0ull,
+                                                          static_cast<unsigned long long>(key[j] + 1));
+                if (prev == 0ull) {
+                    fresh |= 1u << j;
+                    break;
+                }
+                if (prev == key[j] + 1) break;
+            }
+        }
+        // the block's new keys are staged in shared memory (a shared counter
+        // per warp and candidate), then take consecutive slots of uniq with one
+        // global counter update per block and round
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const bool f = (fresh >> j) & 1u;
+            const uint32_t b = __ballot_sync(0xFFFFFFFFu, f);
+            int at = 0;
+            if (b && lane == __ffs(b) - 1) at = atomicAdd(&n_staged, __popc(b));
+            at = __shfl_sync(0xFFFFFFFFu, at, b ? __ffs(b) - 1 : 0);
+            if (f) staged[at + __popc(b & ((1u << lane) - 1u))] = key[j];
+            wide_count_digits(key[j], f, d, h);
+        }
+        __syncthreads();               // the round's keys are staged
+        const int cnt = n_staged;
+        __syncthreads();               // every thread has read the count
+        if (threadIdx.x == 0) {
+            if (cnt > 0)
+                base_sh = atomicAdd(reinterpret_cast<unsigned long long*>(n_uniq), static_cast<unsigned long long>(cnt));
+            n_staged = 0;
+        }
+        __syncthreads();               // base_sh is set, the counter reset
+        for (int e = threadIdx.x; e < cnt; e += kGBlock) uniq[base_sh + e] = staged[e];
+        __syncthreads();               // staged is free for the next round
+    }
+    __syncthreads();
+    wide_flush_digits(d, h, gh);
+}
+
+// Output row j is the j-th distinct candidate in ascending key order: its
+// coordinates and its query site 2o in input coordinates.
+__global__ void __launch_bounds__(kGBlock) kst_outputs_sorted(const uint64_t* __restrict__ keys, int64_t m,
+                                                              const OutLayout O, int4* __restrict__ out_coords,
+                                                              int4* __restrict__ query) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
+    if (j >= m) return;
+    const uint64_t k = keys[j];
+    const int z = static_cast<int>(k & ((uint64_t(1) << O.wz) - 1));
+    const int y = static_cast<int>((k >> O.wz) & ((uint64_t(1) << O.wy) - 1));
+    const int x = static_cast<int>((k >> (O.wz + O.wy)) & ((uint64_t(1) << O.wx) - 1));
+    const int b = static_cast<int>(k >> (O.wz + O.wy + O.wx));
+    out_coords[j] = make_int4(b, x, y, z);
+    query[j] = make_int4(b, 2 * x, 2 * y, 2 * z);
+}
+
+// flags[j] = 1 for the first of each run of equal sorted keys (not no_key).
+__global__ void __launch_bounds__(kGBlock) kst_first(const uint64_t* __restrict__ keys, int64_t m, uint64_t no_key,
                                                      int32_t* __restrict__ flags) {
     const int64_t j = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
     if (j >= m) return;
     const uint64_t k = keys[j];
-    flags[j] = (k != kNoKey && (j == 0 || keys[j - 1] != k)) ? 1 : 0;
+    flags[j] = (k != no_key && (j == 0 || keys[j - 1] != k)) ? 1 : 0;
 }
 
 // Exclusive scan of the first-of-run flags over the whole grid, in three
@@ -668,10 +1225,16 @@ __global__ void __launch_bounds__(kGBlock) kst_outputs(const uint64_t* __restric
     }
 }
 
+__global__ void k_or_status(int32_t* __restrict__ status, const int32_t* __restrict__ extra) {
+    if (threadIdx.x == 0 && *extra) atomicOr(status, *extra);
+}
+
 // Inverse map: for every (o, k) of the strided map with input row i,
 // inv[i][k] = o (one writer per entry: o is fixed by i and k).
 __global__ void __launch_bounds__(kGBlock) kg_inverse_scatter(const int32_t* __restrict__ nbr, int stride, int64_t n,
                                                               int32_t* __restrict__ inv, int inv_stride) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
     if (idx >= n * kTaps) return;
     const int64_t o = idx / kTaps;
@@ -742,8 +1305,9 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
     const int row_bits = std::max(1, bit_len(static_cast<uint64_t>(n_table > 0 ? n_table - 1 : 0)));
     // AUTO: the dense grid on small boxes; else, for K = 3, hashed keys when they
     // pack with the row (outdoor in 3 groups: map 197 -> 130 us), and sorted keys
-    // for K = 5, where the per-row hash lookup of 125 taps measured slower (outdoor
-    // 339 vs 354 us, 240k rows 1364 vs 1747 us)
+    // for K = 5, where the hash lookup of 125 taps (75 bucket reads per row, one
+    // thread per dx plane) measured no faster on outdoor (map 164 vs 164 us) and
+    // slower on 240k rows (631 vs 554 us)
     if (query) {   // strided: the input sites go in a hash table
         if (mapper != SPCONV_MAPPER_AUTO && mapper != SPCONV_MAPPER_HASH) return SPCONV_ERR_UNSUPPORTED;
         mapper = SPCONV_MAPPER_HASH;
@@ -778,12 +1342,37 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
     add(G * t1, 4); add(G * t1, 4);                   // unions, tile orders
     add(V * t1, 4); add(V * t1, 4);                   // counts, seg_off
     add(G, 4);                                        // nonempty tiles per group
-    add(gn, 4); add(gn, 4); add(gn, 4); add(gn, 4);   // mask keys and row ids, ping-pong
+    // The sorts run on the whole-GPU pass (one launch per digit of up to 10
+    // bits) where the key packs with the row into 64 bits; else on the
+    // 8-bit, three-launch passes of rsort.  Mask keys: (g << kg | key) with
+    // the row below; coordinate keys (sorted mapper): key_bits + 1 bits.
+    const int mrb = std::max(1, bit_len(static_cast<uint64_t>(n > 0 ? n - 1 : 0)));
+    const int mbits = kg + bit_len(static_cast<uint64_t>(G) - 1);
+    const WideDigits mdig = wide_digits(mrb, mbits);
+    const bool wide_mask = mdig.passes > 0 && mbits + mrb <= 64 && G * n <= kWideMaxRows;
+    const int ckb = key_bits + 1;
+    const WideDigits cdig = wide_digits(mrb, ckb);
+    const bool wide_coord = !src && mapper == SPCONV_MAPPER_SORTED && cdig.passes > 0 && ckb + mrb <= 64 &&
+                            n <= kWideMaxRows;
+    const int64_t look_words = std::max<int64_t>(1, std::max(wide_mask ? wide_sort_look_words(G * n) : 0,
+                                                             wide_coord ? wide_sort_look_words(n) : 0));
+    const size_t wide_bytes = (wide_mask || wide_coord)
+                                  ? (kWideTickets * kWideBins + kWideCounters) * sizeof(int32_t) +
+                                        static_cast<size_t>(look_words) * 8
+                                  : 0;
+    if (wide_mask) {
+        add(gn, 8); add(gn, 8); add(gn, 4);           // packed mask keys ping-pong, row orders
+    } else {
+        add(gn, 4); add(gn, 4); add(gn, 4); add(gn, 4);   // mask keys and row ids, ping-pong
+    }
     add(rsort::kBins * nb, 4);                        // radix histograms
+    add(wide_bytes, 1);                               // whole-GPU sort: digit totals, tickets, look-back states
     int table_log2 = 11;
     while ((int64_t(1) << table_log2) < kGHashSlotsPerRow * nt1) ++table_log2;
     if (src) {
         // the neighbours come from the strided map
+    } else if (wide_coord) {
+        add(n1, 8); add(n1, 8);                       // packed coordinate keys, ping-pong
     } else if (mapper == SPCONV_MAPPER_SORTED) {
         add(n1, 8); add(n1, 8); add(n1, 4); add(n1, 4);   // coordinate keys and rows, ping-pong
     } else if (mapper == SPCONV_MAPPER_HASH) {
@@ -814,16 +1403,30 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
     int32_t* counts = take<int32_t>(p, V * t1);
     h->seg_off = take<int32_t>(p, V * t1);
     h->tile_nonempty = take<int32_t>(p, G);
-    uint32_t* mkey_a = take<uint32_t>(p, gn);
-    uint32_t* mkey_b = take<uint32_t>(p, gn);
-    uint32_t* perm_a = take<uint32_t>(p, gn);
-    uint32_t* perm_b = take<uint32_t>(p, gn);
+    uint32_t *mkey_a = nullptr, *mkey_b = nullptr, *perm_a = nullptr, *perm_b = nullptr;
+    uint64_t *mpk_a = nullptr, *mpk_b = nullptr;
+    int32_t* perm_w = nullptr;
+    if (wide_mask) {
+        mpk_a = take<uint64_t>(p, gn);
+        mpk_b = take<uint64_t>(p, gn);
+        perm_w = take<int32_t>(p, gn);
+    } else {
+        mkey_a = take<uint32_t>(p, gn);
+        mkey_b = take<uint32_t>(p, gn);
+        perm_a = take<uint32_t>(p, gn);
+        perm_b = take<uint32_t>(p, gn);
+    }
     int32_t* hist = take<int32_t>(p, rsort::kBins * nb);
+    char* wide = take<char>(p, wide_bytes);
+    int32_t* wgh = reinterpret_cast<int32_t*>(wide);                 // [kWideTickets][kWideBins]
+    int32_t* wtickets = wgh + kWideTickets * kWideBins;             // [kWideCounters]
+    uint64_t* wlook = reinterpret_cast<uint64_t*>(wtickets + kWideCounters);
 
     SPCONV_CHECK_CUDA(cudaMemsetAsync(h->status, 0, 4 * sizeof(int32_t), s));
     SPCONV_CHECK_CUDA(cudaMemsetAsync(h->tap_count, 0, V * sizeof(int32_t), s));
     SPCONV_CHECK_CUDA(cudaMemsetAsync(h->totals, 0, 2 * sizeof(int32_t), s));
-    h->perm = reinterpret_cast<int32_t*>(perm_a);
+    h->perm = wide_mask ? perm_w : reinterpret_cast<int32_t*>(perm_a);
+    if (wide_bytes) SPCONV_CHECK_CUDA(cudaMemsetAsync(wide, 0, wide_bytes, s));
     if (n == 0) {
         SPCONV_CHECK_CUDA(cudaMemsetAsync(h->tap_off, 0, (V + 1) * sizeof(int32_t), s));
         return cuda_status(cudaGetLastError());
@@ -841,6 +1444,29 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
                                           cudaMemcpyDeviceToDevice, s));
         SPCONV_CHECK_CUDA(cudaMemcpyAsync(h->status, src->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
         ++launches;
+    } else if (wide_coord) {
+        // packed (key << row bits | row), key_bits + 1 bits of key: an out-of-range
+        // row's all-ones key orders it last; the whole-GPU sort, then the search
+        uint64_t* ck_a = take<uint64_t>(p, n1);
+        uint64_t* ck_b = take<uint64_t>(p, n1);
+        kg_pack_keys_packed<<<capped_blocks(n), kGBlock, 0, s>>>(c4, n, shape3, B, L, ckb, mrb, cdig, ck_a, wgh,
+                                                                 h->status);
+        ++launches;
+        bool in_b = false;
+        SPCONV_CHECK(wide_sort(ck_a, ck_b, n, cdig, wgh, wtickets, 0, wlook, h->status, s, &in_b));
+        launches += cdig.passes;
+        const uint64_t* sv = in_b ? ck_b : ck_a;
+        const uint64_t no_key = (uint64_t(1) << ckb) - 1;
+        if (K == 3)
+            SPCONV_CHECK(launch_chained(kg_search_lockstep<3>, blocks(n, kLockRows), kLockRows * 3, s, sv, n, mrb, no_key, L, h->nbr,
+                                                                              h->tap_count, h->status));
+        else if (K == 5)
+            SPCONV_CHECK(launch_chained(kg_search_lockstep<5>, blocks(n, kLockRows), kLockRows * 5, s, sv, n, mrb, no_key, L, h->nbr,
+                                                                              h->tap_count, h->status));
+        else
+            SPCONV_CHECK(launch_chained(kg_search<true>, blocks(n, kGBlock), kGBlock, s, sv, nullptr, n, mrb, no_key, L, h->nbr,
+                                                                   h->tap_count, h->status));
+        ++launches;
     } else if (mapper == SPCONV_MAPPER_SORTED) {
         uint64_t* ck_a = take<uint64_t>(p, n1);
         uint64_t* ck_b = take<uint64_t>(p, n1);
@@ -851,8 +1477,8 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
         // out-of-range rows carry the all-ones key: one bit above the live ones orders them last
         const bool in_b = rsort::sort_pairs<uint64_t>(ck_a, cv_a, ck_b, cv_b, n, std::min(64, key_bits + 1), hist, s,
                                                       &launches);
-        kg_search<<<blocks(n, kGBlock), kGBlock, 0, s>>>(in_b ? ck_b : ck_a, in_b ? cv_b : cv_a, n, L, h->nbr,
-                                                         h->tap_count, h->status);
+        SPCONV_CHECK(launch_chained(kg_search<false>, blocks(n, kGBlock), kGBlock, s, in_b ? ck_b : ck_a, in_b ? cv_b : cv_a, n, 0, kNoKey,
+                                                                L, h->nbr, h->tap_count, h->status));
         ++launches;
     } else if (mapper == SPCONV_MAPPER_HASH) {
         uint64_t* table = take<uint64_t>(p, size_t(1) << table_log2);
@@ -861,32 +1487,66 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
                                                                     row_bits, h->status);
         const int4* q4 = query ? reinterpret_cast<const int4*>(query) : c4;
         if (K == 3)
-            kg_hash_lookup<3><<<blocks(n, kGBlock), kGBlock, 0, s>>>(q4, n, shape3, B, L, table, table_log2, row_bits,
-                                                                     h->nbr, h->tap_count);
+            SPCONV_CHECK(launch_chained(kg_hash_lookup<3>, blocks(n, LookRows<3>::value), 3 * LookRows<3>::value, s, 
+                q4, n, shape3, B, L, table, table_log2, row_bits, h->nbr, h->tap_count));
         else
-            kg_hash_lookup<5><<<blocks(n, kGBlock), kGBlock, 0, s>>>(q4, n, shape3, B, L, table, table_log2, row_bits,
-                                                                     h->nbr, h->tap_count);
+            SPCONV_CHECK(launch_chained(kg_hash_lookup<5>, blocks(n, LookRows<5>::value), 5 * LookRows<5>::value, s, 
+                q4, n, shape3, B, L, table, table_log2, row_bits, h->nbr, h->tap_count));
         launches += 2;
     } else {
         int32_t* grid = take<int32_t>(p, static_cast<size_t>(cells));
         SPCONV_CHECK_CUDA(cudaMemsetAsync(grid, 0xFF, static_cast<size_t>(cells) * 4, s));
         kg_grid_scatter<<<blocks(n, kGBlock), kGBlock, 0, s>>>(c4, n, shape3, B, L, grid, h->status);
-        kg_grid_lookup<<<blocks(n, kGBlock), kGBlock, 0, s>>>(c4, n, shape3, B, L, grid, h->nbr, h->tap_count);
+        SPCONV_CHECK(launch_chained(kg_grid_lookup, blocks(n, kGBlock), kGBlock, s, c4, n, shape3, B, L, grid, h->nbr, h->tap_count));
         launches += 2;
     }
-    kg_tap_order<<<1, 128, 0, s>>>(h->tap_count, V, kg, h->bit_order == SPCONV_ORDER_CALIBRATED, h->tap_pos);
-    kg_mask_keys<<<blocks(G * n, kGBlock), kGBlock, 0, s>>>(h->nbr, n, h->nbr_stride, G, kg, h->tap_pos, h->mask,
-                                                            mkey_a, perm_a);
-    launches += 2;
-    const bool perm_in_b = rsort::sort_pairs<uint32_t>(mkey_a, perm_a, mkey_b, perm_b, G * n,
-                                                       kg + bit_len(static_cast<uint64_t>(G) - 1), hist, s, &launches);
-    h->perm = reinterpret_cast<int32_t*>(perm_in_b ? perm_b : perm_a);
+    if (src) {   // (a copy precedes it: a plain launch)
+        kg_tap_order<<<1, 128, 0, s>>>(h->tap_count, V, kg, h->bit_order == SPCONV_ORDER_CALIBRATED, h->tap_pos);
+    } else {
+        SPCONV_CHECK(launch_chained(kg_tap_order, 1u, 128u, s, static_cast<const int32_t*>(h->tap_count), V, kg,
+                                    static_cast<int>(h->bit_order == SPCONV_ORDER_CALIBRATED), h->tap_pos));
+    }
     const unsigned tiles = static_cast<unsigned>(G * T);
-    kg_tile_count<<<tiles, kTileRows, 0, s>>>(h->perm, h->mask, n, T, kg, counts, h->tile_union);
-    kg_scan_tiles<<<1, 1024, 0, s>>>(counts, V, G, kg, T, h->tile_union, h->seg_off, h->tap_off, h->totals,
-                                     h->tile_order, h->tile_nonempty);
-    kg_tile_write<<<tiles, kTileRows, 0, s>>>(h->perm, h->mask, h->nbr, h->nbr_stride, n, T, h->n_pad, kg,
-                                              h->seg_off, h->in_rows, h->out_rows, h->gtab);
+    if (wide_mask) {
+        int32_t* mgh = wgh + kWideKeyPassesMax * kWideBins;
+        if (K == 5 && h->nbr_stride == 128)
+            SPCONV_CHECK(launch_chained(kg_mask_keys_rows<5>, capped_blocks(4 * n), kGBlock, s, h->nbr, n, G, kg, mrb, h->tap_pos, mdig,
+                                                                          h->mask, mpk_a, mgh));
+        else if (K == 3 && h->nbr_stride == 28)
+            SPCONV_CHECK(launch_chained(kg_mask_keys_rows<3>, capped_blocks(4 * n), kGBlock, s, h->nbr, n, G, kg, mrb, h->tap_pos, mdig,
+                                                                          h->mask, mpk_a, mgh));
+        else
+            SPCONV_CHECK(launch_chained(kg_mask_keys_packed, capped_blocks(G * n), kGBlock, s, h->nbr, n, h->nbr_stride, G, kg, mrb,
+                                                                         h->tap_pos, mdig, h->mask, mpk_a, mgh));
+        launches += 2;
+        bool in_b = false;
+        SPCONV_CHECK(wide_sort(mpk_a, mpk_b, G * n, mdig, wgh + kWideKeyPassesMax * kWideBins, wtickets,
+                               kWideKeyPassesMax, wlook, h->status, s, &in_b));
+        launches += mdig.passes;
+        SPCONV_CHECK(launch_chained(kg_tile_count<true>, tiles, kTileRows, s, h->perm, in_b ? mpk_b : mpk_a, mrb, h->mask, n, T, kg, counts,
+                                                        h->tile_union));
+    } else {
+        SPCONV_CHECK(launch_chained(kg_mask_keys, blocks(G * n, kGBlock), kGBlock, s, h->nbr, n, h->nbr_stride, G, kg, h->tap_pos, h->mask,
+                                                                mkey_a, perm_a));
+        launches += 2;
+        const bool perm_in_b = rsort::sort_pairs<uint32_t>(mkey_a, perm_a, mkey_b, perm_b, G * n, mbits, hist, s,
+                                                           &launches);
+        h->perm = reinterpret_cast<int32_t*>(perm_in_b ? perm_b : perm_a);
+        SPCONV_CHECK(launch_chained(kg_tile_count<false>, tiles, kTileRows, s, h->perm, nullptr, 0, h->mask, n, T, kg, counts,
+                                                         h->tile_union));
+    }
+    if (T <= kPrefixTilesG && V <= kTileRows) {
+        SPCONV_CHECK(launch_chained(kg_tile_write_prefix, tiles, kTileRows, s, h->perm, h->mask, h->nbr, h->nbr_stride, n, T, h->n_pad, G, kg,
+                                                         counts, h->tap_count, h->tile_union, h->tap_off, h->totals,
+                                                         h->tile_order, h->tile_nonempty, h->in_rows, h->out_rows,
+                                                         h->gtab));
+        launches -= 1;
+    } else {
+        SPCONV_CHECK(launch_chained(kg_scan_tiles, 1, 1024, s, counts, V, G, kg, T, h->tile_union, h->seg_off, h->tap_off, h->totals,
+                                         h->tile_order, h->tile_nonempty));
+        SPCONV_CHECK(launch_chained(kg_tile_write, tiles, kTileRows, s, h->perm, h->mask, h->nbr, h->nbr_stride, n, T, h->n_pad, kg,
+                                                  h->seg_off, h->in_rows, h->out_rows, h->gtab));
+    }
     launches += 3;
     count_launch(launches);
     return cuda_status(cudaGetLastError());
@@ -912,6 +1572,21 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
     size_t bytes = 0;
     auto add = [&](size_t count, size_t elem) { bytes += (count * elem + 255) / 256 * 256; };
     const int64_t nb = rsort::num_tiles(m);
+    // Where the output key takes at most kWideKeyPassesMax digits, the distinct
+    // candidates are found in a hash set and only they are sorted (whole-GPU
+    // pass); else every candidate slot is sorted (8-bit passes) and the first
+    // of each run kept.
+    const WideDigits cdig = wide_digits(0, okey_bits);
+    const bool wide_cand = cdig.passes > 0 && m <= kWideMaxRows;
+    int set_log2 = 11;
+    while ((int64_t(1) << set_log2) < 2 * m) ++set_log2;
+    const size_t set_bytes = wide_cand ? (size_t(1) << set_log2) * 8 : 0;
+    // digit totals, tickets and barrier counters, a status word (padded to 16 bytes), look-back states
+    const size_t wide_bytes = wide_cand ? (kWideTickets * kWideBins + kWideCounters + 4) * sizeof(int32_t) +
+                                              static_cast<size_t>(wide_sort_look_words(m)) * 8
+                                        : 0;
+    add(wide_bytes, 1);
+    add(set_bytes, 1);                            // hash set of the candidates
     add(m, 8); add(m, 8); add(m, 4); add(m, 4);   // candidate keys and (unused) values, ping-pong
     add(m, 4); add(m, 4);                         // first-of-run flags, their exclusive scan
     add((m + kRankBlock - 1) / kRankBlock, 4);    // per-block flag counts
@@ -923,6 +1598,12 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
         return SPCONV_ERR_OOM;
     }
     char* p = static_cast<char*>(scratch);
+    char* wide = take<char>(p, wide_bytes);
+    int32_t* wgh = reinterpret_cast<int32_t*>(wide);
+    int32_t* wtickets = wgh + kWideTickets * kWideBins;
+    int32_t* wstatus = wtickets + kWideCounters;
+    uint64_t* wlook = reinterpret_cast<uint64_t*>(wstatus + 4);
+    uint64_t* cset = take<uint64_t>(p, set_bytes / 8);
     uint64_t* ka = take<uint64_t>(p, m);
     uint64_t* kb = take<uint64_t>(p, m);
     uint32_t* va = take<uint32_t>(p, m);
@@ -946,27 +1627,52 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
     int64_t n_out = 0;
     SPCONV_CHECK_CUDA(cudaMemsetAsync(count, 0, 8, s));
     if (n_in > 0) {
-        kst_candidates<<<blocks(n_in, kGBlock), kGBlock, 0, s>>>(reinterpret_cast<const int4*>(coords), n_in,
-                                                                  make_int3(h->shape[0], h->shape[1], h->shape[2]),
-                                                                  h->batch, O, ka, va);
-        ++launches;
-        const bool in_b = rsort::sort_pairs<uint64_t>(ka, va, kb, vb, m, okey_bits + 1, hist, s, &launches);
-        const uint64_t* sk = in_b ? kb : ka;
-        kst_first<<<blocks(m, kGBlock), kGBlock, 0, s>>>(sk, m, flags);
-        kst_block_count<<<static_cast<unsigned>(rb), kRankBlock, 0, s>>>(flags, m, bcount);
-        kst_block_scan<<<1, kRankBlock, 0, s>>>(bcount, rb);
-        kst_block_rank<<<static_cast<unsigned>(rb), kRankBlock, 0, s>>>(flags, m, bcount, rank);
-        launches += 2;
-        kst_outputs<<<blocks(m, kGBlock), kGBlock, 0, s>>>(sk, flags, rank, m, O,
-                                                           reinterpret_cast<int4*>(h->out_coords), query, m, count);
-        launches += 3;
-        // the one synchronisation: the output count sizes the map
-        SPCONV_CHECK_CUDA(cudaMemcpyAsync(&n_out, count, 8, cudaMemcpyDeviceToHost, s));
-        SPCONV_CHECK_CUDA(cudaStreamSynchronize(s));
+        const int3 ishape = make_int3(h->shape[0], h->shape[1], h->shape[2]);
+        if (wide_cand) {
+            SPCONV_CHECK_CUDA(cudaMemsetAsync(wide, 0, wide_bytes, s));
+            SPCONV_CHECK_CUDA(cudaMemsetAsync(cset, 0, set_bytes, s));
+            kst_dedupe<<<capped_blocks(n_in), kGBlock, 0, s>>>(reinterpret_cast<const int4*>(coords), n_in, ishape,
+                                                               h->batch, O, cset, set_log2, cdig, ka, count, wgh);
+            ++launches;
+            // the one synchronisation: the number of distinct sites sizes the map
+            SPCONV_CHECK_CUDA(cudaMemcpyAsync(&n_out, count, 8, cudaMemcpyDeviceToHost, s));
+            SPCONV_CHECK_CUDA(cudaStreamSynchronize(s));
+            if (n_out > 0) {
+                bool in_b = false;
+                SPCONV_CHECK(wide_sort(ka, kb, n_out, cdig, wgh, wtickets, 0, wlook, wstatus, s, &in_b, true));
+                launches += cdig.passes;
+                SPCONV_CHECK(launch_chained(kst_outputs_sorted, blocks(n_out, kGBlock), kGBlock, s, 
+                    in_b ? kb : ka, n_out, O, reinterpret_cast<int4*>(h->out_coords), query));
+                ++launches;
+            }
+        } else {
+            kst_candidates<<<blocks(n_in, kGBlock), kGBlock, 0, s>>>(reinterpret_cast<const int4*>(coords), n_in,
+                                                                      ishape, h->batch, O, ka, va);
+            ++launches;
+            const bool in_b = rsort::sort_pairs<uint64_t>(ka, va, kb, vb, m, okey_bits + 1, hist, s, &launches);
+            const uint64_t* sk = in_b ? kb : ka;
+            kst_first<<<blocks(m, kGBlock), kGBlock, 0, s>>>(sk, m, kNoKey, flags);
+            kst_block_count<<<static_cast<unsigned>(rb), kRankBlock, 0, s>>>(flags, m, bcount);
+            kst_block_scan<<<1, kRankBlock, 0, s>>>(bcount, rb);
+            kst_block_rank<<<static_cast<unsigned>(rb), kRankBlock, 0, s>>>(flags, m, bcount, rank);
+            launches += 2;
+            kst_outputs<<<blocks(m, kGBlock), kGBlock, 0, s>>>(sk, flags, rank, m, O,
+                                                               reinterpret_cast<int4*>(h->out_coords), query, m, count);
+            launches += 3;
+            // the one synchronisation: the output count sizes the map
+            SPCONV_CHECK_CUDA(cudaMemcpyAsync(&n_out, count, 8, cudaMemcpyDeviceToHost, s));
+            SPCONV_CHECK_CUDA(cudaStreamSynchronize(s));
+        }
     }
     count_launch(launches);
     h->n = n_out;
-    const int rc = grouped_core(h, opt, coords, n_in, reinterpret_cast<const int32_t*>(query), nullptr);
+    int rc = grouped_core(h, opt, coords, n_in, reinterpret_cast<const int32_t*>(query), nullptr);
+    if (rc == SPCONV_OK && wide_cand && h->status) {
+        // a stall of the distinct-site sort shows in the map's status
+        k_or_status<<<1, 32, 0, s>>>(h->status, wstatus);
+        count_launch();
+        rc = cuda_status(cudaGetLastError());
+    }
     cudaFreeAsync(scratch, s);   // stream-ordered: after the kernels that read it
     return rc;
 }

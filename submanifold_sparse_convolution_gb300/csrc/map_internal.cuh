@@ -118,6 +118,50 @@ struct WideArgs {
 
 // Coordinate sort passes the whole-GPU pipeline takes for a key width.
 int wide_key_passes(int key_bits);
+
+// ---- the whole-GPU stable sort on its own, for the other map builders -----
+// Digits of a sort of packed 64-bit values by their bits [lo, lo + bits):
+// the fewest passes of at most kDigitBitsWide bits, as even as possible.
+struct WideDigits {
+    int passes;
+    int shift[kWideKeyPassesMax];   // lowest bit of pass p's digit in the packed value
+    int width[kWideKeyPassesMax];   // its width
+};
+// passes = 0 when bits needs more than kWideKeyPassesMax passes.
+WideDigits wide_digits(int lo, int bits);
+// Look-back state words a sort of n values needs (zeroed by the caller).
+int64_t wide_sort_look_words(int64_t n);
+// Stable LSD sort of the n packed values in a by the digits d, one
+// whole-GPU pass per digit (a and b ping-pong), each launched with
+// programmatic dependent launch.  gh[p][kWideBins] holds pass p's digit
+// totals over all n values (counted by the kernel that wrote a); tickets
+// (kWideCounters ints; passes use the ticket indices ticket0, ticket0 + 1,
+// ...) and look are zero before the first pass.  *in_b: the result is in b.
+// first_plain: the first pass waits for the whole stream before it (a copy
+// or memset precedes it) rather than overlapping a kernel's tail.
+int wide_sort(uint64_t* a, uint64_t* b, int64_t n, const WideDigits& d, const int32_t* gh, int32_t* tickets,
+              int ticket0, uint64_t* look, int32_t* status, cudaStream_t s, bool* in_b, bool first_plain = false);
+
+// In a kernel whose every thread calls it together (whole warps): adds the
+// digits of v under d to the block's histograms h[pass][digit] when valid.
+__device__ __forceinline__ void wide_count_digits(uint64_t v, bool valid, const WideDigits& d,
+                                                  int32_t (*h)[kWideBins]) {
+    const int lane = threadIdx.x & 31;
+    for (int p = 0; p < d.passes; ++p) {
+        const int dg = valid ? static_cast<int>((v >> d.shift[p]) & ((1u << d.width[p]) - 1u)) : kWideBins;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, dg);
+        if (valid && lane == __ffs(peers) - 1) atomicAdd(&h[p][dg], __popc(peers));
+    }
+}
+
+// Adds a block's histograms h (cleared before) into gh[pass][digit] (all
+// threads of the block call it after their counts, behind a barrier).
+__device__ __forceinline__ void wide_flush_digits(const WideDigits& d, int32_t (*h)[kWideBins], int32_t* gh) {
+    for (int i = threadIdx.x; i < d.passes * kWideBins; i += blockDim.x) {
+        const int32_t x = h[i / kWideBins][i % kWideBins];
+        if (x) atomicAdd(gh + i, x);
+    }
+}
 // The whole build on stream s; sms = multiprocessors of the device.
 int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s);
 

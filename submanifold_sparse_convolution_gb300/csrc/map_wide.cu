@@ -1234,6 +1234,87 @@ int hash_table_log2(int64_t n) {
     return l;
 }
 
+namespace {
+
+// One pass of the stable sort on stream s: a CTA per partition of
+// keys_per_cta values (2 kWideKeysPerCta above kBigPassRows); partitions
+// numbered by blockIdx when the device holds the whole grid at once, else by
+// the ticket counter tickets[ticket]; offsets by the two-barrier form when
+// every partition is resident and the digits spread over them, else by
+// decoupled look-back.
+int launch_wide_pass(const uint64_t* in, uint64_t* out, int64_t n, int shift, int width, const int32_t* gh,
+                     uint64_t* look, int32_t* tickets, int ticket, int32_t* status, cudaStream_t s, bool pdl = true) {
+    static int64_t cap_pass[kMaxDevices][2] = {};
+    int dev = 0;
+    SPCONV_CHECK_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return SPCONV_ERR_UNSUPPORTED;
+    if (cap_pass[dev][0] == 0) {
+        int sms = 0;
+        SPCONV_CHECK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        cap_pass[dev][0] = resident_ctas(k_wide_pass<WI>, WT, sms);
+        cap_pass[dev][1] = resident_ctas(k_wide_pass<2 * WI>, WT, sms);
+    }
+    const bool big_pass = n > kBigPassRows;
+    const int64_t keys_per_cta = big_pass ? 2 * kWideKeysPerCta : kWideKeysPerCta;
+    const int64_t parts = (n + keys_per_cta - 1) / keys_per_cta;
+    if (parts > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
+    const bool pass_ticket = parts > cap_pass[dev][big_pass ? 1 : 0];
+    PassArgs pa;
+    pa.in = in;
+    pa.out = out;
+    pa.n = n;
+    pa.shift = shift;
+    pa.width = width;
+    pa.gh = gh;
+    pa.look = look;
+    pa.epoch = next_epoch();
+    pa.ticket = pass_ticket ? tickets + ticket : nullptr;
+    // the barrier form when every partition is resident, each warp scans at
+    // most kScanDigitsPerWarp digits and each lane at most kScanPerLane partitions
+    // (below ~64 partitions a windowed look-back chain is as short and has no barrier)
+    const int64_t bins = int64_t(1) << width;
+    const bool barrier = !pass_ticket && parts > 64 && bins <= parts * WW * kScanDigitsPerWarp &&
+                         parts <= 32 * kScanPerLane;
+    pa.bar = barrier ? tickets + kWideTickets + ticket * kWideBarrierInts : nullptr;
+    pa.status = status;
+    return big_pass ? launch_pdl(k_wide_pass<2 * WI>, static_cast<unsigned>(parts), WT, s, pdl, pa)
+                    : launch_pdl(k_wide_pass<WI>, static_cast<unsigned>(parts), WT, s, pdl, pa);
+}
+
+}  // namespace
+
+WideDigits wide_digits(int lo, int bits) {
+    WideDigits d = {};
+    const int passes = (bits + kDigitBitsWide - 1) / kDigitBitsWide;
+    if (passes > kWideKeyPassesMax) return d;
+    d.passes = passes;
+    for (int p = 0, at = lo; p < passes; ++p) {
+        d.width[p] = bits / passes + (p < bits % passes ? 1 : 0);
+        d.shift[p] = at;
+        at += d.width[p];
+    }
+    return d;
+}
+
+int64_t wide_sort_look_words(int64_t n) {
+    const int64_t keys_per_cta = n > kBigPassRows ? 2 * kWideKeysPerCta : kWideKeysPerCta;
+    return (n + keys_per_cta - 1) / keys_per_cta * kWideBins;
+}
+
+int wide_sort(uint64_t* a, uint64_t* b, int64_t n, const WideDigits& d, const int32_t* gh, int32_t* tickets,
+              int ticket0, uint64_t* look, int32_t* status, cudaStream_t s, bool* in_b, bool first_plain) {
+    *in_b = false;
+    if (d.passes < 1 || ticket0 < 0 || ticket0 + d.passes > kWideTickets) return SPCONV_ERR_UNSUPPORTED;
+    if (n > kWideMaxRows) return SPCONV_ERR_UNSUPPORTED;
+    for (int p = 0; p < d.passes; ++p) {
+        const bool odd = p & 1;
+        SPCONV_CHECK(launch_wide_pass(odd ? b : a, odd ? a : b, n, d.shift[p], d.width[p], gh + p * kWideBins, look,
+                                      tickets, ticket0 + p, status, s, !(first_plain && p == 0)));
+    }
+    *in_b = (d.passes & 1) != 0;
+    return SPCONV_OK;
+}
+
 int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     const int64_t n = a.n;
     // keys per sort CTA: 1024, or 2048 above kBigPassRows (fewer partitions to
@@ -1245,18 +1326,6 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     const int rpt = few ? 1 : 4;
     const unsigned key_blocks = static_cast<unsigned>((n + WT * rpt - 1) / (WT * rpt));
     const unsigned row_blocks = static_cast<unsigned>((n + WT - 1) / WT);
-    // a look-back kernel numbers its partitions by blockIdx when all of its
-    // CTAs fit on the device at once (each waits only on lower ones), else
-    // takes them from a ticket counter in the order the CTAs start
-    static int64_t cap_pass[kMaxDevices][2] = {};
-    int dev = 0;
-    SPCONV_CHECK_CUDA(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= kMaxDevices) return SPCONV_ERR_UNSUPPORTED;
-    if (cap_pass[dev][0] == 0) {
-        cap_pass[dev][0] = resident_ctas(k_wide_pass<WI>, WT, sms);
-        cap_pass[dev][1] = resident_ctas(k_wide_pass<2 * WI>, WT, sms);
-    }
-    const bool pass_ticket = static_cast<int64_t>(parts) > cap_pass[dev][big_pass ? 1 : 0];
     // every thread clears ~8 16-byte words of the largest array
     const int64_t look16 = static_cast<int64_t>(parts) * kWideBins / 2;
     int64_t clear16 = a.mapper == SPCONV_MAPPER_DENSE ? a.cells / 4
@@ -1267,27 +1336,7 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     if (clear_blocks > 4 * sms) clear_blocks = 4 * sms;
     SPCONV_CHECK(launch_pdl(k_wide_clear, static_cast<unsigned>(clear_blocks < 1 ? 1 : clear_blocks), WT, s, false, a));
     auto pass = [&](const uint64_t* in, uint64_t* out, int shift, int width, const int32_t* gh, int ticket) {
-        PassArgs pa;
-        pa.in = in;
-        pa.out = out;
-        pa.n = n;
-        pa.shift = shift;
-        pa.width = width;
-        pa.gh = gh;
-        pa.look = a.look;
-        pa.epoch = next_epoch();
-        pa.ticket = pass_ticket ? a.tickets + ticket : nullptr;
-        // the barrier form when every partition is resident, each warp scans at
-        // most kScanDigitsPerWarp digits and each lane at most kScanPerLane partitions
-        const int64_t bins = int64_t(1) << width;
-        // (below ~64 partitions a windowed look-back chain is as short and has no barrier)
-        const bool barrier = !pass_ticket && parts > 64 &&
-                             bins <= static_cast<int64_t>(parts) * WW * kScanDigitsPerWarp &&
-                             static_cast<int64_t>(parts) <= 32 * kScanPerLane;
-        pa.bar = barrier ? a.tickets + kWideTickets + ticket * kWideBarrierInts : nullptr;
-        pa.status = a.status;
-        return big_pass ? launch_pdl(k_wide_pass<2 * WI>, parts, WT, s, true, pa)
-                        : launch_pdl(k_wide_pass<WI>, parts, WT, s, true, pa);
+        return launch_wide_pass(in, out, n, shift, width, gh, a.look, a.tickets, ticket, a.status, s);
     };
     if (a.mapper == SPCONV_MAPPER_HASH) {
         SPCONV_CHECK(launch_pdl(k_wide_hash_insert, row_blocks, WT, s, true, a));
