@@ -74,9 +74,9 @@ __global__ void __launch_bounds__(256) k_simt(const T* __restrict__ feats, const
 // ---------------------------------------------------------------------------
 // fp32 exact mode, tiled: one CTA per (128-row tile of the mask-sorted order,
 // 64 output channels).  It visits the taps of the tile's mask union in
-// ascending order, 64 input channels at a time ("Neighbour masks and sorted
+// ascending order, 32 input channels at a time ("Neighbour masks and sorted
 // rows": rows of a tile share their taps); for each (tap, channel chunk) the
-// weight slab W[k][c0 .. c0+63][o0 .. o0+63] and the tile's 128 gathered
+// weight slab W[k][c0 .. c0+31][o0 .. o0+63] and the tile's 128 gathered
 // input rows (through the map's gather table; a row without the tap is
 // zeros) are staged in shared memory by cp.async, double-buffered, and each
 // thread accumulates an 8 x 8 block of outputs in registers.  A row without
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(256) k_simt(const T* __restrict__ feats, const
 // ---------------------------------------------------------------------------
 constexpr int kFRows = kTileRows;     // rows per tile
 constexpr int kFCols = 64;            // output channels per CTA
-constexpr int kFK = 64;               // input channels per stage
+constexpr int kFK = 32;               // input channels per stage (3 CTAs per SM fit; 64 admitted 2)
 constexpr int kFThreads = 128;        // 16 row groups x 8 column groups
 constexpr int kFRowStride = kFK + 4;  // floats per staged feature row (16-byte aligned, conflict-free)
 constexpr int kFStageFloats = kFRows * kFRowStride + kFK * kFCols;
@@ -97,7 +97,7 @@ __device__ __forceinline__ void cp_async16(float* dst, const float* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
 
-__global__ void __launch_bounds__(kFThreads, 2) k_fp32_tiled(const float* __restrict__ feats,
+__global__ void __launch_bounds__(kFThreads, 3) k_fp32_tiled(const float* __restrict__ feats,
                                                              const float* __restrict__ w,
                                                              float* __restrict__ out,
                                                              const int32_t* __restrict__ perm,
@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(kFThreads, 2) k_fp32_tiled(const float* __rest
     const uint32_t uni = tile_union[tile];
     const int kcs = (c_in + kFK - 1) / kFK;
     const int n_stages = __popc(uni) * kcs;
-    // the source rows of the current tap, one per staged row this thread loads
-    // (thread t loads rows t / 16 + 8 q, 16-byte chunk t % 16)
+    // stage st: its weight slab and the tile's gathered rows (thread t loads
+    // rows t / (kFK / 4) + q kFThreads / (kFK / 4), 16-byte chunk t % (kFK / 4))
     auto stage = [&](int st, float* buf) {
         // st-th (tap, chunk) of the tile: the tap is the (st / kcs)-th set bit of the union
         uint32_t u = uni;
@@ -132,9 +132,10 @@ __global__ void __launch_bounds__(kFThreads, 2) k_fp32_tiled(const float* __rest
             else
                 *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        // gathered rows: 128 rows of kFK floats
-        const int ch = t & 15;
-        for (int r = t >> 4; r < kFRows; r += kFThreads / 16) {
+        // gathered rows: 128 rows of kFK floats (kFK / 4 16-byte chunks per row)
+        constexpr int kCh = kFK / 4;
+        const int ch = t % kCh;
+        for (int r = t / kCh; r < kFRows; r += kFThreads / kCh) {
             const int32_t j = __ldg(gtab + static_cast<int64_t>(k) * n_pad + tile * kFRows + r);
             float* d = fs + r * kFRowStride + 4 * ch;
             if (j >= 0 && j < n_in && c0 + 4 * ch < c_in)
