@@ -491,62 +491,75 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
             const int32_t* gidx = idx + b * kTaps * BM;
             const __nv_bfloat16* lin = layer == 0 ? p.feats : p.outs[layer - 1];
             const uint8_t* lw = p.wpacks[layer];
-            for (int j = 0; uni && !stop; ++j) {
-                const int k = __ffs(uni) - 1;
-                uni &= uni - 1;
-                for (int kc = 0; kc < p.k_chunks; ++kc, ++f) {
-                    if (static_cast<int>(f % S) != slot) continue;
-                    // all RG source rows of this lane group, read before any copy is issued
-                    int32_t sr[RG];
-                    const int4* gsrc = reinterpret_cast<const int4*>(gidx + j * BM + row0);
+            // this warp's stages of the item: fs in [f, f + stages) with fs % S == slot;
+            // stage fs is chunk kc of the union's j-th tap (taps in ascending order)
+            const uint32_t f_end = f + static_cast<uint32_t>(__popc(uni) * p.k_chunks);
+            uint32_t ucur = uni;   // the union without its first jcur taps
+            int jcur = 0;
+            for (uint32_t fs = f + static_cast<uint32_t>((slot - static_cast<int>(f % S) + S) % S); fs < f_end && !stop;
+                 fs += S) {
+                const int j = static_cast<int>((fs - f) / static_cast<uint32_t>(p.k_chunks));
+                const int kc = static_cast<int>(fs - f) - j * p.k_chunks;
+                for (; jcur < j; ++jcur) ucur &= ucur - 1;
+                const int k = __ffs(ucur) - 1;
+                // all RG source rows of this lane group, read before any copy is issued
+                int32_t sr[RG];
+                const int4* gsrc = reinterpret_cast<const int4*>(gidx + j * BM + row0);
 #pragma unroll
-                    for (int q = 0; q < RG / 4; ++q) {
-                        const int4 v4 = gsrc[q];
-                        sr[4 * q] = v4.x;
-                        sr[4 * q + 1] = v4.y;
-                        sr[4 * q + 2] = v4.z;
-                        sr[4 * q + 3] = v4.w;
-                    }
-                    const uint32_t u = f / S;
-                    if (u > 0 && !warp_wait(&empty[slot], (u - 1) & 1)) {
-                        if (lane == 0) fail();
-                        stop = true;
-                        break;
-                    }
-                    if (lane == 0) {
-                        if (part == 0) {
-                            ptx::mbar_arrive_expect_tx(gfull, b_bytes);
-                            const uint8_t* src =
-                                lw + (static_cast<int64_t>(nb * p.taps_w + p.k0 + k) * p.k_chunks + kc) * b_bytes;
-                            ptx::bulk_copy_g2s(b_smem, src, b_bytes, gfull);
-                        } else {
-                            ptx::mbar_arrive(gfull);
-                        }
-                    }
-                    const int kcol = kc * BK + chunk * 8;
-                    const bool col_ok = kcol < p.c_in;
-                    const __nv_bfloat16* fcol = lin + kcol;
-                    const uint32_t dst0 = a_smem + static_cast<uint32_t>(row0) * 128;
-                    bool bad = false;   // a row index past n: skipped, reported below
-#pragma unroll
-                    for (int i = 0; i < RG; ++i) {
-                        const int32_t src_row = sr[i];
-                        const uint32_t dst = dst0 + i * 128 + ((chunk ^ (i & 7)) << 4);
-                        if (src_row >= 0 && src_row < p.n_in && col_ok)
-                            ptx::cp_async_16(dst, fcol + static_cast<int64_t>(src_row) * p.c_in, 16u);
-                        else
-                            ptx::st_shared_zero16(dst);   // absent neighbour: no memory request
-                        bad |= src_row >= p.n_in;
-                    }
-                    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.status, kStatusInternal);
-                    ptx::cp_async_commit();
-                    ptx::cp_async_wait_all();
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(gfull);
-                    last = f;
+                for (int q = 0; q < RG / 4; ++q) {
+                    const int4 v4 = gsrc[q];
+                    sr[4 * q] = v4.x;
+                    sr[4 * q + 1] = v4.y;
+                    sr[4 * q + 2] = v4.z;
+                    sr[4 * q + 3] = v4.w;
                 }
+                const uint32_t u = fs / S;
+                if (u > 0 && !warp_wait(&empty[slot], (u - 1) & 1)) {
+                    if (lane == 0) fail();
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) {
+                    if (part == 0) {
+                        ptx::mbar_arrive_expect_tx(gfull, b_bytes);
+                        const uint8_t* src =
+                            lw + (static_cast<int64_t>(nb * p.taps_w + p.k0 + k) * p.k_chunks + kc) * b_bytes;
+                        ptx::bulk_copy_g2s(b_smem, src, b_bytes, gfull);
+                    } else {
+                        ptx::mbar_arrive(gfull);
+                    }
+                }
+                const int kcol = kc * BK + chunk * 8;
+                // rows below lim are copied: n, or none when this lane's channels lie past c_in
+                const uint32_t lim = kcol < p.c_in ? static_cast<uint32_t>(p.n_in) : 0u;
+                const char* fcol = reinterpret_cast<const char*>(lin + kcol);
+                const uint32_t row_bytes = static_cast<uint32_t>(p.c_in) * 2u;
+                const uint32_t dst0 = a_smem + static_cast<uint32_t>(row0) * 128;
+                // Each row is one predicated copy or zero store: the producer's
+                // instruction count per row is on the kernel's critical path, so
+                // absent (-1) and out-of-range indices are caught by one unsigned
+                // compare, and a row index past n (skipped: a zero row) is reported
+                // from the largest index of the stage rather than per row.
+                int32_t top = -1;
+#pragma unroll
+                for (int i = 0; i < RG; ++i) {
+                    const int32_t src_row = sr[i];
+                    const uint32_t dst = dst0 + i * 128 + ((chunk ^ (i & 7)) << 4);
+                    if (static_cast<uint32_t>(src_row) < lim)
+                        ptx::cp_async_16(dst, fcol + static_cast<uint64_t>(static_cast<uint32_t>(src_row)) * row_bytes, 16u);
+                    else
+                        ptx::st_shared_zero16(dst);   // absent neighbour: no memory request
+                    top = max(top, src_row);
+                }
+                if (__any_sync(0xFFFFFFFFu, top >= p.n_in) && lane == 0) atomicOr(p.status, kStatusInternal);
+                ptx::cp_async_commit();
+                ptx::cp_async_wait_all();
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(gfull);
+                last = fs;
             }
+            if (!stop) f = f_end;
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&idx_empty[b]);
         }
@@ -560,6 +573,7 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
         // ---------------- MMA issuer: the warp runs the loop, lane 0 issues
         const uint32_t leader = lane == 0;
         const uint32_t idesc = ptx::idesc_bf16_f32(BM, static_cast<uint32_t>(p.n_tile));
+        const uint64_t desc0 = ptx::sdesc_k128(smem_base);   // stage 0's A operand
         uint32_t f = 0;
         int ai = 0;   // items accumulated so far: item ai uses TMEM buffer ai & 1
         bool stop = false;
@@ -598,12 +612,14 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                         stop = true;
                         break;
                     }
-                    const uint32_t a_addr = smem_base + slot * Cfg::kStage;
-                    const uint32_t b_addr = a_addr + kStageA;
+                    // the stage's descriptors: the base one plus the stage's offset / 16 in
+                    // the start-address field (shared addresses stay below 2^18: no carry)
+                    const uint64_t a_desc = desc0 + static_cast<uint64_t>((slot * Cfg::kStage) >> 4);
+                    const uint64_t b_desc = a_desc + static_cast<uint64_t>(kStageA >> 4);
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j) {
-                        ptx::mma_bf16_if(leader, d_tmem, ptx::sdesc_k128(a_addr + 32 * j),
-                                         ptx::sdesc_k128(b_addr + 32 * j), idesc, (first && j == 0) ? 0u : 1u);
+                        ptx::mma_bf16_if(leader, d_tmem, a_desc + 2 * j, b_desc + 2 * j, idesc,
+                                         (first && j == 0) ? 0u : 1u);   // K step 16 bf16 = 32 bytes
                     }
                     first = false;
                     ptx::mma_commit_if(leader, &empty[slot]);
