@@ -539,8 +539,8 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                 // instruction count per row is on the kernel's critical path, so
                 // absent (-1) and out-of-range indices are caught by one unsigned
                 // compare, and a row index past n (skipped: a zero row) is reported
-                // from the largest index of the stage rather than per row.
-                int32_t top = -1;
+                // from one 16-byte word of the indices per lane (the eight lanes of
+                // a group cover its rows) rather than per row.
 #pragma unroll
                 for (int i = 0; i < RG; ++i) {
                     const int32_t src_row = sr[i];
@@ -549,9 +549,13 @@ __global__ void __launch_bounds__(TcConfig<NTMAX>::kThreads, 1) k_tc_gemm(const 
                         ptx::cp_async_16(dst, fcol + static_cast<uint64_t>(static_cast<uint32_t>(src_row)) * row_bytes, 16u);
                     else
                         ptx::st_shared_zero16(dst);   // absent neighbour: no memory request
-                    top = max(top, src_row);
                 }
-                if (__any_sync(0xFFFFFFFFu, top >= p.n_in) && lane == 0) atomicOr(p.status, kStatusInternal);
+                bool past = false;
+                if (chunk < RG / 4) {
+                    const int4 w4 = gsrc[chunk];
+                    past = max(max(w4.x, w4.y), max(w4.z, w4.w)) >= p.n_in;
+                }
+                if (__any_sync(0xFFFFFFFFu, past) && lane == 0) atomicOr(p.status, kStatusInternal);
                 ptx::cp_async_commit();
                 ptx::cp_async_wait_all();
                 ptx::fence_proxy_async_smem();

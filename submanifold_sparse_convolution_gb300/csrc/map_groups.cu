@@ -1388,13 +1388,20 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
     h->arena = arena;
     h->arena_bytes = bytes;
     char* p = static_cast<char*>(arena);
+    // the arrays that start at zero come first, cleared by one memset: the
+    // status, tap counts, totals, the whole-GPU sort's scratch and the hash table
+    char* const zero_begin = p;
     h->status = take<int32_t>(p, 4);
+    h->tap_count = take<int32_t>(p, V);
+    h->totals = take<int32_t>(p, 2);
+    char* wide = take<char>(p, wide_bytes);
+    const bool hashed = !src && !wide_coord && mapper == SPCONV_MAPPER_HASH;
+    uint64_t* table = hashed ? take<uint64_t>(p, size_t(1) << table_log2) : nullptr;
+    const size_t zero_bytes = static_cast<size_t>(p - zero_begin);
     h->nbr = take<int32_t>(p, n1 * h->nbr_stride);
     h->mask = take<uint32_t>(p, gn);
-    h->tap_count = take<int32_t>(p, V);
     h->tap_pos = take<int32_t>(p, V);
     h->tap_off = take<int32_t>(p, V + 1);
-    h->totals = take<int32_t>(p, 2);
     h->in_rows = take<int32_t>(p, V * n1);
     h->out_rows = take<int32_t>(p, V * n1);
     h->gtab = take<int32_t>(p, V * np);
@@ -1417,16 +1424,12 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
         perm_b = take<uint32_t>(p, gn);
     }
     int32_t* hist = take<int32_t>(p, rsort::kBins * nb);
-    char* wide = take<char>(p, wide_bytes);
     int32_t* wgh = reinterpret_cast<int32_t*>(wide);                 // [kWideTickets][kWideBins]
     int32_t* wtickets = wgh + kWideTickets * kWideBins;             // [kWideCounters]
     uint64_t* wlook = reinterpret_cast<uint64_t*>(wtickets + kWideCounters);
 
-    SPCONV_CHECK_CUDA(cudaMemsetAsync(h->status, 0, 4 * sizeof(int32_t), s));
-    SPCONV_CHECK_CUDA(cudaMemsetAsync(h->tap_count, 0, V * sizeof(int32_t), s));
-    SPCONV_CHECK_CUDA(cudaMemsetAsync(h->totals, 0, 2 * sizeof(int32_t), s));
+    SPCONV_CHECK_CUDA(cudaMemsetAsync(zero_begin, 0, zero_bytes, s));
     h->perm = wide_mask ? perm_w : reinterpret_cast<int32_t*>(perm_a);
-    if (wide_bytes) SPCONV_CHECK_CUDA(cudaMemsetAsync(wide, 0, wide_bytes, s));
     if (n == 0) {
         SPCONV_CHECK_CUDA(cudaMemsetAsync(h->tap_off, 0, (V + 1) * sizeof(int32_t), s));
         return cuda_status(cudaGetLastError());
@@ -1481,8 +1484,6 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
                                                                 L, h->nbr, h->tap_count, h->status));
         ++launches;
     } else if (mapper == SPCONV_MAPPER_HASH) {
-        uint64_t* table = take<uint64_t>(p, size_t(1) << table_log2);
-        SPCONV_CHECK_CUDA(cudaMemsetAsync(table, 0, (size_t(1) << table_log2) * 8, s));
         kg_hash_insert<<<blocks(n_table, kGBlock), kGBlock, 0, s>>>(c4, n_table, shape3, B, L, table, table_log2,
                                                                     row_bits, h->status);
         const int4* q4 = query ? reinterpret_cast<const int4*>(query) : c4;
@@ -1598,12 +1599,17 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
         return SPCONV_ERR_OOM;
     }
     char* p = static_cast<char*>(scratch);
+    // what starts at zero comes first, cleared by one memset: the output count,
+    // the whole-GPU sort's scratch and the hash set
+    char* const zero_begin = p;
+    int64_t* count = take<int64_t>(p, 1);
     char* wide = take<char>(p, wide_bytes);
+    uint64_t* cset = take<uint64_t>(p, set_bytes / 8);
+    const size_t zero_bytes = static_cast<size_t>(p - zero_begin);
     int32_t* wgh = reinterpret_cast<int32_t*>(wide);
     int32_t* wtickets = wgh + kWideTickets * kWideBins;
     int32_t* wstatus = wtickets + kWideCounters;
     uint64_t* wlook = reinterpret_cast<uint64_t*>(wstatus + 4);
-    uint64_t* cset = take<uint64_t>(p, set_bytes / 8);
     uint64_t* ka = take<uint64_t>(p, m);
     uint64_t* kb = take<uint64_t>(p, m);
     uint32_t* va = take<uint32_t>(p, m);
@@ -1614,7 +1620,6 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
     int32_t* bcount = take<int32_t>(p, rb);
     int32_t* hist = take<int32_t>(p, rsort::kBins * std::max<int64_t>(1, nb));
     int4* query = take<int4>(p, m);
-    int64_t* count = take<int64_t>(p, 1);
     void* outs = nullptr;
     if (pool_alloc(&outs, static_cast<size_t>(m) * 16, s) != cudaSuccess) {
         cudaGetLastError();
@@ -1625,12 +1630,10 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
     h->out_coords = static_cast<int32_t*>(outs);
     int launches = 0;
     int64_t n_out = 0;
-    SPCONV_CHECK_CUDA(cudaMemsetAsync(count, 0, 8, s));
+    SPCONV_CHECK_CUDA(cudaMemsetAsync(zero_begin, 0, zero_bytes, s));
     if (n_in > 0) {
         const int3 ishape = make_int3(h->shape[0], h->shape[1], h->shape[2]);
         if (wide_cand) {
-            SPCONV_CHECK_CUDA(cudaMemsetAsync(wide, 0, wide_bytes, s));
-            SPCONV_CHECK_CUDA(cudaMemsetAsync(cset, 0, set_bytes, s));
             kst_dedupe<<<capped_blocks(n_in), kGBlock, 0, s>>>(reinterpret_cast<const int4*>(coords), n_in, ishape,
                                                                h->batch, O, cset, set_log2, cdig, ka, count, wgh);
             ++launches;
