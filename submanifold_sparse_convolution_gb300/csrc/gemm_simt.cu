@@ -115,11 +115,24 @@ __global__ void __launch_bounds__(kFThreads, 3) k_fp32_tiled(const float* __rest
     const int n_stages = __popc(uni) * kcs;
     // stage st: its weight slab and the tile's gathered rows (thread t loads
     // rows t / (kFK / 4) + q kFThreads / (kFK / 4), 16-byte chunk t % (kFK / 4))
-    auto stage = [&](int st, float* buf) {
-        // st-th (tap, chunk) of the tile: the tap is the (st / kcs)-th set bit of the union
+    constexpr int kCh = kFK / 4;                           // 16-byte chunks of a staged row
+    constexpr int kRowsPer = kFRows / (kFThreads / kCh);   // rows each thread stages
+    // st-th (tap, chunk) of the tile: the tap is the (st / kcs)-th set bit of the union
+    auto tap_of = [&](int st) {
         uint32_t u = uni;
         for (int j = st / kcs; j > 0; --j) u &= u - 1;
-        const int k = __ffs(u) - 1;
+        return __ffs(u) - 1;
+    };
+    // the source rows of stage st for this thread's staged rows, loaded a stage
+    // ahead of their copies so that their latency hides behind the compute
+    auto load_idx = [&](int st, int32_t (&jr)[kRowsPer]) {
+        const int k = tap_of(st);
+#pragma unroll
+        for (int q = 0; q < kRowsPer; ++q)
+            jr[q] = __ldg(gtab + static_cast<int64_t>(k) * n_pad + tile * kFRows + t / kCh + q * (kFThreads / kCh));
+    };
+    auto stage = [&](int st, float* buf, const int32_t (&jr)[kRowsPer]) {
+        const int k = tap_of(st);
         const int c0 = (st % kcs) * kFK;
         float* fs = buf;
         float* ws = buf + kFRows * kFRowStride;
@@ -133,10 +146,11 @@ __global__ void __launch_bounds__(kFThreads, 3) k_fp32_tiled(const float* __rest
                 *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         // gathered rows: 128 rows of kFK floats (kFK / 4 16-byte chunks per row)
-        constexpr int kCh = kFK / 4;
         const int ch = t % kCh;
-        for (int r = t / kCh; r < kFRows; r += kFThreads / kCh) {
-            const int32_t j = __ldg(gtab + static_cast<int64_t>(k) * n_pad + tile * kFRows + r);
+#pragma unroll
+        for (int q = 0; q < kRowsPer; ++q) {
+            const int r = t / kCh + q * (kFThreads / kCh);
+            const int32_t j = jr[q];
             float* d = fs + r * kFRowStride + 4 * ch;
             if (j >= 0 && j < n_in && c0 + 4 * ch < c_in)
                 cp_async16(d, feats + static_cast<int64_t>(j) * c_in + c0 + 4 * ch);
@@ -151,11 +165,17 @@ __global__ void __launch_bounds__(kFThreads, 3) k_fp32_tiled(const float* __rest
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int v = 0; v < 8; ++v) acc[i][v] = 0.0f;
-    if (n_stages > 0) stage(0, fsm);
+    int32_t jn[kRowsPer];   // the source rows of the next stage to issue
+    if (n_stages > 0) {
+        load_idx(0, jn);
+        stage(0, fsm, jn);
+    }
+    if (n_stages > 1) load_idx(1, jn);
     for (int st = 0; st < n_stages; ++st) {
         float* buf = fsm + (st & 1) * kFStageFloats;
         if (st + 1 < n_stages) {
-            stage(st + 1, fsm + ((st + 1) & 1) * kFStageFloats);
+            stage(st + 1, fsm + ((st + 1) & 1) * kFStageFloats, jn);
+            if (st + 2 < n_stages) load_idx(st + 2, jn);
             asm volatile("cp.async.wait_group 1;" ::: "memory");
         } else {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -164,13 +184,14 @@ __global__ void __launch_bounds__(kFThreads, 3) k_fp32_tiled(const float* __rest
         const float* fs = buf;
         const float* ws = buf + kFRows * kFRowStride;
         const int cmax = c_in - (st % kcs) * kFK < kFK ? c_in - (st % kcs) * kFK : kFK;
-        for (int c = 0; c < cmax; c += 4) {
+        // channels c .. c + 3 of the stage into the 8 x 8 block (cc < lim of them)
+        auto step4 = [&](int c, int lim) {
             float4 f[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) f[i] = *reinterpret_cast<const float4*>(fs + (rg + 16 * i) * kFRowStride + c);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                if (c + cc >= cmax) break;
+                if (cc >= lim) break;
                 const float4 w0 = *reinterpret_cast<const float4*>(ws + (c + cc) * kFCols + 8 * cg);
                 const float4 w1 = *reinterpret_cast<const float4*>(ws + (c + cc) * kFCols + 8 * cg + 4);
                 const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -181,6 +202,13 @@ __global__ void __launch_bounds__(kFThreads, 3) k_fp32_tiled(const float* __rest
                     for (int v = 0; v < 8; ++v) acc[i][v] = fmaf(fv, wv[v], acc[i][v]);
                 }
             }
+        };
+        if (cmax == kFK) {
+            // a full stage: every offset is a compile-time constant
+#pragma unroll
+            for (int c = 0; c < kFK; c += 4) step4(c, 4);
+        } else {
+            for (int c = 0; c < cmax; c += 4) step4(c, cmax - c);
         }
         __syncthreads();   // the buffer is refilled by the next iteration's stage
     }
