@@ -1018,6 +1018,31 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a,
     if (!kPrefix && threadIdx.x < kTaps)
         seg[threadIdx.x] = __ldcg(a.seg_off + static_cast<int64_t>(threadIdx.x) * T + tile);
     const uint32_t uni = __ldcg(a.tile_union + tile);
+    // the row's sort key, mask and neighbours: a chain of two round trips that
+    // overlaps the prefix sums below (they do not depend on each other)
+    const int64_t s = tile * kTileRows + threadIdx.x;
+    bool err_row = false;
+    int32_t r = s < n ? static_cast<int32_t>(__ldcg(ms + s) & rmask) : -1;
+    if (r >= n) {
+        r = -1;
+        err_row = true;
+    }
+    const uint32_t m = r >= 0 ? __ldcg(a.mask + r) : 0u;
+    int32_t v[kNbrStride];
+    if (r >= 0) {
+        const int4* src = reinterpret_cast<const int4*>(a.nbr + static_cast<int64_t>(r) * kNbrStride);
+#pragma unroll
+        for (int q = 0; q < kNbrStride / 4; ++q) {
+            const int4 x = __ldcg(src + q);
+            v[4 * q] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kNbrStride; ++k) v[k] = -1;
+    }
     if (kPrefix) {
         if (threadIdx.x < kTaps) tapc[threadIdx.x] = __ldcg(a.tap_count + threadIdx.x);
         // counts of the earlier tiles: warp w sums taps w, w + 4, ...; lanes stride over the tiles
@@ -1100,28 +1125,6 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a,
             }
         }
     }
-    const int64_t s = tile * kTileRows + threadIdx.x;
-    int32_t r = s < n ? static_cast<int32_t>(__ldcg(ms + s) & rmask) : -1;
-    if (r >= n) {
-        r = -1;
-        atomicOr(&err, kStatusInternal);
-    }
-    const uint32_t m = r >= 0 ? __ldcg(a.mask + r) : 0u;
-    int32_t v[kNbrStride];
-    if (r >= 0) {
-        const int4* src = reinterpret_cast<const int4*>(a.nbr + static_cast<int64_t>(r) * kNbrStride);
-#pragma unroll
-        for (int q = 0; q < kNbrStride / 4; ++q) {
-            const int4 x = __ldcg(src + q);
-            v[4 * q] = x.x;
-            v[4 * q + 1] = x.y;
-            v[4 * q + 2] = x.z;
-            v[4 * q + 3] = x.w;
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < kNbrStride; ++k) v[k] = -1;
-    }
     uint32_t ball[kTaps];
 #pragma unroll
     for (int k = 0; k < kTaps; ++k) {
@@ -1129,6 +1132,7 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a,
         if (lane == 0) wc[warp][k] = __popc(ball[k]);
     }
     __syncthreads();
+    if (err_row) atomicOr(&err, kStatusInternal);   // (err was cleared before the barrier above)
     a.perm[s] = r;
     const uint32_t lt = lanemask_lt();
 #pragma unroll
