@@ -612,13 +612,22 @@ struct PassArgs {
     int32_t* status;
 };
 
+// Look-back window: as many partitions per step as keep the in-flight states
+// at 64 words a thread (one step covers 32 partitions of a 9-bit pass, 16 of
+// a 10-bit one).
+template <int Q>
+constexpr int kLookWindow = 64 / Q;
+
 // Partitions a CTA scans per digit in the barrier form (consecutive, one lane
 // each group), and digits a warp scans at once.
 constexpr int kScanPerLane = 8;
 constexpr int kScanDigitsPerWarp = 4;
 
-template <int WI>
+// Q: digits per thread (Q WT >= 2^width); the look-back reads the states of
+// kLookWindow<Q> partitions per step.
+template <int WI, int Q>
 __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
+    static_assert(Q >= 1 && Q <= kBinsPerThread, "digits per thread");
     // cnt[w][d]: keys of warp w with digit d, then the warp's offset within
     // the CTA's keys of digit d (stable order inside the CTA: warp, item, lane)
     __shared__ uint16_t cnt[WW][kWideBins];
@@ -649,19 +658,19 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
         const int64_t idx = base + static_cast<int64_t>(w) * 32 * WI + 32 * j + lane;
         v[j] = idx < a.n ? __ldcg(a.in + idx) : 0ull;
     }
-    // digit totals -> first output position of every digit (thread t: digits 4t .. 4t+3)
-    int32_t g[kBinsPerThread];
+    // digit totals -> first output position of every digit (thread t: digits Q t .. Q t + Q - 1)
+    int32_t g[Q];
     int32_t gs = 0;
 #pragma unroll
-    for (int q = 0; q < kBinsPerThread; ++q) {
-        const int d = kBinsPerThread * t + q;
+    for (int q = 0; q < Q; ++q) {
+        const int d = Q * t + q;
         g[q] = d < bins ? __ldcg(a.gh + d) : 0;
         gs += g[q];
     }
     int32_t run = block_exclusive(gs, wsum);   // (synchronises the CTA: cnt is cleared after it)
 #pragma unroll
-    for (int q = 0; q < kBinsPerThread; ++q) {
-        gbase[kBinsPerThread * t + q] = run;
+    for (int q = 0; q < Q; ++q) {
+        gbase[Q * t + q] = run;
         run += g[q];
     }
     const uint32_t lt = lanemask_lt();
@@ -683,11 +692,11 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
     __syncthreads();
     // per digit (thread t: digits t, t + WT, ...): offsets of the warps, the
     // CTA's count, published as this partition's aggregate
-    int qd[kBinsPerThread];
-    bool act[kBinsPerThread];
-    int32_t tot[kBinsPerThread];
+    int qd[Q];
+    bool act[Q];
+    int32_t tot[Q];
 #pragma unroll
-    for (int q = 0; q < kBinsPerThread; ++q) {
+    for (int q = 0; q < Q; ++q) {
         const int dd = t + q * WT;
         qd[q] = dd;
         act[q] = dd < bins;
@@ -702,7 +711,7 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
         }
         tot[q] = pre;
     }
-    int32_t ex[kBinsPerThread];
+    int32_t ex[Q];
     if (a.bar != nullptr) {
         // Every partition is resident.  Counts go to pc[digit][partition];
         // after a grid barrier each CTA turns the rows of its own few digits
@@ -713,7 +722,7 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
         const int64_t P = gridDim.x;
         int32_t* pc = reinterpret_cast<int32_t*>(a.look);
 #pragma unroll
-        for (int q = 0; q < kBinsPerThread; ++q)
+        for (int q = 0; q < Q; ++q)
             if (act[q]) pc[qd[q] * P + c] = tot[q];
         grid_barrier(a.bar, P, 0, a.status);
         const int per = static_cast<int>((bins + P - 1) / P);       // digits of this CTA
@@ -752,18 +761,18 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
         }
         grid_barrier(a.bar, P, 1, a.status);
 #pragma unroll
-        for (int q = 0; q < kBinsPerThread; ++q) ex[q] = act[q] ? __ldcg(pc + qd[q] * P + c) : 0;
+        for (int q = 0; q < Q; ++q) ex[q] = act[q] ? __ldcg(pc + qd[q] * P + c) : 0;
     } else {
 #pragma unroll
-        for (int q = 0; q < kBinsPerThread; ++q)
+        for (int q = 0; q < Q; ++q)
             if (act[q]) st_relaxed(a.look + c * kWideBins + qd[q], state(a.epoch, c == 0 ? kPre : kAgg, tot[q]));
-        look_back<kBinsPerThread, 8>(a.look, kWideBins, c, qd, act, a.epoch, ex, a.status);
+        look_back<Q, kLookWindow<Q>>(a.look, kWideBins, c, qd, act, a.epoch, ex, a.status);
 #pragma unroll
-        for (int q = 0; q < kBinsPerThread; ++q)
+        for (int q = 0; q < Q; ++q)
             if (act[q] && c > 0) st_relaxed(a.look + c * kWideBins + qd[q], state(a.epoch, kPre, ex[q] + tot[q]));
     }
 #pragma unroll
-    for (int q = 0; q < kBinsPerThread; ++q)
+    for (int q = 0; q < Q; ++q)
         if (act[q]) excl[qd[q]] = ex[q];
     __syncthreads();
 #pragma unroll
@@ -987,9 +996,13 @@ __global__ void __launch_bounds__(kScanThreads) k_wide_tile_scan(const WideArgs 
     }
 }
 
-// One block of 128 threads per tile: perm, the per-tap pair lists (from the
+// One CTA of kTwThreads per tile: perm, the per-tap pair lists (from the
 // (tap, tile) offsets) and the GEMM gather table (only the taps of the
-// tile's union).
+// tile's union).  Four threads share a row: thread j of the row loads the
+// 16-byte quarters j and j + 4 of its neighbour row and handles those eight
+// taps (4j .. 4j + 3 and 4j + 16 .. 4j + 19), so each thread's path is a
+// quarter of the row's and the SM holds sixteen warps per tile to overlap
+// their memory and instruction latencies.
 // With kPrefix (up to kPrefixTiles tiles) it also does the tile scan's work,
 // so that kernel is not launched: the tile's offset in tap k's list is the
 // tap's start (the exclusive sum of the per-tap totals the lookup counted)
@@ -998,97 +1011,100 @@ __global__ void __launch_bounds__(kScanThreads) k_wide_tile_scan(const WideArgs 
 // number of tiles with a larger union plus those before it with an equal
 // one.  CTA 0 writes the tap offsets and totals.
 constexpr int64_t kPrefixTiles = 1024;
+constexpr int kTwThreads = 4 * kTileRows;
+constexpr int kTwWarps = kTwThreads / 32;
+constexpr int kTwGroupTaps = 7;   // kPrefix: taps summed by each quarter of the CTA
+static_assert(kNbrStride == 32, "a neighbour row is eight 16-byte quarters");
+static_assert(4 * kTwGroupTaps >= kTaps, "four tap groups cover the taps");
+
+// The tap of slot i (0 .. 7) of row thread j (0 .. 3); taps 27 .. 31 are padding.
+__device__ __forceinline__ int tw_tap(int j, int i) { return (i < 4 ? 4 * j : 4 * j + 12) + i; }
 
 template <bool kPrefix>
-__global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a, const uint64_t* __restrict__ ms) {
-    __shared__ int32_t wc[kTileRows / 32][kTaps];
-    __shared__ int32_t seg[kTaps];   // the tile's first pair in every tap's list
+__global__ void __launch_bounds__(kTwThreads) k_wide_tile_write(const WideArgs a, const uint64_t* __restrict__ ms) {
+    __shared__ int32_t wc[kTaps][kTwWarps];   // present rows of each tap per warp, then the warp's first pair
+    __shared__ int32_t seg[kTaps];            // the tile's first pair in every tap's list
     __shared__ int32_t tapc[kTaps];
-    __shared__ int32_t red[3][kTileRows / 32];
+    __shared__ int32_t gsum[4][4][8];         // kPrefix: [tap group][warp of the group][tap of the group]
+    __shared__ int32_t red[3][kTwWarps];
     __shared__ int32_t err;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int rl = t >> 2, j = t & 3;         // row within the tile, tap phase
     const int64_t tile = blockIdx.x;
     const int64_t T = a.n_tiles, n = a.n;
     const uint64_t rmask = (uint64_t(1) << a.row_bits) - 1;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) err = 0;
+    if (t == 0) err = 0;
     pdl_wait();   // the pair offsets (kPrefix: counts) are complete
     pdl_trigger();
-    // the offsets are read once, with the row ids, not inside the per-tap loop
-    // (there they would wait one round trip per tap behind the pair stores)
-    if (!kPrefix && threadIdx.x < kTaps)
-        seg[threadIdx.x] = __ldcg(a.seg_off + static_cast<int64_t>(threadIdx.x) * T + tile);
+    // Loads are issued in the order of their dependences, so that the CTA
+    // waits two round trips in all: the row's sort key together with the
+    // counts of the earlier tiles and every tile's union, then the row's mask
+    // and neighbours (which need the row id) while the sums are reduced.
+    const int64_t s = tile * kTileRows + rl;
+    const uint64_t sv = s < n ? __ldcg(ms + s) : 0ull;
+    if (!kPrefix && t < kTaps) seg[t] = __ldcg(a.seg_off + static_cast<int64_t>(t) * T + tile);
     const uint32_t uni = __ldcg(a.tile_union + tile);
-    // the row's sort key, mask and neighbours: a chain of two round trips that
-    // overlaps the prefix sums below (they do not depend on each other)
-    const int64_t s = tile * kTileRows + threadIdx.x;
+    const int grp = t / kTileRows;   // kPrefix: this thread's tap group (taps 7 grp .. 7 grp + 6)
+    int32_t acc[8];
+    int32_t greater = 0, equal_before = 0, taps_all = 0;
+    if (kPrefix) {
+        if (t < kTaps) tapc[t] = __ldcg(a.tap_count + t);
+        // the group's taps in the tiles t % 128, t % 128 + 128, ... before this one
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0;
+#pragma unroll 4
+        for (int64_t tt = t % kTileRows; tt < tile; tt += kTileRows) {
+#pragma unroll
+            for (int i = 0; i < kTwGroupTaps; ++i) {
+                const int k = kTwGroupTaps * grp + i;
+                acc[i] += k < kTaps ? __ldcg(a.seg_off + static_cast<int64_t>(k) * T + tt) : 0;
+            }
+        }
+        // place in the tile order (tiles with a larger union, then earlier ones
+        // with an equal union), and for CTA 0 the sum of all union sizes
+        const int c = __popc(uni);
+        for (int64_t tt = t; tt < T; tt += kTwThreads) {
+            const int cu = __popc(__ldcg(a.tile_union + tt));
+            greater += cu > c ? 1 : 0;
+            equal_before += (cu == c && tt < tile) ? 1 : 0;
+            taps_all += cu;
+        }
+    }
+    // the row id out of the sort key, then its mask and this thread's two quarters of its neighbours
     bool err_row = false;
-    int32_t r = s < n ? static_cast<int32_t>(__ldcg(ms + s) & rmask) : -1;
+    int32_t r = s < n ? static_cast<int32_t>(sv & rmask) : -1;
     if (r >= n) {
         r = -1;
         err_row = true;
     }
     const uint32_t m = r >= 0 ? __ldcg(a.mask + r) : 0u;
-    int32_t v[kNbrStride];
+    int32_t v[8];
     if (r >= 0) {
         const int4* src = reinterpret_cast<const int4*>(a.nbr + static_cast<int64_t>(r) * kNbrStride);
-#pragma unroll
-        for (int q = 0; q < kNbrStride / 4; ++q) {
-            const int4 x = __ldcg(src + q);
-            v[4 * q] = x.x;
-            v[4 * q + 1] = x.y;
-            v[4 * q + 2] = x.z;
-            v[4 * q + 3] = x.w;
-        }
+        const int4 x0 = __ldcg(src + j), x1 = __ldcg(src + j + 4);
+        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+        v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
     } else {
 #pragma unroll
-        for (int k = 0; k < kNbrStride; ++k) v[k] = -1;
+        for (int i = 0; i < 8; ++i) v[i] = -1;
     }
     if (kPrefix) {
-        if (threadIdx.x < kTaps) tapc[threadIdx.x] = __ldcg(a.tap_count + threadIdx.x);
-        // counts of the earlier tiles: warp w sums taps w, w + 4, ...; lanes stride over the tiles
-        constexpr int kPerWarp = (kTaps + kTileRows / 32 - 1) / (kTileRows / 32);
-        int32_t acc[kPerWarp];
+        // the warp's sum of each of its 8 counters: three exchanges halve the
+        // counters a lane carries (4 + 2 + 1 shuffles), after which lane l holds
+        // counter l % 8 summed over the lanes l ^ {1, 2, 4}; two more add the rest
 #pragma unroll
-        for (int j = 0; j < kPerWarp; ++j) acc[j] = 0;
-        for (int64_t b0 = 0; b0 < tile; b0 += 32 * 4) {
+        for (int h = 4; h >= 1; h >>= 1) {
+            const bool upper = (lane & h) != 0;
 #pragma unroll
-            for (int j = 0; j < kPerWarp; ++j) {
-                const int k = warp + (kTileRows / 32) * j;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int64_t tt = b0 + 32 * u + lane;
-                    if (k < kTaps && tt < tile) acc[j] += __ldcg(a.seg_off + static_cast<int64_t>(k) * T + tt);
-                }
+            for (int i = 0; i < h; ++i) {
+                const int32_t send = upper ? acc[i] : acc[i + h];
+                const int32_t keep = upper ? acc[i + h] : acc[i];
+                acc[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, h);
             }
         }
-#pragma unroll
-        for (int j = 0; j < kPerWarp; ++j) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xFFFFFFFFu, acc[j], o);
-            const int k = warp + (kTileRows / 32) * j;
-            if (lane == 0 && k < kTaps) seg[k] = acc[j];
-        }
-        // place in the tile order, and (for CTA 0) the sum of all union sizes
-        const int c = __popc(uni);
-        int32_t greater = 0, equal_before = 0, taps_all = 0;
-        for (int64_t b0 = 0; b0 < T; b0 += kTileRows * 4) {
-            uint32_t u4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t tt = b0 + kTileRows * u + threadIdx.x;
-                u4[u] = tt < T ? __ldcg(a.tile_union + tt) : 0u;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t tt = b0 + kTileRows * u + threadIdx.x;
-                if (tt < T) {
-                    const int cu = __popc(u4[u]);
-                    greater += cu > c ? 1 : 0;
-                    equal_before += (cu == c && tt < tile) ? 1 : 0;
-                    taps_all += cu;
-                }
-            }
-        }
+        acc[0] += __shfl_xor_sync(0xFFFFFFFFu, acc[0], 8);
+        acc[0] += __shfl_xor_sync(0xFFFFFFFFu, acc[0], 16);
+        if (lane < 8) gsum[grp][warp & 3][lane] = acc[0];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             greater += __shfl_xor_sync(0xFFFFFFFFu, greater, o);
@@ -1100,10 +1116,50 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a,
             red[1][warp] = equal_before;
             red[2][warp] = taps_all;
         }
-        __syncthreads();
-        if (threadIdx.x == 0) {
+    }
+    // the warp's rows with each tap: lanes of one phase (lane % 4 == j) share their taps
+    const uint32_t same = 0x11111111u << j;
+    uint32_t bal[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int k = tw_tap(j, i);
+        bal[i] = __ballot_sync(0xFFFFFFFFu, k < kTaps && ((m >> k) & 1u)) & same;
+        if (lane == j && k < kTaps) wc[k][warp] = __popc(bal[i]);
+    }
+    __syncthreads();
+    // each tap's warp counts -> the warps' first pairs within the tile (two taps per warp,
+    // a 16-lane scan each)
+    if (warp < (kTaps * kTwWarps + 31) / 32) {   // whole warps: every lane takes part in the shuffles
+        const int k = t / kTwWarps, w = t % kTwWarps;
+        const int32_t x = k < kTaps ? wc[k][w] : 0;
+        int32_t inc = x;
+#pragma unroll
+        for (int o = 1; o < kTwWarps; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o, kTwWarps);
+            if (w >= o) inc += y;
+        }
+        if (k < kTaps) wc[k][w] = inc - x;
+    }
+    if (kPrefix && warp == kTwWarps - 1) {
+        // lane k: tap k's start (an exclusive scan of the tap totals) plus its count in the earlier tiles
+        const int32_t x = lane < kTaps ? tapc[lane] : 0;
+        int32_t inc = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        const int32_t start = inc - x;
+        if (lane < kTaps) {
+            const int g = lane / kTwGroupTaps, i = lane % kTwGroupTaps;
+            seg[lane] = start + gsum[g][0][i] + gsum[g][1][i] + gsum[g][2][i] + gsum[g][3][i];
+            if (tile == 0) a.tap_off[lane] = start;
+        }
+        const int32_t pairs = __shfl_sync(0xFFFFFFFFu, inc, 31);
+        if (lane == 0) {
             int32_t g2 = 0, e2 = 0, s2 = 0;
-            for (int w2 = 0; w2 < kTileRows / 32; ++w2) {
+#pragma unroll
+            for (int w2 = 0; w2 < kTwWarps; ++w2) {
                 g2 += red[0][w2];
                 e2 += red[1][w2];
                 s2 += red[2][w2];
@@ -1111,48 +1167,37 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_write(const WideArgs a,
             const int64_t at = static_cast<int64_t>(g2) + e2;
             if (at >= 0 && at < T) a.tile_order[at] = static_cast<int32_t>(tile);
             else atomicOr(&err, kStatusInternal);
-            // the tap starts; CTA 0 publishes them with the totals
-            int32_t run = 0;
-            for (int k = 0; k < kTaps; ++k) {
-                if (tile == 0) a.tap_off[k] = run;
-                seg[k] += run;
-                run += tapc[k];
-            }
             if (tile == 0) {
-                a.tap_off[kTaps] = run;
-                a.totals[0] = run;
+                a.tap_off[kTaps] = pairs;
+                a.totals[0] = pairs;
                 a.totals[1] = s2;
             }
         }
     }
-    uint32_t ball[kTaps];
-#pragma unroll
-    for (int k = 0; k < kTaps; ++k) {
-        ball[k] = __ballot_sync(0xFFFFFFFFu, (m >> k) & 1u);
-        if (lane == 0) wc[warp][k] = __popc(ball[k]);
-    }
     __syncthreads();
-    if (err_row) atomicOr(&err, kStatusInternal);   // (err was cleared before the barrier above)
-    a.perm[s] = r;
+    if (j == 0) {
+        if (err_row) atomicOr(&err, kStatusInternal);
+        a.perm[s] = r;
+    }
     const uint32_t lt = lanemask_lt();
 #pragma unroll
-    for (int k = 0; k < kTaps; ++k) {
-        if (!((uni >> k) & 1u)) continue;
+    for (int i = 0; i < 8; ++i) {
+        const int k = tw_tap(j, i);
+        if (k >= kTaps || !((uni >> k) & 1u)) continue;
         const bool present = (m >> k) & 1u;
         if (present) {
-            int64_t off = static_cast<int64_t>(seg[k]) + __popc(ball[k] & lt);
-            for (int q = 0; q < warp; ++q) off += wc[q][k];
+            const int64_t off = static_cast<int64_t>(seg[k]) + wc[k][warp] + __popc(bal[i] & lt);
             if (off >= 0 && off < kTaps * n) {
-                a.in_rows[off] = v[k];
+                a.in_rows[off] = v[i];
                 a.out_rows[off] = r;
             } else {
                 atomicOr(&err, kStatusInternal);
             }
         }
-        a.gtab[static_cast<int64_t>(k) * a.n_pad + s] = present ? v[k] : -1;
+        a.gtab[static_cast<int64_t>(k) * a.n_pad + s] = present ? v[i] : -1;
     }
     __syncthreads();
-    if (threadIdx.x == 0 && err) atomicOr(a.status, err);
+    if (t == 0 && err) atomicOr(a.status, err);
 }
 
 // The two bounded waits of the sort passes, each against a state that nothing
@@ -1248,21 +1293,26 @@ namespace {
 // decoupled look-back.
 int launch_wide_pass(const uint64_t* in, uint64_t* out, int64_t n, int shift, int width, const int32_t* gh,
                      uint64_t* look, int32_t* tickets, int ticket, int32_t* status, cudaStream_t s, bool pdl = true) {
-    static int64_t cap_pass[kMaxDevices][2] = {};
+    // resident CTAs of each form: [device][keys per CTA: 1024, 2048][digits per thread: 2, 4]
+    static int64_t cap_pass[kMaxDevices][2][2] = {};
     int dev = 0;
     SPCONV_CHECK_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return SPCONV_ERR_UNSUPPORTED;
-    if (cap_pass[dev][0] == 0) {
+    if (width < 1 || width > kDigitBitsWide) return SPCONV_ERR_UNSUPPORTED;
+    if (cap_pass[dev][0][0] == 0) {
         int sms = 0;
         SPCONV_CHECK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        cap_pass[dev][0] = resident_ctas(k_wide_pass<WI>, WT, sms);
-        cap_pass[dev][1] = resident_ctas(k_wide_pass<2 * WI>, WT, sms);
+        cap_pass[dev][0][0] = resident_ctas(k_wide_pass<WI, 2>, WT, sms);
+        cap_pass[dev][0][1] = resident_ctas(k_wide_pass<WI, 4>, WT, sms);
+        cap_pass[dev][1][0] = resident_ctas(k_wide_pass<2 * WI, 2>, WT, sms);
+        cap_pass[dev][1][1] = resident_ctas(k_wide_pass<2 * WI, 4>, WT, sms);
     }
     const bool big_pass = n > kBigPassRows;
+    const bool narrow = (1 << width) <= 2 * WT;   // two digits per thread cover the digit values
     const int64_t keys_per_cta = big_pass ? 2 * kWideKeysPerCta : kWideKeysPerCta;
     const int64_t parts = (n + keys_per_cta - 1) / keys_per_cta;
     if (parts > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
-    const bool pass_ticket = parts > cap_pass[dev][big_pass ? 1 : 0];
+    const bool pass_ticket = parts > cap_pass[dev][big_pass ? 1 : 0][narrow ? 0 : 1];
     PassArgs pa;
     pa.in = in;
     pa.out = out;
@@ -1281,8 +1331,12 @@ int launch_wide_pass(const uint64_t* in, uint64_t* out, int64_t n, int shift, in
                          parts <= 32 * kScanPerLane;
     pa.bar = barrier ? tickets + kWideTickets + ticket * kWideBarrierInts : nullptr;
     pa.status = status;
-    return big_pass ? launch_pdl(k_wide_pass<2 * WI>, static_cast<unsigned>(parts), WT, s, pdl, pa)
-                    : launch_pdl(k_wide_pass<WI>, static_cast<unsigned>(parts), WT, s, pdl, pa);
+    const unsigned grid = static_cast<unsigned>(parts);
+    if (big_pass)
+        return narrow ? launch_pdl(k_wide_pass<2 * WI, 2>, grid, WT, s, pdl, pa)
+                      : launch_pdl(k_wide_pass<2 * WI, 4>, grid, WT, s, pdl, pa);
+    return narrow ? launch_pdl(k_wide_pass<WI, 2>, grid, WT, s, pdl, pa)
+                  : launch_pdl(k_wide_pass<WI, 4>, grid, WT, s, pdl, pa);
 }
 
 }  // namespace
@@ -1377,10 +1431,10 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     const unsigned tiles = static_cast<unsigned>(a.n_tiles);
     SPCONV_CHECK(launch_pdl(k_wide_tile_count, tiles, kTileRows, s, true, a, ms));
     if (a.n_tiles <= kPrefixTiles) {
-        SPCONV_CHECK(launch_pdl(k_wide_tile_write<true>, tiles, kTileRows, s, true, a, ms));
+        SPCONV_CHECK(launch_pdl(k_wide_tile_write<true>, tiles, kTwThreads, s, true, a, ms));
     } else {
         SPCONV_CHECK(launch_pdl(k_wide_tile_scan, 1u, static_cast<unsigned>(kScanThreads), s, true, a));
-        SPCONV_CHECK(launch_pdl(k_wide_tile_write<false>, tiles, kTileRows, s, true, a, ms));
+        SPCONV_CHECK(launch_pdl(k_wide_tile_write<false>, tiles, kTwThreads, s, true, a, ms));
     }
     return SPCONV_OK;
 }
