@@ -367,7 +367,9 @@ int32_t spconv_last_launch_count(void);
  *   which     0: the decoupled look-back of a sort pass, waiting for a
  *             predecessor partition whose state stays unpublished;
  *             1: the grid barrier of a two-CTA grid of which only one CTA
- *             runs.
+ *             runs;
+ *             2: the flag wait of a pass that sums its predecessors'
+ *             counts, on a flag that stays unset.
  *   limit_ns  the wait's limit, 1 ms .. 100 ms.
  *   stream    CUDA stream; the call allocates a few hundred bytes
  *             stream-ordered, synchronises the stream and frees them.

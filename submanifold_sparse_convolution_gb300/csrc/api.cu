@@ -463,7 +463,7 @@ int32_t spconv_last_launch_count(void) { return g_launches; }
 
 int spconv_selftest_wait_timeout(int32_t which, int64_t limit_ns, void* stream) {
     reset_launch_count();
-    if ((which != 0 && which != 1) || limit_ns < 1000000 || limit_ns > 100000000) return SPCONV_ERR_INVALID_ARG;
+    if (which < 0 || which > 2 || limit_ns < 1000000 || limit_ns > 100000000) return SPCONV_ERR_INVALID_ARG;
     return wait_probe(which, static_cast<uint64_t>(limit_ns), static_cast<cudaStream_t>(stream));
 }
 

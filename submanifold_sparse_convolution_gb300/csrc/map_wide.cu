@@ -34,6 +34,7 @@
 // already running.  Every wait is bounded in time.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 
@@ -609,25 +610,116 @@ struct PassArgs {
     uint32_t epoch;
     int32_t* ticket;       // partition counter, or null: partition = blockIdx.x (the whole grid is resident)
     int32_t* bar;          // non-null: prefixes by two grid barriers instead of look-back (see below)
+    uint64_t* words;       // non-null: prefixes and digit totals from every partition's packed counts
     int32_t* status;
+    // the first pass of the mask sort (kMask): its values are made from the
+    // rows' masks, (key << row_bits | row), the key the mask in the tap order
+    const uint32_t* mask;
+    const int32_t* tap_count;
+    int calibrated, row_bits;
 };
 
-// Look-back window: as many partitions per step as keep the in-flight states
-// at 64 words a thread (one step covers 32 partitions of a 9-bit pass, 16 of
-// a 10-bit one).
+// Partitions the look-back reads per step.
+constexpr int kLookWindow = 8;
+
+// The all-partition form (every partition resident, at most kSumFormParts):
+// each partition publishes its digit counts as self-validating 64-bit words
+// -- a tag in the high half (the pass's epoch with bit 31 set, which no count
+// and no older state word has there) and two 16-bit counts in the low half,
+// digits Q t + 2h and Q t + 2h + 1 in word h of thread t -- and reads every
+// partition's words until all carry the tag.  No fence, flag or chain of
+// prefixes: one store, then one round of loads.  Low halves are added as
+// packed pairs over chunks of at most kSumChunk<Q> partitions (31 x 2048 <
+// 2^16) before they are widened.
+constexpr int64_t kSumFormParts = 64;
 template <int Q>
-constexpr int kLookWindow = 64 / Q;
+constexpr int kSumChunk = Q == 2 ? 31 : 15;
+
+__device__ __forceinline__ uint64_t word_tag(uint32_t epoch) {
+    return static_cast<uint64_t>(0x80000000u | (epoch & 0x7FFFFFFFu)) << 32;
+}
+
+// Partition c of P publishes its counts tot and gathers, per digit, the count
+// over the partitions before it (ex) and over all of them (all).  Every
+// thread of the CTA calls it.  A partition that does not publish within the
+// wait limit records a timeout (the sums are then wrong but the kernel ends).
+template <int Q>
+__device__ void exchange_counts(uint64_t* words, int64_t P, int64_t c, uint32_t epoch, const int32_t (&tot)[Q],
+                                int32_t (&ex)[Q], int32_t (&all)[Q], int32_t* status,
+                                uint64_t limit_ns = ptx::kWaitLimitNs) {
+    constexpr int NW = Q / 2;
+    constexpr int CH = kSumChunk<Q>;
+    const int t = threadIdx.x;
+    const uint64_t tag = word_tag(epoch);
+#pragma unroll
+    for (int h = 0; h < NW; ++h) {
+        const uint32_t lo = (static_cast<uint32_t>(tot[2 * h]) & 0xFFFFu) |
+                            ((static_cast<uint32_t>(tot[2 * h + 1]) & 0xFFFFu) << 16);
+        st_relaxed(words + (c * NW + h) * WT + t, tag | lo);
+    }
+#pragma unroll
+    for (int q = 0; q < Q; ++q) ex[q] = all[q] = 0;
+    uint64_t t0 = 0;
+    bool gave_up = false;
+    for (int64_t p0 = 0; p0 < P; p0 += CH) {
+        const int np = P - p0 < CH ? static_cast<int>(P - p0) : CH;
+        uint32_t need = gave_up ? 0u : (1u << np) - 1u;
+        uint32_t run_all[NW], run_ex[NW];
+#pragma unroll
+        for (int h = 0; h < NW; ++h) run_all[h] = run_ex[h] = 0;
+        while (need != 0u) {
+            uint64_t x[CH][NW];
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+#pragma unroll
+                for (int h = 0; h < NW; ++h)
+                    x[i][h] = ((need >> i) & 1u) ? ld_relaxed(words + ((p0 + i) * NW + h) * WT + t) : 0ull;
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+                if (!((need >> i) & 1u)) continue;
+                bool ok = true;
+#pragma unroll
+                for (int h = 0; h < NW; ++h) ok &= (x[i][h] & 0xFFFFFFFF00000000ull) == tag;
+                if (!ok) continue;
+                need &= ~(1u << i);
+#pragma unroll
+                for (int h = 0; h < NW; ++h) {
+                    const uint32_t lo = static_cast<uint32_t>(x[i][h]);
+                    run_all[h] += lo;
+                    run_ex[h] += p0 + i < c ? lo : 0u;
+                }
+            }
+            if (need == 0u) break;
+            if (t0 == 0) {
+                t0 = ptx::globaltimer();
+            } else if (ptx::globaltimer() - t0 > limit_ns) {
+                atomicOr(status, kStatusTimeout);
+                gave_up = true;
+                break;
+            }
+            __nanosleep(64);
+        }
+#pragma unroll
+        for (int h = 0; h < NW; ++h) {
+            all[2 * h] += static_cast<int32_t>(run_all[h] & 0xFFFFu);
+            all[2 * h + 1] += static_cast<int32_t>(run_all[h] >> 16);
+            ex[2 * h] += static_cast<int32_t>(run_ex[h] & 0xFFFFu);
+            ex[2 * h + 1] += static_cast<int32_t>(run_ex[h] >> 16);
+        }
+    }
+}
 
 // Partitions a CTA scans per digit in the barrier form (consecutive, one lane
 // each group), and digits a warp scans at once.
 constexpr int kScanPerLane = 8;
 constexpr int kScanDigitsPerWarp = 4;
 
-// Q: digits per thread (Q WT >= 2^width); the look-back reads the states of
-// kLookWindow<Q> partitions per step.
-template <int WI, int Q>
+// Q: digits per thread (Q WT >= 2^width), consecutive digits Q t .. Q t + Q - 1.
+// kMask: the first pass of the mask sort, which makes its values from the
+// masks (only with the all-partition form, which needs no digit totals).
+template <int WI, int Q, bool kMask = false>
 __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
-    static_assert(Q >= 1 && Q <= kBinsPerThread, "digits per thread");
+    static_assert(Q == 2 || Q == 4, "digits per thread");
     // cnt[w][d]: keys of warp w with digit d, then the warp's offset within
     // the CTA's keys of digit d (stable order inside the CTA: warp, item, lane)
     __shared__ uint16_t cnt[WW][kWideBins];
@@ -635,6 +727,9 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
     __shared__ int32_t excl[kWideBins];    // keys of each digit in the partitions before this one
     __shared__ int32_t wsum[WW];
     __shared__ int32_t part_sh, err;
+    // kMask: the taps' key bits and, per byte of a mask, the key bits it sets
+    __shared__ int32_t mtaps[kMask ? kTaps : 1], mpos[kMask ? kTaps : 1];
+    __shared__ uint32_t mtab[kMask ? 4 : 1][kMask ? 256 : 1];
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const int bins = 1 << a.width;
     const uint64_t dmask = static_cast<uint64_t>(bins - 1);
@@ -653,25 +748,76 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
     const int64_t base = c * WT * WI;
     uint64_t v[WI];
     int d[WI], rk[WI];
+    if (kMask) {
+        // the masks and tap counts; the key of a mask puts tap k at bit pos[k]
+        // (calibrated: taps by descending count, ties by index), assembled from
+        // four byte tables so that a key costs four shared loads
+        uint32_t mk[WI];
 #pragma unroll
-    for (int j = 0; j < WI; ++j) {
-        const int64_t idx = base + static_cast<int64_t>(w) * 32 * WI + 32 * j + lane;
-        v[j] = idx < a.n ? __ldcg(a.in + idx) : 0ull;
+        for (int j = 0; j < WI; ++j) {
+            const int64_t idx = base + static_cast<int64_t>(w) * 32 * WI + 32 * j + lane;
+            mk[j] = idx < a.n ? __ldcg(a.mask + idx) : 0u;
+        }
+        if (t < kTaps) mtaps[t] = __ldcg(a.tap_count + t);
+        __syncthreads();
+        if (t < kTaps) {
+            int32_t rank = t;
+            if (a.calibrated) {
+                const int32_t ck = mtaps[t];
+                rank = 0;
+                for (int jj = 0; jj < kTaps; ++jj) {
+                    const int32_t cj = mtaps[jj];
+                    rank += (cj > ck || (cj == ck && jj < t)) ? 1 : 0;
+                }
+            }
+            mpos[t] = rank;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t x = 0;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const int k = 8 * i + b;
+                if (k < kTaps && ((t >> b) & 1)) x |= 1u << mpos[k];
+            }
+            mtab[i][t] = x;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < WI; ++j) {
+            const int64_t idx = base + static_cast<int64_t>(w) * 32 * WI + 32 * j + lane;
+            const uint32_t m = mk[j];
+            const uint32_t key = mtab[0][m & 255u] | mtab[1][(m >> 8) & 255u] | mtab[2][(m >> 16) & 255u] |
+                                 mtab[3][m >> 24];
+            v[j] = idx < a.n ? (static_cast<uint64_t>(key) << a.row_bits) | static_cast<uint64_t>(idx) : 0ull;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < WI; ++j) {
+            const int64_t idx = base + static_cast<int64_t>(w) * 32 * WI + 32 * j + lane;
+            v[j] = idx < a.n ? __ldcg(a.in + idx) : 0ull;
+        }
     }
-    // digit totals -> first output position of every digit (thread t: digits Q t .. Q t + Q - 1)
-    int32_t g[Q];
-    int32_t gs = 0;
+    // digit totals -> first output position of every digit (thread t: digits Q t .. Q t + Q - 1);
+    // the all-partition form takes them from the partitions' published counts instead
+    if (a.words == nullptr) {
+        int32_t g[Q];
+        int32_t gs = 0;
 #pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        const int d = Q * t + q;
-        g[q] = d < bins ? __ldcg(a.gh + d) : 0;
-        gs += g[q];
-    }
-    int32_t run = block_exclusive(gs, wsum);   // (synchronises the CTA: cnt is cleared after it)
+        for (int q = 0; q < Q; ++q) {
+            const int d = Q * t + q;
+            g[q] = d < bins ? __ldcg(a.gh + d) : 0;
+            gs += g[q];
+        }
+        int32_t run = block_exclusive(gs, wsum);   // (synchronises the CTA: cnt is cleared after it)
 #pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        gbase[Q * t + q] = run;
-        run += g[q];
+        for (int q = 0; q < Q; ++q) {
+            gbase[Q * t + q] = run;
+            run += g[q];
+        }
+    } else {
+        __syncthreads();   // cnt is cleared
     }
     const uint32_t lt = lanemask_lt();
 #pragma unroll
@@ -690,14 +836,14 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
         __syncwarp();
     }
     __syncthreads();
-    // per digit (thread t: digits t, t + WT, ...): offsets of the warps, the
-    // CTA's count, published as this partition's aggregate
+    // per digit (thread t: digits Q t .. Q t + Q - 1): offsets of the warps,
+    // the CTA's count, published as this partition's aggregate
     int qd[Q];
     bool act[Q];
     int32_t tot[Q];
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
-        const int dd = t + q * WT;
+        const int dd = Q * t + q;
         qd[q] = dd;
         act[q] = dd < bins;
         int32_t x[WW];
@@ -762,11 +908,27 @@ __global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
         grid_barrier(a.bar, P, 1, a.status);
 #pragma unroll
         for (int q = 0; q < Q; ++q) ex[q] = act[q] ? __ldcg(pc + qd[q] * P + c) : 0;
+    } else if (a.words != nullptr) {
+        // Every partition is resident and there are at most kSumFormParts:
+        // each publishes its counts and reads every partition's, which gives
+        // both its prefix and the digit totals (the first output position of
+        // every digit, an exclusive scan in digit order).
+        int32_t all[Q];
+        exchange_counts<Q>(a.words, gridDim.x, c, a.epoch, tot, ex, all, a.status);
+        int32_t gs = 0;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) gs += all[q];
+        int32_t run = block_exclusive(gs, wsum);
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            gbase[Q * t + q] = run;
+            run += all[q];
+        }
     } else {
 #pragma unroll
         for (int q = 0; q < Q; ++q)
             if (act[q]) st_relaxed(a.look + c * kWideBins + qd[q], state(a.epoch, c == 0 ? kPre : kAgg, tot[q]));
-        look_back<Q, kLookWindow<Q>>(a.look, kWideBins, c, qd, act, a.epoch, ex, a.status);
+        look_back<Q, kLookWindow>(a.look, kWideBins, c, qd, act, a.epoch, ex, a.status);
 #pragma unroll
         for (int q = 0; q < Q; ++q)
             if (act[q] && c > 0) st_relaxed(a.look + c * kWideBins + qd[q], state(a.epoch, kPre, ex[q] + tot[q]));
@@ -1200,11 +1362,13 @@ __global__ void __launch_bounds__(kTwThreads) k_wide_tile_write(const WideArgs a
     if (t == 0 && err) atomicOr(a.status, err);
 }
 
-// The two bounded waits of the sort passes, each against a state that nothing
-// will ever publish, with a short limit: which = 0, the look-back of
+// The three bounded waits of the sort passes, each against a state that
+// nothing will ever publish, with a short limit: which = 0, the look-back of
 // partition 1 over partition 0 (whose state words stay zero); which = 1, the
-// grid barrier of a two-CTA grid entered by the only CTA launched.  Both must
-// give up after limit_ns and set kStatusTimeout; nothing else is touched.
+// grid barrier of a two-CTA grid entered by the only CTA launched; which = 2,
+// the count exchange of the all-partition form (a partition that never publishes).
+// Each must give up after limit_ns and set kStatusTimeout; nothing else is
+// touched.
 __global__ void __launch_bounds__(WT) k_wait_probe(int which, const uint64_t* look, int32_t* bar, int32_t* status,
                                                    uint64_t limit_ns) {
     if (which == 0) {
@@ -1212,8 +1376,13 @@ __global__ void __launch_bounds__(WT) k_wait_probe(int which, const uint64_t* lo
         const bool act[1] = {true};
         int32_t ex[1];
         look_back<1, 8>(look, kWideBins, 1, q, act, 1u, ex, status, limit_ns);
-    } else {
+    } else if (which == 1) {
         grid_barrier(bar, 2, 0, status, limit_ns);
+    } else {
+        // partition 1 of 2: partition 0's words stay zero
+        const int32_t tot[2] = {0, 0};
+        int32_t ex[2], all[2];
+        exchange_counts<2>(const_cast<uint64_t*>(look), 2, 1, 1u, tot, ex, all, status, limit_ns);
     }
 }
 
@@ -1291,8 +1460,13 @@ namespace {
 // the ticket counter tickets[ticket]; offsets by the two-barrier form when
 // every partition is resident and the digits spread over them, else by
 // decoupled look-back.
-int launch_wide_pass(const uint64_t* in, uint64_t* out, int64_t n, int shift, int width, const int32_t* gh,
-                     uint64_t* look, int32_t* tickets, int ticket, int32_t* status, cudaStream_t s, bool pdl = true) {
+// The form a pass over n values with digits of `width` bits takes on this device.
+struct PassPlan {
+    bool big, narrow, ticket, barrier, all;
+    int64_t parts;
+};
+
+int plan_wide_pass(int64_t n, int width, PassPlan* pl) {
     // resident CTAs of each form: [device][keys per CTA: 1024, 2048][digits per thread: 2, 4]
     static int64_t cap_pass[kMaxDevices][2][2] = {};
     int dev = 0;
@@ -1302,18 +1476,41 @@ int launch_wide_pass(const uint64_t* in, uint64_t* out, int64_t n, int shift, in
     if (cap_pass[dev][0][0] == 0) {
         int sms = 0;
         SPCONV_CHECK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        cap_pass[dev][0][0] = resident_ctas(k_wide_pass<WI, 2>, WT, sms);
+        // (the mask form of the first mask pass has the resources of its plain form or fewer CTAs)
+        const int64_t m0 = resident_ctas(k_wide_pass<WI, 2, true>, WT, sms);
+        const int64_t m1 = resident_ctas(k_wide_pass<2 * WI, 2, true>, WT, sms);
+        cap_pass[dev][0][0] = std::min(resident_ctas(k_wide_pass<WI, 2>, WT, sms), m0);
         cap_pass[dev][0][1] = resident_ctas(k_wide_pass<WI, 4>, WT, sms);
-        cap_pass[dev][1][0] = resident_ctas(k_wide_pass<2 * WI, 2>, WT, sms);
+        cap_pass[dev][1][0] = std::min(resident_ctas(k_wide_pass<2 * WI, 2>, WT, sms), m1);
         cap_pass[dev][1][1] = resident_ctas(k_wide_pass<2 * WI, 4>, WT, sms);
     }
-    const bool big_pass = n > kBigPassRows;
-    const bool narrow = (1 << width) <= 2 * WT;   // two digits per thread cover the digit values
-    const int64_t keys_per_cta = big_pass ? 2 * kWideKeysPerCta : kWideKeysPerCta;
-    const int64_t parts = (n + keys_per_cta - 1) / keys_per_cta;
-    if (parts > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
-    const bool pass_ticket = parts > cap_pass[dev][big_pass ? 1 : 0][narrow ? 0 : 1];
-    PassArgs pa;
+    pl->big = n > kBigPassRows;
+    pl->narrow = (1 << width) <= 2 * WT;   // two digits per thread cover the digit values
+    const int64_t keys_per_cta = pl->big ? 2 * kWideKeysPerCta : kWideKeysPerCta;
+    pl->parts = (n + keys_per_cta - 1) / keys_per_cta;
+    if (pl->parts > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
+    pl->ticket = pl->parts > cap_pass[dev][pl->big ? 1 : 0][pl->narrow ? 0 : 1];
+    // the barrier form when every partition is resident, each warp scans at
+    // most kScanDigitsPerWarp digits and each lane at most kScanPerLane partitions
+    const int64_t bins = int64_t(1) << width;
+    pl->barrier = !pl->ticket && pl->parts > kSumFormParts && bins <= pl->parts * WW * kScanDigitsPerWarp &&
+                  pl->parts <= 32 * kScanPerLane;
+    // a few resident partitions: each reads every partition's packed counts
+    // (parts x Q / 2 x WT words of the look-back buffer)
+    pl->all = !pl->ticket && !pl->barrier && pl->parts <= kSumFormParts;
+    return SPCONV_OK;
+}
+
+// One pass of the stable sort on stream s, in the form plan_wide_pass gives.
+// mask_src: the first pass of the mask sort, its values made from the masks
+// (the all-partition form and 9-bit digits only).
+int launch_wide_pass(const uint64_t* in, uint64_t* out, int64_t n, int shift, int width, const int32_t* gh,
+                     uint64_t* look, int32_t* tickets, int ticket, int32_t* status, cudaStream_t s, bool pdl = true,
+                     const WideArgs* mask_src = nullptr) {
+    PassPlan pl;
+    SPCONV_CHECK(plan_wide_pass(n, width, &pl));
+    if (mask_src && (!pl.all || !pl.narrow)) return SPCONV_ERR_INTERNAL;
+    PassArgs pa = {};
     pa.in = in;
     pa.out = out;
     pa.n = n;
@@ -1322,21 +1519,25 @@ int launch_wide_pass(const uint64_t* in, uint64_t* out, int64_t n, int shift, in
     pa.gh = gh;
     pa.look = look;
     pa.epoch = next_epoch();
-    pa.ticket = pass_ticket ? tickets + ticket : nullptr;
-    // the barrier form when every partition is resident, each warp scans at
-    // most kScanDigitsPerWarp digits and each lane at most kScanPerLane partitions
-    // (below ~64 partitions a windowed look-back chain is as short and has no barrier)
-    const int64_t bins = int64_t(1) << width;
-    const bool barrier = !pass_ticket && parts > 64 && bins <= parts * WW * kScanDigitsPerWarp &&
-                         parts <= 32 * kScanPerLane;
-    pa.bar = barrier ? tickets + kWideTickets + ticket * kWideBarrierInts : nullptr;
+    pa.ticket = pl.ticket ? tickets + ticket : nullptr;
+    pa.bar = pl.barrier ? tickets + kWideTickets + ticket * kWideBarrierInts : nullptr;
+    pa.words = pl.all ? look : nullptr;
     pa.status = status;
-    const unsigned grid = static_cast<unsigned>(parts);
-    if (big_pass)
-        return narrow ? launch_pdl(k_wide_pass<2 * WI, 2>, grid, WT, s, pdl, pa)
-                      : launch_pdl(k_wide_pass<2 * WI, 4>, grid, WT, s, pdl, pa);
-    return narrow ? launch_pdl(k_wide_pass<WI, 2>, grid, WT, s, pdl, pa)
-                  : launch_pdl(k_wide_pass<WI, 4>, grid, WT, s, pdl, pa);
+    if (mask_src) {
+        pa.mask = mask_src->mask;
+        pa.tap_count = mask_src->tap_count;
+        pa.calibrated = mask_src->calibrated;
+        pa.row_bits = mask_src->row_bits;
+    }
+    const unsigned grid = static_cast<unsigned>(pl.parts);
+    if (mask_src)
+        return pl.big ? launch_pdl(k_wide_pass<2 * WI, 2, true>, grid, WT, s, pdl, pa)
+                      : launch_pdl(k_wide_pass<WI, 2, true>, grid, WT, s, pdl, pa);
+    if (pl.big)
+        return pl.narrow ? launch_pdl(k_wide_pass<2 * WI, 2>, grid, WT, s, pdl, pa)
+                         : launch_pdl(k_wide_pass<2 * WI, 4>, grid, WT, s, pdl, pa);
+    return pl.narrow ? launch_pdl(k_wide_pass<WI, 2>, grid, WT, s, pdl, pa)
+                     : launch_pdl(k_wide_pass<WI, 4>, grid, WT, s, pdl, pa);
 }
 
 }  // namespace
@@ -1375,8 +1576,8 @@ int wide_sort(uint64_t* a, uint64_t* b, int64_t n, const WideDigits& d, const in
 
 int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     const int64_t n = a.n;
-    // keys per sort CTA: 1024, or 2048 above kBigPassRows (fewer partitions to
-    // look back over: 94k rows 97 -> 90 us per build, 32k rows 57.6 vs 58.6)
+    // keys per sort CTA: 1024, or 2048 above kBigPassRows (fewer partitions
+    // whose counts every partition reads: 32k rows 52.9 -> 50.8 us per build)
     const bool big_pass = n > kBigPassRows;
     const int64_t keys_per_cta = big_pass ? 2 * kWideKeysPerCta : kWideKeysPerCta;
     const unsigned parts = static_cast<unsigned>((n + keys_per_cta - 1) / keys_per_cta);
@@ -1422,9 +1623,20 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
         SPCONV_CHECK(launch_pdl(k_wide_grid_scatter, row_blocks, WT, s, true, a));
         SPCONV_CHECK(launch_pdl(k_wide_grid_lookup, row_blocks, WT, s, true, a));
     }
-    SPCONV_CHECK(few ? launch_pdl(k_wide_mask_keys<1>, key_blocks, WT, s, true, a)
-                     : launch_pdl(k_wide_mask_keys<4>, key_blocks, WT, s, true, a));
-    for (int p = 0; p < kWideMaskPasses; ++p)
+    // the mask sort: when its passes read every partition's counts (few rows),
+    // the first pass makes the keys from the masks itself; otherwise a kernel
+    // makes them with the digit totals the other forms need
+    PassPlan mp;
+    SPCONV_CHECK(plan_wide_pass(n, kMaskWidth, &mp));
+    if (mp.all) {
+        SPCONV_CHECK(launch_wide_pass(nullptr, a.vb, n, a.row_bits, kMaskWidth, nullptr, a.look, a.tickets,
+                                      kWideKeyPassesMax, a.status, s, true, &a));
+    } else {
+        SPCONV_CHECK(few ? launch_pdl(k_wide_mask_keys<1>, key_blocks, WT, s, true, a)
+                         : launch_pdl(k_wide_mask_keys<4>, key_blocks, WT, s, true, a));
+        SPCONV_CHECK(pass(a.va, a.vb, a.row_bits, kMaskWidth, a.gh + kWideKeyPassesMax * kWideBins, kWideKeyPassesMax));
+    }
+    for (int p = 1; p < kWideMaskPasses; ++p)
         SPCONV_CHECK(pass((p & 1) ? a.vb : a.va, (p & 1) ? a.va : a.vb, a.row_bits + kMaskWidth * p, kMaskWidth,
                           a.gh + (kWideKeyPassesMax + p) * kWideBins, kWideKeyPassesMax + p));
     const uint64_t* ms = (kWideMaskPasses & 1) ? a.vb : a.va;

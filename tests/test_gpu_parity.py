@@ -902,18 +902,18 @@ def test_launch_count_reported():
     assert sc.last_launch_count() == 3          # weight pack + GEMM + bf16 rounding pass
 
 
-@pytest.mark.parametrize("which", [0, 1])
+@pytest.mark.parametrize("which", [0, 1, 2])
 def test_bounded_wait_times_out_and_gpu_keeps_working(which):
-    """A sort pass's look-back (0) or grid barrier (1) waits on a state that nothing publishes,
-    with a 50 ms limit: it gives up, the call reports SPCONV_ERR_TIMEOUT, and the context still
-    builds and convolves correctly afterwards."""
+    """A sort pass's look-back (0), grid barrier (1) or predecessor flag (2) waits on a state
+    that nothing publishes, with a 50 ms limit: it gives up, the call reports
+    SPCONV_ERR_TIMEOUT, and the context still builds and convolves correctly afterwards."""
     import time
     lib = sc.library()
     stream = torch.cuda.current_stream().cuda_stream
     t = time.perf_counter()
     assert lib.spconv_selftest_wait_timeout(which, 50_000_000, stream) == -8
     assert time.perf_counter() - t < 10.0
-    assert lib.spconv_selftest_wait_timeout(2, 50_000_000, stream) == -1
+    assert lib.spconv_selftest_wait_timeout(3, 50_000_000, stream) == -1
     assert lib.spconv_selftest_wait_timeout(which, 10, stream) == -1
     wl = S.random_cloud(881, 3000, shape=(16, 16, 16), c_in=64, c_out=64)
     m = build(wl)
