@@ -717,8 +717,9 @@ constexpr int kScanDigitsPerWarp = 4;
 // Q: digits per thread (Q WT >= 2^width), consecutive digits Q t .. Q t + Q - 1.
 // kMask: the first pass of the mask sort, which makes its values from the
 // masks (only with the all-partition form, which needs no digit totals).
+// (2048 keys of 10-bit digits need more registers than two CTAs per SM allow)
 template <int WI, int Q, bool kMask = false>
-__global__ void __launch_bounds__(WT) k_wide_pass(const PassArgs a) {
+__global__ void __launch_bounds__(WT, WI * Q > 16 ? 1 : 2) k_wide_pass(const PassArgs a) {
     static_assert(Q == 2 || Q == 4, "digits per thread");
     // cnt[w][d]: keys of warp w with digit d, then the warp's offset within
     // the CTA's keys of digit d (stable order inside the CTA: warp, item, lane)
