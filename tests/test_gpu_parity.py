@@ -881,18 +881,17 @@ def test_launch_count_reported():
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="sorted", pipeline="fused")
     assert sc.last_launch_count() == 4                # cluster sort, search, cluster rest, write
     # (up to 1024 tiles the tile write also does the tile scan's work: no scan launch)
+    # (up to 64 sort partitions the first mask pass makes the mask keys itself)
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="dense", pipeline="wide")
-    assert sc.last_launch_count() == 9                # clear, scatter, lookup, mask keys, 3 passes,
-                                                      # tile count/write
+    assert sc.last_launch_count() == 8                # clear, scatter, lookup, 3 passes, tile count/write
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="sorted", pipeline="wide")
-    assert sc.last_launch_count() == 11               # clear, keys, 2 passes (15-bit keys), search, mask keys,
+    assert sc.last_launch_count() == 10               # clear, keys, 2 passes (15-bit keys), search,
                                                       # 3 passes, tile count/write
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, mapper="hash", pipeline="wide")
-    assert sc.last_launch_count() == 9                # clear, insert, lookup, mask keys, 3 passes,
-                                                      # tile count/write
+    assert sc.last_launch_count() == 8                # clear, insert, lookup, 3 passes, tile count/write
     big = S.random_cloud(52, 140000, shape=(100, 100, 40))
     sc.build_map(big.coords.cuda(), big.spatial_shape, 1, mapper="hash", pipeline="wide")
-    assert sc.last_launch_count() == 10               # 1094 tiles: the tile scan runs
+    assert sc.last_launch_count() == 10               # 69 partitions: mask keys; 1094 tiles: the tile scan
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, pipeline="multi")
     assert sc.last_launch_count() > 5
     sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
