@@ -630,11 +630,11 @@ constexpr int kLookWindow = 8;
 // digits Q t + 2h and Q t + 2h + 1 in word h of thread t -- and reads every
 // partition's words until all carry the tag.  No fence, flag or chain of
 // prefixes: one store, then one round of loads.  Low halves are added as
-// packed pairs over chunks of at most kSumChunk<Q> partitions (31 x 2048 <
-// 2^16) before they are widened.
+// packed pairs over chunks of at most kSumChunk<WI, Q> partitions (chunk x
+// keys per partition < 2^16) before they are widened.
 constexpr int64_t kSumFormParts = 64;
-template <int Q>
-constexpr int kSumChunk = Q == 2 ? 31 : 15;
+template <int WI, int Q>
+constexpr int kSumChunk = (Q == 2 ? 31 : 15) < 65535 / (WT * WI) ? (Q == 2 ? 31 : 15) : 65535 / (WT * WI);
 
 __device__ __forceinline__ uint64_t word_tag(uint32_t epoch) {
     return static_cast<uint64_t>(0x80000000u | (epoch & 0x7FFFFFFFu)) << 32;
@@ -649,12 +649,12 @@ __device__ __forceinline__ uint64_t word_tag(uint32_t epoch) {
 // rereading the missing words).  The words alone decide what is read: a
 // partition that does not publish within the wait limit records a timeout
 // (the sums are then wrong but the kernel ends).
-template <int Q>
+template <int Q, int CH>
 __device__ void exchange_counts(uint64_t* words, int64_t P, int64_t c, uint32_t epoch, const int32_t (&tot)[Q],
                                 int32_t (&ex)[Q], int32_t (&all)[Q], int32_t* status, int32_t* arrive,
                                 uint64_t limit_ns = ptx::kWaitLimitNs) {
     constexpr int NW = Q / 2;
-    constexpr int CH = kSumChunk<Q>;
+    static_assert(CH >= 1 && CH <= 31, "partitions per chunk");
     const int t = threadIdx.x;
     const uint64_t tag = word_tag(epoch);
 #pragma unroll
@@ -936,7 +936,7 @@ __global__ void __launch_bounds__(WT, WI * Q > 16 ? 1 : 2) k_wide_pass(const Pas
         // both its prefix and the digit totals (the first output position of
         // every digit, an exclusive scan in digit order).
         int32_t all[Q];
-        exchange_counts<Q>(a.words, gridDim.x, c, a.epoch, tot, ex, all, a.status, a.arrive);
+        exchange_counts<Q, kSumChunk<WI, Q>>(a.words, gridDim.x, c, a.epoch, tot, ex, all, a.status, a.arrive);
         int32_t gs = 0;
 #pragma unroll
         for (int q = 0; q < Q; ++q) gs += all[q];
@@ -1404,7 +1404,7 @@ __global__ void __launch_bounds__(WT) k_wait_probe(int which, const uint64_t* lo
         // partition 1 of 2: partition 0's words stay zero
         const int32_t tot[2] = {0, 0};
         int32_t ex[2], all[2];
-        exchange_counts<2>(const_cast<uint64_t*>(look), 2, 1, 1u, tot, ex, all, status, nullptr, limit_ns);
+        exchange_counts<2, 31>(const_cast<uint64_t*>(look), 2, 1, 1u, tot, ex, all, status, nullptr, limit_ns);
     }
 }
 
@@ -1482,15 +1482,19 @@ namespace {
 // the ticket counter tickets[ticket]; offsets by the two-barrier form when
 // every partition is resident and the digits spread over them, else by
 // decoupled look-back.
-// The form a pass over n values with digits of `width` bits takes on this device.
+// The form a pass over n values with digits of `width` bits takes on this
+// device.  Keys per partition: 1024, 2048 above kBigPassRows, 4096 above
+// kHugePassRows for digits of up to 9 bits (fewer partitions: the
+// all-partition form reaches 262k rows).
 struct PassPlan {
-    bool big, narrow, ticket, barrier, all;
+    int size;   // keys per partition: kWideKeysPerCta << size
+    bool narrow, ticket, barrier, all;
     int64_t parts;
 };
 
 int plan_wide_pass(int64_t n, int width, PassPlan* pl) {
-    // resident CTAs of each form: [device][keys per CTA: 1024, 2048][digits per thread: 2, 4]
-    static int64_t cap_pass[kMaxDevices][2][2] = {};
+    // resident CTAs of each form: [device][size][digits per thread: 2, 4]
+    static int64_t cap_pass[kMaxDevices][3][2] = {};
     int dev = 0;
     SPCONV_CHECK_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return SPCONV_ERR_UNSUPPORTED;
@@ -1498,20 +1502,23 @@ int plan_wide_pass(int64_t n, int width, PassPlan* pl) {
     if (cap_pass[dev][0][0] == 0) {
         int sms = 0;
         SPCONV_CHECK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        // (the mask form of the first mask pass has the resources of its plain form or fewer CTAs)
-        const int64_t m0 = resident_ctas(k_wide_pass<WI, 2, true>, WT, sms);
-        const int64_t m1 = resident_ctas(k_wide_pass<2 * WI, 2, true>, WT, sms);
-        cap_pass[dev][0][0] = std::min(resident_ctas(k_wide_pass<WI, 2>, WT, sms), m0);
+        // (the mask form of the first mask pass may hold fewer CTAs than its plain form)
+        cap_pass[dev][0][0] = std::min(resident_ctas(k_wide_pass<WI, 2>, WT, sms),
+                                       resident_ctas(k_wide_pass<WI, 2, true>, WT, sms));
         cap_pass[dev][0][1] = resident_ctas(k_wide_pass<WI, 4>, WT, sms);
-        cap_pass[dev][1][0] = std::min(resident_ctas(k_wide_pass<2 * WI, 2>, WT, sms), m1);
+        cap_pass[dev][1][0] = std::min(resident_ctas(k_wide_pass<2 * WI, 2>, WT, sms),
+                                       resident_ctas(k_wide_pass<2 * WI, 2, true>, WT, sms));
         cap_pass[dev][1][1] = resident_ctas(k_wide_pass<2 * WI, 4>, WT, sms);
+        cap_pass[dev][2][0] = std::min(resident_ctas(k_wide_pass<4 * WI, 2>, WT, sms),
+                                       resident_ctas(k_wide_pass<4 * WI, 2, true>, WT, sms));
+        cap_pass[dev][2][1] = 0;   // (not used: wide digits stay at 2048 keys)
     }
-    pl->big = n > kBigPassRows;
     pl->narrow = (1 << width) <= 2 * WT;   // two digits per thread cover the digit values
-    const int64_t keys_per_cta = pl->big ? 2 * kWideKeysPerCta : kWideKeysPerCta;
+    pl->size = n > kHugePassRows && pl->narrow ? 2 : n > kBigPassRows ? 1 : 0;
+    const int64_t keys_per_cta = static_cast<int64_t>(kWideKeysPerCta) << pl->size;
     pl->parts = (n + keys_per_cta - 1) / keys_per_cta;
     if (pl->parts > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
-    pl->ticket = pl->parts > cap_pass[dev][pl->big ? 1 : 0][pl->narrow ? 0 : 1];
+    pl->ticket = pl->parts > cap_pass[dev][pl->size][pl->narrow ? 0 : 1];
     // the barrier form when every partition is resident, each warp scans at
     // most kScanDigitsPerWarp digits and each lane at most kScanPerLane partitions
     const int64_t bins = int64_t(1) << width;
@@ -1554,9 +1561,11 @@ int launch_wide_pass(const uint64_t* in, uint64_t* out, int64_t n, int shift, in
     }
     const unsigned grid = static_cast<unsigned>(pl.parts);
     if (mask_src)
-        return pl.big ? launch_pdl(k_wide_pass<2 * WI, 2, true>, grid, WT, s, pdl, pa)
-                      : launch_pdl(k_wide_pass<WI, 2, true>, grid, WT, s, pdl, pa);
-    if (pl.big)
+        return pl.size == 2 ? launch_pdl(k_wide_pass<4 * WI, 2, true>, grid, WT, s, pdl, pa)
+             : pl.size == 1 ? launch_pdl(k_wide_pass<2 * WI, 2, true>, grid, WT, s, pdl, pa)
+                            : launch_pdl(k_wide_pass<WI, 2, true>, grid, WT, s, pdl, pa);
+    if (pl.size == 2) return launch_pdl(k_wide_pass<4 * WI, 2>, grid, WT, s, pdl, pa);
+    if (pl.size == 1)
         return pl.narrow ? launch_pdl(k_wide_pass<2 * WI, 2>, grid, WT, s, pdl, pa)
                          : launch_pdl(k_wide_pass<2 * WI, 4>, grid, WT, s, pdl, pa);
     return pl.narrow ? launch_pdl(k_wide_pass<WI, 2>, grid, WT, s, pdl, pa)
@@ -1579,7 +1588,7 @@ WideDigits wide_digits(int lo, int bits) {
 }
 
 int64_t wide_sort_look_words(int64_t n) {
-    const int64_t keys_per_cta = n > kBigPassRows ? 2 * kWideKeysPerCta : kWideKeysPerCta;
+    const int64_t keys_per_cta = n > kBigPassRows ? 2 * kWideKeysPerCta : kWideKeysPerCta;   // (at least the parts of any pass)
     return (n + keys_per_cta - 1) / keys_per_cta * kWideBins;
 }
 
