@@ -68,7 +68,9 @@ constexpr int kWideMaskPasses = 3;       // 27-bit mask keys, 9-bit digits
 constexpr int kWideTickets = kWideKeyPassesMax + kWideMaskPasses;   // one per sort pass
 constexpr int kWideBarrierInts = 33;                // a grid barrier: 32 arrival counters + a release counter
 // the tickets, then a grid barrier per sort pass
-constexpr int kWideCounters = kWideTickets + kWideTickets * kWideBarrierInts;
+// rounded up to 16 bytes: callers place 64-bit arrays right after the counters
+constexpr int kWideCounters = (kWideTickets + kWideTickets * kWideBarrierInts + 3) / 4 * 4;
+static_assert(kWideCounters % 4 == 0, "the counters keep what follows them 16-byte aligned");
 constexpr int64_t kWideMaxRows = int64_t(1) << 26;
 // Hash mapper table: the smallest power of two >= kHashSlotsPerRow * n
 // entries, in buckets of kHashBucket (one 32-byte sector).  At a load of at

@@ -1596,6 +1596,9 @@ int wide_sort(uint64_t* a, uint64_t* b, int64_t n, const WideDigits& d, const in
               int ticket0, uint64_t* look, int32_t* status, cudaStream_t s, bool* in_b, bool first_plain) {
     *in_b = false;
     if (d.passes < 1 || ticket0 < 0 || ticket0 + d.passes > kWideTickets) return SPCONV_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(look) % 16 != 0 || reinterpret_cast<uintptr_t>(a) % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(b) % 8 != 0)
+        return SPCONV_ERR_INTERNAL;   // 64-bit words throughout
     if (n > kWideMaxRows) return SPCONV_ERR_UNSUPPORTED;
     for (int p = 0; p < d.passes; ++p) {
         const bool odd = p & 1;
@@ -1608,6 +1611,9 @@ int wide_sort(uint64_t* a, uint64_t* b, int64_t n, const WideDigits& d, const in
 
 int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     const int64_t n = a.n;
+    if (reinterpret_cast<uintptr_t>(a.look) % 16 != 0 || reinterpret_cast<uintptr_t>(a.va) % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(a.vb) % 8 != 0)
+        return SPCONV_ERR_INTERNAL;   // 64-bit words throughout
     // keys per sort CTA: 1024, or 2048 above kBigPassRows (fewer partitions
     // whose counts every partition reads: 32k rows 52.9 -> 50.8 us per build)
     const bool big_pass = n > kBigPassRows;

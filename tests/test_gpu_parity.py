@@ -891,7 +891,8 @@ def test_launch_count_reported():
     assert sc.last_launch_count() == 8                # clear, insert, lookup, 3 passes, tile count/write
     big = S.random_cloud(52, 140000, shape=(100, 100, 40))
     sc.build_map(big.coords.cuda(), big.spatial_shape, 1, mapper="hash", pipeline="wide")
-    assert sc.last_launch_count() == 9                # 35 partitions of 4096 keys; 1094 tiles: the tile scan
+    assert sc.last_launch_count() == 9                # 35 partitions of 4096 keys; 1094 tiles: tile count,
+                                                      # the tile scan, tile write
     bigger = S.random_cloud(53, 300000, shape=(100, 100, 40))
     sc.build_map(bigger.coords.cuda(), bigger.spatial_shape, 1, mapper="hash", pipeline="wide")
     assert sc.last_launch_count() == 10               # 74 partitions: the mask-key kernel; the tile scan
