@@ -333,6 +333,15 @@ __device__ __forceinline__ uint64_t packed_key(int4 q, const WideArgs& a) {
            static_cast<uint64_t>(q.w + 1);
 }
 
+// Table entries: (key << 32 | row) when keys fit 32 bits (kKey32: a slot's key
+// and row are its two halves, compared with 32-bit instructions), else
+// (key << row_bits | row).  Either way an entry is never 0: keys are >= 1.
+template <bool kKey32>
+__device__ __forceinline__ uint64_t hash_entry(uint64_t key, int64_t row, int row_bits) {
+    return (key << (kKey32 ? 32 : row_bits)) | static_cast<uint64_t>(row);
+}
+
+template <bool kKey32>
 __global__ void __launch_bounds__(WT) k_wide_hash_insert(const WideArgs a) {
     pdl_trigger();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * WT + threadIdx.x;
@@ -344,7 +353,8 @@ __global__ void __launch_bounds__(WT) k_wide_hash_insert(const WideArgs a) {
     int32_t err = (valid && !ok) ? kStatusRange : 0;
     if (ok) {
         // key >= 1 (every field is offset by one), so an entry is never 0 (empty)
-        const uint64_t entry = (key << a.row_bits) | static_cast<uint64_t>(i);
+        const uint64_t entry = hash_entry<kKey32>(key, i, a.row_bits);
+        const int ks = kKey32 ? 32 : a.row_bits;
         const int lb = a.table_log2 - 2;
         const uint64_t bmask = (uint64_t(1) << lb) - 1;
         uint64_t b = hash_bucket(key >> 1, lb);
@@ -354,7 +364,7 @@ __global__ void __launch_bounds__(WT) k_wide_hash_insert(const WideArgs a) {
                 const unsigned long long prev = atomicCAS(
                     reinterpret_cast<unsigned long long*>(a.table + b * kHashBucket + j), 0ull,
                     static_cast<unsigned long long>(entry));
-                if (prev == 0ull || (prev >> a.row_bits) == key) {   // placed, or the same voxel twice
+                if (prev == 0ull || (prev >> ks) == key) {   // placed, or the same voxel twice
                     if (prev != 0ull) err |= kStatusDuplicate;
                     placed = true;
                     break;
@@ -388,6 +398,33 @@ __device__ __forceinline__ bool bucket_scan(ulonglong2 lo, ulonglong2 hi, uint64
     return open;
 }
 
+// bucket_scan for 32-bit keys: key and row are the halves of a slot, and the
+// column's keys kc - 1, kc, kc + 1 are the slots whose key minus (kc - 1) is
+// 0, 1 or 2 (unsigned); an empty slot is excluded by its zero key.
+__device__ __forceinline__ bool bucket_scan32(ulonglong2 lo, ulonglong2 hi, uint64_t kc, int32_t& v0, int32_t& v1,
+                                              int32_t& v2) {
+    const uint64_t s[4] = {lo.x, lo.y, hi.x, hi.y};
+    const uint32_t base = static_cast<uint32_t>(kc) - 1u;
+    bool open = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t key = static_cast<uint32_t>(s[j] >> 32);
+        const int32_t row = static_cast<int32_t>(static_cast<uint32_t>(s[j]));
+        open |= key == 0u;
+        const uint32_t d = key == 0u ? 3u : key - base;   // 3 and above: not the column's
+        v0 = d == 0u ? row : v0;
+        v1 = d == 1u ? row : v1;
+        v2 = d == 2u ? row : v2;
+    }
+    return open;
+}
+
+template <bool kKey32>
+__device__ __forceinline__ bool scan_bucket(ulonglong2 lo, ulonglong2 hi, uint64_t kc, int row_bits, int32_t& v0,
+                                            int32_t& v1, int32_t& v2) {
+    return kKey32 ? bucket_scan32(lo, hi, kc, v0, v1, v2) : bucket_scan(lo, hi, kc, row_bits, v0, v1, v2);
+}
+
 // Three threads per row, one dx plane each, 128 rows per block: every
 // thread's 6 bucket reads are in flight at once (a thread per row with the
 // planes in turn had only a third of the reads in flight and waited three
@@ -395,7 +432,8 @@ __device__ __forceinline__ bool bucket_scan(ulonglong2 lo, ulonglong2 hi, uint64
 // coalesced.
 constexpr int kHashLookupRows = 128;
 
-__global__ void __launch_bounds__(kHashLookupRows * 3) k_wide_hash_lookup(const WideArgs a) {
+template <bool kKey32>
+__global__ void __launch_bounds__(kHashLookupRows * 3, 2) k_wide_hash_lookup(const WideArgs a) {
     __shared__ int32_t rows_s[kHashLookupRows][kNbrStride + 1];   // +1: conflict-free row and column access
     __shared__ uint32_t mask_s[kHashLookupRows];
     __shared__ int32_t cnt[kTaps];
@@ -424,7 +462,10 @@ __global__ void __launch_bounds__(kHashLookupRows * 3) k_wide_hash_lookup(const 
     uint64_t kc[3];
     uint32_t pending = 0;
 #pragma unroll
-    for (int c = 0; c < 3; ++c) kc[c] = key + a.koff[9 * p + 3 * c + 1];   // the column's dz = 0 key
+    for (int c = 0; c < 3; ++c) {   // the column's dz = 0 key (32-bit keys: known to fit the low half)
+        const uint64_t k64 = key + a.koff[9 * p + 3 * c + 1];
+        kc[c] = kKey32 ? static_cast<uint64_t>(static_cast<uint32_t>(k64)) : k64;
+    }
 #pragma unroll
     for (int r = 0; r < 6; ++r) {
         if (ok) {
@@ -434,8 +475,8 @@ __global__ void __launch_bounds__(kHashLookupRows * 3) k_wide_hash_lookup(const 
     }
 #pragma unroll
     for (int r = 0; r < 6; ++r)
-        if (ok && !bucket_scan(lo[r], hi[r], kc[r >> 1], a.row_bits, v[3 * (r >> 1)], v[3 * (r >> 1) + 1],
-                               v[3 * (r >> 1) + 2]))
+        if (ok && !scan_bucket<kKey32>(lo[r], hi[r], kc[r >> 1], a.row_bits, v[3 * (r >> 1)], v[3 * (r >> 1) + 1],
+                                       v[3 * (r >> 1) + 2]))
             pending |= 1u << r;
     for (uint64_t step = 1; __any_sync(0xFFFFFFFFu, pending != 0u) && step <= bmask; ++step) {
 #pragma unroll
@@ -447,8 +488,8 @@ __global__ void __launch_bounds__(kHashLookupRows * 3) k_wide_hash_lookup(const 
         }
 #pragma unroll
         for (int r = 0; r < 6; ++r)
-            if (((pending >> r) & 1u) && bucket_scan(lo[r], hi[r], kc[r >> 1], a.row_bits, v[3 * (r >> 1)],
-                                                     v[3 * (r >> 1) + 1], v[3 * (r >> 1) + 2]))
+            if (((pending >> r) & 1u) && scan_bucket<kKey32>(lo[r], hi[r], kc[r >> 1], a.row_bits, v[3 * (r >> 1)],
+                                                             v[3 * (r >> 1) + 1], v[3 * (r >> 1) + 2]))
                 pending &= ~(1u << r);
     }
     uint32_t m = 0;
@@ -1636,9 +1677,14 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
         return launch_wide_pass(in, out, n, shift, width, gh, a.look, a.tickets, ticket, a.status, s);
     };
     if (a.mapper == SPCONV_MAPPER_HASH) {
-        SPCONV_CHECK(launch_pdl(k_wide_hash_insert, row_blocks, WT, s, true, a));
-        SPCONV_CHECK(launch_pdl(k_wide_hash_lookup, static_cast<unsigned>((n + kHashLookupRows - 1) / kHashLookupRows),
-                                3 * kHashLookupRows, s, true, a));
+        const unsigned look_blocks = static_cast<unsigned>((n + kHashLookupRows - 1) / kHashLookupRows);
+        if (a.key_bits <= 32) {
+            SPCONV_CHECK(launch_pdl(k_wide_hash_insert<true>, row_blocks, WT, s, true, a));
+            SPCONV_CHECK(launch_pdl(k_wide_hash_lookup<true>, look_blocks, 3 * kHashLookupRows, s, true, a));
+        } else {
+            SPCONV_CHECK(launch_pdl(k_wide_hash_insert<false>, row_blocks, WT, s, true, a));
+            SPCONV_CHECK(launch_pdl(k_wide_hash_lookup<false>, look_blocks, 3 * kHashLookupRows, s, true, a));
+        }
     } else if (a.mapper == SPCONV_MAPPER_SORTED) {
         const int passes = wide_key_passes(a.key_bits);
         if (passes > kWideKeyPassesMax) return SPCONV_ERR_UNSUPPORTED;
