@@ -828,19 +828,25 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write(const int32_t* __rest
     }
     __syncthreads();
     const uint32_t lt = rsort::lanemask_lt();
-    for (int j = 0; j < kg; ++j) {
+    // the row's neighbours of the group's present taps, all requested before
+    // the first is stored (a load beside each store would wait for each in turn)
+    int32_t vv[kMaxGroupTaps];
+    const int32_t* nrow = nbr + (r >= 0 ? static_cast<int64_t>(r) * stride : 0) + g * kg;
+#pragma unroll
+    for (int j = 0; j < kMaxGroupTaps; ++j) vv[j] = (j < kg && ((m >> j) & 1u)) ? __ldcg(nrow + j) : -1;
+#pragma unroll
+    for (int j = 0; j < kMaxGroupTaps; ++j) {
+        if (j >= kg) break;
         const int64_t k = g * kg + j;
         const bool present = (m >> j) & 1u;
         const uint32_t b = __ballot_sync(0xFFFFFFFFu, present);
-        int32_t v = -1;
         if (present) {
-            v = nbr[static_cast<int64_t>(r) * stride + k];
             int32_t off = seg[j] + __popc(b & lt);
             for (int w = 0; w < warp; ++w) off += wc[w][j];
-            in_rows[off] = v;
+            in_rows[off] = vv[j];
             out_rows[off] = r;
         }
-        gtab[k * n_pad + s] = v;
+        gtab[k * n_pad + s] = vv[j];
     }
 }
 
@@ -892,7 +898,8 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write_prefix(
     for (int j = warp; j < kg; j += W) {
         const int32_t* row = counts + (g * kg + j) * n_tiles;
         int32_t acc = 0;
-        for (int64_t tt = lane; tt < t; tt += 32) acc += row[tt];
+#pragma unroll 8
+        for (int64_t tt = lane; tt < t; tt += 32) acc += __ldcg(row + tt);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
         if (lane == 0) wc[0][j] = acc;   // (wc is reused below)
@@ -951,19 +958,25 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write_prefix(
     }
     __syncthreads();
     const uint32_t lt = rsort::lanemask_lt();
-    for (int j = 0; j < kg; ++j) {
+    // the row's neighbours of the group's present taps, all requested before
+    // the first is stored (a load beside each store would wait for each in turn)
+    int32_t vv[kMaxGroupTaps];
+    const int32_t* nrow = nbr + (r >= 0 ? static_cast<int64_t>(r) * stride : 0) + g * kg;
+#pragma unroll
+    for (int j = 0; j < kMaxGroupTaps; ++j) vv[j] = (j < kg && ((m >> j) & 1u)) ? __ldcg(nrow + j) : -1;
+#pragma unroll
+    for (int j = 0; j < kMaxGroupTaps; ++j) {
+        if (j >= kg) break;
         const int64_t k = g * kg + j;
         const bool present = (m >> j) & 1u;
         const uint32_t b = __ballot_sync(0xFFFFFFFFu, present);
-        int32_t v = -1;
         if (present) {
-            v = nbr[static_cast<int64_t>(r) * stride + k];
             int32_t off = seg[j] + __popc(b & lt);
             for (int w = 0; w < warp; ++w) off += wc[w][j];
-            in_rows[off] = v;
+            in_rows[off] = vv[j];
             out_rows[off] = r;
         }
-        gtab[k * n_pad + s] = v;
+        gtab[k * n_pad + s] = vv[j];
     }
 }
 
