@@ -858,8 +858,6 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write(const int32_t* __rest
 // group's order is the number of the group's tiles with a larger union plus
 // those before it with an equal one.  Block (g, 0) writes the group's count
 // of tiles with a nonempty union, block (0, 0) the tap offsets and totals.
-constexpr int64_t kPrefixTilesG = 512;
-
 __global__ void __launch_bounds__(kTileRows) kg_tile_write_prefix(
     const int32_t* __restrict__ perm, const uint32_t* __restrict__ mask, const int32_t* __restrict__ nbr, int stride,
     int64_t n, int64_t n_tiles, int64_t n_pad, int G, int kg, const int32_t* __restrict__ counts,
@@ -977,6 +975,186 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write_prefix(
             out_rows[off] = r;
         }
         gtab[k * n_pad + s] = vv[j];
+    }
+}
+
+// kg_tile_write_prefix with four threads a row (used while its blocks fill at
+// most two waves of the device: it holds fewer blocks per SM): block (g, t)
+// of kGtThreads, thread j of a row takes the
+// group's taps j, j + 4, ... (at most kGtSlots of them) and requests their
+// neighbours together; ranks within the tile come from ballots masked to the
+// lanes of one phase and a scan over the warps (one thread walking all of a
+// group's taps was ~25 dependent steps per row).  The pairs of the group's
+// taps for the rows of tile t go to the tile's offsets in each tap's list;
+// gtab[k][s] = neighbour of the row at position s of the group's order (-1
+// when absent or past n).
+// As kg_tile_write_prefix, the block finds its own offsets and its place in
+// the group's tile order (groups of up to kPrefixTilesG tiles).
+constexpr int64_t kPrefixTilesG = 512;
+constexpr int kGtThreads = 4 * kTileRows;
+constexpr int kGtWarps = kGtThreads / 32;
+constexpr int kGtSlots = (kMaxGroupTaps + 3) / 4;   // taps per thread
+constexpr int kGtGroupTaps = 8;                     // taps summed by each quarter of the block
+static_assert(4 * kGtGroupTaps >= kMaxGroupTaps, "four quarters cover a group's taps");
+
+__global__ void __launch_bounds__(kGtThreads) kg_tile_write4(
+    const int32_t* __restrict__ perm, const uint32_t* __restrict__ mask, const int32_t* __restrict__ nbr, int stride,
+    int64_t n, int64_t n_tiles, int64_t n_pad, int G, int kg, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ tap_count, const uint32_t* __restrict__ tile_union, int32_t* __restrict__ tap_off,
+    int32_t* __restrict__ totals, int32_t* __restrict__ tile_order, int32_t* __restrict__ nonempty,
+    int32_t* __restrict__ in_rows, int32_t* __restrict__ out_rows, int32_t* __restrict__ gtab) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ int32_t wc[kMaxGroupTaps][kGtWarps];   // rows with each tap per warp, then the warp's first pair
+    __shared__ int32_t seg[kMaxGroupTaps];            // the tile's first pair in each of the group's lists
+    __shared__ int32_t tstart[kMaxTaps + 1];          // every tap's first pair
+    __shared__ int32_t gsum[4][4][kGtGroupTaps];      // [quarter][its warp][tap of the quarter]
+    __shared__ int32_t wsum[kGtWarps];
+    __shared__ int32_t red[4][kGtWarps];
+    const int64_t g = blockIdx.x / n_tiles, t = blockIdx.x % n_tiles;
+    const int V = G * kg;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rl = tid >> 2, j = tid & 3;   // row within the tile, tap phase
+    const int64_t s = t * kTileRows + rl;
+    const bool valid = s < n;
+    // the row (two dependent round trips), requested before the sums below
+    const int32_t r = valid ? __ldcg(perm + g * n + s) : -1;
+    const uint32_t m = valid ? __ldcg(mask + g * n + r) : 0u;
+    int32_t vv[kGtSlots];
+    const int32_t* nrow = nbr + (r >= 0 ? static_cast<int64_t>(r) * stride : 0) + g * kg;
+#pragma unroll
+    for (int i = 0; i < kGtSlots; ++i) {
+        const int jj = j + 4 * i;
+        vv[i] = (jj < kg && ((m >> jj) & 1u)) ? __ldcg(nrow + jj) : -1;
+    }
+    {
+        // tap starts: exclusive prefix of the tap counts (V <= kGtThreads)
+        const int32_t tc = tid < V ? __ldcg(tap_count + tid) : 0;
+        // the quarter's taps in the tiles before t: thread tid takes tiles tid % 128, + 128, ...
+        const int grp = tid / kTileRows;
+        int32_t acc[kGtGroupTaps];
+#pragma unroll
+        for (int i = 0; i < kGtGroupTaps; ++i) acc[i] = 0;
+#pragma unroll 4
+        for (int64_t tt = tid % kTileRows; tt < t; tt += kTileRows) {
+#pragma unroll
+            for (int i = 0; i < kGtGroupTaps; ++i) {
+                const int jj = kGtGroupTaps * grp + i;
+                acc[i] += jj < kg ? __ldcg(counts + (g * kg + jj) * n_tiles + tt) : 0;
+            }
+        }
+        // place in the group's tile order; nonempty tiles; (block 0, 0) the sum of all union sizes
+        const int c = __popc(__ldcg(tile_union + g * n_tiles + t));
+        int32_t greater = 0, equal_before = 0, nonzero = 0, taps_all = 0;
+        for (int64_t tt = tid; tt < n_tiles; tt += kGtThreads) {
+            const int cu = __popc(__ldcg(tile_union + g * n_tiles + tt));
+            greater += cu > c ? 1 : 0;
+            equal_before += (cu == c && tt < t) ? 1 : 0;
+            nonzero += cu > 0 ? 1 : 0;
+        }
+        if (g == 0 && t == 0)
+            for (int64_t tt = tid; tt < G * n_tiles; tt += kGtThreads) taps_all += __popc(__ldcg(tile_union + tt));
+        int32_t inc = tc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane == 31) wsum[warp] = inc;
+        // each of the quarter's 8 counters over the warp: three exchanges halve
+        // the counters a lane carries, two more add the rest; lane l then holds counter l
+#pragma unroll
+        for (int h = 4; h >= 1; h >>= 1) {
+            const bool upper = (lane & h) != 0;
+#pragma unroll
+            for (int i = 0; i < h; ++i) {
+                const int32_t send = upper ? acc[i] : acc[i + h];
+                const int32_t keep = upper ? acc[i + h] : acc[i];
+                acc[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, h);
+            }
+        }
+        acc[0] += __shfl_xor_sync(0xFFFFFFFFu, acc[0], 8);
+        acc[0] += __shfl_xor_sync(0xFFFFFFFFu, acc[0], 16);
+        if (lane < kGtGroupTaps) gsum[grp][warp & 3][lane] = acc[0];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            greater += __shfl_xor_sync(0xFFFFFFFFu, greater, o);
+            equal_before += __shfl_xor_sync(0xFFFFFFFFu, equal_before, o);
+            nonzero += __shfl_xor_sync(0xFFFFFFFFu, nonzero, o);
+            taps_all += __shfl_xor_sync(0xFFFFFFFFu, taps_all, o);
+        }
+        if (lane == 0) {
+            red[0][warp] = greater;
+            red[1][warp] = equal_before;
+            red[2][warp] = nonzero;
+            red[3][warp] = taps_all;
+        }
+        __syncthreads();   // wsum
+        int32_t before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kGtWarps; ++w) {
+            before += w < warp ? wsum[w] : 0;
+            total += wsum[w];
+        }
+        if (tid <= V) tstart[tid] = tid < V ? before + inc - tc : total;
+    }
+    // the warp's rows with each of the group's taps: lanes of one phase share their taps
+    const uint32_t same = 0x11111111u << j;
+#pragma unroll
+    for (int i = 0; i < kGtSlots; ++i) {
+        const int jj = j + 4 * i;
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, jj < kg && ((m >> jj) & 1u)) & same;
+        if (lane == j && jj < kg) wc[jj][warp] = __popc(b);
+    }
+    __syncthreads();
+    // each tap's warp counts -> the warps' first pairs within the tile (two taps per warp)
+    if (warp < (kg * kGtWarps + 31) / 32) {   // whole warps: every lane takes part in the shuffles
+        const int jj = tid / kGtWarps, w = tid % kGtWarps;
+        const int32_t x = jj < kg ? wc[jj][w] : 0;
+        int32_t inc = x;
+#pragma unroll
+        for (int o = 1; o < kGtWarps; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o, kGtWarps);
+            if (w >= o) inc += y;
+        }
+        if (jj < kg) wc[jj][w] = inc - x;
+    }
+    if (warp == kGtWarps - 1) {
+        if (lane < kg) {
+            const int q = lane / kGtGroupTaps, i = lane % kGtGroupTaps;
+            seg[lane] = tstart[g * kg + lane] + gsum[q][0][i] + gsum[q][1][i] + gsum[q][2][i] + gsum[q][3][i];
+        }
+        if (lane == 0) {
+            int32_t gs = 0, es = 0, nz = 0, ta = 0;
+            for (int w = 0; w < kGtWarps; ++w) {
+                gs += red[0][w];
+                es += red[1][w];
+                nz += red[2][w];
+                ta += red[3][w];
+            }
+            tile_order[g * n_tiles + gs + es] = static_cast<int32_t>(t);
+            if (t == 0) nonempty[g] = nz;
+            if (g == 0 && t == 0) {
+                totals[0] = tstart[V];
+                totals[1] = ta;
+            }
+        }
+    }
+    if (g == 0 && t == 0 && tid <= V) tap_off[tid] = tstart[tid];
+    __syncthreads();
+    // the pairs and the gather table
+    const uint32_t lt = rsort::lanemask_lt();
+#pragma unroll
+    for (int i = 0; i < kGtSlots; ++i) {
+        const int jj = j + 4 * i;
+        const bool present = jj < kg && ((m >> jj) & 1u);
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, present) & same;
+        if (present) {
+            const int32_t off = seg[jj] + wc[jj][warp] + __popc(b & lt);
+            in_rows[off] = vv[i];
+            out_rows[off] = r;
+        }
+        if (jj < kg) gtab[(g * kg + jj) * n_pad + s] = vv[i];
     }
 }
 
@@ -1549,17 +1727,34 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
         SPCONV_CHECK(launch_chained(kg_tile_count<false>, tiles, kTileRows, s, h->perm, nullptr, 0, h->mask, n, T, kg, counts,
                                                          h->tile_union));
     }
+    // four threads a row while its blocks fill at most two waves; else one
+    // (outdoor maps: strided, 600 blocks, 178.4 -> 168.9 us; three groups,
+    // 759 blocks, 64.4 -> 68.7 us and kernel size 5, 1265, 137.0 -> 137.5)
+    static int64_t cap4[kMaxDevices] = {};
+    int dev = 0;
+    SPCONV_CHECK_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return SPCONV_ERR_UNSUPPORTED;
+    if (cap4[dev] == 0) {
+        int sms = 0, b = 0;
+        SPCONV_CHECK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        SPCONV_CHECK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kg_tile_write4, kGtThreads, 0));
+        cap4[dev] = std::max<int64_t>(1, static_cast<int64_t>(b) * sms);
+    }
     if (T <= kPrefixTilesG && V <= kTileRows) {
-        SPCONV_CHECK(launch_chained(kg_tile_write_prefix, tiles, kTileRows, s, h->perm, h->mask, h->nbr, h->nbr_stride, n, T, h->n_pad, G, kg,
-                                                         counts, h->tap_count, h->tile_union, h->tap_off, h->totals,
-                                                         h->tile_order, h->tile_nonempty, h->in_rows, h->out_rows,
-                                                         h->gtab));
+        if (static_cast<int64_t>(tiles) <= 2 * cap4[dev])
+            SPCONV_CHECK(launch_chained(kg_tile_write4, tiles, kGtThreads, s, h->perm, h->mask, h->nbr, h->nbr_stride, n,
+                                        T, h->n_pad, G, kg, counts, h->tap_count, h->tile_union, h->tap_off,
+                                        h->totals, h->tile_order, h->tile_nonempty, h->in_rows, h->out_rows, h->gtab));
+        else
+            SPCONV_CHECK(launch_chained(kg_tile_write_prefix, tiles, kTileRows, s, h->perm, h->mask, h->nbr, h->nbr_stride,
+                                        n, T, h->n_pad, G, kg, counts, h->tap_count, h->tile_union, h->tap_off,
+                                        h->totals, h->tile_order, h->tile_nonempty, h->in_rows, h->out_rows, h->gtab));
         launches -= 1;
     } else {
         SPCONV_CHECK(launch_chained(kg_scan_tiles, 1, 1024, s, counts, V, G, kg, T, h->tile_union, h->seg_off, h->tap_off, h->totals,
                                          h->tile_order, h->tile_nonempty));
-        SPCONV_CHECK(launch_chained(kg_tile_write, tiles, kTileRows, s, h->perm, h->mask, h->nbr, h->nbr_stride, n, T, h->n_pad, kg,
-                                                  h->seg_off, h->in_rows, h->out_rows, h->gtab));
+        SPCONV_CHECK(launch_chained(kg_tile_write, tiles, kTileRows, s, h->perm, h->mask, h->nbr, h->nbr_stride, n, T,
+                                    h->n_pad, kg, h->seg_off, h->in_rows, h->out_rows, h->gtab));
     }
     launches += 3;
     count_launch(launches);
