@@ -1204,10 +1204,12 @@ __global__ void __launch_bounds__(kGBlock) kst_candidates(const int4* __restrict
 
 // The distinct candidates without sorting them all: each input site's up to
 // 8 output keys go into a hash set (slot = key + 1, 0 empty, linear probing
-// from a multiplicative hash); the thread whose insertion creates an entry
-// appends the key to uniq[] (the count in *n_uniq) and counts its digits for
-// the sort of the distinct keys.  The set has at least twice as many slots
-// as there can be candidates, so a probe always ends.
+// from a multiplicative hash), one thread per candidate (a thread per input
+// site and its 8 candidates in turn was 26 us on outdoor, cold); the thread
+// whose insertion creates an entry appends the key to uniq[] (the count in
+// *n_uniq) and counts its digits for the sort of the distinct keys.  The set
+// has at least twice as many slots as there can be candidates, so a probe
+// always ends.
 __device__ __forceinline__ uint64_t set_slot(uint64_t key, int log2) {
     return (key * 0x9E3779B97F4A7C15ull) >> (64 - log2);
 }
@@ -1219,7 +1221,7 @@ __global__ void __launch_bounds__(kGBlock) kst_dedupe(const int4* __restrict__ c
     pdl_trigger();
     pdl_wait();
     __shared__ int32_t h[kWideKeyPassesMax][kWideBins];
-    __shared__ uint64_t staged[8 * kGBlock];   // the block's new keys of one round
+    __shared__ uint64_t staged[kGBlock];   // the block's new keys of one round
     __shared__ int32_t n_staged;
     __shared__ unsigned long long base_sh;
     for (int i = threadIdx.x; i < kWideKeyPassesMax * kWideBins; i += kGBlock) (&h[0][0])[i] = 0;
@@ -1227,71 +1229,59 @@ __global__ void __launch_bounds__(kGBlock) kst_dedupe(const int4* __restrict__ c
     __syncthreads();
     const uint64_t smask = (uint64_t(1) << set_log2) - 1;
     const int lane = threadIdx.x & 31;
-    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kGBlock; i0 < n; i0 += static_cast<int64_t>(gridDim.x) * kGBlock) {
-        const int64_t i = i0 + threadIdx.x;
+    // one candidate a thread: eight lanes share an input site, lane j taking
+    // parity choice j (bit a: the second choice on axis a)
+    const int64_t m = 8 * n;
+    for (int64_t q0 = static_cast<int64_t>(blockIdx.x) * kGBlock; q0 < m; q0 += static_cast<int64_t>(gridDim.x) * kGBlock) {
+        const int64_t q = q0 + threadIdx.x;
+        const int64_t i = q >> 3;
+        const int j = static_cast<int>(q & 7);
         int4 c = make_int4(-1, -1, -1, -1);
-        bool ok = false;
-        if (i < n) {
-            c = coords[i];
-            ok = in_range(c, shape, batch);
+        bool v = false;
+        if (q < m) {
+            c = __ldcg(coords + i);
+            v = in_range(c, shape, batch);
         }
-        // the candidate of parity choice j (bit a: the second choice on axis a), if any:
         // an even coordinate has o = c / 2 only, an odd one (c - 1) / 2 and (c + 1) / 2
-        uint64_t key[8];
-        uint32_t valid = 0;
+        int o[3];
+        const int cc[3] = {c.y, c.z, c.w};
+        const int lim[3] = {O.shape.x, O.shape.y, O.shape.z};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            bool v = ok;
-            int o[3];
-            const int cc[3] = {c.y, c.z, c.w};
-            const int lim[3] = {O.shape.x, O.shape.y, O.shape.z};
-#pragma unroll
-            for (int a = 0; a < 3; ++a) {
-                const int second = (j >> a) & 1;
-                const bool odd = cc[a] & 1;
-                if (!odd && second) v = false;
-                o[a] = odd ? (second ? (cc[a] + 1) >> 1 : (cc[a] - 1) >> 1) : cc[a] >> 1;
-                if (o[a] < 0 || o[a] >= lim[a]) v = false;
-            }
-            key[j] = v ? out_key(c.x, o[0], o[1], o[2], O) : 0ull;
-            valid |= (v ? 1u : 0u) << j;
+        for (int a = 0; a < 3; ++a) {
+            const int second = (j >> a) & 1;
+            const bool odd = cc[a] & 1;
+            if (!odd && second) v = false;
+            o[a] = odd ? (second ? (cc[a] + 1) >> 1 : (cc[a] - 1) >> 1) : cc[a] >> 1;
+            if (o[a] < 0 || o[a] >= lim[a]) v = false;
         }
-        // the first slot of every candidate, read together; most end there
-        uint64_t seen[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) seen[j] = ((valid >> j) & 1u) ? __ldcg(set + set_slot(key[j], set_log2)) : 0ull;
-        uint32_t fresh = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (!((valid >> j) & 1u) || seen[j] == key[j] + 1) continue;
-            uint64_t slot = set_slot(key[j], set_log2);
-            uint64_t cur = seen[j];
+        const uint64_t key = v ? out_key(c.x, o[0], o[1], o[2], O) : 0ull;
+        bool fresh = false;
+        if (v) {
+            // most probes end at the first slot
+            uint64_t slot = set_slot(key, set_log2);
+            uint64_t cur = __ldcg(set + slot);
             for (uint64_t probe = 0; probe <= smask; ++probe, slot = (slot + 1) & smask) {
                 if (probe > 0) cur = __ldcg(set + slot);
-                if (cur == key[j] + 1) break;
+                if (cur == key + 1) break;
                 if (cur != 0ull) continue;
                 const unsigned long long prev = atomicCAS(reinterpret_cast<unsigned long long*>(set + slot), 0ull,
-                                                          static_cast<unsigned long long>(key[j] + 1));
+                                                          static_cast<unsigned long long>(key + 1));
                 if (prev == 0ull) {
-                    fresh |= 1u << j;
+                    fresh = true;
                     break;
                 }
-                if (prev == key[j] + 1) break;
+                if (prev == key + 1) break;
             }
         }
-        // the block's new keys are staged in shared memory (a shared counter
-        // per warp and candidate), then take consecutive slots of uniq with one
-        // global counter update per block and round
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const bool f = (fresh >> j) & 1u;
-            const uint32_t b = __ballot_sync(0xFFFFFFFFu, f);
-            int at = 0;
-            if (b && lane == __ffs(b) - 1) at = atomicAdd(&n_staged, __popc(b));
-            at = __shfl_sync(0xFFFFFFFFu, at, b ? __ffs(b) - 1 : 0);
-            if (f) staged[at + __popc(b & ((1u << lane) - 1u))] = key[j];
-            wide_count_digits(key[j], f, d, h);
-        }
+        // the block's new keys are staged in shared memory (one shared counter
+        // update per warp), then take consecutive slots of uniq with one global
+        // counter update per block and round
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, fresh);
+        int at = 0;
+        if (b && lane == __ffs(b) - 1) at = atomicAdd(&n_staged, __popc(b));
+        at = __shfl_sync(0xFFFFFFFFu, at, b ? __ffs(b) - 1 : 0);
+        if (fresh) staged[at + __popc(b & ((1u << lane) - 1u))] = key;
+        wide_count_digits(key, fresh, d, h);
         __syncthreads();               // the round's keys are staged
         const int cnt = n_staged;
         __syncthreads();               // every thread has read the count
@@ -1842,7 +1832,7 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
     if (n_in > 0) {
         const int3 ishape = make_int3(h->shape[0], h->shape[1], h->shape[2]);
         if (wide_cand) {
-            kst_dedupe<<<capped_blocks(n_in), kGBlock, 0, s>>>(reinterpret_cast<const int4*>(coords), n_in, ishape,
+            kst_dedupe<<<capped_blocks(8 * n_in), kGBlock, 0, s>>>(reinterpret_cast<const int4*>(coords), n_in, ishape,
                                                                h->batch, O, cset, set_log2, cdig, ka, count, wgh);
             ++launches;
             // the one synchronisation: the number of distinct sites sizes the map
