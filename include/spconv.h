@@ -207,7 +207,8 @@ int spconv_build_map(const int32_t* coords_dev, int64_t n, const int32_t* spatia
  *   opt: mapper AUTO or HASH, pipeline AUTO or MULTI, gemm not TAP_MAJOR,
  *        groups 0 or 1 (else SPCONV_ERR_UNSUPPORTED).
  * Synchronises the stream once: the number of output sites sizes the map.
- * spconv_map_info gives n (output sites), n_in and out_shape;
+ * spconv_map_rows gives n (output sites) and n_in without a second
+ * synchronisation; spconv_map_info also out_shape;
  * spconv_map_out_coords copies the output sites' coordinates.
  */
 int spconv_build_map_strided(const int32_t* coords_dev, int64_t n, const int32_t* spatial_shape,
@@ -312,6 +313,15 @@ int spconv_map_status(spconv_map_t map);
 
 /* Fill *info (synchronises the map's stream). */
 int spconv_map_info(spconv_map_t map, spconv_map_info_t* info);
+
+/*
+ * The map's row count (output sites) and the count of the sites its
+ * neighbours index (n_in; = rows but for strided and inverse maps), both
+ * known on the host once the build call has returned: no synchronisation
+ * and no device access.  Either pointer may be NULL.  Returns
+ * SPCONV_ERR_INVALID_ARG for a NULL map.
+ */
+int spconv_map_rows(spconv_map_t map, int64_t* n, int64_t* n_in);
 
 /*
  * Copy the map's arrays into caller device buffers (any may be NULL):

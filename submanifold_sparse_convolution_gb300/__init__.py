@@ -224,9 +224,9 @@ def build_map_strided(coords: torch.Tensor, spatial_shape: Optional[Sequence[int
                                       int(batch_size), int(kernel_size), int(stride), ctypes.byref(opt),
                                       _stream_ptr(stream), ctypes.byref(h))
     _check(rc, "spconv_build_map_strided")
-    info = _native.MapInfo()
-    _check(lib.spconv_map_info(h, ctypes.byref(info)), "spconv_map_info")
-    return Map(h, int(info.n), coords, 3, n_in=int(coords.shape[0]))
+    rows = ctypes.c_int64(0)
+    _check(lib.spconv_map_rows(h, ctypes.byref(rows), None), "spconv_map_rows")   # (no second synchronisation)
+    return Map(h, int(rows.value), coords, 3, n_in=int(coords.shape[0]))
 
 
 def build_map_inverse(m: Map, bit_order: str = "calibrated") -> Map:

@@ -70,6 +70,7 @@ SIGNATURES = {
                                                   ctypes.POINTER(Epilogue), ctypes.c_void_p]),
     "spconv_map_status": (ctypes.c_int, [ctypes.c_void_p]),
     "spconv_map_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(MapInfo)]),
+    "spconv_map_rows": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     "spconv_map_export": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_void_p] * 6 + [ctypes.c_void_p]),
     "spconv_map_destroy": (None, [ctypes.c_void_p]),
     "spconv_kernel_map_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, c_int32_p, ctypes.c_int32,

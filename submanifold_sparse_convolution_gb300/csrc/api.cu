@@ -419,6 +419,13 @@ int spconv_map_info(spconv_map_t map, spconv_map_info_t* info) {
     return SPCONV_OK;
 }
 
+int spconv_map_rows(spconv_map_t map, int64_t* n, int64_t* n_in) {
+    if (!map) return SPCONV_ERR_INVALID_ARG;
+    if (n) *n = map->n;
+    if (n_in) *n_in = map->n_in >= 0 ? map->n_in : map->n;
+    return SPCONV_OK;
+}
+
 int spconv_map_export(spconv_map_t map, int32_t* nbr_dev, uint32_t* mask_dev, int32_t* perm_dev,
                       int32_t* tap_off_dev, int32_t* in_rows_dev, int32_t* out_rows_dev, void* stream) {
     reset_launch_count();

@@ -82,6 +82,7 @@ def test_host_side_argument_errors(lib):
     assert lib.spconv_map_status(None) == -1
     info = _native.MapInfo()
     assert lib.spconv_map_info(None, ctypes.byref(info)) == -1
+    assert lib.spconv_map_rows(None, None, None) == -1
     assert lib.spconv_map_export(None, None, None, None, None, None, None, None) == -1
     lib.spconv_map_destroy(None)
     lib.spconv_wpack_destroy(None)

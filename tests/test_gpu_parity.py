@@ -7,6 +7,8 @@ outputs |out - ref| <= 1e-5.  Every case, the full-size workloads included,
 compares every output row: the fp64 oracle evaluates all rows with its OpenMP
 threads (each row summed by one thread in a fixed order).
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -818,6 +820,9 @@ def test_strided_and_inverse_forward(c_in, c_out, dtype):
     y = sc.subm_forward(m, f.cuda(), w.cuda())
     assert sc.map_status(m) == 0 and y.shape == (m.n, c_out)
     oc, nbr = oracle.strided_map(wl.coords.numpy(), wl.spatial_shape, 2)
+    rows, rows_in = ctypes.c_int64(-1), ctypes.c_int64(-1)   # the host-side counts, no synchronisation
+    assert sc.library().spconv_map_rows(m.handle, ctypes.byref(rows), ctypes.byref(rows_in)) == 0
+    assert rows.value == m.n == oc.shape[0] and rows_in.value == wl.n == sc.map_info(m)["n_in"]
     check = check_fp32 if dtype == torch.float32 else check_bf16
     check(y, oracle.conv_f64(nbr, f.double().numpy(), w.double().numpy()))
     # the inverse convolution back onto the input sites, with its own weights and a fused ReLU
