@@ -892,15 +892,26 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write_prefix(
         total += wsum[w];
     }
     if (threadIdx.x <= V) tstart[threadIdx.x] = threadIdx.x < V ? before + inc - tc : total;
-    // ---- the counts of the group's taps in the tiles before t: warp w sums taps w, w + W, ...
-    for (int j = warp; j < kg; j += W) {
-        const int32_t* row = counts + (g * kg + j) * n_tiles;
-        int32_t acc = 0;
-#pragma unroll 8
-        for (int64_t tt = lane; tt < t; tt += 32) acc += __ldcg(row + tt);
+    // ---- the counts of the group's taps in the tiles before t: warp w sums
+    // taps w, w + W, ..., the loads of all its taps in flight together
+    constexpr int kTapsPerWarp = (kMaxGroupTaps + W - 1) / W;
+    int32_t acc[kTapsPerWarp];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-        if (lane == 0) wc[0][j] = acc;   // (wc is reused below)
+    for (int i = 0; i < kTapsPerWarp; ++i) acc[i] = 0;
+#pragma unroll 2
+    for (int64_t tt = lane; tt < t; tt += 32) {
+#pragma unroll
+        for (int i = 0; i < kTapsPerWarp; ++i) {
+            const int j = warp + W * i;
+            acc[i] += j < kg ? __ldcg(counts + (g * kg + j) * n_tiles + tt) : 0;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kTapsPerWarp; ++i) {
+        const int j = warp + W * i;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xFFFFFFFFu, acc[i], o);
+        if (lane == 0 && j < kg) wc[0][j] = acc[i];   // (wc is reused below)
     }
     // ---- place in the group's tile order; nonempty tiles; (block 0, 0) the sum of all union sizes
     const int c = __popc(tile_union[g * n_tiles + t]);
