@@ -607,17 +607,35 @@ __global__ void __launch_bounds__(kGBlock) kg_mask_keys_packed(const int32_t* __
 // mask and key of groups q, q + 4, ...; entry g n + i gets group g's.
 template <int K>
 __global__ void __launch_bounds__(kGBlock) kg_mask_keys_rows(const int32_t* __restrict__ nbr, int64_t n, int G,
-                                                             int kg, int rbits, const int32_t* __restrict__ tap_pos,
+                                                             int kg, int rbits, const int32_t* __restrict__ tap_count,
+                                                             int calibrated, int32_t* __restrict__ tap_pos,
                                                              const WideDigits d, uint32_t* __restrict__ mask,
                                                              uint64_t* __restrict__ packed,
                                                              int32_t* __restrict__ gh) {
     pdl_trigger();
     pdl_wait();
     constexpr int V = K * K * K, NQ = (V + 3) / 4, NW = (V + 31) / 32;   // taps, 16-byte words of a row, bitmap words
+    __shared__ int32_t cnt[V];
     __shared__ int32_t pos[V];
     __shared__ int32_t h[kWideKeyPassesMax][kWideBins];
-    for (int k = threadIdx.x; k < V; k += kGBlock) pos[k] = tap_pos[k];
+    for (int k = threadIdx.x; k < V; k += kGBlock) cnt[k] = __ldcg(tap_count + k);
     for (int i = threadIdx.x; i < kWideKeyPassesMax * kWideBins; i += kGBlock) (&h[0][0])[i] = 0;
+    __syncthreads();
+    // each block ranks the taps itself, as kg_tap_order does (block 0 also stores the ranks)
+    for (int k = threadIdx.x; k < V; k += kGBlock) {
+        const int g0 = k / kg * kg;
+        int rank = k - g0;
+        if (calibrated) {
+            const int32_t ck = cnt[k];
+            rank = 0;
+            for (int j = g0; j < g0 + kg; ++j) {
+                const int32_t cj = cnt[j];
+                rank += (cj > ck || (cj == ck && j < k)) ? 1 : 0;
+            }
+        }
+        pos[k] = rank;
+        if (blockIdx.x == 0) tap_pos[k] = rank;
+    }
     __syncthreads();
     const int q = threadIdx.x & 3;
     for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kGBlock; t0 < 4 * n; t0 += static_cast<int64_t>(gridDim.x) * kGBlock) {
@@ -1693,25 +1711,32 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
         SPCONV_CHECK(launch_chained(kg_grid_lookup, blocks(n, kGBlock), kGBlock, s, c4, n, shape3, B, L, grid, h->nbr, h->tap_count));
         launches += 2;
     }
+    // the rows' mask-key kernel ranks the taps itself; the others read kg_tap_order's ranks
+    const bool rows_keys = wide_mask && ((K == 5 && h->nbr_stride == 128) || (K == 3 && h->nbr_stride == 28));
+    const int calibrated = h->bit_order == SPCONV_ORDER_CALIBRATED;
     if (src) {   // (a copy precedes it: a plain launch)
-        kg_tap_order<<<1, 128, 0, s>>>(h->tap_count, V, kg, h->bit_order == SPCONV_ORDER_CALIBRATED, h->tap_pos);
-    } else {
+        kg_tap_order<<<1, 128, 0, s>>>(h->tap_count, V, kg, calibrated, h->tap_pos);
+        ++launches;
+    } else if (!rows_keys) {
         SPCONV_CHECK(launch_chained(kg_tap_order, 1u, 128u, s, static_cast<const int32_t*>(h->tap_count), V, kg,
-                                    static_cast<int>(h->bit_order == SPCONV_ORDER_CALIBRATED), h->tap_pos));
+                                    calibrated, h->tap_pos));
+        ++launches;
     }
     const unsigned tiles = static_cast<unsigned>(G * T);
     if (wide_mask) {
         int32_t* mgh = wgh + kWideKeyPassesMax * kWideBins;
         if (K == 5 && h->nbr_stride == 128)
-            SPCONV_CHECK(launch_chained(kg_mask_keys_rows<5>, capped_blocks(4 * n), kGBlock, s, h->nbr, n, G, kg, mrb, h->tap_pos, mdig,
-                                                                          h->mask, mpk_a, mgh));
+            SPCONV_CHECK(launch_chained(kg_mask_keys_rows<5>, capped_blocks(4 * n), kGBlock, s, h->nbr, n, G, kg, mrb,
+                                        static_cast<const int32_t*>(h->tap_count), calibrated, h->tap_pos, mdig,
+                                        h->mask, mpk_a, mgh));
         else if (K == 3 && h->nbr_stride == 28)
-            SPCONV_CHECK(launch_chained(kg_mask_keys_rows<3>, capped_blocks(4 * n), kGBlock, s, h->nbr, n, G, kg, mrb, h->tap_pos, mdig,
-                                                                          h->mask, mpk_a, mgh));
+            SPCONV_CHECK(launch_chained(kg_mask_keys_rows<3>, capped_blocks(4 * n), kGBlock, s, h->nbr, n, G, kg, mrb,
+                                        static_cast<const int32_t*>(h->tap_count), calibrated, h->tap_pos, mdig,
+                                        h->mask, mpk_a, mgh));
         else
             SPCONV_CHECK(launch_chained(kg_mask_keys_packed, capped_blocks(G * n), kGBlock, s, h->nbr, n, h->nbr_stride, G, kg, mrb,
                                                                          h->tap_pos, mdig, h->mask, mpk_a, mgh));
-        launches += 2;
+        launches += 1;
         bool in_b = false;
         SPCONV_CHECK(wide_sort(mpk_a, mpk_b, G * n, mdig, wgh + kWideKeyPassesMax * kWideBins, wtickets,
                                kWideKeyPassesMax, wlook, h->status, s, &in_b));
@@ -1721,7 +1746,7 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
     } else {
         SPCONV_CHECK(launch_chained(kg_mask_keys, blocks(G * n, kGBlock), kGBlock, s, h->nbr, n, h->nbr_stride, G, kg, h->tap_pos, h->mask,
                                                                 mkey_a, perm_a));
-        launches += 2;
+        launches += 1;
         const bool perm_in_b = rsort::sort_pairs<uint32_t>(mkey_a, perm_a, mkey_b, perm_b, G * n, mbits, hist, s,
                                                            &launches);
         h->perm = reinterpret_cast<int32_t*>(perm_in_b ? perm_b : perm_a);
