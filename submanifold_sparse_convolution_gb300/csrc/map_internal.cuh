@@ -1,5 +1,7 @@
-// Declarations shared by the two kernel-map pipelines (map.cu: one kernel per
-// step, any size; map_fused.cu: one cluster launch for up to kFusedMaxRows).
+// Declarations shared by the kernel-map pipelines (map.cu: one kernel per
+// step, any size; map_fused.cu: one cluster launch for up to kFusedMaxRows;
+// map_wide.cu: whole-GPU passes; map_groups.cu: offset groups, kernel size 5
+// and strided maps).
 #pragma once
 #include <cuda_runtime.h>
 
@@ -137,9 +139,11 @@ int64_t wide_sort_look_words(int64_t n);
 // Stable LSD sort of the n packed values in a by the digits d, one
 // whole-GPU pass per digit (a and b ping-pong), each launched with
 // programmatic dependent launch.  gh[p][kWideBins] holds pass p's digit
-// totals over all n values (counted by the kernel that wrote a); tickets
+// totals over all n values (counted by the kernel that wrote a; a pass in the
+// count-exchange form derives them itself and does not read them); tickets
 // (kWideCounters ints; passes use the ticket indices ticket0, ticket0 + 1,
-// ...) and look are zero before the first pass.  *in_b: the result is in b.
+// ... as tickets or arrival counters) and look are zero before the first
+// pass; look is 16-byte aligned.  *in_b: the result is in b.
 // first_plain: the first pass waits for the whole stream before it (a copy
 // or memset precedes it) rather than overlapping a kernel's tail.
 int wide_sort(uint64_t* a, uint64_t* b, int64_t n, const WideDigits& d, const int32_t* gh, int32_t* tickets,

@@ -3,35 +3,44 @@
 // The cluster pipeline (map_fused.cu) runs every sort pass on the 16 SMs of
 // one thread-block cluster; a pass then costs ~8 us at 32k rows and grows
 // with the rows per SM (~40 us at 240k rows).  Here each stable LSD radix
-// pass is one kernel over all SMs, 1024 keys per CTA, with decoupled
-// look-back: a CTA ranks its keys, publishes its per-digit counts, sums the
-// counts of the CTAs before it (stopping at the first that has published its
-// inclusive prefix), publishes its own inclusive prefix and scatters.  The
-// digit totals of every pass come from one histogram kernel that reads the
-// keys once.  Kernels follow each other with programmatic dependent launch.
-//
-// When every partition of a pass is resident at once (up to ~300 CTAs), the
-// look-back is replaced by two grid barriers: partitions publish their
-// counts, each CTA scans a few digits across all partitions, partitions read
-// their prefixes back -- about seven memory round trips whatever the number
-// of partitions, where a look-back chain grows with it.
+// pass is one kernel over all SMs.  A partition of 1024 keys (2048 from 16k
+// rows, 4096 from 128k rows for digits of up to 9 bits) is ranked stably by
+// one CTA, which then needs, per digit, the keys of that digit in the
+// partitions before it and in all partitions.  It gets them in one of three
+// forms:
+//  - up to 64 resident partitions, a count exchange: every partition writes
+//    its digit counts as self-validating words (an epoch tag in the high
+//    half, two 16-bit counts in the low half), bumps an arrival counter and
+//    reads every partition's words in one round.  That gives the digit
+//    totals as well, so no histogram kernel runs before the pass, and the
+//    first pass of the mask sort makes the mask keys itself;
+//  - up to 256 resident partitions, two grid barriers: partitions publish
+//    their counts, each CTA scans a few digits across all partitions,
+//    partitions read their prefixes back (about seven memory round trips
+//    whatever the number of partitions);
+//  - otherwise decoupled look-back: a CTA takes its partition from a ticket
+//    counter (so it only waits on CTAs already running), publishes its
+//    counts, sums those of the CTAs before it up to the first inclusive
+//    prefix, publishes its own.  The digit totals then come from the
+//    histogram kernel that wrote the keys.
+// Kernels follow each other with programmatic dependent launch.
 //
 // Steps (sorted-key mapper):  pack keys + histograms of all key digits ->
-// key passes -> neighbour search (map_search.cu) -> mask keys + histograms
-// of the mask digits -> mask passes -> per-tile pair counts -> one-CTA scan
-// of the (tap, tile) offsets and the tile order -> pair lists, gather table
-// and row order.  The dense mapper replaces the first three steps by a
-// presence-grid scatter and a 27-lookup pass.  Results are bit-identical to
-// the other pipelines: the same packed keys, the same stable order, the same
-// outputs.  Every kernel lets the next one launch as soon as all of its CTAs
-// run (the next waits for its completion before reading anything).
+// key passes -> neighbour search (map_search.cu) -> mask keys (inside the
+// first mask pass where the exchange runs) -> mask passes -> per-tile pair
+// counts -> (above 1024 tiles) one-CTA scan of the (tap, tile) offsets and
+// the tile order -> pair lists, gather table and row order.  The hash mapper
+// replaces the first three steps by an insert and a lookup, the dense mapper
+// by a presence-grid scatter and a 27-lookup pass.  Results are
+// bit-identical to the other pipelines: the same packed keys, the same
+// stable order, the same outputs.  Every kernel lets the next one launch as
+// soon as all of its CTAs run (the next waits for its completion before
+// reading anything).
 //
-// Look-back state words are (epoch << 32 | flag << 30 | count): every launch
-// that publishes states takes a fresh epoch, so a state left by an earlier
-// launch in the same memory never reads as ready and the buffers need no
-// clearing.  A CTA whose grid may not be resident at once takes its
-// partition from a ticket counter, so it only ever waits on CTAs that are
-// already running.  Every wait is bounded in time.
+// State and count words carry an epoch: every launch that publishes them
+// takes a fresh one, so a word left by an earlier launch in the same memory
+// never reads as ready and the buffers need no clearing.  Every wait is
+// bounded in time.
 #include <cuda_runtime.h>
 
 #include <algorithm>
