@@ -62,7 +62,7 @@ int launch_map_fused(const FusedArgs& a, int cluster, cudaStream_t s);
 // ---- whole-GPU pipeline (map_wide.cu) --------------------------------------
 constexpr int kWideKeysPerCta = 1024;    // keys per CTA (look-back partition) of a sort pass
 constexpr int64_t kBigPassRows = 16384;  // above this, twice as many keys per sort CTA
-constexpr int64_t kHugePassRows = 131072;  // above this, four times as many (digits of up to 9 bits)
+constexpr int64_t kHugePassRows = 131072;  // above this, four times as many
 constexpr int kWideBins = 1024;          // histogram width: digits of up to 10 bits
 constexpr int kDigitBitsWide = 10;
 constexpr int kWideKeyPassesMax = 4;     // coordinate keys of up to 40 bits

@@ -4,7 +4,7 @@
 // one thread-block cluster; a pass then costs ~8 us at 32k rows and grows
 // with the rows per SM (~40 us at 240k rows).  Here each stable LSD radix
 // pass is one kernel over all SMs.  A partition of 1024 keys (2048 from 16k
-// rows, 4096 from 128k rows for digits of up to 9 bits) is ranked stably by
+// rows, 4096 from 128k rows) is ranked stably by
 // one CTA, which then needs, per digit, the keys of that digit in the
 // partitions before it and in all partitions.  It gets them in one of three
 // forms:
@@ -1534,8 +1534,8 @@ namespace {
 // decoupled look-back.
 // The form a pass over n values with digits of `width` bits takes on this
 // device.  Keys per partition: 1024, 2048 above kBigPassRows, 4096 above
-// kHugePassRows for digits of up to 9 bits (fewer partitions: the
-// all-partition form reaches 262k rows).
+// kHugePassRows (fewer partitions: the count exchange reaches 262k rows;
+// stage-sized kernel-size-5 maps 523.9 -> 497.3 us with 10-bit digits too).
 struct PassPlan {
     int size;   // keys per partition: kWideKeysPerCta << size
     bool narrow, ticket, barrier, all;
@@ -1561,10 +1561,10 @@ int plan_wide_pass(int64_t n, int width, PassPlan* pl) {
         cap_pass[dev][1][1] = resident_ctas(k_wide_pass<2 * WI, 4>, WT, sms);
         cap_pass[dev][2][0] = std::min(resident_ctas(k_wide_pass<4 * WI, 2>, WT, sms),
                                        resident_ctas(k_wide_pass<4 * WI, 2, true>, WT, sms));
-        cap_pass[dev][2][1] = 0;   // (not used: wide digits stay at 2048 keys)
+        cap_pass[dev][2][1] = resident_ctas(k_wide_pass<4 * WI, 4>, WT, sms);
     }
     pl->narrow = (1 << width) <= 2 * WT;   // two digits per thread cover the digit values
-    pl->size = n > kHugePassRows && pl->narrow ? 2 : n > kBigPassRows ? 1 : 0;
+    pl->size = n > kHugePassRows ? 2 : n > kBigPassRows ? 1 : 0;
     const int64_t keys_per_cta = static_cast<int64_t>(kWideKeysPerCta) << pl->size;
     pl->parts = (n + keys_per_cta - 1) / keys_per_cta;
     if (pl->parts > 0x7FFFFFFF) return SPCONV_ERR_UNSUPPORTED;
@@ -1614,7 +1614,9 @@ int launch_wide_pass(const uint64_t* in, uint64_t* out, int64_t n, int shift, in
         return pl.size == 2 ? launch_pdl(k_wide_pass<4 * WI, 2, true>, grid, WT, s, pdl, pa)
              : pl.size == 1 ? launch_pdl(k_wide_pass<2 * WI, 2, true>, grid, WT, s, pdl, pa)
                             : launch_pdl(k_wide_pass<WI, 2, true>, grid, WT, s, pdl, pa);
-    if (pl.size == 2) return launch_pdl(k_wide_pass<4 * WI, 2>, grid, WT, s, pdl, pa);
+    if (pl.size == 2)
+        return pl.narrow ? launch_pdl(k_wide_pass<4 * WI, 2>, grid, WT, s, pdl, pa)
+                         : launch_pdl(k_wide_pass<4 * WI, 4>, grid, WT, s, pdl, pa);
     if (pl.size == 1)
         return pl.narrow ? launch_pdl(k_wide_pass<2 * WI, 2>, grid, WT, s, pdl, pa)
                          : launch_pdl(k_wide_pass<2 * WI, 4>, grid, WT, s, pdl, pa);
