@@ -224,28 +224,59 @@ __global__ void __launch_bounds__(kGBlock) kg_search(const uint64_t* __restrict_
         if (cnt[k]) atomicAdd(&tap_count[k], cnt[k]);
 }
 
+// The kernel-map row width of kernel size K (V taps rounded up to whole
+// 16-byte words), which the staged search and lookup below write whole.
+template <int K>
+struct NbrStride {
+    static constexpr int value = (K * K * K + 3) / 4 * 4;
+};
+
+// A block's kernel-map rows, assembled in shared memory (initialised to -1)
+// and written whole, 16 bytes a thread: rows_s[j] goes to row rid(j) of nbr
+// (skipped when rid(j) < 0).  Every thread of the block calls it.
+template <int RB, int ST, typename RowOf>
+__device__ __forceinline__ void write_rows(const int32_t (&rows_s)[RB][ST], RowOf rid, int32_t* __restrict__ nbr) {
+    static_assert(ST % 4 == 0, "rows of whole 16-byte words");
+    constexpr int Q = ST / 4;
+    for (int t = threadIdx.x; t < RB * Q; t += blockDim.x) {
+        const int j = t / Q, c = t % Q;
+        const int64_t r = rid(j);
+        if (r >= 0)
+            reinterpret_cast<int4*>(nbr + r * ST)[c] = reinterpret_cast<const int4*>(&rows_s[j][0])[c];
+    }
+}
+
 // The same search over the packed values (key << rbits | row) for kernel size
 // K, with the K^2 column searches of a row in lockstep: every step of the
 // binary searches issues the probes of all columns still open at once, and
 // the K keys after every lower bound are read together, so a row waits
 // ~log2(n) memory round trips rather than K^2 log2(n).
-constexpr int kLockRows = 128;   // rows per block; K threads per row, one per dx plane
+// The block's rows (at their original row index, scattered) are assembled in
+// shared memory and written whole, so the map needs no -1 fill first (kernel
+// size 5: its 16.6 MB memset and ~50 scattered 4-byte stores per row gone).
+template <int K>
+struct LockRows {   // rows per block; K threads per row, one per dx plane
+    static constexpr int value = K == 3 ? 128 : 64;
+};
 
 template <int K>
-__global__ void __launch_bounds__(kLockRows * K) kg_search_lockstep(const uint64_t* __restrict__ sv, int64_t n,
-                                                                    int rbits, uint64_t no_key, const GLayout L,
-                                                                    int32_t* __restrict__ nbr,
-                                                                    int32_t* __restrict__ tap_count,
-                                                                    int32_t* __restrict__ status) {
+__global__ void __launch_bounds__(LockRows<K>::value * K) kg_search_lockstep(const uint64_t* __restrict__ sv, int64_t n,
+                                                                             int rbits, uint64_t no_key, const GLayout L,
+                                                                             int32_t* __restrict__ nbr,
+                                                                             int32_t* __restrict__ tap_count,
+                                                                             int32_t* __restrict__ status) {
     pdl_trigger();
     pdl_wait();
-    constexpr int R = (K - 1) / 2, V = K * K * K;
+    constexpr int R = (K - 1) / 2, V = K * K * K, LR = LockRows<K>::value, ST = NbrStride<K>::value;
     __shared__ int32_t cnt[V];
-    for (int k = threadIdx.x; k < V; k += kLockRows * K) cnt[k] = 0;
-    __syncthreads();
-    const int plane = threadIdx.x / kLockRows;   // dx = plane - R (warp-uniform)
+    __shared__ __align__(16) int32_t rows_s[LR][ST];
+    __shared__ int64_t rid[LR];
+    for (int k = threadIdx.x; k < V; k += LR * K) cnt[k] = 0;
+    for (int k = threadIdx.x; k < LR * ST; k += LR * K) (&rows_s[0][0])[k] = -1;
+    const int plane = threadIdx.x / LR;   // dx = plane - R (warp-uniform)
+    const int rl = threadIdx.x % LR;
     const uint64_t rmask = (uint64_t(1) << rbits) - 1;
-    const int64_t s = static_cast<int64_t>(blockIdx.x) * kLockRows + threadIdx.x % kLockRows;
+    const int64_t s = static_cast<int64_t>(blockIdx.x) * LR + rl;
     bool ok = s < n;
     uint64_t q = 0;
     int64_t row = 0;
@@ -256,6 +287,8 @@ __global__ void __launch_bounds__(kLockRows * K) kg_search_lockstep(const uint64
         ok = q != no_key;
         if (ok && plane == R && s > 0 && (__ldcg(sv + s - 1) >> rbits) == q) atomicOr(status, kStatusDuplicate);
     }
+    if (plane == 0) rid[rl] = s < n ? row : -1;   // (a row out of range is written as all -1)
+    __syncthreads();
     if (ok) {
         // the plane's K columns c = K plane + e; those before the row's own
         // column hold smaller keys than its own, those after it larger ones
@@ -298,14 +331,15 @@ __global__ void __launch_bounds__(kLockRows * K) kg_search_lockstep(const uint64
                 const uint64_t d = (vv[j] >> rbits) - lo_t;
                 if (vv[j] != ~0ull && d <= static_cast<uint64_t>(2 * R)) {
                     const int k = c * K + static_cast<int>(d);
-                    nbr[row * L.stride + k] = static_cast<int32_t>(vv[j] & rmask);
+                    rows_s[rl][k] = static_cast<int32_t>(vv[j] & rmask);
                     atomicAdd(&cnt[k], 1);
                 }
             }
         }
     }
     __syncthreads();
-    for (int k = threadIdx.x; k < V; k += kLockRows * K)
+    write_rows(rows_s, [&](int j) { return rid[j]; }, nbr);
+    for (int k = threadIdx.x; k < V; k += LR * K)
         if (cnt[k]) atomicAdd(&tap_count[k], cnt[k]);
 }
 
@@ -374,8 +408,8 @@ __global__ void __launch_bounds__(kGBlock) kg_hash_insert(const int4* __restrict
 // K threads per row, one per dx plane (kLookRows rows per block, each warp
 // in one plane): the plane's K columns' bucket reads (r + 1 pairs each) in
 // flight together; the rare reads that meet a full bucket go on, all of the
-// warp's in the same extra round.  nbr is cleared to -1 beforehand; only
-// present neighbours are written.
+// warp's in the same extra round.  The block's rows are staged in
+// shared memory (absent neighbours -1) and written whole.
 template <int K>
 struct LookRows {
     static constexpr int value = K == 3 ? 128 : 64;   // 5 x 64 threads keep the 15 bucket reads in registers
@@ -390,12 +424,17 @@ __global__ void __launch_bounds__(LookRows<K>::value * K) kg_hash_lookup(const i
     pdl_trigger();
     pdl_wait();
     constexpr int r = (K - 1) / 2, V = K * K * K, NP = r + 1;   // pairs per column
-    constexpr int kRows = LookRows<K>::value;
+    constexpr int kRows = LookRows<K>::value, ST = NbrStride<K>::value;
     __shared__ int32_t cnt[V];
+    // the block's rows (consecutive), written whole at the end: no -1 fill of the map first
+    __shared__ __align__(16) int32_t rows_s[kRows][ST];
     for (int k = threadIdx.x; k < V; k += kRows * K) cnt[k] = 0;
+    for (int k = threadIdx.x; k < kRows * ST; k += kRows * K) (&rows_s[0][0])[k] = -1;
     __syncthreads();
     const int p = threadIdx.x / kRows;   // this thread's dx plane
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * kRows + threadIdx.x % kRows;
+    const int il = threadIdx.x % kRows;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kRows;
+    const int64_t i = row0 + il;
     const bool ok = i < n && in_range(coords[i], shape, batch);
     const uint64_t key = ok ? g_key(coords[i], L) : 0ull;
     const int lb = log2 - 2;
@@ -427,7 +466,7 @@ __global__ void __launch_bounds__(LookRows<K>::value * K) kg_hash_lookup(const i
                     open |= sl[j] == 0ull;
                     const uint64_t d = (sl[j] >> row_bits) - lo_t;
                     if (sl[j] != 0ull && d < static_cast<uint64_t>(K)) {
-                        nbr[i * L.stride + K * K * p + K * c + static_cast<int>(d)] = static_cast<int32_t>(sl[j] & rmask);
+                        rows_s[il][K * K * p + K * c + static_cast<int>(d)] = static_cast<int32_t>(sl[j] & rmask);
                         found |= 1u << (K * c + static_cast<int>(d));
                     }
                 }
@@ -448,6 +487,7 @@ __global__ void __launch_bounds__(LookRows<K>::value * K) kg_hash_lookup(const i
         }
     }
     __syncthreads();
+    write_rows(rows_s, [&](int j) { return row0 + j < n ? row0 + j : int64_t(-1); }, nbr);
     for (int k = threadIdx.x; k < V; k += kRows * K)
         if (cnt[k]) atomicAdd(&tap_count[k], cnt[k]);
 }
@@ -1644,7 +1684,12 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
         SPCONV_CHECK_CUDA(cudaMemsetAsync(h->tap_off, 0, (V + 1) * sizeof(int32_t), s));
         return cuda_status(cudaGetLastError());
     }
-    SPCONV_CHECK_CUDA(cudaMemsetAsync(h->nbr, 0xFF, static_cast<size_t>(n) * h->nbr_stride * sizeof(int32_t), s));
+    // the staged search and lookup (kernel size 3 or 5) write every entry of
+    // the map's rows; the other mappers fill only the neighbours they find
+    // (rows of NbrStride<K> entries: the stride set above for every K)
+    const bool staged = (K == 3 || K == 5) && !src && (wide_coord || mapper == SPCONV_MAPPER_HASH);
+    if (!staged)
+        SPCONV_CHECK_CUDA(cudaMemsetAsync(h->nbr, 0xFF, static_cast<size_t>(n) * h->nbr_stride * sizeof(int32_t), s));
 
     const int4* c4 = reinterpret_cast<const int4*>(coords);
     const int3 shape3 = make_int3(X, Y, Z);
@@ -1671,11 +1716,11 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
         const uint64_t* sv = in_b ? ck_b : ck_a;
         const uint64_t no_key = (uint64_t(1) << ckb) - 1;
         if (K == 3)
-            SPCONV_CHECK(launch_chained(kg_search_lockstep<3>, blocks(n, kLockRows), kLockRows * 3, s, sv, n, mrb, no_key, L, h->nbr,
-                                                                              h->tap_count, h->status));
+            SPCONV_CHECK(launch_chained(kg_search_lockstep<3>, blocks(n, LockRows<3>::value), LockRows<3>::value * 3, s, sv,
+                                        n, mrb, no_key, L, h->nbr, h->tap_count, h->status));
         else if (K == 5)
-            SPCONV_CHECK(launch_chained(kg_search_lockstep<5>, blocks(n, kLockRows), kLockRows * 5, s, sv, n, mrb, no_key, L, h->nbr,
-                                                                              h->tap_count, h->status));
+            SPCONV_CHECK(launch_chained(kg_search_lockstep<5>, blocks(n, LockRows<5>::value), LockRows<5>::value * 5, s, sv,
+                                        n, mrb, no_key, L, h->nbr, h->tap_count, h->status));
         else
             SPCONV_CHECK(launch_chained(kg_search<true>, blocks(n, kGBlock), kGBlock, s, sv, nullptr, n, mrb, no_key, L, h->nbr,
                                                                    h->tap_count, h->status));
