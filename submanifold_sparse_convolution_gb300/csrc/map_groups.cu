@@ -1707,12 +1707,14 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
         // row's all-ones key orders it last; the whole-GPU sort, then the search
         uint64_t* ck_a = take<uint64_t>(p, n1);
         uint64_t* ck_b = take<uint64_t>(p, n1);
-        kg_pack_keys_packed<<<capped_blocks(n), kGBlock, 0, s>>>(c4, n, shape3, B, L, ckb, mrb, cdig, ck_a, wgh,
-                                                                 h->status);
+        // (the digits are counted only for passes that read the totals)
+        bool ctot = false;
+        SPCONV_CHECK(wide_sort_reads_totals(n, cdig, &ctot));
+        kg_pack_keys_packed<<<capped_blocks(n), kGBlock, 0, s>>>(c4, n, shape3, B, L, ckb, mrb,
+                                                                 ctot ? cdig : no_counts(cdig), ck_a, wgh, h->status);
         ++launches;
         bool in_b = false;
         SPCONV_CHECK(wide_sort(ck_a, ck_b, n, cdig, wgh, wtickets, 0, wlook, h->status, s, &in_b));
-        launches += cdig.passes;
         const uint64_t* sv = in_b ? ck_b : ck_a;
         const uint64_t no_key = (uint64_t(1) << ckb) - 1;
         if (K == 3)
@@ -1770,22 +1772,24 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
     const unsigned tiles = static_cast<unsigned>(G * T);
     if (wide_mask) {
         int32_t* mgh = wgh + kWideKeyPassesMax * kWideBins;
+        bool mtot = false;
+        SPCONV_CHECK(wide_sort_reads_totals(G * n, mdig, &mtot));
+        const WideDigits mcnt = mtot ? mdig : no_counts(mdig);   // digits the key kernel counts
         if (K == 5 && h->nbr_stride == 128)
             SPCONV_CHECK(launch_chained(kg_mask_keys_rows<5>, capped_blocks(4 * n), kGBlock, s, h->nbr, n, G, kg, mrb,
-                                        static_cast<const int32_t*>(h->tap_count), calibrated, h->tap_pos, mdig,
+                                        static_cast<const int32_t*>(h->tap_count), calibrated, h->tap_pos, mcnt,
                                         h->mask, mpk_a, mgh));
         else if (K == 3 && h->nbr_stride == 28)
             SPCONV_CHECK(launch_chained(kg_mask_keys_rows<3>, capped_blocks(4 * n), kGBlock, s, h->nbr, n, G, kg, mrb,
-                                        static_cast<const int32_t*>(h->tap_count), calibrated, h->tap_pos, mdig,
+                                        static_cast<const int32_t*>(h->tap_count), calibrated, h->tap_pos, mcnt,
                                         h->mask, mpk_a, mgh));
         else
             SPCONV_CHECK(launch_chained(kg_mask_keys_packed, capped_blocks(G * n), kGBlock, s, h->nbr, n, h->nbr_stride, G, kg, mrb,
-                                                                         h->tap_pos, mdig, h->mask, mpk_a, mgh));
+                                                                         h->tap_pos, mcnt, h->mask, mpk_a, mgh));
         launches += 1;
         bool in_b = false;
         SPCONV_CHECK(wide_sort(mpk_a, mpk_b, G * n, mdig, wgh + kWideKeyPassesMax * kWideBins, wtickets,
                                kWideKeyPassesMax, wlook, h->status, s, &in_b));
-        launches += mdig.passes;
         SPCONV_CHECK(launch_chained(kg_tile_count<true>, tiles, kTileRows, s, h->perm, in_b ? mpk_b : mpk_a, mrb, h->mask, n, T, kg, counts,
                                                         h->tile_union));
     } else {
@@ -1913,8 +1917,14 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
     if (n_in > 0) {
         const int3 ishape = make_int3(h->shape[0], h->shape[1], h->shape[2]);
         if (wide_cand) {
+            // the distinct sites number at most m: where a sort of m values runs
+            // every pass in the count exchange, so does theirs (fewer partitions),
+            // and their digits need no counting
+            bool stot = false;
+            SPCONV_CHECK(wide_sort_reads_totals(m, cdig, &stot));
             kst_dedupe<<<capped_blocks(8 * n_in), kGBlock, 0, s>>>(reinterpret_cast<const int4*>(coords), n_in, ishape,
-                                                               h->batch, O, cset, set_log2, cdig, ka, count, wgh);
+                                                               h->batch, O, cset, set_log2,
+                                                               stot ? cdig : no_counts(cdig), ka, count, wgh);
             ++launches;
             // the one synchronisation: the number of distinct sites sizes the map
             SPCONV_CHECK_CUDA(cudaMemcpyAsync(&n_out, count, 8, cudaMemcpyDeviceToHost, s));
@@ -1922,7 +1932,6 @@ int build_map_strided(MapHandle* h, const int32_t* coords, int64_t n_in, const s
             if (n_out > 0) {
                 bool in_b = false;
                 SPCONV_CHECK(wide_sort(ka, kb, n_out, cdig, wgh, wtickets, 0, wlook, wstatus, s, &in_b, true));
-                launches += cdig.passes;
                 SPCONV_CHECK(launch_chained(kst_outputs_sorted, blocks(n_out, kGBlock), kGBlock, s, 
                     in_b ? kb : ka, n_out, O, reinterpret_cast<int4*>(h->out_coords), query));
                 ++launches;

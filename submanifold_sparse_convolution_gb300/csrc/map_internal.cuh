@@ -148,6 +148,15 @@ int64_t wide_sort_look_words(int64_t n);
 // or memset precedes it) rather than overlapping a kernel's tail.
 int wide_sort(uint64_t* a, uint64_t* b, int64_t n, const WideDigits& d, const int32_t* gh, int32_t* tickets,
               int ticket0, uint64_t* look, int32_t* status, cudaStream_t s, bool* in_b, bool first_plain = false);
+// Whether a sort of up to n values by the digits d reads digit totals
+// counted beforehand (gh): not when every pass runs in the count exchange,
+// whose partitions derive the totals from each other's counts.  The kernel
+// that writes the values then need not count them: it gets no_counts(d).
+int wide_sort_reads_totals(int64_t n, const WideDigits& d, bool* reads);
+inline WideDigits no_counts(WideDigits d) {
+    d.passes = 0;
+    return d;
+}
 
 // In a kernel whose every thread calls it together (whole warps): adds the
 // digits of v under d to the block's histograms h[pass][digit] when valid.

@@ -1644,6 +1644,16 @@ int64_t wide_sort_look_words(int64_t n) {
     return (n + keys_per_cta - 1) / keys_per_cta * kWideBins;
 }
 
+int wide_sort_reads_totals(int64_t n, const WideDigits& d, bool* reads) {
+    *reads = false;
+    for (int p = 0; p < d.passes; ++p) {
+        PassPlan pl;
+        SPCONV_CHECK(plan_wide_pass(std::max<int64_t>(1, n), d.width[p], &pl));
+        if (!pl.all) *reads = true;
+    }
+    return SPCONV_OK;
+}
+
 int wide_sort(uint64_t* a, uint64_t* b, int64_t n, const WideDigits& d, const int32_t* gh, int32_t* tickets,
               int ticket0, uint64_t* look, int32_t* status, cudaStream_t s, bool* in_b, bool first_plain) {
     *in_b = false;
@@ -1706,8 +1716,17 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
             kd.shift[p] = at;
             at += kd.width[p];
         }
-        SPCONV_CHECK(few ? launch_pdl(k_wide_keys<1>, key_blocks, WT, s, true, a, kd)
-                         : launch_pdl(k_wide_keys<4>, key_blocks, WT, s, true, a, kd));
+        // (no digit counts where every key pass runs in the count exchange)
+        KeyDigits kc = kd;
+        bool reads = false;
+        for (int p = 0; p < passes; ++p) {
+            PassPlan pl;
+            SPCONV_CHECK(plan_wide_pass(n, kd.width[p], &pl));
+            reads |= !pl.all;
+        }
+        if (!reads) kc.passes = 0;
+        SPCONV_CHECK(few ? launch_pdl(k_wide_keys<1>, key_blocks, WT, s, true, a, kc)
+                         : launch_pdl(k_wide_keys<4>, key_blocks, WT, s, true, a, kc));
         for (int p = 0; p < passes; ++p)
             SPCONV_CHECK(pass((p & 1) ? a.vb : a.va, (p & 1) ? a.va : a.vb, a.row_bits + kd.shift[p], kd.width[p],
                               a.gh + p * kWideBins, p));

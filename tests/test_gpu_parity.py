@@ -903,6 +903,13 @@ def test_launch_count_reported():
     assert sc.last_launch_count() == 10               # 74 partitions: the mask-key kernel; the tile scan
     sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, pipeline="multi")
     assert sc.last_launch_count() > 5
+    # kernel size 5 (5 groups), sorted keys; every whole-GPU pass counted once
+    sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, kernel_size=5, mapper="sorted")
+    assert sc.last_launch_count() == 10         # pack, 2 passes (16-bit keys), search, mask keys,
+                                                # 3 passes, tile count/write
+    sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, groups=3, mapper="hash")
+    assert sc.last_launch_count() == 7          # insert, lookup, mask keys, 2 passes (11-bit keys),
+                                                # tile count/write
     sc.subm_forward(m, wl.feats.cuda(), wl.weights[0].cuda())
     assert sc.last_launch_count() == 2          # weight pack + GEMM
     mt = sc.build_map(wl.coords.cuda(), wl.spatial_shape, 1, gemm="tap_major")
