@@ -1088,13 +1088,16 @@ __global__ void __launch_bounds__(kTileRows) k_wide_tile_count(const WideArgs a,
     if (t == 0 && err) atomicOr(a.status, err);
 }
 
-// One CTA: the exclusive scan of the (tap, tile) counts in tap-major order
-// (each tap's list starts where the previous tap's ends) in place, the tap
-// offsets and totals, and the tiles in descending order of union size,
-// stable in the tile index (a counting sort over the 28 sizes: warp w takes
-// a contiguous range of tiles, 32 at a time).  It is a chain of dependent
-// steps on one SM, so its global reads are issued together up front: the
-// first round of counts and (up to kUnionCache tiles) every tile's union.
+// The exclusive scan of the (tap, tile) counts in tap-major order (each
+// tap's list starts where the previous tap's ends) in place, the tap offsets
+// and totals, and the tiles in descending order of union size, stable in the
+// tile index.  One launch of kTaps + 1 CTAs: CTA k < kTaps scans tap k's T
+// counts from the tap's start, the exclusive sum of the per-tap pair totals
+// the lookup counted (so the taps need nothing from each other; a tap whose
+// counts do not add up to its total is reported); CTA kTaps does the tile
+// order, a counting sort over the 28 union sizes in which warp w takes a
+// contiguous range of tiles, 32 at a time.  (One CTA doing all of it was a
+// chain of 27 T / 8192 rounds: 24.8 us on stage's 1,875 tiles.)
 constexpr int kScanThreads = 1024;
 constexpr int kScanWarps = kScanThreads / 32;
 constexpr int kScanPer = 8;                          // values per thread and round
@@ -1107,77 +1110,94 @@ __global__ void __launch_bounds__(kScanThreads) k_wide_tile_scan(const WideArgs 
     __shared__ int32_t wsum[kScanWarps];
     __shared__ int32_t wcnt[kScanWarps][kTaps + 1];
     __shared__ int32_t bbase[kTaps + 1];
-    __shared__ int32_t tap_sum;
+    __shared__ int32_t tap_sum, tap_start;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const int64_t T = a.n_tiles;
-    const int64_t m = kTaps * T;
     const bool cached = T <= kUnionCache;
     if (t < kScanWarps * (kTaps + 1)) (&wcnt[0][0])[t] = 0;
     if (t == 0) tap_sum = 0;
     pdl_wait();   // counts and unions of every tile are complete
     pdl_trigger();
-    // the unions, in flight together with the first round of counts
+    if (blockIdx.x < kTaps) {
+        const int k = blockIdx.x;
+        // the taps' starts: an exclusive scan of the per-tap totals (warp 0)
+        if (w == 0) {
+            const int32_t tot = lane < kTaps ? __ldcg(a.tap_count + lane) : 0;
+            int32_t inc = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            if (lane == k) tap_start = inc - tot;
+            if (k == 0) {   // CTA 0 writes the tap offsets and the pair total
+                if (lane < kTaps) a.tap_off[lane] = inc - tot;
+                if (lane == kTaps - 1) {
+                    a.tap_off[kTaps] = inc;
+                    a.totals[0] = inc;
+                }
+            }
+        }
+        __syncthreads();
+        // tap k's counts, in rounds of kScanRound values: coalesced loads into
+        // shared memory, each thread scans kScanPer consecutive values there,
+        // a block scan of the thread sums, coalesced stores
+        int32_t* seg = a.seg_off + static_cast<int64_t>(k) * T;
+        const int32_t first = tap_start;
+        int32_t carry = first;
+        for (int64_t r0 = 0; r0 < T; r0 += kScanRound) {
+#pragma unroll
+            for (int q = 0; q < kScanPer; ++q) {
+                const int64_t i = r0 + static_cast<int64_t>(q) * kScanThreads + t;
+                buf[q * kScanThreads + t] = i < T ? __ldcg(seg + i) : 0;
+            }
+            __syncthreads();
+            int4 v[kScanPer / 4];
+#pragma unroll
+            for (int q = 0; q < kScanPer / 4; ++q) v[q] = reinterpret_cast<const int4*>(buf)[t * (kScanPer / 4) + q];
+            int32_t sum = 0;
+#pragma unroll
+            for (int q = 0; q < kScanPer / 4; ++q) sum += v[q].x + v[q].y + v[q].z + v[q].w;
+            int32_t inc = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            if (lane == 31) wsum[w] = inc;
+            __syncthreads();
+            int32_t before = 0, total = 0;
+            for (int i = 0; i < kScanWarps; ++i) {
+                const int32_t x = wsum[i];
+                before += i < w ? x : 0;
+                total += x;
+            }
+            int32_t run = carry + before + inc - sum;
+#pragma unroll
+            for (int q = 0; q < kScanPer / 4; ++q) {
+                int4 o4;
+                o4.x = run; run += v[q].x;
+                o4.y = run; run += v[q].y;
+                o4.z = run; run += v[q].z;
+                o4.w = run; run += v[q].w;
+                reinterpret_cast<int4*>(buf)[t * (kScanPer / 4) + q] = o4;
+            }
+            carry += total;
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < kScanPer; ++q) {
+                const int64_t i = r0 + static_cast<int64_t>(q) * kScanThreads + t;
+                if (i < T) seg[i] = buf[q * kScanThreads + t];
+            }
+            __syncthreads();   // buf and wsum are reused
+        }
+        if (t == 0 && carry - first != __ldcg(a.tap_count + k)) atomicOr(a.status, kStatusInternal);
+        return;
+    }
+    // ---- tile order (CTA kTaps); the unions up to kUnionCache tiles in shared memory
     if (cached)
         for (int64_t i = t; i < T; i += kScanThreads) uc[i] = __ldcg(a.tile_union + i);
-    // ---- pair offsets, in rounds of kScanRound values: coalesced loads into
-    // shared memory, each thread scans kScanPer consecutive values there,
-    // a block scan of the thread sums, coalesced stores
-    int32_t carry = 0;
-    for (int64_t r0 = 0; r0 < m; r0 += kScanRound) {
-#pragma unroll
-        for (int k = 0; k < kScanPer; ++k) {
-            const int64_t i = r0 + static_cast<int64_t>(k) * kScanThreads + t;
-            buf[k * kScanThreads + t] = i < m ? __ldcg(a.seg_off + i) : 0;
-        }
-        __syncthreads();
-        int4 v[kScanPer / 4];
-#pragma unroll
-        for (int k = 0; k < kScanPer / 4; ++k) v[k] = reinterpret_cast<const int4*>(buf)[t * (kScanPer / 4) + k];
-        int32_t sum = 0;
-#pragma unroll
-        for (int k = 0; k < kScanPer / 4; ++k) sum += v[k].x + v[k].y + v[k].z + v[k].w;
-        int32_t inc = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-            if (lane >= o) inc += y;
-        }
-        if (lane == 31) wsum[w] = inc;
-        __syncthreads();
-        int32_t before = 0, total = 0;
-        for (int i = 0; i < kScanWarps; ++i) {
-            const int32_t x = wsum[i];
-            before += i < w ? x : 0;
-            total += x;
-        }
-        int32_t run = carry + before + inc - sum;
-#pragma unroll
-        for (int k = 0; k < kScanPer / 4; ++k) {
-            int4 o4;
-            o4.x = run; run += v[k].x;
-            o4.y = run; run += v[k].y;
-            o4.z = run; run += v[k].z;
-            o4.w = run; run += v[k].w;
-            reinterpret_cast<int4*>(buf)[t * (kScanPer / 4) + k] = o4;
-        }
-        carry += total;
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < kScanPer; ++k) {
-            const int64_t i = r0 + static_cast<int64_t>(k) * kScanThreads + t;
-            if (i < m) a.seg_off[i] = buf[k * kScanThreads + t];
-        }
-        if (t < kTaps) {   // the taps whose first pair falls in this round
-            const int64_t at = static_cast<int64_t>(t) * T - r0;
-            if (at >= 0 && at < kScanRound) a.tap_off[t] = buf[at];
-        }
-        __syncthreads();   // buf and wsum are reused
-    }
-    if (t == 0) {
-        a.tap_off[kTaps] = carry;
-        a.totals[0] = carry;
-    }
-    // ---- tile order
+    __syncthreads();
     const int64_t tw = (T + kScanWarps - 1) / kScanWarps;
     const int64_t t0 = w * tw < T ? w * tw : T;
     const int64_t t1 = t0 + tw < T ? t0 + tw : T;
@@ -1759,7 +1779,8 @@ int launch_map_wide(const WideArgs& a, int sms, cudaStream_t s) {
     if (a.n_tiles <= kPrefixTiles) {
         SPCONV_CHECK(launch_pdl(k_wide_tile_write<true>, tiles, kTwThreads, s, true, a, ms));
     } else {
-        SPCONV_CHECK(launch_pdl(k_wide_tile_scan, 1u, static_cast<unsigned>(kScanThreads), s, true, a));
+        SPCONV_CHECK(launch_pdl(k_wide_tile_scan, static_cast<unsigned>(kTaps + 1), static_cast<unsigned>(kScanThreads), s,
+                                true, a));
         SPCONV_CHECK(launch_pdl(k_wide_tile_write<false>, tiles, kTwThreads, s, true, a, ms));
     }
     return SPCONV_OK;
