@@ -779,41 +779,59 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_count(int32_t* __restrict__
     }
 }
 
-// One block: exclusive scan of counts[V][T] into seg_off, the tap offsets and
-// the pair total; each group's tiles ordered by descending union size
-// (stable), with the number of tiles whose union is not empty (they come
-// first); the sum of union sizes over all tiles.
+// The (tap, tile) counts scanned into the per-tap pair offsets, the tap
+// offsets and the pair total; each group's tiles in descending order of
+// union size (stable), with the number of tiles whose union is not empty
+// (they come first); the sum of union sizes over all tiles.  One launch of
+// V + 1 CTAs: CTA k < V scans tap k's T counts from
+// the tap's start, the exclusive sum of the per-tap pair totals the search
+// counted (a tap whose counts do not add up to its total is reported); CTA V
+// does the tile orders.  (One CTA scanning all V T counts took ~29 rounds on
+// a kernel-size-5 stage map.)
 __global__ void __launch_bounds__(1024) kg_scan_tiles(const int32_t* __restrict__ counts, int V, int G, int kg,
-                                                      int64_t n_tiles, const uint32_t* __restrict__ tile_union,
+                                                      int64_t n_tiles, const int32_t* __restrict__ tap_count,
+                                                      const uint32_t* __restrict__ tile_union,
                                                       int32_t* __restrict__ seg_off, int32_t* __restrict__ tap_off,
                                                       int32_t* __restrict__ totals,
                                                       int32_t* __restrict__ tile_order,
-                                                      int32_t* __restrict__ nonempty) {
+                                                      int32_t* __restrict__ nonempty, int32_t* __restrict__ status) {
     pdl_trigger();
     pdl_wait();
     __shared__ int32_t hist[kMaxGroups][kMaxGroupTaps + 1];
-    for (int i = threadIdx.x; i < kMaxGroups * (kMaxGroupTaps + 1); i += 1024) (&hist[0][0])[i] = 0;
-    const int64_t m = V * n_tiles;
-    // seg_off is the exclusive scan of counts; a tap's list starts at the
-    // offset of its first tile (one division per run of entries)
-    const int32_t total = rsort::block_scan_exclusive(
-        counts, seg_off, m, [&](int64_t i0, const int32_t (&v)[rsort::kScanPer]) {
-            int64_t k = i0 / n_tiles, t = i0 - k * n_tiles;
+    __shared__ int32_t pre[kMaxTaps + 1];   // exclusive prefix of the tap totals, and their sum
+    __shared__ int32_t wpre[4];
+    static_assert(kMaxTaps < 128, "four warps scan the tap totals");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (static_cast<int>(blockIdx.x) < V) {
+        const int k = blockIdx.x;
+        int32_t tot = 0, inc = 0;
+        if (warp < 4) {
+            tot = threadIdx.x < V ? __ldcg(tap_count + threadIdx.x) : 0;
+            inc = tot;
 #pragma unroll
-            for (int j = 0; j < rsort::kScanPer; ++j) {
-                if (t == 0 && i0 + j < m) tap_off[k] = v[j];
-                if (++t == n_tiles) {
-                    t = 0;
-                    ++k;
-                }
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (lane >= o) inc += y;
             }
-        });
-    if (threadIdx.x == 0) {
-        tap_off[V] = total;
-        totals[0] = total;
+            if (lane == 31) wpre[warp] = inc;
+        }
+        __syncthreads();
+        if (warp < 4) {
+            int32_t before = 0;
+            for (int q = 0; q < warp; ++q) before += wpre[q];
+            if (static_cast<int>(threadIdx.x) <= V) pre[threadIdx.x] = before + inc - tot;
+        }
+        __syncthreads();
+        if (k == 0) {   // CTA 0 writes the tap offsets and the pair total
+            for (int i = threadIdx.x; i <= V; i += 1024) tap_off[i] = pre[i];
+            if (threadIdx.x == 0) totals[0] = pre[V];
+        }
+        const int32_t end = rsort::block_scan_exclusive(counts + k * n_tiles, seg_off + k * n_tiles, n_tiles,
+                                                        rsort::NoVisit(), pre[k]);
+        if (threadIdx.x == 0 && end != pre[k + 1]) atomicOr(status, kStatusInternal);
+        return;
     }
-    if (n_tiles == 0)
-        for (int k = threadIdx.x; k < V; k += 1024) tap_off[k] = 0;
+    for (int i = threadIdx.x; i < kMaxGroups * (kMaxGroupTaps + 1); i += 1024) (&hist[0][0])[i] = 0;
     __syncthreads();
     // per group, a counting sort of its tiles by descending union size, stable in t
     int32_t tap_sum = 0;
@@ -840,7 +858,6 @@ __global__ void __launch_bounds__(1024) kg_scan_tiles(const int32_t* __restrict_
     // warp g places group g's tiles, 32 at a time: each at its bucket's next
     // free position, tiles of one bucket in t order (ranked among the lanes
     // that share the bucket)
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (warp < G) {
         const uint32_t* un = tile_union + warp * n_tiles;
         int32_t* ord = tile_order + warp * n_tiles;
@@ -1826,8 +1843,9 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
                                         h->totals, h->tile_order, h->tile_nonempty, h->in_rows, h->out_rows, h->gtab));
         launches -= 1;
     } else {
-        SPCONV_CHECK(launch_chained(kg_scan_tiles, 1, 1024, s, counts, V, G, kg, T, h->tile_union, h->seg_off, h->tap_off, h->totals,
-                                         h->tile_order, h->tile_nonempty));
+        SPCONV_CHECK(launch_chained(kg_scan_tiles, static_cast<unsigned>(V + 1), 1024u, s, counts, V, G, kg, T,
+                                    static_cast<const int32_t*>(h->tap_count), h->tile_union, h->seg_off, h->tap_off,
+                                    h->totals, h->tile_order, h->tile_nonempty, h->status));
         SPCONV_CHECK(launch_chained(kg_tile_write, tiles, kTileRows, s, h->perm, h->mask, h->nbr, h->nbr_stride, n, T,
                                     h->n_pad, kg, h->seg_off, h->in_rows, h->out_rows, h->gtab));
     }

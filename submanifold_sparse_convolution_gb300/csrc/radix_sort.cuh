@@ -65,17 +65,19 @@ __global__ void __launch_bounds__(kThreads) upsweep(const K* __restrict__ keys, 
 // the block's 32 warp sums; every load of a round is issued before its first
 // barrier.  on(i0, v) is called once per round by every thread whose run
 // starts inside the array, after it stored dst[i0 + j] = v[j] for the j with
-// i0 + j < m.  Returns the total, in every thread.
+// i0 + j < m.  The scan starts from carry0 (dst[0] = carry0); returns
+// carry0 plus the total, in every thread.
 constexpr int kScanPer = 16;
 static_assert(kScanThreads == 1024, "the block scan holds one warp sum per lane");
 
 template <typename F>
-__device__ __forceinline__ int32_t block_scan_exclusive(const int32_t* src, int32_t* dst, int64_t m, F on) {
+__device__ __forceinline__ int32_t block_scan_exclusive(const int32_t* src, int32_t* dst, int64_t m, F on,
+                                                        int32_t carry0 = 0) {
     __shared__ int32_t wsum[2][kScanThreads / 32];
     constexpr int64_t kRound = static_cast<int64_t>(kScanPer) * kScanThreads;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const bool vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) == 0;
-    int32_t carry = 0;
+    int32_t carry = carry0;
     int buf = 0;
     for (int64_t base = 0; base < m; base += kRound, buf ^= 1) {
         const int64_t i0 = base + static_cast<int64_t>(kScanPer) * t;
