@@ -253,6 +253,29 @@ def test_dense_and_sorted_mappers_agree(name):
             assert torch.equal(a[key], b[key]), (mapper, key)
 
 
+def test_dense_mapper_past_the_self_scanning_tile_limits():
+    """A dense-grid map with more tiles than the tile writes that scan for
+    themselves take (1024 for one group, 512 per group): the tile scans then
+    start every tap's list from the per-tap totals the grid lookup counted.
+    Kernel size 3 against the oracle and the hash mapper; kernel size 5 (five
+    groups, 1,172 tiles each) against the sorted mapper."""
+    wl = S.random_cloud(61, 150000, shape=(160, 160, 160))
+    a = sc.map_export(build(wl, "dense", pipeline="wide"))
+    assert a["info"]["mapper"] == "dense" and a["info"]["n_tiles"] > 1024
+    assert_map_equal(a, oracle_map(wl.coords.numpy(), wl.spatial_shape, wl.batch_size))
+    b = sc.map_export(build(wl, "hash", pipeline="wide"))
+    for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
+        assert torch.equal(a[key], b[key]), key
+    c5 = wl.coords.cuda()
+    d5 = sc.build_map(c5, wl.spatial_shape, 1, kernel_size=5, mapper="dense")
+    s5 = sc.build_map(c5, wl.spatial_shape, 1, kernel_size=5, mapper="sorted")
+    assert sc.map_status(d5) == 0 and sc.map_status(s5) == 0
+    ed, es = sc.map_export(d5), sc.map_export(s5)
+    assert ed["info"]["mapper"] == "dense" and ed["info"]["groups"] == 5
+    for key in ("nbr", "mask", "perm", "tap_off", "in_rows", "out_rows"):
+        assert torch.equal(ed[key], es[key]), key
+
+
 def test_derived_shape_and_batch():
     wl = S.random_cloud(21, 900, shape=(10, 11, 12), batch_size=3)
     explicit = sc.map_export(build(wl))
