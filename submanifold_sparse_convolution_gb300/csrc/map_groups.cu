@@ -120,8 +120,9 @@ __global__ void __launch_bounds__(kGBlock) kg_pack_keys(const int4* __restrict__
 
 // The same keys packed with the row for the whole-GPU sort: (key << rbits) |
 // row, the key kb = key_bits + 1 bits wide (all ones for an out-of-range
-// row, which orders it last); counts every sort pass's digits.  Grid-stride,
-// so that whole warps take part in the digit counts.
+// row, which orders it last); counts the digits of the passes in d (the
+// caller passes none where no pass reads the totals).  Grid-stride, so that
+// whole warps take part in the digit counts.
 __global__ void __launch_bounds__(kGBlock) kg_pack_keys_packed(const int4* __restrict__ coords, int64_t n, int3 shape,
                                                                int batch, const GLayout L, int kb, int rbits,
                                                                const WideDigits d, uint64_t* __restrict__ packed,
@@ -600,7 +601,8 @@ __global__ void __launch_bounds__(kGBlock) kg_mask_keys(const int32_t* __restric
 }
 
 // The same keys packed with the row for the whole-GPU sort: entry g n + i is
-// (((g << kg) | key) << rbits) | i; counts every sort pass's digits.
+// (((g << kg) | key) << rbits) | i; counts the digits of the passes in d
+// (none where no pass reads the totals).
 __global__ void __launch_bounds__(kGBlock) kg_mask_keys_packed(const int32_t* __restrict__ nbr, int64_t n, int stride,
                                                                int G, int kg, int rbits,
                                                                const int32_t* __restrict__ tap_pos,
@@ -1293,7 +1295,8 @@ __global__ void __launch_bounds__(kGBlock) kst_candidates(const int4* __restrict
 // from a multiplicative hash), one thread per candidate (a thread per input
 // site and its 8 candidates in turn was 26 us on outdoor, cold); the thread
 // whose insertion creates an entry appends the key to uniq[] (the count in
-// *n_uniq) and counts its digits for the sort of the distinct keys.  The set
+// *n_uniq) and counts its digits for the sort of the distinct keys (the
+// passes in d: none where no pass of that sort reads the totals).  The set
 // has at least twice as many slots as there can be candidates, so a probe
 // always ends.
 __device__ __forceinline__ uint64_t set_slot(uint64_t key, int log2) {

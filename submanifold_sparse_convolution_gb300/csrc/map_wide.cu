@@ -25,11 +25,12 @@
 //    histogram kernel that wrote the keys.
 // Kernels follow each other with programmatic dependent launch.
 //
-// Steps (sorted-key mapper):  pack keys + histograms of all key digits ->
-// key passes -> neighbour search (map_search.cu) -> mask keys (inside the
-// first mask pass where the exchange runs) -> mask passes -> per-tile pair
-// counts -> (above 1024 tiles) one-CTA scan of the (tap, tile) offsets and
-// the tile order -> pair lists, gather table and row order.  The hash mapper
+// Steps (sorted-key mapper):  pack keys (+ histograms of the key digits
+// where a pass reads digit totals) -> key passes -> neighbour search
+// (map_search.cu) -> mask keys (inside the first mask pass where the
+// exchange runs) -> mask passes -> per-tile pair counts -> (above 1024
+// tiles) the scan of the (tap, tile) offsets, one CTA per tap, and the tile
+// order -> pair lists, gather table and row order.  The hash mapper
 // replaces the first three steps by an insert and a lookup, the dense mapper
 // by a presence-grid scatter and a 27-lookup pass.  Results are
 // bit-identical to the other pipelines: the same packed keys, the same
@@ -257,7 +258,8 @@ struct KeyDigits {
 };
 
 // ---------------------------------------------------------------------------
-// sorted-key mapper: packed keys and the digit counts of every key pass
+// sorted-key mapper: packed keys and the digit counts of the key passes in
+// kd (none where every pass runs in the count exchange)
 // ---------------------------------------------------------------------------
 template <int kRowsPerThread>
 __global__ void __launch_bounds__(WT) k_wide_keys(const WideArgs a, const KeyDigits kd) {
