@@ -374,6 +374,196 @@ __device__ __forceinline__ uint64_t g_key(int4 c, const GLayout& L) {
            static_cast<uint64_t>(c.w + L.r);
 }
 
+// ---------------------------------------------------------------------------
+// column index over the sorted keys: z is the key's lowest field, so the
+// voxels of one (b, x, y) column are one run of the sorted array.  A table of
+// (column key + 1, run start | run length << 32) entries, two per 32-byte
+// bucket, lets a row find each of its K^2 neighbour columns with one bucket
+// read and the run's few keys, instead of a binary search of ~log2(n) round
+// trips per column.
+// ---------------------------------------------------------------------------
+constexpr int kColBucket = 2;   // entries (16 bytes each) per 32-byte bucket
+constexpr int64_t kColIndexRows = 65536;
+
+// Entries of the column table for n rows: at least 4 n (columns number at
+// most n, so a bucket is rarely full), a power of two.
+inline int col_table_log2(int64_t n) {
+    int l = 11;
+    while ((int64_t(1) << l) < 4 * std::max<int64_t>(1, n)) ++l;
+    return l;
+}
+
+// The thread of each column's first sorted position measures the run and
+// enters it; the table is zero before.  Out-of-range rows (the all-ones key)
+// sort last and are skipped.
+__global__ void __launch_bounds__(kGBlock) kg_col_insert(const uint64_t* __restrict__ sv, int64_t n, int rbits,
+                                                         uint64_t no_key, int wz, int log2,
+                                                         uint64_t* __restrict__ table,
+                                                         int32_t* __restrict__ status) {
+    pdl_trigger();
+    pdl_wait();
+    const int64_t s = static_cast<int64_t>(blockIdx.x) * kGBlock + threadIdx.x;
+    if (s >= n) return;
+    const uint64_t q = __ldcg(sv + s) >> rbits;
+    if (q == no_key) return;
+    const uint64_t ck = q >> wz;
+    if (s > 0 && ((__ldcg(sv + s - 1) >> rbits) >> wz) == ck) return;   // not the run's first voxel
+    int64_t e = s + 1;
+    while (e < n) {
+        const uint64_t qe = __ldcg(sv + e) >> rbits;
+        if (qe == no_key || (qe >> wz) != ck) break;
+        ++e;
+    }
+    const uint64_t val = static_cast<uint64_t>(s) | (static_cast<uint64_t>(e - s) << 32);
+    const int lb = log2 - 1;   // buckets of kColBucket entries
+    const uint64_t bmask = (uint64_t(1) << lb) - 1;
+    uint64_t b = g_bucket(ck, lb);
+    for (uint64_t probe = 0; probe <= bmask; ++probe, b = (b + 1) & bmask) {
+        for (int j = 0; j < kColBucket; ++j) {
+            uint64_t* ent = table + 2 * (b * kColBucket + j);
+            if (atomicCAS(reinterpret_cast<unsigned long long*>(ent), 0ull,
+                          static_cast<unsigned long long>(ck + 1)) == 0ull) {
+                ent[1] = val;
+                return;
+            }
+        }
+    }
+    atomicOr(status, kStatusInternal);   // a full table: cannot happen at load <= 1/4
+}
+
+// The sorted mapper's search through the column index (kernel size K, K
+// threads per row, one per dx plane, LockRows<K> rows per block): a plane's K
+// (dx, dy) columns are found with their bucket reads in flight together, then
+// each column's dz window -- at most K consecutive keys of its run, from the
+// first key at or past dz = -r -- is read; a run longer than K is first
+// searched for that key (in lockstep over the plane's columns).  Rows are
+// staged in shared memory and written whole, as in kg_search_lockstep.
+template <int K>
+__global__ void __launch_bounds__(LockRows<K>::value * K) kg_col_search(const uint64_t* __restrict__ sv, int64_t n,
+                                                                        int rbits, uint64_t no_key, const GLayout L,
+                                                                        int log2, const uint64_t* __restrict__ table,
+                                                                        int32_t* __restrict__ nbr,
+                                                                        int32_t* __restrict__ tap_count,
+                                                                        int32_t* __restrict__ status) {
+    pdl_trigger();
+    pdl_wait();
+    constexpr int R = (K - 1) / 2, V = K * K * K, LR = LockRows<K>::value, ST = NbrStride<K>::value;
+    __shared__ int32_t cnt[V];
+    __shared__ __align__(16) int32_t rows_s[LR][ST];
+    __shared__ int64_t rid[LR];
+    for (int k = threadIdx.x; k < V; k += LR * K) cnt[k] = 0;
+    for (int k = threadIdx.x; k < LR * ST; k += LR * K) (&rows_s[0][0])[k] = -1;
+    const int plane = threadIdx.x / LR;   // dx = plane - R (warp-uniform)
+    const int rl = threadIdx.x % LR;
+    const uint64_t rmask = (uint64_t(1) << rbits) - 1;
+    const int64_t s = static_cast<int64_t>(blockIdx.x) * LR + rl;
+    bool ok = s < n;
+    uint64_t q = 0;
+    int64_t row = 0;
+    if (ok) {
+        const uint64_t v = __ldcg(sv + s);
+        q = v >> rbits;
+        row = static_cast<int64_t>(v & rmask);
+        ok = q != no_key;
+        if (ok && plane == R && s > 0 && (__ldcg(sv + s - 1) >> rbits) == q) atomicOr(status, kStatusDuplicate);
+    }
+    if (plane == 0) rid[rl] = s < n ? row : -1;   // (a row out of range is written as all -1)
+    __syncthreads();
+    if (ok) {
+        const int lb = log2 - 1;
+        const uint64_t bmask = (uint64_t(1) << lb) - 1;
+        const uint64_t zq = q & ((uint64_t(1) << L.wz) - 1);   // z + r >= r: zq - R >= 0
+        // the plane's columns (the +r padding keeps every field in range: no borrow)
+        uint64_t cke[K];
+        ulonglong2 blo[K], bhi[K];
+#pragma unroll
+        for (int e = 0; e < K; ++e) {
+            cke[e] = (q >> L.wz) + (static_cast<uint64_t>(static_cast<int64_t>(plane - R)) << L.wy) +
+                     static_cast<uint64_t>(static_cast<int64_t>(e - R));
+            g_load_bucket(table + 2 * kColBucket * g_bucket(cke[e], lb), blo[e], bhi[e]);
+        }
+        int64_t lo[K], hi[K], re[K];   // search range and run end of each column (empty when absent)
+#pragma unroll
+        for (int e = 0; e < K; ++e) {
+            uint64_t val = 0;
+            bool found = false;
+            if (blo[e].x == cke[e] + 1) {
+                val = blo[e].y;
+                found = true;
+            } else if (bhi[e].x == cke[e] + 1) {
+                val = bhi[e].y;
+                found = true;
+            } else if (blo[e].x != 0ull && bhi[e].x != 0ull) {
+                // a full bucket: the column may sit in the buckets after it (rare)
+                uint64_t b = g_bucket(cke[e], lb);
+                for (uint64_t probe = 1; probe <= bmask && !found; ++probe) {
+                    b = (b + 1) & bmask;
+                    ulonglong2 x, y;
+                    g_load_bucket(table + 2 * kColBucket * b, x, y);
+                    if (x.x == cke[e] + 1) {
+                        val = x.y;
+                        found = true;
+                    } else if (y.x == cke[e] + 1) {
+                        val = y.y;
+                        found = true;
+                    } else if (x.x == 0ull || y.x == 0ull) {
+                        break;   // an empty slot: the column has no voxel
+                    }
+                }
+            }
+            lo[e] = found ? static_cast<int64_t>(val & 0xFFFFFFFFull) : 0;
+            re[e] = found ? lo[e] + static_cast<int64_t>(val >> 32) : 0;
+            if (re[e] > n || lo[e] > re[e]) {   // a corrupt entry: never read past the array
+                atomicOr(status, kStatusInternal);
+                lo[e] = re[e] = 0;
+            }
+            hi[e] = re[e] - lo[e] > K ? re[e] : lo[e];   // only a run longer than K is searched
+        }
+        // the first key at or past the column's dz = -r key (lower bound, in
+        // lockstep over the plane's columns; a run is at most Z + 2r long)
+        for (int it = 0; it < 40; ++it) {
+            uint64_t kk[K];
+#pragma unroll
+            for (int e = 0; e < K; ++e) kk[e] = lo[e] < hi[e] ? (__ldcg(sv + ((lo[e] + hi[e]) >> 1)) >> rbits) : 0ull;
+            bool open = false;
+#pragma unroll
+            for (int e = 0; e < K; ++e) {
+                if (lo[e] < hi[e]) {
+                    const int64_t mid = (lo[e] + hi[e]) >> 1;
+                    if (kk[e] < (cke[e] << L.wz) + zq - R)
+                        lo[e] = mid + 1;
+                    else
+                        hi[e] = mid;
+                    open |= lo[e] < hi[e];
+                }
+            }
+            if (!open) break;
+        }
+        // at most K keys from there lie in the column's dz window (keys are unique)
+#pragma unroll
+        for (int e = 0; e < K; ++e) {
+            const int c = plane * K + e;
+            const uint64_t lo_t = (cke[e] << L.wz) + zq - R;   // the column's dz = -r key
+            uint64_t vv[K];
+#pragma unroll
+            for (int j = 0; j < K; ++j) vv[j] = lo[e] + j < re[e] ? __ldcg(sv + lo[e] + j) : ~0ull;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                const uint64_t d = (vv[j] >> rbits) - lo_t;
+                if (vv[j] != ~0ull && d <= static_cast<uint64_t>(2 * R)) {
+                    const int k = c * K + static_cast<int>(d);
+                    rows_s[rl][k] = static_cast<int32_t>(vv[j] & rmask);
+                    atomicAdd(&cnt[k], 1);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    write_rows(rows_s, [&](int j) { return rid[j]; }, nbr);
+    for (int k = threadIdx.x; k < V; k += LR * K)
+        if (cnt[k]) atomicAdd(&tap_count[k], cnt[k]);
+}
+
 __global__ void __launch_bounds__(kGBlock) kg_hash_insert(const int4* __restrict__ coords, int64_t n, int3 shape,
                                                           int batch, const GLayout L, uint64_t* __restrict__ table,
                                                           int log2, int row_bits, int32_t* __restrict__ status) {
@@ -1639,10 +1829,18 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
     add(wide_bytes, 1);                               // whole-GPU sort: digit totals, tickets, look-back states
     int table_log2 = 11;
     while ((int64_t(1) << table_log2) < kGHashSlotsPerRow * nt1) ++table_log2;
+    // Kernel size 5 above kColIndexRows: the sorted search through a column
+    // index.  Measured against the lockstep binary searches (map µs): stage
+    // (240k rows) 405 -> 363, large (94.5k) 198 -> 191; but outdoor (32k)
+    // 116.6 -> 119.6 and three groups of kernel size 3 70.7 -> 81.0, where
+    // the index's build and clearing cost more than the searches save.
+    const bool col_index = wide_coord && K == 5 && n > kColIndexRows;
+    const int col_log2 = col_table_log2(n);
     if (src) {
         // the neighbours come from the strided map
     } else if (wide_coord) {
         add(n1, 8); add(n1, 8);                       // packed coordinate keys, ping-pong
+        if (col_index) add(size_t(2) << col_log2, 8);  // column index (2 words an entry)
     } else if (mapper == SPCONV_MAPPER_SORTED) {
         add(n1, 8); add(n1, 8); add(n1, 4); add(n1, 4);   // coordinate keys and rows, ping-pong
     } else if (mapper == SPCONV_MAPPER_HASH) {
@@ -1667,6 +1865,7 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
     char* wide = take<char>(p, wide_bytes);
     const bool hashed = !src && !wide_coord && mapper == SPCONV_MAPPER_HASH;
     uint64_t* table = hashed ? take<uint64_t>(p, size_t(1) << table_log2) : nullptr;
+    uint64_t* col_table = col_index ? take<uint64_t>(p, size_t(2) << col_log2) : nullptr;
     const size_t zero_bytes = static_cast<size_t>(p - zero_begin);
     h->nbr = take<int32_t>(p, n1 * h->nbr_stride);
     h->mask = take<uint32_t>(p, gn);
@@ -1737,7 +1936,15 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
         SPCONV_CHECK(wide_sort(ck_a, ck_b, n, cdig, wgh, wtickets, 0, wlook, h->status, s, &in_b));
         const uint64_t* sv = in_b ? ck_b : ck_a;
         const uint64_t no_key = (uint64_t(1) << ckb) - 1;
-        if (K == 3)
+        if (col_index) {
+            // each (b, x, y) column's run entered in the column index, then the search through it
+            SPCONV_CHECK(launch_chained(kg_col_insert, blocks(n, kGBlock), kGBlock, s, sv, n, mrb, no_key, L.wz, col_log2,
+                                        col_table, h->status));
+            ++launches;
+            SPCONV_CHECK(launch_chained(kg_col_search<5>, blocks(n, LockRows<5>::value), LockRows<5>::value * 5, s, sv, n,
+                                        mrb, no_key, L, col_log2, static_cast<const uint64_t*>(col_table), h->nbr,
+                                        h->tap_count, h->status));
+        } else if (K == 3)
             SPCONV_CHECK(launch_chained(kg_search_lockstep<3>, blocks(n, LockRows<3>::value), LockRows<3>::value * 3, s, sv,
                                         n, mrb, no_key, L, h->nbr, h->tap_count, h->status));
         else if (K == 5)
