@@ -103,12 +103,15 @@ __global__ void __launch_bounds__(kFThreads, 3) k_fp32_tiled(const float* __rest
                                                              const int32_t* __restrict__ perm,
                                                              const int32_t* __restrict__ gtab,
                                                              const uint32_t* __restrict__ tile_union,
+                                                             const int32_t* __restrict__ tile_order,
                                                              int64_t n, int64_t n_pad, int64_t n_in, int c_in,
                                                              int c_out, Epilogue epi, int32_t* __restrict__ status) {
     extern __shared__ float fsm[];
     const int t = threadIdx.x;
     const int cg = t & 7, rg = t >> 3;        // columns 8 cg .. + 7; rows rg + 16 i
-    const int64_t tile = blockIdx.x;
+    // CTAs start in blockIdx order: taking the tiles by descending union size
+    // (their cost) puts the cheapest last, where they fill the final wave
+    const int64_t tile = tile_order ? tile_order[blockIdx.x] : blockIdx.x;
     const int o0 = blockIdx.y * kFCols;
     const uint32_t uni = tile_union[tile];
     const int kcs = (c_in + kFK - 1) / kFK;
@@ -253,7 +256,7 @@ int launch_fp32_tiled(const MapHandle* h, const void* feats, const void* w, void
     const dim3 grid(static_cast<unsigned>(h->n_tiles), static_cast<unsigned>(c_out / kFCols));
     k_fp32_tiled<<<grid, kFThreads, kFSmem, s>>>(
         static_cast<const float*>(feats), static_cast<const float*>(w), static_cast<float*>(out), h->perm, h->gtab,
-        h->tile_union, h->n, h->n_pad, h->n_in >= 0 ? h->n_in : h->n, c_in, c_out, epi, h->status);
+        h->tile_union, h->tile_order, h->n, h->n_pad, h->n_in >= 0 ? h->n_in : h->n, c_in, c_out, epi, h->status);
     count_launch();
     return cuda_status(cudaGetLastError());
 }
