@@ -1066,8 +1066,9 @@ __global__ void __launch_bounds__(1024) kg_scan_tiles(const int32_t* __restrict_
     }
 }
 
-// Block (g, t): the pairs of the group's taps for the rows of tile t, at the
-// tile's offsets in each tap's list, ranked by position in the tile; and
+// Block (g, i) handles tile t, the i-th of group g's tile order: the pairs of
+// the group's taps for the rows of tile t, at the tile's offsets in each
+// tap's list, ranked by position in the tile; and
 // gtab[k][s] = neighbour of the row at position s of the group's order (-1
 // when absent or past n).
 __global__ void __launch_bounds__(kTileRows) kg_tile_write(const int32_t* __restrict__ perm,
@@ -1075,6 +1076,7 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write(const int32_t* __rest
                                                            const int32_t* __restrict__ nbr, int stride, int64_t n,
                                                            int64_t n_tiles, int64_t n_pad, int kg,
                                                            const int32_t* __restrict__ seg_off,
+                                                           const int32_t* __restrict__ tile_order,
                                                            int32_t* __restrict__ in_rows,
                                                            int32_t* __restrict__ out_rows,
                                                            int32_t* __restrict__ gtab) {
@@ -1082,7 +1084,10 @@ __global__ void __launch_bounds__(kTileRows) kg_tile_write(const int32_t* __rest
     pdl_wait();
     __shared__ int32_t wc[kTileRows / 32][kMaxGroupTaps];
     __shared__ int32_t seg[kMaxGroupTaps];
-    const int64_t g = blockIdx.x / n_tiles, t = blockIdx.x % n_tiles;
+    // block (g, i) takes the i-th tile of group g's tile order (descending
+    // union size): the costliest start first, the cheapest fill the last wave
+    const int64_t g = blockIdx.x / n_tiles;
+    const int64_t t = __ldcg(tile_order + blockIdx.x);
     const int64_t s = t * kTileRows + threadIdx.x;
     const bool valid = s < n;
     const int32_t r = valid ? perm[g * n + s] : -1;
@@ -2057,7 +2062,8 @@ int grouped_core(MapHandle* h, const spconv_options_t* opt, const int32_t* coord
                                     static_cast<const int32_t*>(h->tap_count), h->tile_union, h->seg_off, h->tap_off,
                                     h->totals, h->tile_order, h->tile_nonempty, h->status));
         SPCONV_CHECK(launch_chained(kg_tile_write, tiles, kTileRows, s, h->perm, h->mask, h->nbr, h->nbr_stride, n, T,
-                                    h->n_pad, kg, h->seg_off, h->in_rows, h->out_rows, h->gtab));
+                                    h->n_pad, kg, h->seg_off, static_cast<const int32_t*>(h->tile_order), h->in_rows,
+                                    h->out_rows, h->gtab));
     }
     launches += 3;
     count_launch(launches);
